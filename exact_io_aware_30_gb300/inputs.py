@@ -1,0 +1,162 @@
+"""Seeded synthetic inputs shared by the GPU path's tests/bench and the oracle.
+
+This module holds no attention arithmetic: it draws Q, K, V, rounds them to
+the 16-bit storage type and hands out both the raw 16-bit patterns (for the
+GPU library) and the exactly widened float64 values (for the CPU oracle).
+
+Recipe (the same for every workload):
+  * numpy ``Generator(PCG64(seed))``; Q, then K, then V drawn in that order
+    with ``standard_normal(shape, dtype=float32)``, shape [B, H, S, d];
+  * round-to-nearest-even to bf16 (or fp16 for the fp16 workload);
+  * the "spiky keys" workload then picks, per (b, h), round(0.01 * Sk)
+    distinct key rows with ``rng.choice(Sk, n, replace=False)`` and multiplies
+    them by 8 (a power of two: exact in both 16-bit types);
+  * scale = 1/sqrt(d) as float32.
+
+The five named workloads mirror the cases the pages discuss: a tiny
+single-head case, a batched causal case, 8k tokens x 32 heads ("FlashAttention:
+IO-aware attention kernels", section "Why you'd care"), an 18 000-token
+document with d = 128 ("Flash attention and memory-efficient attention
+variants", section "The wall you hit is not the one you expect"), and a
+d = 256 case with rare large keys that force running-max jumps.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BF16 = "bf16"
+FP16 = "fp16"
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    Sq: int
+    Sk: int
+    d: int
+    dtype: str
+    mask: str          # "none" | "causal" | "window"
+    window: int = 0
+    spiky_keys: bool = False
+    seed: int = 0
+    notes: str = field(default="", compare=False)
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0) / np.sqrt(np.float32(self.d)))
+
+    def shape_q(self):
+        return (self.B, self.H, self.Sq, self.d)
+
+    def shape_kv(self):
+        return (self.B, self.H, self.Sk, self.d)
+
+
+# The five workloads, indexed 0..4; seed = 1001 + index.
+WORKLOADS = [
+    Workload("tiny_b1h1_s256_d64_bf16_nomask", 1, 1, 256, 256, 64, BF16, "none", seed=1001),
+    Workload("b4h16_s2048_d128_bf16_causal", 4, 16, 2048, 2048, 128, BF16, "causal", seed=1002),
+    Workload("b1h32_s8192_d128_fp16_causal", 1, 32, 8192, 8192, 128, FP16, "causal", seed=1003),
+    Workload("b1h16_s18000_d128_bf16_window4096", 1, 16, 18000, 18000, 128, BF16, "window",
+             window=4096, seed=1004),
+    Workload("b2h8_s4096_d256_bf16_nomask_spikykeys", 2, 8, 4096, 4096, 256, BF16, "none",
+             spiky_keys=True, seed=1005),
+]
+
+
+def workload(index_or_name) -> Workload:
+    if isinstance(index_or_name, int):
+        return WORKLOADS[index_or_name]
+    for w in WORKLOADS:
+        if w.name == index_or_name:
+            return w
+    raise KeyError(index_or_name)
+
+
+# ----------------------------------------------------------------------------
+# 16-bit encodings (storage conversions only)
+# ----------------------------------------------------------------------------
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 to bf16 (round to nearest, ties to even); uint16 bits."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (b >> np.uint32(16)) & np.uint32(1)
+    rounded = b + np.uint32(0x7FFF) + lsb
+    out = (rounded >> np.uint32(16)).astype(np.uint16)
+    nan = np.isnan(x)
+    if nan.any():
+        out[nan] = np.uint16(0x7FC0)
+    return out
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def f32_to_fp16_bits(x: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def fp16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    return f32_to_bf16_bits(x) if dtype == BF16 else f32_to_fp16_bits(x)
+
+
+def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
+    return bf16_bits_to_f64(bits) if dtype == BF16 else fp16_bits_to_f64(bits)
+
+
+def round_to_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float64 values of x after rounding to the 16-bit type."""
+    return bits_to_f64(to_bits(np.asarray(x, dtype=np.float32), dtype), dtype)
+
+
+# ----------------------------------------------------------------------------
+# Generators
+# ----------------------------------------------------------------------------
+
+@dataclass
+class Inputs:
+    workload: Workload
+    q_bits: np.ndarray   # uint16 [B,H,Sq,d]
+    k_bits: np.ndarray   # uint16 [B,H,Sk,d]
+    v_bits: np.ndarray   # uint16 [B,H,Sk,d]
+
+    def f64(self):
+        dt = self.workload.dtype
+        return (bits_to_f64(self.q_bits, dt), bits_to_f64(self.k_bits, dt),
+                bits_to_f64(self.v_bits, dt))
+
+
+def generate(w: Workload, seed: int | None = None) -> Inputs:
+    """Draw one workload's Q, K, V by the recipe in the module docstring."""
+    rng = np.random.Generator(np.random.PCG64(w.seed if seed is None else seed))
+    q = rng.standard_normal(w.shape_q(), dtype=np.float32)
+    k = rng.standard_normal(w.shape_kv(), dtype=np.float32)
+    v = rng.standard_normal(w.shape_kv(), dtype=np.float32)
+    qb, kb, vb = to_bits(q, w.dtype), to_bits(k, w.dtype), to_bits(v, w.dtype)
+    del q, k, v
+    if w.spiky_keys:
+        n = int(round(0.01 * w.Sk))
+        kf = bits_to_f64(kb, w.dtype)
+        for b in range(w.B):
+            for h in range(w.H):
+                rows = rng.choice(w.Sk, n, replace=False)
+                kf[b, h, rows, :] *= 8.0
+        kb = to_bits(kf.astype(np.float32), w.dtype)
+    return Inputs(w, qb, kb, vb)
+
+
+def custom(B, H, Sq, Sk, d, dtype=BF16, mask="none", window=0, seed=0, spiky_keys=False,
+           name="custom") -> Inputs:
+    """An ad-hoc shape drawn by the same recipe."""
+    w = Workload(name, B, H, Sq, Sk, d, dtype, mask, window, spiky_keys, seed)
+    return generate(w)

@@ -1,0 +1,405 @@
+"""Pins for the fp64 oracle: values the pages print, closed forms, invariants,
+library routines it must reduce to, and planted mistakes the pins must catch.
+
+Nothing here calls the GPU library; these run on any CPU.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from exact_io_aware_30_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _close(x, printed, digits, slack=0.0):
+    """x agrees with a value printed to `digits` decimals.
+
+    ``slack`` allows for a hand trace that rounded its intermediates before
+    combining them (the page's 6.6164 is 0.4698 + 6.1465 from 4-5 digit
+    factors; the exact value is 6.61634).
+    """
+    return abs(float(x) - float(printed)) <= 0.5 * 10.0 ** (-digits) + slack + 1e-12
+
+
+HAND = 1e-4  # rounding slack of the hand-traced intermediates
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------
+# 1. The pages' worked examples
+# ---------------------------------------------------------------------------
+
+def check_worked_example(orc):
+    g = _load("worked_example.json")
+    q = np.array(g["q"])
+    K = np.array(g["K"])
+    V = np.array(g["V"])
+    tr = orc.online_trace(q, K, V, g["scale"], g["block_size"])
+    for t, ref in enumerate(g["after_tile"]):
+        assert _close(tr["m"][t], ref["m"], 6)
+        assert _close(tr["l"][t], ref["l"], ref["l_digits"])
+        for c in range(2):
+            assert _close(tr["o_unnorm"][t][c], ref["o_unnorm"][c], ref["o_digits"], HAND)
+    # the correction factor applied at tile 2 and tile 2's weights
+    corr = math.exp(tr["m"][0] - tr["m"][1])
+    assert _close(corr, g["correction_tile2"], g["correction_digits"])
+    for c in range(2):
+        assert _close(tr["o"][c], g["output"][c], g["output_digits"])
+    # direct softmax probabilities of the naive form
+    P = orc.probs(q[None, :], K, g["scale"])
+    for j in range(4):
+        assert _close(P[0, j], g["probs"][j], g["probs_digits"])
+    assert abs(P.sum() - 1.0) < 1e-14
+    # tile-2 unnormalised weights exp(s - m) = P * l
+    for jj, j in enumerate((2, 3)):
+        assert _close(P[0, j] * tr["l"][-1], g["tile2_p"][jj], g["tile2_p_digits"])
+    # naive form on the same data, via the [B,H,S,d] entry point
+    o, lse = orc.attention(q[None, None, None, :], K[None, None], V[None, None], g["scale"])
+    for c in range(2):
+        assert _close(o[0, 0, 0, c], g["output"][c], g["output_digits"])
+    # lse = m + ln l with the printed l (derived, not printed)
+    assert abs(lse[0, 0, 0] - (3.0 + math.log(g["after_tile"][1]["l"]))) < 1e-5
+    # one block of four keys (the block_size = 4 question)
+    b4 = g["block4"]
+    tr4 = orc.online_trace(q, K, V, g["scale"], 4)
+    assert _close(tr4["l"][0], b4["l"], b4["l_digits"])
+    for j in range(4):
+        assert _close(P[0, j] * tr4["l"][0], b4["p_unnorm"][j], b4["p_digits"])
+    for c in range(2):
+        assert _close(tr4["o"][c], b4["output"][c], b4["output_digits"])
+
+
+def test_worked_example_trace():
+    check_worked_example(oracle.default())
+
+
+def check_online_softmax_1d(orc):
+    g = _load("online_softmax_1d.json")
+    s = np.array(g["scores"])
+    # scores s_j = q . k_j with q = [1,0,0,0] and k_j = [s_j,0,0,0] (zero
+    # padding leaves the scores unchanged); values are one-hot rows
+    q = np.array([1.0, 0.0, 0.0, 0.0])
+    K = np.zeros((4, 4))
+    K[:, 0] = s
+    V = np.eye(4)
+    tr = orc.online_trace(q, K, V, 1.0, g["block_size"])
+    dg = g["digits"]
+    assert _close(tr["m"][0], g["block1_max"], dg)
+    assert _close(tr["l"][0], g["block1_sum"], dg)
+    assert _close(math.exp(tr["m"][0] - tr["m"][1]), g["rescale"], dg)
+    # printed as 0.135 x 1.135 ~ 0.153 from the rounded factors (exact 0.15365)
+    assert _close(math.exp(tr["m"][0] - tr["m"][1]) * tr["l"][0], g["rescaled_block1_sum"], dg,
+                  1e-3)
+    assert _close(tr["m"][1], g["final_max"], dg)
+    assert _close(tr["l"][1], g["direct_denominator"], dg)
+    # the output with one-hot values is the probability vector itself
+    assert abs(tr["o"].sum() - 1.0) < 1e-14
+    assert np.argmax(tr["o"]) == 3
+
+
+def test_online_softmax_1d_example():
+    check_online_softmax_1d(oracle.default())
+
+
+# ---------------------------------------------------------------------------
+# 2. Reductions to library routines (scipy softmax / logsumexp, torch SDPA)
+# ---------------------------------------------------------------------------
+
+def _window_bool(Sq, Sk, W):
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    return (j <= i) & (j > i - W)
+
+
+def check_library_reduction(orc, rng):
+    sp = pytest.importorskip("scipy.special")
+    for (B, H, Sq, Sk, d) in [(1, 2, 7, 7, 5), (2, 1, 5, 9, 3), (1, 1, 13, 6, 8)]:
+        q, k, v = _rand(rng, B, H, Sq, d), _rand(rng, B, H, Sk, d), _rand(rng, B, H, Sk, d)
+        scale = 0.37
+        S = scale * np.einsum("bhid,bhjd->bhij", q, k)
+        ref_o = sp.softmax(S, axis=-1) @ v
+        ref_lse = sp.logsumexp(S, axis=-1)
+        o, lse = orc.attention(q, k, v, scale, "none")
+        np.testing.assert_allclose(o, ref_o, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-13)
+
+
+def test_reduces_to_scipy_softmax_no_mask():
+    check_library_reduction(oracle.default(), np.random.default_rng(1))
+
+
+def check_torch_sdpa(orc, rng):
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for (Sq, Sk, d, W) in [(9, 9, 4, 3), (6, 11, 3, 1), (12, 5, 2, 4)]:
+        q, k, v = _rand(rng, 1, 2, Sq, d), _rand(rng, 1, 2, Sk, d), _rand(rng, 1, 2, Sk, d)
+        scale = 1.0 / math.sqrt(d)
+        tq, tk, tv = (torch.from_numpy(x) for x in (q, k, v))
+        # causal: torch's is_causal is the top-left aligned lower triangle
+        ref = F.scaled_dot_product_attention(tq, tk, tv, is_causal=True, scale=scale).numpy()
+        o, _ = orc.attention(q, k, v, scale, "causal")
+        rows_ok = np.arange(Sq) < Sk  # torch leaves no row empty with Sq <= Sk
+        np.testing.assert_allclose(o[:, :, rows_ok], ref[:, :, rows_ok], rtol=1e-12, atol=1e-12)
+        # sliding window: the same boolean band handed to torch explicitly
+        band = _window_bool(Sq, Sk, W)
+        full = band.any(axis=1)
+        ref_w = F.scaled_dot_product_attention(tq, tk, tv, attn_mask=torch.from_numpy(band),
+                                               scale=scale).numpy()
+        o_w, lse_w = orc.attention(q, k, v, scale, "window", W)
+        np.testing.assert_allclose(o_w[:, :, full], ref_w[:, :, full], rtol=1e-12, atol=1e-12)
+        # rows that see no key: guarded to zero output and -inf lse
+        assert np.all(o_w[:, :, ~full] == 0.0)
+        assert np.all(np.isneginf(lse_w[:, :, ~full]))
+
+
+def test_matches_torch_sdpa_causal_and_window():
+    check_torch_sdpa(oracle.default(), np.random.default_rng(2))
+
+
+# ---------------------------------------------------------------------------
+# 3. Closed forms and special cases
+# ---------------------------------------------------------------------------
+
+def check_closed_forms(orc, rng):
+    d = 6
+    # one key: O = v0, lse = scale * q . k0
+    q, k, v = _rand(rng, 1, 1, 4, d), _rand(rng, 1, 1, 1, d), _rand(rng, 1, 1, 1, d)
+    o, lse = orc.attention(q, k, v, 0.5, "none")
+    np.testing.assert_allclose(o[0, 0], np.repeat(v[0, 0], 4, axis=0), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse[0, 0], 0.5 * q[0, 0] @ k[0, 0, 0], rtol=1e-14)
+    # identical keys under a causal mask: row i averages v_0..v_i, lse = s + ln(i+1)
+    Sq = 7
+    q = _rand(rng, 1, 1, Sq, d)
+    k = np.repeat(_rand(rng, 1, 1, 1, d), Sq, axis=2)
+    v = _rand(rng, 1, 1, Sq, d)
+    o, lse = orc.attention(q, k, v, 0.3, "causal")
+    for i in range(Sq):
+        np.testing.assert_allclose(o[0, 0, i], v[0, 0, :i + 1].mean(axis=0), rtol=1e-13, atol=1e-14)
+        s = 0.3 * q[0, 0, i] @ k[0, 0, 0]
+        assert abs(lse[0, 0, i] - (s + math.log(i + 1))) < 1e-12
+    # scale = 0: every visible key has the same weight
+    q, k, v = _rand(rng, 1, 1, 5, d), _rand(rng, 1, 1, 8, d), _rand(rng, 1, 1, 8, d)
+    o, lse = orc.attention(q, k, v, 0.0, "none")
+    np.testing.assert_allclose(o[0, 0], np.tile(v[0, 0].mean(axis=0), (5, 1)), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse[0, 0], math.log(8), rtol=1e-14)
+    # causal row 0 sees only key 0
+    q, k, v = _rand(rng, 1, 1, 6, d), _rand(rng, 1, 1, 6, d), _rand(rng, 1, 1, 6, d)
+    o, _ = orc.attention(q, k, v, 0.4, "causal")
+    assert np.array_equal(o[0, 0, 0], v[0, 0, 0])
+    # window of one key: O_i = v_i exactly, lse_i = scale q_i . k_i
+    o, lse = orc.attention(q, k, v, 0.4, "window", 1)
+    assert np.array_equal(o[0, 0], v[0, 0])
+    np.testing.assert_allclose(lse[0, 0], 0.4 * np.einsum("id,id->i", q[0, 0], k[0, 0]), rtol=1e-14)
+    # a window at least as wide as the sequence is the causal mask
+    o_c, lse_c = orc.attention(q, k, v, 0.4, "causal")
+    o_w, lse_w = orc.attention(q, k, v, 0.4, "window", 6)
+    assert np.array_equal(o_c, o_w) and np.array_equal(lse_c, lse_w)
+    # one dominant key: the output is (almost exactly) that key's value row
+    q = np.ones((1, 1, 3, d))
+    k = np.zeros((1, 1, 5, d))
+    k[0, 0, 2] = 40.0
+    v = _rand(rng, 1, 1, 5, d)
+    o, _ = orc.attention(q, k, v, 1.0, "none")
+    np.testing.assert_allclose(o[0, 0], np.tile(v[0, 0, 2], (3, 1)), rtol=0, atol=1e-90)
+
+
+def test_closed_forms():
+    check_closed_forms(oracle.default(), np.random.default_rng(3))
+
+
+# ---------------------------------------------------------------------------
+# 4. Invariants
+# ---------------------------------------------------------------------------
+
+def check_invariants(orc, rng):
+    d = 5
+    for mask, W in (("none", 0), ("causal", 0), ("window", 3)):
+        q, k, v = _rand(rng, 1, 1, 9, d), _rand(rng, 1, 1, 9, d), _rand(rng, 1, 1, 9, d)
+        P = orc.probs(q[0, 0], k[0, 0], 0.45, mask, W)
+        np.testing.assert_allclose(P.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+        # invisible pairs carry exactly zero weight
+        i = np.arange(9)[:, None]
+        j = np.arange(9)[None, :]
+        vis = np.ones((9, 9), bool) if mask == "none" else (j <= i) & ((j > i - W) if W else True)
+        assert np.all(P[~vis] == 0.0) and np.all(P[vis] > 0.0)
+        # lse equals an independently ordered log-sum-exp of the visible scores
+        _, lse = orc.attention(q, k, v, 0.45, mask, W)
+        for r in range(9):
+            s = np.sort(0.45 * (k[0, 0][vis[r]] @ q[0, 0, r]))[::-1]
+            ref = s[0] + math.log(math.fsum(math.exp(x - s[0]) for x in s))
+            assert abs(lse[0, 0, r] - ref) < 1e-13
+    # keys a row cannot see do not affect it: overwrite them with large garbage
+    q, k, v = _rand(rng, 1, 1, 8, d), _rand(rng, 1, 1, 8, d), _rand(rng, 1, 1, 8, d)
+    o1, l1 = orc.attention(q, k, v, 0.5, "causal")
+    k2, v2 = k.copy(), v.copy()
+    k2[0, 0, 5:] = 1e6
+    v2[0, 0, 5:] = -3e7
+    o2, l2 = orc.attention(q, k2, v2, 0.5, "causal")
+    assert np.array_equal(o1[0, 0, :5], o2[0, 0, :5]) and np.array_equal(l1[0, 0, :5], l2[0, 0, :5])
+    # permuting query rows permutes the output (no mask)
+    perm = rng.permutation(8)
+    o3, l3 = orc.attention(q[:, :, perm], k, v, 0.5, "none")
+    o4, l4 = orc.attention(q, k, v, 0.5, "none")
+    assert np.array_equal(o3, o4[:, :, perm]) and np.array_equal(l3, l4[:, :, perm])
+    # permuting key/value rows together changes only the summation order
+    o5, l5 = orc.attention(q, k[:, :, perm], v[:, :, perm], 0.5, "none")
+    np.testing.assert_allclose(o5, o4, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(l5, l4, rtol=1e-13)
+
+
+def test_invariants():
+    check_invariants(oracle.default(), np.random.default_rng(4))
+
+
+def check_blocked_equals_naive(orc, rng):
+    for (B, H, Sq, Sk, d) in [(1, 2, 9, 9, 3), (2, 1, 5, 11, 4), (1, 1, 14, 6, 2)]:
+        q, k, v = _rand(rng, B, H, Sq, d), _rand(rng, B, H, Sk, d), _rand(rng, B, H, Sk, d)
+        for mask, W in (("none", 0), ("causal", 0), ("window", 1), ("window", 4)):
+            o_ref, l_ref = orc.attention(q, k, v, 0.6, mask, W)
+            for bs in list(range(1, Sk + 2)):
+                o, l = orc.attention_blocked(q, k, v, 0.6, mask, W, block_size=bs)
+                np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-13)
+                fin = np.isfinite(l_ref)
+                assert np.array_equal(fin, np.isfinite(l))
+                np.testing.assert_allclose(l[fin], l_ref[fin], rtol=1e-12, atol=1e-13)
+
+
+def test_blocked_equals_naive_every_block_size():
+    check_blocked_equals_naive(oracle.default(), np.random.default_rng(5))
+
+
+def check_brute_force(orc, rng):
+    """Exhaustive tiny shapes against a straight triple loop in Python floats."""
+    for Sq in (1, 3, 5):
+        for Sk in (1, 2, 4):
+            for d in (1, 3):
+                q, k, v = _rand(rng, 1, 1, Sq, d), _rand(rng, 1, 1, Sk, d), _rand(rng, 1, 1, Sk, d)
+                for mask, W in (("none", 0), ("causal", 0), ("window", 2)):
+                    o, lse = orc.attention(q, k, v, 0.8, mask, W)
+                    for i in range(Sq):
+                        vis = [j for j in range(Sk)
+                               if mask == "none" or (j <= i and (mask != "window" or j > i - W))]
+                        if not vis:
+                            assert np.all(o[0, 0, i] == 0) and lse[0, 0, i] == -math.inf
+                            continue
+                        s = {j: 0.8 * sum(q[0, 0, i, c] * k[0, 0, j, c] for c in range(d)) for j in vis}
+                        w = {j: math.exp(s[j]) for j in vis}
+                        tot = math.fsum(w.values())
+                        for c in range(d):
+                            ref = math.fsum(w[j] * v[0, 0, j, c] for j in vis) / tot
+                            assert abs(o[0, 0, i, c] - ref) <= 1e-12 * (1 + abs(ref))
+                        assert abs(lse[0, 0, i] - math.log(tot)) < 1e-12
+
+
+def test_brute_force_tiny():
+    check_brute_force(oracle.default(), np.random.default_rng(6))
+
+
+def test_row_subset_matches_full():
+    rng = np.random.default_rng(7)
+    q, k, v = _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4)
+    o, lse = oracle.attention(q, k, v, 0.5, "window", 3)
+    rows = np.array([0, 17, 59, 33, 9])
+    o_s, l_s = oracle.attention(q, k, v, 0.5, "window", 3, rows=rows)
+    assert np.array_equal(o_s, o.reshape(-1, 4)[rows])
+    assert np.array_equal(l_s, lse.reshape(-1)[rows])
+
+
+def test_rejects_bad_arguments():
+    z = np.zeros((1, 1, 2, 2))
+    with pytest.raises(ValueError):
+        oracle.attention(z, z, z, 1.0, "window", 0)
+    with pytest.raises(ValueError):
+        oracle.attention(z, z, z, 1.0, 7)
+    with pytest.raises(ValueError):
+        oracle.attention(z, z, z, 1.0, "none", rows=[4])
+
+
+def test_visible_pair_counts_agree():
+    from exact_io_aware_30_gb300 import metrics
+    for Sq, Sk in ((1, 1), (7, 7), (9, 4), (4, 9), (300, 300), (257, 130)):
+        for mask, W in (("none", 0), ("causal", 0), ("window", 1), ("window", 5), ("window", 400)):
+            assert metrics.visible_pairs_closed_form(Sq, Sk, mask, W) == \
+                oracle.visible_pairs(Sq, Sk, mask, W)
+    # the causal count is S(S+1)/2
+    assert metrics.visible_pairs_closed_form(8192, 8192, "causal") == 8192 * 8193 // 2
+
+
+# ---------------------------------------------------------------------------
+# 5. Planted mistakes: each mutation of the oracle's C source must fail a pin
+# ---------------------------------------------------------------------------
+
+MUTATIONS = [
+    ("dropped scale", "Si[j] = scale * dot;", "Si[j] = dot;"),
+    ("causal off by one", "if (j > i)\n        return 0;", "if (j >= i)\n        return 0;"),
+    ("window off by one", "j <= i - (int64_t)window", "j < i - (int64_t)window"),
+    ("transposed score (k.q over wrong row)", "const double *qi = q + flat * (int64_t)d;",
+     "const double *qi = q + (flat / Sq * Sq) * (int64_t)d;"),
+    ("wrong correction sign", "exp(m - m_new)", "exp(m_new - m)"),
+    ("lse without max", "mrow[r - r0] + log(lrow[r - r0])", "log(lrow[r - r0])"),
+    ("no normalisation", "Si[j] /= l;\n                lrow", "Si[j] /= 1.0;\n                lrow"),
+    ("unguarded empty row", "if (m == -INFINITY) { /* no visible key: guarded row */",
+     "if (0) {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    src = open(oracle._SRC).read()
+    assert old in src, f"mutation anchor for '{name}' not found"
+    mutated = tmp_path / "mutant.c"
+    mutated.write_text(src.replace(old, new, 1))
+    lib = oracle.compile_source(str(mutated), str(tmp_path / "libmutant.so"))
+    orc = oracle.OracleLib(lib)
+    checks = [check_worked_example, check_online_softmax_1d, check_library_reduction,
+              check_torch_sdpa, check_closed_forms, check_invariants,
+              check_blocked_equals_naive, check_brute_force]
+    caught = 0
+    for chk in checks:
+        try:
+            with np.errstate(all="ignore"):
+                if chk in (check_worked_example, check_online_softmax_1d):
+                    chk(orc)
+                else:
+                    chk(orc, np.random.default_rng(11))
+        except (AssertionError, ValueError, FloatingPointError):
+            caught += 1
+    assert caught >= 1, f"no pin caught the planted mistake '{name}'"
+
+
+# ---------------------------------------------------------------------------
+# 6. Input generator sanity (storage rounding only)
+# ---------------------------------------------------------------------------
+
+def test_bf16_rounding_is_nearest_even():
+    x = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 3.0e-3, 65504.0], np.float32)
+    bits = inputs.f32_to_bf16_bits(x)
+    back = inputs.bf16_bits_to_f64(bits)
+    # ties go to even mantissa; torch's conversion agrees
+    torch = pytest.importorskip("torch")
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(back, ref)
+
+
+def test_generator_is_seeded_and_spiky():
+    w = inputs.Workload("t", 1, 2, 300, 300, 64, inputs.BF16, "none", spiky_keys=True, seed=5)
+    a, b = inputs.generate(w), inputs.generate(w)
+    assert np.array_equal(a.k_bits, b.k_bits) and np.array_equal(a.q_bits, b.q_bits)
+    k = inputs.bits_to_f64(a.k_bits, inputs.BF16)
+    norms = np.abs(k).max(axis=-1)
+    for h in range(2):
+        assert (norms[0, h] > 8.0).sum() >= 1
+    assert len(inputs.WORKLOADS) == 5
