@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark: fused attention forward TFLOP/s (mask-adjusted) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload INDEX|NAME]
+
+One step = one fused forward (the whole hot path) over the workload's Q, K, V,
+already resident in device memory.  The default workload is the causal
+8192-token x 32-head, head dim 128, fp16 case.  L2 is flushed (a 256 MiB
+write) before every timed step; each step's kernel is timed with CUDA events
+on the launching stream.  Prints one JSON line (rank 0).
+
+With --gpus N > 1 (under torchrun) every rank runs an independent replica of
+the workload on its own GPU (the forward needs no exchange between ranks),
+time = max over ranks, value = N x per-replica FLOPs / time ("weak").
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_io_aware_30_gb300 import inputs, metrics  # noqa: E402
+
+DEFAULT_WORKLOAD = 2
+METRIC = "attention fwd TFLOP/s (mask-adjusted) and % of GB300 dense BF16 peak"
+FALLBACK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_NAME = "fa_fwd_kernel"
+
+
+# ----------------------------------------------------------------------------
+# helpers shared by both arms
+# ----------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def reduce_max_time(ms: float, world: int, device=None) -> float:
+    """Max over ranks of a per-rank time (identity when world == 1)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(flops_per_replica: float, n_replicas: int, max_ms: float) -> float:
+    """TFLOP/s of the whole job: every replica's work over the slowest rank's time."""
+    return flops_per_replica * n_replicas / (max_ms * 1e-3) / 1e12
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_digest() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_io_aware_30_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "fa_fwd_kernel_traffic.md")
+    if not os.path.exists(path):
+        return None
+    digest = kernel_source_digest()
+    pat = re.compile(r"^traffic\s+(\S+)\s+source=(\w+)\s+bytes_per_launch=(\d+)", re.M)
+    for m in pat.finditer(open(path).read()):
+        if m.group(1) == workload_name and m.group(2) == digest:
+            return int(m.group(3))
+    return None
+
+
+def physical_gpu_index(logical: int):
+    """nvidia-smi index of a CUDA device (None if it cannot be told)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if not vis:
+        return logical
+    parts = [p.strip() for p in vis.split(",")]
+    if logical < len(parts) and parts[logical].isdigit():
+        return int(parts[logical])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            sel = [f"--id={self.gpu}"] if self.gpu is not None else []
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *sel, f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the fp64 oracle on a bounded sample of the workload
+# ----------------------------------------------------------------------------
+
+def cpu_oracle_sample(w, inp=None, target_s: float = 12.0, threads: int | None = None):
+    """Time the oracle (as it stands) on a spread sample of query rows.
+
+    Returns (TFLOP/s, cores, description).  The sample is grown from a small
+    calibration run so that the timed call takes about target_s seconds.
+    """
+    import oracle
+    if threads:
+        oracle.set_threads(threads)
+    cores = oracle.max_threads()
+    if inp is None:
+        inp = inputs.generate(w)
+    qf, kf, vf = inp.f64()
+    BH, Sq = w.B * w.H, w.Sq
+    total = BH * Sq
+
+    def rows_and_flops(n):
+        idx = np.linspace(0, total - 1, num=min(n, total)).astype(np.int64)
+        i = idx % Sq
+        if w.mask == "none":
+            vis = np.full(i.shape, w.Sk)
+        elif w.mask == "causal":
+            vis = np.minimum(i + 1, w.Sk)
+        else:
+            vis = np.clip(np.minimum(i, w.Sk - 1) - np.maximum(0, i - w.window + 1) + 1, 0, None)
+        return idx, 4.0 * w.d * float(vis.sum())
+
+    n = 64
+    while True:
+        rows, fl = rows_and_flops(n)
+        t0 = time.perf_counter()
+        oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= 0.5 or n >= total:
+            break
+        n *= 4
+    n_final = int(min(total, max(64, n * target_s / max(dt, 1e-6))))
+    rows, fl = rows_and_flops(n_final)
+    t0 = time.perf_counter()
+    oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
+    dt = time.perf_counter() - t0
+    desc = (f"{len(rows)} of {total} query rows (evenly spaced over all heads), "
+            f"{fl / 1e9:.1f} GFLOP mask-adjusted, {dt:.1f} s, fp64 oracle")
+    return fl / dt / 1e12, cores, desc, dt
+
+
+# ----------------------------------------------------------------------------
+# arms
+# ----------------------------------------------------------------------------
+
+def run_ours(args, w):
+    import torch
+    from exact_io_aware_30_gb300 import build, fa
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.build()
+    fa.load()
+
+    inp = inputs.generate(w)
+    tdt = torch.bfloat16 if w.dtype == inputs.BF16 else torch.float16
+    host = [torch.from_numpy(b.view(np.int16)).view(tdt).pin_memory()
+            for b in (inp.q_bits, inp.k_bits, inp.v_bits)]
+    q, k, v = (t.to(dev) for t in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flops = metrics.attention_flops(w)
+
+    def step():
+        fa.forward(q, k, v, scale=w.scale, mask=w.mask, window=w.window, out=o, lse=lse,
+                   stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if fa.device_error() != fa.FA_OK:
+        raise RuntimeError("device pipeline timeout during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(physical_gpu_index(local if world > 1 else 0))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    for i in range(args.steps):
+        flush.fill_(1.0)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = float(np.mean(kernel_ms))
+    # end-to-end through the public API from pinned host buffers
+    e2e_steps = max(3, min(args.steps, 20))
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        qd = host[0].to(dev, non_blocking=True)
+        kd = host[1].to(dev, non_blocking=True)
+        vd = host[2].to(dev, non_blocking=True)
+        fa.forward(qd, kd, vd, scale=w.scale, mask=w.mask, window=w.window, out=o, lse=lse,
+                   stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if fa.device_error() != fa.FA_OK:
+        raise RuntimeError("device pipeline timeout during the timed region")
+
+    max_ms = reduce_max_time(ms, world, dev)
+    max_e2e = reduce_max_time(e2e_ms, world, dev)
+    value = whole_job_value(flops, world, max_ms)
+    peak_tf, _, peak_src = load_peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    result = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            tf, cores, desc, _ = cpu_oracle_sample(w, inp)
+            cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                   "sample": desc}
+        result = {
+            "metric": METRIC,
+            "value": value,
+            "unit": "TFLOP/s",
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": max_ms,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16" if w.dtype == inputs.FP16 else "bf16",
+            "data": "synthetic (seeded N(0,1), rounded to the 16-bit type)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk,
+                       "head_dim": w.d, "mask": w.mask, "window": w.window,
+                       "flops_per_step": flops, "l2": "flushed (256 MiB write) before every step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "kernel": fa.describe(w.d, w.mask,
+                                             fa.DTYPE_FP16 if w.dtype == inputs.FP16 else fa.DTYPE_BF16)},
+            "pct_of_peak": 100.0 * achieved / peak_tf,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf,
+                         "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                         "peak_source": f"{peak_src} dense bf16 (fp16 has the same nominal rate)",
+                         "traffic": recorded_traffic(w.name),
+                         "algorithmic_bytes": metrics.algorithmic_bytes(w),
+                         "kernel": KERNEL_NAME, "kernel_ms_median": float(np.median(kernel_ms)),
+                         "kernel_ms_min": float(np.min(kernel_ms))},
+            "cpu_baseline": cpu,
+            "e2e": {"value": whole_job_value(flops, world, max_e2e), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in host)),
+                    "d2h_bytes_per_step": int(o.numel() * o.element_size()
+                                              + lse.numel() * lse.element_size()),
+                    "ms_per_step": max_e2e},
+            "gpu_launches": args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return result
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    inp = inputs.generate(w)
+    # each step: a bounded sample of the workload, sized so that warm-up plus
+    # the timed steps stay within a few minutes
+    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, inp, target_s=per_step * 0.25)
+    vals, times, desc, cores = [], [], "", 0
+    for _ in range(args.steps):
+        tf, cores, desc, dt = cpu_oracle_sample(w, inp, target_s=per_step)
+        vals.append(tf)
+        times.append(dt)
+    value = float(np.mean(vals))
+    result = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": float(np.mean(times)) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1), rounded to the 16-bit type)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk,
+                   "head_dim": w.d, "mask": w.mask, "window": w.window},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=str(DEFAULT_WORKLOAD))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    wl = int(args.workload) if args.workload.isdigit() else args.workload
+    w = inputs.workload(wl)
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,290 @@
+// fa_api.cu -- host side of the C ABI declared in include/fa.h: argument
+// validation, TMA tensor-map encoding, kernel selection and launch.
+//
+// Validation happens before anything is enqueued and never falls back to a
+// different kernel: an unsupported head dim, dtype or mask is an error
+// ("FlashAttention: IO-aware attention kernels", section "Failure modes" --
+// a silent fallback is the failure to avoid).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool probed = false;
+    bool supported = false;
+    int num_sms = 0;
+    bool attr_set[6] = {false, false, false, false, false, false};
+};
+
+std::mutex g_mutex;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_probed = false;
+
+bool log_enabled() {
+    const char *e = std::getenv("FA_LOG");
+    return e && e[0] && e[0] != '0';
+}
+
+// Probe the current device once: compute capability 10.3 and SM count.
+fa_status device_info(int *dev_out, DeviceInfo **info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.probed) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return FA_ERR_CUDA;
+        d.supported = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        d.probed = true;
+    }
+    *dev_out = dev;
+    *info = &d;
+    return d.supported ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encode_probed) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult qres;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &qres) == cudaSuccess &&
+            qres == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        g_encode_probed = true;
+    }
+    return g_encode;
+}
+
+// 4-D map over a contiguous [B, H, S, d] 16-bit tensor: dims {d, S, H, B},
+// box {64, rows, 1, 1}, 128-byte swizzle.  Rows past S read as zero, per
+// head, because S is its own dimension.
+bool make_map(CUtensorMap *m, const void *base, int d, int S, int H, int B, int rows, bool fp16) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)S, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[3] = {(cuuint64_t)d * e, (cuuint64_t)S * d * e, (cuuint64_t)H * S * d * e};
+    cuuint32_t box[4] = {64, (cuuint32_t)rows, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(m, fp16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                     const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int head_dim_index(int d) { return d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : -1; }
+
+int nq_for(int d) { return d == 256 ? Cfg<256>::NQ : d == 128 ? Cfg<128>::NQ : Cfg<64>::NQ; }
+int bn_for(int d) { return d == 256 ? Cfg<256>::BN : d == 128 ? Cfg<128>::BN : Cfg<64>::BN; }
+int slots_for(int d) {
+    return d == 256 ? Cfg<256>::SLOTS : d == 128 ? Cfg<128>::SLOTS : Cfg<64>::SLOTS;
+}
+
+// Size / kind checks shared by fa_fwd and fa_workspace_query.
+fa_status check_sizes(int B, int H, int Sq, int Sk, int d, int mask_kind, int window, int dtype) {
+    if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
+    if (head_dim_index(d) < 0) return FA_ERR_UNSUPPORTED;
+    if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL &&
+        mask_kind != FA_MASK_SLIDING_WINDOW)
+        return FA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || Sk < 1 || Sq < 0) return FA_ERR_INVALID_ARG;
+    if (mask_kind == FA_MASK_SLIDING_WINDOW && window < 1) return FA_ERR_INVALID_ARG;
+    const long long nq = nq_for(d);
+    const long long groups = ((long long)Sq + 128 * nq - 1) / (128 * nq);
+    if ((long long)B * H * groups > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+template <int D, bool kFP16>
+fa_status launch(const Params &p, int num_sms, DeviceInfo &info, cudaStream_t stream) {
+    using C = Cfg<D>;
+    auto kern = fa_fwd_kernel<D, kFP16>;
+    const int slot = head_dim_index(D) * 2 + (kFP16 ? 1 : 0);
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!info.attr_set[slot]) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::SMEM_BYTES) != cudaSuccess)
+                return FA_ERR_CUDA;
+            // The warpgroup register re-balance inside the kernel assumes the
+            // launch allocation it was designed for; never launch otherwise.
+            cudaFuncAttributes attr;
+            if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FA_ERR_CUDA;
+            if (C::REBALANCE && attr.numRegs != C::REG_LAUNCH) return FA_ERR_UNSUPPORTED;
+            info.attr_set[slot] = true;
+        }
+    }
+    const int grid = p.n_units < num_sms ? p.n_units : num_sms;
+    kern<<<grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                   int Sq, int Sk, int d, float scale, int mask_kind, int window, int dtype,
+                   cudaStream_t stream) {
+    fa_status st = check_sizes(B, H, Sq, Sk, d, mask_kind, window, dtype);
+    if (st != FA_OK) return st;
+    if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+    const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+    if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
+    const size_t qo_bytes = (size_t)B * H * Sq * d * 2, kv_bytes = (size_t)B * H * Sk * d * 2;
+    const size_t lse_bytes = (size_t)B * H * Sq * 4;
+    if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
+        overlaps(o, qo_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, o, qo_bytes) ||
+        overlaps(lse, lse_bytes, q, qo_bytes) || overlaps(lse, lse_bytes, k, kv_bytes) ||
+        overlaps(lse, lse_bytes, v, kv_bytes))
+        return FA_ERR_INVALID_ARG;
+
+    int dev = 0;
+    DeviceInfo *info = nullptr;
+    st = device_info(&dev, &info);
+    if (st != FA_OK) return st;
+    if (Sq == 0) return FA_OK;
+
+    const bool fp16 = dtype == FA_DTYPE_FP16;
+    const int nq = nq_for(d), bn = bn_for(d);
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_q, q, d, Sq, H, B, 128, fp16) || !make_map(&p.tm_k, k, d, Sk, H, B, bn, fp16) ||
+        !make_map(&p.tm_v, v, d, Sk, H, B, bn, fp16))
+        return FA_ERR_CUDA;
+    p.o = o;
+    p.lse = lse;
+    p.B = B;
+    p.H = H;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.mask_kind = mask_kind;
+    p.window = (mask_kind == FA_MASK_SLIDING_WINDOW) ? window : 0;
+    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    p.n_qtiles = (Sq + 127) / 128;
+    p.n_groups = (p.n_qtiles + nq - 1) / nq;
+    p.n_units = B * H * p.n_groups;
+
+    if (log_enabled()) {
+        char buf[256];
+        fa_describe(d, mask_kind, dtype, buf, sizeof buf);
+        std::fprintf(stderr, "[fa] %s B=%d H=%d Sq=%d Sk=%d units=%d grid=%d\n", buf, B, H, Sq, Sk,
+                     p.n_units, p.n_units < info->num_sms ? p.n_units : info->num_sms);
+    }
+
+    switch (d) {
+        case 64:
+            return fp16 ? launch<64, true>(p, info->num_sms, *info, stream)
+                        : launch<64, false>(p, info->num_sms, *info, stream);
+        case 128:
+            return fp16 ? launch<128, true>(p, info->num_sms, *info, stream)
+                        : launch<128, false>(p, info->num_sms, *info, stream);
+        case 256:
+            return fp16 ? launch<256, true>(p, info->num_sms, *info, stream)
+                        : launch<256, false>(p, info->num_sms, *info, stream);
+        default:
+            return FA_ERR_UNSUPPORTED;
+    }
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
+                 int Sq, int Sk, int d, float scale, int mask_kind, int window,
+                 fa_stream_t stream) {
+    return fa::fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, d, scale, mask_kind, window, FA_DTYPE_BF16,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                      int H, int Sq, int Sk, int d, float scale, int mask_kind, int window,
+                      fa_stream_t stream) {
+    return fa::fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, d, scale, mask_kind, window, FA_DTYPE_FP16,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_workspace_query(int B, int H, int Sq, int Sk, int d, int mask_kind, int window,
+                             int dtype, size_t *bytes) {
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    *bytes = 0;
+    fa_status st = fa::check_sizes(B, H, Sq, Sk, d, mask_kind, window, dtype);
+    if (st != FA_OK) return st;
+    int dev = 0;
+    fa::DeviceInfo *info = nullptr;
+    return fa::device_info(&dev, &info);
+}
+
+const char *fa_status_string(fa_status s) {
+    switch (s) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG: invalid size, pointer, window or scale";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED: head dim, dtype, mask kind or GPU not supported";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED: q/k/v/o need 16-byte alignment, lse 4-byte";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA call or the kernel launch failed";
+        case FA_ERR_DEVICE_TIMEOUT: return "FA_ERR_DEVICE_TIMEOUT: a kernel pipeline wait timed out";
+        default: return "FA_ERR_UNKNOWN";
+    }
+}
+
+fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
+    if (!buf || len == 0) return FA_ERR_INVALID_ARG;
+    fa_status st = fa::check_sizes(1, 1, 1, 1, d, mask_kind, 1, dtype);
+    if (st != FA_OK) {
+        std::snprintf(buf, len, "unsupported");
+        return st;
+    }
+    static const char *masks[] = {"none", "causal", "sliding_window"};
+    std::snprintf(buf, len,
+                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d q_tiles_per_cta=%d "
+                  "kv_ring=%d threads=%d smem=%d mask=%s persistent",
+                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::nq_for(d),
+                  fa::slots_for(d), 32 * (4 * fa::nq_for(d) + 2),
+                  d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES
+                                                               : fa::Cfg<256>::SMEM_BYTES,
+                  masks[mask_kind]);
+    return FA_OK;
+}
+
+fa_status fa_get_device_error(void) {
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    if (v == 0) return FA_OK;
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_fa_status, &zero, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_ERR_DEVICE_TIMEOUT;
+}
+
+}  // extern "C"

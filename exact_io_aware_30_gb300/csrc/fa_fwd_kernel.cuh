@@ -1,0 +1,756 @@
+// fa_fwd_kernel.cuh -- fused exact attention forward for sm_103a (GB300).
+//
+// What it computes: for every (batch, head) and query row i,
+//   O_i = sum_j softmax_j(scale * q_i . k_j) v_j   over the keys j visible to i,
+//   lse_i = ln sum_j exp(scale * q_i . k_j),
+// by the tiled forward pass with the online softmax ("FlashAttention: Why
+// Tiling Attention Makes Transformers Fast Without Changing the Result",
+// sections "Online softmax: correct as you go" and "The tiled forward pass";
+// "Flash attention and memory-efficient attention variants", section "Tiling
+// and the running (online) softmax"): key/value tiles stream through shared
+// memory, each query row keeps a running max m, a running sum l and an
+// unnormalised accumulator rescaled by exp(m_old - m_new), and the row is
+// divided by l once at the end.  Score and probability tiles live only in
+// tensor memory.
+//
+// GB300 mapping (one CTA per SM, persistent over work units):
+//   * a work unit is NQ query tiles of 128 rows of one (batch, head);
+//     units are taken longest-first in a snake order over the CTAs;
+//   * one TMA warp streams Q tiles and a ring of K / V tiles (128-byte
+//     swizzled, 64 columns per box) into shared memory under mbarriers;
+//   * one MMA warp (a single issuing lane) runs S = Q K^T (both operands in
+//     shared memory) and O += P V (P read from tensor memory) as tcgen05
+//     MMAs with fp32 accumulators in tensor memory;
+//   * NQ softmax warpgroups own one query row per thread (= one TMEM lane):
+//     they read a row of S, apply the mask on boundary tiles only, update the
+//     running max / sum, write P (16-bit) back over S, rescale O in tensor
+//     memory when the max grew enough, and run the epilogue (O / l, lse).
+//   With NQ = 2 the two warpgroups ping-pong: the tensor core computes one
+//   tile's MMAs while the other tile's softmax runs.
+//
+// Rescaling is deferred until the running max has grown by more than 2^8
+// (log2 units).  Until then the accumulator and the sum both stay referenced
+// to the same stale max, so the final O_acc / l is unchanged (the pages'
+// remark that FlashAttention-2 "defers most rescaling"); the stale reference
+// only lets unnormalised weights reach 2^8, far from fp32/bf16 limits.
+#pragma once
+
+#include <stdint.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;  // query rows per tile = M of every MMA = TMEM lanes
+constexpr int kMaskNone = 0;
+constexpr int kMaskCausal = 1;
+constexpr int kMaskWindow = 2;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+constexpr float kRescaleLog2 = 8.0f;              // rescale O when the max grows > 2^8
+constexpr float kLn2 = 0.693147180559945309f;
+
+// Device status word: 0 = fine; else 0x100 + the wait site that timed out.
+// (This header is compiled into exactly one translation unit.)
+__device__ int g_fa_status = 0;
+
+struct Params {
+    CUtensorMap tm_q;  // [B, H, Sq, d] 16-bit, box {64, 128, 1, 1}, 128-B swizzle
+    CUtensorMap tm_k;  // [B, H, Sk, d], box {64, BN, 1, 1}
+    CUtensorMap tm_v;  // [B, H, Sk, d], box {64, BN, 1, 1}
+    void *o;           // [B, H, Sq, d] 16-bit
+    float *lse;        // [B, H, Sq] fp32
+    int B, H, Sq, Sk;
+    int mask_kind, window;
+    float scale_log2;  // scale * log2(e)
+    int n_qtiles;      // ceil(Sq / 128)
+    int n_groups;      // ceil(n_qtiles / NQ): units per (batch, head)
+    int n_units;       // B * H * n_groups
+};
+
+template <int D>
+struct Cfg {
+    static constexpr int BN = (D == 256) ? 64 : 128;   // keys per K/V tile
+    static constexpr int NQ = (D == 256) ? 1 : 2;      // query tiles per unit
+    static constexpr int SLOTS = (D == 64) ? 8 : 4;    // K/V ring depth (tiles)
+    // Warps: NQ softmax warpgroups, then the MMA warp and the TMA warp.  With
+    // two softmax warpgroups the last warpgroup is padded to four warps so
+    // that registers can be moved to the softmax warpgroups (setmaxnreg acts
+    // per warpgroup): at launch 384 threads x 168 registers; afterwards
+    // 2 x 128 x REG_SOFTMAX + 128 x REG_OTHER, which must not exceed that.
+    static constexpr int NUM_WARPS = (NQ == 2) ? 12 : 6;
+    static constexpr int NUM_THREADS = 32 * NUM_WARPS;
+    static constexpr int MMA_WARP = 4 * NQ;
+    static constexpr int TMA_WARP = 4 * NQ + 1;
+    static constexpr bool REBALANCE = (NQ == 2);
+    static constexpr int REG_LAUNCH = 168;
+    static constexpr int REG_SOFTMAX = 224;
+    static constexpr int REG_OTHER = 56;
+    static_assert(!REBALANCE || 2 * 128 * REG_SOFTMAX + 128 * REG_OTHER <= NUM_THREADS * REG_LAUNCH,
+                  "register split exceeds the launch allocation");
+    static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
+    static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
+    static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
+    static constexpr int Q_BYTES = kBM * D * 2;
+    static constexpr int SLOT_BYTES = BN * D * 2;
+    // Tensor memory: S/P buffers 0,1 at columns 0 and BN; O accumulators from 256.
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = BN;              // column stride between S buffers
+    static constexpr uint32_t O_COL0 = 256;
+    // Barrier indices.
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_QEMPTY = B_QFULL + NQ;
+    static constexpr int B_KVFULL = B_QEMPTY + NQ;
+    static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
+    static constexpr int B_SFULL = B_KVEMPTY + SLOTS;
+    static constexpr int B_PFULL = B_SFULL + 2;
+    static constexpr int B_OFULL = B_PFULL + 2;
+    static constexpr int B_OFREE = B_OFULL + NQ;
+    static constexpr int B_DRAIN = B_OFREE + NQ;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SMEM_TILES = NQ * Q_BYTES + SLOTS * SLOT_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
+    static_assert(O_COL0 + NQ * D <= TMEM_COLS, "tensor memory overflow");
+    static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
+    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+};
+
+// ---------------------------------------------------------------- helpers
+
+// Shared-memory matrix descriptor, 128-byte swizzle, tcgen05 format.
+// K-major operands: rows of 128 bytes, 8-row groups 1024 bytes apart (SBO);
+// the leading offset is unused.  MN-major (V as the B operand of P V): 8-row
+// groups along K 1024 bytes apart (SBO), 64-element column boxes `lbo` apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, A/B bf16 or fp16,
+// A K-major, B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool fp16, bool b_mn_major) {
+    return (1u << 4) | ((fp16 ? 0u : 1u) << 7) | ((fp16 ? 0u : 1u) << 10) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
+
+// Bounded wait: gives up (and raises the abort flag and the device status
+// word) after kWaitLimitNs, or as soon as another role has aborted.
+__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           int site) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicCAS(&g_fa_status, 0, 0x100 + site);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                         int site) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return wait_bar_slow(bar, parity, abort_flag, site);
+}
+
+// Wait used only while shutting down after an abort: ignores the abort flag.
+__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
+    }
+}
+
+// Unit k of this CTA in a snake order: even rounds left to right, odd rounds
+// right to left, so that with units sorted longest-first each CTA's sum of
+// work stays close to the others'.
+__device__ __forceinline__ int unit_at(int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return (k & 1) ? k * G + (G - 1 - c) : k * G + c;
+}
+
+template <int D>
+struct Unit {
+    int b, h;
+    int i0[Cfg<D>::NQ];     // first query row of each tile
+    int lo[Cfg<D>::NQ];     // K/V tile range [lo, hi) each tile must visit
+    int hi[Cfg<D>::NQ];
+    bool exists[Cfg<D>::NQ];  // tile has rows < Sq
+    bool valid[Cfg<D>::NQ];   // exists and sees at least one key tile
+    int ulo, uhi;             // union of the valid ranges
+    bool any;
+};
+
+// Key tiles a query tile [i0, i0 + 128) has to visit: skip tiles the mask
+// hides entirely (causal: keys past the last row; window: keys before the
+// first row's window).
+template <int D>
+__device__ __forceinline__ void kv_range(int i0, const Params &p, int &lo, int &hi) {
+    constexpr int BN = Cfg<D>::BN;
+    const int row_end = min(i0 + kBM, p.Sq);
+    int key_end = p.Sk;
+    if (p.mask_kind != kMaskNone) key_end = min(p.Sk, row_end);
+    int key_beg = 0;
+    if (p.mask_kind == kMaskWindow) key_beg = max(0, i0 - p.window + 1);
+    if (key_beg >= key_end) {
+        lo = 0;
+        hi = 0;
+        return;
+    }
+    lo = key_beg / BN;
+    hi = (key_end + BN - 1) / BN;
+}
+
+template <int D>
+__device__ __forceinline__ void decode_unit(int u, const Params &p, Unit<D> &un) {
+    constexpr int NQ = Cfg<D>::NQ;
+    const int BH = p.B * p.H;
+    const int gi = u / BH;
+    const int bh = u - gi * BH;
+    const int g = p.n_groups - 1 - gi;  // longest first (causal / window)
+    un.b = bh / p.H;
+    un.h = bh - un.b * p.H;
+    un.ulo = 0x7fffffff;
+    un.uhi = 0;
+    un.any = false;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const int i0 = (g * NQ + q) * kBM;
+        un.i0[q] = i0;
+        un.exists[q] = i0 < p.Sq;
+        un.lo[q] = 0;
+        un.hi[q] = 0;
+        if (un.exists[q]) kv_range<D>(i0, p, un.lo[q], un.hi[q]);
+        un.valid[q] = un.exists[q] && un.lo[q] < un.hi[q];
+        if (un.valid[q]) {
+            un.ulo = min(un.ulo, un.lo[q]);
+            un.uhi = max(un.uhi, un.hi[q]);
+            un.any = true;
+        }
+    }
+}
+
+// True if some (row, key) pair of this query tile x key tile is hidden.
+template <int D>
+__device__ __forceinline__ bool tile_needs_mask(int i0, int j, const Params &p) {
+    constexpr int BN = Cfg<D>::BN;
+    const int k0 = j * BN;
+    if (k0 + BN > p.Sk) return true;
+    if (p.mask_kind == kMaskNone) return false;
+    if (k0 + BN - 1 > i0) return true;
+    if (p.mask_kind == kMaskWindow && k0 <= i0 + kBM - 1 - p.window) return true;
+    return false;
+}
+
+// ---------------------------------------------------------------- TMA role
+
+template <int D>
+__device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
+                         volatile int *abort_flag) {
+    using C = Cfg<D>;
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    const uint64_t pol_q = ptx::policy_evict_first();
+    uint32_t kv_it = 0;
+    uint32_t q_cnt[C::NQ];
+#pragma unroll
+    for (int q = 0; q < C::NQ; ++q) q_cnt[q] = 0;
+    bool ok = true;
+
+    for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= p.n_units) break;
+        Unit<D> un;
+        decode_unit<D>(u, p, un);
+        if (!un.any) continue;
+#pragma unroll
+        for (int q = 0; q < C::NQ; ++q) {
+            if (!un.valid[q] || !ok) continue;
+            if (!wait_bar(bar_addr(bars, C::B_QEMPTY + q), (q_cnt[q] & 1) ^ 1, abort_flag, 1)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = bar_addr(bars, C::B_QFULL + q);
+            ptx::mbar_arrive_expect_tx(fb, C::Q_BYTES);
+            const uint32_t dst = ptx::smem_addr(sQ + q * C::Q_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::CHUNKS; ++c)
+                ptx::tma_load_4d(dst + c * C::Q_CHUNK, &p.tm_q, fb, c * 64, un.i0[q], un.h, un.b,
+                                 pol_q);
+            ++q_cnt[q];
+        }
+        for (int j = un.ulo; j < un.uhi && ok; ++j) {
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {
+                const uint32_t slot = kv_it % C::SLOTS;
+                if (!wait_bar(bar_addr(bars, C::B_KVEMPTY + slot), ((kv_it / C::SLOTS) & 1) ^ 1,
+                              abort_flag, 2)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_addr(bars, C::B_KVFULL + slot);
+                ptx::mbar_arrive_expect_tx(fb, C::SLOT_BYTES);
+                const uint32_t dst = ptx::smem_addr(sKV + slot * C::SLOT_BYTES);
+                const CUtensorMap *m = kv ? &p.tm_v : &p.tm_k;
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    ptx::tma_load_4d(dst + c * C::KV_CHUNK, m, fb, c * 64, j * C::BN, un.h, un.b,
+                                     pol_kv);
+                ++kv_it;
+            }
+        }
+    }
+    if (!ok) {
+        // Let every copy already issued land before the CTA can exit.
+        // Slot s has been filled ceil((kv_it - s) / SLOTS) times so far.
+#pragma unroll
+        for (int s = 0; s < C::SLOTS; ++s) {
+            const uint32_t fills = kv_it > (uint32_t)s ? (kv_it - (uint32_t)s + C::SLOTS - 1) / C::SLOTS : 0u;
+            if (fills) wait_bar_drain(bar_addr(bars, C::B_KVFULL + s), (fills - 1) & 1);
+        }
+#pragma unroll
+        for (int q = 0; q < C::NQ; ++q)
+            if (q_cnt[q]) wait_bar_drain(bar_addr(bars, C::B_QFULL + q), (q_cnt[q] - 1) & 1);
+    }
+}
+
+// ---------------------------------------------------------------- MMA role
+
+template <int D, bool kFP16>
+__device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
+                         uint32_t tmem, volatile int *abort_flag) {
+    using C = Cfg<D>;
+    constexpr int NQ = C::NQ;
+    constexpr uint32_t kIdescS = make_idesc(kBM, C::BN, kFP16, false);
+    constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
+
+    uint32_t kv_it = 0;
+    uint32_t q_cnt[NQ], p_cnt[2], ofree_cnt[NQ];
+    bool o_used[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        q_cnt[q] = 0;
+        ofree_cnt[q] = 0;
+        o_used[q] = false;
+    }
+    p_cnt[0] = p_cnt[1] = 0;
+    uint32_t t_cnt = 0;  // tiles issued (NQ == 1: S buffer = t & 1)
+    bool ok = true;
+
+    for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= p.n_units) break;
+        Unit<D> un;
+        decode_unit<D>(u, p, un);
+        if (!un.any) continue;
+        const uint32_t kv_base = kv_it;
+
+        auto wait_kv = [&](uint32_t idx) -> bool {
+            return wait_bar(bar_addr(bars, C::B_KVFULL + idx % C::SLOTS), (idx / C::SLOTS) & 1,
+                            abort_flag, 3);
+        };
+        auto release_kv = [&](uint32_t idx) { ptx::mma_commit(bar_addr(bars, C::B_KVEMPTY + idx % C::SLOTS)); };
+        auto kidx = [&](int j) -> uint32_t { return kv_base + 2u * (uint32_t)(j - un.ulo); };
+        // S_b = Q_q K_j^T
+        auto issue_s = [&](int q, int j, int b) {
+            const uint32_t slot = kidx(j) % C::SLOTS;
+            const uint32_t a0 = ptx::smem_addr(sQ + q * C::Q_BYTES);
+            const uint32_t b0 = ptx::smem_addr(sKV + slot * C::SLOT_BYTES);
+            const uint32_t d_tmem = tmem + (uint32_t)b * C::S_COL;
+            const uint64_t da = smem_desc(a0, 16), db = smem_desc(b0, 16);
+#pragma unroll 1
+            for (int kk = 0; kk < D / 16; ++kk) {
+                // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
+                const uint32_t off_a = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
+                const uint32_t off_b = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
+                ptx::mma_ss(d_tmem, da + off_a, db + off_b, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
+        };
+        // O_q (+)= P_b V_j
+        auto issue_pv = [&](int q, int j, int b, bool first) {
+            const uint32_t slot = (kidx(j) + 1) % C::SLOTS;
+            const uint32_t v0 = ptx::smem_addr(sKV + slot * C::SLOT_BYTES);
+            const uint32_t d_tmem = tmem + C::O_COL0 + (uint32_t)q * D;
+            const uint32_t p_tmem = tmem + (uint32_t)b * C::S_COL;
+            const uint64_t dv = smem_desc(v0, C::KV_CHUNK);
+#pragma unroll 1
+            for (int kk = 0; kk < C::BN / 16; ++kk) {
+                // 16 keys = two 8-row groups (2048 bytes) per step; P: 8 columns.
+                ptx::mma_ts(d_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4), kIdescO,
+                            (!first || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(bar_addr(bars, C::B_OFULL + q));
+        };
+        auto wait_p = [&](int b, uint32_t parity) -> bool {
+            if (!wait_bar(bar_addr(bars, C::B_PFULL + b), parity, abort_flag, 4)) return false;
+            ptx::tc_fence_after();
+            return true;
+        };
+        auto wait_ofree = [&](int q) -> bool {
+            if (!o_used[q]) return true;
+            const bool r = wait_bar(bar_addr(bars, C::B_OFREE + q), ofree_cnt[q] & 1, abort_flag, 5);
+            ++ofree_cnt[q];
+            ptx::tc_fence_after();
+            return r;
+        };
+
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            if (!un.valid[q] || !ok) continue;
+            ok = wait_bar(bar_addr(bars, C::B_QFULL + q), q_cnt[q] & 1, abort_flag, 6);
+        }
+        if (!ok) break;
+
+        if constexpr (NQ == 2) {
+            // Prologue: first S of every tile that starts at the union's first tile.
+            if (!wait_kv(kidx(un.ulo))) { ok = false; break; }
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+                if (un.valid[q] && un.lo[q] == un.ulo) issue_s(q, un.ulo, q);
+            release_kv(kidx(un.ulo));
+            for (int j = un.ulo; j < un.uhi && ok; ++j) {
+                bool v_ready = false, k_ready = false;
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    if (!un.valid[q] || !ok) continue;
+                    if (j >= un.lo[q] && j < un.hi[q]) {
+                        if (!v_ready) {
+                            if (!wait_kv(kidx(j) + 1)) { ok = false; break; }
+                            v_ready = true;
+                        }
+                        if (!wait_p(q, p_cnt[q] & 1)) { ok = false; break; }
+                        ++p_cnt[q];
+                        if (j == un.lo[q] && !wait_ofree(q)) { ok = false; break; }
+                        issue_pv(q, j, q, j == un.lo[q]);
+                        if (j + 1 < un.hi[q]) {
+                            if (!k_ready) {
+                                if (!wait_kv(kidx(j + 1))) { ok = false; break; }
+                                k_ready = true;
+                            }
+                            issue_s(q, j + 1, q);
+                        }
+                    } else if (j + 1 == un.lo[q]) {
+                        if (!k_ready) {
+                            if (!wait_kv(kidx(j + 1))) { ok = false; break; }
+                            k_ready = true;
+                        }
+                        issue_s(q, j + 1, q);
+                    }
+                }
+                if (!ok) break;
+                release_kv(kidx(j) + 1);
+                if (j + 1 < un.uhi) {
+                    if (!k_ready && !wait_kv(kidx(j + 1))) { ok = false; break; }
+                    release_kv(kidx(j + 1));
+                }
+            }
+        } else {
+            // One query tile, S double-buffered across consecutive key tiles.
+            const uint32_t t0 = t_cnt;
+            if (!wait_kv(kidx(un.ulo))) { ok = false; break; }
+            issue_s(0, un.ulo, t0 & 1);
+            release_kv(kidx(un.ulo));
+            if (un.ulo + 1 < un.uhi) {
+                if (!wait_kv(kidx(un.ulo + 1))) { ok = false; break; }
+                issue_s(0, un.ulo + 1, (t0 + 1) & 1);
+                release_kv(kidx(un.ulo + 1));
+            }
+            for (int j = un.ulo; j < un.uhi; ++j) {
+                const uint32_t t = t0 + (uint32_t)(j - un.ulo);
+                const int b = t & 1;
+                if (!wait_kv(kidx(j) + 1)) { ok = false; break; }
+                if (!wait_p(b, (t >> 1) & 1)) { ok = false; break; }
+                if (j == un.ulo && !wait_ofree(0)) { ok = false; break; }
+                issue_pv(0, j, b, j == un.ulo);
+                release_kv(kidx(j) + 1);
+                if (j + 2 < un.uhi) {
+                    if (!wait_kv(kidx(j + 2))) { ok = false; break; }
+                    issue_s(0, j + 2, b);
+                    release_kv(kidx(j + 2));
+                }
+            }
+            t_cnt = t0 + (uint32_t)(un.uhi - un.ulo);
+        }
+        if (!ok) break;
+        kv_it = kv_base + 2u * (uint32_t)(un.uhi - un.ulo);
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+            if (!un.valid[q]) continue;
+            ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + q));
+            ++q_cnt[q];
+            o_used[q] = true;
+        }
+    }
+    // Every MMA issued must finish before tensor memory is released.
+    ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+// ---------------------------------------------------------------- softmax role
+
+// One thread's row of an S tile (BN fp32 columns) from tensor memory.
+template <int BN>
+__device__ __forceinline__ void load_s_row(uint32_t taddr, uint32_t (&r)[BN]) {
+    ptx::tmem_ld_x32<0>(taddr, r);
+    ptx::tmem_ld_x32<32>(taddr + 32, r);
+    if constexpr (BN == 128) {
+        ptx::tmem_ld_x32<64>(taddr + 64, r);
+        ptx::tmem_ld_x32<96>(taddr + 96, r);
+    }
+}
+
+// One thread's row of P (BN 16-bit values packed in BN/2 columns) to tensor memory.
+template <int BN>
+__device__ __forceinline__ void store_p_row(uint32_t taddr, const uint32_t (&r)[BN / 2]) {
+    ptx::tmem_st_x32<0>(taddr, r);
+    if constexpr (BN == 128) ptx::tmem_st_x32<32>(taddr + 32, r);
+}
+
+template <int D, bool kFP16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
+}
+
+template <int D, bool kFP16>
+__device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tmem,
+                             volatile int *abort_flag) {
+    using C = Cfg<D>;
+    constexpr int NQ = C::NQ;
+    constexpr int BN = C::BN;
+    const int tid = threadIdx.x - wg * 128;                // query row within the tile
+    const uint32_t lane_off = (uint32_t)((tid >> 5) * 32) << 16;  // this warp's TMEM lanes
+    const int q = (NQ == 2) ? wg : 0;
+    const float c = p.scale_log2;
+    uint32_t t_cnt = 0;  // S tiles consumed
+    uint32_t o_cnt = 0;  // O completions consumed
+    bool ok = true;
+
+    for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= p.n_units) break;
+        Unit<D> un;
+        decode_unit<D>(u, p, un);
+        if (!un.exists[q]) continue;
+        const int row = un.i0[q] + tid;
+        const bool row_ok = row < p.Sq;
+        const size_t row_flat = ((size_t)(un.b * p.H + un.h)) * (size_t)p.Sq + (size_t)row;
+        if (!un.valid[q]) {
+            // No key visible to any row of this tile: guarded output.
+            if (row_ok) {
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
+#pragma unroll
+                for (int cc = 0; cc < D / 8; ++cc) ptx::st_global_v4(orow + cc * 16, 0, 0, 0, 0);
+                p.lse[row_flat] = -INFINITY;
+            }
+            continue;
+        }
+        // Visible key columns of this row, as absolute key indices [key_lo, key_hi].
+        const int key_hi = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row, p.Sk - 1);
+        const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
+
+        float m_ref = -INFINITY;  // max the accumulator and sum are referenced to (log2 units)
+        float l = 0.f;
+        const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)q * D;
+
+        for (int j = un.lo[q]; j < un.hi[q]; ++j) {
+            const uint32_t t = t_cnt++;
+            const int b = (NQ == 2) ? q : (int)(t & 1);
+            const uint32_t par = (NQ == 2) ? (t & 1) : ((t >> 1) & 1);
+            if (!wait_bar(bar_addr(bars, C::B_SFULL + b), par, abort_flag, 7)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t s_tmem = tmem + lane_off + (uint32_t)b * C::S_COL;
+
+            uint32_t sr[BN];
+            load_s_row<BN>(s_tmem, sr);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<BN>(sr);
+
+            const bool masked = tile_needs_mask<D>(un.i0[q], j, p);
+            if (masked) {
+                const int c_lo = key_lo - j * BN, c_hi = key_hi - j * BN;
+#pragma unroll
+                for (int i = 0; i < BN; ++i)
+                    if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
+            }
+            // Row max of this tile (raw scores; scale >= 0 keeps the order).
+            float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+            float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+            for (int i = 4; i < BN; i += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(sr[i]));
+                mx1 = fmaxf(mx1, __uint_as_float(sr[i + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(sr[i + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(sr[i + 3]));
+            }
+            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
+            const float m_new = fmaxf(m_ref, m_tile);
+
+            float alpha = 1.f;
+            bool rescale = false;
+            if (j > un.lo[q]) {
+                // The previous P V of this tile must be complete before O is touched.
+                if (!wait_bar(bar_addr(bars, C::B_OFULL + q), o_cnt & 1, abort_flag, 8)) { ok = false; break; }
+                ++o_cnt;
+                ptx::tc_fence_after();
+                if (m_new > m_ref + kRescaleLog2) {
+                    alpha = ptx::ex2_approx(m_ref - m_new);  // 0 while m_ref is -inf
+                    m_ref = m_new;
+                    rescale = true;
+                }
+            } else {
+                m_ref = m_new;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t ov[32];
+                    ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence<32>(ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+                    ptx::tmem_st_x32<0>(o_tmem + cc * 32, ov);
+                }
+            }
+            // Unnormalised probabilities against m_ref, their sum, and P as 16-bit.
+            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+            float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int i = 0; i < BN; i += 4) {
+                const float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+                const float x2 = __uint_as_float(sr[i + 2]), x3 = __uint_as_float(sr[i + 3]);
+                float e0 = ptx::ex2_approx(fmaf(x0, c, neg));
+                float e1 = ptx::ex2_approx(fmaf(x1, c, neg));
+                float e2 = ptx::ex2_approx(fmaf(x2, c, neg));
+                float e3 = ptx::ex2_approx(fmaf(x3, c, neg));
+                if (masked) {  // hidden keys weigh exactly 0 (also when scale == 0)
+                    e0 = (x0 == -INFINITY) ? 0.f : e0;
+                    e1 = (x1 == -INFINITY) ? 0.f : e1;
+                    e2 = (x2 == -INFINITY) ? 0.f : e2;
+                    e3 = (x3 == -INFINITY) ? 0.f : e3;
+                }
+                ps0 += e0;
+                ps1 += e1;
+                ps2 += e2;
+                ps3 += e3;
+                pk[i / 2] = pack2<D, kFP16>(e0, e1);
+                pk[i / 2 + 1] = pack2<D, kFP16>(e2, e3);
+            }
+            l = alpha * l + ((ps0 + ps1) + (ps2 + ps3));
+            store_p_row<BN>(s_tmem, pk);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + b));
+        }
+        if (!ok) break;
+
+        // Epilogue: wait for the last P V, divide by l once, store O and lse.
+        if (!wait_bar(bar_addr(bars, C::B_OFULL + q), o_cnt & 1, abort_flag, 9)) { ok = false; break; }
+        ++o_cnt;
+        ptx::tc_fence_after();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(ov);
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                w[i] = pack2<D, kFP16>(__uint_as_float(ov[2 * i]) * inv_l,
+                                       __uint_as_float(ov[2 * i + 1]) * inv_l);
+            if (row_ok) {
+#pragma unroll
+                for (int v4 = 0; v4 < 4; ++v4)
+                    ptx::st_global_v4(orow + cc * 64 + v4 * 16, w[4 * v4], w[4 * v4 + 1],
+                                      w[4 * v4 + 2], w[4 * v4 + 3]);
+            }
+        }
+        if (row_ok) p.lse[row_flat] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE + q));
+    }
+}
+
+// ---------------------------------------------------------------- kernel
+
+template <int D, bool kFP16>
+__global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
+    fa_fwd_kernel(const __grid_constant__ Params p) {
+    using C = Cfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sKV = smem + C::NQ * C::Q_BYTES;
+    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    const uint32_t bars = ptx::smem_addr(bar_mem);
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+    const uint32_t lane = ptx::lane_id();
+
+    if (threadIdx.x == 0) {
+        for (int q = 0; q < C::NQ; ++q) {
+            ptx::mbar_init(bar_addr(bars, C::B_QFULL + q), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + q), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_OFULL + q), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_OFREE + q), 128);
+        }
+        for (int s = 0; s < C::SLOTS; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_KVFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_KVEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), 128);
+        }
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        *abort_flag = 0;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == C::TMA_WARP && lane == 0) {
+        ptx::prefetch_tensormap(&p.tm_q);
+        ptx::prefetch_tensormap(&p.tm_k);
+        ptx::prefetch_tensormap(&p.tm_v);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp < 4 * C::NQ) {
+        if constexpr (C::REBALANCE) ptx::setmaxnreg_inc<C::REG_SOFTMAX>();
+        softmax_role<D, kFP16>(p, warp >> 2, bars, tmem, abort_flag);
+    } else {
+        if constexpr (C::REBALANCE) ptx::setmaxnreg_dec<C::REG_OTHER>();
+        if (warp == C::MMA_WARP) {
+            if (lane == 0) mma_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+        } else if (warp == C::TMA_WARP) {
+            if (lane == 0) tma_role<D>(p, sQ, sKV, bars, abort_flag);
+        }
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

@@ -1,0 +1,193 @@
+"""ctypes binding of libfa.so (include/fa.h) -- argument marshalling only.
+
+Every step of the attention forward runs inside the library's CUDA kernel;
+this module checks tensor metadata, allocates outputs with torch and passes
+raw pointers and sizes through the C ABI.  If the library is missing or
+refuses a request, it raises: there is no other code path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+from . import build as _build
+
+FA_OK = 0
+FA_ERR_INVALID_ARG = 1
+FA_ERR_UNSUPPORTED = 2
+FA_ERR_MISALIGNED = 3
+FA_ERR_CUDA = 4
+FA_ERR_DEVICE_TIMEOUT = 5
+
+MASK_NONE = 0
+MASK_CAUSAL = 1
+MASK_SLIDING_WINDOW = 2
+MASKS = {"none": MASK_NONE, "causal": MASK_CAUSAL, "window": MASK_SLIDING_WINDOW,
+         "sliding_window": MASK_SLIDING_WINDOW}
+
+DTYPE_BF16 = 0
+DTYPE_FP16 = 1
+
+# Every entry point declared in include/fa.h.
+EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_workspace_query", "fa_status_string",
+           "fa_describe", "fa_get_device_error")
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load libfa.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise FAError(-1, f"{p} is missing: build it with exact_io_aware_30_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        fwd_args = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _vp]
+        for name in ("fa_fwd", "fa_fwd_fp16"):
+            fn = getattr(lib, name)
+            fn.restype = _i
+            fn.argtypes = fwd_args
+        lib.fa_workspace_query.restype = _i
+        lib.fa_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i,
+                                           ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_status_string.restype = ctypes.c_char_p
+        lib.fa_status_string.argtypes = [_i]
+        lib.fa_describe.restype = _i
+        lib.fa_describe.argtypes = [_i, _i, _i, ctypes.c_char_p, ctypes.c_size_t]
+        lib.fa_get_device_error.restype = _i
+        lib.fa_get_device_error.argtypes = []
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != FA_OK:
+        raise FAError(status, f"{what}: {status_string(status)}")
+
+
+def mask_code(mask) -> int:
+    return MASKS[mask] if isinstance(mask, str) else int(mask)
+
+
+def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+            Sq: int, Sk: int, d: int, scale: float, mask_kind: int, window: int,
+            stream: int, dtype: int = DTYPE_BF16) -> int:
+    """Call fa_fwd / fa_fwd_fp16 with raw device pointers; returns the status."""
+    lib = load()
+    fn = lib.fa_fwd if dtype == DTYPE_BF16 else lib.fa_fwd_fp16
+    return fn(_vp(q_ptr), _vp(k_ptr), _vp(v_ptr), _vp(o_ptr), _vp(lse_ptr), int(B), int(H),
+              int(Sq), int(Sk), int(d), ctypes.c_float(scale), int(mask_kind), int(window),
+              _vp(stream))
+
+
+def workspace_query(B, H, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):
+    """(status, bytes) of fa_workspace_query."""
+    n = ctypes.c_size_t(12345)
+    st = load().fa_workspace_query(int(B), int(H), int(Sq), int(Sk), int(d), mask_code(mask),
+                                   int(window), int(dtype), ctypes.byref(n))
+    return st, n.value
+
+
+def describe(d: int, mask="none", dtype=DTYPE_BF16) -> str:
+    buf = ctypes.create_string_buffer(256)
+    st = load().fa_describe(int(d), mask_code(mask), int(dtype), buf, 256)
+    _check(st, "fa_describe")
+    return buf.value.decode()
+
+
+def device_error() -> int:
+    return load().fa_get_device_error()
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return DTYPE_BF16
+    if t.dtype == torch.float16:
+        return DTYPE_FP16
+    raise FAError(FA_ERR_UNSUPPORTED, f"dtype {t.dtype} is not supported (bf16 / fp16 only)")
+
+
+def forward(q, k, v, scale: float | None = None, mask="none", window: int = 0,
+            out=None, lse=None, stream=None):
+    """Fused attention forward on CUDA tensors [B, H, S, d] (bf16 or fp16).
+
+    Returns (o, lse): o like q, lse fp32 [B, H, Sq].  Enqueued on ``stream``
+    (default: torch's current stream of q's device); raises FAError if the
+    library rejects the call.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not t.is_cuda:
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous [B,H,S,d] tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise FAError(FA_ERR_INVALID_ARG, "q, k, v must share one dtype")
+    dt = _dtype_code(q)
+    B, H, Sq, d = q.shape
+    Sk = k.shape[2]
+    if tuple(k.shape) != (B, H, Sk, d) or tuple(v.shape) != (B, H, Sk, d):
+        raise FAError(FA_ERR_INVALID_ARG, "k and v must be [B,H,Sk,d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                 B, H, Sq, Sk, d, float(scale), mask_code(mask), int(window), sp, dt)
+    _check(st, "fa_fwd")
+    return out, lse
+
+
+def forward_host(q, k, v, scale: float | None = None, mask="none", window: int = 0,
+                 device=None, stream=None):
+    """End-to-end call from host (CPU) tensors: copy in, run, copy out.
+
+    q, k, v are CPU tensors (pinned for asynchronous copies).  Returns CPU
+    (o, lse) after the stream has finished.
+    """
+    import torch
+    dev = torch.device(device or "cuda")
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.stream(stream):
+        qd = q.to(dev, non_blocking=True)
+        kd = k.to(dev, non_blocking=True)
+        vd = v.to(dev, non_blocking=True)
+        o, lse = forward(qd, kd, vd, scale, mask, window, stream=stream)
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+    stream.synchronize()
+    return o_h, l_h

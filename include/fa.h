@@ -1,0 +1,124 @@
+/*
+ * fa.h -- C ABI of the GB300 (sm_103a) exact attention forward library.
+ *
+ * The operation ("FlashAttention: IO-aware attention kernels", table "What
+ * goes in, what comes out"; "FlashAttention: Why Tiling Attention Makes
+ * Transformers Fast Without Changing the Result", section "The tiled forward
+ * pass"): for every batch b and head h,
+ *
+ *     O   = softmax(scale * Q K^T  restricted to visible keys) V
+ *     lse = per-row natural-log sum of exp(scale * q_i . k_j) over visible j
+ *
+ * computed in one fused pass: key/value tiles stream through on-chip memory
+ * while each query row keeps a running max, a running sum and an
+ * unnormalised accumulator; the S x S score and probability matrices are
+ * never written to device memory.  The result is exact up to floating-point
+ * rounding order: inputs are 16-bit, products accumulate in fp32, the
+ * probabilities are rounded to the input type before the P V product, and O
+ * is rounded to the input type once at the end.
+ *
+ * Masks (readings of the pages, which name causal and sliding-window masks
+ * but not their alignment):
+ *   FA_MASK_NONE            every key j < Sk is visible;
+ *   FA_MASK_CAUSAL          key j visible to query i iff j <= i (top-left
+ *                           aligned: query 0 sees key 0, also when Sq != Sk);
+ *   FA_MASK_SLIDING_WINDOW  causal and j > i - window: `window` keys
+ *                           including the diagonal.
+ * A query row that sees no key (only possible with a window and Sq > Sk)
+ * gets O = 0 and lse = -inf, never NaN.  Arbitrary boolean masks are not
+ * supported and are rejected, never silently run another way.
+ *
+ * All entry points are plain C.  No entry point allocates device memory, and
+ * none falls back to a slower path: an unsupported request returns an error.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t (struct CUstream_st*); NULL = legacy stream. */
+typedef struct CUstream_st *fa_stream_t;
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,    /* sizes, pointers, mask/window or scale invalid  */
+    FA_ERR_UNSUPPORTED = 2,    /* head dim, dtype, mask kind or GPU not supported */
+    FA_ERR_MISALIGNED = 3,     /* q, k, v, o not 16-byte aligned or lse not 4    */
+    FA_ERR_CUDA = 4,           /* a CUDA runtime/driver call or the launch failed */
+    FA_ERR_DEVICE_TIMEOUT = 5  /* a kernel's pipeline wait ran out (device flag)  */
+} fa_status;
+
+enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 1, FA_MASK_SLIDING_WINDOW = 2 };
+enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 };
+
+/*
+ * fa_fwd -- fused attention forward, bf16 inputs and output.
+ *
+ *   q    device pointer, [B, H, Sq, d] bf16, contiguous row-major, 16-B aligned
+ *   k, v device pointers, [B, H, Sk, d] bf16, contiguous, 16-B aligned
+ *   o    device pointer, [B, H, Sq, d] bf16 output; must not overlap q, k, v
+ *   lse  device pointer, [B, H, Sq] fp32 output (natural-log logsumexp of the
+ *        scaled scores of each row), 4-B aligned; must not overlap the others
+ *   B, H >= 1; Sk >= 1; Sq >= 0 (Sq == 0 returns FA_OK and enqueues nothing)
+ *   d    head dimension: 64, 128 or 256 (else FA_ERR_UNSUPPORTED)
+ *   scale  multiplies Q K^T; finite and >= 0 (callers usually pass 1/sqrt(d))
+ *   mask_kind  FA_MASK_NONE, FA_MASK_CAUSAL or FA_MASK_SLIDING_WINDOW
+ *   window  keys per row for FA_MASK_SLIDING_WINDOW (>= 1); ignored otherwise
+ *   stream  CUDA stream to enqueue on
+ *
+ * Ownership: every buffer belongs to the caller; the library keeps no pointer
+ * after returning and allocates nothing.  The call validates its arguments
+ * synchronously (nothing is enqueued on error), then enqueues one kernel
+ * launch and returns; results are ready when the stream reaches that point.
+ * Re-entrant: concurrent calls on different streams are independent.
+ * A kernel whose internal pipeline wait exceeds its time limit (about 2 s)
+ * stops early and raises a device flag read by fa_get_device_error().
+ */
+fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                 int B, int H, int Sq, int Sk, int d, float scale,
+                 int mask_kind, int window, fa_stream_t stream);
+
+/* fa_fwd_fp16 -- identical to fa_fwd with fp16 q, k, v and o. */
+fa_status fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
+                      int B, int H, int Sq, int Sk, int d, float scale,
+                      int mask_kind, int window, fa_stream_t stream);
+
+/*
+ * fa_workspace_query -- device scratch bytes fa_fwd needs for this problem
+ * (always 0: the forward keeps every intermediate on chip, so its memory is
+ * linear in the sequence length -- "FlashAttention: Why Tiling...", section
+ * "The tiled forward pass").  Returns exactly the status fa_fwd would return
+ * for these sizes on the current device (pointer checks aside), so it is also
+ * the support probe: FA_OK means the fused kernel will run, never a fallback.
+ * bytes must be non-NULL.
+ */
+fa_status fa_workspace_query(int B, int H, int Sq, int Sk, int d, int mask_kind,
+                             int window, int dtype, size_t *bytes);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *fa_status_string(fa_status status);
+
+/*
+ * fa_describe -- writes into buf (NUL-terminated, truncated to len) the kernel
+ * and tile configuration fa_fwd selects for this head dim / mask / dtype, so
+ * a caller can log which kernel ran.  FA_ERR_UNSUPPORTED if none would.
+ */
+fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len);
+
+/*
+ * fa_get_device_error -- reads and clears the device status word of the
+ * current device that kernels set when a pipeline wait times out.  The
+ * caller synchronises the stream first.  FA_OK if no kernel raised it,
+ * FA_ERR_DEVICE_TIMEOUT if one did, FA_ERR_CUDA if it cannot be read.
+ */
+fa_status fa_get_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

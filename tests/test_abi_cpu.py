@@ -1,0 +1,131 @@
+"""The C-ABI library builds, loads and exports what include/fa.h declares, and
+rejects invalid calls synchronously -- all without a GPU (no compute call is
+made: every call here fails validation before touching the device)."""
+import os
+import re
+
+import pytest
+
+from exact_io_aware_30_gb300 import build, fa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return fa.load()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "fa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    assert _declared_functions() == sorted(fa.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_sm103a_only():
+    # one -gencode, sm_103a; the oracle is never linked into it
+    assert build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+    with open(build.LIB_PATH, "rb") as f:
+        blob = f.read()
+    assert b"oracle_attn" not in blob
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = fa.status_string(code)
+        assert s.startswith("FA_")
+    assert fa.status_string(99) == "FA_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("mask", ["none", "causal", "window"])
+@pytest.mark.parametrize("dtype", [fa.DTYPE_BF16, fa.DTYPE_FP16])
+def test_describe_names_the_kernel(lib, d, mask, dtype):
+    s = fa.describe(d, mask, dtype)
+    assert f"d={d}" in s and "tcgen05" in s
+    assert ("fp16" if dtype == fa.DTYPE_FP16 else "bf16") in s
+
+
+def test_describe_rejects_unsupported(lib):
+    with pytest.raises(fa.FAError) as e:
+        fa.describe(96, "none")
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+FAKE = 0x7F0000001000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _fwd(**kw):
+    a = dict(q_ptr=FAKE, k_ptr=FAKE + (1 << 30), v_ptr=FAKE + (2 << 30), o_ptr=FAKE + (3 << 30),
+             lse_ptr=FAKE + (4 << 30), B=1, H=1, Sq=128, Sk=128, d=128, scale=0.088,
+             mask_kind=fa.MASK_NONE, window=0, stream=0, dtype=fa.DTYPE_BF16)
+    a.update(kw)
+    return fa.fwd_raw(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=32), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_kind=3), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(Sk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sq=-1), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_kind=fa.MASK_SLIDING_WINDOW, window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-0.5), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=FAKE + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o_ptr=FAKE + (3 << 30) + 2), fa.FA_ERR_MISALIGNED),
+    (dict(lse_ptr=FAKE + (4 << 30) + 2), fa.FA_ERR_MISALIGNED),
+    (dict(o_ptr=FAKE + 64), fa.FA_ERR_INVALID_ARG),                # o overlaps q
+    (dict(lse_ptr=FAKE + (3 << 30) + 1024), fa.FA_ERR_INVALID_ARG),  # lse inside o
+    (dict(B=1 << 16, H=1 << 16), fa.FA_ERR_INVALID_ARG),             # unit count overflows
+])
+def test_invalid_calls_are_rejected_before_launch(lib, kw, status):
+    for dt in (fa.DTYPE_BF16, fa.DTYPE_FP16):
+        kw2 = dict(kw)
+        kw2.setdefault("dtype", dt)
+        assert _fwd(**kw2) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((1, 1, 128, 128, 96, "none", 0, 0), fa.FA_ERR_UNSUPPORTED),
+    ((1, 1, 128, 128, 128, "none", 0, 5), fa.FA_ERR_UNSUPPORTED),
+    ((0, 1, 128, 128, 128, "none", 0, 0), fa.FA_ERR_INVALID_ARG),
+    ((1, 1, 128, 128, 128, "window", 0, 0), fa.FA_ERR_INVALID_ARG),
+])
+def test_workspace_query_matches_fwd_verdict(lib, args, status):
+    st, nbytes = fa.workspace_query(*args)
+    assert st == status
+    assert nbytes == 0
+    B, H, Sq, Sk, d, mask, window, dtype = args
+    if dtype not in (fa.DTYPE_BF16, fa.DTYPE_FP16):
+        return  # the dtype is implied by the fa_fwd / fa_fwd_fp16 symbol
+    assert _fwd(B=B, H=H, Sq=Sq, Sk=Sk, d=d, mask_kind=fa.mask_code(mask), window=window,
+                dtype=dtype) == status
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    with pytest.raises(fa.FAError):
+        fa.forward(q, q, q)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(fa.FAError):
+        fa.load(str(tmp_path / "libfa.so"))
