@@ -157,6 +157,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     fa_status st = check_sizes(B, H, Sq, Sk, d, mask_kind, window, dtype);
     if (st != FA_OK) return st;
     if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+    if (Sq == 0) return FA_OK;  // nothing to compute; empty tensors may have null pointers
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
@@ -173,7 +174,6 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     DeviceInfo *info = nullptr;
     st = device_info(&dev, &info);
     if (st != FA_OK) return st;
-    if (Sq == 0) return FA_OK;
 
     const bool fp16 = dtype == FA_DTYPE_FP16;
     const int nq = nq_for(d), bn = bn_for(d);

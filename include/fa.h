@@ -63,7 +63,8 @@ enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 };
  *   o    device pointer, [B, H, Sq, d] bf16 output; must not overlap q, k, v
  *   lse  device pointer, [B, H, Sq] fp32 output (natural-log logsumexp of the
  *        scaled scores of each row), 4-B aligned; must not overlap the others
- *   B, H >= 1; Sk >= 1; Sq >= 0 (Sq == 0 returns FA_OK and enqueues nothing)
+ *   B, H >= 1; Sk >= 1; Sq >= 0 (Sq == 0: FA_OK once the sizes, kinds and scale
+ *        are valid; nothing is enqueued and the pointers are not examined)
  *   d    head dimension: 64, 128 or 256 (else FA_ERR_UNSUPPORTED)
  *   scale  multiplies Q K^T; finite and >= 0 (callers usually pass 1/sqrt(d))
  *   mask_kind  FA_MASK_NONE, FA_MASK_CAUSAL or FA_MASK_SLIDING_WINDOW
