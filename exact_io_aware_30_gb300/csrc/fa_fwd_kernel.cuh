@@ -580,13 +580,15 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
             float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
-            for (int i = 4; i < BN; i += 4) {
-                mx0 = fmaxf(mx0, __uint_as_float(sr[i]));
-                mx1 = fmaxf(mx1, __uint_as_float(sr[i + 1]));
-                mx2 = fmaxf(mx2, __uint_as_float(sr[i + 2]));
-                mx3 = fmaxf(mx3, __uint_as_float(sr[i + 3]));
+            for (int i = 4; i < BN; i += 8) {
+                mx0 = ptx::max3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+                mx1 = ptx::max3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+                if (i + 4 < BN) {
+                    mx2 = ptx::max3(mx2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+                    mx3 = ptx::max3(mx3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+                }
             }
-            const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+            const float mx = fmaxf(ptx::max3(mx0, mx1, mx2), mx3);
             const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
             const float m_new = fmaxf(m_ref, m_tile);
 
@@ -617,32 +619,30 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
                     ptx::tmem_st_x32<0>(o_tmem + cc * 32, ov);
                 }
             }
-            // Unnormalised probabilities against m_ref, their sum, and P as 16-bit.
+            // Unnormalised probabilities against m_ref, rounded to 16 bits for the
+            // P V product; l sums the rounded values, so the weights the MMA
+            // uses are exactly the ones O is divided by.
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            float ps0 = 0.f, ps1 = 0.f, ps2 = 0.f, ps3 = 0.f;
+            const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(neg, neg);
+            float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
             uint32_t pk[BN / 2];
 #pragma unroll
-            for (int i = 0; i < BN; i += 4) {
+            for (int i = 0; i < BN; i += 2) {
                 const float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
-                const float x2 = __uint_as_float(sr[i + 2]), x3 = __uint_as_float(sr[i + 3]);
-                float e0 = ptx::ex2_approx(fmaf(x0, c, neg));
-                float e1 = ptx::ex2_approx(fmaf(x1, c, neg));
-                float e2 = ptx::ex2_approx(fmaf(x2, c, neg));
-                float e3 = ptx::ex2_approx(fmaf(x3, c, neg));
+                float y0, y1;
+                ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(x0, x1), c2, n2), y0, y1);
+                float e0 = ptx::ex2_approx(y0);
+                float e1 = ptx::ex2_approx(y1);
                 if (masked) {  // hidden keys weigh exactly 0 (also when scale == 0)
                     e0 = (x0 == -INFINITY) ? 0.f : e0;
                     e1 = (x1 == -INFINITY) ? 0.f : e1;
-                    e2 = (x2 == -INFINITY) ? 0.f : e2;
-                    e3 = (x3 == -INFINITY) ? 0.f : e3;
                 }
-                ps0 += e0;
-                ps1 += e1;
-                ps2 += e2;
-                ps3 += e3;
-                pk[i / 2] = pack2<D, kFP16>(e0, e1);
-                pk[i / 2 + 1] = pack2<D, kFP16>(e2, e3);
+                const uint32_t pw = pack2<D, kFP16>(e0, e1);
+                pk[i / 2] = pw;
+                float &acc = ((i >> 1) & 3) == 0 ? ls0 : ((i >> 1) & 3) == 1 ? ls1 : ((i >> 1) & 3) == 2 ? ls2 : ls3;
+                acc = kFP16 ? ptx::add_f16x2_to_f32(pw, acc) : ptx::add_bf16x2_to_f32(pw, acc);
             }
-            l = alpha * l + ((ps0 + ps1) + (ps2 + ps3));
+            l = alpha * l + ((ls0 + ls1) + (ls2 + ls3));
             store_p_row<BN>(s_tmem, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
