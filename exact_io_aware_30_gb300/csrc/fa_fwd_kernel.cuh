@@ -71,7 +71,7 @@ template <int D>
 struct Cfg {
     static constexpr int BN = (D == 256) ? 64 : 128;   // keys per K/V tile
     static constexpr int NQ = (D == 256) ? 1 : 2;      // query tiles per unit
-    static constexpr int SLOTS = (D == 64) ? 8 : 4;    // K/V ring depth (tiles)
+    static constexpr int SLOTS = (D == 64) ? 10 : 5;   // K/V ring depth (tiles)
     // Warps: NQ softmax warpgroups, then the MMA warp and the TMA warp.  With
     // two softmax warpgroups the last warpgroup is padded to four warps so
     // that registers can be moved to the softmax warpgroups (setmaxnreg acts
@@ -515,6 +515,66 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
 }
 
+// Row max of one S tile (raw scores; scale >= 0 preserves the order).  With
+// kMasked, columns outside [c_lo, c_hi] are first set to -inf.
+template <int BN, bool kMasked>
+__device__ __forceinline__ float tile_row_max(uint32_t (&sr)[BN], int c_lo, int c_hi) {
+    if constexpr (kMasked) {
+#pragma unroll
+        for (int i = 0; i < BN; ++i)
+            if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
+    }
+    float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+    float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+    for (int i = 4; i < BN; i += 8) {
+        mx0 = ptx::max3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+        mx1 = ptx::max3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+        if (i + 4 < BN) {
+            mx2 = ptx::max3(mx2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+            mx3 = ptx::max3(mx3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+        }
+    }
+    return fmaxf(ptx::max3(mx0, mx1, mx2), mx3);
+}
+
+// p = 2^(s*c - m) for one row of a tile, packed to 16 bits into pk; adds the
+// exact fp32 sum of p to l_exact (for the logsumexp) and the sum of the
+// rounded 16-bit p to l_round (the divisor of O, so that the weights the
+// P V product uses sum exactly to what O is divided by).
+template <int BN, bool kFP16, bool kMasked>
+__device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, float neg,
+                                             uint32_t (&pk)[BN / 2], float &l_exact,
+                                             float &l_round) {
+    const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(neg, neg);
+    uint64_t le0 = ptx::f32x2(0.f, 0.f), le1 = le0;
+    float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < BN; i += 2) {
+        const float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+        float y0, y1;
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(x0, x1), c2, n2), y0, y1);
+        float e0 = ptx::ex2_approx(y0);
+        float e1 = ptx::ex2_approx(y1);
+        if constexpr (kMasked) {  // hidden keys weigh exactly 0 (also when scale == 0)
+            e0 = (x0 == -INFINITY) ? 0.f : e0;
+            e1 = (x1 == -INFINITY) ? 0.f : e1;
+        }
+        const uint32_t pw = kFP16 ? ptx::pack_f16x2(e0, e1) : ptx::pack_bf16x2(e0, e1);
+        pk[i / 2] = pw;
+        if ((i >> 1) & 1)
+            le1 = ptx::add_f32x2(le1, ptx::f32x2(e0, e1));
+        else
+            le0 = ptx::add_f32x2(le0, ptx::f32x2(e0, e1));
+        float &acc = ((i >> 1) & 3) == 0 ? lr0 : ((i >> 1) & 3) == 1 ? lr1 : ((i >> 1) & 3) == 2 ? lr2 : lr3;
+        acc = kFP16 ? ptx::add_f16x2_to_f32(pw, acc) : ptx::add_bf16x2_to_f32(pw, acc);
+    }
+    float a0, a1;
+    ptx::unpack_f32x2(ptx::add_f32x2(le0, le1), a0, a1);
+    l_exact += a0 + a1;
+    l_round += (lr0 + lr1) + (lr2 + lr3);
+}
+
 template <int D, bool kFP16>
 __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tmem,
                              volatile int *abort_flag) {
@@ -552,8 +612,9 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
         const int key_hi = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row, p.Sk - 1);
         const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
 
-        float m_ref = -INFINITY;  // max the accumulator and sum are referenced to (log2 units)
-        float l = 0.f;
+        float m_ref = -INFINITY;  // max the accumulator and sums are referenced to (log2 units)
+        float l = 0.f;            // sum of the rounded P actually multiplied into O
+        float l_exact = 0.f;      // fp32 sum of P (for the logsumexp)
         const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)q * D;
 
         for (int j = un.lo[q]; j < un.hi[q]; ++j) {
@@ -570,35 +631,22 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             ptx::reg_fence<BN>(sr);
 
             const bool masked = tile_needs_mask<D>(un.i0[q], j, p);
-            if (masked) {
-                const int c_lo = key_lo - j * BN, c_hi = key_hi - j * BN;
-#pragma unroll
-                for (int i = 0; i < BN; ++i)
-                    if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
-            }
-            // Row max of this tile (raw scores; scale >= 0 keeps the order).
-            float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-            float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
-#pragma unroll
-            for (int i = 4; i < BN; i += 8) {
-                mx0 = ptx::max3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-                mx1 = ptx::max3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-                if (i + 4 < BN) {
-                    mx2 = ptx::max3(mx2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-                    mx3 = ptx::max3(mx3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
-                }
-            }
-            const float mx = fmaxf(ptx::max3(mx0, mx1, mx2), mx3);
+            const float mx = masked ? tile_row_max<BN, true>(sr, key_lo - j * BN, key_hi - j * BN)
+                                    : tile_row_max<BN, false>(sr, 0, 0);
             const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
             const float m_new = fmaxf(m_ref, m_tile);
 
             float alpha = 1.f;
             bool rescale = false;
             if (j > un.lo[q]) {
-                // The previous P V of this tile must be complete before O is touched.
-                if (!wait_bar(bar_addr(bars, C::B_OFULL + q), o_cnt & 1, abort_flag, 8)) { ok = false; break; }
+                // O may be touched only once the previous P V has finished.  With
+                // two query tiles that is implied by S being full (this tile's S
+                // MMA was issued after that P V), so only the phase is counted.
+                if constexpr (NQ == 1) {
+                    if (!wait_bar(bar_addr(bars, C::B_OFULL + q), o_cnt & 1, abort_flag, 8)) { ok = false; break; }
+                    ptx::tc_fence_after();
+                }
                 ++o_cnt;
-                ptx::tc_fence_after();
                 if (m_new > m_ref + kRescaleLog2) {
                     alpha = ptx::ex2_approx(m_ref - m_new);  // 0 while m_ref is -inf
                     m_ref = m_new;
@@ -619,30 +667,14 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
                     ptx::tmem_st_x32<0>(o_tmem + cc * 32, ov);
                 }
             }
-            // Unnormalised probabilities against m_ref, rounded to 16 bits for the
-            // P V product; l sums the rounded values, so the weights the MMA
-            // uses are exactly the ones O is divided by.
             const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(neg, neg);
-            float ls0 = 0.f, ls1 = 0.f, ls2 = 0.f, ls3 = 0.f;
+            l *= alpha;
+            l_exact *= alpha;
             uint32_t pk[BN / 2];
-#pragma unroll
-            for (int i = 0; i < BN; i += 2) {
-                const float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
-                float y0, y1;
-                ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(x0, x1), c2, n2), y0, y1);
-                float e0 = ptx::ex2_approx(y0);
-                float e1 = ptx::ex2_approx(y1);
-                if (masked) {  // hidden keys weigh exactly 0 (also when scale == 0)
-                    e0 = (x0 == -INFINITY) ? 0.f : e0;
-                    e1 = (x1 == -INFINITY) ? 0.f : e1;
-                }
-                const uint32_t pw = pack2<D, kFP16>(e0, e1);
-                pk[i / 2] = pw;
-                float &acc = ((i >> 1) & 3) == 0 ? ls0 : ((i >> 1) & 3) == 1 ? ls1 : ((i >> 1) & 3) == 2 ? ls2 : ls3;
-                acc = kFP16 ? ptx::add_f16x2_to_f32(pw, acc) : ptx::add_bf16x2_to_f32(pw, acc);
-            }
-            l = alpha * l + ((ls0 + ls1) + (ls2 + ls3));
+            if (masked)
+                tile_row_exp<BN, kFP16, true>(sr, c, neg, pk, l_exact, l);
+            else
+                tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, l_exact, l);
             store_p_row<BN>(s_tmem, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
@@ -674,7 +706,7 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
                                       w[4 * v4 + 2], w[4 * v4 + 3]);
             }
         }
-        if (row_ok) p.lse[row_flat] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+        if (row_ok) p.lse[row_flat] = (l_exact > 0.f) ? (m_ref + log2f(l_exact)) * kLn2 : -INFINITY;
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_OFREE + q));
     }

@@ -247,6 +247,13 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     return r;
 }
 
+// a + b on both lanes.
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // acc + (both 16-bit values of a packed pair, widened exactly to fp32).
 __device__ __forceinline__ float add_bf16x2_to_f32(uint32_t pair, float acc) {
     float r;
