@@ -137,11 +137,6 @@ fa_status launch(const Params &p, int num_sms, DeviceInfo &info, cudaStream_t st
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM_BYTES) != cudaSuccess)
                 return FA_ERR_CUDA;
-            // The warpgroup register re-balance inside the kernel assumes the
-            // launch allocation it was designed for; never launch otherwise.
-            cudaFuncAttributes attr;
-            if (cudaFuncGetAttributes(&attr, kern) != cudaSuccess) return FA_ERR_CUDA;
-            if (C::REBALANCE && attr.numRegs != C::REG_LAUNCH) return FA_ERR_UNSUPPORTED;
             info.attr_set[slot] = true;
         }
     }
@@ -269,7 +264,7 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
                   "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d q_tiles_per_cta=%d "
-                  "kv_ring=%d threads=%d smem=%d mask=%s persistent",
+                  "s_buffers_per_q_tile=2 kv_ring=%d threads=%d smem=%d mask=%s persistent",
                   d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::nq_for(d),
                   fa::slots_for(d), 32 * (4 * fa::nq_for(d) + 2),
                   d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES

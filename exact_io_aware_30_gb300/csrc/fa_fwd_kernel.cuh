@@ -69,49 +69,44 @@ struct Params {
 
 template <int D>
 struct Cfg {
-    static constexpr int BN = (D == 256) ? 64 : 128;   // keys per K/V tile
-    static constexpr int NQ = (D == 256) ? 1 : 2;      // query tiles per unit
-    static constexpr int SLOTS = (D == 64) ? 10 : 5;   // K/V ring depth (tiles)
-    // Warps: NQ softmax warpgroups, then the MMA warp and the TMA warp.  With
-    // two softmax warpgroups the last warpgroup is padded to four warps so
-    // that registers can be moved to the softmax warpgroups (setmaxnreg acts
-    // per warpgroup): at launch 384 threads x 168 registers; afterwards
-    // 2 x 128 x REG_SOFTMAX + 128 x REG_OTHER, which must not exceed that.
-    static constexpr int NUM_WARPS = (NQ == 2) ? 12 : 6;
+    static constexpr int BN = 64;                        // keys per K/V tile
+    static constexpr int NQ = (D == 256) ? 1 : 2;        // query tiles per unit
+    static constexpr int SLOTS = (D == 64) ? 16 : (D == 128) ? 10 : 5;  // K/V ring depth (tiles)
+    // Warps: NQ softmax warpgroups (warps 0 .. 4*NQ-1), then the MMA warp and
+    // the TMA warp.  With 10 warps, three share an SM sub-partition, so the
+    // compiler caps registers at 168 per thread, which the 64-column softmax
+    // rows fit without spilling.
+    static constexpr int NUM_WARPS = 4 * NQ + 2;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
     static constexpr int MMA_WARP = 4 * NQ;
     static constexpr int TMA_WARP = 4 * NQ + 1;
-    static constexpr bool REBALANCE = (NQ == 2);
-    static constexpr int REG_LAUNCH = 168;
-    static constexpr int REG_SOFTMAX = 224;
-    static constexpr int REG_OTHER = 56;
-    static_assert(!REBALANCE || 2 * 128 * REG_SOFTMAX + 128 * REG_OTHER <= NUM_THREADS * REG_LAUNCH,
-                  "register split exceeds the launch allocation");
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int SLOT_BYTES = BN * D * 2;
-    // Tensor memory: S/P buffers 0,1 at columns 0 and BN; O accumulators from 256.
+    // Tensor memory: two S/P buffers per query tile (BN columns each) at
+    // columns (2q + b) * BN, O accumulators (D columns each) from column 256.
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t S_COL = BN;              // column stride between S buffers
     static constexpr uint32_t O_COL0 = 256;
     // Barrier indices.
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = B_QFULL + NQ;
     static constexpr int B_KVFULL = B_QEMPTY + NQ;
     static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
-    static constexpr int B_SFULL = B_KVEMPTY + SLOTS;
-    static constexpr int B_PFULL = B_SFULL + 2;
-    static constexpr int B_OFULL = B_PFULL + 2;
-    static constexpr int B_OFREE = B_OFULL + NQ;
+    static constexpr int B_SFULL = B_KVEMPTY + SLOTS;   // [2 * NQ]: S buffer (q, b) computed
+    static constexpr int B_PFULL = B_SFULL + 2 * NQ;    // [2 * NQ]: P buffer (q, b) written
+    static constexpr int B_OFULL = B_PFULL + 2 * NQ;    // [NQ]: one phase per P V
+    static constexpr int B_OFREE = B_OFULL + NQ;        // [NQ]: epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + NQ;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_TILES = NQ * Q_BYTES + SLOTS * SLOT_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
     static_assert(O_COL0 + NQ * D <= TMEM_COLS, "tensor memory overflow");
-    static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
+    static_assert(2 * NQ * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+
+    __device__ static constexpr uint32_t s_col(int q, int b) { return (uint32_t)((2 * q + b) * BN); }
 };
 
 // ---------------------------------------------------------------- helpers
@@ -324,20 +319,22 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
                          uint32_t tmem, volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int NQ = C::NQ;
-    constexpr uint32_t kIdescS = make_idesc(kBM, C::BN, kFP16, false);
+    constexpr int BN = C::BN;
+    constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
     constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
 
-    uint32_t kv_it = 0;
-    uint32_t q_cnt[NQ], p_cnt[2], ofree_cnt[NQ];
+    uint32_t kv_it = 0;          // K/V ring fills consumed so far
+    uint32_t q_cnt[NQ];          // Q tiles consumed per query slot
+    uint32_t t_cnt[NQ];          // key tiles processed per query slot (S/P buffer = t & 1)
+    uint32_t ofree_cnt[NQ];      // epilogues waited for per O accumulator
     bool o_used[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) {
         q_cnt[q] = 0;
+        t_cnt[q] = 0;
         ofree_cnt[q] = 0;
         o_used[q] = false;
     }
-    p_cnt[0] = p_cnt[1] = 0;
-    uint32_t t_cnt = 0;  // tiles issued (NQ == 1: S buffer = t & 1)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
@@ -347,55 +344,13 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
         decode_unit<D>(u, p, un);
         if (!un.any) continue;
         const uint32_t kv_base = kv_it;
-
+        auto kidx = [&](int j) -> uint32_t { return kv_base + 2u * (uint32_t)(j - un.ulo); };
         auto wait_kv = [&](uint32_t idx) -> bool {
             return wait_bar(bar_addr(bars, C::B_KVFULL + idx % C::SLOTS), (idx / C::SLOTS) & 1,
                             abort_flag, 3);
         };
-        auto release_kv = [&](uint32_t idx) { ptx::mma_commit(bar_addr(bars, C::B_KVEMPTY + idx % C::SLOTS)); };
-        auto kidx = [&](int j) -> uint32_t { return kv_base + 2u * (uint32_t)(j - un.ulo); };
-        // S_b = Q_q K_j^T
-        auto issue_s = [&](int q, int j, int b) {
-            const uint32_t slot = kidx(j) % C::SLOTS;
-            const uint32_t a0 = ptx::smem_addr(sQ + q * C::Q_BYTES);
-            const uint32_t b0 = ptx::smem_addr(sKV + slot * C::SLOT_BYTES);
-            const uint32_t d_tmem = tmem + (uint32_t)b * C::S_COL;
-            const uint64_t da = smem_desc(a0, 16), db = smem_desc(b0, 16);
-#pragma unroll 1
-            for (int kk = 0; kk < D / 16; ++kk) {
-                // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
-                const uint32_t off_a = ((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4;
-                const uint32_t off_b = ((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4;
-                ptx::mma_ss(d_tmem, da + off_a, db + off_b, kIdescS, kk > 0 ? 1u : 0u);
-            }
-            ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
-        };
-        // O_q (+)= P_b V_j
-        auto issue_pv = [&](int q, int j, int b, bool first) {
-            const uint32_t slot = (kidx(j) + 1) % C::SLOTS;
-            const uint32_t v0 = ptx::smem_addr(sKV + slot * C::SLOT_BYTES);
-            const uint32_t d_tmem = tmem + C::O_COL0 + (uint32_t)q * D;
-            const uint32_t p_tmem = tmem + (uint32_t)b * C::S_COL;
-            const uint64_t dv = smem_desc(v0, C::KV_CHUNK);
-#pragma unroll 1
-            for (int kk = 0; kk < C::BN / 16; ++kk) {
-                // 16 keys = two 8-row groups (2048 bytes) per step; P: 8 columns.
-                ptx::mma_ts(d_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4), kIdescO,
-                            (!first || kk > 0) ? 1u : 0u);
-            }
-            ptx::mma_commit(bar_addr(bars, C::B_OFULL + q));
-        };
-        auto wait_p = [&](int b, uint32_t parity) -> bool {
-            if (!wait_bar(bar_addr(bars, C::B_PFULL + b), parity, abort_flag, 4)) return false;
-            ptx::tc_fence_after();
-            return true;
-        };
-        auto wait_ofree = [&](int q) -> bool {
-            if (!o_used[q]) return true;
-            const bool r = wait_bar(bar_addr(bars, C::B_OFREE + q), ofree_cnt[q] & 1, abort_flag, 5);
-            ++ofree_cnt[q];
-            ptx::tc_fence_after();
-            return r;
+        auto release_kv = [&](uint32_t idx) {
+            ptx::mma_commit(bar_addr(bars, C::B_KVEMPTY + idx % C::SLOTS));
         };
 
 #pragma unroll
@@ -405,83 +360,98 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
         }
         if (!ok) break;
 
-        if constexpr (NQ == 2) {
-            // Prologue: first S of every tile that starts at the union's first tile.
-            if (!wait_kv(kidx(un.ulo))) { ok = false; break; }
+        // S_q(x) is issued one key tile ahead of P_q V: the softmax of tile j
+        // overlaps the S MMA of tile j + 1 (two S buffers per query tile).
+        int ns[NQ];
 #pragma unroll
-            for (int q = 0; q < NQ; ++q)
-                if (un.valid[q] && un.lo[q] == un.ulo) issue_s(q, un.ulo, q);
-            release_kv(kidx(un.ulo));
-            for (int j = un.ulo; j < un.uhi && ok; ++j) {
-                bool v_ready = false, k_ready = false;
+        for (int q = 0; q < NQ; ++q) ns[q] = un.lo[q];
+        int k_ready = un.ulo - 1;  // highest key tile waited for
+        int k_rel = un.ulo;        // next key tile to hand back to the TMA warp
+
+        for (int j = un.ulo; j < un.uhi && ok; ++j) {
+            // 1. every S of key tiles <= j + 1
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    if (!un.valid[q] || !ok) continue;
-                    if (j >= un.lo[q] && j < un.hi[q]) {
-                        if (!v_ready) {
-                            if (!wait_kv(kidx(j) + 1)) { ok = false; break; }
-                            v_ready = true;
-                        }
-                        if (!wait_p(q, p_cnt[q] & 1)) { ok = false; break; }
-                        ++p_cnt[q];
-                        if (j == un.lo[q] && !wait_ofree(q)) { ok = false; break; }
-                        issue_pv(q, j, q, j == un.lo[q]);
-                        if (j + 1 < un.hi[q]) {
-                            if (!k_ready) {
-                                if (!wait_kv(kidx(j + 1))) { ok = false; break; }
-                                k_ready = true;
-                            }
-                            issue_s(q, j + 1, q);
-                        }
-                    } else if (j + 1 == un.lo[q]) {
-                        if (!k_ready) {
-                            if (!wait_kv(kidx(j + 1))) { ok = false; break; }
-                            k_ready = true;
-                        }
-                        issue_s(q, j + 1, q);
+            for (int q = 0; q < NQ; ++q) {
+                if (!un.valid[q]) continue;
+                while (ns[q] < un.hi[q] && ns[q] <= j + 1) {
+                    const int x = ns[q];
+                    if (x > k_ready) {
+                        if (!wait_kv(kidx(x))) { ok = false; break; }
+                        k_ready = x;
+                    }
+                    const int b = (int)((t_cnt[q] + (uint32_t)(x - un.lo[q])) & 1u);
+                    const uint32_t a0 = ptx::smem_addr(sQ + q * C::Q_BYTES);
+                    const uint32_t b0 = ptx::smem_addr(sKV + (kidx(x) % C::SLOTS) * C::SLOT_BYTES);
+                    const uint32_t d_tmem = tmem + C::s_col(q, b);
+                    const uint64_t da = smem_desc(a0, 16), db = smem_desc(b0, 16);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
+                        const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
+                        const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+                        ptx::mma_ss(d_tmem, da + off_a, db + off_b, kIdescS, kk > 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bar_addr(bars, C::B_SFULL + 2 * q + b));
+                    ++ns[q];
+                    if (ns[q] == un.hi[q]) {  // last read of this Q tile in the unit
+                        ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + q));
+                        ++q_cnt[q];
                     }
                 }
                 if (!ok) break;
-                release_kv(kidx(j) + 1);
-                if (j + 1 < un.uhi) {
-                    if (!k_ready && !wait_kv(kidx(j + 1))) { ok = false; break; }
-                    release_kv(kidx(j + 1));
+            }
+            if (!ok) break;
+            // every S that reads key tiles <= k_ready has been issued
+            while (k_rel <= k_ready) {
+                release_kv(kidx(k_rel));
+                ++k_rel;
+            }
+            // 2. O_q (+)= P_q V_j for every query tile that sees key tile j
+            bool v_ready = false;
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                if (!un.valid[q] || j < un.lo[q] || j >= un.hi[q]) continue;
+                if (!v_ready) {
+                    if (!wait_kv(kidx(j) + 1)) { ok = false; break; }
+                    v_ready = true;
                 }
-            }
-        } else {
-            // One query tile, S double-buffered across consecutive key tiles.
-            const uint32_t t0 = t_cnt;
-            if (!wait_kv(kidx(un.ulo))) { ok = false; break; }
-            issue_s(0, un.ulo, t0 & 1);
-            release_kv(kidx(un.ulo));
-            if (un.ulo + 1 < un.uhi) {
-                if (!wait_kv(kidx(un.ulo + 1))) { ok = false; break; }
-                issue_s(0, un.ulo + 1, (t0 + 1) & 1);
-                release_kv(kidx(un.ulo + 1));
-            }
-            for (int j = un.ulo; j < un.uhi; ++j) {
-                const uint32_t t = t0 + (uint32_t)(j - un.ulo);
-                const int b = t & 1;
-                if (!wait_kv(kidx(j) + 1)) { ok = false; break; }
-                if (!wait_p(b, (t >> 1) & 1)) { ok = false; break; }
-                if (j == un.ulo && !wait_ofree(0)) { ok = false; break; }
-                issue_pv(0, j, b, j == un.ulo);
-                release_kv(kidx(j) + 1);
-                if (j + 2 < un.uhi) {
-                    if (!wait_kv(kidx(j + 2))) { ok = false; break; }
-                    issue_s(0, j + 2, b);
-                    release_kv(kidx(j + 2));
+                const uint32_t t = t_cnt[q] + (uint32_t)(j - un.lo[q]);
+                const int b = (int)(t & 1u);
+                if (!wait_bar(bar_addr(bars, C::B_PFULL + 2 * q + b), (t >> 1) & 1u, abort_flag, 4)) {
+                    ok = false;
+                    break;
                 }
+                ptx::tc_fence_after();
+                const bool first = (j == un.lo[q]);
+                if (first && o_used[q]) {
+                    if (!wait_bar(bar_addr(bars, C::B_OFREE + q), ofree_cnt[q] & 1, abort_flag, 5)) {
+                        ok = false;
+                        break;
+                    }
+                    ++ofree_cnt[q];
+                    ptx::tc_fence_after();
+                }
+                const uint32_t v0 = ptx::smem_addr(sKV + ((kidx(j) + 1) % C::SLOTS) * C::SLOT_BYTES);
+                const uint32_t d_tmem = tmem + C::O_COL0 + (uint32_t)q * D;
+                const uint32_t p_tmem = tmem + C::s_col(q, b);
+                const uint64_t dv = smem_desc(v0, C::KV_CHUNK);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    // 16 keys = two 8-row groups (2048 bytes) per step; P: 8 columns.
+                    ptx::mma_ts(d_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4),
+                                kIdescO, (!first || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(bar_addr(bars, C::B_OFULL + q));
             }
-            t_cnt = t0 + (uint32_t)(un.uhi - un.ulo);
+            if (!ok) break;
+            release_kv(kidx(j) + 1);
         }
         if (!ok) break;
         kv_it = kv_base + 2u * (uint32_t)(un.uhi - un.ulo);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
             if (!un.valid[q]) continue;
-            ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + q));
-            ++q_cnt[q];
+            t_cnt[q] += (uint32_t)(un.hi[q] - un.lo[q]);
             o_used[q] = true;
         }
     }
@@ -585,8 +555,7 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
     const uint32_t lane_off = (uint32_t)((tid >> 5) * 32) << 16;  // this warp's TMEM lanes
     const int q = (NQ == 2) ? wg : 0;
     const float c = p.scale_log2;
-    uint32_t t_cnt = 0;  // S tiles consumed
-    uint32_t o_cnt = 0;  // O completions consumed
+    uint32_t t_cnt = 0;  // key tiles processed by this warpgroup (S/P buffer = t & 1)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
@@ -617,13 +586,16 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
         float l_exact = 0.f;      // fp32 sum of P (for the logsumexp)
         const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)q * D;
 
+        uint32_t t = 0;  // this warpgroup's tile counter at the current key tile
         for (int j = un.lo[q]; j < un.hi[q]; ++j) {
-            const uint32_t t = t_cnt++;
-            const int b = (NQ == 2) ? q : (int)(t & 1);
-            const uint32_t par = (NQ == 2) ? (t & 1) : ((t >> 1) & 1);
-            if (!wait_bar(bar_addr(bars, C::B_SFULL + b), par, abort_flag, 7)) { ok = false; break; }
+            t = t_cnt++;
+            const int b = (int)(t & 1u);
+            if (!wait_bar(bar_addr(bars, C::B_SFULL + 2 * q + b), (t >> 1) & 1u, abort_flag, 7)) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_off + (uint32_t)b * C::S_COL;
+            const uint32_t s_tmem = tmem + lane_off + C::s_col(q, b);
 
             uint32_t sr[BN];
             load_s_row<BN>(s_tmem, sr);
@@ -639,14 +611,6 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             float alpha = 1.f;
             bool rescale = false;
             if (j > un.lo[q]) {
-                // O may be touched only once the previous P V has finished.  With
-                // two query tiles that is implied by S being full (this tile's S
-                // MMA was issued after that P V), so only the phase is counted.
-                if constexpr (NQ == 1) {
-                    if (!wait_bar(bar_addr(bars, C::B_OFULL + q), o_cnt & 1, abort_flag, 8)) { ok = false; break; }
-                    ptx::tc_fence_after();
-                }
-                ++o_cnt;
                 if (m_new > m_ref + kRescaleLog2) {
                     alpha = ptx::ex2_approx(m_ref - m_new);  // 0 while m_ref is -inf
                     m_ref = m_new;
@@ -655,7 +619,20 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             } else {
                 m_ref = m_new;
             }
+            // O-barrier phases (one per P V of this query slot, numbered like t)
+            // are consumed in order: phase t-1 (P V of the previous key tile) is
+            // waited for before P of this tile is released, i.e. before P V of
+            // tile t can exist.  S of this tile implies P V of tile t-2 is done,
+            // so the barrier is then at phase t-1 or t and a parity wait on t-1
+            // is unambiguous.  The first tile of a unit has nothing to wait for:
+            // the previous unit's epilogue consumed its last phase.
             if (__any_sync(0xffffffffu, rescale)) {
+                // O may be touched only once the previous P V has finished.
+                if (!wait_bar(bar_addr(bars, C::B_OFULL + q), (t - 1u) & 1u, abort_flag, 8)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t ov[32];
@@ -676,15 +653,20 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             else
                 tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, l_exact, l);
             store_p_row<BN>(s_tmem, pk);
+            if (j > un.lo[q] &&
+                !wait_bar(bar_addr(bars, C::B_OFULL + q), (t - 1u) & 1u, abort_flag, 10)) {
+                ok = false;
+                break;
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + b));
+            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + 2 * q + b));
         }
         if (!ok) break;
 
-        // Epilogue: wait for the last P V, divide by l once, store O and lse.
-        if (!wait_bar(bar_addr(bars, C::B_OFULL + q), o_cnt & 1, abort_flag, 9)) { ok = false; break; }
-        ++o_cnt;
+        // Epilogue: wait for the last P V (phase t; phase t-1 was consumed
+        // above), divide by l once, store O and lse.
+        if (!wait_bar(bar_addr(bars, C::B_OFULL + q), t & 1u, abort_flag, 9)) { ok = false; break; }
         ptx::tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
@@ -742,7 +724,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
             ptx::mbar_init(bar_addr(bars, C::B_KVFULL + s), 1);
             ptx::mbar_init(bar_addr(bars, C::B_KVEMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 2 * C::NQ; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
             ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), 128);
         }
@@ -766,15 +748,11 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp < 4 * C::NQ) {
-        if constexpr (C::REBALANCE) ptx::setmaxnreg_inc<C::REG_SOFTMAX>();
         softmax_role<D, kFP16>(p, warp >> 2, bars, tmem, abort_flag);
+    } else if (warp == C::MMA_WARP) {
+        if (lane == 0) mma_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else {
-        if constexpr (C::REBALANCE) ptx::setmaxnreg_dec<C::REG_OTHER>();
-        if (warp == C::MMA_WARP) {
-            if (lane == 0) mma_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
-        } else if (warp == C::TMA_WARP) {
-            if (lane == 0) tma_role<D>(p, sQ, sKV, bars, abort_flag);
-        }
+        if (lane == 0) tma_role<D>(p, sQ, sKV, bars, abort_flag);
     }
     __syncwarp();
     ptx::tc_fence_before();
