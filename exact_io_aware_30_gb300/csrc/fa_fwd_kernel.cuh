@@ -69,13 +69,15 @@ struct Params {
 
 template <int D>
 struct Cfg {
-    static constexpr int BN = 64;                        // keys per K/V tile
-    static constexpr int NQ = (D == 256) ? 1 : 2;        // query tiles per unit
-    static constexpr int SLOTS = (D == 64) ? 16 : (D == 128) ? 10 : 5;  // K/V ring depth (tiles)
+    // One query tile per unit with two S buffers: the S MMA of key tile j+1
+    // runs while the softmax works on tile j.  d = 256 uses 64-key tiles so
+    // that two S buffers and its 256-column O fit in tensor memory and a
+    // 5-deep K/V ring fits in shared memory.
+    static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
+    static constexpr int NQ = 1;                         // query tiles per unit
+    static constexpr int SLOTS = (D == 64) ? 12 : (D == 128) ? 6 : 5;  // K/V ring depth (tiles)
     // Warps: NQ softmax warpgroups (warps 0 .. 4*NQ-1), then the MMA warp and
-    // the TMA warp.  With 10 warps, three share an SM sub-partition, so the
-    // compiler caps registers at 168 per thread, which the 64-column softmax
-    // rows fit without spilling.
+    // the TMA warp.
     static constexpr int NUM_WARPS = 4 * NQ + 2;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
     static constexpr int MMA_WARP = 4 * NQ;
