@@ -264,10 +264,9 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
                   "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d q_tiles_per_cta=%d "
-                  "s_buffers=2 softmax_warpgroups=2(column halves) kv_ring=%d threads=%d smem=%d "
-                  "mask=%s persistent",
+                  "s_buffers_per_q_tile=2 kv_ring=%d threads=%d smem=%d mask=%s persistent",
                   d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::nq_for(d),
-                  fa::slots_for(d), fa::Cfg<128>::NUM_THREADS,
+                  fa::slots_for(d), 32 * (4 * fa::nq_for(d) + 2),
                   d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES
                                                                : fa::Cfg<256>::SMEM_BYTES,
                   masks[mask_kind]);

@@ -47,6 +47,7 @@ constexpr int kMaskCausal = 1;
 constexpr int kMaskWindow = 2;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
 constexpr float kRescaleLog2 = 8.0f;              // rescale O when the max grows > 2^8
+constexpr float kRescaleBound = 256.0f;           // 2^kRescaleLog2
 constexpr float kLn2 = 0.693147180559945309f;
 
 // Device status word: 0 = fine; else 0x100 + the wait site that timed out.
@@ -71,19 +72,17 @@ template <int D>
 struct Cfg {
     // One query tile per unit with two S buffers: the S MMA of key tile j+1
     // runs while the softmax works on tile j.  d = 256 uses 64-key tiles so
-    // that two S buffers and its 256-column O fit in tensor memory.
+    // that two S buffers and its 256-column O fit in tensor memory and a
+    // 5-deep K/V ring fits in shared memory.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
     static constexpr int NQ = 1;                         // query tiles per unit
-    static constexpr int SLOTS = (D == 64) ? 12 : (D == 128) ? 5 : 4;  // K/V ring depth (tiles)
-    // Warps 0-3 and 4-7: two softmax warpgroups sharing the 128 query rows,
-    // the first taking key columns [0, BN/2) of every S tile (and O columns
-    // [0, D/2)), the second the other half; warp 8 issues MMAs, warp 9 TMA.
-    static constexpr int HALF_N = BN / 2;                // S columns per softmax thread
-    static constexpr int HALF_D = D / 2;                 // O columns per softmax thread
-    static constexpr int NUM_WARPS = 10;
+    static constexpr int SLOTS = (D == 64) ? 12 : (D == 128) ? 6 : 5;  // K/V ring depth (tiles)
+    // Warps: NQ softmax warpgroups (warps 0 .. 4*NQ-1), then the MMA warp and
+    // the TMA warp.
+    static constexpr int NUM_WARPS = 4 * NQ + 2;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
-    static constexpr int MMA_WARP = 8;
-    static constexpr int TMA_WARP = 9;
+    static constexpr int MMA_WARP = 4 * NQ;
+    static constexpr int TMA_WARP = 4 * NQ + 1;
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
@@ -103,12 +102,9 @@ struct Cfg {
     static constexpr int B_OFULL = B_PFULL + 2 * NQ;    // [NQ]: one phase per P V
     static constexpr int B_OFREE = B_OFULL + NQ;        // [NQ]: epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + NQ;
-    static constexpr int B_XCH = B_DRAIN + 1;           // [4]: halves of 32 rows exchanged
-    static constexpr int NUM_BARS = B_XCH + 4;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_TILES = NQ * Q_BYTES + SLOTS * SLOT_BYTES;
-    // Exchange area between the two halves of a row: [2 slots][2 halves][2][128] fp32.
-    static constexpr int XCH_FLOATS = 2 * 2 * 2 * 128;
-    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + XCH_FLOATS * 4 + NUM_BARS * 8 + 16;
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
     static_assert(O_COL0 + NQ * D <= TMEM_COLS, "tensor memory overflow");
     static_assert(2 * NQ * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
@@ -444,12 +440,8 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
                 const uint64_t dv = smem_desc(v0, C::KV_CHUNK);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 keys = two 8-row groups (2048 bytes) of V per step.  P of key
-                    // half h sits at the start of that half's S columns, 2 keys per
-                    // column: keys 16kk.. are at column h*HALF_N + (16kk mod HALF_N)/2.
-                    constexpr int kPerHalf = C::HALF_N / 16;
-                    const uint32_t p_col = (uint32_t)((kk / kPerHalf) * C::HALF_N + (kk % kPerHalf) * 8);
-                    ptx::mma_ts(d_tmem, p_tmem + p_col, dv + (uint32_t)((kk * 2048) >> 4),
+                    // 16 keys = two 8-row groups (2048 bytes) per step; P: 8 columns.
+                    ptx::mma_ts(d_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4),
                                 kIdescO, (!first || kk > 0) ? 1u : 0u);
                 }
                 ptx::mma_commit(bar_addr(bars, C::B_OFULL + q));
@@ -473,25 +465,35 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
 
 // ---------------------------------------------------------------- softmax role
 
-// N consecutive fp32 columns of this thread's TMEM lane (N = 32 or 64).
-template <int N>
-__device__ __forceinline__ void load_row(uint32_t taddr, uint32_t (&r)[N]) {
+// One thread's row of an S tile (BN fp32 columns) from tensor memory.
+template <int BN>
+__device__ __forceinline__ void load_s_row(uint32_t taddr, uint32_t (&r)[BN]) {
     ptx::tmem_ld_x32<0>(taddr, r);
-    if constexpr (N == 64) ptx::tmem_ld_x32<32>(taddr + 32, r);
+    ptx::tmem_ld_x32<32>(taddr + 32, r);
+    if constexpr (BN == 128) {
+        ptx::tmem_ld_x32<64>(taddr + 64, r);
+        ptx::tmem_ld_x32<96>(taddr + 96, r);
+    }
 }
 
-// N/2 packed 16-bit pairs (P of N keys) to this thread's TMEM lane.
-template <int N>
-__device__ __forceinline__ void store_p_half(uint32_t taddr, const uint32_t (&r)[N / 2]) {
-    if constexpr (N == 64)
-        ptx::tmem_st_x32<0>(taddr, r);
-    else
-        ptx::tmem_st_x16<0>(taddr, r);
+// One thread's row of P (BN 16-bit values packed in BN/2 columns) to tensor memory.
+template <int BN>
+__device__ __forceinline__ void store_p_row(uint32_t taddr, const uint32_t (&r)[BN / 2]) {
+    ptx::tmem_st_x32<0>(taddr, r);
+    if constexpr (BN == 128) ptx::tmem_st_x32<32>(taddr + 32, r);
 }
 
 template <int D, bool kFP16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
+}
+
+// Hidden keys of a boundary tile (columns outside [c_lo, c_hi]) become -inf.
+template <int BN>
+__device__ __forceinline__ void apply_mask(uint32_t (&sr)[BN], int c_lo, int c_hi) {
+#pragma unroll
+    for (int i = 0; i < BN; ++i)
+        if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
 }
 
 // Row max of one S tile (raw scores; scale >= 0 preserves the order).  With
@@ -554,41 +556,17 @@ __device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, 
     l_round += (lr0 + lr1) + (lr2 + lr3);
 }
 
-// Exchange one fp32 per thread with the thread of the other column half that
-// owns the same query row: write own value, arrive on the row group's
-// barrier, wait for the phase, read the partner's value.  Two value slots
-// alternate with the phase, so a slot is rewritten only after the partner has
-// passed the next exchange (and therefore read it).
-__device__ __forceinline__ bool exchange2(float *xch, uint32_t xbar, uint32_t &cnt, int h, int r,
-                                          float a0, float a1, float &b0, float &b1,
-                                          volatile int *abort_flag) {
-    const int slot = (int)(cnt & 1u);
-    float *mine = xch + ((slot * 2 + h) * 2) * 128;
-    mine[r] = a0;
-    mine[128 + r] = a1;
-    ptx::mbar_arrive(xbar);
-    if (!wait_bar(xbar, cnt & 1u, abort_flag, 11)) return false;
-    ++cnt;
-    const float *other = xch + ((slot * 2 + (1 - h)) * 2) * 128;
-    b0 = other[r];
-    b1 = other[128 + r];
-    return true;
-}
-
 template <int D, bool kFP16>
-__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch,
+__device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tmem,
                              volatile int *abort_flag) {
     using C = Cfg<D>;
+    constexpr int NQ = C::NQ;
     constexpr int BN = C::BN;
-    constexpr int HN = C::HALF_N;
-    constexpr int HD = C::HALF_D;
-    const int h = (int)(threadIdx.x >> 7);      // column half
-    const int r = (int)(threadIdx.x & 127);     // query row within the tile = TMEM lane
-    const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
-    const uint32_t xbar = bar_addr(bars, C::B_XCH + (r >> 5));
+    const int tid = threadIdx.x - wg * 128;                // query row within the tile
+    const uint32_t lane_off = (uint32_t)((tid >> 5) * 32) << 16;  // this warp's TMEM lanes
+    const int q = (NQ == 2) ? wg : 0;
     const float c = p.scale_log2;
-    uint32_t t_cnt = 0;  // key tiles processed (S/P buffer = t & 1)
-    uint32_t x_cnt = 0;  // exchanges with the other half
+    uint32_t t_cnt = 0;  // key tiles processed by this warpgroup (S/P buffer = t & 1)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
@@ -596,86 +574,106 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
         if (u >= p.n_units) break;
         Unit<D> un;
         decode_unit<D>(u, p, un);
-        if (!un.exists[0]) continue;
-        const int row = un.i0[0] + r;
+        if (!un.exists[q]) continue;
+        const int row = un.i0[q] + tid;
         const bool row_ok = row < p.Sq;
         const size_t row_flat = ((size_t)(un.b * p.H + un.h)) * (size_t)p.Sq + (size_t)row;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2 + (size_t)h * HD * 2;
-        if (!un.valid[0]) {
+        if (!un.valid[q]) {
             // No key visible to any row of this tile: guarded output.
             if (row_ok) {
+                uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
 #pragma unroll
-                for (int cc = 0; cc < HD / 8; ++cc) ptx::st_global_v4(orow + cc * 16, 0, 0, 0, 0);
-                if (h == 0) p.lse[row_flat] = -INFINITY;
+                for (int cc = 0; cc < D / 8; ++cc) ptx::st_global_v4(orow + cc * 16, 0, 0, 0, 0);
+                p.lse[row_flat] = -INFINITY;
             }
             continue;
         }
-        // Visible keys of this row: absolute key indices [key_lo, key_hi].
+        // Visible key columns of this row, as absolute key indices [key_lo, key_hi].
         const int key_hi = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row, p.Sk - 1);
         const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
 
         float m_ref = -INFINITY;  // max the accumulator and sums are referenced to (log2 units)
-        float l = 0.f;            // this half's sum of the rounded P multiplied into O
-        float l_exact = 0.f;      // this half's fp32 sum of P (for the logsumexp)
-        const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)(h * HD);
+        float l = 0.f;            // sum of the rounded P actually multiplied into O
+        float l_exact = 0.f;      // fp32 sum of P (for the logsumexp)
+        const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)q * D;
 
-        uint32_t t = 0;
-        for (int j = un.lo[0]; j < un.hi[0]; ++j) {
+        uint32_t t = 0;  // this warpgroup's tile counter at the current key tile
+        for (int j = un.lo[q]; j < un.hi[q]; ++j) {
             t = t_cnt++;
             const int b = (int)(t & 1u);
-            if (!wait_bar(bar_addr(bars, C::B_SFULL + b), (t >> 1) & 1u, abort_flag, 7)) {
+            if (!wait_bar(bar_addr(bars, C::B_SFULL + 2 * q + b), (t >> 1) & 1u, abort_flag, 7)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_off + C::s_col(0, b) + (uint32_t)(h * HN);
+            const uint32_t s_tmem = tmem + lane_off + C::s_col(q, b);
 
-            uint32_t sr[HN];
-            load_row<HN>(s_tmem, sr);
+            uint32_t sr[BN];
+            load_s_row<BN>(s_tmem, sr);
             ptx::tmem_wait_ld();
-            ptx::reg_fence<HN>(sr);
+            ptx::reg_fence<BN>(sr);
 
-            const bool masked = tile_needs_mask<D>(un.i0[0], j, p);
-            const int k0 = j * BN + h * HN;  // first key of this half
-            const float mx_h = masked ? tile_row_max<HN, true>(sr, key_lo - k0, key_hi - k0)
-                                      : tile_row_max<HN, false>(sr, 0, 0);
-            float mx_o, unused;
-            if (!exchange2(xch, xbar, x_cnt, h, r, mx_h, 0.f, mx_o, unused, abort_flag)) {
-                ok = false;
-                break;
+            const bool masked = tile_needs_mask<D>(un.i0[q], j, p);
+            if (masked) apply_mask<BN>(sr, key_lo - j * BN, key_hi - j * BN);
+
+            // Fast path: exponentiate against the current reference max without
+            // looking for this tile's max.  Weights above 2^8 (the max grew by
+            // more than the deferral bound) always push the tile's sum above
+            // 2^8, so a sum within the bound proves the reference is still
+            // valid; otherwise (and on a row's first tile, when there is no
+            // reference yet) the tile takes the slow path below.
+            uint32_t pk[BN / 2];
+            float le_t = 0.f, lr_t = 0.f;  // this tile's exact and rounded sums
+            bool slow = (j == un.lo[q]) || (m_ref == -INFINITY);
+            if (!slow) {
+                if (masked)
+                    tile_row_exp<BN, kFP16, true>(sr, c, -m_ref, pk, le_t, lr_t);
+                else
+                    tile_row_exp<BN, kFP16, false>(sr, c, -m_ref, pk, le_t, lr_t);
+                slow = !(le_t <= kRescaleBound);  // also catches inf
             }
-            const float mx = fmaxf(mx_h, mx_o);
-            const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
-            const float m_new = fmaxf(m_ref, m_tile);
-
-            // Both halves see the same maxima and so take the same decisions.
             float alpha = 1.f;
             bool rescale = false;
-            if (j > un.lo[0]) {
-                if (m_new > m_ref + kRescaleLog2) {
+            if (slow) {
+                const float mx = tile_row_max<BN, false>(sr, 0, 0);
+                const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
+                const float m_new = fmaxf(m_ref, m_tile);
+                bool redo = true;
+                if (j == un.lo[q]) {
+                    m_ref = m_new;
+                } else if (m_new > m_ref + kRescaleLog2) {
                     alpha = ptx::ex2_approx(m_ref - m_new);  // 0 while m_ref is -inf
                     m_ref = m_new;
                     rescale = true;
+                } else {
+                    redo = false;  // the fast-path weights are within the bound
                 }
-            } else {
-                m_ref = m_new;
+                if (redo) {
+                    const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
+                    le_t = 0.f;
+                    lr_t = 0.f;
+                    if (masked)
+                        tile_row_exp<BN, kFP16, true>(sr, c, neg, pk, le_t, lr_t);
+                    else
+                        tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, le_t, lr_t);
+                }
             }
-            // O-barrier phases (one per P V, numbered like t) are consumed in
-            // order: phase t-1 (P V of the previous key tile) is waited for
-            // before P of this tile is released, i.e. before P V of tile t can
-            // exist.  S of this tile implies P V of tile t-2 is done, so the
-            // barrier is then at phase t-1 or t and a parity wait on t-1 is
-            // unambiguous.  The first tile of a unit has nothing to wait for:
+            // O-barrier phases (one per P V of this query slot, numbered like t)
+            // are consumed in order: phase t-1 (P V of the previous key tile) is
+            // waited for before P of this tile is released, i.e. before P V of
+            // tile t can exist.  S of this tile implies P V of tile t-2 is done,
+            // so the barrier is then at phase t-1 or t and a parity wait on t-1
+            // is unambiguous.  The first tile of a unit has nothing to wait for:
             // the previous unit's epilogue consumed its last phase.
             if (__any_sync(0xffffffffu, rescale)) {
                 // O may be touched only once the previous P V has finished.
-                if (!wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8)) {
+                if (!wait_bar(bar_addr(bars, C::B_OFULL + q), (t - 1u) & 1u, abort_flag, 8)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < HD / 32; ++cc) {
+                for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t ov[32];
                     ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
                     ptx::tmem_wait_ld();
@@ -685,40 +683,28 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
                     ptx::tmem_st_x32<0>(o_tmem + cc * 32, ov);
                 }
             }
-            const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-            l *= alpha;
-            l_exact *= alpha;
-            uint32_t pk[HN / 2];
-            if (masked)
-                tile_row_exp<HN, kFP16, true>(sr, c, neg, pk, l_exact, l);
-            else
-                tile_row_exp<HN, kFP16, false>(sr, c, neg, pk, l_exact, l);
-            // P of this half's keys over the start of this half's S columns.
-            store_p_half<HN>(s_tmem, pk);
-            if (j > un.lo[0] &&
-                !wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 10)) {
+            l = alpha * l + lr_t;
+            l_exact = alpha * l_exact + le_t;
+            store_p_row<BN>(s_tmem, pk);
+            if (j > un.lo[q] &&
+                !wait_bar(bar_addr(bars, C::B_OFULL + q), (t - 1u) & 1u, abort_flag, 10)) {
                 ok = false;
                 break;
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + b));
+            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + 2 * q + b));
         }
         if (!ok) break;
 
-        // Epilogue: combine the halves' sums, wait for the last P V (phase t;
-        // phase t-1 was consumed above), divide by l once, store O and lse.
-        float l_o, le_o;
-        if (!exchange2(xch, xbar, x_cnt, h, r, l, l_exact, l_o, le_o, abort_flag)) {
-            ok = false;
-            break;
-        }
-        const float l_sum = l + l_o, le_sum = l_exact + le_o;
-        if (!wait_bar(bar_addr(bars, C::B_OFULL), t & 1u, abort_flag, 9)) { ok = false; break; }
+        // Epilogue: wait for the last P V (phase t; phase t-1 was consumed
+        // above), divide by l once, store O and lse.
+        if (!wait_bar(bar_addr(bars, C::B_OFULL + q), t & 1u, abort_flag, 9)) { ok = false; break; }
         ptx::tc_fence_after();
-        const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
 #pragma unroll
-        for (int cc = 0; cc < HD / 32; ++cc) {
+        for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
             ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
             ptx::tmem_wait_ld();
@@ -735,10 +721,9 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
                                       w[4 * v4 + 2], w[4 * v4 + 3]);
             }
         }
-        if (row_ok && h == 0)
-            p.lse[row_flat] = (le_sum > 0.f) ? (m_ref + log2f(le_sum)) * kLn2 : -INFINITY;
+        if (row_ok) p.lse[row_flat] = (l_exact > 0.f) ? (m_ref + log2f(l_exact)) * kLn2 : -INFINITY;
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE + q));
     }
 }
 
@@ -756,7 +741,6 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-    float *xch = reinterpret_cast<float *>(smem + C::SMEM_TILES + C::NUM_BARS * 8 + 16);
     const uint32_t bars = ptx::smem_addr(bar_mem);
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
@@ -767,7 +751,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
             ptx::mbar_init(bar_addr(bars, C::B_QFULL + q), 1);
             ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + q), 1);
             ptx::mbar_init(bar_addr(bars, C::B_OFULL + q), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_OFREE + q), 256);
+            ptx::mbar_init(bar_addr(bars, C::B_OFREE + q), 128);
         }
         for (int s = 0; s < C::SLOTS; ++s) {
             ptx::mbar_init(bar_addr(bars, C::B_KVFULL + s), 1);
@@ -775,10 +759,9 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2 * C::NQ; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), 256);
+            ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), 128);
         }
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
-        for (int g = 0; g < 4; ++g) ptx::mbar_init(bar_addr(bars, C::B_XCH + g), 64);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
@@ -797,8 +780,8 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp < 8) {
-        softmax_role<D, kFP16>(p, bars, tmem, xch, abort_flag);
+    if (warp < 4 * C::NQ) {
+        softmax_role<D, kFP16>(p, warp >> 2, bars, tmem, abort_flag);
     } else if (warp == C::MMA_WARP) {
         if (lane == 0) mma_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else {
