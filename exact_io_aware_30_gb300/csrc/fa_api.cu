@@ -99,10 +99,9 @@ bool make_map(CUtensorMap *m, const void *base, int d, int S, int H, int B, int 
 
 int head_dim_index(int d) { return d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : -1; }
 
-int nq_for(int d) { return d == 256 ? Cfg<256>::NQ : d == 128 ? Cfg<128>::NQ : Cfg<64>::NQ; }
 int bn_for(int d) { return d == 256 ? Cfg<256>::BN : d == 128 ? Cfg<128>::BN : Cfg<64>::BN; }
-int slots_for(int d) {
-    return d == 256 ? Cfg<256>::SLOTS : d == 128 ? Cfg<128>::SLOTS : Cfg<64>::SLOTS;
+int stages_for(int d) {
+    return d == 256 ? Cfg<256>::STAGES : d == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
 }
 
 // Size / kind checks shared by fa_fwd and fa_workspace_query.
@@ -114,8 +113,7 @@ fa_status check_sizes(int B, int H, int Sq, int Sk, int d, int mask_kind, int wi
         return FA_ERR_UNSUPPORTED;
     if (B < 1 || H < 1 || Sk < 1 || Sq < 0) return FA_ERR_INVALID_ARG;
     if (mask_kind == FA_MASK_SLIDING_WINDOW && window < 1) return FA_ERR_INVALID_ARG;
-    const long long nq = nq_for(d);
-    const long long groups = ((long long)Sq + 128 * nq - 1) / (128 * nq);
+    const long long groups = ((long long)Sq + 127) / 128;
     if ((long long)B * H * groups > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     if ((long long)B * H > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     return FA_OK;
@@ -171,7 +169,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     if (st != FA_OK) return st;
 
     const bool fp16 = dtype == FA_DTYPE_FP16;
-    const int nq = nq_for(d), bn = bn_for(d);
+    const int bn = bn_for(d);
     Params p;
     std::memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_q, q, d, Sq, H, B, 128, fp16) || !make_map(&p.tm_k, k, d, Sk, H, B, bn, fp16) ||
@@ -187,8 +185,7 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     p.window = (mask_kind == FA_MASK_SLIDING_WINDOW) ? window : 0;
     p.scale_log2 = (float)((double)scale * 1.4426950408889634);
     p.n_qtiles = (Sq + 127) / 128;
-    p.n_groups = (p.n_qtiles + nq - 1) / nq;
-    p.n_units = B * H * p.n_groups;
+    p.n_units = B * H * p.n_qtiles;
 
     if (log_enabled()) {
         char buf[256];
@@ -263,10 +260,10 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     }
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
-                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d q_tiles_per_cta=%d "
-                  "s_buffers_per_q_tile=2 kv_ring=%d threads=%d smem=%d mask=%s persistent",
-                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::nq_for(d),
-                  fa::slots_for(d), 32 * (4 * fa::nq_for(d) + 2),
+                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=2 "
+                  "kv_stages=%d threads=%d smem=%d mask=%s persistent",
+                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::stages_for(d),
+                  fa::Cfg<128>::NUM_THREADS,
                   d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES
                                                                : fa::Cfg<256>::SMEM_BYTES,
                   masks[mask_kind]);

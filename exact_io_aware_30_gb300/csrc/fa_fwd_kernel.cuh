@@ -14,25 +14,29 @@
 // tensor memory.
 //
 // GB300 mapping (one CTA per SM, persistent over work units):
-//   * a work unit is NQ query tiles of 128 rows of one (batch, head);
-//     units are taken longest-first in a snake order over the CTAs;
-//   * one TMA warp streams Q tiles and a ring of K / V tiles (128-byte
-//     swizzled, 64 columns per box) into shared memory under mbarriers;
+//   * a work unit is one query tile of 128 rows of one (batch, head); units
+//     are taken longest-first in a snake order over the CTAs;
+//   * one TMA warp streams the Q tile and a ring of stages into shared
+//     memory (128-byte swizzle, 64 columns per box); stage k of a unit holds
+//     key tile k and value tile k-1, the two tiles one MMA iteration uses;
 //   * one MMA warp (a single issuing lane) runs S = Q K^T (both operands in
 //     shared memory) and O += P V (P read from tensor memory) as tcgen05
-//     MMAs with fp32 accumulators in tensor memory;
-//   * NQ softmax warpgroups own one query row per thread (= one TMEM lane):
-//     they read a row of S, apply the mask on boundary tiles only, update the
-//     running max / sum, write P (16-bit) back over S, rescale O in tensor
-//     memory when the max grew enough, and run the epilogue (O / l, lse).
-//   With NQ = 2 the two warpgroups ping-pong: the tensor core computes one
-//   tile's MMAs while the other tile's softmax runs.
+//     MMAs with fp32 accumulators in tensor memory.  S has two buffers: the
+//     S MMA of key tile j+1 is issued before P V of tile j, so it runs while
+//     the softmax works on tile j;
+//   * one softmax warpgroup owns the 128 rows, one row per thread (= one
+//     TMEM lane): it reads a row of S, masks boundary tiles, exponentiates,
+//     writes P (16-bit) back over S, rescales O in tensor memory when the max
+//     grew enough, and runs the epilogue (O / l, lse).
 //
 // Rescaling is deferred until the running max has grown by more than 2^8
-// (log2 units).  Until then the accumulator and the sum both stay referenced
+// (log2 units).  Until then the accumulator and the sums both stay referenced
 // to the same stale max, so the final O_acc / l is unchanged (the pages'
 // remark that FlashAttention-2 "defers most rescaling"); the stale reference
-// only lets unnormalised weights reach 2^8, far from fp32/bf16 limits.
+// only lets unnormalised weights reach 2^8, far from fp32/bf16/fp16 limits.
+// The tile max itself is only computed when needed: a weight above 2^8
+// pushes the tile's sum above 2^8, so a tile whose sum stays within the bound
+// is valid as computed against the current reference.
 #pragma once
 
 #include <stdint.h>
@@ -63,53 +67,47 @@ struct Params {
     int B, H, Sq, Sk;
     int mask_kind, window;
     float scale_log2;  // scale * log2(e)
-    int n_qtiles;      // ceil(Sq / 128)
-    int n_groups;      // ceil(n_qtiles / NQ): units per (batch, head)
-    int n_units;       // B * H * n_groups
+    int n_qtiles;      // ceil(Sq / 128): units per (batch, head)
+    int n_units;       // B * H * n_qtiles
 };
 
 template <int D>
 struct Cfg {
-    // One query tile per unit with two S buffers: the S MMA of key tile j+1
-    // runs while the softmax works on tile j.  d = 256 uses 64-key tiles so
-    // that two S buffers and its 256-column O fit in tensor memory and a
-    // 5-deep K/V ring fits in shared memory.
+    // d = 256 uses 64-key tiles so that two S buffers and its 256-column O fit
+    // in tensor memory and two stages fit in shared memory.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
-    static constexpr int NQ = 1;                         // query tiles per unit
-    static constexpr int SLOTS = (D == 64) ? 12 : (D == 128) ? 6 : 5;  // K/V ring depth (tiles)
-    // Warps: NQ softmax warpgroups (warps 0 .. 4*NQ-1), then the MMA warp and
-    // the TMA warp.
-    static constexpr int NUM_WARPS = 4 * NQ + 2;
+    static constexpr int STAGES = (D == 64) ? 6 : (D == 128) ? 3 : 2;
+    // Warps 0-3: softmax warpgroup; warp 4: MMA issue; warp 5: TMA.
+    static constexpr int NUM_WARPS = 6;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
-    static constexpr int MMA_WARP = 4 * NQ;
-    static constexpr int TMA_WARP = 4 * NQ + 1;
+    static constexpr int MMA_WARP = 4;
+    static constexpr int TMA_WARP = 5;
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
     static constexpr int Q_BYTES = kBM * D * 2;
-    static constexpr int SLOT_BYTES = BN * D * 2;
-    // Tensor memory: two S/P buffers per query tile (BN columns each) at
-    // columns (2q + b) * BN, O accumulators (D columns each) from column 256.
+    static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K part at 0, V part at TILE_BYTES
+    // Tensor memory: S/P buffers at columns 0 and BN, O from column 256.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t O_COL0 = 256;
     // Barrier indices.
     static constexpr int B_QFULL = 0;
-    static constexpr int B_QEMPTY = B_QFULL + NQ;
-    static constexpr int B_KVFULL = B_QEMPTY + NQ;
-    static constexpr int B_KVEMPTY = B_KVFULL + SLOTS;
-    static constexpr int B_SFULL = B_KVEMPTY + SLOTS;   // [2 * NQ]: S buffer (q, b) computed
-    static constexpr int B_PFULL = B_SFULL + 2 * NQ;    // [2 * NQ]: P buffer (q, b) written
-    static constexpr int B_OFULL = B_PFULL + 2 * NQ;    // [NQ]: one phase per P V
-    static constexpr int B_OFREE = B_OFULL + NQ;        // [NQ]: epilogue has read O
-    static constexpr int B_DRAIN = B_OFREE + NQ;
+    static constexpr int B_QEMPTY = 1;
+    static constexpr int B_STFULL = 2;                  // [STAGES]
+    static constexpr int B_STEMPTY = B_STFULL + STAGES; // [STAGES]
+    static constexpr int B_SFULL = B_STEMPTY + STAGES;  // [2]: S buffer b computed
+    static constexpr int B_PFULL = B_SFULL + 2;         // [2]: P buffer b written
+    static constexpr int B_OFULL = B_PFULL + 2;         // one phase per P V
+    static constexpr int B_OFINAL = B_OFULL + 1;        // one phase per unit: last P V done
+    static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
+    static constexpr int B_DRAIN = B_OFREE + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
-    static constexpr int SMEM_TILES = NQ * Q_BYTES + SLOTS * SLOT_BYTES;
+    static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
-    static_assert(O_COL0 + NQ * D <= TMEM_COLS, "tensor memory overflow");
-    static_assert(2 * NQ * BN <= (int)O_COL0, "S buffers overlap O");
+    static_assert(O_COL0 + D <= TMEM_COLS, "tensor memory overflow");
+    static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
-
-    __device__ static constexpr uint32_t s_col(int q, int b) { return (uint32_t)((2 * q + b) * BN); }
 };
 
 // ---------------------------------------------------------------- helpers
@@ -135,7 +133,7 @@ __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base
 
 // Bounded wait: gives up (and raises the abort flag and the device status
 // word) after kWaitLimitNs, or as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            int site) {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {
@@ -156,7 +154,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Wait used only while shutting down after an abort: ignores the abort flag.
-__device__ __forceinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
+__device__ __noinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = ptx::globaltimer_ns();
     while (!ptx::mbar_try_wait(bar, parity)) {
         if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
@@ -171,65 +169,35 @@ __device__ __forceinline__ int unit_at(int k) {
     return (k & 1) ? k * G + (G - 1 - c) : k * G + c;
 }
 
-template <int D>
+// One work unit: query tile [i0, i0 + 128) of head (b, h) and the key tiles
+// [lo, hi) it has to visit (tiles the mask hides entirely are skipped:
+// causal keys past the tile's last row, window keys before its first row's
+// window).  valid = the tile sees at least one key tile.
 struct Unit {
-    int b, h;
-    int i0[Cfg<D>::NQ];     // first query row of each tile
-    int lo[Cfg<D>::NQ];     // K/V tile range [lo, hi) each tile must visit
-    int hi[Cfg<D>::NQ];
-    bool exists[Cfg<D>::NQ];  // tile has rows < Sq
-    bool valid[Cfg<D>::NQ];   // exists and sees at least one key tile
-    int ulo, uhi;             // union of the valid ranges
-    bool any;
+    int b, h, i0, lo, hi;
+    bool valid;
 };
 
-// Key tiles a query tile [i0, i0 + 128) has to visit: skip tiles the mask
-// hides entirely (causal: keys past the last row; window: keys before the
-// first row's window).
 template <int D>
-__device__ __forceinline__ void kv_range(int i0, const Params &p, int &lo, int &hi) {
+__device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
     constexpr int BN = Cfg<D>::BN;
-    const int row_end = min(i0 + kBM, p.Sq);
-    int key_end = p.Sk;
-    if (p.mask_kind != kMaskNone) key_end = min(p.Sk, row_end);
-    int key_beg = 0;
-    if (p.mask_kind == kMaskWindow) key_beg = max(0, i0 - p.window + 1);
-    if (key_beg >= key_end) {
-        lo = 0;
-        hi = 0;
-        return;
-    }
-    lo = key_beg / BN;
-    hi = (key_end + BN - 1) / BN;
-}
-
-template <int D>
-__device__ __forceinline__ void decode_unit(int u, const Params &p, Unit<D> &un) {
-    constexpr int NQ = Cfg<D>::NQ;
+    Unit un;
     const int BH = p.B * p.H;
     const int gi = u / BH;
     const int bh = u - gi * BH;
-    const int g = p.n_groups - 1 - gi;  // longest first (causal / window)
+    const int g = p.n_qtiles - 1 - gi;  // longest first (causal / window)
     un.b = bh / p.H;
     un.h = bh - un.b * p.H;
-    un.ulo = 0x7fffffff;
-    un.uhi = 0;
-    un.any = false;
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        const int i0 = (g * NQ + q) * kBM;
-        un.i0[q] = i0;
-        un.exists[q] = i0 < p.Sq;
-        un.lo[q] = 0;
-        un.hi[q] = 0;
-        if (un.exists[q]) kv_range<D>(i0, p, un.lo[q], un.hi[q]);
-        un.valid[q] = un.exists[q] && un.lo[q] < un.hi[q];
-        if (un.valid[q]) {
-            un.ulo = min(un.ulo, un.lo[q]);
-            un.uhi = max(un.uhi, un.hi[q]);
-            un.any = true;
-        }
-    }
+    un.i0 = g * kBM;
+    const int row_end = min(un.i0 + kBM, p.Sq);
+    int key_end = p.Sk;
+    if (p.mask_kind != kMaskNone) key_end = min(p.Sk, row_end);
+    int key_beg = 0;
+    if (p.mask_kind == kMaskWindow) key_beg = max(0, un.i0 - p.window + 1);
+    un.valid = key_beg < key_end;
+    un.lo = un.valid ? key_beg / BN : 0;
+    un.hi = un.valid ? (key_end + BN - 1) / BN : 0;
+    return un;
 }
 
 // True if some (row, key) pair of this query tile x key tile is hidden.
@@ -246,72 +214,73 @@ __device__ __forceinline__ bool tile_needs_mask(int i0, int j, const Params &p) 
 
 // ---------------------------------------------------------------- TMA role
 
+// Stage k of a unit with n key tiles (k = 0 .. n) holds key tile lo+k (if
+// k < n) at offset 0 and value tile lo+k-1 (if k >= 1) at TILE_BYTES.
 template <int D>
 __device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
                          volatile int *abort_flag) {
     using C = Cfg<D>;
     const uint64_t pol_kv = ptx::policy_evict_last();
     const uint64_t pol_q = ptx::policy_evict_first();
-    uint32_t kv_it = 0;
-    uint32_t q_cnt[C::NQ];
-#pragma unroll
-    for (int q = 0; q < C::NQ; ++q) q_cnt[q] = 0;
+    uint32_t st_it = 0;  // stages filled so far
+    uint32_t q_cnt = 0;  // Q tiles loaded so far
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
         const int u = unit_at(k);
         if (u >= p.n_units) break;
-        Unit<D> un;
-        decode_unit<D>(u, p, un);
-        if (!un.any) continue;
+        const Unit un = decode_unit<D>(u, p);
+        if (!un.valid) continue;
+        if (!wait_bar(bar_addr(bars, C::B_QEMPTY), (q_cnt & 1) ^ 1, abort_flag, 1)) {
+            ok = false;
+            break;
+        }
+        {
+            const uint32_t fb = bar_addr(bars, C::B_QFULL);
+            ptx::mbar_arrive_expect_tx(fb, C::Q_BYTES);
+            const uint32_t dst = ptx::smem_addr(sQ);
 #pragma unroll
-        for (int q = 0; q < C::NQ; ++q) {
-            if (!un.valid[q] || !ok) continue;
-            if (!wait_bar(bar_addr(bars, C::B_QEMPTY + q), (q_cnt[q] & 1) ^ 1, abort_flag, 1)) {
+            for (int c = 0; c < C::CHUNKS; ++c)
+                ptx::tma_load_4d(dst + c * C::Q_CHUNK, &p.tm_q, fb, c * 64, un.i0, un.h, un.b, pol_q);
+            ++q_cnt;
+        }
+        const int n = un.hi - un.lo;
+        for (int s = 0; s <= n; ++s) {
+            const uint32_t slot = st_it % C::STAGES;
+            if (!wait_bar(bar_addr(bars, C::B_STEMPTY + slot), ((st_it / C::STAGES) & 1) ^ 1,
+                          abort_flag, 2)) {
                 ok = false;
                 break;
             }
-            const uint32_t fb = bar_addr(bars, C::B_QFULL + q);
-            ptx::mbar_arrive_expect_tx(fb, C::Q_BYTES);
-            const uint32_t dst = ptx::smem_addr(sQ + q * C::Q_BYTES);
-#pragma unroll
-            for (int c = 0; c < C::CHUNKS; ++c)
-                ptx::tma_load_4d(dst + c * C::Q_CHUNK, &p.tm_q, fb, c * 64, un.i0[q], un.h, un.b,
-                                 pol_q);
-            ++q_cnt[q];
-        }
-        for (int j = un.ulo; j < un.uhi && ok; ++j) {
-#pragma unroll
-            for (int kv = 0; kv < 2; ++kv) {
-                const uint32_t slot = kv_it % C::SLOTS;
-                if (!wait_bar(bar_addr(bars, C::B_KVEMPTY + slot), ((kv_it / C::SLOTS) & 1) ^ 1,
-                              abort_flag, 2)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t fb = bar_addr(bars, C::B_KVFULL + slot);
-                ptx::mbar_arrive_expect_tx(fb, C::SLOT_BYTES);
-                const uint32_t dst = ptx::smem_addr(sKV + slot * C::SLOT_BYTES);
-                const CUtensorMap *m = kv ? &p.tm_v : &p.tm_k;
+            const bool has_k = s < n, has_v = s >= 1;
+            const uint32_t fb = bar_addr(bars, C::B_STFULL + slot);
+            ptx::mbar_arrive_expect_tx(fb, (has_k ? C::TILE_BYTES : 0) + (has_v ? C::TILE_BYTES : 0));
+            const uint32_t dst = ptx::smem_addr(sKV + slot * C::STAGE_BYTES);
+            if (has_k) {
 #pragma unroll
                 for (int c = 0; c < C::CHUNKS; ++c)
-                    ptx::tma_load_4d(dst + c * C::KV_CHUNK, m, fb, c * 64, j * C::BN, un.h, un.b,
-                                     pol_kv);
-                ++kv_it;
+                    ptx::tma_load_4d(dst + c * C::KV_CHUNK, &p.tm_k, fb, c * 64, (un.lo + s) * C::BN,
+                                     un.h, un.b, pol_kv);
             }
+            if (has_v) {
+#pragma unroll
+                for (int c = 0; c < C::CHUNKS; ++c)
+                    ptx::tma_load_4d(dst + C::TILE_BYTES + c * C::KV_CHUNK, &p.tm_v, fb, c * 64,
+                                     (un.lo + s - 1) * C::BN, un.h, un.b, pol_kv);
+            }
+            ++st_it;
         }
     }
     if (!ok) {
         // Let every copy already issued land before the CTA can exit.
-        // Slot s has been filled ceil((kv_it - s) / SLOTS) times so far.
+        // Slot s has been filled ceil((st_it - s) / STAGES) times so far.
 #pragma unroll
-        for (int s = 0; s < C::SLOTS; ++s) {
-            const uint32_t fills = kv_it > (uint32_t)s ? (kv_it - (uint32_t)s + C::SLOTS - 1) / C::SLOTS : 0u;
-            if (fills) wait_bar_drain(bar_addr(bars, C::B_KVFULL + s), (fills - 1) & 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            const uint32_t fills =
+                st_it > (uint32_t)s ? (st_it - (uint32_t)s + C::STAGES - 1) / C::STAGES : 0u;
+            if (fills) wait_bar_drain(bar_addr(bars, C::B_STFULL + s), (fills - 1) & 1);
         }
-#pragma unroll
-        for (int q = 0; q < C::NQ; ++q)
-            if (q_cnt[q]) wait_bar_drain(bar_addr(bars, C::B_QFULL + q), (q_cnt[q] - 1) & 1);
+        if (q_cnt) wait_bar_drain(bar_addr(bars, C::B_QFULL), (q_cnt - 1) & 1);
     }
 }
 
@@ -321,142 +290,97 @@ template <int D, bool kFP16>
 __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
                          uint32_t tmem, volatile int *abort_flag) {
     using C = Cfg<D>;
-    constexpr int NQ = C::NQ;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
     constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
+    const uint32_t q_addr = ptx::smem_addr(sQ);
+    const uint32_t kv_addr = ptx::smem_addr(sKV);
+    const uint64_t dq = smem_desc(q_addr, 16);
+    const uint32_t o_tmem = tmem + C::O_COL0;
 
-    uint32_t kv_it = 0;          // K/V ring fills consumed so far
-    uint32_t q_cnt[NQ];          // Q tiles consumed per query slot
-    uint32_t t_cnt[NQ];          // key tiles processed per query slot (S/P buffer = t & 1)
-    uint32_t ofree_cnt[NQ];      // epilogues waited for per O accumulator
-    bool o_used[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        q_cnt[q] = 0;
-        t_cnt[q] = 0;
-        ofree_cnt[q] = 0;
-        o_used[q] = false;
-    }
+    uint32_t st_it = 0;      // stages consumed so far
+    uint32_t t_cnt = 0;      // key tiles processed (S/P buffer = t & 1)
+    uint32_t q_cnt = 0;      // Q tiles consumed
+    uint32_t ofree_cnt = 0;  // epilogues waited for
+    bool o_used = false;
     bool ok = true;
+
+    // S_b = Q K^T with K at the start of stage `slot`.
+    auto issue_s = [&](uint32_t slot, uint32_t b) {
+        const uint64_t dk = smem_desc(kv_addr + slot * C::STAGE_BYTES, 16);
+        const uint32_t d_tmem = tmem + b * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
+            const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
+            const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+            ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
+    };
+    auto wait_stage = [&](uint32_t idx) -> bool {
+        return wait_bar(bar_addr(bars, C::B_STFULL + idx % C::STAGES), (idx / C::STAGES) & 1,
+                        abort_flag, 3);
+    };
 
     for (int k = 0; ok; ++k) {
         const int u = unit_at(k);
         if (u >= p.n_units) break;
-        Unit<D> un;
-        decode_unit<D>(u, p, un);
-        if (!un.any) continue;
-        const uint32_t kv_base = kv_it;
-        auto kidx = [&](int j) -> uint32_t { return kv_base + 2u * (uint32_t)(j - un.ulo); };
-        auto wait_kv = [&](uint32_t idx) -> bool {
-            return wait_bar(bar_addr(bars, C::B_KVFULL + idx % C::SLOTS), (idx / C::SLOTS) & 1,
-                            abort_flag, 3);
-        };
-        auto release_kv = [&](uint32_t idx) {
-            ptx::mma_commit(bar_addr(bars, C::B_KVEMPTY + idx % C::SLOTS));
-        };
+        const Unit un = decode_unit<D>(u, p);
+        if (!un.valid) continue;
+        const int n = un.hi - un.lo;
+        const uint32_t base = st_it;
 
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            if (!un.valid[q] || !ok) continue;
-            ok = wait_bar(bar_addr(bars, C::B_QFULL + q), q_cnt[q] & 1, abort_flag, 6);
-        }
-        if (!ok) break;
+        if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, abort_flag, 6)) { ok = false; break; }
+        // Stage 0 holds the first key tile only.
+        if (!wait_stage(base)) { ok = false; break; }
+        issue_s(base % C::STAGES, t_cnt & 1u);
+        if (n == 1) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
+        ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
 
-        // S_q(x) is issued one key tile ahead of P_q V: the softmax of tile j
-        // overlaps the S MMA of tile j + 1 (two S buffers per query tile).
-        int ns[NQ];
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) ns[q] = un.lo[q];
-        int k_ready = un.ulo - 1;  // highest key tile waited for
-        int k_rel = un.ulo;        // next key tile to hand back to the TMA warp
-
-        for (int j = un.ulo; j < un.uhi && ok; ++j) {
-            // 1. every S of key tiles <= j + 1
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                if (!un.valid[q]) continue;
-                while (ns[q] < un.hi[q] && ns[q] <= j + 1) {
-                    const int x = ns[q];
-                    if (x > k_ready) {
-                        if (!wait_kv(kidx(x))) { ok = false; break; }
-                        k_ready = x;
-                    }
-                    const int b = (int)((t_cnt[q] + (uint32_t)(x - un.lo[q])) & 1u);
-                    const uint32_t a0 = ptx::smem_addr(sQ + q * C::Q_BYTES);
-                    const uint32_t b0 = ptx::smem_addr(sKV + (kidx(x) % C::SLOTS) * C::SLOT_BYTES);
-                    const uint32_t d_tmem = tmem + C::s_col(q, b);
-                    const uint64_t da = smem_desc(a0, 16), db = smem_desc(b0, 16);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
-                        const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
-                        const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
-                        ptx::mma_ss(d_tmem, da + off_a, db + off_b, kIdescS, kk > 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(bar_addr(bars, C::B_SFULL + 2 * q + b));
-                    ++ns[q];
-                    if (ns[q] == un.hi[q]) {  // last read of this Q tile in the unit
-                        ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + q));
-                        ++q_cnt[q];
-                    }
-                }
-                if (!ok) break;
+        for (int i = 0; i < n; ++i) {
+            const uint32_t t = t_cnt + (uint32_t)i;
+            const uint32_t sidx = base + 1u + (uint32_t)i;  // stage: key tile i+1, value tile i
+            const uint32_t slot = sidx % C::STAGES;
+            if (!wait_stage(sidx)) { ok = false; break; }
+            if (i + 1 < n) {
+                // S of the next key tile, into the other buffer (whose P V was
+                // issued last iteration), ahead of this tile's P V.
+                issue_s(slot, (t + 1u) & 1u);
+                if (i + 2 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
             }
-            if (!ok) break;
-            // every S that reads key tiles <= k_ready has been issued
-            while (k_rel <= k_ready) {
-                release_kv(kidx(k_rel));
-                ++k_rel;
+            const uint32_t b = t & 1u;
+            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)b), (t >> 1) & 1u, abort_flag, 4)) {
+                ok = false;
+                break;
             }
-            // 2. O_q (+)= P_q V_j for every query tile that sees key tile j
-            bool v_ready = false;
-#pragma unroll
-            for (int q = 0; q < NQ; ++q) {
-                if (!un.valid[q] || j < un.lo[q] || j >= un.hi[q]) continue;
-                if (!v_ready) {
-                    if (!wait_kv(kidx(j) + 1)) { ok = false; break; }
-                    v_ready = true;
-                }
-                const uint32_t t = t_cnt[q] + (uint32_t)(j - un.lo[q]);
-                const int b = (int)(t & 1u);
-                if (!wait_bar(bar_addr(bars, C::B_PFULL + 2 * q + b), (t >> 1) & 1u, abort_flag, 4)) {
+            ptx::tc_fence_after();
+            if (i == 0 && o_used) {
+                if (!wait_bar(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, abort_flag, 5)) {
                     ok = false;
                     break;
                 }
+                ++ofree_cnt;
                 ptx::tc_fence_after();
-                const bool first = (j == un.lo[q]);
-                if (first && o_used[q]) {
-                    if (!wait_bar(bar_addr(bars, C::B_OFREE + q), ofree_cnt[q] & 1, abort_flag, 5)) {
-                        ok = false;
-                        break;
-                    }
-                    ++ofree_cnt[q];
-                    ptx::tc_fence_after();
-                }
-                const uint32_t v0 = ptx::smem_addr(sKV + ((kidx(j) + 1) % C::SLOTS) * C::SLOT_BYTES);
-                const uint32_t d_tmem = tmem + C::O_COL0 + (uint32_t)q * D;
-                const uint32_t p_tmem = tmem + C::s_col(q, b);
-                const uint64_t dv = smem_desc(v0, C::KV_CHUNK);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 keys = two 8-row groups (2048 bytes) per step; P: 8 columns.
-                    ptx::mma_ts(d_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4),
-                                kIdescO, (!first || kk > 0) ? 1u : 0u);
-                }
-                ptx::mma_commit(bar_addr(bars, C::B_OFULL + q));
             }
-            if (!ok) break;
-            release_kv(kidx(j) + 1);
+            // O (+)= P V
+            const uint64_t dv = smem_desc(kv_addr + slot * C::STAGE_BYTES + C::TILE_BYTES, C::KV_CHUNK);
+            const uint32_t p_tmem = tmem + b * BN;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk) {
+                // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
+                ptx::mma_ts(o_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4), kIdescO,
+                            (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(bar_addr(bars, C::B_OFULL));
+            if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
+            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));
         }
         if (!ok) break;
-        kv_it = kv_base + 2u * (uint32_t)(un.uhi - un.ulo);
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-            if (!un.valid[q]) continue;
-            t_cnt[q] += (uint32_t)(un.hi[q] - un.lo[q]);
-            o_used[q] = true;
-        }
+        st_it = base + (uint32_t)n + 1u;
+        t_cnt += (uint32_t)n;
+        ++q_cnt;
+        o_used = true;
     }
     // Every MMA issued must finish before tensor memory is released.
     ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
@@ -483,7 +407,7 @@ __device__ __forceinline__ void store_p_row(uint32_t taddr, const uint32_t (&r)[
     if constexpr (BN == 128) ptx::tmem_st_x32<32>(taddr + 32, r);
 }
 
-template <int D, bool kFP16>
+template <bool kFP16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
 }
@@ -496,15 +420,9 @@ __device__ __forceinline__ void apply_mask(uint32_t (&sr)[BN], int c_lo, int c_h
         if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
 }
 
-// Row max of one S tile (raw scores; scale >= 0 preserves the order).  With
-// kMasked, columns outside [c_lo, c_hi] are first set to -inf.
-template <int BN, bool kMasked>
-__device__ __forceinline__ float tile_row_max(uint32_t (&sr)[BN], int c_lo, int c_hi) {
-    if constexpr (kMasked) {
-#pragma unroll
-        for (int i = 0; i < BN; ++i)
-            if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
-    }
+// Row max of one S tile (raw scores; scale >= 0 preserves the order).
+template <int BN>
+__device__ __forceinline__ float tile_row_max(const uint32_t (&sr)[BN]) {
     float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
     float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
 #pragma unroll
@@ -541,7 +459,7 @@ __device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, 
             e0 = (x0 == -INFINITY) ? 0.f : e0;
             e1 = (x1 == -INFINITY) ? 0.f : e1;
         }
-        const uint32_t pw = kFP16 ? ptx::pack_f16x2(e0, e1) : ptx::pack_bf16x2(e0, e1);
+        const uint32_t pw = pack2<kFP16>(e0, e1);
         pk[i / 2] = pw;
         if ((i >> 1) & 1)
             le1 = ptx::add_f32x2(le1, ptx::f32x2(e0, e1));
@@ -557,74 +475,71 @@ __device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, 
 }
 
 template <int D, bool kFP16>
-__device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tmem,
+__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
                              volatile int *abort_flag) {
     using C = Cfg<D>;
-    constexpr int NQ = C::NQ;
     constexpr int BN = C::BN;
-    const int tid = threadIdx.x - wg * 128;                // query row within the tile
-    const uint32_t lane_off = (uint32_t)((tid >> 5) * 32) << 16;  // this warp's TMEM lanes
-    const int q = (NQ == 2) ? wg : 0;
+    const int r = (int)threadIdx.x;                           // query row within the tile
+    const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
+    const uint32_t o_tmem = tmem + lane_off + C::O_COL0;
     const float c = p.scale_log2;
-    uint32_t t_cnt = 0;  // key tiles processed by this warpgroup (S/P buffer = t & 1)
+    uint32_t t_cnt = 0;  // key tiles processed (S/P buffer = t & 1; one P V each)
+    uint32_t u_cnt = 0;  // units completed (one O-final phase each)
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
         const int u = unit_at(k);
         if (u >= p.n_units) break;
-        Unit<D> un;
-        decode_unit<D>(u, p, un);
-        if (!un.exists[q]) continue;
-        const int row = un.i0[q] + tid;
+        const Unit un = decode_unit<D>(u, p);
+        if (un.i0 >= p.Sq) continue;
+        const int row = un.i0 + r;
         const bool row_ok = row < p.Sq;
         const size_t row_flat = ((size_t)(un.b * p.H + un.h)) * (size_t)p.Sq + (size_t)row;
-        if (!un.valid[q]) {
+        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
+        if (!un.valid) {
             // No key visible to any row of this tile: guarded output.
             if (row_ok) {
-                uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
 #pragma unroll
                 for (int cc = 0; cc < D / 8; ++cc) ptx::st_global_v4(orow + cc * 16, 0, 0, 0, 0);
                 p.lse[row_flat] = -INFINITY;
             }
             continue;
         }
-        // Visible key columns of this row, as absolute key indices [key_lo, key_hi].
+        // Visible keys of this row: absolute key indices [key_lo, key_hi].
         const int key_hi = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row, p.Sk - 1);
         const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
 
         float m_ref = -INFINITY;  // max the accumulator and sums are referenced to (log2 units)
-        float l = 0.f;            // sum of the rounded P actually multiplied into O
+        float l = 0.f;            // sum of the rounded P multiplied into O
         float l_exact = 0.f;      // fp32 sum of P (for the logsumexp)
-        const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)q * D;
 
-        uint32_t t = 0;  // this warpgroup's tile counter at the current key tile
-        for (int j = un.lo[q]; j < un.hi[q]; ++j) {
-            t = t_cnt++;
+        for (int j = un.lo; j < un.hi; ++j) {
+            const uint32_t t = t_cnt++;
             const int b = (int)(t & 1u);
-            if (!wait_bar(bar_addr(bars, C::B_SFULL + 2 * q + b), (t >> 1) & 1u, abort_flag, 7)) {
+            if (!wait_bar(bar_addr(bars, C::B_SFULL + b), (t >> 1) & 1u, abort_flag, 7)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_off + C::s_col(q, b);
+            const uint32_t s_tmem = tmem + lane_off + (uint32_t)(b * BN);
 
             uint32_t sr[BN];
             load_s_row<BN>(s_tmem, sr);
             ptx::tmem_wait_ld();
             ptx::reg_fence<BN>(sr);
 
-            const bool masked = tile_needs_mask<D>(un.i0[q], j, p);
+            const bool masked = tile_needs_mask<D>(un.i0, j, p);
             if (masked) apply_mask<BN>(sr, key_lo - j * BN, key_hi - j * BN);
 
             // Fast path: exponentiate against the current reference max without
             // looking for this tile's max.  Weights above 2^8 (the max grew by
             // more than the deferral bound) always push the tile's sum above
-            // 2^8, so a sum within the bound proves the reference is still
-            // valid; otherwise (and on a row's first tile, when there is no
-            // reference yet) the tile takes the slow path below.
+            // 2^8, so a sum within the bound proves the reference still valid;
+            // otherwise (and on a row's first tile, when there is no reference
+            // yet) the tile takes the slow path below.
             uint32_t pk[BN / 2];
             float le_t = 0.f, lr_t = 0.f;  // this tile's exact and rounded sums
-            bool slow = (j == un.lo[q]) || (m_ref == -INFINITY);
+            bool slow = (j == un.lo) || (m_ref == -INFINITY);
             if (!slow) {
                 if (masked)
                     tile_row_exp<BN, kFP16, true>(sr, c, -m_ref, pk, le_t, lr_t);
@@ -635,11 +550,11 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             float alpha = 1.f;
             bool rescale = false;
             if (slow) {
-                const float mx = tile_row_max<BN, false>(sr, 0, 0);
+                const float mx = tile_row_max<BN>(sr);
                 const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
                 const float m_new = fmaxf(m_ref, m_tile);
                 bool redo = true;
-                if (j == un.lo[q]) {
+                if (j == un.lo) {
                     m_ref = m_new;
                 } else if (m_new > m_ref + kRescaleLog2) {
                     alpha = ptx::ex2_approx(m_ref - m_new);  // 0 while m_ref is -inf
@@ -658,16 +573,13 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
                         tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, le_t, lr_t);
                 }
             }
-            // O-barrier phases (one per P V of this query slot, numbered like t)
-            // are consumed in order: phase t-1 (P V of the previous key tile) is
-            // waited for before P of this tile is released, i.e. before P V of
-            // tile t can exist.  S of this tile implies P V of tile t-2 is done,
-            // so the barrier is then at phase t-1 or t and a parity wait on t-1
-            // is unambiguous.  The first tile of a unit has nothing to wait for:
-            // the previous unit's epilogue consumed its last phase.
             if (__any_sync(0xffffffffu, rescale)) {
-                // O may be touched only once the previous P V has finished.
-                if (!wait_bar(bar_addr(bars, C::B_OFULL + q), (t - 1u) & 1u, abort_flag, 8)) {
+                // O may be touched only once the previous P V has finished: wait
+                // for phase t-1 of the O barrier (one phase per P V, numbered like
+                // t).  S of this tile was issued after P V of tile t-2 and P V of
+                // tile t cannot exist before this tile's P, so the barrier is at
+                // phase t-1 or t and the parity wait is unambiguous.
+                if (!wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8)) {
                     ok = false;
                     break;
                 }
@@ -686,23 +598,17 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             l = alpha * l + lr_t;
             l_exact = alpha * l_exact + le_t;
             store_p_row<BN>(s_tmem, pk);
-            if (j > un.lo[q] &&
-                !wait_bar(bar_addr(bars, C::B_OFULL + q), (t - 1u) & 1u, abort_flag, 10)) {
-                ok = false;
-                break;
-            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + 2 * q + b));
+            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + b));
         }
         if (!ok) break;
 
-        // Epilogue: wait for the last P V (phase t; phase t-1 was consumed
-        // above), divide by l once, store O and lse.
-        if (!wait_bar(bar_addr(bars, C::B_OFULL + q), t & 1u, abort_flag, 9)) { ok = false; break; }
+        // Epilogue: wait for the unit's last P V, divide by l once, store O and lse.
+        if (!wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9)) { ok = false; break; }
+        ++u_cnt;
         ptx::tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t ov[32];
@@ -712,8 +618,8 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
             uint32_t w[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                w[i] = pack2<D, kFP16>(__uint_as_float(ov[2 * i]) * inv_l,
-                                       __uint_as_float(ov[2 * i + 1]) * inv_l);
+                w[i] = pack2<kFP16>(__uint_as_float(ov[2 * i]) * inv_l,
+                                    __uint_as_float(ov[2 * i + 1]) * inv_l);
             if (row_ok) {
 #pragma unroll
                 for (int v4 = 0; v4 < 4; ++v4)
@@ -723,7 +629,7 @@ __device__ void softmax_role(const Params &p, int wg, uint32_t bars, uint32_t tm
         }
         if (row_ok) p.lse[row_flat] = (l_exact > 0.f) ? (m_ref + log2f(l_exact)) * kLn2 : -INFINITY;
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE + q));
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
     }
 }
 
@@ -737,7 +643,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem;
-    uint8_t *sKV = smem + C::NQ * C::Q_BYTES;
+    uint8_t *sKV = smem + C::Q_BYTES;
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -747,20 +653,19 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     const uint32_t lane = ptx::lane_id();
 
     if (threadIdx.x == 0) {
-        for (int q = 0; q < C::NQ; ++q) {
-            ptx::mbar_init(bar_addr(bars, C::B_QFULL + q), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + q), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_OFULL + q), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_OFREE + q), 128);
+        ptx::mbar_init(bar_addr(bars, C::B_QFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_QEMPTY), 1);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_STFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_STEMPTY + s), 1);
         }
-        for (int s = 0; s < C::SLOTS; ++s) {
-            ptx::mbar_init(bar_addr(bars, C::B_KVFULL + s), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_KVEMPTY + s), 1);
-        }
-        for (int b = 0; b < 2 * C::NQ; ++b) {
+        for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
             ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), 128);
         }
+        ptx::mbar_init(bar_addr(bars, C::B_OFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_OFREE), 128);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -780,8 +685,8 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp < 4 * C::NQ) {
-        softmax_role<D, kFP16>(p, warp >> 2, bars, tmem, abort_flag);
+    if (warp < 4) {
+        softmax_role<D, kFP16>(p, bars, tmem, abort_flag);
     } else if (warp == C::MMA_WARP) {
         if (lane == 0) mma_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else {
