@@ -19,11 +19,13 @@
 //   * one TMA warp streams the Q tile and a ring of stages into shared
 //     memory (128-byte swizzle, 64 columns per box); stage k of a unit holds
 //     key tile k and value tile k-1, the two tiles one MMA iteration uses;
-//   * one MMA warp (a single issuing lane) runs S = Q K^T (both operands in
-//     shared memory) and O += P V (P read from tensor memory) as tcgen05
-//     MMAs with fp32 accumulators in tensor memory.  S has two buffers: the
-//     S MMA of key tile j+1 is issued before P V of tile j, so it runs while
-//     the softmax works on tile j;
+//   * two MMA warps (one issuing lane each) run the tcgen05 MMAs with fp32
+//     accumulators in tensor memory: one issues S = Q K^T (both operands in
+//     shared memory) into two S buffers, each as soon as the softmax has
+//     read the buffer's previous tile, so S of tile j+2 is computed while
+//     the softmax works on tile j+1; the other issues O += P V (P read from
+//     its own tensor-memory area) as soon as the softmax has written P, plus
+//     l += P 1, the row sums of exactly the 16-bit P used;
 //   * one softmax warpgroup owns the 128 rows, one row per thread (= one
 //     TMEM lane): it reads a row of S, masks boundary tiles, exponentiates,
 //     writes P (16-bit) back over S, rescales O in tensor memory when the max
@@ -77,23 +79,26 @@ struct Cfg {
     // in tensor memory and two stages fit in shared memory.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
     static constexpr int STAGES = (D == 64) ? 6 : (D == 128) ? 3 : 2;
-    // Warps 0-3: softmax warpgroup; warp 4: MMA issue; warp 5: TMA.
-    static constexpr int NUM_WARPS = 6;
+    // Warps 0-3: softmax warpgroup; warp 4: S MMAs; warp 5: P V MMAs; warp 6: TMA.
+    static constexpr int NUM_WARPS = 7;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
-    static constexpr int MMA_WARP = 4;
-    static constexpr int TMA_WARP = 5;
+    static constexpr int S_WARP = 4;
+    static constexpr int PV_WARP = 5;
+    static constexpr int TMA_WARP = 6;
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K part at 0, V part at TILE_BYTES
-    // Tensor memory: S/P buffers at columns 0 and BN, O from O_COL0, then
-    // 16 columns L_COL0.. that accumulate P times a column of ones: the row
-    // sums of the rounded 16-bit P the P V product actually used.
+    // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, then 16
+    // columns L_COL0.. that accumulate P times a column of ones (the row sums
+    // of the rounded 16-bit P the P V product actually used), and the P area
+    // (BN/2 columns, two 16-bit values per column) at P_COL0.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t O_COL0 = (D == 256) ? 128 : 256;
     static constexpr uint32_t L_COL0 = O_COL0 + D;
+    static constexpr uint32_t P_COL0 = 448;
     static constexpr int ONES_BYTES = 8 * 128;          // one 8-row swizzle atom of 16-bit ones
     // Barrier indices.
     static constexpr int B_QFULL = 0;
@@ -101,15 +106,16 @@ struct Cfg {
     static constexpr int B_STFULL = 2;                  // [STAGES]
     static constexpr int B_STEMPTY = B_STFULL + STAGES; // [STAGES]
     static constexpr int B_SFULL = B_STEMPTY + STAGES;  // [2]: S buffer b computed
-    static constexpr int B_PFULL = B_SFULL + 2;         // [2]: P buffer b written
-    static constexpr int B_OFULL = B_PFULL + 2;         // one phase per P V
+    static constexpr int B_SFREE = B_SFULL + 2;         // [2]: S buffer b read by the softmax
+    static constexpr int B_PFULL = B_SFREE + 2;         // P area written
+    static constexpr int B_OFULL = B_PFULL + 1;         // one phase per P V
     static constexpr int B_OFINAL = B_OFULL + 1;        // one phase per unit: last P V done
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
-    static constexpr int B_DRAIN = B_OFREE + 1;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
+    static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES + ONES_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
-    static_assert(L_COL0 + 16 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(L_COL0 + 16 <= P_COL0 && P_COL0 + BN / 2 <= TMEM_COLS, "tensor memory overflow");
     static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
@@ -290,48 +296,20 @@ __device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
 
 // ---------------------------------------------------------------- MMA role
 
+// S issuer: S_b = Q K^T for every key tile, into buffer b = t & 1 as soon as
+// the softmax has read that buffer's previous tile.
 template <int D, bool kFP16>
-__device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
-                         uint32_t tmem, volatile int *abort_flag) {
+__device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
+                           uint32_t tmem, volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
-    constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
-    constexpr uint32_t kIdescL = make_idesc(kBM, 16, kFP16, true);
-    const uint32_t q_addr = ptx::smem_addr(sQ);
-    // All-ones operand: one 8-row atom read for both 8-key groups of every
-    // 16-key step (group stride 0).
-    const uint64_t d_ones =
-        smem_desc(ptx::smem_addr(sQ + C::Q_BYTES + C::STAGES * C::STAGE_BYTES), 1024, 0);
-    const uint32_t l_tmem = tmem + C::L_COL0;
+    const uint64_t dq = smem_desc(ptx::smem_addr(sQ), 16);
     const uint32_t kv_addr = ptx::smem_addr(sKV);
-    const uint64_t dq = smem_desc(q_addr, 16);
-    const uint32_t o_tmem = tmem + C::O_COL0;
-
-    uint32_t st_it = 0;      // stages consumed so far
-    uint32_t t_cnt = 0;      // key tiles processed (S/P buffer = t & 1)
-    uint32_t q_cnt = 0;      // Q tiles consumed
-    uint32_t ofree_cnt = 0;  // epilogues waited for
-    bool o_used = false;
+    uint32_t st_it = 0;  // stages seen so far
+    uint32_t t_cnt = 0;  // key tiles issued (S buffer = t & 1)
+    uint32_t q_cnt = 0;  // Q tiles consumed
     bool ok = true;
-
-    // S_b = Q K^T with K at the start of stage `slot`.
-    auto issue_s = [&](uint32_t slot, uint32_t b) {
-        const uint64_t dk = smem_desc(kv_addr + slot * C::STAGE_BYTES, 16);
-        const uint32_t d_tmem = tmem + b * BN;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
-            const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
-            const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
-            ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
-    };
-    auto wait_stage = [&](uint32_t idx) -> bool {
-        return wait_bar(bar_addr(bars, C::B_STFULL + idx % C::STAGES), (idx / C::STAGES) & 1,
-                        abort_flag, 3);
-    };
 
     for (int k = 0; ok; ++k) {
         const int u = unit_at(k);
@@ -340,30 +318,86 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
         const uint32_t base = st_it;
-
         if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, abort_flag, 6)) { ok = false; break; }
-        // Stage 0 holds the first key tile only.
-        if (!wait_stage(base)) { ok = false; break; }
-        issue_s(base % C::STAGES, t_cnt & 1u);
-        if (n == 1) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
-        ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
-
         for (int i = 0; i < n; ++i) {
             const uint32_t t = t_cnt + (uint32_t)i;
-            const uint32_t sidx = base + 1u + (uint32_t)i;  // stage: key tile i+1, value tile i
+            const uint32_t sidx = base + (uint32_t)i;  // stage i holds key tile i
             const uint32_t slot = sidx % C::STAGES;
-            if (!wait_stage(sidx)) { ok = false; break; }
-            if (i + 1 < n) {
-                // S of the next key tile, into the other buffer (whose P V was
-                // issued last iteration), ahead of this tile's P V.
-                issue_s(slot, (t + 1u) & 1u);
-                if (i + 2 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
-            }
             const uint32_t b = t & 1u;
-            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)b), (t >> 1) & 1u, abort_flag, 4)) {
+            if (!wait_bar(bar_addr(bars, C::B_STFULL + slot), (sidx / C::STAGES) & 1, abort_flag, 3)) {
                 ok = false;
                 break;
             }
+            if (t >= 2 &&  // the softmax has read tile t-2 out of this buffer
+                !wait_bar(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1u) & 1u, abort_flag, 12)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint64_t dk = smem_desc(kv_addr + slot * C::STAGE_BYTES, 16);
+            const uint32_t d_tmem = tmem + b * BN;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
+                const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
+                const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+                ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
+            if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
+            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));           // this issuer's half
+        }
+        if (!ok) break;
+        // The last stage holds only a value tile: release this issuer's half.
+        ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + (base + (uint32_t)n) % C::STAGES));
+        st_it = base + (uint32_t)n + 1u;
+        t_cnt += (uint32_t)n;
+        ++q_cnt;
+    }
+    ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+// P V issuer: O (+)= P V and l (+)= P 1 for every key tile, as soon as the
+// softmax has written P.
+template <int D, bool kFP16>
+__device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
+                            uint32_t tmem, volatile int *abort_flag) {
+    using C = Cfg<D>;
+    constexpr int BN = C::BN;
+    constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
+    constexpr uint32_t kIdescL = make_idesc(kBM, 16, kFP16, true);
+    const uint32_t kv_addr = ptx::smem_addr(sKV);
+    // All-ones operand: one 8-row atom read for both 8-key groups of every
+    // 16-key step (group stride 0).
+    const uint64_t d_ones = smem_desc(ptx::smem_addr(sQ + C::Q_BYTES + C::STAGES * C::STAGE_BYTES), 1024, 0);
+    const uint32_t o_tmem = tmem + C::O_COL0;
+    const uint32_t l_tmem = tmem + C::L_COL0;
+    const uint32_t p_tmem = tmem + C::P_COL0;
+    uint32_t st_it = 0;      // stages seen so far
+    uint32_t t_cnt = 0;      // key tiles processed (one P V each)
+    uint32_t ofree_cnt = 0;  // epilogues waited for
+    bool o_used = false;
+    bool ok = true;
+
+    for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= p.n_units) break;
+        const Unit un = decode_unit<D>(u, p);
+        if (!un.valid) continue;
+        const int n = un.hi - un.lo;
+        const uint32_t base = st_it;
+        // The first stage holds only a key tile: release this issuer's half.
+        ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
+        for (int i = 0; i < n; ++i) {
+            const uint32_t t = t_cnt + (uint32_t)i;
+            const uint32_t sidx = base + 1u + (uint32_t)i;  // stage i+1 holds value tile i
+            const uint32_t slot = sidx % C::STAGES;
+            if (!wait_bar(bar_addr(bars, C::B_STFULL + slot), (sidx / C::STAGES) & 1, abort_flag, 3)) {
+                ok = false;
+                break;
+            }
+            if (!wait_bar(bar_addr(bars, C::B_PFULL), t & 1u, abort_flag, 4)) { ok = false; break; }
             ptx::tc_fence_after();
             if (i == 0 && o_used) {
                 if (!wait_bar(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, abort_flag, 5)) {
@@ -373,9 +407,7 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
                 ++ofree_cnt;
                 ptx::tc_fence_after();
             }
-            // O (+)= P V
             const uint64_t dv = smem_desc(kv_addr + slot * C::STAGE_BYTES + C::TILE_BYTES, C::KV_CHUNK);
-            const uint32_t p_tmem = tmem + b * BN;
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
                 // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
@@ -388,17 +420,15 @@ __device__ void mma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
                 ptx::mma_ts(l_tmem, p_tmem + kk * 8, d_ones, kIdescL, (i > 0 || kk > 0) ? 1u : 0u);
             ptx::mma_commit(bar_addr(bars, C::B_OFULL));
             if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
-            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));
+            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));  // this issuer's half
         }
         if (!ok) break;
         st_it = base + (uint32_t)n + 1u;
         t_cnt += (uint32_t)n;
-        ++q_cnt;
         o_used = true;
     }
-    // Every MMA issued must finish before tensor memory is released.
-    ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
-    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+    ptx::mma_commit(bar_addr(bars, C::B_DRAIN + 1));
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
 }
 
 // ---------------------------------------------------------------- softmax role
@@ -491,6 +521,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
     const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
     const uint32_t o_tmem = tmem + lane_off + C::O_COL0;
     const uint32_t l_tmem = tmem + lane_off + C::L_COL0;
+    const uint32_t p_area = tmem + lane_off + C::P_COL0;
     const float c = p.scale_log2;
     uint32_t t_cnt = 0;  // key tiles processed (S/P buffer = t & 1; one P V each)
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
@@ -535,6 +566,9 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
             load_s_row<BN>(s_tmem, sr);
             ptx::tmem_wait_ld();
             ptx::reg_fence<BN>(sr);
+            // The S buffer may now be overwritten with tile t+2.
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(bars, C::B_SFREE + b));
 
             const bool masked = tile_needs_mask<D>(un.i0, j, p);
             if (masked) apply_mask<BN>(sr, key_lo - j * BN, key_hi - j * BN);
@@ -580,13 +614,16 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
                         tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, le_t);
                 }
             }
+            // P V of the previous key tile must be finished before O is rescaled
+            // or the P area rewritten: wait for phase t-1 of the O barrier (one
+            // phase per P V, numbered like t).  Phase t-2 was waited for on the
+            // previous tile (or, on a unit's first tile, covered by the
+            // previous unit's final barrier) and P V of tile t cannot exist
+            // before this tile's P, so the barrier is at phase t-1 or t and the
+            // parity wait is unambiguous.
+            const bool need_pv = (j > un.lo);
             if (__any_sync(0xffffffffu, rescale)) {
-                // O may be touched only once the previous P V has finished: wait
-                // for phase t-1 of the O barrier (one phase per P V, numbered like
-                // t).  S of this tile was issued after P V of tile t-2 and P V of
-                // tile t cannot exist before this tile's P, so the barrier is at
-                // phase t-1 or t and the parity wait is unambiguous.
-                if (!wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8)) {
+                if (need_pv && !wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8)) {
                     ok = false;
                     break;
                 }
@@ -610,10 +647,15 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
                 ptx::tmem_st_x16<0>(l_tmem, lv);
             }
             l_exact = alpha * l_exact + le_t;
-            store_p_row<BN>(s_tmem, pk);
+            if (need_pv && !wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 10)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            store_p_row<BN>(p_area, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + b));
+            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
         }
         if (!ok) break;
 
@@ -675,21 +717,23 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_QEMPTY), 1);
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar_addr(bars, C::B_STFULL + s), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_STEMPTY + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_STEMPTY + s), 2);  // one arrival per issuer
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), 128);
+            ptx::mbar_init(bar_addr(bars, C::B_SFREE + b), 128);
         }
+        ptx::mbar_init(bar_addr(bars, C::B_PFULL), 128);
         ptx::mbar_init(bar_addr(bars, C::B_OFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFREE), 128);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
-    if (warp == C::MMA_WARP) {
+    if (warp == C::S_WARP) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::TMEM_COLS);
         ptx::tmem_relinquish();
     }
@@ -712,15 +756,17 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
 
     if (warp < 4) {
         softmax_role<D, kFP16>(p, bars, tmem, abort_flag);
-    } else if (warp == C::MMA_WARP) {
-        if (lane == 0) mma_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+    } else if (warp == C::S_WARP) {
+        if (lane == 0) mma_s_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+    } else if (warp == C::PV_WARP) {
+        if (lane == 0) mma_pv_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else {
         if (lane == 0) tma_role<D>(p, sQ, sKV, bars, abort_flag);
     }
     __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == C::MMA_WARP) {
+    if (warp == C::S_WARP) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TMEM_COLS);
     }
