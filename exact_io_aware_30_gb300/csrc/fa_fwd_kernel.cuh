@@ -24,8 +24,7 @@
 //     shared memory) into two S buffers, each as soon as the softmax has
 //     read the buffer's previous tile, so S of tile j+2 is computed while
 //     the softmax works on tile j+1; the other issues O += P V (P read from
-//     its own tensor-memory area) as soon as the softmax has written P, plus
-//     l += P 1, the row sums of exactly the 16-bit P used;
+//     its own tensor-memory area) as soon as the softmax has written P;
 //   * one softmax warpgroup owns the 128 rows, one row per thread (= one
 //     TMEM lane): it reads a row of S, masks boundary tiles, exponentiates,
 //     writes P (16-bit) back over S, rescales O in tensor memory when the max
@@ -91,15 +90,11 @@ struct Cfg {
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K part at 0, V part at TILE_BYTES
-    // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, then 16
-    // columns L_COL0.. that accumulate P times a column of ones (the row sums
-    // of the rounded 16-bit P the P V product actually used), and the P area
-    // (BN/2 columns, two 16-bit values per column) at P_COL0.
+    // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, and the P
+    // area (BN/2 columns, two 16-bit values per column) at P_COL0.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t O_COL0 = (D == 256) ? 128 : 256;
-    static constexpr uint32_t L_COL0 = O_COL0 + D;
     static constexpr uint32_t P_COL0 = 448;
-    static constexpr int ONES_BYTES = 8 * 128;          // one 8-row swizzle atom of 16-bit ones
     // Barrier indices.
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = 1;
@@ -113,9 +108,9 @@ struct Cfg {
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
     static constexpr int NUM_BARS = B_DRAIN + 2;
-    static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES + ONES_BYTES;
+    static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
-    static_assert(L_COL0 + 16 <= P_COL0 && P_COL0 + BN / 2 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(O_COL0 + D <= P_COL0 && P_COL0 + BN / 2 <= TMEM_COLS, "tensor memory overflow");
     static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
@@ -348,8 +343,18 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
             ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));           // this issuer's half
         }
         if (!ok) break;
-        // The last stage holds only a value tile: release this issuer's half.
-        ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + (base + (uint32_t)n) % C::STAGES));
+        // The last stage holds only a value tile: release this issuer's half,
+        // but only once it has been filled, so that the arrival cannot count
+        // towards the slot's previous fill while the other issuer still reads it.
+        {
+            const uint32_t sidx = base + (uint32_t)n;
+            if (!wait_bar(bar_addr(bars, C::B_STFULL + sidx % C::STAGES), (sidx / C::STAGES) & 1,
+                          abort_flag, 3)) {
+                ok = false;
+                break;
+            }
+            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + sidx % C::STAGES));
+        }
         st_it = base + (uint32_t)n + 1u;
         t_cnt += (uint32_t)n;
         ++q_cnt;
@@ -358,21 +363,16 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
     wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
 }
 
-// P V issuer: O (+)= P V and l (+)= P 1 for every key tile, as soon as the
-// softmax has written P.
+// P V issuer: O (+)= P V for every key tile, as soon as the softmax has
+// written P.
 template <int D, bool kFP16>
 __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
                             uint32_t tmem, volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
-    constexpr uint32_t kIdescL = make_idesc(kBM, 16, kFP16, true);
     const uint32_t kv_addr = ptx::smem_addr(sKV);
-    // All-ones operand: one 8-row atom read for both 8-key groups of every
-    // 16-key step (group stride 0).
-    const uint64_t d_ones = smem_desc(ptx::smem_addr(sQ + C::Q_BYTES + C::STAGES * C::STAGE_BYTES), 1024, 0);
     const uint32_t o_tmem = tmem + C::O_COL0;
-    const uint32_t l_tmem = tmem + C::L_COL0;
     const uint32_t p_tmem = tmem + C::P_COL0;
     uint32_t st_it = 0;      // stages seen so far
     uint32_t t_cnt = 0;      // key tiles processed (one P V each)
@@ -387,7 +387,13 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
         const uint32_t base = st_it;
-        // The first stage holds only a key tile: release this issuer's half.
+        // The first stage holds only a key tile: release this issuer's half once
+        // it has been filled (see the S issuer).
+        if (!wait_bar(bar_addr(bars, C::B_STFULL + base % C::STAGES), (base / C::STAGES) & 1,
+                      abort_flag, 3)) {
+            ok = false;
+            break;
+        }
         ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
         for (int i = 0; i < n; ++i) {
             const uint32_t t = t_cnt + (uint32_t)i;
@@ -414,10 +420,6 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
                 ptx::mma_ts(o_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4), kIdescO,
                             (i > 0 || kk > 0) ? 1u : 0u);
             }
-            // l (+)= P 1: row sums of exactly the 16-bit P just used.
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                ptx::mma_ts(l_tmem, p_tmem + kk * 8, d_ones, kIdescL, (i > 0 || kk > 0) ? 1u : 0u);
             ptx::mma_commit(bar_addr(bars, C::B_OFULL));
             if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
             ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));  // this issuer's half
@@ -482,13 +484,18 @@ __device__ __forceinline__ float tile_row_max(const uint32_t (&sr)[BN]) {
 }
 
 // p = 2^(s*c - m) for one row of a tile, packed to 16 bits into pk; adds the
-// exact fp32 sum of p to l_exact.  (The divisor of O, the sum of the rounded
-// 16-bit p, is accumulated by the tensor core as P times a column of ones.)
+// exact fp32 sum of p to l_exact (for the logsumexp) and, for bf16, the sum of
+// the rounded 16-bit p to l_round: the divisor of O, so that the weights the
+// P V product uses sum exactly to what O is divided by.  bf16 keeps only 8
+// significant bits, enough for a dominant weight's rounding to show in O;
+// fp16's 11 bits make that negligible, so fp16 divides by the exact sum.
 template <int BN, bool kFP16, bool kMasked>
 __device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, float neg,
-                                             uint32_t (&pk)[BN / 2], float &l_exact) {
+                                             uint32_t (&pk)[BN / 2], float &l_exact,
+                                             float &l_round) {
     const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(neg, neg);
     uint64_t le0 = ptx::f32x2(0.f, 0.f), le1 = le0;
+    float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
 #pragma unroll
     for (int i = 0; i < BN; i += 2) {
         const float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
@@ -506,10 +513,18 @@ __device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, 
             le1 = ptx::add_f32x2(le1, ptx::f32x2(e0, e1));
         else
             le0 = ptx::add_f32x2(le0, ptx::f32x2(e0, e1));
+        if constexpr (!kFP16) {
+            float &acc = ((i >> 1) & 3) == 0 ? lr0 : ((i >> 1) & 3) == 1 ? lr1 : ((i >> 1) & 3) == 2 ? lr2 : lr3;
+            acc = ptx::add_bf16x2_to_f32(pw, acc);
+        }
     }
     float a0, a1;
     ptx::unpack_f32x2(ptx::add_f32x2(le0, le1), a0, a1);
     l_exact += a0 + a1;
+    if constexpr (kFP16)
+        l_round += a0 + a1;
+    else
+        l_round += (lr0 + lr1) + (lr2 + lr3);
 }
 
 template <int D, bool kFP16>
@@ -520,7 +535,6 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
     const int r = (int)threadIdx.x;                           // query row within the tile
     const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
     const uint32_t o_tmem = tmem + lane_off + C::O_COL0;
-    const uint32_t l_tmem = tmem + lane_off + C::L_COL0;
     const uint32_t p_area = tmem + lane_off + C::P_COL0;
     const float c = p.scale_log2;
     uint32_t t_cnt = 0;  // key tiles processed (S/P buffer = t & 1; one P V each)
@@ -550,6 +564,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
         const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
 
         float m_ref = -INFINITY;  // max the accumulator and sums are referenced to (log2 units)
+        float l = 0.f;            // the divisor of O (see tile_row_exp)
         float l_exact = 0.f;      // fp32 sum of P (for the logsumexp)
 
         for (int j = un.lo; j < un.hi; ++j) {
@@ -580,13 +595,13 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
             // otherwise (and on a row's first tile, when there is no reference
             // yet) the tile takes the slow path below.
             uint32_t pk[BN / 2];
-            float le_t = 0.f;  // this tile's exact fp32 sum
+            float le_t = 0.f, lr_t = 0.f;  // this tile's exact and rounded sums
             bool slow = (j == un.lo) || (m_ref == -INFINITY);
             if (!slow) {
                 if (masked)
-                    tile_row_exp<BN, kFP16, true>(sr, c, -m_ref, pk, le_t);
+                    tile_row_exp<BN, kFP16, true>(sr, c, -m_ref, pk, le_t, lr_t);
                 else
-                    tile_row_exp<BN, kFP16, false>(sr, c, -m_ref, pk, le_t);
+                    tile_row_exp<BN, kFP16, false>(sr, c, -m_ref, pk, le_t, lr_t);
                 slow = !(le_t <= kRescaleBound);  // also catches inf
             }
             float alpha = 1.f;
@@ -608,10 +623,11 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
                 if (redo) {
                     const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
                     le_t = 0.f;
+                    lr_t = 0.f;
                     if (masked)
-                        tile_row_exp<BN, kFP16, true>(sr, c, neg, pk, le_t);
+                        tile_row_exp<BN, kFP16, true>(sr, c, neg, pk, le_t, lr_t);
                     else
-                        tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, le_t);
+                        tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, le_t, lr_t);
                 }
             }
             // P V of the previous key tile must be finished before O is rescaled
@@ -638,14 +654,8 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
                     for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
                     ptx::tmem_st_x32<0>(o_tmem + cc * 32, ov);
                 }
-                uint32_t lv[16];
-                ptx::tmem_ld_x16<0>(l_tmem, lv);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence<16>(lv);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) lv[i] = __float_as_uint(__uint_as_float(lv[i]) * alpha);
-                ptx::tmem_st_x16<0>(l_tmem, lv);
             }
+            l = alpha * l + lr_t;
             l_exact = alpha * l_exact + le_t;
             if (need_pv && !wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 10)) {
                 ok = false;
@@ -663,11 +673,6 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
         if (!wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9)) { ok = false; break; }
         ++u_cnt;
         ptx::tc_fence_after();
-        uint32_t lv[16];
-        ptx::tmem_ld_x16<0>(l_tmem, lv);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<16>(lv);
-        const float l = __uint_as_float(lv[0]);  // sum of the rounded P multiplied into O
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -736,13 +741,6 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     if (warp == C::S_WARP) {
         ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::TMEM_COLS);
         ptx::tmem_relinquish();
-    }
-    if (warp < 4) {
-        // The all-ones operand of the row-sum MMA: 16-bit 1.0 everywhere.
-        uint32_t *ones = reinterpret_cast<uint32_t *>(sQ + C::Q_BYTES + C::STAGES * C::STAGE_BYTES);
-        const uint32_t one2 = kFP16 ? 0x3C003C00u : 0x3F803F80u;
-        for (int i = threadIdx.x; i < C::ONES_BYTES / 4; i += 128) ones[i] = one2;
-        ptx::fence_proxy_async_smem();
     }
     if (warp == C::TMA_WARP && lane == 0) {
         ptx::prefetch_tensormap(&p.tm_q);
