@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cfloat>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -183,7 +184,14 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     p.Sk = Sk;
     p.mask_kind = mask_kind;
     p.window = (mask_kind == FA_MASK_SLIDING_WINDOW) ? window : 0;
-    p.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    // The kernel needs a positive exponent scale: a hidden key is a score of
+    // -inf, whose weight 2^(-inf * c - m) is 0 only for c > 0.  scale == 0
+    // (and any scale whose product underflows) runs with c = 2^-126: for every
+    // score below 2^100 in magnitude, s * c - m then lies within 2^-25 of 0,
+    // so each visible weight is 1 to fp32 precision -- the uniform weights
+    // of a zero scale.
+    p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
+    p.o_vec8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     p.n_qtiles = (Sq + 127) / 128;
     p.n_units = B * H * p.n_qtiles;
 
@@ -260,7 +268,7 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     }
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
-                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=2 "
+                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=2 softmax_wgs=2 "
                   "kv_stages=%d threads=%d smem=%d mask=%s persistent",
                   d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::stages_for(d),
                   fa::Cfg<128>::NUM_THREADS,

@@ -67,9 +67,10 @@ struct Params {
     float *lse;        // [B, H, Sq] fp32
     int B, H, Sq, Sk;
     int mask_kind, window;
-    float scale_log2;  // scale * log2(e)
+    float scale_log2;  // scale * log2(e), kept positive (see the API)
     int n_qtiles;      // ceil(Sq / 128): units per (batch, head)
     int n_units;       // B * H * n_qtiles
+    int o_vec8;        // O is 32-byte aligned: 32-byte stores
 };
 
 template <int D>
@@ -77,13 +78,17 @@ struct Cfg {
     // d = 256 uses 64-key tiles so that two S buffers and its 256-column O fit
     // in tensor memory and two stages fit in shared memory.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
+    static constexpr int HALF = BN / 2;                  // key columns per softmax warpgroup
     static constexpr int STAGES = (D == 64) ? 6 : (D == 128) ? 3 : 2;
-    // Warps 0-3: softmax warpgroup; warp 4: S MMAs; warp 5: P V MMAs; warp 6: TMA.
-    static constexpr int NUM_WARPS = 7;
+    // Warps 0-7: two softmax warpgroups (warpgroup h owns key columns
+    // [h*HALF, (h+1)*HALF) of every tile, all 128 rows); warp 8: S MMAs;
+    // warp 9: P V MMAs; warp 10: TMA.
+    static constexpr int NUM_SOFTMAX = 256;
+    static constexpr int NUM_WARPS = 11;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
-    static constexpr int S_WARP = 4;
-    static constexpr int PV_WARP = 5;
-    static constexpr int TMA_WARP = 6;
+    static constexpr int S_WARP = 8;
+    static constexpr int PV_WARP = 9;
+    static constexpr int TMA_WARP = 10;
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
@@ -109,7 +114,8 @@ struct Cfg {
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
     static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES;
-    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16;
+    static constexpr int XCH_BYTES = 2 * kBM * 4;  // one fp32 per row and warpgroup
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 + XCH_BYTES;
     static_assert(O_COL0 + D <= P_COL0 && P_COL0 + BN / 2 <= TMEM_COLS, "tensor memory overflow");
     static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
@@ -203,18 +209,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
     un.lo = un.valid ? key_beg / BN : 0;
     un.hi = un.valid ? (key_end + BN - 1) / BN : 0;
     return un;
-}
-
-// True if some (row, key) pair of this query tile x key tile is hidden.
-template <int D>
-__device__ __forceinline__ bool tile_needs_mask(int i0, int j, const Params &p) {
-    constexpr int BN = Cfg<D>::BN;
-    const int k0 = j * BN;
-    if (k0 + BN > p.Sk) return true;
-    if (p.mask_kind == kMaskNone) return false;
-    if (k0 + BN - 1 > i0) return true;
-    if (p.mask_kind == kMaskWindow && k0 <= i0 + kBM - 1 - p.window) return true;
-    return false;
 }
 
 // ---------------------------------------------------------------- TMA role
@@ -435,22 +429,22 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
 
 // ---------------------------------------------------------------- softmax role
 
-// One thread's row of an S tile (BN fp32 columns) from tensor memory.
-template <int BN>
-__device__ __forceinline__ void load_s_row(uint32_t taddr, uint32_t (&r)[BN]) {
+constexpr uint32_t kSoftmaxBar = 1;  // named barrier of the two softmax warpgroups
+
+// Loads this thread's N score columns (N = 32 or 64) from tensor memory.
+template <int N>
+__device__ __forceinline__ void load_s_cols(uint32_t taddr, uint32_t (&r)[N]) {
     ptx::tmem_ld_x32<0>(taddr, r);
-    ptx::tmem_ld_x32<32>(taddr + 32, r);
-    if constexpr (BN == 128) {
-        ptx::tmem_ld_x32<64>(taddr + 64, r);
-        ptx::tmem_ld_x32<96>(taddr + 96, r);
-    }
+    if constexpr (N == 64) ptx::tmem_ld_x32<32>(taddr + 32, r);
 }
 
-// One thread's row of P (BN 16-bit values packed in BN/2 columns) to tensor memory.
-template <int BN>
-__device__ __forceinline__ void store_p_row(uint32_t taddr, const uint32_t (&r)[BN / 2]) {
-    ptx::tmem_st_x32<0>(taddr, r);
-    if constexpr (BN == 128) ptx::tmem_st_x32<32>(taddr + 32, r);
+// Stores N/2 packed words of P (N 16-bit values) to tensor memory.
+template <int N>
+__device__ __forceinline__ void store_p_cols(uint32_t taddr, const uint32_t (&r)[N / 2]) {
+    if constexpr (N == 64)
+        ptx::tmem_st_x32<0>(taddr, r);
+    else
+        ptx::tmem_st_x16<0>(taddr, r);
 }
 
 template <bool kFP16>
@@ -458,55 +452,57 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
 }
 
-// Hidden keys of a boundary tile (columns outside [c_lo, c_hi]) become -inf.
-template <int BN>
-__device__ __forceinline__ void apply_mask(uint32_t (&sr)[BN], int c_lo, int c_hi) {
+// Hidden keys (columns outside [c_lo, c_hi]) become -inf, whose weight
+// 2^(-inf * c - m) is exactly 0 for the positive exponent scale c.
+template <int N>
+__device__ __forceinline__ void apply_mask(uint32_t (&sr)[N], int c_lo, int c_hi) {
 #pragma unroll
-    for (int i = 0; i < BN; ++i)
+    for (int i = 0; i < N; ++i)
         if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
 }
 
-// Row max of one S tile (raw scores; scale >= 0 preserves the order).
-template <int BN>
-__device__ __forceinline__ float tile_row_max(const uint32_t (&sr)[BN]) {
-    float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-    float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
-#pragma unroll
-    for (int i = 4; i < BN; i += 8) {
-        mx0 = ptx::max3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-        mx1 = ptx::max3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-        if (i + 4 < BN) {
-            mx2 = ptx::max3(mx2, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-            mx3 = ptx::max3(mx3, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
-        }
-    }
-    return fmaxf(ptx::max3(mx0, mx1, mx2), mx3);
+// True if some (row, key) pair of this query tile x N keys from kc is hidden.
+template <int N>
+__device__ __forceinline__ bool cols_need_mask(int i0, int kc, const Params &p) {
+    if (kc + N > p.Sk) return true;
+    if (p.mask_kind == kMaskNone) return false;
+    if (kc + N - 1 > i0) return true;
+    if (p.mask_kind == kMaskWindow && kc <= i0 + kBM - 1 - p.window) return true;
+    return false;
 }
 
-// p = 2^(s*c - m) for one row of a tile, packed to 16 bits into pk; adds the
-// exact fp32 sum of p to l_exact (for the logsumexp) and, for bf16, the sum of
-// the rounded 16-bit p to l_round: the divisor of O, so that the weights the
-// P V product uses sum exactly to what O is divided by.  bf16 keeps only 8
+// Max of N raw scores (the exponent scale is positive, so it keeps the order).
+template <int N>
+__device__ __forceinline__ float row_max(const uint32_t (&sr)[N]) {
+    float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+#pragma unroll
+    for (int i = 2; i < N; i += 4) {
+        mx0 = ptx::max3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+        if (i + 3 < N) mx1 = ptx::max3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+    }
+    return fmaxf(mx0, mx1);
+}
+
+// p = 2^(s*c - m) for N scores, packed to 16 bits into pk; adds the exact
+// fp32 sum of p to l_exact (for the logsumexp) and, for bf16, the sum of the
+// rounded 16-bit p to l_round: the divisor of O, so that the weights the P V
+// product uses sum exactly to what O is divided by.  bf16 keeps only 8
 // significant bits, enough for a dominant weight's rounding to show in O;
 // fp16's 11 bits make that negligible, so fp16 divides by the exact sum.
-template <int BN, bool kFP16, bool kMasked>
-__device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, float neg,
-                                             uint32_t (&pk)[BN / 2], float &l_exact,
-                                             float &l_round) {
+template <int N, bool kFP16>
+__device__ __forceinline__ void row_exp(const uint32_t (&sr)[N], float c, float neg,
+                                        uint32_t (&pk)[N / 2], float &l_exact, float &l_round) {
     const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(neg, neg);
     uint64_t le0 = ptx::f32x2(0.f, 0.f), le1 = le0;
     float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
 #pragma unroll
-    for (int i = 0; i < BN; i += 2) {
-        const float x0 = __uint_as_float(sr[i]), x1 = __uint_as_float(sr[i + 1]);
+    for (int i = 0; i < N; i += 2) {
         float y0, y1;
-        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(x0, x1), c2, n2), y0, y1);
-        float e0 = ptx::ex2_approx(y0);
-        float e1 = ptx::ex2_approx(y1);
-        if constexpr (kMasked) {  // hidden keys weigh exactly 0 (also when scale == 0)
-            e0 = (x0 == -INFINITY) ? 0.f : e0;
-            e1 = (x1 == -INFINITY) ? 0.f : e1;
-        }
+        ptx::unpack_f32x2(
+            ptx::fma_f32x2(ptx::f32x2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), c2, n2),
+            y0, y1);
+        const float e0 = ptx::ex2_approx(y0);
+        const float e1 = ptx::ex2_approx(y1);
         const uint32_t pw = pack2<kFP16>(e0, e1);
         pk[i / 2] = pw;
         if ((i >> 1) & 1)
@@ -527,35 +523,54 @@ __device__ __forceinline__ void tile_row_exp(const uint32_t (&sr)[BN], float c, 
         l_round += (lr0 + lr1) + (lr2 + lr3);
 }
 
+// Hands v to the partner thread (same row, other warpgroup) and returns the
+// partner's value.  The caller guarantees that the partner has finished
+// reading the previous exchange (a softmax barrier lies in between).
+__device__ __forceinline__ float swap_with_partner(float *xch, int h, int r, float v) {
+    xch[h * kBM + r] = v;
+    ptx::named_bar_sync(kSoftmaxBar, 256);
+    return xch[(h ^ 1) * kBM + r];
+}
+
+// Two softmax warpgroups; thread (h, r) owns row r and key columns
+// [h*HALF, (h+1)*HALF) of every tile, and columns [h*D/2, (h+1)*D/2) of O.
+// Both partners of a row keep the same reference max m_ref: they exchange
+// their half-row maxima whenever the reference is set or moves.
+//
+// Every softmax thread runs the same sequence of named barriers (the
+// decisions that choose barriers are CTA-uniform), and a pipeline wait that
+// gives up does not leave the loop: the thread carries on through the
+// schedule with whatever tensor memory holds, so that no partner is left at
+// a barrier.  The device status word reports the failure.
 template <int D, bool kFP16>
-__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
+__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch,
                              volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
-    const int r = (int)threadIdx.x;                           // query row within the tile
+    constexpr int HALF = C::HALF;
+    const int h = (int)(threadIdx.x >> 7);                      // key-column half
+    const int r = (int)(threadIdx.x & 127);                     // query row within the tile
     const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
-    const uint32_t o_tmem = tmem + lane_off + C::O_COL0;
-    const uint32_t p_area = tmem + lane_off + C::P_COL0;
+    const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)(h * (D / 2));
+    const uint32_t p_area = tmem + lane_off + C::P_COL0 + (uint32_t)(h * (HALF / 2));
     const float c = p.scale_log2;
-    uint32_t t_cnt = 0;  // key tiles processed (S/P buffer = t & 1; one P V each)
+    uint32_t t_cnt = 0;  // key tiles processed (S buffer = t & 1; one P V each)
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
-    bool ok = true;
 
-    for (int k = 0; ok; ++k) {
+    for (int k = 0;; ++k) {
         const int u = unit_at(k);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
-        if (un.i0 >= p.Sq) continue;
         const int row = un.i0 + r;
         const bool row_ok = row < p.Sq;
         const size_t row_flat = ((size_t)(un.b * p.H + un.h)) * (size_t)p.Sq + (size_t)row;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
+        uint8_t *ohalf = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2 + (size_t)(h * D);
         if (!un.valid) {
             // No key visible to any row of this tile: guarded output.
             if (row_ok) {
 #pragma unroll
-                for (int cc = 0; cc < D / 8; ++cc) ptx::st_global_v4(orow + cc * 16, 0, 0, 0, 0);
-                p.lse[row_flat] = -INFINITY;
+                for (int cc = 0; cc < D / 16; ++cc) ptx::st_global_v4(ohalf + cc * 16, 0, 0, 0, 0);
+                if (h == 0) p.lse[row_flat] = -INFINITY;
             }
             continue;
         }
@@ -564,71 +579,61 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
         const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
 
         float m_ref = -INFINITY;  // max the accumulator and sums are referenced to (log2 units)
-        float l = 0.f;            // the divisor of O (see tile_row_exp)
-        float l_exact = 0.f;      // fp32 sum of P (for the logsumexp)
+        float l = 0.f;            // this half's share of the divisor of O (see row_exp)
+        float l_exact = 0.f;      // this half's fp32 sum of P (for the logsumexp)
 
         for (int j = un.lo; j < un.hi; ++j) {
             const uint32_t t = t_cnt++;
             const int b = (int)(t & 1u);
-            if (!wait_bar(bar_addr(bars, C::B_SFULL + b), (t >> 1) & 1u, abort_flag, 7)) {
-                ok = false;
-                break;
-            }
+            wait_bar(bar_addr(bars, C::B_SFULL + b), (t >> 1) & 1u, abort_flag, 7);
             ptx::tc_fence_after();
-            const uint32_t s_tmem = tmem + lane_off + (uint32_t)(b * BN);
-
-            uint32_t sr[BN];
-            load_s_row<BN>(s_tmem, sr);
+            uint32_t sr[HALF];
+            load_s_cols<HALF>(tmem + lane_off + (uint32_t)(b * BN + h * HALF), sr);
             ptx::tmem_wait_ld();
-            ptx::reg_fence<BN>(sr);
+            ptx::reg_fence<HALF>(sr);
             // The S buffer may now be overwritten with tile t+2.
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_SFREE + b));
 
-            const bool masked = tile_needs_mask<D>(un.i0, j, p);
-            if (masked) apply_mask<BN>(sr, key_lo - j * BN, key_hi - j * BN);
+            const int kc = j * BN + h * HALF;  // first key of this thread's columns
+            if (cols_need_mask<HALF>(un.i0, kc, p)) apply_mask<HALF>(sr, key_lo - kc, key_hi - kc);
 
-            // Fast path: exponentiate against the current reference max without
-            // looking for this tile's max.  Weights above 2^8 (the max grew by
-            // more than the deferral bound) always push the tile's sum above
-            // 2^8, so a sum within the bound proves the reference still valid;
-            // otherwise (and on a row's first tile, when there is no reference
-            // yet) the tile takes the slow path below.
-            uint32_t pk[BN / 2];
-            float le_t = 0.f, lr_t = 0.f;  // this tile's exact and rounded sums
-            bool slow = (j == un.lo) || (m_ref == -INFINITY);
-            if (!slow) {
-                if (masked)
-                    tile_row_exp<BN, kFP16, true>(sr, c, -m_ref, pk, le_t, lr_t);
-                else
-                    tile_row_exp<BN, kFP16, false>(sr, c, -m_ref, pk, le_t, lr_t);
-                slow = !(le_t <= kRescaleBound);  // also catches inf
+            // A unit's first tile sets the reference from the row max.  Later
+            // tiles exponentiate against the current reference without looking
+            // for the max: a weight above 2^8 (the max grew by more than the
+            // deferral bound) pushes its half's sum above 2^8, so when no half
+            // of any row exceeds the bound every weight is valid as computed.
+            // Otherwise (a CTA-wide vote) the halves exchange their maxima and
+            // each row whose max grew by more than the bound moves its
+            // reference, rescales and exponentiates again.
+            const bool first = (j == un.lo);
+            if (first) {
+                const float hm = row_max<HALF>(sr);
+                ptx::named_bar_sync(kSoftmaxBar, 256);  // previous exchange fully read
+                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, hm));
+                m_ref = (mx == -INFINITY) ? -INFINITY : mx * c;
             }
+            uint32_t pk[HALF / 2];
+            float le_t, lr_t;  // this tile's exact and rounded sums (this half)
             float alpha = 1.f;
             bool rescale = false;
-            if (slow) {
-                const float mx = tile_row_max<BN>(sr);
-                const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c;
-                const float m_new = fmaxf(m_ref, m_tile);
-                bool redo = true;
-                if (j == un.lo) {
-                    m_ref = m_new;
-                } else if (m_new > m_ref + kRescaleLog2) {
-                    alpha = ptx::ex2_approx(m_ref - m_new);  // 0 while m_ref is -inf
-                    m_ref = m_new;
-                    rescale = true;
-                } else {
-                    redo = false;  // the fast-path weights are within the bound
-                }
-                if (redo) {
-                    const float neg = (m_ref == -INFINITY) ? 0.f : -m_ref;
-                    le_t = 0.f;
-                    lr_t = 0.f;
-                    if (masked)
-                        tile_row_exp<BN, kFP16, true>(sr, c, neg, pk, le_t, lr_t);
-                    else
-                        tile_row_exp<BN, kFP16, false>(sr, c, neg, pk, le_t, lr_t);
-                }
+#pragma unroll 1
+            for (int pass = 0;; ++pass) {
+                le_t = 0.f;
+                lr_t = 0.f;
+                row_exp<HALF, kFP16>(sr, c, (m_ref == -INFINITY) ? 0.f : -m_ref, pk, le_t, lr_t);
+                if (first || pass > 0) break;
+                // No reference yet (every earlier key of the row hidden) counts
+                // as exceeding the bound as soon as a key is visible.
+                const bool over = !(le_t <= kRescaleBound) || (m_ref == -INFINITY && le_t != 0.f);
+                if (!ptx::named_bar_any(kSoftmaxBar, 256, over)) break;
+                const float hm = row_max<HALF>(sr);
+                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, hm));
+                const float m_new = fmaxf(m_ref, (mx == -INFINITY) ? -INFINITY : mx * c);
+                if (!(m_new > m_ref + kRescaleLog2)) break;  // weights within the bound
+                alpha = ptx::ex2_approx(m_ref - m_new);      // 0 while m_ref is -inf
+                m_ref = m_new;
+                rescale = true;
             }
             // P V of the previous key tile must be finished before O is rescaled
             // or the P area rewritten: wait for phase t-1 of the O barrier (one
@@ -639,13 +644,10 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
             // parity wait is unambiguous.
             const bool need_pv = (j > un.lo);
             if (__any_sync(0xffffffffu, rescale)) {
-                if (need_pv && !wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8)) {
-                    ok = false;
-                    break;
-                }
+                if (need_pv) wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8);
                 ptx::tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t ov[32];
                     ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
                     ptx::tmem_wait_ld();
@@ -657,25 +659,29 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
             }
             l = alpha * l + lr_t;
             l_exact = alpha * l_exact + le_t;
-            if (need_pv && !wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 10)) {
-                ok = false;
-                break;
-            }
+            if (need_pv) wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 10);
             ptx::tc_fence_after();
-            store_p_row<BN>(p_area, pk);
+            store_p_cols<HALF>(p_area, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
         }
-        if (!ok) break;
 
-        // Epilogue: wait for the unit's last P V, divide by l once, store O and lse.
-        if (!wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9)) { ok = false; break; }
+        // Epilogue: wait for the unit's last P V, combine the halves' sums,
+        // divide by l once, store this half of the O row (and lse).
+        wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9);
         ++u_cnt;
         ptx::tc_fence_after();
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        ptx::named_bar_sync(kSoftmaxBar, 256);  // previous exchange fully read
+        const float l_all = l + swap_with_partner(xch, h, r, l);
+        float le_all = l_all;
+        if constexpr (!kFP16) {
+            ptx::named_bar_sync(kSoftmaxBar, 256);
+            le_all = l_exact + swap_with_partner(xch, h, r, l_exact);
+        }
+        const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = 0; cc < D / 64; ++cc) {
             uint32_t ov[32];
             ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
             ptx::tmem_wait_ld();
@@ -686,13 +692,20 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem,
                 w[i] = pack2<kFP16>(__uint_as_float(ov[2 * i]) * inv_l,
                                     __uint_as_float(ov[2 * i + 1]) * inv_l);
             if (row_ok) {
+                uint8_t *dst = ohalf + cc * 64;
+                if (p.o_vec8) {
+                    ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+                    ptx::st_global_v8(dst + 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+                } else {
 #pragma unroll
-                for (int v4 = 0; v4 < 4; ++v4)
-                    ptx::st_global_v4(orow + cc * 64 + v4 * 16, w[4 * v4], w[4 * v4 + 1],
-                                      w[4 * v4 + 2], w[4 * v4 + 3]);
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        ptx::st_global_v4(dst + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                          w[4 * v4 + 3]);
+                }
             }
         }
-        if (row_ok) p.lse[row_flat] = (l_exact > 0.f) ? (m_ref + log2f(l_exact)) * kLn2 : -INFINITY;
+        if (row_ok && h == 0)
+            p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
     }
@@ -712,6 +725,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    float *xch = reinterpret_cast<float *>(tmem_holder + 4);
     const uint32_t bars = ptx::smem_addr(bar_mem);
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
@@ -726,12 +740,12 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_SFREE + b), 128);
+            ptx::mbar_init(bar_addr(bars, C::B_SFREE + b), C::NUM_SOFTMAX);
         }
-        ptx::mbar_init(bar_addr(bars, C::B_PFULL), 128);
+        ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_SOFTMAX);
         ptx::mbar_init(bar_addr(bars, C::B_OFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
-        ptx::mbar_init(bar_addr(bars, C::B_OFREE), 128);
+        ptx::mbar_init(bar_addr(bars, C::B_OFREE), C::NUM_SOFTMAX);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
         *abort_flag = 0;
@@ -752,8 +766,8 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp < 4) {
-        softmax_role<D, kFP16>(p, bars, tmem, abort_flag);
+    if (warp < C::NUM_SOFTMAX / 32) {
+        softmax_role<D, kFP16>(p, bars, tmem, xch, abort_flag);
     } else if (warp == C::S_WARP) {
         if (lane == 0) mma_s_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else if (warp == C::PV_WARP) {

@@ -272,5 +272,31 @@ __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, ui
                  : "memory");
 }
 
+// 32 bytes in one store (sm_100 family); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// ------------------------------------------------------------ named barriers
+// Barrier `id` over `n` threads (a multiple of 32); orders shared memory like
+// __syncthreads among the participants.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Same barrier, returning the OR of `pred` over all participants.
+__device__ __forceinline__ bool named_bar_any(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
 }  // namespace ptx
 }  // namespace fa
