@@ -95,11 +95,14 @@ struct Cfg {
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K part at 0, V part at TILE_BYTES
-    // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, and the P
-    // area (BN/2 columns, two 16-bit values per column) at P_COL0.
+    // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, and two P
+    // areas (BN/2 columns each, two 16-bit values per column) at P_COL0 and
+    // P_COL0 + P_STRIDE; P of key tile t goes to area t & 1, so the softmax
+    // of tile t+1 never waits for P V of tile t.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t O_COL0 = (D == 256) ? 128 : 256;
-    static constexpr uint32_t P_COL0 = 448;
+    static constexpr uint32_t P_COL0 = 384;
+    static constexpr uint32_t P_STRIDE = 64;
     // Barrier indices.
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = 1;
@@ -107,16 +110,18 @@ struct Cfg {
     static constexpr int B_STEMPTY = B_STFULL + STAGES; // [STAGES]
     static constexpr int B_SFULL = B_STEMPTY + STAGES;  // [2]: S buffer b computed
     static constexpr int B_SFREE = B_SFULL + 2;         // [2]: S buffer b read by the softmax
-    static constexpr int B_PFULL = B_SFREE + 2;         // P area written
-    static constexpr int B_OFULL = B_PFULL + 1;         // one phase per P V
-    static constexpr int B_OFINAL = B_OFULL + 1;        // one phase per unit: last P V done
+    static constexpr int B_PFULL = B_SFREE + 2;         // [2]: P area b written
+    static constexpr int B_OFULL = B_PFULL + 2;         // [2]: P V from P area b done
+    static constexpr int B_OFINAL = B_OFULL + 2;        // one phase per unit: last P V done
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
     static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES;
     static constexpr int XCH_BYTES = 2 * kBM * 4;  // one fp32 per row and warpgroup
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 + XCH_BYTES;
-    static_assert(O_COL0 + D <= P_COL0 && P_COL0 + BN / 2 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
+                  "tensor memory overflow");
+    static_assert(BN / 2 <= (int)P_STRIDE, "P areas overlap");
     static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
@@ -397,7 +402,14 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
                 ok = false;
                 break;
             }
-            if (!wait_bar(bar_addr(bars, C::B_PFULL), t & 1u, abort_flag, 4)) { ok = false; break; }
+            // P of tile t is in area t & 1; that area's barrier completes once per
+            // two tiles, and the softmax cannot write P of tile t+2 before this
+            // P V has run, so the parity wait is unambiguous.
+            const uint32_t pb = t & 1u;
+            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, abort_flag, 4)) {
+                ok = false;
+                break;
+            }
             ptx::tc_fence_after();
             if (i == 0 && o_used) {
                 if (!wait_bar(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, abort_flag, 5)) {
@@ -411,10 +423,10 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk) {
                 // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
-                ptx::mma_ts(o_tmem, p_tmem + kk * 8, dv + (uint32_t)((kk * 2048) >> 4), kIdescO,
-                            (i > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_ts(o_tmem, p_tmem + pb * C::P_STRIDE + kk * 8,
+                            dv + (uint32_t)((kk * 2048) >> 4), kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
             }
-            ptx::mma_commit(bar_addr(bars, C::B_OFULL));
+            ptx::mma_commit(bar_addr(bars, C::B_OFULL + (int)pb));
             if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
             ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));  // this issuer's half
         }
@@ -552,7 +564,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
     const int r = (int)(threadIdx.x & 127);                     // query row within the tile
     const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
     const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)(h * (D / 2));
-    const uint32_t p_area = tmem + lane_off + C::P_COL0 + (uint32_t)(h * (HALF / 2));
+    const uint32_t p_half = tmem + lane_off + C::P_COL0 + (uint32_t)(h * (HALF / 2));
     const float c = p.scale_log2;
     uint32_t t_cnt = 0;  // key tiles processed (S buffer = t & 1; one P V each)
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
@@ -635,16 +647,20 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
                 m_ref = m_new;
                 rescale = true;
             }
-            // P V of the previous key tile must be finished before O is rescaled
-            // or the P area rewritten: wait for phase t-1 of the O barrier (one
-            // phase per P V, numbered like t).  Phase t-2 was waited for on the
-            // previous tile (or, on a unit's first tile, covered by the
-            // previous unit's final barrier) and P V of tile t cannot exist
-            // before this tile's P, so the barrier is at phase t-1 or t and the
-            // parity wait is unambiguous.
-            const bool need_pv = (j > un.lo);
+            // O barrier b completes once for each tile whose P sits in area b:
+            // completion k of barrier t & 1 is P V of tile t with k = t >> 1.
+            // Rescaling O needs every earlier P V finished: wait for P V of tile
+            // t-1 (a commit covers all earlier MMAs of its issuer).  Rewriting P
+            // area t & 1 needs P V of tile t-2.  The P V of the unit's previous
+            // unit are covered by its final barrier.  Each barrier's next
+            // completion needs a P this thread has not written yet, and the one
+            // before was waited for two tiles ago, so the parity waits are
+            // unambiguous.
+            const uint32_t pb = t & 1u;
             if (__any_sync(0xffffffffu, rescale)) {
-                if (need_pv) wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 8);
+                if (j > un.lo)
+                    wait_bar(bar_addr(bars, C::B_OFULL + (int)((t - 1u) & 1u)), ((t - 1u) >> 1) & 1u,
+                             abort_flag, 8);
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc) {
@@ -659,12 +675,13 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             }
             l = alpha * l + lr_t;
             l_exact = alpha * l_exact + le_t;
-            if (need_pv) wait_bar(bar_addr(bars, C::B_OFULL), (t - 1u) & 1u, abort_flag, 10);
+            if (j >= un.lo + 2)
+                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((t >> 1) - 1u) & 1u, abort_flag, 10);
             ptx::tc_fence_after();
-            store_p_cols<HALF>(p_area, pk);
+            store_p_cols<HALF>(p_half + pb * C::P_STRIDE, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
+            ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + (int)pb));
         }
 
         // Epilogue: wait for the unit's last P V, combine the halves' sums,
@@ -742,8 +759,10 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
             ptx::mbar_init(bar_addr(bars, C::B_SFREE + b), C::NUM_SOFTMAX);
         }
-        ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_SOFTMAX);
-        ptx::mbar_init(bar_addr(bars, C::B_OFULL), 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), C::NUM_SOFTMAX);
+            ptx::mbar_init(bar_addr(bars, C::B_OFULL + b), 1);
+        }
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFREE), C::NUM_SOFTMAX);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);

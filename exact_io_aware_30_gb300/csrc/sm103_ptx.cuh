@@ -279,6 +279,17 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t (&w)[8]) {
                  : "memory");
 }
 
+// ------------------------------------------------------------ register split
+// Per-warpgroup register budget (all four warps of a warpgroup execute it).
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ------------------------------------------------------------ named barriers
 // Barrier `id` over `n` threads (a multiple of 32); orders shared memory like
 // __syncthreads among the participants.
