@@ -224,6 +224,7 @@ template <int D>
 __device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
                          volatile int *abort_flag) {
     using C = Cfg<D>;
+    const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint64_t pol_kv = ptx::policy_evict_last();
     const uint64_t pol_q = ptx::policy_evict_first();
     uint32_t st_it = 0;  // stages filled so far
@@ -239,15 +240,15 @@ __device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
             ok = false;
             break;
         }
-        {
+        if (leader) {
             const uint32_t fb = bar_addr(bars, C::B_QFULL);
             ptx::mbar_arrive_expect_tx(fb, C::Q_BYTES);
             const uint32_t dst = ptx::smem_addr(sQ);
 #pragma unroll
             for (int c = 0; c < C::CHUNKS; ++c)
                 ptx::tma_load_4d(dst + c * C::Q_CHUNK, &p.tm_q, fb, c * 64, un.i0, un.h, un.b, pol_q);
-            ++q_cnt;
         }
+        ++q_cnt;
         const int n = un.hi - un.lo;
         for (int s = 0; s <= n; ++s) {
             const uint32_t slot = st_it % C::STAGES;
@@ -257,20 +258,22 @@ __device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
                 break;
             }
             const bool has_k = s < n, has_v = s >= 1;
-            const uint32_t fb = bar_addr(bars, C::B_STFULL + slot);
-            ptx::mbar_arrive_expect_tx(fb, (has_k ? C::TILE_BYTES : 0) + (has_v ? C::TILE_BYTES : 0));
-            const uint32_t dst = ptx::smem_addr(sKV + slot * C::STAGE_BYTES);
-            if (has_k) {
+            if (leader) {
+                const uint32_t fb = bar_addr(bars, C::B_STFULL + slot);
+                ptx::mbar_arrive_expect_tx(fb, (has_k ? C::TILE_BYTES : 0) + (has_v ? C::TILE_BYTES : 0));
+                const uint32_t dst = ptx::smem_addr(sKV + slot * C::STAGE_BYTES);
+                if (has_k) {
 #pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    ptx::tma_load_4d(dst + c * C::KV_CHUNK, &p.tm_k, fb, c * 64, (un.lo + s) * C::BN,
-                                     un.h, un.b, pol_kv);
-            }
-            if (has_v) {
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        ptx::tma_load_4d(dst + c * C::KV_CHUNK, &p.tm_k, fb, c * 64, (un.lo + s) * C::BN,
+                                         un.h, un.b, pol_kv);
+                }
+                if (has_v) {
 #pragma unroll
-                for (int c = 0; c < C::CHUNKS; ++c)
-                    ptx::tma_load_4d(dst + C::TILE_BYTES + c * C::KV_CHUNK, &p.tm_v, fb, c * 64,
-                                     (un.lo + s - 1) * C::BN, un.h, un.b, pol_kv);
+                    for (int c = 0; c < C::CHUNKS; ++c)
+                        ptx::tma_load_4d(dst + C::TILE_BYTES + c * C::KV_CHUNK, &p.tm_v, fb, c * 64,
+                                         (un.lo + s - 1) * C::BN, un.h, un.b, pol_kv);
+                }
             }
             ++st_it;
         }
@@ -298,6 +301,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
+    const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint64_t dq = smem_desc(ptx::smem_addr(sQ), 16);
     const uint32_t kv_addr = ptx::smem_addr(sKV);
     uint32_t st_it = 0;  // stages seen so far
@@ -330,16 +334,19 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
             ptx::tc_fence_after();
             const uint64_t dk = smem_desc(kv_addr + slot * C::STAGE_BYTES, 16);
             const uint32_t d_tmem = tmem + b * BN;
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
-                const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
-                const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
-                ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
+                    const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
+                    const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+                    ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
+                if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
+                ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));           // this issuer's half
             }
-            ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
-            if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
-            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));           // this issuer's half
+            __syncwarp();
         }
         if (!ok) break;
         // The last stage holds only a value tile: release this issuer's half,
@@ -352,13 +359,15 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
                 ok = false;
                 break;
             }
-            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + sidx % C::STAGES));
+            if (leader) ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + sidx % C::STAGES));
+            __syncwarp();
         }
         st_it = base + (uint32_t)n + 1u;
         t_cnt += (uint32_t)n;
         ++q_cnt;
     }
-    ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    __syncwarp();
     wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
 }
 
@@ -370,6 +379,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
+    const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint32_t kv_addr = ptx::smem_addr(sKV);
     const uint32_t o_tmem = tmem + C::O_COL0;
     const uint32_t p_tmem = tmem + C::P_COL0;
@@ -393,7 +403,8 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
             ok = false;
             break;
         }
-        ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
+        if (leader) ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
+        __syncwarp();
         for (int i = 0; i < n; ++i) {
             const uint32_t t = t_cnt + (uint32_t)i;
             const uint32_t sidx = base + 1u + (uint32_t)i;  // stage i+1 holds value tile i
@@ -420,28 +431,35 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
                 ptx::tc_fence_after();
             }
             const uint64_t dv = smem_desc(kv_addr + slot * C::STAGE_BYTES + C::TILE_BYTES, C::KV_CHUNK);
+            if (leader) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
-                ptx::mma_ts(o_tmem, p_tmem + pb * C::P_STRIDE + kk * 8,
-                            dv + (uint32_t)((kk * 2048) >> 4), kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
+                    ptx::mma_ts(o_tmem, p_tmem + pb * C::P_STRIDE + kk * 8,
+                                dv + (uint32_t)((kk * 2048) >> 4), kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                ptx::mma_commit(bar_addr(bars, C::B_OFULL + (int)pb));
+                if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
+                ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));  // this issuer's half
             }
-            ptx::mma_commit(bar_addr(bars, C::B_OFULL + (int)pb));
-            if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
-            ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));  // this issuer's half
+            __syncwarp();
         }
         if (!ok) break;
         st_it = base + (uint32_t)n + 1u;
         t_cnt += (uint32_t)n;
         o_used = true;
     }
-    ptx::mma_commit(bar_addr(bars, C::B_DRAIN + 1));
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN + 1));
+    __syncwarp();
     wait_bar_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
 }
 
 // ---------------------------------------------------------------- softmax role
 
-constexpr uint32_t kSoftmaxBar = 1;  // named barrier of the two softmax warpgroups
+// Warp w of softmax warpgroup 0 and warp w of warpgroup 1 own the same 32
+// rows (TMEM lanes); the pair synchronises on named barrier 1 + w, 64 threads.
+constexpr uint32_t kPairBar0 = 1;
+constexpr uint32_t kPairThreads = 64;
 
 // Loads this thread's N score columns (N = 32 or 64) from tensor memory.
 template <int N>
@@ -537,10 +555,10 @@ __device__ __forceinline__ void row_exp(const uint32_t (&sr)[N], float c, float 
 
 // Hands v to the partner thread (same row, other warpgroup) and returns the
 // partner's value.  The caller guarantees that the partner has finished
-// reading the previous exchange (a softmax barrier lies in between).
-__device__ __forceinline__ float swap_with_partner(float *xch, int h, int r, float v) {
+// reading the previous exchange (a pair barrier lies in between).
+__device__ __forceinline__ float swap_with_partner(float *xch, int h, int r, uint32_t bar, float v) {
     xch[h * kBM + r] = v;
-    ptx::named_bar_sync(kSoftmaxBar, 256);
+    ptx::named_bar_sync(bar, kPairThreads);
     return xch[(h ^ 1) * kBM + r];
 }
 
@@ -549,11 +567,11 @@ __device__ __forceinline__ float swap_with_partner(float *xch, int h, int r, flo
 // Both partners of a row keep the same reference max m_ref: they exchange
 // their half-row maxima whenever the reference is set or moves.
 //
-// Every softmax thread runs the same sequence of named barriers (the
-// decisions that choose barriers are CTA-uniform), and a pipeline wait that
-// gives up does not leave the loop: the thread carries on through the
-// schedule with whatever tensor memory holds, so that no partner is left at
-// a barrier.  The device status word reports the failure.
+// The two warps of a pair run the same sequence of pair barriers (the
+// decisions that choose barriers are uniform over the pair), and a pipeline
+// wait that gives up does not leave the loop: the thread carries on through
+// the schedule with whatever tensor memory holds, so that no partner is left
+// at a barrier.  The device status word reports the failure.
 template <int D, bool kFP16>
 __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch,
                              volatile int *abort_flag) {
@@ -563,6 +581,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
     const int h = (int)(threadIdx.x >> 7);                      // key-column half
     const int r = (int)(threadIdx.x & 127);                     // query row within the tile
     const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
+    const uint32_t pair_bar = kPairBar0 + (uint32_t)(r >> 5);    // barrier shared with the partner warp
     const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)(h * (D / 2));
     const uint32_t p_half = tmem + lane_off + C::P_COL0 + (uint32_t)(h * (HALF / 2));
     const float c = p.scale_log2;
@@ -615,14 +634,14 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // for the max: a weight above 2^8 (the max grew by more than the
             // deferral bound) pushes its half's sum above 2^8, so when no half
             // of any row exceeds the bound every weight is valid as computed.
-            // Otherwise (a CTA-wide vote) the halves exchange their maxima and
+            // Otherwise (a vote of the warp pair) the halves exchange their maxima and
             // each row whose max grew by more than the bound moves its
             // reference, rescales and exponentiates again.
             const bool first = (j == un.lo);
             if (first) {
                 const float hm = row_max<HALF>(sr);
-                ptx::named_bar_sync(kSoftmaxBar, 256);  // previous exchange fully read
-                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, hm));
+                ptx::named_bar_sync(pair_bar, kPairThreads);  // previous exchange fully read
+                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, pair_bar, hm));
                 m_ref = (mx == -INFINITY) ? -INFINITY : mx * c;
             }
             uint32_t pk[HALF / 2];
@@ -638,9 +657,9 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
                 // No reference yet (every earlier key of the row hidden) counts
                 // as exceeding the bound as soon as a key is visible.
                 const bool over = !(le_t <= kRescaleBound) || (m_ref == -INFINITY && le_t != 0.f);
-                if (!ptx::named_bar_any(kSoftmaxBar, 256, over)) break;
+                if (!ptx::named_bar_any(pair_bar, kPairThreads, over)) break;
                 const float hm = row_max<HALF>(sr);
-                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, hm));
+                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, pair_bar, hm));
                 const float m_new = fmaxf(m_ref, (mx == -INFINITY) ? -INFINITY : mx * c);
                 if (!(m_new > m_ref + kRescaleLog2)) break;  // weights within the bound
                 alpha = ptx::ex2_approx(m_ref - m_new);      // 0 while m_ref is -inf
@@ -689,12 +708,12 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
         wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9);
         ++u_cnt;
         ptx::tc_fence_after();
-        ptx::named_bar_sync(kSoftmaxBar, 256);  // previous exchange fully read
-        const float l_all = l + swap_with_partner(xch, h, r, l);
+        ptx::named_bar_sync(pair_bar, kPairThreads);  // previous exchange fully read
+        const float l_all = l + swap_with_partner(xch, h, r, pair_bar, l);
         float le_all = l_all;
         if constexpr (!kFP16) {
-            ptx::named_bar_sync(kSoftmaxBar, 256);
-            le_all = l_exact + swap_with_partner(xch, h, r, l_exact);
+            ptx::named_bar_sync(pair_bar, kPairThreads);
+            le_all = l_exact + swap_with_partner(xch, h, r, pair_bar, l_exact);
         }
         const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
 #pragma unroll
@@ -788,11 +807,11 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     if (warp < C::NUM_SOFTMAX / 32) {
         softmax_role<D, kFP16>(p, bars, tmem, xch, abort_flag);
     } else if (warp == C::S_WARP) {
-        if (lane == 0) mma_s_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+        mma_s_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else if (warp == C::PV_WARP) {
-        if (lane == 0) mma_pv_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+        mma_pv_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
     } else {
-        if (lane == 0) tma_role<D>(p, sQ, sKV, bars, abort_flag);
+        tma_role<D>(p, sQ, sKV, bars, abort_flag);
     }
     __syncwarp();
     ptx::tc_fence_before();
