@@ -101,9 +101,8 @@ bool make_map(CUtensorMap *m, const void *base, int d, int S, int H, int B, int 
 int head_dim_index(int d) { return d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : -1; }
 
 int bn_for(int d) { return d == 256 ? Cfg<256>::BN : d == 128 ? Cfg<128>::BN : Cfg<64>::BN; }
-int stages_for(int d) {
-    return d == 256 ? Cfg<256>::STAGES : d == 128 ? Cfg<128>::STAGES : Cfg<64>::STAGES;
-}
+int k_slots_for(int d) { return d == 256 ? Cfg<256>::KST : d == 128 ? Cfg<128>::KST : Cfg<64>::KST; }
+int v_slots_for(int d) { return d == 256 ? Cfg<256>::VST : d == 128 ? Cfg<128>::VST : Cfg<64>::VST; }
 
 // Size / kind checks shared by fa_fwd and fa_workspace_query.
 fa_status check_sizes(int B, int H, int Sq, int Sk, int d, int mask_kind, int window, int dtype) {
@@ -269,8 +268,8 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
                   "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=2 softmax_wgs=2 "
-                  "kv_stages=%d threads=%d smem=%d mask=%s persistent",
-                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::stages_for(d),
+                  "k_slots=%d v_slots=%d threads=%d smem=%d mask=%s persistent",
+                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::k_slots_for(d), fa::v_slots_for(d),
                   fa::Cfg<128>::NUM_THREADS,
                   d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES
                                                                : fa::Cfg<256>::SMEM_BYTES,

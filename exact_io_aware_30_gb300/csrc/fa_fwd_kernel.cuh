@@ -76,25 +76,27 @@ struct Params {
 template <int D>
 struct Cfg {
     // d = 256 uses 64-key tiles so that two S buffers and its 256-column O fit
-    // in tensor memory and two stages fit in shared memory.
+    // in tensor memory.  K and V tiles stream through two rings of KST and
+    // VST slots (one tile each), filling the shared memory left after Q.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
     static constexpr int HALF = BN / 2;                  // key columns per softmax warpgroup
-    static constexpr int STAGES = (D == 64) ? 6 : (D == 128) ? 3 : 2;
+    static constexpr int KST = (D == 64) ? 8 : (D == 128) ? 4 : 3;
+    static constexpr int VST = (D == 64) ? 4 : 2;
     // Warps 0-7: two softmax warpgroups (warpgroup h owns key columns
     // [h*HALF, (h+1)*HALF) of every tile, all 128 rows); warp 8: S MMAs;
-    // warp 9: P V MMAs; warp 10: TMA.
+    // warp 9: P V MMAs; warp 10: TMA of Q and K; warp 11: TMA of V.
     static constexpr int NUM_SOFTMAX = 256;
-    static constexpr int NUM_WARPS = 11;
+    static constexpr int NUM_WARPS = 12;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
     static constexpr int S_WARP = 8;
     static constexpr int PV_WARP = 9;
     static constexpr int TMA_WARP = 10;
+    static constexpr int TMA_V_WARP = 11;
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
-    static constexpr int STAGE_BYTES = 2 * TILE_BYTES; // K part at 0, V part at TILE_BYTES
     // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, and two P
     // areas (BN/2 columns each, two 16-bit values per column) at P_COL0 and
     // P_COL0 + P_STRIDE; P of key tile t goes to area t & 1, so the softmax
@@ -106,9 +108,11 @@ struct Cfg {
     // Barrier indices.
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = 1;
-    static constexpr int B_STFULL = 2;                  // [STAGES]
-    static constexpr int B_STEMPTY = B_STFULL + STAGES; // [STAGES]
-    static constexpr int B_SFULL = B_STEMPTY + STAGES;  // [2]: S buffer b computed
+    static constexpr int B_KFULL = 2;                   // [KST]: K slot loaded
+    static constexpr int B_KEMPTY = B_KFULL + KST;      // [KST]: K slot read by its S MMAs
+    static constexpr int B_VFULL = B_KEMPTY + KST;      // [VST]: V slot loaded
+    static constexpr int B_VEMPTY = B_VFULL + VST;      // [VST]: V slot read by its P V MMAs
+    static constexpr int B_SFULL = B_VEMPTY + VST;      // [2]: S buffer b computed
     static constexpr int B_SFREE = B_SFULL + 2;         // [2]: S buffer b read by the softmax
     static constexpr int B_PFULL = B_SFREE + 2;         // [2]: P area b written
     static constexpr int B_OFULL = B_PFULL + 2;         // [2]: P V from P area b done
@@ -116,7 +120,7 @@ struct Cfg {
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
     static constexpr int NUM_BARS = B_DRAIN + 2;
-    static constexpr int SMEM_TILES = Q_BYTES + STAGES * STAGE_BYTES;
+    static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
     static constexpr int XCH_BYTES = 2 * kBM * 4;  // one fp32 per row and warpgroup
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 + XCH_BYTES;
     static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
@@ -169,6 +173,24 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     return wait_bar_slow(bar, parity, abort_flag, site);
 }
 
+// Same bounded wait for the TMA producers, whose waits are off the critical
+// path: a short sleep between polls leaves the issue slots of the
+// sub-partition to the softmax warps that share it.
+__device__ __noinline__ bool wait_bar_backoff(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                              int site) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (;;) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicCAS(&g_fa_status, 0, 0x100 + site);
+            return false;
+        }
+        __nanosleep(256);
+    }
+}
+
 // Wait used only while shutting down after an abort: ignores the abort flag.
 __device__ __noinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = ptx::globaltimer_ns();
@@ -216,27 +238,59 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
     return un;
 }
 
-// ---------------------------------------------------------------- TMA role
+// ---------------------------------------------------------------- TMA roles
 
-// Stage k of a unit with n key tiles (k = 0 .. n) holds key tile lo+k (if
-// k < n) at offset 0 and value tile lo+k-1 (if k >= 1) at TILE_BYTES.
+// Loads tile `key0 / BN` of a K or V tensor into the next slot of its ring
+// (the whole warp waits for the slot, one lane issues).
 template <int D>
-__device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
-                         volatile int *abort_flag) {
+__device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *ring, uint32_t bars,
+                                             int full0, int empty0, int nslots, uint32_t &it,
+                                             int key0, const Unit &un, bool leader, uint64_t pol,
+                                             volatile int *abort_flag) {
     using C = Cfg<D>;
-    const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
+    const uint32_t slot = it % (uint32_t)nslots;
+    if (!wait_bar_backoff(bar_addr(bars, empty0 + (int)slot), ((it / (uint32_t)nslots) & 1) ^ 1,
+                          abort_flag, 2))
+        return false;
+    if (leader) {
+        const uint32_t fb = bar_addr(bars, full0 + (int)slot);
+        ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+        const uint32_t dst = ptx::smem_addr(ring + slot * C::TILE_BYTES);
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c)
+            ptx::tma_load_4d(dst + c * C::KV_CHUNK, tm, fb, c * 64, key0, un.h, un.b, pol);
+    }
+    ++it;
+    return true;
+}
+
+// Waits until every copy into a ring that was issued has landed (slot s of a
+// ring with m slots has been filled ceil((it - s) / m) times).
+__device__ __forceinline__ void drain_ring(uint32_t bars, int full0, int nslots, uint32_t it) {
+    for (int sl = 0; sl < nslots; ++sl) {
+        const uint32_t fills = it > (uint32_t)sl ? (it - (uint32_t)sl + nslots - 1) / (uint32_t)nslots : 0u;
+        if (fills) wait_bar_drain(bar_addr(bars, full0 + sl), (fills - 1) & 1);
+    }
+}
+
+// Q and K producer: per unit the Q tile, then the unit's key tiles in order.
+// V has its own producer warp, so a key tile never waits behind a value slot.
+template <int D>
+__device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t bars,
+                            volatile int *abort_flag) {
+    using C = Cfg<D>;
+    const bool leader = ptx::lane_id() == 0;
     const uint64_t pol_kv = ptx::policy_evict_last();
     const uint64_t pol_q = ptx::policy_evict_first();
-    uint32_t st_it = 0;  // stages filled so far
+    uint32_t k_it = 0;   // K tiles loaded so far
     uint32_t q_cnt = 0;  // Q tiles loaded so far
     bool ok = true;
-
     for (int k = 0; ok; ++k) {
         const int u = unit_at(k);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
-        if (!wait_bar(bar_addr(bars, C::B_QEMPTY), (q_cnt & 1) ^ 1, abort_flag, 1)) {
+        if (!wait_bar_backoff(bar_addr(bars, C::B_QEMPTY), (q_cnt & 1) ^ 1, abort_flag, 1)) {
             ok = false;
             break;
         }
@@ -249,62 +303,50 @@ __device__ void tma_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t ba
                 ptx::tma_load_4d(dst + c * C::Q_CHUNK, &p.tm_q, fb, c * 64, un.i0, un.h, un.b, pol_q);
         }
         ++q_cnt;
-        const int n = un.hi - un.lo;
-        for (int s = 0; s <= n; ++s) {
-            const uint32_t slot = st_it % C::STAGES;
-            if (!wait_bar(bar_addr(bars, C::B_STEMPTY + slot), ((st_it / C::STAGES) & 1) ^ 1,
-                          abort_flag, 2)) {
-                ok = false;
-                break;
-            }
-            const bool has_k = s < n, has_v = s >= 1;
-            if (leader) {
-                const uint32_t fb = bar_addr(bars, C::B_STFULL + slot);
-                ptx::mbar_arrive_expect_tx(fb, (has_k ? C::TILE_BYTES : 0) + (has_v ? C::TILE_BYTES : 0));
-                const uint32_t dst = ptx::smem_addr(sKV + slot * C::STAGE_BYTES);
-                if (has_k) {
-#pragma unroll
-                    for (int c = 0; c < C::CHUNKS; ++c)
-                        ptx::tma_load_4d(dst + c * C::KV_CHUNK, &p.tm_k, fb, c * 64, (un.lo + s) * C::BN,
-                                         un.h, un.b, pol_kv);
-                }
-                if (has_v) {
-#pragma unroll
-                    for (int c = 0; c < C::CHUNKS; ++c)
-                        ptx::tma_load_4d(dst + C::TILE_BYTES + c * C::KV_CHUNK, &p.tm_v, fb, c * 64,
-                                         (un.lo + s - 1) * C::BN, un.h, un.b, pol_kv);
-                }
-            }
-            ++st_it;
-        }
+        for (int j = un.lo; j < un.hi && ok; ++j)
+            ok = load_kv_tile<D>(&p.tm_k, sK, bars, C::B_KFULL, C::B_KEMPTY, C::KST, k_it, j * C::BN, un,
+                                 leader, pol_kv, abort_flag);
     }
-    if (!ok) {
-        // Let every copy already issued land before the CTA can exit.
-        // Slot s has been filled ceil((st_it - s) / STAGES) times so far.
-#pragma unroll
-        for (int s = 0; s < C::STAGES; ++s) {
-            const uint32_t fills =
-                st_it > (uint32_t)s ? (st_it - (uint32_t)s + C::STAGES - 1) / C::STAGES : 0u;
-            if (fills) wait_bar_drain(bar_addr(bars, C::B_STFULL + s), (fills - 1) & 1);
-        }
+    if (!ok) {  // let every copy already issued land before the CTA can exit
+        drain_ring(bars, C::B_KFULL, C::KST, k_it);
         if (q_cnt) wait_bar_drain(bar_addr(bars, C::B_QFULL), (q_cnt - 1) & 1);
     }
 }
 
-// ---------------------------------------------------------------- MMA role
+// V producer: the units' value tiles in order.
+template <int D>
+__device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, volatile int *abort_flag) {
+    using C = Cfg<D>;
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    uint32_t v_it = 0;  // V tiles loaded so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+        const int u = unit_at(k);
+        if (u >= p.n_units) break;
+        const Unit un = decode_unit<D>(u, p);
+        if (!un.valid) continue;
+        for (int j = un.lo; j < un.hi && ok; ++j)
+            ok = load_kv_tile<D>(&p.tm_v, sV, bars, C::B_VFULL, C::B_VEMPTY, C::VST, v_it, j * C::BN, un,
+                                 leader, pol_kv, abort_flag);
+    }
+    if (!ok) drain_ring(bars, C::B_VFULL, C::VST, v_it);
+}
+
+// ---------------------------------------------------------------- MMA roles
 
 // S issuer: S_b = Q K^T for every key tile, into buffer b = t & 1 as soon as
 // the softmax has read that buffer's previous tile.
 template <int D, bool kFP16>
-__device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
+__device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t bars,
                            uint32_t tmem, volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
     const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint64_t dq = smem_desc(ptx::smem_addr(sQ), 16);
-    const uint32_t kv_addr = ptx::smem_addr(sKV);
-    uint32_t st_it = 0;  // stages seen so far
+    const uint32_t k_addr = ptx::smem_addr(sK);
+    uint32_t k_it = 0;   // K tiles consumed
     uint32_t t_cnt = 0;  // key tiles issued (S buffer = t & 1)
     uint32_t q_cnt = 0;  // Q tiles consumed
     bool ok = true;
@@ -315,14 +357,12 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
-        const uint32_t base = st_it;
         if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, abort_flag, 6)) { ok = false; break; }
-        for (int i = 0; i < n; ++i) {
+        for (int i = 0; i < n; ++i, ++k_it) {
             const uint32_t t = t_cnt + (uint32_t)i;
-            const uint32_t sidx = base + (uint32_t)i;  // stage i holds key tile i
-            const uint32_t slot = sidx % C::STAGES;
+            const uint32_t slot = k_it % C::KST;
             const uint32_t b = t & 1u;
-            if (!wait_bar(bar_addr(bars, C::B_STFULL + slot), (sidx / C::STAGES) & 1, abort_flag, 3)) {
+            if (!wait_bar(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, abort_flag, 3)) {
                 ok = false;
                 break;
             }
@@ -332,7 +372,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
                 break;
             }
             ptx::tc_fence_after();
-            const uint64_t dk = smem_desc(kv_addr + slot * C::STAGE_BYTES, 16);
+            const uint64_t dk = smem_desc(k_addr + slot * C::TILE_BYTES, 16);
             const uint32_t d_tmem = tmem + b * BN;
             if (leader) {
 #pragma unroll
@@ -344,25 +384,11 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
                 }
                 ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
                 if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
-                ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));           // this issuer's half
+                ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + (int)slot));
             }
             __syncwarp();
         }
         if (!ok) break;
-        // The last stage holds only a value tile: release this issuer's half,
-        // but only once it has been filled, so that the arrival cannot count
-        // towards the slot's previous fill while the other issuer still reads it.
-        {
-            const uint32_t sidx = base + (uint32_t)n;
-            if (!wait_bar(bar_addr(bars, C::B_STFULL + sidx % C::STAGES), (sidx / C::STAGES) & 1,
-                          abort_flag, 3)) {
-                ok = false;
-                break;
-            }
-            if (leader) ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + sidx % C::STAGES));
-            __syncwarp();
-        }
-        st_it = base + (uint32_t)n + 1u;
         t_cnt += (uint32_t)n;
         ++q_cnt;
     }
@@ -374,16 +400,16 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t 
 // P V issuer: O (+)= P V for every key tile, as soon as the softmax has
 // written P.
 template <int D, bool kFP16>
-__device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t bars,
-                            uint32_t tmem, volatile int *abort_flag) {
+__device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_t tmem,
+                            volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
     const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
-    const uint32_t kv_addr = ptx::smem_addr(sKV);
+    const uint32_t v_addr = ptx::smem_addr(sV);
     const uint32_t o_tmem = tmem + C::O_COL0;
     const uint32_t p_tmem = tmem + C::P_COL0;
-    uint32_t st_it = 0;      // stages seen so far
+    uint32_t v_it = 0;       // V tiles consumed
     uint32_t t_cnt = 0;      // key tiles processed (one P V each)
     uint32_t ofree_cnt = 0;  // epilogues waited for
     bool o_used = false;
@@ -395,21 +421,10 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
-        const uint32_t base = st_it;
-        // The first stage holds only a key tile: release this issuer's half once
-        // it has been filled (see the S issuer).
-        if (!wait_bar(bar_addr(bars, C::B_STFULL + base % C::STAGES), (base / C::STAGES) & 1,
-                      abort_flag, 3)) {
-            ok = false;
-            break;
-        }
-        if (leader) ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + base % C::STAGES));
-        __syncwarp();
-        for (int i = 0; i < n; ++i) {
+        for (int i = 0; i < n; ++i, ++v_it) {
             const uint32_t t = t_cnt + (uint32_t)i;
-            const uint32_t sidx = base + 1u + (uint32_t)i;  // stage i+1 holds value tile i
-            const uint32_t slot = sidx % C::STAGES;
-            if (!wait_bar(bar_addr(bars, C::B_STFULL + slot), (sidx / C::STAGES) & 1, abort_flag, 3)) {
+            const uint32_t slot = v_it % C::VST;
+            if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, abort_flag, 3)) {
                 ok = false;
                 break;
             }
@@ -430,7 +445,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
                 ++ofree_cnt;
                 ptx::tc_fence_after();
             }
-            const uint64_t dv = smem_desc(kv_addr + slot * C::STAGE_BYTES + C::TILE_BYTES, C::KV_CHUNK);
+            const uint64_t dv = smem_desc(v_addr + slot * C::TILE_BYTES, C::KV_CHUNK);
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
@@ -440,12 +455,11 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sQ, uint8_t *sKV, uint32_t
                 }
                 ptx::mma_commit(bar_addr(bars, C::B_OFULL + (int)pb));
                 if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
-                ptx::mma_commit(bar_addr(bars, C::B_STEMPTY + slot));  // this issuer's half
+                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + (int)slot));
             }
             __syncwarp();
         }
         if (!ok) break;
-        st_it = base + (uint32_t)n + 1u;
         t_cnt += (uint32_t)n;
         o_used = true;
     }
@@ -757,7 +771,8 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem;
-    uint8_t *sKV = smem + C::Q_BYTES;
+    uint8_t *sK = smem + C::Q_BYTES;
+    uint8_t *sV = sK + C::KST * C::TILE_BYTES;
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -770,9 +785,13 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar_addr(bars, C::B_QFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_QEMPTY), 1);
-        for (int s = 0; s < C::STAGES; ++s) {
-            ptx::mbar_init(bar_addr(bars, C::B_STFULL + s), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_STEMPTY + s), 2);  // one arrival per issuer
+        for (int s = 0; s < C::KST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_KFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_VFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_VEMPTY + s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
@@ -807,11 +826,13 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     if (warp < C::NUM_SOFTMAX / 32) {
         softmax_role<D, kFP16>(p, bars, tmem, xch, abort_flag);
     } else if (warp == C::S_WARP) {
-        mma_s_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+        mma_s_role<D, kFP16>(p, sQ, sK, bars, tmem, abort_flag);
     } else if (warp == C::PV_WARP) {
-        mma_pv_role<D, kFP16>(p, sQ, sKV, bars, tmem, abort_flag);
+        mma_pv_role<D, kFP16>(p, sV, bars, tmem, abort_flag);
+    } else if (warp == C::TMA_WARP) {
+        tma_qk_role<D>(p, sQ, sK, bars, abort_flag);
     } else {
-        tma_role<D>(p, sQ, sKV, bars, abort_flag);
+        tma_v_role<D>(p, sV, bars, abort_flag);
     }
     __syncwarp();
     ptx::tc_fence_before();
