@@ -411,14 +411,19 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (smaller profiling case of the same kernel)")
+    ap.add_argument("--seq", type=int, default=0,
+                    help="override Sq = Sk (sequence-length sweeps of the same kernel)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     wl = int(args.workload) if args.workload.isdigit() else args.workload
     w = inputs.workload(wl)
-    if args.heads:
+    if args.heads or args.seq:
         import dataclasses
-        w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
+        if args.heads:
+            w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
+        if args.seq:
+            w = dataclasses.replace(w, Sq=args.seq, Sk=args.seq, name=f"{w.name}_s{args.seq}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -15,6 +15,10 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <algorithm>
+#include <queue>
+#include <utility>
+#include <vector>
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
@@ -31,6 +35,7 @@ struct DeviceInfo {
     bool probed = false;
     bool supported = false;
     int num_sms = 0;
+    int l2_bytes = 0;
     bool attr_set[6] = {false, false, false, false, false, false};
 };
 
@@ -59,6 +64,8 @@ fa_status device_info(int *dev_out, DeviceInfo **info) {
             return FA_ERR_CUDA;
         d.supported = (major == 10 && minor == 3);
         d.num_sms = sms;
+        int l2 = 0;
+        if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) == cudaSuccess) d.l2_bytes = l2;
         d.probed = true;
     }
     *dev_out = dev;
@@ -103,6 +110,98 @@ int head_dim_index(int d) { return d == 64 ? 0 : d == 128 ? 1 : d == 256 ? 2 : -
 int bn_for(int d) { return d == 256 ? Cfg<256>::BN : d == 128 ? Cfg<128>::BN : Cfg<64>::BN; }
 int k_slots_for(int d) { return d == 256 ? Cfg<256>::KST : d == 128 ? Cfg<128>::KST : Cfg<64>::KST; }
 int v_slots_for(int d) { return d == 256 ? Cfg<256>::VST : d == 128 ? Cfg<128>::VST : Cfg<64>::VST; }
+
+// Key tiles a query tile visits (the kernel's decode, on the host).
+int unit_tiles(const Params &p, int gq, int bn) {
+    const int i0 = gq * 128;
+    const int row_end = i0 + 128 < p.Sq ? i0 + 128 : p.Sq;
+    int key_end = p.Sk;
+    if (p.mask_kind != FA_MASK_NONE) key_end = p.Sk < row_end ? p.Sk : row_end;
+    int key_beg = 0;
+    if (p.mask_kind == FA_MASK_SLIDING_WINDOW) key_beg = i0 - p.window + 1 > 0 ? i0 - p.window + 1 : 0;
+    if (key_beg >= key_end) return 0;
+    return (key_end + bn - 1) / bn - key_beg / bn;
+}
+
+// (Batch, head) pairs are scheduled in groups whose K and V -- what every
+// query tile of a head re-reads -- fit in a third of the L2, so that the CTAs
+// working on a group find them there: K/V then come from DRAM about once and
+// DRAM traffic grows with S rather than S^2.
+int heads_per_group(const Params &p, int d, int l2_bytes) {
+    const int BH = p.B * p.H;
+    const double kv_head = 2.0 * (double)p.Sk * d * 2.0;
+    const double budget = (l2_bytes > 0 ? (double)l2_bytes : 96.0e6) / 3.0;
+    const int g = (int)(budget / kv_head);
+    return g < 1 ? 1 : (g > BH ? BH : g);
+}
+
+// The kernel's unit numbering (decode_unit): groups of heads_per_group
+// heads, longest query tiles first inside a group.  Returns the query tile.
+int unit_qtile(const Params &p, int u) {
+    const int BH = p.B * p.H, G = p.heads_per_group, nq = p.n_qtiles;
+    const int h0 = (u / (G * nq)) * G;
+    const int Gg = G < BH - h0 ? G : BH - h0;
+    return nq - 1 - (u - h0 * nq) / Gg;
+}
+
+// Per-CTA unit lists: units in the numbering above are dealt in turn to the
+// CTA with the least work so far (cost: key tiles plus three tiles of
+// per-unit overhead), and each CTA runs its units in the order received, so
+// that all CTAs work on the same group of heads at about the same time.
+// Schedules are cached per shape.  Returns false (snake order) when the
+// shape is too large to describe in the kernel parameters.
+struct SchedKey {
+    int B, H, Sq, Sk, d, mask, window, grid, G;
+    bool operator==(const SchedKey &o) const {
+        return B == o.B && H == o.H && Sq == o.Sq && Sk == o.Sk && d == o.d && mask == o.mask &&
+               window == o.window && grid == o.grid && G == o.G;
+    }
+};
+struct SchedEntry {
+    SchedKey key;
+    std::vector<uint16_t> off, ids;
+};
+std::vector<SchedEntry> g_sched_cache;  // guarded by g_mutex; a few recent shapes
+
+bool build_schedule(Params &p, int d, int bn, int grid) {
+    if (grid > kMaxSchedGrid || p.n_units > kMaxSchedUnits) return false;
+    const SchedKey key{p.B, p.H, p.Sq, p.Sk, d, p.mask_kind, p.window, grid, p.heads_per_group};
+    std::lock_guard<std::mutex> lock(g_mutex);
+    const SchedEntry *hit = nullptr;
+    for (const auto &e : g_sched_cache)
+        if (e.key == key) hit = &e;
+    if (!hit) {
+        const int nq = p.n_qtiles;
+        std::vector<double> cost(nq);
+        for (int g = 0; g < nq; ++g) {
+            const int t = unit_tiles(p, g, bn);
+            cost[g] = t > 0 ? t + 3.0 : 0.5;
+        }
+        std::vector<std::vector<uint16_t>> lists(grid);
+        using Slot = std::pair<double, int>;
+        std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> free_at;
+        for (int c = 0; c < grid; ++c) free_at.push({0.0, c});
+        for (int u = 0; u < p.n_units; ++u) {
+            const Slot s = free_at.top();
+            free_at.pop();
+            lists[s.second].push_back((uint16_t)u);
+            free_at.push({s.first + cost[unit_qtile(p, u)], s.second});
+        }
+        SchedEntry e;
+        e.key = key;
+        e.off.assign(grid + 1, 0);
+        for (int c = 0; c < grid; ++c) {
+            e.off[c + 1] = (uint16_t)(e.off[c] + lists[c].size());
+            e.ids.insert(e.ids.end(), lists[c].begin(), lists[c].end());
+        }
+        if (g_sched_cache.size() >= 8) g_sched_cache.erase(g_sched_cache.begin());
+        g_sched_cache.push_back(std::move(e));
+        hit = &g_sched_cache.back();
+    }
+    std::memcpy(p.sched_off, hit->off.data(), hit->off.size() * sizeof(uint16_t));
+    std::memcpy(p.sched_ids, hit->ids.data(), hit->ids.size() * sizeof(uint16_t));
+    return true;
+}
 
 // Size / kind checks shared by fa_fwd and fa_workspace_query.
 fa_status check_sizes(int B, int H, int Sq, int Sk, int d, int mask_kind, int window, int dtype) {
@@ -193,6 +292,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     p.o_vec8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     p.n_qtiles = (Sq + 127) / 128;
     p.n_units = B * H * p.n_qtiles;
+    p.heads_per_group = heads_per_group(p, d, info->l2_bytes);
+    p.sched = build_schedule(p, d, bn, p.n_units < info->num_sms ? p.n_units : info->num_sms) ? 1 : 0;
 
     if (log_enabled()) {
         char buf[256];

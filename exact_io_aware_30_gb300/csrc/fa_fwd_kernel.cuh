@@ -59,6 +59,9 @@ constexpr float kLn2 = 0.693147180559945309f;
 // (This header is compiled into exactly one translation unit.)
 __device__ int g_fa_status = 0;
 
+constexpr int kMaxSchedGrid = 256;     // CTAs a precomputed schedule can describe
+constexpr int kMaxSchedUnits = 12288;  // units a precomputed schedule can hold
+
 struct Params {
     CUtensorMap tm_q;  // [B, H, Sq, d] 16-bit, box {64, 128, 1, 1}, 128-B swizzle
     CUtensorMap tm_k;  // [B, H, Sk, d], box {64, BN, 1, 1}
@@ -70,8 +73,15 @@ struct Params {
     float scale_log2;  // scale * log2(e), kept positive (see the API)
     int n_qtiles;      // ceil(Sq / 128): units per (batch, head)
     int n_units;       // B * H * n_qtiles
+    int heads_per_group;  // (batch, head) pairs scheduled together (K/V kept in L2)
     int o_vec8;        // O is 32-byte aligned: 32-byte stores
+    // Schedule: with sched = 1, CTA c runs units sched_ids[sched_off[c] ..
+    // sched_off[c+1]) in that order (built on the host); else the snake order.
+    int sched;
+    uint16_t sched_off[kMaxSchedGrid + 1];
+    uint16_t sched_ids[kMaxSchedUnits];
 };
+static_assert(sizeof(Params) <= 32764, "kernel parameter space");
 
 template <int D>
 struct Cfg {
@@ -199,10 +209,15 @@ __device__ __noinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
-// Unit k of this CTA in a snake order: even rounds left to right, odd rounds
+// Unit k of this CTA (n_units once the CTA has no more): from the host's
+// schedule, or else in a snake order (even rounds left to right, odd rounds
 // right to left, so that with units sorted longest-first each CTA's sum of
-// work stays close to the others'.
-__device__ __forceinline__ int unit_at(int k) {
+// work stays close to the others').
+__device__ __forceinline__ int unit_at(int k, const Params &p) {
+    if (p.sched) {
+        const int o = (int)p.sched_off[blockIdx.x] + k;
+        return o < (int)p.sched_off[blockIdx.x + 1] ? (int)p.sched_ids[o] : p.n_units;
+    }
     const int G = gridDim.x, c = blockIdx.x;
     return (k & 1) ? k * G + (G - 1 - c) : k * G + c;
 }
@@ -220,10 +235,18 @@ template <int D>
 __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
     constexpr int BN = Cfg<D>::BN;
     Unit un;
+    // Units come in groups of heads_per_group (batch, head) pairs whose K and
+    // V fit in L2 together; inside a group, longest query tiles first
+    // (causal / window work grows with the tile index), heads interleaved.
     const int BH = p.B * p.H;
-    const int gi = u / BH;
-    const int bh = u - gi * BH;
-    const int g = p.n_qtiles - 1 - gi;  // longest first (causal / window)
+    const int G = p.heads_per_group;
+    const int grp = u / (G * p.n_qtiles);
+    const int h0 = grp * G;
+    const int Gg = min(G, BH - h0);  // heads in this (possibly last, smaller) group
+    const int idx = u - h0 * p.n_qtiles;
+    const int gi = idx / Gg;
+    const int bh = h0 + (idx - gi * Gg);
+    const int g = p.n_qtiles - 1 - gi;
     un.b = bh / p.H;
     un.h = bh - un.b * p.H;
     un.i0 = g * kBM;
@@ -286,7 +309,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
     uint32_t q_cnt = 0;  // Q tiles loaded so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-        const int u = unit_at(k);
+        const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
@@ -322,7 +345,7 @@ __device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, volatile
     uint32_t v_it = 0;  // V tiles loaded so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-        const int u = unit_at(k);
+        const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
@@ -352,7 +375,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-        const int u = unit_at(k);
+        const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
@@ -416,7 +439,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
     bool ok = true;
 
     for (int k = 0; ok; ++k) {
-        const int u = unit_at(k);
+        const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
@@ -603,7 +626,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
 
     for (int k = 0;; ++k) {
-        const int u = unit_at(k);
+        const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         const int row = un.i0 + r;
@@ -628,6 +651,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
         float l_exact = 0.f;      // this half's fp32 sum of P (for the logsumexp)
 
         for (int j = un.lo; j < un.hi; ++j) {
+            const int i = j - un.lo;  // step within the unit
             const uint32_t t = t_cnt++;
             const int b = (int)(t & 1u);
             wait_bar(bar_addr(bars, C::B_SFULL + b), (t >> 1) & 1u, abort_flag, 7);
@@ -651,7 +675,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // Otherwise (a vote of the warp pair) the halves exchange their maxima and
             // each row whose max grew by more than the bound moves its
             // reference, rescales and exponentiates again.
-            const bool first = (j == un.lo);
+            const bool first = (i == 0);
             if (first) {
                 const float hm = row_max<HALF>(sr);
                 ptx::named_bar_sync(pair_bar, kPairThreads);  // previous exchange fully read
@@ -691,7 +715,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // unambiguous.
             const uint32_t pb = t & 1u;
             if (__any_sync(0xffffffffu, rescale)) {
-                if (j > un.lo)
+                if (i > 0)
                     wait_bar(bar_addr(bars, C::B_OFULL + (int)((t - 1u) & 1u)), ((t - 1u) >> 1) & 1u,
                              abort_flag, 8);
                 ptx::tc_fence_after();
@@ -708,7 +732,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             }
             l = alpha * l + lr_t;
             l_exact = alpha * l_exact + le_t;
-            if (j >= un.lo + 2)
+            if (i >= 2)
                 wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((t >> 1) - 1u) & 1u, abort_flag, 10);
             ptx::tc_fence_after();
             store_p_cols<HALF>(p_half + pb * C::P_STRIDE, pk);
