@@ -108,7 +108,7 @@ def test_invalid_calls_are_rejected_before_launch(lib, kw, status):
     ((0, 1, 128, 128, 128, "none", 0, 0), fa.FA_ERR_INVALID_ARG),
     ((1, 1, 128, 128, 128, "window", 0, 0), fa.FA_ERR_INVALID_ARG),
 ])
-def test_workspace_query_matches_fwd_verdict(lib, args, status):
+def test_workspace_query_matches_fwd_status(lib, args, status):
     st, nbytes = fa.workspace_query(*args)
     assert st == status
     assert nbytes == 0
