@@ -272,7 +272,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     Params p;
     std::memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_q, q, d, Sq, H, B, 128, fp16) || !make_map(&p.tm_k, k, d, Sk, H, B, bn, fp16) ||
-        !make_map(&p.tm_v, v, d, Sk, H, B, bn, fp16))
+        !make_map(&p.tm_v, v, d, Sk, H, B, bn, fp16) ||
+        (d <= 128 && !make_map(&p.tm_o, o, d, Sq, H, B, 128, fp16)))
         return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;

@@ -66,6 +66,7 @@ struct Params {
     CUtensorMap tm_q;  // [B, H, Sq, d] 16-bit, box {64, 128, 1, 1}, 128-B swizzle
     CUtensorMap tm_k;  // [B, H, Sk, d], box {64, BN, 1, 1}
     CUtensorMap tm_v;  // [B, H, Sk, d], box {64, BN, 1, 1}
+    CUtensorMap tm_o;  // [B, H, Sq, d] 16-bit, box {64, 128, 1, 1}, 128-B swizzle (d <= 128)
     void *o;           // [B, H, Sq, d] 16-bit
     float *lse;        // [B, H, Sq] fp32
     int B, H, Sq, Sk;
@@ -90,7 +91,7 @@ struct Cfg {
     // VST slots (one tile each), filling the shared memory left after Q.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
     static constexpr int HALF = BN / 2;                  // key columns per softmax warpgroup
-    static constexpr int KST = (D == 64) ? 8 : (D == 128) ? 4 : 3;
+    static constexpr int KST = (D == 64) ? 8 : 3;
     static constexpr int VST = (D == 64) ? 4 : 2;
     // Warps 0-7: two softmax warpgroups (warpgroup h owns key columns
     // [h*HALF, (h+1)*HALF) of every tile, all 128 rows); warp 8: S MMAs;
@@ -130,7 +131,11 @@ struct Cfg {
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
     static constexpr int NUM_BARS = B_DRAIN + 2;
-    static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
+    // d <= 128: the epilogue stages the normalised O tile (the Q tile's shape)
+    // in shared memory for one bulk tensor store; d = 256 has no room for it
+    // and stores rows directly.
+    static constexpr int O_STAGE_BYTES = (D <= 128) ? Q_BYTES : 0;
+    static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES + O_STAGE_BYTES;
     static constexpr int XCH_BYTES = 2 * kBM * 4;  // one fp32 per row and warpgroup
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 + XCH_BYTES;
     static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
@@ -497,6 +502,8 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
 // rows (TMEM lanes); the pair synchronises on named barrier 1 + w, 64 threads.
 constexpr uint32_t kPairBar0 = 1;
 constexpr uint32_t kPairThreads = 64;
+// Barrier of all 256 softmax threads around the staged O tile.
+constexpr uint32_t kEpilogueBar = 5;
 
 // Loads this thread's N score columns (N = 32 or 64) from tensor memory.
 template <int N>
@@ -610,7 +617,7 @@ __device__ __forceinline__ float swap_with_partner(float *xch, int h, int r, uin
 // the schedule with whatever tensor memory holds, so that no partner is left
 // at a barrier.  The device status word reports the failure.
 template <int D, bool kFP16>
-__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch,
+__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch, uint8_t *sO,
                              volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
@@ -754,34 +761,77 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             le_all = l_exact + swap_with_partner(xch, h, r, pair_bar, l_exact);
         }
         const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+        if constexpr (C::O_STAGE_BYTES > 0) {
+            // Normalise this thread's D/2 columns of O into registers, release
+            // O to the next unit's P V, then stage the tile in shared memory in
+            // the tensor map's layout (64-column boxes of 128-byte rows, 16-byte
+            // chunks swizzled by row & 7) and write it with one bulk store.
+            // Rows past Sq fall outside the tensor and are not written.
+            uint32_t w[D / 4];
 #pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-            uint32_t ov[32];
-            ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<32>(ov);
-            uint32_t w[16];
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t ov[32];
+                ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<32>(ov);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                w[i] = pack2<kFP16>(__uint_as_float(ov[2 * i]) * inv_l,
-                                    __uint_as_float(ov[2 * i + 1]) * inv_l);
-            if (row_ok) {
-                uint8_t *dst = ohalf + cc * 64;
-                if (p.o_vec8) {
-                    ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
-                    ptx::st_global_v8(dst + 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
-                } else {
+                for (int e = 0; e < 16; ++e)
+                    w[cc * 16 + e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
+                                                  __uint_as_float(ov[2 * e + 1]) * inv_l);
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+            const uint32_t so = ptx::smem_addr(sO);
+            if (threadIdx.x == 0) ptx::bulk_wait_read_all();  // the previous tile has left sO
+            ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
 #pragma unroll
-                    for (int v4 = 0; v4 < 4; ++v4)
-                        ptx::st_global_v4(dst + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                                          w[4 * v4 + 3]);
+            for (int c = 0; c < D / 16; ++c) {
+                const int col = h * (D / 2) + c * 8;  // first of the chunk's 8 columns
+                const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + r * 128 +
+                                                      ((((col & 63) >> 3) ^ (r & 7)) << 4));
+                ptx::st_shared_v4(addr, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            }
+            ptx::fence_proxy_async_smem();
+            ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
+            if (threadIdx.x == 0) {
+#pragma unroll
+                for (int bx = 0; bx < D / 64; ++bx)
+                    ptx::tma_store_4d(&p.tm_o, so + bx * (kBM * 128), bx * 64, un.i0, un.h, un.b);
+                ptx::bulk_commit_group();
+            }
+        } else {
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t ov[32];
+                ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<32>(ov);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
+                                        __uint_as_float(ov[2 * e + 1]) * inv_l);
+                if (row_ok) {
+                    uint8_t *dst = ohalf + cc * 64;
+                    if (p.o_vec8) {
+                        ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+                        ptx::st_global_v8(dst + 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+                    } else {
+#pragma unroll
+                        for (int v4 = 0; v4 < 4; ++v4)
+                            ptx::st_global_v4(dst + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                              w[4 * v4 + 3]);
+                    }
                 }
             }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
         }
         if (row_ok && h == 0)
             p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+    }
+    if constexpr (C::O_STAGE_BYTES > 0) {
+        if (threadIdx.x == 0) ptx::bulk_wait_all();  // sO must outlive the stores
     }
 }
 
@@ -797,6 +847,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint8_t *sQ = smem;
     uint8_t *sK = smem + C::Q_BYTES;
     uint8_t *sV = sK + C::KST * C::TILE_BYTES;
+    uint8_t *sO = sV + C::VST * C::TILE_BYTES;  // O staging (d <= 128)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -841,6 +892,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         ptx::prefetch_tensormap(&p.tm_q);
         ptx::prefetch_tensormap(&p.tm_k);
         ptx::prefetch_tensormap(&p.tm_v);
+        if (C::O_STAGE_BYTES > 0) ptx::prefetch_tensormap(&p.tm_o);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -848,7 +900,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp < C::NUM_SOFTMAX / 32) {
-        softmax_role<D, kFP16>(p, bars, tmem, xch, abort_flag);
+        softmax_role<D, kFP16>(p, bars, tmem, xch, sO, abort_flag);
     } else if (warp == C::S_WARP) {
         mma_s_role<D, kFP16>(p, sQ, sK, bars, tmem, abort_flag);
     } else if (warp == C::PV_WARP) {
