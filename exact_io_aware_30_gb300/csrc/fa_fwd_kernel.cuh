@@ -136,7 +136,7 @@ struct Cfg {
     // and stores rows directly.
     static constexpr int O_STAGE_BYTES = (D <= 128) ? Q_BYTES : 0;
     static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES + O_STAGE_BYTES;
-    static constexpr int XCH_BYTES = 2 * kBM * 4;  // one fp32 per row and warpgroup
+    static constexpr int XCH_BYTES = 3 * kBM * 4;  // per row: two sums and the reference max
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 + XCH_BYTES;
     static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
                   "tensor memory overflow");
@@ -498,41 +498,23 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
 
 // ---------------------------------------------------------------- softmax role
 
-// Warp w of softmax warpgroup 0 and warp w of warpgroup 1 own the same 32
-// rows (TMEM lanes); the pair synchronises on named barrier 1 + w, 64 threads.
+// Softmax warp w (0..7) owns the 16 TMEM lanes [32 (w & 3) + 16 (w >> 2), +16)
+// -- 16 query rows -- and every key column of each S tile.  In the 16-lane
+// tcgen05 shapes, thread t holds rows t/4 and t/4 + 8 of that block; a row's
+// columns are spread over the 4 threads of a quad, so its max and sum are
+// combined with two shuffles and the softmax warps never wait for one another
+// during a unit.  The epilogue uses the one-row-per-thread 32x32b shape (warp
+// w: rows 32 (w & 3) + lane, O columns half w >> 2), so the two warps that own
+// a 32-row block meet once per unit on named barrier 1 + (w & 3) to hand each
+// other the row sums.
 constexpr uint32_t kPairBar0 = 1;
 constexpr uint32_t kPairThreads = 64;
 // Barrier of all 256 softmax threads around the staged O tile.
 constexpr uint32_t kEpilogueBar = 5;
 
-// Loads this thread's N score columns (N = 32 or 64) from tensor memory.
-template <int N>
-__device__ __forceinline__ void load_s_cols(uint32_t taddr, uint32_t (&r)[N]) {
-    ptx::tmem_ld_x32<0>(taddr, r);
-    if constexpr (N == 64) ptx::tmem_ld_x32<32>(taddr + 32, r);
-}
-
-// Stores N/2 packed words of P (N 16-bit values) to tensor memory.
-template <int N>
-__device__ __forceinline__ void store_p_cols(uint32_t taddr, const uint32_t (&r)[N / 2]) {
-    if constexpr (N == 64)
-        ptx::tmem_st_x32<0>(taddr, r);
-    else
-        ptx::tmem_st_x16<0>(taddr, r);
-}
-
 template <bool kFP16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
-}
-
-// Hidden keys (columns outside [c_lo, c_hi]) become -inf, whose weight
-// 2^(-inf * c - m) is exactly 0 for the positive exponent scale c.
-template <int N>
-__device__ __forceinline__ void apply_mask(uint32_t (&sr)[N], int c_lo, int c_hi) {
-#pragma unroll
-    for (int i = 0; i < N; ++i)
-        if (i < c_lo || i > c_hi) sr[i] = __float_as_uint(-INFINITY);
 }
 
 // True if some (row, key) pair of this query tile x N keys from kc is hidden.
@@ -545,89 +527,121 @@ __device__ __forceinline__ bool cols_need_mask(int i0, int kc, const Params &p) 
     return false;
 }
 
-// Max of N raw scores (the exponent scale is positive, so it keeps the order).
-template <int N>
-__device__ __forceinline__ float row_max(const uint32_t (&sr)[N]) {
-    float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+// Register e of a thread's NR tile registers (16x256b layout) holds column
+// 8 (e / 4) + 2 tq + (e & 1) of row a (e & 2 == 0) or row b.  Hidden keys --
+// columns outside the row's [lo, hi] -- become -inf, whose weight
+// 2^(-inf * c - m) is exactly 0 for the positive exponent scale c.
+template <int NR>
+__device__ __forceinline__ void quad_mask(uint32_t (&sr)[NR], int tq, int lo_a, int hi_a, int lo_b,
+                                          int hi_b) {
 #pragma unroll
-    for (int i = 2; i < N; i += 4) {
-        mx0 = ptx::max3(mx0, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-        if (i + 3 < N) mx1 = ptx::max3(mx1, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+    for (int e = 0; e < NR; ++e) {
+        const int col = 8 * (e >> 2) + 2 * tq + (e & 1);
+        const bool hid = (e & 2) ? (col < lo_b || col > hi_b) : (col < lo_a || col > hi_a);
+        if (hid) sr[e] = __float_as_uint(-INFINITY);
     }
-    return fmaxf(mx0, mx1);
 }
 
-// p = 2^(s*c - m) for N scores, packed to 16 bits into pk; adds the exact
-// fp32 sum of p to l_exact (for the logsumexp) and, for bf16, the sum of the
-// rounded 16-bit p to l_round: the divisor of O, so that the weights the P V
-// product uses sum exactly to what O is divided by.  bf16 keeps only 8
-// significant bits, enough for a dominant weight's rounding to show in O;
-// fp16's 11 bits make that negligible, so fp16 divides by the exact sum.
-template <int N, bool kFP16>
-__device__ __forceinline__ void row_exp(const uint32_t (&sr)[N], float c, float neg,
-                                        uint32_t (&pk)[N / 2], float &l_exact, float &l_round) {
-    const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(neg, neg);
-    uint64_t le0 = ptx::f32x2(0.f, 0.f), le1 = le0;
-    float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
+// Max over the thread's columns of row a (ma) and row b (mb), then over the
+// quad: every thread of the quad ends with the two full-row maxima.
+template <int NR>
+__device__ __forceinline__ void quad_row_max(const uint32_t (&sr)[NR], float &ma, float &mb) {
+    float a0 = __uint_as_float(sr[0]), a1 = __uint_as_float(sr[1]);
+    float b0 = __uint_as_float(sr[2]), b1 = __uint_as_float(sr[3]);
 #pragma unroll
-    for (int i = 0; i < N; i += 2) {
+    for (int e = 4; e < NR; e += 8) {
+        a0 = ptx::max3(a0, __uint_as_float(sr[e]), __uint_as_float(sr[e + 1]));
+        b0 = ptx::max3(b0, __uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3]));
+        if (e + 4 < NR) {
+            a1 = ptx::max3(a1, __uint_as_float(sr[e + 4]), __uint_as_float(sr[e + 5]));
+            b1 = ptx::max3(b1, __uint_as_float(sr[e + 6]), __uint_as_float(sr[e + 7]));
+        }
+    }
+    ma = fmaxf(a0, a1);
+    mb = fmaxf(b0, b1);
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+}
+
+// p = 2^(s*c - m) for the thread's NR scores (rows a and b, references ma and
+// mb given as na = -ma, nb = -mb), packed to 16 bits into pk in the 16x128b
+// register order (pk[2k] row a, pk[2k+1] row b of packed column 4k + tq).
+// Adds the exact fp32 sums of p to le_a / le_b (for the logsumexp) and to
+// lr_a / lr_b the divisor of O: for bf16 the sum of the rounded 16-bit p, so
+// that the weights the P V product uses sum exactly to what O is divided by
+// (bf16 keeps only 8 significant bits, enough for a dominant weight's
+// rounding to show in O); fp16's 11 bits make that negligible, so fp16
+// divides by the exact sum.
+template <int NR, bool kFP16>
+__device__ __forceinline__ void quad_exp(const uint32_t (&sr)[NR], float c, float na, float nb,
+                                         uint32_t (&pk)[NR / 2], float &le_a, float &le_b,
+                                         float &lr_a, float &lr_b) {
+    const uint64_t c2 = ptx::f32x2(c, c);
+    const uint64_t na2 = ptx::f32x2(na, na), nb2 = ptx::f32x2(nb, nb);
+    uint64_t sa = ptx::f32x2(0.f, 0.f), sb = sa;
+    float ra0 = 0.f, ra1 = 0.f, rb0 = 0.f, rb1 = 0.f;
+#pragma unroll
+    for (int e = 0; e < NR; e += 2) {
+        const bool row_b = (e & 2) != 0;
         float y0, y1;
-        ptx::unpack_f32x2(
-            ptx::fma_f32x2(ptx::f32x2(__uint_as_float(sr[i]), __uint_as_float(sr[i + 1])), c2, n2),
-            y0, y1);
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])),
+                                         c2, row_b ? nb2 : na2),
+                          y0, y1);
         const float e0 = ptx::ex2_approx(y0);
         const float e1 = ptx::ex2_approx(y1);
         const uint32_t pw = pack2<kFP16>(e0, e1);
-        pk[i / 2] = pw;
-        if ((i >> 1) & 1)
-            le1 = ptx::add_f32x2(le1, ptx::f32x2(e0, e1));
+        pk[e / 2] = pw;
+        if (row_b)
+            sb = ptx::add_f32x2(sb, ptx::f32x2(e0, e1));
         else
-            le0 = ptx::add_f32x2(le0, ptx::f32x2(e0, e1));
+            sa = ptx::add_f32x2(sa, ptx::f32x2(e0, e1));
         if constexpr (!kFP16) {
-            float &acc = ((i >> 1) & 3) == 0 ? lr0 : ((i >> 1) & 3) == 1 ? lr1 : ((i >> 1) & 3) == 2 ? lr2 : lr3;
+            const bool odd = (e >> 2) & 1;
+            float &acc = row_b ? (odd ? rb1 : rb0) : (odd ? ra1 : ra0);
             acc = ptx::add_bf16x2_to_f32(pw, acc);
         }
     }
-    float a0, a1;
-    ptx::unpack_f32x2(ptx::add_f32x2(le0, le1), a0, a1);
-    l_exact += a0 + a1;
-    if constexpr (kFP16)
-        l_round += a0 + a1;
-    else
-        l_round += (lr0 + lr1) + (lr2 + lr3);
+    float a0, a1, b0, b1;
+    ptx::unpack_f32x2(sa, a0, a1);
+    ptx::unpack_f32x2(sb, b0, b1);
+    le_a += a0 + a1;
+    le_b += b0 + b1;
+    if constexpr (kFP16) {
+        lr_a += a0 + a1;
+        lr_b += b0 + b1;
+    } else {
+        lr_a += ra0 + ra1;
+        lr_b += rb0 + rb1;
+    }
 }
 
-// Hands v to the partner thread (same row, other warpgroup) and returns the
-// partner's value.  The caller guarantees that the partner has finished
-// reading the previous exchange (a pair barrier lies in between).
-__device__ __forceinline__ float swap_with_partner(float *xch, int h, int r, uint32_t bar, float v) {
-    xch[h * kBM + r] = v;
-    ptx::named_bar_sync(bar, kPairThreads);
-    return xch[(h ^ 1) * kBM + r];
+// Sum over the quad (all 4 threads end with the total).
+__device__ __forceinline__ float quad_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    return v;
 }
 
-// Two softmax warpgroups; thread (h, r) owns row r and key columns
-// [h*HALF, (h+1)*HALF) of every tile, and columns [h*D/2, (h+1)*D/2) of O.
-// Both partners of a row keep the same reference max m_ref: they exchange
-// their half-row maxima whenever the reference is set or moves.
-//
-// The two warps of a pair run the same sequence of pair barriers (the
-// decisions that choose barriers are uniform over the pair), and a pipeline
-// wait that gives up does not leave the loop: the thread carries on through
-// the schedule with whatever tensor memory holds, so that no partner is left
-// at a barrier.  The device status word reports the failure.
 template <int D, bool kFP16>
 __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch, uint8_t *sO,
                              volatile int *abort_flag) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
-    constexpr int HALF = C::HALF;
-    const int h = (int)(threadIdx.x >> 7);                      // key-column half
-    const int r = (int)(threadIdx.x & 127);                     // query row within the tile
-    const uint32_t lane_off = (uint32_t)((r >> 5) * 32) << 16;  // this warp's TMEM lanes
-    const uint32_t pair_bar = kPairBar0 + (uint32_t)(r >> 5);    // barrier shared with the partner warp
-    const uint32_t o_tmem = tmem + lane_off + C::O_COL0 + (uint32_t)(h * (D / 2));
-    const uint32_t p_half = tmem + lane_off + C::P_COL0 + (uint32_t)(h * (HALF / 2));
+    constexpr int NR = BN / 2;  // registers of one S tile per thread: 2 rows x BN/4 columns
+    const int warp = (int)(threadIdx.x >> 5), t = (int)(threadIdx.x & 31);
+    const int qw = warp & 3, hh = warp >> 2;
+    const int tq = t & 3;
+    const int rblk = 32 * qw + 16 * hh;   // first tile row (TMEM lane) of this warp's 16
+    const int ra = rblk + (t >> 2);       // this thread's two rows in the 16-lane shapes
+    const int rb = ra + 8;
+    const uint32_t blk = tmem + ((uint32_t)rblk << 16);
+    const uint32_t o_blk = blk + C::O_COL0;   // all O columns of the 16 rows (rescales)
+    const int re = 32 * qw + t;               // row of the one-row-per-thread epilogue
+    const uint32_t o_tmem = tmem + ((uint32_t)(32 * qw) << 16) + C::O_COL0 + (uint32_t)(hh * (D / 2));
+    const uint32_t pair_bar = kPairBar0 + (uint32_t)qw;
+    float *xl = xch, *xle = xch + kBM, *xm = xch + 2 * kBM;  // per-row sums and reference
     const float c = p.scale_log2;
     uint32_t t_cnt = 0;  // key tiles processed (S buffer = t & 1; one P V each)
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
@@ -636,130 +650,161 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
         const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
-        const int row = un.i0 + r;
-        const bool row_ok = row < p.Sq;
-        const size_t row_flat = ((size_t)(un.b * p.H + un.h)) * (size_t)p.Sq + (size_t)row;
-        uint8_t *ohalf = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2 + (size_t)(h * D);
+        const int row_e = un.i0 + re;
+        const bool row_ok = row_e < p.Sq;
+        const size_t head = (size_t)(un.b * p.H + un.h) * (size_t)p.Sq;
+        const size_t row_flat = head + (size_t)row_e;
+        uint8_t *ohalf = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2 + (size_t)(hh * D);
         if (!un.valid) {
             // No key visible to any row of this tile: guarded output.
             if (row_ok) {
 #pragma unroll
                 for (int cc = 0; cc < D / 16; ++cc) ptx::st_global_v4(ohalf + cc * 16, 0, 0, 0, 0);
-                if (h == 0) p.lse[row_flat] = -INFINITY;
+                if (hh == 0) p.lse[row_flat] = -INFINITY;
             }
             continue;
         }
-        // Visible keys of this row: absolute key indices [key_lo, key_hi].
-        const int key_hi = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row, p.Sk - 1);
-        const int key_lo = (p.mask_kind == kMaskWindow) ? row - p.window + 1 : 0;
+        // Visible keys of rows a and b: absolute key indices [lo, hi].
+        const int row_a = un.i0 + ra, row_b = un.i0 + rb;
+        const int hi_a = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row_a, p.Sk - 1);
+        const int hi_b = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row_b, p.Sk - 1);
+        const int lo_a = (p.mask_kind == kMaskWindow) ? row_a - p.window + 1 : 0;
+        const int lo_b = (p.mask_kind == kMaskWindow) ? row_b - p.window + 1 : 0;
 
-        float m_ref = -INFINITY;  // max the accumulator and sums are referenced to (log2 units)
-        float l = 0.f;            // this half's share of the divisor of O (see row_exp)
-        float l_exact = 0.f;      // this half's fp32 sum of P (for the logsumexp)
+        // Per row: the max the accumulator and sums are referenced to (log2
+        // units), and this thread's share of the divisor of O and of the fp32
+        // sum of P (for the logsumexp).
+        float m_a = -INFINITY, m_b = -INFINITY;
+        float l_a = 0.f, l_b = 0.f, le_a = 0.f, le_b = 0.f;
 
         for (int j = un.lo; j < un.hi; ++j) {
             const int i = j - un.lo;  // step within the unit
-            const uint32_t t = t_cnt++;
-            const int b = (int)(t & 1u);
-            wait_bar(bar_addr(bars, C::B_SFULL + b), (t >> 1) & 1u, abort_flag, 7);
+            const uint32_t tt = t_cnt++;
+            const int b = (int)(tt & 1u);
+            wait_bar(bar_addr(bars, C::B_SFULL + b), (tt >> 1) & 1u, abort_flag, 7);
             ptx::tc_fence_after();
-            uint32_t sr[HALF];
-            load_s_cols<HALF>(tmem + lane_off + (uint32_t)(b * BN + h * HALF), sr);
+            uint32_t sr[NR];
+            ptx::tmem_ld_16x256b_x8<0>(blk + (uint32_t)(b * BN), sr);
+            if constexpr (NR == 64) ptx::tmem_ld_16x256b_x8<32>(blk + (uint32_t)(b * BN) + 64, sr);
             ptx::tmem_wait_ld();
-            ptx::reg_fence<HALF>(sr);
+            ptx::reg_fence<NR>(sr);
             // The S buffer may now be overwritten with tile t+2.
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_SFREE + b));
 
-            const int kc = j * BN + h * HALF;  // first key of this thread's columns
-            if (cols_need_mask<HALF>(un.i0, kc, p)) apply_mask<HALF>(sr, key_lo - kc, key_hi - kc);
+            const int kc = j * BN;  // first key of the tile
+            if (cols_need_mask<BN>(un.i0, kc, p)) quad_mask<NR>(sr, tq, lo_a - kc, hi_a - kc, lo_b - kc, hi_b - kc);
 
-            // A unit's first tile sets the reference from the row max.  Later
-            // tiles exponentiate against the current reference without looking
-            // for the max: a weight above 2^8 (the max grew by more than the
-            // deferral bound) pushes its half's sum above 2^8, so when no half
-            // of any row exceeds the bound every weight is valid as computed.
-            // Otherwise (a vote of the warp pair) the halves exchange their maxima and
-            // each row whose max grew by more than the bound moves its
-            // reference, rescales and exponentiates again.
+            // A unit's first tile sets the references from the row maxima.
+            // Later tiles exponentiate against the current references without
+            // looking for the max: a weight above 2^8 (the max grew by more
+            // than the deferral bound) pushes its thread's partial sum above
+            // 2^8, so when no thread of the warp exceeds the bound every weight
+            // is valid as computed.  Otherwise the warp takes the row maxima,
+            // and each row whose max grew by more than the bound moves its
+            // reference, rescales and is exponentiated again.
             const bool first = (i == 0);
             if (first) {
-                const float hm = row_max<HALF>(sr);
-                ptx::named_bar_sync(pair_bar, kPairThreads);  // previous exchange fully read
-                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, pair_bar, hm));
-                m_ref = (mx == -INFINITY) ? -INFINITY : mx * c;
+                float ma, mb;
+                quad_row_max<NR>(sr, ma, mb);
+                m_a = (ma == -INFINITY) ? -INFINITY : ma * c;
+                m_b = (mb == -INFINITY) ? -INFINITY : mb * c;
             }
-            uint32_t pk[HALF / 2];
-            float le_t, lr_t;  // this tile's exact and rounded sums (this half)
-            float alpha = 1.f;
+            uint32_t pk[NR / 2];
+            float le_at, le_bt, lr_at, lr_bt;  // this tile's sums (this thread's columns)
+            float alpha_a = 1.f, alpha_b = 1.f;
             bool rescale = false;
 #pragma unroll 1
             for (int pass = 0;; ++pass) {
-                le_t = 0.f;
-                lr_t = 0.f;
-                row_exp<HALF, kFP16>(sr, c, (m_ref == -INFINITY) ? 0.f : -m_ref, pk, le_t, lr_t);
+                le_at = le_bt = lr_at = lr_bt = 0.f;
+                quad_exp<NR, kFP16>(sr, c, (m_a == -INFINITY) ? 0.f : -m_a,
+                                    (m_b == -INFINITY) ? 0.f : -m_b, pk, le_at, le_bt, lr_at, lr_bt);
                 if (first || pass > 0) break;
                 // No reference yet (every earlier key of the row hidden) counts
                 // as exceeding the bound as soon as a key is visible.
-                const bool over = !(le_t <= kRescaleBound) || (m_ref == -INFINITY && le_t != 0.f);
-                if (!ptx::named_bar_any(pair_bar, kPairThreads, over)) break;
-                const float hm = row_max<HALF>(sr);
-                const float mx = fmaxf(hm, swap_with_partner(xch, h, r, pair_bar, hm));
-                const float m_new = fmaxf(m_ref, (mx == -INFINITY) ? -INFINITY : mx * c);
-                if (!(m_new > m_ref + kRescaleLog2)) break;  // weights within the bound
-                alpha = ptx::ex2_approx(m_ref - m_new);      // 0 while m_ref is -inf
-                m_ref = m_new;
+                const bool over = !(le_at <= kRescaleBound) || !(le_bt <= kRescaleBound) ||
+                                  (m_a == -INFINITY && le_at != 0.f) ||
+                                  (m_b == -INFINITY && le_bt != 0.f);
+                if (!__any_sync(0xffffffffu, over)) break;
+                float ma, mb;
+                quad_row_max<NR>(sr, ma, mb);
+                const float na = fmaxf(m_a, (ma == -INFINITY) ? -INFINITY : ma * c);
+                const float nb = fmaxf(m_b, (mb == -INFINITY) ? -INFINITY : mb * c);
+                const bool up_a = na > m_a + kRescaleLog2, up_b = nb > m_b + kRescaleLog2;
+                if (!__any_sync(0xffffffffu, up_a || up_b)) break;  // weights within the bound
+                if (up_a) {
+                    alpha_a = ptx::ex2_approx(m_a - na);  // 0 while m_a is -inf
+                    m_a = na;
+                }
+                if (up_b) {
+                    alpha_b = ptx::ex2_approx(m_b - nb);
+                    m_b = nb;
+                }
                 rescale = true;
             }
             // O barrier b completes once for each tile whose P sits in area b:
             // completion k of barrier t & 1 is P V of tile t with k = t >> 1.
             // Rescaling O needs every earlier P V finished: wait for P V of tile
             // t-1 (a commit covers all earlier MMAs of its issuer).  Rewriting P
-            // area t & 1 needs P V of tile t-2.  The P V of the unit's previous
-            // unit are covered by its final barrier.  Each barrier's next
-            // completion needs a P this thread has not written yet, and the one
-            // before was waited for two tiles ago, so the parity waits are
-            // unambiguous.
-            const uint32_t pb = t & 1u;
-            if (__any_sync(0xffffffffu, rescale)) {
+            // area t & 1 needs P V of tile t-2.  The P V of the previous unit
+            // are covered by its final barrier.  Each barrier's next completion
+            // needs a P this thread has not written yet, and the one before was
+            // waited for two tiles ago, so the parity waits are unambiguous.
+            const uint32_t pb = tt & 1u;
+            if (rescale) {  // warp-uniform
                 if (i > 0)
-                    wait_bar(bar_addr(bars, C::B_OFULL + (int)((t - 1u) & 1u)), ((t - 1u) >> 1) & 1u,
+                    wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u,
                              abort_flag, 8);
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc) {
                     uint32_t ov[32];
-                    ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+                    ptx::tmem_ld_16x256b_x8<0>(o_blk + cc * 64, ov);
                     ptx::tmem_wait_ld();
                     ptx::reg_fence<32>(ov);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-                    ptx::tmem_st_x32<0>(o_tmem + cc * 32, ov);
+                    for (int e = 0; e < 32; ++e)
+                        ov[e] = __float_as_uint(__uint_as_float(ov[e]) * ((e & 2) ? alpha_b : alpha_a));
+                    ptx::tmem_st_16x256b_x8<0>(o_blk + cc * 64, ov);
                 }
             }
-            l = alpha * l + lr_t;
-            l_exact = alpha * l_exact + le_t;
+            l_a = alpha_a * l_a + lr_at;
+            l_b = alpha_b * l_b + lr_bt;
+            le_a = alpha_a * le_a + le_at;
+            le_b = alpha_b * le_b + le_bt;
             if (i >= 2)
-                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((t >> 1) - 1u) & 1u, abort_flag, 10);
+                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, abort_flag, 10);
             ptx::tc_fence_after();
-            store_p_cols<HALF>(p_half + pb * C::P_STRIDE, pk);
+            if constexpr (NR == 64)
+                ptx::tmem_st_16x128b_x16<0>(blk + C::P_COL0 + pb * C::P_STRIDE, pk);
+            else
+                ptx::tmem_st_16x128b_x8<0>(blk + C::P_COL0 + pb * C::P_STRIDE, pk);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + (int)pb));
         }
 
-        // Epilogue: wait for the unit's last P V, combine the halves' sums,
-        // divide by l once, store this half of the O row (and lse).
+        // Epilogue: wait for the unit's last P V; full-row sums over the quad,
+        // handed through shared memory to the one-row-per-thread layout; divide
+        // by l once; store this warp's half of the O row (and lse).
         wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9);
         ++u_cnt;
         ptx::tc_fence_after();
-        ptx::named_bar_sync(pair_bar, kPairThreads);  // previous exchange fully read
-        const float l_all = l + swap_with_partner(xch, h, r, pair_bar, l);
-        float le_all = l_all;
-        if constexpr (!kFP16) {
+        {
+            const float sa = quad_sum(l_a), sb = quad_sum(l_b);
+            const float ea = kFP16 ? sa : quad_sum(le_a), eb = kFP16 ? sb : quad_sum(le_b);
+            ptx::named_bar_sync(pair_bar, kPairThreads);  // the previous unit's values fully read
+            if (tq == 0) {
+                xl[ra] = sa;
+                xl[rb] = sb;
+                xle[ra] = ea;
+                xle[rb] = eb;
+                xm[ra] = m_a;
+                xm[rb] = m_b;
+            }
             ptx::named_bar_sync(pair_bar, kPairThreads);
-            le_all = l_exact + swap_with_partner(xch, h, r, pair_bar, l_exact);
         }
+        const float l_all = xl[re], le_all = xle[re], m_ref = xm[re];
         const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
         if constexpr (C::O_STAGE_BYTES > 0) {
             // Normalise this thread's D/2 columns of O into registers, release
@@ -785,11 +830,11 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             if (threadIdx.x == 0) ptx::bulk_wait_read_all();  // the previous tile has left sO
             ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
 #pragma unroll
-            for (int c = 0; c < D / 16; ++c) {
-                const int col = h * (D / 2) + c * 8;  // first of the chunk's 8 columns
-                const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + r * 128 +
-                                                      ((((col & 63) >> 3) ^ (r & 7)) << 4));
-                ptx::st_shared_v4(addr, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            for (int cidx = 0; cidx < D / 16; ++cidx) {
+                const int col = hh * (D / 2) + cidx * 8;  // first of the chunk's 8 columns
+                const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + re * 128 +
+                                                      ((((col & 63) >> 3) ^ (re & 7)) << 4));
+                ptx::st_shared_v4(addr, w[4 * cidx], w[4 * cidx + 1], w[4 * cidx + 2], w[4 * cidx + 3]);
             }
             ptx::fence_proxy_async_smem();
             ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
@@ -827,7 +872,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
         }
-        if (row_ok && h == 0)
+        if (row_ok && hh == 0)
             p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
     }
     if constexpr (C::O_STAGE_BYTES > 0) {
