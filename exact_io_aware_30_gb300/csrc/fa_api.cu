@@ -291,6 +291,17 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     // of a zero scale.
     p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
     p.o_vec8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
+    p.wait_limit_ns = fa::kWaitLimitNs;
+    // Test hook: FA_DEBUG_STALL_MS=N makes the launch's first softmax wait
+    // one that nothing completes, with N ms as the wait limit, so that the
+    // bounded-wait path can be exercised without any fault.
+    if (const char *e = std::getenv("FA_DEBUG_STALL_MS")) {
+        const long ms = std::strtol(e, nullptr, 10);
+        if (ms > 0 && ms <= 10000) {
+            p.stall_test = 1;
+            p.wait_limit_ns = (uint64_t)ms * 1000000ull;
+        }
+    }
     p.n_qtiles = (Sq + 127) / 128;
     p.n_units = B * H * p.n_qtiles;
     p.heads_per_group = heads_per_group(p, d, info->l2_bytes);

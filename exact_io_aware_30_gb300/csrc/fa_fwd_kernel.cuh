@@ -50,10 +50,17 @@ constexpr int kBM = 128;  // query rows per tile = M of every MMA = TMEM lanes
 constexpr int kMaskNone = 0;
 constexpr int kMaskCausal = 1;
 constexpr int kMaskWindow = 2;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a pipeline wait gives up after 2 s
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // default limit of a pipeline wait: 2 s
 constexpr float kRescaleLog2 = 8.0f;              // rescale O when the max grows > 2^8
 constexpr float kRescaleBound = 256.0f;           // 2^kRescaleLog2
 constexpr float kLn2 = 0.693147180559945309f;
+
+// Per-CTA control block in shared memory.
+struct Ctl {
+    volatile int abort;  // a role gave up waiting: the others stop too
+    int pad;
+    uint64_t limit_ns;   // how long a pipeline wait may take
+};
 
 // Device status word: 0 = fine; else 0x100 + the wait site that timed out.
 // (This header is compiled into exactly one translation unit.)
@@ -76,6 +83,8 @@ struct Params {
     int n_units;       // B * H * n_qtiles
     int heads_per_group;  // (batch, head) pairs scheduled together (K/V kept in L2)
     int o_vec8;        // O is 32-byte aligned: 32-byte stores
+    uint64_t wait_limit_ns;  // limit of every pipeline wait
+    int stall_test;          // test only: the softmax's first wait is on a barrier nothing completes
     // Schedule: with sched = 1, CTA c runs units sched_ids[sched_off[c] ..
     // sched_off[c+1]) in that order (built on the host); else the snake order.
     int sched;
@@ -130,14 +139,15 @@ struct Cfg {
     static constexpr int B_OFINAL = B_OFULL + 2;        // one phase per unit: last P V done
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
-    static constexpr int NUM_BARS = B_DRAIN + 2;
+    static constexpr int B_NEVER = B_DRAIN + 2;         // no arrivals (the stall test's wait)
+    static constexpr int NUM_BARS = B_NEVER + 1;
     // d <= 128: the epilogue stages the normalised O tile (the Q tile's shape)
     // in shared memory for one bulk tensor store; d = 256 has no room for it
     // and stores rows directly.
     static constexpr int O_STAGE_BYTES = (D <= 128) ? Q_BYTES : 0;
     static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES + O_STAGE_BYTES;
     static constexpr int XCH_BYTES = 3 * kBM * 4;  // per row: two sums and the reference max
-    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 16 + XCH_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 24 + XCH_BYTES;
     static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
                   "tensor memory overflow");
     static_assert(BN / 2 <= (int)P_STRIDE, "P areas overlap");
@@ -167,38 +177,39 @@ __host__ __device__ constexpr uint32_t make_idesc(int M, int N, bool fp16, bool 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
 
 // Bounded wait: gives up (and raises the abort flag and the device status
-// word) after kWaitLimitNs, or as soon as another role has aborted.
-__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+// word) after the control block's limit, or as soon as another role has
+// aborted.
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, Ctl *ctl,
                                            int site) {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
+        if (ctl->abort) return false;
+        if (ptx::globaltimer_ns() - t0 > ctl->limit_ns) {
+            ctl->abort = 1;
             atomicCAS(&g_fa_status, 0, 0x100 + site);
             return false;
         }
     }
 }
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl *ctl,
                                          int site) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    return wait_bar_slow(bar, parity, abort_flag, site);
+    return wait_bar_slow(bar, parity, ctl, site);
 }
 
 // Same bounded wait for the TMA producers, whose waits are off the critical
 // path: a short sleep between polls leaves the issue slots of the
 // sub-partition to the softmax warps that share it.
-__device__ __noinline__ bool wait_bar_backoff(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+__device__ __noinline__ bool wait_bar_backoff(uint32_t bar, uint32_t parity, Ctl *ctl,
                                               int site) {
     const uint64_t t0 = ptx::globaltimer_ns();
     for (;;) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
-            *abort_flag = 1;
+        if (ctl->abort) return false;
+        if (ptx::globaltimer_ns() - t0 > ctl->limit_ns) {
+            ctl->abort = 1;
             atomicCAS(&g_fa_status, 0, 0x100 + site);
             return false;
         }
@@ -274,11 +285,11 @@ template <int D>
 __device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *ring, uint32_t bars,
                                              int full0, int empty0, int nslots, uint32_t &it,
                                              int key0, const Unit &un, bool leader, uint64_t pol,
-                                             volatile int *abort_flag) {
+                                             Ctl *ctl) {
     using C = Cfg<D>;
     const uint32_t slot = it % (uint32_t)nslots;
     if (!wait_bar_backoff(bar_addr(bars, empty0 + (int)slot), ((it / (uint32_t)nslots) & 1) ^ 1,
-                          abort_flag, 2))
+                          ctl, 2))
         return false;
     if (leader) {
         const uint32_t fb = bar_addr(bars, full0 + (int)slot);
@@ -305,7 +316,7 @@ __device__ __forceinline__ void drain_ring(uint32_t bars, int full0, int nslots,
 // V has its own producer warp, so a key tile never waits behind a value slot.
 template <int D>
 __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t bars,
-                            volatile int *abort_flag) {
+                            Ctl *ctl) {
     using C = Cfg<D>;
     const bool leader = ptx::lane_id() == 0;
     const uint64_t pol_kv = ptx::policy_evict_last();
@@ -318,7 +329,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
-        if (!wait_bar_backoff(bar_addr(bars, C::B_QEMPTY), (q_cnt & 1) ^ 1, abort_flag, 1)) {
+        if (!wait_bar_backoff(bar_addr(bars, C::B_QEMPTY), (q_cnt & 1) ^ 1, ctl, 1)) {
             ok = false;
             break;
         }
@@ -333,7 +344,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
         ++q_cnt;
         for (int j = un.lo; j < un.hi && ok; ++j)
             ok = load_kv_tile<D>(&p.tm_k, sK, bars, C::B_KFULL, C::B_KEMPTY, C::KST, k_it, j * C::BN, un,
-                                 leader, pol_kv, abort_flag);
+                                 leader, pol_kv, ctl);
     }
     if (!ok) {  // let every copy already issued land before the CTA can exit
         drain_ring(bars, C::B_KFULL, C::KST, k_it);
@@ -343,7 +354,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
 
 // V producer: the units' value tiles in order.
 template <int D>
-__device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, volatile int *abort_flag) {
+__device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, Ctl *ctl) {
     using C = Cfg<D>;
     const bool leader = ptx::lane_id() == 0;
     const uint64_t pol_kv = ptx::policy_evict_last();
@@ -356,7 +367,7 @@ __device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, volatile
         if (!un.valid) continue;
         for (int j = un.lo; j < un.hi && ok; ++j)
             ok = load_kv_tile<D>(&p.tm_v, sV, bars, C::B_VFULL, C::B_VEMPTY, C::VST, v_it, j * C::BN, un,
-                                 leader, pol_kv, abort_flag);
+                                 leader, pol_kv, ctl);
     }
     if (!ok) drain_ring(bars, C::B_VFULL, C::VST, v_it);
 }
@@ -367,7 +378,7 @@ __device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, volatile
 // the softmax has read that buffer's previous tile.
 template <int D, bool kFP16>
 __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t bars,
-                           uint32_t tmem, volatile int *abort_flag) {
+                           uint32_t tmem, Ctl *ctl) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
@@ -385,17 +396,17 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
-        if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, abort_flag, 6)) { ok = false; break; }
+        if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, ctl, 6)) { ok = false; break; }
         for (int i = 0; i < n; ++i, ++k_it) {
             const uint32_t t = t_cnt + (uint32_t)i;
             const uint32_t slot = k_it % C::KST;
             const uint32_t b = t & 1u;
-            if (!wait_bar(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, abort_flag, 3)) {
+            if (!wait_bar(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, ctl, 3)) {
                 ok = false;
                 break;
             }
             if (t >= 2 &&  // the softmax has read tile t-2 out of this buffer
-                !wait_bar(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1u) & 1u, abort_flag, 12)) {
+                !wait_bar(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1u) & 1u, ctl, 12)) {
                 ok = false;
                 break;
             }
@@ -429,7 +440,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
 // written P.
 template <int D, bool kFP16>
 __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_t tmem,
-                            volatile int *abort_flag) {
+                            Ctl *ctl) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
@@ -452,7 +463,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
         for (int i = 0; i < n; ++i, ++v_it) {
             const uint32_t t = t_cnt + (uint32_t)i;
             const uint32_t slot = v_it % C::VST;
-            if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, abort_flag, 3)) {
+            if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, ctl, 3)) {
                 ok = false;
                 break;
             }
@@ -460,13 +471,13 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
             // two tiles, and the softmax cannot write P of tile t+2 before this
             // P V has run, so the parity wait is unambiguous.
             const uint32_t pb = t & 1u;
-            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, abort_flag, 4)) {
+            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, ctl, 4)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             if (i == 0 && o_used) {
-                if (!wait_bar(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, abort_flag, 5)) {
+                if (!wait_bar(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, ctl, 5)) {
                     ok = false;
                     break;
                 }
@@ -626,7 +637,7 @@ __device__ __forceinline__ float quad_sum(float v) {
 
 template <int D, bool kFP16>
 __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch, uint8_t *sO,
-                             volatile int *abort_flag) {
+                             Ctl *ctl) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr int NR = BN / 2;  // registers of one S tile per thread: 2 rows x BN/4 columns
@@ -681,7 +692,11 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             const int i = j - un.lo;  // step within the unit
             const uint32_t tt = t_cnt++;
             const int b = (int)(tt & 1u);
-            wait_bar(bar_addr(bars, C::B_SFULL + b), (tt >> 1) & 1u, abort_flag, 7);
+            // (Under the stall test the CTA's first wait is on a barrier no one
+            // arrives at: it runs out, and the kernel winds down with the
+            // device status word set.)
+            wait_bar(bar_addr(bars, (p.stall_test && tt == 0) ? C::B_NEVER : C::B_SFULL + b),
+                     (tt >> 1) & 1u, ctl, 7);
             ptx::tc_fence_after();
             uint32_t sr[NR];
             ptx::tmem_ld_16x256b_x8<0>(blk + (uint32_t)(b * BN), sr);
@@ -754,7 +769,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             if (rescale) {  // warp-uniform
                 if (i > 0)
                     wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u,
-                             abort_flag, 8);
+                             ctl, 8);
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc) {
@@ -773,7 +788,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             le_a = alpha_a * le_a + le_at;
             le_b = alpha_b * le_b + le_bt;
             if (i >= 2)
-                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, abort_flag, 10);
+                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, ctl, 10);
             ptx::tc_fence_after();
             if constexpr (NR == 64)
                 ptx::tmem_st_16x128b_x16<0>(blk + C::P_COL0 + pb * C::P_STRIDE, pk);
@@ -787,7 +802,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
         // Epilogue: wait for the unit's last P V; full-row sums over the quad,
         // handed through shared memory to the one-row-per-thread layout; divide
         // by l once; store this warp's half of the O row (and lse).
-        wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, abort_flag, 9);
+        wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, ctl, 9);
         ++u_cnt;
         ptx::tc_fence_after();
         {
@@ -895,8 +910,8 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint8_t *sO = sV + C::VST * C::TILE_BYTES;  // O staging (d <= 128)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
-    float *xch = reinterpret_cast<float *>(tmem_holder + 4);
+    Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);    // 8-byte aligned
+    float *xch = reinterpret_cast<float *>(tmem_holder + 6);
     const uint32_t bars = ptx::smem_addr(bar_mem);
 
     const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
@@ -925,7 +940,9 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_OFREE), C::NUM_SOFTMAX);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
-        *abort_flag = 0;
+        ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
+        ctl->abort = 0;
+        ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();
         ptx::fence_proxy_async_smem();
     }
@@ -945,15 +962,15 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp < C::NUM_SOFTMAX / 32) {
-        softmax_role<D, kFP16>(p, bars, tmem, xch, sO, abort_flag);
+        softmax_role<D, kFP16>(p, bars, tmem, xch, sO, ctl);
     } else if (warp == C::S_WARP) {
-        mma_s_role<D, kFP16>(p, sQ, sK, bars, tmem, abort_flag);
+        mma_s_role<D, kFP16>(p, sQ, sK, bars, tmem, ctl);
     } else if (warp == C::PV_WARP) {
-        mma_pv_role<D, kFP16>(p, sV, bars, tmem, abort_flag);
+        mma_pv_role<D, kFP16>(p, sV, bars, tmem, ctl);
     } else if (warp == C::TMA_WARP) {
-        tma_qk_role<D>(p, sQ, sK, bars, abort_flag);
+        tma_qk_role<D>(p, sQ, sK, bars, ctl);
     } else {
-        tma_v_role<D>(p, sV, bars, abort_flag);
+        tma_v_role<D>(p, sV, bars, ctl);
     }
     __syncwarp();
     ptx::tc_fence_before();

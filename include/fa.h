@@ -115,6 +115,11 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len);
  * current device that kernels set when a pipeline wait times out.  The
  * caller synchronises the stream first.  FA_OK if no kernel raised it,
  * FA_ERR_DEVICE_TIMEOUT if one did, FA_ERR_CUDA if it cannot be read.
+ * A kernel that times out stops its pipeline and finishes normally (its O
+ * and lse are then undefined); the context stays usable.  For testing that
+ * path, the environment variable FA_DEBUG_STALL_MS=N (1..10000) makes each
+ * launch's first softmax wait one that nothing completes, with a limit of
+ * N ms instead of about 2 s.
  */
 fa_status fa_get_device_error(void);
 
