@@ -635,6 +635,111 @@ __device__ __forceinline__ float quad_sum(float v) {
     return v;
 }
 
+// A unit's epilogue: wait for its last P V; full-row sums over the quad,
+// handed through shared memory to the one-row-per-thread layout; divide by l
+// once; store this warp's half of the O row (and lse).
+template <int D, bool kFP16>
+__device__ __noinline__ void softmax_epilogue(const Params &p, uint32_t bars, Ctl *ctl, float *xch,
+                                              uint8_t *sO, uint32_t o_tmem, uint32_t u_cnt, int i0,
+                                              int hd, int bt, size_t row_flat, bool row_ok,
+                                              uint8_t *ohalf, float m_a, float m_b, float l_a,
+                                              float l_b, float le_a, float le_b) {
+    using C = Cfg<D>;
+    const int warp = (int)(threadIdx.x >> 5), t = (int)(threadIdx.x & 31);
+    const int qw = warp & 3, hh = warp >> 2;
+    const int tq = t & 3;
+    const int ra = 32 * qw + 16 * hh + (t >> 2), rb = ra + 8;
+    const int re = 32 * qw + t;
+    const uint32_t pair_bar = kPairBar0 + (uint32_t)qw;
+    float *xl = xch, *xle = xch + kBM, *xm = xch + 2 * kBM;
+    wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, ctl, 9);  // u_cnt: units finished before
+    ptx::tc_fence_after();
+    {
+        const float sa = quad_sum(l_a), sb = quad_sum(l_b);
+        const float ea = kFP16 ? sa : quad_sum(le_a), eb = kFP16 ? sb : quad_sum(le_b);
+        ptx::named_bar_sync(pair_bar, kPairThreads);  // the previous unit's values fully read
+        if (tq == 0) {
+            xl[ra] = sa;
+            xl[rb] = sb;
+            xle[ra] = ea;
+            xle[rb] = eb;
+            xm[ra] = m_a;
+            xm[rb] = m_b;
+        }
+        ptx::named_bar_sync(pair_bar, kPairThreads);
+    }
+    const float l_all = xl[re], le_all = xle[re], m_ref = xm[re];
+    const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+    if constexpr (C::O_STAGE_BYTES > 0) {
+        // Normalise this thread's D/2 columns of O into registers, release
+        // O to the next unit's P V, then stage the tile in shared memory in
+        // the tensor map's layout (64-column boxes of 128-byte rows, 16-byte
+        // chunks swizzled by row & 7) and write it with one bulk store.
+        // Rows past Sq fall outside the tensor and are not written.
+        uint32_t w[D / 4];
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[cc * 16 + e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
+                                              __uint_as_float(ov[2 * e + 1]) * inv_l);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+        const uint32_t so = ptx::smem_addr(sO);
+        if (threadIdx.x == 0) ptx::bulk_wait_read_all();  // the previous tile has left sO
+        ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
+#pragma unroll
+        for (int cidx = 0; cidx < D / 16; ++cidx) {
+            const int col = hh * (D / 2) + cidx * 8;  // first of the chunk's 8 columns
+            const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + re * 128 +
+                                                  ((((col & 63) >> 3) ^ (re & 7)) << 4));
+            ptx::st_shared_v4(addr, w[4 * cidx], w[4 * cidx + 1], w[4 * cidx + 2], w[4 * cidx + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int bx = 0; bx < D / 64; ++bx)
+                ptx::tma_store_4d(&p.tm_o, so + bx * (kBM * 128), bx * 64, i0, hd, bt);
+            ptx::bulk_commit_group();
+        }
+    } else {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(ov);
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
+                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
+            if (row_ok) {
+                uint8_t *dst = ohalf + cc * 64;
+                if (p.o_vec8) {
+                    ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+                    ptx::st_global_v8(dst + 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+                } else {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        ptx::st_global_v4(dst + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                          w[4 * v4 + 3]);
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+    }
+    if (row_ok && hh == 0)
+        p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
+}
+
 template <int D, bool kFP16>
 __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch, uint8_t *sO,
                              Ctl *ctl) {
@@ -651,8 +756,6 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
     const uint32_t o_blk = blk + C::O_COL0;   // all O columns of the 16 rows (rescales)
     const int re = 32 * qw + t;               // row of the one-row-per-thread epilogue
     const uint32_t o_tmem = tmem + ((uint32_t)(32 * qw) << 16) + C::O_COL0 + (uint32_t)(hh * (D / 2));
-    const uint32_t pair_bar = kPairBar0 + (uint32_t)qw;
-    float *xl = xch, *xle = xch + kBM, *xm = xch + 2 * kBM;  // per-row sums and reference
     const float c = p.scale_log2;
     uint32_t t_cnt = 0;  // key tiles processed (S buffer = t & 1; one P V each)
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
@@ -799,96 +902,11 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + (int)pb));
         }
 
-        // Epilogue: wait for the unit's last P V; full-row sums over the quad,
-        // handed through shared memory to the one-row-per-thread layout; divide
-        // by l once; store this warp's half of the O row (and lse).
-        wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, ctl, 9);
+        // Epilogue, out of line: it runs once per unit, and keeping it out of
+        // the tile loop keeps the loop's code compact.
+        softmax_epilogue<D, kFP16>(p, bars, ctl, xch, sO, o_tmem, u_cnt, un.i0, un.h, un.b, row_flat,
+                                   row_ok, ohalf, m_a, m_b, l_a, l_b, le_a, le_b);
         ++u_cnt;
-        ptx::tc_fence_after();
-        {
-            const float sa = quad_sum(l_a), sb = quad_sum(l_b);
-            const float ea = kFP16 ? sa : quad_sum(le_a), eb = kFP16 ? sb : quad_sum(le_b);
-            ptx::named_bar_sync(pair_bar, kPairThreads);  // the previous unit's values fully read
-            if (tq == 0) {
-                xl[ra] = sa;
-                xl[rb] = sb;
-                xle[ra] = ea;
-                xle[rb] = eb;
-                xm[ra] = m_a;
-                xm[rb] = m_b;
-            }
-            ptx::named_bar_sync(pair_bar, kPairThreads);
-        }
-        const float l_all = xl[re], le_all = xle[re], m_ref = xm[re];
-        const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
-        if constexpr (C::O_STAGE_BYTES > 0) {
-            // Normalise this thread's D/2 columns of O into registers, release
-            // O to the next unit's P V, then stage the tile in shared memory in
-            // the tensor map's layout (64-column boxes of 128-byte rows, 16-byte
-            // chunks swizzled by row & 7) and write it with one bulk store.
-            // Rows past Sq fall outside the tensor and are not written.
-            uint32_t w[D / 4];
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t ov[32];
-                ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence<32>(ov);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[cc * 16 + e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
-                                                  __uint_as_float(ov[2 * e + 1]) * inv_l);
-            }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
-            const uint32_t so = ptx::smem_addr(sO);
-            if (threadIdx.x == 0) ptx::bulk_wait_read_all();  // the previous tile has left sO
-            ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
-#pragma unroll
-            for (int cidx = 0; cidx < D / 16; ++cidx) {
-                const int col = hh * (D / 2) + cidx * 8;  // first of the chunk's 8 columns
-                const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + re * 128 +
-                                                      ((((col & 63) >> 3) ^ (re & 7)) << 4));
-                ptx::st_shared_v4(addr, w[4 * cidx], w[4 * cidx + 1], w[4 * cidx + 2], w[4 * cidx + 3]);
-            }
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
-            if (threadIdx.x == 0) {
-#pragma unroll
-                for (int bx = 0; bx < D / 64; ++bx)
-                    ptx::tma_store_4d(&p.tm_o, so + bx * (kBM * 128), bx * 64, un.i0, un.h, un.b);
-                ptx::bulk_commit_group();
-            }
-        } else {
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-                uint32_t ov[32];
-                ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence<32>(ov);
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
-                                        __uint_as_float(ov[2 * e + 1]) * inv_l);
-                if (row_ok) {
-                    uint8_t *dst = ohalf + cc * 64;
-                    if (p.o_vec8) {
-                        ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
-                        ptx::st_global_v8(dst + 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
-                    } else {
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4)
-                            ptx::st_global_v4(dst + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
-                                              w[4 * v4 + 3]);
-                    }
-                }
-            }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
-        }
-        if (row_ok && hh == 0)
-            p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
     }
     if constexpr (C::O_STAGE_BYTES > 0) {
         if (threadIdx.x == 0) ptx::bulk_wait_all();  // sO must outlive the stores
