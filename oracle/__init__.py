@@ -78,6 +78,19 @@ def _mask(mask) -> int:
     return int(mask)
 
 
+def _shapes(q: np.ndarray, k: np.ndarray, v: np.ndarray):
+    """(B, H, Sq, d, Hkv, Sk) of q [B,H,Sq,d] and k, v [B,Hkv,Sk,d]."""
+    if q.ndim != 4 or k.ndim != 4:
+        raise ValueError("q, k, v must be 4-D [B,heads,S,d]")
+    B, H, Sq, d = q.shape
+    Hkv, Sk = k.shape[1], k.shape[2]
+    if k.shape != (B, Hkv, Sk, d) or v.shape != (B, Hkv, Sk, d):
+        raise ValueError("k and v must be [B,Hkv,Sk,d] matching q")
+    if Hkv < 1 or H % Hkv != 0:
+        raise ValueError("the K/V head count must divide the query head count")
+    return B, H, Sq, d, Hkv, Sk
+
+
 class OracleLib:
     """ctypes front end of one compiled oracle library."""
 
@@ -86,13 +99,13 @@ class OracleLib:
         lib.oracle_attn_naive.restype = ctypes.c_int
         lib.oracle_attn_naive.argtypes = [
             _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
             _i64p, ctypes.c_int64, _dp, _dp]
         lib.oracle_attn_blocked.restype = ctypes.c_int
         lib.oracle_attn_blocked.argtypes = [
             _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-            _dp, _dp]
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, _dp, _dp]
         lib.oracle_online_trace.restype = ctypes.c_int
         lib.oracle_online_trace.argtypes = [
             _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
@@ -117,27 +130,26 @@ class OracleLib:
     def attention(self, q, k, v, scale: float, mask="none", window: int = 0, rows=None):
         """Naive fp64 attention.
 
-        q: [B,H,Sq,d], k, v: [B,H,Sk,d].  Returns (o, lse): o is [B,H,Sq,d]
+        q: [B,H,Sq,d], k, v: [B,Hkv,Sk,d] with Hkv dividing H (grouped-query
+        attention: query head h reads K/V head h // (H // Hkv); Hkv == H is
+        plain multi-head attention).  Returns (o, lse): o is [B,H,Sq,d]
         and lse [B,H,Sq] when ``rows`` is None; otherwise ``rows`` lists flat
         query-row indices (b*H + h)*Sq + i and o is [len(rows), d], lse
         [len(rows)].
         """
         q, k, v = _f64(q), _f64(k), _f64(v)
-        B, H, Sq, d = q.shape
-        Sk = k.shape[2]
-        if k.shape != (B, H, Sk, d) or v.shape != (B, H, Sk, d):
-            raise ValueError("k and v must be [B,H,Sk,d] matching q")
+        B, H, Sq, d, Hkv, Sk = _shapes(q, k, v)
         if rows is None:
             o = np.empty((B, H, Sq, d), np.float64)
             lse = np.empty((B, H, Sq), np.float64)
-            rc = self.lib.oracle_attn_naive(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Sk, d,
+            rc = self.lib.oracle_attn_naive(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, Sq, Sk, d,
                                             float(scale), _mask(mask), int(window), None, 0,
                                             _ptr(o), _ptr(lse))
         else:
             r = np.ascontiguousarray(rows, dtype=np.int64)
             o = np.empty((r.size, d), np.float64)
             lse = np.empty((r.size,), np.float64)
-            rc = self.lib.oracle_attn_naive(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Sk, d,
+            rc = self.lib.oracle_attn_naive(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, Sq, Sk, d,
                                             float(scale), _mask(mask), int(window),
                                             r.ctypes.data_as(_i64p), r.size, _ptr(o), _ptr(lse))
         if rc != 0:
@@ -146,13 +158,14 @@ class OracleLib:
 
     def attention_blocked(self, q, k, v, scale: float, mask="none", window: int = 0,
                           block_size: int = 2):
-        """Blocked online-softmax fp64 attention (second, independent form)."""
+        """Blocked online-softmax fp64 attention (second, independent form).
+
+        Shapes as in ``attention`` (K/V may have fewer heads than Q)."""
         q, k, v = _f64(q), _f64(k), _f64(v)
-        B, H, Sq, d = q.shape
-        Sk = k.shape[2]
+        B, H, Sq, d, Hkv, Sk = _shapes(q, k, v)
         o = np.empty((B, H, Sq, d), np.float64)
         lse = np.empty((B, H, Sq), np.float64)
-        rc = self.lib.oracle_attn_blocked(_ptr(q), _ptr(k), _ptr(v), B, H, Sq, Sk, d,
+        rc = self.lib.oracle_attn_blocked(_ptr(q), _ptr(k), _ptr(v), B, H, Hkv, Sq, Sk, d,
                                           float(scale), _mask(mask), int(window),
                                           int(block_size), _ptr(o), _ptr(lse))
         if rc != 0:

@@ -52,8 +52,16 @@
  * section "Worked example: tracing the running statistics by hand") can be
  * checked step by step.
  *
- * All arrays are C-contiguous [B, H, S, d] (q: S=Sq, k and v: S=Sk), o is
- * [rows, d], lse is [rows].  Functions return 0 on success, -1 on bad
+ * Grouped-query attention (a variant the first page names: "FlashAttention:
+ * Why Tiling...", section "Using it in practice"): K and V carry Hkv heads,
+ * Hkv dividing H, and query head h reads K/V head h / (H / Hkv), i.e. each run
+ * of H/Hkv consecutive query heads shares one K/V head (the reading of the
+ * page, which names the variant without defining it; it is the grouping
+ * PyTorch's enable_gqa uses).  Hkv == H is ordinary multi-head attention,
+ * Hkv == 1 multi-query attention.
+ *
+ * All arrays are C-contiguous (q: [B, H, Sq, d]; k and v: [B, Hkv, Sk, d]),
+ * o is [rows, d], lse is [rows].  Functions return 0 on success, -1 on bad
  * arguments.
  */
 #include <math.h>
@@ -82,15 +90,23 @@ static int orc_visible(int mask_kind, int window, int64_t i, int64_t j)
     return 1;
 }
 
-static int orc_check(int B, int H, int Sq, int Sk, int d, int mask_kind, int window)
+static int orc_check(int B, int H, int Hkv, int Sq, int Sk, int d, int mask_kind, int window)
 {
-    if (B < 1 || H < 1 || Sq < 0 || Sk < 1 || d < 1)
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Sq < 0 || Sk < 1 || d < 1)
         return -1;
     if (mask_kind < 0 || mask_kind > 2)
         return -1;
     if (mask_kind == ORC_MASK_WINDOW && window < 1)
         return -1;
     return 0;
+}
+
+/* Offset of the K/V head that query head (b, h) reads, in elements. */
+static int64_t orc_kv_offset(int64_t bh, int H, int Hkv, int Sk, int d)
+{
+    const int64_t b = bh / H, h = bh % H;
+    const int64_t kvh = h / (H / Hkv);
+    return (b * Hkv + kvh) * (int64_t)Sk * d;
 }
 
 void oracle_set_threads(int n)
@@ -119,12 +135,12 @@ int oracle_max_threads(void)
  * turns them into probability rows P in place, then forms O = P V.
  */
 int oracle_attn_naive(const double *q, const double *k, const double *v,
-                      int B, int H, int Sq, int Sk, int d, double scale,
+                      int B, int H, int Hkv, int Sq, int Sk, int d, double scale,
                       int mask_kind, int window,
                       const int64_t *rows, int64_t nrows,
                       double *o, double *lse)
 {
-    if (orc_check(B, H, Sq, Sk, d, mask_kind, window) != 0)
+    if (orc_check(B, H, Hkv, Sq, Sk, d, mask_kind, window) != 0)
         return -1;
     const int64_t total_rows = (int64_t)B * H * Sq;
     if (rows == NULL)
@@ -159,7 +175,7 @@ int oracle_attn_naive(const double *q, const double *k, const double *v,
                 const int64_t flat = rows ? rows[r] : r;
                 const int64_t bh = flat / Sq, i = flat % Sq;
                 const double *qi = q + flat * (int64_t)d;
-                const double *kh = k + bh * (int64_t)Sk * d;
+                const double *kh = k + orc_kv_offset(bh, H, Hkv, Sk, d);
                 double *Si = S + (r - r0) * (int64_t)Sk;
                 for (int64_t j = 0; j < Sk; ++j) {
                     if (!orc_visible(mask_kind, window, i, j)) {
@@ -201,7 +217,7 @@ int oracle_attn_naive(const double *q, const double *k, const double *v,
             for (int64_t r = r0; r < r1; ++r) {
                 const int64_t flat = rows ? rows[r] : r;
                 const int64_t bh = flat / Sq;
-                const double *vh = v + bh * (int64_t)Sk * d;
+                const double *vh = v + orc_kv_offset(bh, H, Hkv, Sk, d);
                 const double *Pi = S + (r - r0) * (int64_t)Sk;
                 double *oi = o + r * (int64_t)d;
                 for (int c = 0; c < d; ++c)
@@ -300,11 +316,11 @@ static int64_t orc_online_row(const double *qi, const double *kh, const double *
 }
 
 int oracle_attn_blocked(const double *q, const double *k, const double *v,
-                        int B, int H, int Sq, int Sk, int d, double scale,
+                        int B, int H, int Hkv, int Sq, int Sk, int d, double scale,
                         int mask_kind, int window, int block_size,
                         double *o, double *lse)
 {
-    if (orc_check(B, H, Sq, Sk, d, mask_kind, window) != 0 || block_size < 1)
+    if (orc_check(B, H, Hkv, Sq, Sk, d, mask_kind, window) != 0 || block_size < 1)
         return -1;
     const int64_t total_rows = (int64_t)B * H * Sq;
     int failed = 0;
@@ -321,8 +337,8 @@ int oracle_attn_blocked(const double *q, const double *k, const double *v,
             if (sblk == NULL || acc == NULL)
                 continue;
             const int64_t bh = flat / Sq, i = flat % Sq;
-            orc_online_row(q + flat * (int64_t)d, k + bh * (int64_t)Sk * d,
-                           v + bh * (int64_t)Sk * d, Sk, d, scale, mask_kind, window, i,
+            orc_online_row(q + flat * (int64_t)d, k + orc_kv_offset(bh, H, Hkv, Sk, d),
+                           v + orc_kv_offset(bh, H, Hkv, Sk, d), Sk, d, scale, mask_kind, window, i,
                            block_size, sblk, acc, o + flat * (int64_t)d, lse + flat,
                            NULL, NULL, NULL);
         }
@@ -364,7 +380,7 @@ int oracle_online_trace(const double *qi, const double *kh, const double *vh,
 int oracle_probs(const double *qh, const double *kh, int Sq, int Sk, int d, double scale,
                  int mask_kind, int window, double *P)
 {
-    if (orc_check(1, 1, Sq, Sk, d, mask_kind, window) != 0)
+    if (orc_check(1, 1, 1, Sq, Sk, d, mask_kind, window) != 0)
         return -1;
     for (int64_t i = 0; i < Sq; ++i) {
         double *Pi = P + i * (int64_t)Sk;

@@ -308,6 +308,48 @@ def test_brute_force_tiny():
     check_brute_force(oracle.default(), np.random.default_rng(6))
 
 
+def check_gqa(orc, rng):
+    """Grouped-query attention: query head h reads K/V head h // (H // Hkv).
+
+    Pinned three ways that do not use the oracle's own head indexing: against
+    the multi-head oracle on K/V with each head repeated H // Hkv times in a row
+    (the grouping PyTorch's enable_gqa uses), against torch's SDPA on the same
+    repeated K/V, and one query head at a time against a one-head call on the
+    K/V head named explicitly.  The blocked form must agree too.
+    """
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for (H, Hkv, Sq, Sk, d) in ((4, 2, 7, 9, 3), (6, 3, 5, 5, 4), (4, 1, 6, 8, 2), (3, 3, 4, 4, 2)):
+        B = 2
+        q = _rand(rng, B, H, Sq, d)
+        k, v = _rand(rng, B, Hkv, Sk, d), _rand(rng, B, Hkv, Sk, d)
+        g = H // Hkv
+        k_rep, v_rep = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+        for mask, W in (("none", 0), ("causal", 0), ("window", 3)):
+            o, lse = orc.attention(q, k, v, 0.7, mask, W)
+            o_m, lse_m = orc.attention(q, k_rep, v_rep, 0.7, mask, W)
+            np.testing.assert_allclose(o, o_m, rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(lse, lse_m, rtol=1e-13, atol=1e-13)
+            ob, lb = orc.attention_blocked(q, k, v, 0.7, mask, W, block_size=2)
+            np.testing.assert_allclose(ob, o, rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(lb, lse, rtol=1e-11, atol=1e-12)
+            for b in range(B):
+                for h in range(H):
+                    o1, l1 = orc.attention(q[b:b + 1, h:h + 1], k[b:b + 1, h // g:h // g + 1],
+                                           v[b:b + 1, h // g:h // g + 1], 0.7, mask, W)
+                    np.testing.assert_allclose(o[b, h], o1[0, 0], rtol=1e-13, atol=1e-13)
+                    np.testing.assert_allclose(lse[b, h], l1[0, 0], rtol=1e-13, atol=1e-13)
+        ref = F.scaled_dot_product_attention(
+            torch.from_numpy(q), torch.from_numpy(k).repeat_interleave(g, dim=1),
+            torch.from_numpy(v).repeat_interleave(g, dim=1), scale=0.7).numpy()
+        o, _ = orc.attention(q, k, v, 0.7, "none")
+        np.testing.assert_allclose(o, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_query_heads():
+    check_gqa(oracle.default(), np.random.default_rng(8))
+
+
 def test_row_subset_matches_full():
     rng = np.random.default_rng(7)
     q, k, v = _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4)
@@ -326,6 +368,11 @@ def test_rejects_bad_arguments():
         oracle.attention(z, z, z, 1.0, 7)
     with pytest.raises(ValueError):
         oracle.attention(z, z, z, 1.0, "none", rows=[4])
+    q3, k2 = np.zeros((1, 3, 2, 2)), np.zeros((1, 2, 2, 2))
+    with pytest.raises(ValueError):  # K/V head count must divide the query head count
+        oracle.attention(q3, k2, k2, 1.0, "none")
+    with pytest.raises(ValueError):
+        oracle.attention_blocked(q3, k2, k2, 1.0, "none")
 
 
 def test_visible_pair_counts_agree():
@@ -353,6 +400,8 @@ MUTATIONS = [
     ("no normalisation", "Si[j] /= l;\n                lrow", "Si[j] /= 1.0;\n                lrow"),
     ("unguarded empty row", "if (m == -INFINITY) { /* no visible key: guarded row */",
      "if (0) {"),
+    ("K/V head by modulo", "const int64_t kvh = h / (H / Hkv);", "const int64_t kvh = h % Hkv;"),
+    ("K/V head ignores batch", "return (b * Hkv + kvh)", "return (kvh)"),
 ]
 
 
@@ -366,7 +415,7 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
     orc = oracle.OracleLib(lib)
     checks = [check_worked_example, check_online_softmax_1d, check_library_reduction,
               check_torch_sdpa, check_closed_forms, check_invariants,
-              check_blocked_equals_naive, check_brute_force]
+              check_blocked_equals_naive, check_brute_force, check_gqa]
     caught = 0
     for chk in checks:
         try:
