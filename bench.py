@@ -328,8 +328,8 @@ def run_ours(args, w):
             "vs_baseline": None,
             "dtype": "f16" if w.dtype == inputs.FP16 else "bf16",
             "data": "synthetic (seeded N(0,1), rounded to the 16-bit type)",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk,
-                       "head_dim": w.d, "mask": w.mask, "window": w.window,
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads,
+                       "Sq": w.Sq, "Sk": w.Sk, "head_dim": w.d, "mask": w.mask, "window": w.window,
                        "flops_per_step": flops, "l2": "flushed (256 MiB write) before every step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                        "kernel": fa.describe(w.d, w.mask,
@@ -389,8 +389,8 @@ def run_reference(args, w):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded N(0,1), rounded to the 16-bit type)",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "Sq": w.Sq, "Sk": w.Sk,
-                   "head_dim": w.d, "mask": w.mask, "window": w.window},
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads, "Sq": w.Sq,
+                   "Sk": w.Sk, "head_dim": w.d, "mask": w.mask, "window": w.window},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -413,17 +413,23 @@ def main(argv=None):
                     help="override the head count (smaller profiling case of the same kernel)")
     ap.add_argument("--seq", type=int, default=0,
                     help="override Sq = Sk (sequence-length sweeps of the same kernel)")
+    ap.add_argument("--kv-heads", type=int, default=0,
+                    help="K/V heads shared by the query heads (grouped-query attention)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     wl = int(args.workload) if args.workload.isdigit() else args.workload
     w = inputs.workload(wl)
-    if args.heads or args.seq:
+    if args.heads or args.seq or args.kv_heads:
         import dataclasses
         if args.heads:
             w = dataclasses.replace(w, H=args.heads, name=f"{w.name}_h{args.heads}")
         if args.seq:
             w = dataclasses.replace(w, Sq=args.seq, Sk=args.seq, name=f"{w.name}_s{args.seq}")
+        if args.kv_heads:
+            if args.kv_heads < 1 or w.H % args.kv_heads:
+                ap.error("--kv-heads must divide the head count")
+            w = dataclasses.replace(w, Hkv=args.kv_heads, name=f"{w.name}_kv{args.kv_heads}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

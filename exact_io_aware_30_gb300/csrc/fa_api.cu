@@ -126,13 +126,15 @@ int unit_tiles(const Params &p, int gq, int bn) {
 // (Batch, head) pairs are scheduled in groups whose K and V -- what every
 // query tile of a head re-reads -- fit in a third of the L2, so that the CTAs
 // working on a group find them there: K/V then come from DRAM about once and
-// DRAM traffic grows with S rather than S^2.
+// DRAM traffic grows with S rather than S^2.  With grouped-query attention a
+// group holds whole runs of the kv_group query heads that share a K/V head.
 int heads_per_group(const Params &p, int d, int l2_bytes) {
     const int BH = p.B * p.H;
     const double kv_head = 2.0 * (double)p.Sk * d * 2.0;
     const double budget = (l2_bytes > 0 ? (double)l2_bytes : 96.0e6) / 3.0;
-    const int g = (int)(budget / kv_head);
-    return g < 1 ? 1 : (g > BH ? BH : g);
+    const long long n_kv = (long long)(budget / kv_head);
+    const long long g = (n_kv < 1 ? 1 : n_kv) * p.kv_group;
+    return g > BH ? BH : (int)g;
 }
 
 // The kernel's unit numbering (decode_unit): groups of heads_per_group
@@ -244,17 +246,18 @@ fa_status launch(const Params &p, int num_sms, DeviceInfo &info, cudaStream_t st
 }
 
 fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
-                   int Sq, int Sk, int d, float scale, int mask_kind, int window, int dtype,
-                   cudaStream_t stream) {
+                   int Hkv, int Sq, int Sk, int d, float scale, int mask_kind, int window,
+                   int dtype, cudaStream_t stream) {
     fa_status st = check_sizes(B, H, Sq, Sk, d, mask_kind, window, dtype);
     if (st != FA_OK) return st;
+    if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
     if (Sq == 0) return FA_OK;  // nothing to compute; empty tensors may have null pointers
     if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
     const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                           reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
     if ((a16 & 15u) || (reinterpret_cast<uintptr_t>(lse) & 3u)) return FA_ERR_MISALIGNED;
-    const size_t qo_bytes = (size_t)B * H * Sq * d * 2, kv_bytes = (size_t)B * H * Sk * d * 2;
+    const size_t qo_bytes = (size_t)B * H * Sq * d * 2, kv_bytes = (size_t)B * Hkv * Sk * d * 2;
     const size_t lse_bytes = (size_t)B * H * Sq * 4;
     if (overlaps(o, qo_bytes, q, qo_bytes) || overlaps(o, qo_bytes, k, kv_bytes) ||
         overlaps(o, qo_bytes, v, kv_bytes) || overlaps(lse, lse_bytes, o, qo_bytes) ||
@@ -271,14 +274,16 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     const int bn = bn_for(d);
     Params p;
     std::memset(&p, 0, sizeof(p));
-    if (!make_map(&p.tm_q, q, d, Sq, H, B, 128, fp16) || !make_map(&p.tm_k, k, d, Sk, H, B, bn, fp16) ||
-        !make_map(&p.tm_v, v, d, Sk, H, B, bn, fp16) ||
+    if (!make_map(&p.tm_q, q, d, Sq, H, B, 128, fp16) ||
+        !make_map(&p.tm_k, k, d, Sk, Hkv, B, bn, fp16) ||
+        !make_map(&p.tm_v, v, d, Sk, Hkv, B, bn, fp16) ||
         (d <= 128 && !make_map(&p.tm_o, o, d, Sq, H, B, 128, fp16)))
         return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;
     p.B = B;
     p.H = H;
+    p.kv_group = H / Hkv;
     p.Sq = Sq;
     p.Sk = Sk;
     p.mask_kind = mask_kind;
@@ -310,8 +315,8 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     if (log_enabled()) {
         char buf[256];
         fa_describe(d, mask_kind, dtype, buf, sizeof buf);
-        std::fprintf(stderr, "[fa] %s B=%d H=%d Sq=%d Sk=%d units=%d grid=%d\n", buf, B, H, Sq, Sk,
-                     p.n_units, p.n_units < info->num_sms ? p.n_units : info->num_sms);
+        std::fprintf(stderr, "[fa] %s B=%d H=%d Hkv=%d Sq=%d Sk=%d units=%d grid=%d\n", buf, B, H,
+                     Hkv, Sq, Sk, p.n_units, p.n_units < info->num_sms ? p.n_units : info->num_sms);
     }
 
     switch (d) {
@@ -337,14 +342,21 @@ extern "C" {
 fa_status fa_fwd(const void *q, const void *k, const void *v, void *o, float *lse, int B, int H,
                  int Sq, int Sk, int d, float scale, int mask_kind, int window,
                  fa_stream_t stream) {
-    return fa::fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, d, scale, mask_kind, window, FA_DTYPE_BF16,
-                        reinterpret_cast<cudaStream_t>(stream));
+    return fa::fwd_impl(q, k, v, o, lse, B, H, H, Sq, Sk, d, scale, mask_kind, window,
+                        FA_DTYPE_BF16, reinterpret_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse, int B,
                       int H, int Sq, int Sk, int d, float scale, int mask_kind, int window,
                       fa_stream_t stream) {
-    return fa::fwd_impl(q, k, v, o, lse, B, H, Sq, Sk, d, scale, mask_kind, window, FA_DTYPE_FP16,
+    return fa::fwd_impl(q, k, v, o, lse, B, H, H, Sq, Sk, d, scale, mask_kind, window,
+                        FA_DTYPE_FP16, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse, int B,
+                     int H, int H_kv, int Sq, int Sk, int d, float scale, int mask_kind,
+                     int window, int dtype, fa_stream_t stream) {
+    return fa::fwd_impl(q, k, v, o, lse, B, H, H_kv, Sq, Sk, d, scale, mask_kind, window, dtype,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -71,8 +71,8 @@ constexpr int kMaxSchedUnits = 12288;  // units a precomputed schedule can hold
 
 struct Params {
     CUtensorMap tm_q;  // [B, H, Sq, d] 16-bit, box {64, 128, 1, 1}, 128-B swizzle
-    CUtensorMap tm_k;  // [B, H, Sk, d], box {64, BN, 1, 1}
-    CUtensorMap tm_v;  // [B, H, Sk, d], box {64, BN, 1, 1}
+    CUtensorMap tm_k;  // [B, Hkv, Sk, d], box {64, BN, 1, 1}
+    CUtensorMap tm_v;  // [B, Hkv, Sk, d], box {64, BN, 1, 1}
     CUtensorMap tm_o;  // [B, H, Sq, d] 16-bit, box {64, 128, 1, 1}, 128-B swizzle (d <= 128)
     void *o;           // [B, H, Sq, d] 16-bit
     float *lse;        // [B, H, Sq] fp32
@@ -82,6 +82,7 @@ struct Params {
     int n_qtiles;      // ceil(Sq / 128): units per (batch, head)
     int n_units;       // B * H * n_qtiles
     int heads_per_group;  // (batch, head) pairs scheduled together (K/V kept in L2)
+    int kv_group;      // query heads per K/V head (H / Hkv; 1 = multi-head)
     int o_vec8;        // O is 32-byte aligned: 32-byte stores
     uint64_t wait_limit_ns;  // limit of every pipeline wait
     int stall_test;          // test only: the softmax's first wait is on a barrier nothing completes
@@ -243,7 +244,7 @@ __device__ __forceinline__ int unit_at(int k, const Params &p) {
 // causal keys past the tile's last row, window keys before its first row's
 // window).  valid = the tile sees at least one key tile.
 struct Unit {
-    int b, h, i0, lo, hi;
+    int b, h, kvh, i0, lo, hi;  // kvh: the K/V head query head h reads
     bool valid;
 };
 
@@ -265,6 +266,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
     const int g = p.n_qtiles - 1 - gi;
     un.b = bh / p.H;
     un.h = bh - un.b * p.H;
+    un.kvh = un.h / p.kv_group;
     un.i0 = g * kBM;
     const int row_end = min(un.i0 + kBM, p.Sq);
     int key_end = p.Sk;
@@ -297,7 +299,7 @@ __device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *rin
         const uint32_t dst = ptx::smem_addr(ring + slot * C::TILE_BYTES);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
-            ptx::tma_load_4d(dst + c * C::KV_CHUNK, tm, fb, c * 64, key0, un.h, un.b, pol);
+            ptx::tma_load_4d(dst + c * C::KV_CHUNK, tm, fb, c * 64, key0, un.kvh, un.b, pol);
     }
     ++it;
     return true;

@@ -31,7 +31,7 @@ DTYPE_BF16 = 0
 DTYPE_FP16 = 1
 
 # Every entry point declared in include/fa.h.
-EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_workspace_query", "fa_status_string",
+EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_workspace_query", "fa_status_string",
            "fa_describe", "fa_get_device_error")
 
 
@@ -67,6 +67,9 @@ def load(path: str | None = None):
             fn = getattr(lib, name)
             fn.restype = _i
             fn.argtypes = fwd_args
+        lib.fa_fwd_gqa.restype = _i
+        lib.fa_fwd_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
+                                   ctypes.c_float, _i, _i, _i, _vp]
         lib.fa_workspace_query.restype = _i
         lib.fa_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i,
                                            ctypes.POINTER(ctypes.c_size_t)]
@@ -105,6 +108,16 @@ def fwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int
               _vp(stream))
 
 
+def fwd_gqa_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B: int, H: int,
+                H_kv: int, Sq: int, Sk: int, d: int, scale: float, mask_kind: int, window: int,
+                stream: int, dtype: int = DTYPE_BF16) -> int:
+    """Call fa_fwd_gqa (K/V with H_kv heads) with raw device pointers; returns the status."""
+    return load().fa_fwd_gqa(_vp(q_ptr), _vp(k_ptr), _vp(v_ptr), _vp(o_ptr), _vp(lse_ptr),
+                             int(B), int(H), int(H_kv), int(Sq), int(Sk), int(d),
+                             ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
+                             _vp(stream))
+
+
 def workspace_query(B, H, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):
     """(status, bytes) of fa_workspace_query."""
     n = ctypes.c_size_t(12345)
@@ -137,6 +150,10 @@ def forward(q, k, v, scale: float | None = None, mask="none", window: int = 0,
             out=None, lse=None, stream=None):
     """Fused attention forward on CUDA tensors [B, H, S, d] (bf16 or fp16).
 
+    k and v may carry fewer heads than q (grouped-query attention: [B, H_kv,
+    Sk, d] with H_kv dividing H, query head h reading K/V head h // (H //
+    H_kv)); that case goes through fa_fwd_gqa, the rest through fa_fwd /
+    fa_fwd_fp16.
     Returns (o, lse): o like q, lse fp32 [B, H, Sq].  Enqueued on ``stream``
     (default: torch's current stream of q's device); raises FAError if the
     library rejects the call.
@@ -151,9 +168,9 @@ def forward(q, k, v, scale: float | None = None, mask="none", window: int = 0,
         raise FAError(FA_ERR_INVALID_ARG, "q, k, v must share one dtype")
     dt = _dtype_code(q)
     B, H, Sq, d = q.shape
-    Sk = k.shape[2]
-    if tuple(k.shape) != (B, H, Sk, d) or tuple(v.shape) != (B, H, Sk, d):
-        raise FAError(FA_ERR_INVALID_ARG, "k and v must be [B,H,Sk,d] matching q")
+    H_kv, Sk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, H_kv, Sk, d) or tuple(v.shape) != (B, H_kv, Sk, d):
+        raise FAError(FA_ERR_INVALID_ARG, "k and v must be [B,H_kv,Sk,d] matching q")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -163,9 +180,15 @@ def forward(q, k, v, scale: float | None = None, mask="none", window: int = 0,
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                 B, H, Sq, Sk, d, float(scale), mask_code(mask), int(window), sp, dt)
-    _check(st, "fa_fwd")
+    if H_kv == H:
+        st = fwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                     B, H, Sq, Sk, d, float(scale), mask_code(mask), int(window), sp, dt)
+        _check(st, "fa_fwd")
+    else:
+        st = fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                         lse.data_ptr(), B, H, H_kv, Sq, Sk, d, float(scale), mask_code(mask),
+                         int(window), sp, dt)
+        _check(st, "fa_fwd_gqa")
     return out, lse
 
 

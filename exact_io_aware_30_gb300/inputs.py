@@ -6,9 +6,10 @@ GPU library) and the exactly widened float64 values (for the CPU oracle).
 
 Recipe (the same for every workload):
   * numpy ``Generator(PCG64(seed))``; Q, then K, then V drawn in that order
-    with ``standard_normal(shape, dtype=float32)``, shape [B, H, S, d];
+    with ``standard_normal(shape, dtype=float32)``, shape [B, H, S, d] (K and
+    V: [B, Hkv, Sk, d], Hkv = H unless the workload shares K/V heads);
   * round-to-nearest-even to bf16 (or fp16 for the fp16 workload);
-  * the "spiky keys" workload then picks, per (b, h), round(0.01 * Sk)
+  * the "spiky keys" workload then picks, per (b, K/V head), round(0.01 * Sk)
     distinct key rows with ``rng.choice(Sk, n, replace=False)`` and multiplies
     them by 8 (a power of two: exact in both 16-bit types);
   * scale = 1/sqrt(d) as float32.
@@ -43,6 +44,7 @@ class Workload:
     window: int = 0
     spiky_keys: bool = False
     seed: int = 0
+    Hkv: int = 0       # K/V heads (grouped-query attention); 0 = H
     notes: str = field(default="", compare=False)
 
     @property
@@ -52,8 +54,12 @@ class Workload:
     def shape_q(self):
         return (self.B, self.H, self.Sq, self.d)
 
+    @property
+    def kv_heads(self) -> int:
+        return self.Hkv if self.Hkv > 0 else self.H
+
     def shape_kv(self):
-        return (self.B, self.H, self.Sk, self.d)
+        return (self.B, self.kv_heads, self.Sk, self.d)
 
 
 # The five workloads, indexed 0..4; seed = 1001 + index.
@@ -127,8 +133,8 @@ def round_to_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
 class Inputs:
     workload: Workload
     q_bits: np.ndarray   # uint16 [B,H,Sq,d]
-    k_bits: np.ndarray   # uint16 [B,H,Sk,d]
-    v_bits: np.ndarray   # uint16 [B,H,Sk,d]
+    k_bits: np.ndarray   # uint16 [B,Hkv,Sk,d]
+    v_bits: np.ndarray   # uint16 [B,Hkv,Sk,d]
 
     def f64(self):
         dt = self.workload.dtype
@@ -148,7 +154,7 @@ def generate(w: Workload, seed: int | None = None) -> Inputs:
         n = int(round(0.01 * w.Sk))
         kf = bits_to_f64(kb, w.dtype)
         for b in range(w.B):
-            for h in range(w.H):
+            for h in range(w.kv_heads):
                 rows = rng.choice(w.Sk, n, replace=False)
                 kf[b, h, rows, :] *= 8.0
         kb = to_bits(kf.astype(np.float32), w.dtype)
@@ -156,7 +162,7 @@ def generate(w: Workload, seed: int | None = None) -> Inputs:
 
 
 def custom(B, H, Sq, Sk, d, dtype=BF16, mask="none", window=0, seed=0, spiky_keys=False,
-           name="custom") -> Inputs:
-    """An ad-hoc shape drawn by the same recipe."""
-    w = Workload(name, B, H, Sq, Sk, d, dtype, mask, window, spiky_keys, seed)
+           name="custom", Hkv=0) -> Inputs:
+    """An ad-hoc shape drawn by the same recipe (Hkv > 0: K/V with Hkv heads)."""
+    w = Workload(name, B, H, Sq, Sk, d, dtype, mask, window, spiky_keys, seed, Hkv)
     return generate(w)

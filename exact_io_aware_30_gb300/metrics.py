@@ -44,6 +44,7 @@ def attention_flops(w) -> float:
 def algorithmic_bytes(w) -> int:
     """Bytes the fused forward must move at minimum: read Q,K,V once, write O, lse."""
     e = 2
-    return (e * w.B * w.H * (w.Sq * w.d + 2 * w.Sk * w.d)   # Q, K, V
+    hkv = getattr(w, "kv_heads", w.H)                        # K/V heads (grouped-query)
+    return (e * w.B * (w.H * w.Sq * w.d + 2 * hkv * w.Sk * w.d)   # Q, K, V
             + e * w.B * w.H * w.Sq * w.d                      # O
             + 4 * w.B * w.H * w.Sq)                           # lse fp32

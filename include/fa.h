@@ -89,6 +89,27 @@ fa_status fa_fwd_fp16(const void *q, const void *k, const void *v, void *o, floa
                       int mask_kind, int window, fa_stream_t stream);
 
 /*
+ * fa_fwd_gqa -- the same forward with grouped-query attention: K and V carry
+ * H_kv heads and each run of H / H_kv consecutive query heads shares one, so
+ * that query head h reads K/V head h / (H / H_kv).  (The pages name
+ * grouped-query attention as a later variant of the method without defining
+ * it -- "FlashAttention: Why Tiling...", section "Using it in practice"; this
+ * grouping is the reading taken, the one PyTorch's enable_gqa uses.)
+ * H_kv == H is fa_fwd / fa_fwd_fp16; H_kv == 1 is multi-query attention.
+ *
+ *   q, o  [B, H, Sq, d]; k, v [B, H_kv, Sk, d]; lse [B, H, Sq] fp32
+ *   H_kv  >= 1 and dividing H, else FA_ERR_INVALID_ARG
+ *   dtype FA_DTYPE_BF16 or FA_DTYPE_FP16 (q, k, v and o alike)
+ * Every other argument, the ownership, the errors and the device flag are as
+ * for fa_fwd; fa_workspace_query with (B, H, ...) answers for this call too
+ * once H_kv divides H.  K/V tiles of a shared head are read by all of its
+ * query heads from the L2, so DRAM reads of K and V shrink by H / H_kv.
+ */
+fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int H, int H_kv, int Sq, int Sk, int d, float scale,
+                     int mask_kind, int window, int dtype, fa_stream_t stream);
+
+/*
  * fa_workspace_query -- device scratch bytes fa_fwd needs for this problem
  * (always 0: the forward keeps every intermediate on chip, so its memory is
  * linear in the sequence length -- "FlashAttention: Why Tiling...", section

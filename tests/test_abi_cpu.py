@@ -102,6 +102,45 @@ def test_invalid_calls_are_rejected_before_launch(lib, kw, status):
         assert _fwd(**kw2) == status
 
 
+def _fwd_gqa(**kw):
+    a = dict(q_ptr=FAKE, k_ptr=FAKE + (1 << 30), v_ptr=FAKE + (2 << 30), o_ptr=FAKE + (3 << 30),
+             lse_ptr=FAKE + (4 << 30), B=1, H=4, H_kv=2, Sq=128, Sk=128, d=128, scale=0.088,
+             mask_kind=fa.MASK_NONE, window=0, stream=0, dtype=fa.DTYPE_BF16)
+    a.update(kw)
+    return fa.fwd_gqa_raw(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),      # H_kv must divide H
+    (dict(H_kv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(H_kv=-2), fa.FA_ERR_INVALID_ARG),
+    (dict(H=2, H_kv=4), fa.FA_ERR_INVALID_ARG),
+    (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_kind=fa.MASK_SLIDING_WINDOW, window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(k_ptr=FAKE + (1 << 30) + 8), fa.FA_ERR_MISALIGNED),
+    # o overlaps the (smaller) K block: [B, H_kv, Sk, d] = 64 KiB from k_ptr
+    (dict(o_ptr=FAKE + (1 << 30) + 65536 - 16), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+])
+def test_gqa_invalid_calls_are_rejected_before_launch(lib, kw, status):
+    assert _fwd_gqa(**kw) == status
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=FAKE + 8), fa.FA_ERR_MISALIGNED),
+    (dict(o_ptr=FAKE + 64), fa.FA_ERR_INVALID_ARG),
+])
+def test_gqa_entry_with_equal_heads_validates_like_fa_fwd(lib, kw, status):
+    for dt in (fa.DTYPE_BF16, fa.DTYPE_FP16):
+        kw2 = dict(kw, dtype=dt)
+        assert _fwd(**kw2) == status
+        assert _fwd_gqa(H=1, H_kv=1, **kw2) == status
+
+
 @pytest.mark.parametrize("args,status", [
     ((1, 1, 128, 128, 96, "none", 0, 0), fa.FA_ERR_UNSUPPORTED),
     ((1, 1, 128, 128, 128, "none", 0, 5), fa.FA_ERR_UNSUPPORTED),

@@ -82,8 +82,9 @@ def compare(o, lse, o_ref, lse_ref, dtype, raw_max=None):
     return stats
 
 
-def full_case(B, H, Sq, Sk, d, dtype, mask, window=0, seed=0, spiky=False, scale=None):
-    inp = inputs.custom(B, H, Sq, Sk, d, dtype, mask, window, seed=seed, spiky_keys=spiky)
+def full_case(B, H, Sq, Sk, d, dtype, mask, window=0, seed=0, spiky=False, scale=None, Hkv=0):
+    inp = inputs.custom(B, H, Sq, Sk, d, dtype, mask, window, seed=seed, spiky_keys=spiky,
+                        Hkv=Hkv)
     sc = inp.workload.scale if scale is None else scale
     o, lse = run_gpu(inp, scale=sc)
     qf, kf, vf = inp.f64()
@@ -241,6 +242,77 @@ def test_workload_full_size_sampled(idx):
     o, lse = run_gpu(inp)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
     rows = _sample_rows(w, 384, np.random.default_rng(idx))
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
+    stats = compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype)
+    print(f"{w.name}: {stats}")
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query / multi-query attention (fa_fwd_gqa): K/V carry H_kv heads,
+# query head h reads K/V head h // (H // H_kv)
+# ---------------------------------------------------------------------------
+
+GQA_CASES = [(4, 2, "none", 0, 300, 300), (4, 1, "causal", 0, 300, 173),
+             (6, 3, "window", 17, 173, 300), (8, 2, "causal", 0, 1000, 1000),
+             (3, 1, "window", 200, 129, 129)]
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP16])
+def test_gqa_parity(d, dtype):
+    for i, (H, Hkv, mask, window, Sq, Sk) in enumerate(GQA_CASES):
+        full_case(2, H, Sq, Sk, d, dtype, mask, window, seed=600 + i, Hkv=Hkv)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_gqa_matches_mha_on_repeated_kv_bitwise(d):
+    # the kernel's arithmetic does not depend on which head a K/V tile came
+    # from, so sharing heads must give the very bits of the multi-head run on
+    # K/V with every head repeated H // H_kv times
+    inp = inputs.custom(2, 8, 500, 500, d, inputs.BF16, "causal", seed=700 + d, Hkv=2)
+    o_g, l_g = run_gpu(inp)
+    kb, vb = (np.repeat(b, 4, axis=1) for b in (inp.k_bits, inp.v_bits))
+    w = inputs.Workload("mha", 2, 8, 500, 500, d, inputs.BF16, "causal")
+    o_m, l_m = run_gpu(inputs.Inputs(w, inp.q_bits, kb, vb))
+    assert np.array_equal(o_g, o_m) and np.array_equal(l_g, l_m)
+
+
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP16])
+def test_gqa_entry_with_equal_heads_is_fa_fwd(dtype):
+    inp = inputs.custom(1, 3, 300, 300, 128, dtype, "window", 64, seed=13)
+    w = inp.workload
+    q, k, v = (_to_dev(b, dtype) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    o1, l1 = fa.forward(q, k, v, scale=w.scale, mask="window", window=64)
+    o2, l2 = torch.empty_like(q), torch.empty_like(l1)
+    st = fa.fwd_gqa_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o2.data_ptr(), l2.data_ptr(),
+                        1, 3, 3, 300, 300, 128, w.scale, fa.MASK_SLIDING_WINDOW, 64,
+                        torch.cuda.current_stream().cuda_stream,
+                        fa.DTYPE_BF16 if dtype == inputs.BF16 else fa.DTYPE_FP16)
+    assert st == fa.FA_OK
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_gqa_bad_head_count_raises():
+    q = torch.zeros(1, 3, 8, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward(q, k, k)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG
+
+
+GQA_FULL = inputs.Workload("b1h32kv8_s8192_d128_fp16_causal_gqa", 1, 32, 8192, 8192, 128,
+                           inputs.FP16, "causal", seed=1013, Hkv=8)
+
+
+def test_gqa_full_size_sampled():
+    # 8k tokens x 32 query heads sharing 8 K/V heads, in the benchmark's launch
+    w = GQA_FULL
+    inp = inputs.generate(w)
+    o, lse = run_gpu(inp)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    rows = _sample_rows(w, 384, np.random.default_rng(31))
     qf, kf, vf = inp.f64()
     o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
     stats = compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype)
