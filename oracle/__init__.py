@@ -114,6 +114,11 @@ class OracleLib:
         lib.oracle_probs.argtypes = [
             _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double,
             ctypes.c_int, ctypes.c_int, _dp]
+        lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = [
+            _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
+            _dp, _dp, _dp]
         lib.oracle_set_threads.restype = None
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -172,6 +177,26 @@ class OracleLib:
             raise ValueError("oracle_attn_blocked rejected its arguments")
         return o, lse
 
+    def attention_bwd(self, q, k, v, dout, scale: float, mask="none", window: int = 0):
+        """Gradients (dq, dk, dv) of sum(O * dout) for O = attention(q, k, v).
+
+        Shapes as in ``attention``; dout like q.  dk, dv have k's shape (with
+        shared K/V heads they sum over the query heads that read them).
+        """
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        B, H, Sq, d, Hkv, Sk = _shapes(q, k, v)
+        if dout.shape != q.shape:
+            raise ValueError("dout must have q's shape")
+        dq = np.empty_like(q)
+        dk = np.empty_like(k)
+        dv = np.empty_like(v)
+        rc = self.lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B, H, Hkv, Sq, Sk,
+                                      d, float(scale), _mask(mask), int(window), _ptr(dq),
+                                      _ptr(dk), _ptr(dv))
+        if rc != 0:
+            raise ValueError("oracle_attn_bwd rejected its arguments")
+        return dq, dk, dv
+
     def online_trace(self, q_row, K, V, scale: float, block_size: int):
         """Running (m, l, unnormalised O) after each key block for one query row.
 
@@ -228,6 +253,10 @@ def attention(*args, **kwargs):
 
 def attention_blocked(*args, **kwargs):
     return default().attention_blocked(*args, **kwargs)
+
+
+def attention_bwd(*args, **kwargs):
+    return default().attention_bwd(*args, **kwargs)
 
 
 def online_trace(*args, **kwargs):

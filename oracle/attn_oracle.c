@@ -412,3 +412,116 @@ int oracle_probs(const double *qh, const double *kh, int Sq, int Sk, int d, doub
     }
     return 0;
 }
+
+/*
+ * Gradients of the attention output, by the chain the first page gives for the
+ * backward pass ("FlashAttention: Why Tiling...", section "The backward pass:
+ * recompute instead of storing"), written out for whole rows instead of tiles:
+ * with dO the gradient of the loss with respect to O,
+ *
+ *   P_ij  = softmax row i of the scaled, masked scores (as in the forward)
+ *   dV_j  = sum_i P_ij dO_i                      (dV = P^T dO)
+ *   dP_ij = dO_i . v_j                           (dP = dO V^T)
+ *   dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik)      (softmax Jacobian on row i)
+ *   dQ_i  = scale * sum_j dS_ij k_j              (S = scale Q K^T)
+ *   dK_j  = scale * sum_i dS_ij q_i
+ *
+ * Hidden pairs have P_ij = 0 and so dS_ij = 0; a row with no visible key
+ * contributes nothing.  With grouped K/V heads, dK and dV of a K/V head sum
+ * over the query heads that read it.  q, dout, dq: [B, H, Sq, d]; k, v, dk,
+ * dv: [B, Hkv, Sk, d].  One worker per (b, K/V head), so no two workers write
+ * the same dK/dV rows.
+ */
+int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
+                    int B, int H, int Hkv, int Sq, int Sk, int d, double scale,
+                    int mask_kind, int window, double *dq, double *dk, double *dv)
+{
+    if (orc_check(B, H, Hkv, Sq, Sk, d, mask_kind, window) != 0)
+        return -1;
+    const int group = H / Hkv;
+    const int64_t n_kv = (int64_t)B * Hkv;
+    int failed = 0;
+#pragma omp parallel
+    {
+        double *P = (double *)malloc(sizeof(double) * (size_t)Sk);
+        double *dP = (double *)malloc(sizeof(double) * (size_t)Sk);
+        if (P == NULL || dP == NULL) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bk = 0; bk < n_kv; ++bk) {
+            if (P == NULL || dP == NULL)
+                continue;
+            const int64_t b = bk / Hkv, kvh = bk % Hkv;
+            const double *kh = k + bk * (int64_t)Sk * d;
+            const double *vh = v + bk * (int64_t)Sk * d;
+            double *dkh = dk + bk * (int64_t)Sk * d;
+            double *dvh = dv + bk * (int64_t)Sk * d;
+            for (int64_t x = 0; x < (int64_t)Sk * d; ++x) {
+                dkh[x] = 0.0;
+                dvh[x] = 0.0;
+            }
+            for (int64_t h = kvh * group; h < (kvh + 1) * group; ++h) {
+                const int64_t bh = b * H + h;
+                for (int64_t i = 0; i < Sq; ++i) {
+                    const double *qi = q + (bh * Sq + i) * (int64_t)d;
+                    const double *doi = dout + (bh * Sq + i) * (int64_t)d;
+                    double *dqi = dq + (bh * Sq + i) * (int64_t)d;
+                    for (int c = 0; c < d; ++c)
+                        dqi[c] = 0.0;
+                    /* Row i of P, as the forward forms it. */
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < Sk; ++j) {
+                        double s = -INFINITY;
+                        if (orc_visible(mask_kind, window, i, j)) {
+                            const double *kj = kh + j * (int64_t)d;
+                            double dot = 0.0;
+                            for (int c = 0; c < d; ++c)
+                                dot += qi[c] * kj[c];
+                            s = scale * dot;
+                        }
+                        P[j] = s;
+                        if (s > m)
+                            m = s;
+                    }
+                    if (m == -INFINITY)
+                        continue; /* no visible key: no gradient flows through row i */
+                    double l = 0.0;
+                    for (int64_t j = 0; j < Sk; ++j) {
+                        P[j] = (P[j] == -INFINITY) ? 0.0 : exp(P[j] - m);
+                        l += P[j];
+                    }
+                    for (int64_t j = 0; j < Sk; ++j)
+                        P[j] /= l;
+                    /* dP_ij = dO_i . v_j and the Jacobian's row term sum_k P_ik dP_ik. */
+                    double rowdot = 0.0;
+                    for (int64_t j = 0; j < Sk; ++j) {
+                        const double *vj = vh + j * (int64_t)d;
+                        double dot = 0.0;
+                        for (int c = 0; c < d; ++c)
+                            dot += doi[c] * vj[c];
+                        dP[j] = dot;
+                        rowdot += P[j] * dot;
+                    }
+                    for (int64_t j = 0; j < Sk; ++j) {
+                        if (P[j] == 0.0)
+                            continue;
+                        const double ds = P[j] * (dP[j] - rowdot);
+                        const double *kj = kh + j * (int64_t)d;
+                        double *dkj = dkh + j * (int64_t)d;
+                        double *dvj = dvh + j * (int64_t)d;
+                        for (int c = 0; c < d; ++c) {
+                            dqi[c] += scale * ds * kj[c];
+                            dkj[c] += scale * ds * qi[c];
+                            dvj[c] += P[j] * doi[c];
+                        }
+                    }
+                }
+            }
+        }
+        free(P);
+        free(dP);
+    }
+    return failed ? -1 : 0;
+}

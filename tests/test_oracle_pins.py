@@ -350,6 +350,103 @@ def test_grouped_query_heads():
     check_gqa(oracle.default(), np.random.default_rng(8))
 
 
+# ---------------------------------------------------------------------------
+# Backward: gradients of sum(O * dO)
+# ---------------------------------------------------------------------------
+
+def _loss(orc, q, k, v, g, scale, mask, W):
+    o, _ = orc.attention(q, k, v, scale, mask, W)
+    return math.fsum((o * g).ravel())
+
+
+def check_bwd_finite_differences(orc, rng):
+    """Every gradient element against a central difference of the forward."""
+    h = 1e-6
+    for (H, Hkv, Sq, Sk, d, mask, W) in ((2, 2, 4, 5, 3, "none", 0), (2, 1, 5, 4, 2, "causal", 0),
+                                         (2, 2, 6, 3, 2, "window", 2)):
+        q, k, v = _rand(rng, 1, H, Sq, d), _rand(rng, 1, Hkv, Sk, d), _rand(rng, 1, Hkv, Sk, d)
+        g = _rand(rng, 1, H, Sq, d)
+        grads = orc.attention_bwd(q, k, v, g, 0.6, mask, W)
+        for x, gx in zip((q, k, v), grads):
+            for idx in np.ndindex(x.shape):
+                old = x[idx]
+                x[idx] = old + h
+                lp = _loss(orc, q, k, v, g, 0.6, mask, W)
+                x[idx] = old - h
+                lm = _loss(orc, q, k, v, g, 0.6, mask, W)
+                x[idx] = old
+                assert abs(gx[idx] - (lp - lm) / (2 * h)) < 1e-7, (mask, idx)
+
+
+def test_bwd_matches_finite_differences():
+    check_bwd_finite_differences(oracle.default(), np.random.default_rng(21))
+
+
+def check_bwd_torch(orc, rng):
+    """fp64 autograd through torch's SDPA (band masks passed explicitly)."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for (H, Hkv, Sq, Sk, d, mask, W) in ((2, 2, 7, 9, 4, "none", 0), (4, 2, 9, 9, 3, "causal", 0),
+                                         (3, 1, 8, 10, 5, "window", 3)):
+        q, k, v = _rand(rng, 2, H, Sq, d), _rand(rng, 2, Hkv, Sk, d), _rand(rng, 2, Hkv, Sk, d)
+        g = _rand(rng, 2, H, Sq, d)
+        tq, tk, tv = (torch.from_numpy(x.copy()).requires_grad_(True) for x in (q, k, v))
+        rep = H // Hkv
+        if mask == "none":
+            am = None
+        elif mask == "causal":
+            am = torch.from_numpy(np.tril(np.ones((Sq, Sk), bool)))
+        else:
+            am = torch.from_numpy(_window_bool(Sq, Sk, W))
+        o = F.scaled_dot_product_attention(tq, tk.repeat_interleave(rep, dim=1),
+                                           tv.repeat_interleave(rep, dim=1), attn_mask=am,
+                                           scale=0.45)
+        o.backward(torch.from_numpy(g))
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, 0.45, mask, W)
+        np.testing.assert_allclose(dq, tq.grad.numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dk, tk.grad.numpy(), rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(dv, tv.grad.numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_bwd_matches_torch_autograd():
+    check_bwd_torch(oracle.default(), np.random.default_rng(22))
+
+
+def check_bwd_closed_forms(orc, rng):
+    # one key: every P is 1, so dS = 0 (dQ = dK = 0) and dV = sum_i dO_i
+    q, k, v, g = _rand(rng, 1, 2, 6, 3), _rand(rng, 1, 2, 1, 3), _rand(rng, 1, 2, 1, 3), \
+        _rand(rng, 1, 2, 6, 3)
+    dq, dk, dv = orc.attention_bwd(q, k, v, g, 0.9, "none")
+    assert np.abs(dq).max() < 1e-14 and np.abs(dk).max() < 1e-14
+    np.testing.assert_allclose(dv[:, :, 0], g.sum(axis=2), rtol=1e-13, atol=1e-14)
+    # scale 0: uniform weights 1/Sk, no gradient reaches q or k
+    q, k, v, g = _rand(rng, 1, 1, 5, 4), _rand(rng, 1, 1, 7, 4), _rand(rng, 1, 1, 7, 4), \
+        _rand(rng, 1, 1, 5, 4)
+    dq, dk, dv = orc.attention_bwd(q, k, v, g, 0.0, "none")
+    assert np.abs(dq).max() == 0 and np.abs(dk).max() == 0
+    np.testing.assert_allclose(dv[0, 0], np.tile(g[0, 0].sum(axis=0) / 7, (7, 1)), rtol=1e-13)
+    # causal, scale 0: key j is seen by rows i >= j, each with weight 1/(i+1)
+    dq, dk, dv = orc.attention_bwd(q[:, :, :5], k[:, :, :5], v[:, :, :5], g, 0.0, "causal")
+    for j in range(5):
+        ref = sum(g[0, 0, i] / (i + 1) for i in range(j, 5))
+        np.testing.assert_allclose(dv[0, 0, j], ref, rtol=1e-13)
+    # rows of P sum to one, so sum_j dV_j = sum over rows that see a key of dO_i,
+    # and the softmax Jacobian's rows sum to zero, so sum_j dK_j = 0
+    for mask, W in (("none", 0), ("causal", 0), ("window", 2)):
+        q, k, v, g = _rand(rng, 2, 3, 9, 4), _rand(rng, 2, 3, 6, 4), _rand(rng, 2, 3, 6, 4), \
+            _rand(rng, 2, 3, 9, 4)
+        dq, dk, dv = orc.attention_bwd(q, k, v, g, 0.8, mask, W)
+        _, lse = orc.attention(q, k, v, 0.8, mask, W)
+        seen = np.isfinite(lse)[..., None]
+        np.testing.assert_allclose(dv.sum(axis=2), (g * seen).sum(axis=2), rtol=1e-12, atol=1e-12)
+        assert np.abs(dk.sum(axis=2)).max() < 1e-12
+        assert np.all(dq[~np.isfinite(lse)] == 0)
+
+
+def test_bwd_closed_forms():
+    check_bwd_closed_forms(oracle.default(), np.random.default_rng(23))
+
+
 def test_row_subset_matches_full():
     rng = np.random.default_rng(7)
     q, k, v = _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4)
@@ -402,6 +499,15 @@ MUTATIONS = [
      "if (0) {"),
     ("K/V head by modulo", "const int64_t kvh = h / (H / Hkv);", "const int64_t kvh = h % Hkv;"),
     ("K/V head ignores batch", "return (b * Hkv + kvh)", "return (kvh)"),
+    ("bwd: Jacobian row term dropped", "const double ds = P[j] * (dP[j] - rowdot);",
+     "const double ds = P[j] * dP[j];"),
+    ("bwd: Jacobian row term sign", "const double ds = P[j] * (dP[j] - rowdot);",
+     "const double ds = P[j] * (dP[j] + rowdot);"),
+    ("bwd: dK without scale", "dkj[c] += scale * ds * qi[c];", "dkj[c] += ds * qi[c];"),
+    ("bwd: dQ from q", "dqi[c] += scale * ds * kj[c];", "dqi[c] += scale * ds * qi[c];"),
+    ("bwd: dV from dS", "dvj[c] += P[j] * doi[c];", "dvj[c] += ds * doi[c];"),
+    ("bwd: unnormalised P", "P[j] /= l;", "P[j] /= 1.0;"),
+    ("bwd: dP against k", "dot += doi[c] * vj[c];", "dot += doi[c] * kh[j * (int64_t)d + c];"),
 ]
 
 
@@ -415,7 +521,8 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
     orc = oracle.OracleLib(lib)
     checks = [check_worked_example, check_online_softmax_1d, check_library_reduction,
               check_torch_sdpa, check_closed_forms, check_invariants,
-              check_blocked_equals_naive, check_brute_force, check_gqa]
+              check_blocked_equals_naive, check_brute_force, check_gqa,
+              check_bwd_finite_differences, check_bwd_torch, check_bwd_closed_forms]
     caught = 0
     for chk in checks:
         try:
