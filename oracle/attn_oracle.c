@@ -429,9 +429,22 @@ int oracle_probs(const double *qh, const double *kh, int Sq, int Sk, int d, doub
  * Hidden pairs have P_ij = 0 and so dS_ij = 0; a row with no visible key
  * contributes nothing.  With grouped K/V heads, dK and dV of a K/V head sum
  * over the query heads that read it.  q, dout, dq: [B, H, Sq, d]; k, v, dk,
- * dv: [B, Hkv, Sk, d].  One worker per (b, K/V head), so no two workers write
- * the same dK/dV rows.
+ * dv: [B, Hkv, Sk, d].
+ *
+ * Two passes so that both can run in parallel without shared accumulators:
+ * the first goes over query rows (P_i, dP_i, the Jacobian's row term, dQ_i,
+ * and the row's max and sum of exponentials); the second goes over key rows
+ * and forms each P_ij again from that row's max and sum, then dS_ij, and
+ * accumulates dK_j and dV_j.
  */
+static double orc_dot(const double *a, const double *b, int d)
+{
+    double s = 0.0;
+    for (int c = 0; c < d; ++c)
+        s += a[c] * b[c];
+    return s;
+}
+
 int oracle_attn_bwd(const double *q, const double *k, const double *v, const double *dout,
                     int B, int H, int Hkv, int Sq, int Sk, int d, double scale,
                     int mask_kind, int window, double *dq, double *dk, double *dv)
@@ -439,8 +452,20 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
     if (orc_check(B, H, Hkv, Sq, Sk, d, mask_kind, window) != 0)
         return -1;
     const int group = H / Hkv;
-    const int64_t n_kv = (int64_t)B * Hkv;
+    const int64_t n_rows = (int64_t)B * H * Sq;
+    /* per query row: max m_i, sum of exponentials l_i, row term sum_k P_ik dP_ik */
+    double *rm = (double *)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1));
+    double *rl = (double *)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1));
+    double *rt = (double *)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1));
+    if (rm == NULL || rl == NULL || rt == NULL) {
+        free(rm);
+        free(rl);
+        free(rt);
+        return -1;
+    }
     int failed = 0;
+
+    /* Pass 1: query rows. */
 #pragma omp parallel
     {
         double *P = (double *)malloc(sizeof(double) * (size_t)Sk);
@@ -449,79 +474,89 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
 #pragma omp atomic write
             failed = 1;
         }
-#pragma omp for schedule(dynamic, 1)
-        for (int64_t bk = 0; bk < n_kv; ++bk) {
+#pragma omp for schedule(dynamic, 16)
+        for (int64_t r = 0; r < n_rows; ++r) {
             if (P == NULL || dP == NULL)
                 continue;
-            const int64_t b = bk / Hkv, kvh = bk % Hkv;
-            const double *kh = k + bk * (int64_t)Sk * d;
-            const double *vh = v + bk * (int64_t)Sk * d;
-            double *dkh = dk + bk * (int64_t)Sk * d;
-            double *dvh = dv + bk * (int64_t)Sk * d;
-            for (int64_t x = 0; x < (int64_t)Sk * d; ++x) {
-                dkh[x] = 0.0;
-                dvh[x] = 0.0;
+            const int64_t bh = r / Sq, i = r % Sq;
+            const double *kh = k + orc_kv_offset(bh, H, Hkv, Sk, d);
+            const double *vh = v + orc_kv_offset(bh, H, Hkv, Sk, d);
+            const double *qi = q + r * (int64_t)d;
+            const double *doi = dout + r * (int64_t)d;
+            double *dqi = dq + r * (int64_t)d;
+            for (int c = 0; c < d; ++c)
+                dqi[c] = 0.0;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < Sk; ++j) {
+                P[j] = orc_visible(mask_kind, window, i, j)
+                           ? scale * orc_dot(qi, kh + j * (int64_t)d, d) : -INFINITY;
+                if (P[j] > m)
+                    m = P[j];
             }
-            for (int64_t h = kvh * group; h < (kvh + 1) * group; ++h) {
-                const int64_t bh = b * H + h;
-                for (int64_t i = 0; i < Sq; ++i) {
-                    const double *qi = q + (bh * Sq + i) * (int64_t)d;
-                    const double *doi = dout + (bh * Sq + i) * (int64_t)d;
-                    double *dqi = dq + (bh * Sq + i) * (int64_t)d;
-                    for (int c = 0; c < d; ++c)
-                        dqi[c] = 0.0;
-                    /* Row i of P, as the forward forms it. */
-                    double m = -INFINITY;
-                    for (int64_t j = 0; j < Sk; ++j) {
-                        double s = -INFINITY;
-                        if (orc_visible(mask_kind, window, i, j)) {
-                            const double *kj = kh + j * (int64_t)d;
-                            double dot = 0.0;
-                            for (int c = 0; c < d; ++c)
-                                dot += qi[c] * kj[c];
-                            s = scale * dot;
-                        }
-                        P[j] = s;
-                        if (s > m)
-                            m = s;
-                    }
-                    if (m == -INFINITY)
-                        continue; /* no visible key: no gradient flows through row i */
-                    double l = 0.0;
-                    for (int64_t j = 0; j < Sk; ++j) {
-                        P[j] = (P[j] == -INFINITY) ? 0.0 : exp(P[j] - m);
-                        l += P[j];
-                    }
-                    for (int64_t j = 0; j < Sk; ++j)
-                        P[j] /= l;
-                    /* dP_ij = dO_i . v_j and the Jacobian's row term sum_k P_ik dP_ik. */
-                    double rowdot = 0.0;
-                    for (int64_t j = 0; j < Sk; ++j) {
-                        const double *vj = vh + j * (int64_t)d;
-                        double dot = 0.0;
-                        for (int c = 0; c < d; ++c)
-                            dot += doi[c] * vj[c];
-                        dP[j] = dot;
-                        rowdot += P[j] * dot;
-                    }
-                    for (int64_t j = 0; j < Sk; ++j) {
-                        if (P[j] == 0.0)
-                            continue;
-                        const double ds = P[j] * (dP[j] - rowdot);
-                        const double *kj = kh + j * (int64_t)d;
-                        double *dkj = dkh + j * (int64_t)d;
-                        double *dvj = dvh + j * (int64_t)d;
-                        for (int c = 0; c < d; ++c) {
-                            dqi[c] += scale * ds * kj[c];
-                            dkj[c] += scale * ds * qi[c];
-                            dvj[c] += P[j] * doi[c];
-                        }
-                    }
-                }
+            rm[r] = m;
+            rl[r] = 0.0;
+            rt[r] = 0.0;
+            if (m == -INFINITY)
+                continue; /* no visible key: no gradient flows through row i */
+            double l = 0.0;
+            for (int64_t j = 0; j < Sk; ++j) {
+                P[j] = (P[j] == -INFINITY) ? 0.0 : exp(P[j] - m);
+                l += P[j];
             }
+            for (int64_t j = 0; j < Sk; ++j)
+                P[j] /= l;
+            double rowdot = 0.0;
+            for (int64_t j = 0; j < Sk; ++j) {
+                dP[j] = orc_dot(doi, vh + j * (int64_t)d, d);
+                rowdot += P[j] * dP[j];
+            }
+            for (int64_t j = 0; j < Sk; ++j) {
+                if (P[j] == 0.0)
+                    continue;
+                const double ds = P[j] * (dP[j] - rowdot);
+                const double *kj = kh + j * (int64_t)d;
+                for (int c = 0; c < d; ++c)
+                    dqi[c] += scale * ds * kj[c];
+            }
+            rl[r] = l;
+            rt[r] = rowdot;
         }
         free(P);
         free(dP);
     }
+
+    /* Pass 2: key rows of every K/V head, over the query heads that read it. */
+    const int64_t n_keys = (int64_t)B * Hkv * Sk;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (int64_t kr = 0; kr < n_keys; ++kr) {
+        const int64_t bk = kr / Sk, j = kr % Sk;
+        const int64_t b = bk / Hkv, kvh = bk % Hkv;
+        const double *kj = k + kr * (int64_t)d;
+        const double *vj = v + kr * (int64_t)d;
+        double *dkj = dk + kr * (int64_t)d;
+        double *dvj = dv + kr * (int64_t)d;
+        for (int c = 0; c < d; ++c) {
+            dkj[c] = 0.0;
+            dvj[c] = 0.0;
+        }
+        for (int64_t h = kvh * group; h < (kvh + 1) * group; ++h) {
+            for (int64_t i = 0; i < Sq; ++i) {
+                const int64_t r = (b * H + h) * Sq + i;
+                if (rl[r] == 0.0 || !orc_visible(mask_kind, window, i, j))
+                    continue;
+                const double *qi = q + r * (int64_t)d;
+                const double *doi = dout + r * (int64_t)d;
+                const double Pij = exp(scale * orc_dot(qi, kj, d) - rm[r]) / rl[r];
+                const double ds = Pij * (orc_dot(doi, vj, d) - rt[r]);
+                for (int c = 0; c < d; ++c) {
+                    dkj[c] += scale * ds * qi[c];
+                    dvj[c] += Pij * doi[c];
+                }
+            }
+        }
+    }
+    free(rm);
+    free(rl);
+    free(rt);
     return failed ? -1 : 0;
 }

@@ -499,15 +499,19 @@ MUTATIONS = [
      "if (0) {"),
     ("K/V head by modulo", "const int64_t kvh = h / (H / Hkv);", "const int64_t kvh = h % Hkv;"),
     ("K/V head ignores batch", "return (b * Hkv + kvh)", "return (kvh)"),
-    ("bwd: Jacobian row term dropped", "const double ds = P[j] * (dP[j] - rowdot);",
+    ("bwd: Jacobian row term dropped (dQ pass)", "const double ds = P[j] * (dP[j] - rowdot);",
      "const double ds = P[j] * dP[j];"),
-    ("bwd: Jacobian row term sign", "const double ds = P[j] * (dP[j] - rowdot);",
-     "const double ds = P[j] * (dP[j] + rowdot);"),
+    ("bwd: Jacobian row term sign (dK/dV pass)", "const double ds = Pij * (orc_dot(doi, vj, d) - rt[r]);",
+     "const double ds = Pij * (orc_dot(doi, vj, d) + rt[r]);"),
     ("bwd: dK without scale", "dkj[c] += scale * ds * qi[c];", "dkj[c] += ds * qi[c];"),
     ("bwd: dQ from q", "dqi[c] += scale * ds * kj[c];", "dqi[c] += scale * ds * qi[c];"),
-    ("bwd: dV from dS", "dvj[c] += P[j] * doi[c];", "dvj[c] += ds * doi[c];"),
-    ("bwd: unnormalised P", "P[j] /= l;", "P[j] /= 1.0;"),
-    ("bwd: dP against k", "dot += doi[c] * vj[c];", "dot += doi[c] * kh[j * (int64_t)d + c];"),
+    ("bwd: dV from dS", "dvj[c] += Pij * doi[c];", "dvj[c] += ds * doi[c];"),
+    ("bwd: unnormalised P (dQ pass)", "P[j] /= l;\n            double rowdot", "P[j] /= 1.0;\n            double rowdot"),
+    ("bwd: P without the row sum (dK/dV pass)", "- rm[r]) / rl[r];", "- rm[r]);"),
+    ("bwd: dP against k", "dP[j] = orc_dot(doi, vh + j * (int64_t)d, d);",
+     "dP[j] = orc_dot(doi, kh + j * (int64_t)d, d);"),
+    ("bwd: key pass skips the causal mask", "if (rl[r] == 0.0 || !orc_visible(mask_kind, window, i, j))",
+     "if (rl[r] == 0.0)"),
 ]
 
 
