@@ -359,6 +359,147 @@ def run_ours(args, w):
     return result
 
 
+def cpu_oracle_bwd_sample(w, inp, dout_bits, target_s: float = 12.0):
+    """The fp64 oracle's backward on whole heads of the workload (heads are
+    independent), as many as fit in about target_s seconds.
+    Returns (TFLOP/s, cores, description)."""
+    import oracle
+    cores = oracle.max_threads()
+    qf, kf, vf = inp.f64()
+    dof = inputs.bits_to_f64(dout_bits, w.dtype)
+    per_head = metrics.attention_bwd_flops(w) / (w.B * w.H)
+    g = w.H // w.kv_heads
+
+    def run(nh):
+        t0 = time.perf_counter()
+        oracle.attention_bwd(qf[:1, :nh], kf[:1, :max(1, nh // g)], vf[:1, :max(1, nh // g)],
+                             dof[:1, :nh], w.scale, w.mask, w.window)
+        return time.perf_counter() - t0
+
+    dt1 = run(g)  # one K/V head's group of query heads
+    nh = g * max(1, min(w.H // g, int(target_s / max(dt1, 1e-6))))
+    dt = run(nh) if nh != g else dt1
+    desc = (f"{nh} of {w.B * w.H} heads (batch 0), {per_head * nh / 1e9:.1f} GFLOP "
+            f"mask-adjusted, {dt:.1f} s, fp64 oracle backward")
+    return per_head * nh / dt / 1e12, cores, desc
+
+
+def run_ours_bwd(args, w):
+    """One step = one fa_bwd call (row statistics, dK/dV and dQ kernels) over
+    resident Q, K, V, O, lse and dO; O and lse come from one forward call."""
+    import torch
+    from exact_io_aware_30_gb300 import build, fa
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    fa.load()
+    inp = inputs.generate(w)
+    dob = inputs.grad_output(w)
+    tdt = torch.bfloat16 if w.dtype == inputs.BF16 else torch.float16
+    host = [torch.from_numpy(b.view(np.int16)).view(tdt).pin_memory()
+            for b in (inp.q_bits, inp.k_bits, inp.v_bits, dob)]
+    q, k, v, do = (t.to(dev) for t in host)
+    stream = torch.cuda.current_stream(dev)
+    o, lse = fa.forward(q, k, v, scale=w.scale, mask=w.mask, window=w.window, stream=stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    st, ws_bytes = fa.bwd_workspace_query(w.B, w.H, w.kv_heads, w.Sq, w.Sk, w.d, w.mask,
+                                          w.window, fa.DTYPE_FP16 if w.dtype == inputs.FP16
+                                          else fa.DTYPE_BF16)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flops = metrics.attention_bwd_flops(w)
+
+    def step(qq=q, kk=k, vv=v, oo=o, ll=lse, dd=do):
+        fa.backward(qq, kk, vv, oo, ll, dd, scale=w.scale, mask=w.mask, window=w.window, dq=dq,
+                    dk=dk, dv=dv, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if fa.device_error() != fa.FA_OK:
+        raise RuntimeError("device pipeline timeout during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(physical_gpu_index(0))
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(1.0)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    call_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
+    ms = float(np.mean(call_ms))
+    # end to end from pinned host buffers: Q, K, V, O, lse, dO in; dQ, dK, dV out
+    lse_h = lse.cpu().pin_memory()
+    o_h = o.cpu().pin_memory()
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (dq, dk, dv)]
+    e2e_steps = max(3, min(args.steps, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        qd, kd, vd, dd = (t.to(dev, non_blocking=True) for t in host)
+        od = o_h.to(dev, non_blocking=True)
+        ld = lse_h.to(dev, non_blocking=True)
+        step(qd, kd, vd, od, ld, dd)
+        for h_, d_ in zip(outs_h, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if fa.device_error() != fa.FA_OK:
+        raise RuntimeError("device pipeline timeout during the timed region")
+    peak_tf, _, peak_src = load_peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in host) + o_h.numel() * 2 + lse_h.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    cpu = None
+    if not args.no_cpu_baseline:
+        tf, cores, desc = cpu_oracle_bwd_sample(w, inp, dob)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc}
+    dtc = fa.DTYPE_FP16 if w.dtype == inputs.FP16 else fa.DTYPE_BF16
+    result = {
+        "metric": "attention bwd TFLOP/s (mask-adjusted, 10*d per visible pair)",
+        "value": achieved,
+        "unit": "TFLOP/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16" if w.dtype == inputs.FP16 else "bf16",
+        "data": "synthetic (seeded N(0,1), rounded to the 16-bit type; dO likewise)",
+        "config": {"workload": "bwd_" + w.name, "B": w.B, "H": w.H, "H_kv": w.kv_heads,
+                   "Sq": w.Sq, "Sk": w.Sk, "head_dim": w.d, "mask": w.mask, "window": w.window,
+                   "flops_per_step": flops, "l2": "flushed (256 MiB write) before every step",
+                   "parallelism": "single GPU", "kernel": fa.describe(w.d, w.mask, dtc)},
+        "pct_of_peak": 100.0 * achieved / peak_tf,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf,
+                     "peak_source": f"{peak_src} dense bf16 (fp16 has the same nominal rate)",
+                     "traffic": None,
+                     "algorithmic_bytes": metrics.bwd_algorithmic_bytes(w),
+                     "kernel": "fa_bwd call (prep + dK/dV + dQ kernels)",
+                     "kernel_ms_median": float(np.median(call_ms)),
+                     "kernel_ms_min": float(np.min(call_ms))},
+        "cpu_baseline": cpu,
+        "e2e": {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -413,6 +554,8 @@ def main(argv=None):
                     help="override the head count (smaller profiling case of the same kernel)")
     ap.add_argument("--seq", type=int, default=0,
                     help="override Sq = Sk (sequence-length sweeps of the same kernel)")
+    ap.add_argument("--direction", choices=["fwd", "bwd"], default="fwd",
+                    help="bwd: time the backward (fa_bwd) on the same workload")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="K/V heads shared by the query heads (grouped-query attention)")
     args = ap.parse_args(argv)
@@ -432,6 +575,8 @@ def main(argv=None):
             w = dataclasses.replace(w, Hkv=args.kv_heads, name=f"{w.name}_kv{args.kv_heads}")
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.direction == "bwd":
+        return run_ours_bwd(args, w)
     return run_ours(args, w)
 
 

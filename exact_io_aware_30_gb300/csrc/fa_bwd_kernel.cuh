@@ -1,0 +1,859 @@
+// fa_bwd_kernel.cuh -- attention backward for sm_103a (GB300): dQ, dK, dV of
+// O = softmax(scale * Q K^T) V from Q, K, V, O, the forward's per-row lse and
+// dO, by recomputation ("FlashAttention: Why Tiling Attention Makes
+// Transformers Fast Without Changing the Result", section "The backward pass:
+// recompute instead of storing"): every score tile is rebuilt on chip from Q
+// and K, its probabilities from the stored row statistic,
+//   P_ij  = exp(scale q_i . k_j - lse_i)          (0 for hidden pairs)
+//   dV_j  = sum_i P_ij dO_i
+//   dP_ij = dO_i . v_j
+//   dS_ij = P_ij (dP_ij - delta_i)                 (softmax Jacobian)
+//   dQ_i  = scale sum_j dS_ij k_j,   dK_j = scale sum_i dS_ij q_i,
+// and no S x S matrix reaches device memory.  delta_i is the Jacobian's row
+// term sum_j P_ij dP_ij, taken as dO_i . O_i: both equal sum_j P_ij dO_i . v_j
+// because O_i = sum_j P_ij v_j, and the second needs one pass over a row of O
+// instead of a row of P.
+//
+// Three launches on the caller's stream:
+//   1. fa_bwd_prep_kernel: per query row, delta_i and lse_i * log2(e) (+inf
+//      for a row that sees no key and for padding rows, so that their P is 0)
+//      into a caller-provided workspace, rows padded per head to a multiple of
+//      128;
+//   2. fa_bwd_dkdv_kernel: one CTA per (batch, K/V head, 128-key tile).  K and
+//      V stay in shared memory; 64-row tiles of Q and dO of every query head
+//      that reads this K/V head stream through a ring.  Per step the MMA warp
+//      computes S^T = K Q^T and dP^T = V dO^T into tensor memory (lane = key),
+//      the four compute warps turn them into P^T and dS^T (16-bit, tensor
+//      memory), and the MMA warp accumulates dV += P^T dO and dK += dS^T Q in
+//      tensor memory (P^T and dS^T as the A operand from tensor memory);
+//   3. fa_bwd_dq_kernel: one CTA per (batch, head, 128-row query tile).  Q and
+//      dO stay in shared memory, K/V tiles stream through a ring; per step
+//      S = Q K^T and dP = dO V^T (lane = query row), dS in tensor memory, and
+//      dQ += dS K with K read as the MN-major B operand.
+// Two kernels instead of one with atomic dQ updates keep the result
+// deterministic and need no fp32 dQ buffer; the price is that S and dP are
+// formed twice (7 tile products per (query, key) tile instead of 5).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct BwdParams {
+    CUtensorMap tm_q;   // [B, H, Sq, d] 16-bit, box {64, query rows per tile, 1, 1}
+    CUtensorMap tm_do;  // like tm_q, over dO
+    CUtensorMap tm_k;   // [B, Hkv, Sk, d], box {64, keys per tile, 1, 1}
+    CUtensorMap tm_v;   // like tm_k, over V
+    void *dq;           // [B, H, Sq, d] 16-bit
+    void *dk;           // [B, Hkv, Sk, d] 16-bit
+    void *dv;           // [B, Hkv, Sk, d] 16-bit
+    const float *l2;    // [B*H, Sq_pad]: lse * log2(e); +inf for keyless and padding rows
+    const float *delta; // [B*H, Sq_pad]: dO_i . O_i; 0 for padding rows
+    int B, H, Hkv, kv_group, Sq, Sk, Sq_pad;
+    int mask_kind, window;
+    float scale_log2;  // scale * log2(e), kept positive (as in the forward)
+    float scale;       // the multiplier of dQ and dK
+    int n_units;       // CTAs of the launch
+    int n_tiles;       // dK/dV: key tiles per K/V head; dQ: query tiles per head
+    uint64_t wait_limit_ns;
+};
+
+constexpr int kBwdPadRows = 128;  // workspace rows per head are padded to this multiple
+
+// ---------------------------------------------------------------- prep
+
+template <bool kFP16>
+__device__ __forceinline__ float2 widen2(uint32_t w) {
+    if constexpr (kFP16) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        return __half22float2(h);
+    } else {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+}
+
+// One row per D/8 threads (16 bytes of O and dO each).
+template <int D, bool kFP16>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const uint16_t *__restrict__ o, const uint16_t *__restrict__ dout,
+                       const float *__restrict__ lse, float *__restrict__ l2,
+                       float *__restrict__ delta, long long BH, int Sq, int Sq_pad) {
+    constexpr int TPR = D / 8;
+    constexpr int RPB = 256 / TPR;
+    const int sub = (int)threadIdx.x % TPR;
+    const long long r = (long long)blockIdx.x * RPB + (long long)(threadIdx.x / TPR);
+    const long long rows = BH * (long long)Sq_pad;
+    const long long bh = r / Sq_pad;
+    const int i = (int)(r - bh * Sq_pad);
+    const bool real = r < rows && i < Sq;
+    float acc = 0.f;
+    if (real) {
+        const size_t off = ((size_t)bh * (size_t)Sq + (size_t)i) * D + (size_t)sub * 8;
+        const uint4 a = *reinterpret_cast<const uint4 *>(o + off);
+        const uint4 g = *reinterpret_cast<const uint4 *>(dout + off);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = widen2<kFP16>(aw[e]), y = widen2<kFP16>(gw[e]);
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
+        }
+    }
+#pragma unroll
+    for (int m = TPR / 2; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (sub == 0 && r < rows) {
+        float L = INFINITY;
+        if (real) {
+            const float ls = lse[(size_t)bh * (size_t)Sq + (size_t)i];
+            L = (ls == -INFINITY) ? INFINITY : ls * 1.4426950408889634f;
+        }
+        l2[r] = L;
+        delta[r] = real ? acc : 0.f;
+    }
+}
+
+// ---------------------------------------------------------------- shared helpers
+
+template <bool kFP16>
+__device__ __forceinline__ uint32_t pack2b(float lo, float hi) {
+    return kFP16 ? ptx::pack_f16x2(lo, hi) : ptx::pack_bf16x2(lo, hi);
+}
+
+// Stores 32 fp32 values (times `mul`) of one row as 16-bit to dst (16-byte aligned).
+template <bool kFP16>
+__device__ __forceinline__ void store_row32(void *dst, const uint32_t (&r)[32], float mul) {
+    uint32_t w[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        w[c] = pack2b<kFP16>(__uint_as_float(r[2 * c]) * mul, __uint_as_float(r[2 * c + 1]) * mul);
+    uint8_t *d8 = static_cast<uint8_t *>(dst);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        ptx::st_global_v4(d8 + 16 * c, w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+__device__ __forceinline__ void store_zero_row(void *dst, int bytes) {
+    uint8_t *d8 = static_cast<uint8_t *>(dst);
+    for (int c = 0; c < bytes; c += 16) ptx::st_global_v4(d8 + c, 0u, 0u, 0u, 0u);
+}
+
+// 16-column steps of a 128-byte-swizzled K-major operand made of 64-column
+// boxes `box` bytes apart: 32 bytes inside a box, then the next box.
+__device__ __forceinline__ uint32_t kmajor_step(int kk, int box) {
+    return (uint32_t)(((kk >> 2) * box + (kk & 3) * 32) >> 4);
+}
+
+// ---------------------------------------------------------------- dK / dV
+
+template <int D>
+struct BwdKVCfg {
+    static constexpr int BM = 64;    // query rows per step (N of S^T, K of dV / dK)
+    static constexpr int BN = 128;   // keys per CTA (M of every MMA = TMEM lanes)
+    static constexpr int ST = 3;     // stages of the (Q, dO, statistics) ring
+    static constexpr int KV_BOX = BN * 128;
+    static constexpr int Q_BOX = BM * 128;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int STAT_BYTES = 2 * BM * 4;  // l2 of the step's rows, then delta
+    static constexpr int NUM_COMPUTE = 128;        // warps 0-3: one key row per thread
+    static constexpr int MMA_WARP = 4;
+    static constexpr int TMA_WARP = 5;
+    static constexpr int NUM_THREADS = 192;
+    // Tensor memory: dV and dK accumulators, S^T and dP^T (fp32, 64 columns
+    // each), P^T and dS^T (16-bit pairs, 32 columns each).
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t DV_COL = 0;
+    static constexpr uint32_t DK_COL = 128;
+    static constexpr uint32_t S_COL = 256;
+    static constexpr uint32_t DP_COL = 320;
+    static constexpr uint32_t P_COL = 384;
+    static constexpr uint32_t DS_COL = 416;
+    static constexpr int B_KVFULL = 0;
+    static constexpr int B_QFULL = 1;              // [ST]
+    static constexpr int B_QEMPTY = B_QFULL + ST;  // [ST]
+    static constexpr int B_SFULL = B_QEMPTY + ST;
+    static constexpr int B_SFREE = B_SFULL + 1;
+    static constexpr int B_PFULL = B_SFREE + 1;
+    static constexpr int B_PFREE = B_PFULL + 1;
+    static constexpr int B_DONE = B_PFREE + 1;
+    static constexpr int B_DRAIN = B_DONE + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
+    static_assert(D <= 128, "dK and dV accumulators need 2 x d tensor-memory columns");
+    static_assert(DK_COL + D <= S_COL && DS_COL + BM / 2 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+};
+
+// The rows of the K/V tile of one CTA and the query tiles that see them.
+struct KVUnit {
+    int b, kvh, j0, jend;  // keys [j0, jend)
+    int it_lo, n_i;        // query tiles it_lo .. it_lo + n_i of every query head of the group
+    int steps;             // kv_group * n_i
+};
+
+__device__ __forceinline__ KVUnit decode_kv_unit(const BwdParams &p) {
+    KVUnit u;
+    const int n_bk = p.B * p.Hkv;
+    const int jt = (int)blockIdx.x / n_bk;  // key tile: all heads' first tiles first (longest)
+    const int bk = (int)blockIdx.x - jt * n_bk;
+    u.b = bk / p.Hkv;
+    u.kvh = bk - u.b * p.Hkv;
+    u.j0 = jt * 128;
+    u.jend = min(u.j0 + 128, p.Sk);
+    // query rows that see one of these keys
+    const int row_lo = (p.mask_kind == kMaskNone) ? 0 : u.j0;
+    long long row_hi = p.Sq;
+    if (p.mask_kind == kMaskWindow) row_hi = min(row_hi, (long long)u.jend - 1 + (long long)p.window);
+    if (row_lo >= row_hi) {
+        u.it_lo = 0;
+        u.n_i = 0;
+    } else {
+        u.it_lo = row_lo / 64;
+        u.n_i = (int)((row_hi + 63) / 64) - u.it_lo;
+    }
+    u.steps = p.kv_group * u.n_i;
+    return u;
+}
+
+template <int D>
+__device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
+                                uint8_t *sQ, uint8_t *sDO, uint8_t *sStat, uint32_t bars,
+                                Ctl *ctl) {
+    using C = BwdKVCfg<D>;
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t pol_last = ptx::policy_evict_last();
+    if (un.steps == 0) return;  // no query row sees these keys: nothing to load
+    if (leader) {
+        const uint32_t fb = bar_addr(bars, C::B_KVFULL);
+        ptx::mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            ptx::tma_load_4d(ptx::smem_addr(sK) + c * C::KV_BOX, &p.tm_k, fb, c * 64, un.j0, un.kvh, un.b,
+                             pol_last);
+            ptx::tma_load_4d(ptx::smem_addr(sV) + c * C::KV_BOX, &p.tm_v, fb, c * 64, un.j0, un.kvh, un.b,
+                             pol_last);
+        }
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int s = 0; s < un.steps; ++s) {
+        const int slot = s % C::ST;
+        if (!wait_bar_backoff(bar_addr(bars, C::B_QEMPTY + slot), ((s / C::ST) & 1) ^ 1, ctl, 21)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            const int hq = un.kvh * p.kv_group + s / un.n_i;
+            const int i0 = (un.it_lo + s % un.n_i) * C::BM;
+            const uint32_t fb = bar_addr(bars, C::B_QFULL + slot);
+            ptx::mbar_arrive_expect_tx(fb, 2 * C::Q_BYTES + C::STAT_BYTES);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                ptx::tma_load_4d(ptx::smem_addr(sQ + slot * C::Q_BYTES) + c * C::Q_BOX, &p.tm_q, fb, c * 64,
+                                 i0, hq, un.b, pol_last);
+                ptx::tma_load_4d(ptx::smem_addr(sDO + slot * C::Q_BYTES) + c * C::Q_BOX, &p.tm_do, fb,
+                                 c * 64, i0, hq, un.b, pol_last);
+            }
+            const size_t row0 = ((size_t)un.b * p.H + hq) * (size_t)p.Sq_pad + (size_t)i0;
+            const uint32_t st = ptx::smem_addr(sStat + slot * C::STAT_BYTES);
+            ptx::bulk_load(st, p.l2 + row0, C::BM * 4, fb);
+            ptx::bulk_load(st + C::BM * 4, p.delta + row0, C::BM * 4, fb);
+        }
+        __syncwarp();
+        ++issued;
+    }
+    // Let every copy already issued land before the CTA can exit.
+    wait_bar_drain(bar_addr(bars, C::B_KVFULL), 0);
+    if (!ok) {
+        for (int s = issued - C::ST > 0 ? issued - C::ST : 0; s < issued; ++s)
+            wait_bar_drain(bar_addr(bars, C::B_QFULL + s % C::ST), (s / C::ST) & 1);
+    }
+}
+
+template <int D, bool kFP16>
+__device__ void bwd_kv_mma_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
+                                uint8_t *sQ, uint8_t *sDO, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+    using C = BwdKVCfg<D>;
+    constexpr uint32_t kIdescS = make_idesc(C::BN, C::BM, kFP16, false);  // M = keys, N = query rows
+    constexpr uint32_t kIdescG = make_idesc(C::BN, D, kFP16, true);       // dV, dK: N = d, B MN-major
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t dk_desc = smem_desc(ptx::smem_addr(sK), 16);
+    const uint64_t dv_desc = smem_desc(ptx::smem_addr(sV), 16);
+    bool ok = un.steps == 0 || wait_bar(bar_addr(bars, C::B_KVFULL), 0, ctl, 22);
+    for (int t = 0; ok && t <= un.steps; ++t) {
+        if (t < un.steps) {
+            const int slot = t % C::ST;
+            if (!wait_bar(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 23)) {
+                ok = false;
+                break;
+            }
+            // the compute warps have read S^T and dP^T of step t-1
+            if (t >= 1 && !wait_bar(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 24)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+                const uint64_t qd = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), 16);
+                const uint64_t od = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), 16);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::S_COL, dk_desc + kmajor_step(kk, C::KV_BOX),
+                                qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::DP_COL, dv_desc + kmajor_step(kk, C::KV_BOX),
+                                od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            }
+            __syncwarp();
+        }
+        if (t >= 1) {
+            const int tp = t - 1, slot = tp % C::ST;
+            if (!wait_bar(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 25)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+                // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
+                // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
+                const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), C::Q_BOX);
+                const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), C::Q_BOX);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
+                                kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + (uint32_t)((kk * 2048) >> 4),
+                                kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+                ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
+                if (tp + 1 == un.steps) ptx::mma_commit(bar_addr(bars, C::B_DONE));
+            }
+            __syncwarp();
+        }
+    }
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    __syncwarp();
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+template <int D, bool kFP16>
+__device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const uint8_t *sStat,
+                                    uint32_t bars, uint32_t tmem, Ctl *ctl) {
+    using C = BwdKVCfg<D>;
+    const int tid = (int)threadIdx.x;  // = key row of the tile = TMEM lane
+    const int warp = tid >> 5;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int j = un.j0 + tid;
+    const bool row_ok = j < p.Sk;
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < un.steps; ++t) {
+        const int slot = t % C::ST;
+        const int i0 = (un.it_lo + t % un.n_i) * C::BM;
+        // The statistics arrived with the step's Q tile; S^T and dP^T are ready.
+        ok = ok && wait_bar(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
+        ok = ok && wait_bar(bar_addr(bars, C::B_SFULL), t & 1, ctl, 27);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        uint32_t s[64], dp[64];
+        ptx::tmem_ld_x32<0>(lane_base + C::S_COL, s);
+        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
+        ptx::tmem_ld_x32<0>(lane_base + C::DP_COL, dp);
+        ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 32, dp);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<64>(s);
+        ptx::reg_fence<64>(dp);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
+
+        // Query column i0 + col is visible to key j iff lo <= col < hi.
+        int lo = 0, hi = C::BM;
+        if (p.mask_kind != kMaskNone) lo = j - i0;
+        if (p.mask_kind == kMaskWindow) hi = (int)min((long long)C::BM, (long long)j + p.window - i0);
+        if (!row_ok) lo = C::BM;
+        const bool masked = lo > 0 || hi < C::BM;
+        const float4 *L4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES);
+        const float4 *D4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4);
+        uint32_t pw[32], dsw[32];
+#pragma unroll
+        for (int q = 0; q < C::BM / 4; ++q) {
+            const float4 l = L4[q], dl = D4[q];
+            const float lv[4] = {l.x, l.y, l.z, l.w}, dv[4] = {dl.x, dl.y, dl.z, dl.w};
+            float pv[4], dsv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int col = 4 * q + e;
+                float pe = ptx::ex2_approx(fmaf(__uint_as_float(s[col]), c, -lv[e]));
+                if (masked) pe = (col >= lo && col < hi) ? pe : 0.f;
+                pv[e] = pe;
+                dsv[e] = pe * (__uint_as_float(dp[col]) - dv[e]);
+            }
+            pw[2 * q] = pack2b<kFP16>(pv[0], pv[1]);
+            pw[2 * q + 1] = pack2b<kFP16>(pv[2], pv[3]);
+            dsw[2 * q] = pack2b<kFP16>(dsv[0], dsv[1]);
+            dsw[2 * q + 1] = pack2b<kFP16>(dsv[2], dsv[3]);
+        }
+        // dV / dK of step t-1 have read the P and dS areas
+        if (t >= 1 && !wait_bar(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 28)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        ptx::tmem_st_x32<0>(lane_base + C::P_COL, pw);
+        ptx::tmem_st_x32<0>(lane_base + C::DS_COL, dsw);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
+    }
+
+    // Epilogue: dV and scale * dK of this thread's key row.
+    if (un.steps > 0) {
+        if (!ok || !wait_bar(bar_addr(bars, C::B_DONE), 0, ctl, 29)) return;
+        ptx::tc_fence_after();
+    }
+    const size_t row = ((size_t)un.b * p.Hkv + un.kvh) * (size_t)p.Sk + (size_t)j;
+    uint8_t *dv_row = static_cast<uint8_t *>(p.dv) + row * D * 2;
+    uint8_t *dk_row = static_cast<uint8_t *>(p.dk) + row * D * 2;
+    if (un.steps == 0) {
+        if (row_ok) {
+            store_zero_row(dv_row, D * 2);
+            store_zero_row(dk_row, D * 2);
+        }
+        return;
+    }
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld_x32<0>(lane_base + C::DV_COL + cc * 32, r);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(r);
+        if (row_ok) store_row32<kFP16>(dv_row + cc * 64, r, 1.f);
+        ptx::tmem_ld_x32<0>(lane_base + C::DK_COL + cc * 32, r);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(r);
+        if (row_ok) store_row32<kFP16>(dk_row + cc * 64, r, p.scale);
+    }
+}
+
+template <int D, bool kFP16>
+__global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ BwdParams p) {
+    using C = BwdKVCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sK = smem;
+    uint8_t *sV = sK + C::KV_BYTES;
+    uint8_t *sQ = sV + C::KV_BYTES;
+    uint8_t *sDO = sQ + C::ST * C::Q_BYTES;
+    uint8_t *sStat = sDO + C::ST * C::Q_BYTES;
+    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
+    Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);  // 8-byte aligned
+    const uint32_t bars = ptx::smem_addr(bar_mem);
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar_addr(bars, C::B_KVFULL), 1);
+        for (int s = 0; s < C::ST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_QFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + s), 1);
+        }
+        ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_SFREE), C::NUM_COMPUTE);
+        ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_COMPUTE);
+        ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ctl->abort = 0;
+        ctl->limit_ns = p.wait_limit_ns;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == C::TMA_WARP && ptx::lane_id() == 0) {
+        ptx::prefetch_tensormap(&p.tm_q);
+        ptx::prefetch_tensormap(&p.tm_do);
+        ptx::prefetch_tensormap(&p.tm_k);
+        ptx::prefetch_tensormap(&p.tm_v);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const KVUnit un = decode_kv_unit(p);
+
+    if (warp < C::NUM_COMPUTE / 32) {
+        bwd_kv_compute_role<D, kFP16>(p, un, sStat, bars, tmem, ctl);
+    } else if (warp == C::MMA_WARP) {
+        bwd_kv_mma_role<D, kFP16>(p, un, sK, sV, sQ, sDO, bars, tmem, ctl);
+    } else {
+        bwd_kv_tma_role<D>(p, un, sK, sV, sQ, sDO, sStat, bars, ctl);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------- dQ
+
+template <int D>
+struct BwdQCfg {
+    static constexpr int BM = 128;                // query rows per CTA = TMEM lanes
+    static constexpr int BN = 128;                // keys per step
+    static constexpr int KST = (D == 64) ? 3 : 2; // K/V stages
+    static constexpr int Q_BOX = BM * 128;
+    static constexpr int KV_BOX = BN * 128;
+    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int KV_BYTES = BN * D * 2;
+    static constexpr int NUM_COMPUTE = 128;       // warps 0-3: one query row per thread
+    static constexpr int MMA_WARP = 4;
+    static constexpr int TMA_WARP = 5;
+    static constexpr int NUM_THREADS = 192;
+    // Tensor memory: S and dP (fp32, BN columns each), the dQ accumulator,
+    // dS (16-bit pairs, BN/2 columns).
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0;
+    static constexpr uint32_t DP_COL = 128;
+    static constexpr uint32_t DQ_COL = 256;
+    static constexpr uint32_t DS_COL = 384;
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_KVFULL = 1;                // [KST]
+    static constexpr int B_KVEMPTY = B_KVFULL + KST;  // [KST]
+    static constexpr int B_SFULL = B_KVEMPTY + KST;
+    static constexpr int B_SFREE = B_SFULL + 1;
+    static constexpr int B_PFULL = B_SFREE + 1;
+    static constexpr int B_PFREE = B_PFULL + 1;
+    static constexpr int B_DONE = B_PFREE + 1;
+    static constexpr int B_DRAIN = B_DONE + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SMEM_TILES = 2 * Q_BYTES + KST * 2 * KV_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
+    static_assert(D <= 128, "one dQ accumulator of d columns next to S and dP");
+    static_assert(DQ_COL + D <= DS_COL && DS_COL + BN / 2 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+};
+
+struct QUnit {
+    int b, h, kvh, i0;
+    int lo, n;  // key tiles lo .. lo + n
+};
+
+__device__ __forceinline__ QUnit decode_q_unit(const BwdParams &p) {
+    QUnit u;
+    const int BH = p.B * p.H;
+    const int g = p.n_tiles - 1 - (int)blockIdx.x / BH;  // longest query tiles first
+    const int bh = (int)blockIdx.x % BH;
+    u.b = bh / p.H;
+    u.h = bh - u.b * p.H;
+    u.kvh = u.h / p.kv_group;
+    u.i0 = g * 128;
+    const int row_end = min(u.i0 + 128, p.Sq);
+    int key_end = p.Sk;
+    if (p.mask_kind != kMaskNone) key_end = min(p.Sk, row_end);
+    int key_beg = 0;
+    if (p.mask_kind == kMaskWindow) key_beg = max(0, u.i0 - p.window + 1);
+    if (key_beg < key_end) {
+        u.lo = key_beg / 128;
+        u.n = (key_end + 127) / 128 - u.lo;
+    } else {
+        u.lo = 0;
+        u.n = 0;
+    }
+    return u;
+}
+
+template <int D>
+__device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
+                               uint8_t *sKV, uint32_t bars, Ctl *ctl) {
+    using C = BwdQCfg<D>;
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t pol_last = ptx::policy_evict_last();
+    const uint64_t pol_first = ptx::policy_evict_first();
+    if (un.n == 0) return;
+    if (leader) {
+        const uint32_t fb = bar_addr(bars, C::B_QFULL);
+        ptx::mbar_arrive_expect_tx(fb, 2 * C::Q_BYTES);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            ptx::tma_load_4d(ptx::smem_addr(sQ) + c * C::Q_BOX, &p.tm_q, fb, c * 64, un.i0, un.h, un.b,
+                             pol_first);
+            ptx::tma_load_4d(ptx::smem_addr(sDO) + c * C::Q_BOX, &p.tm_do, fb, c * 64, un.i0, un.h, un.b,
+                             pol_first);
+        }
+    }
+    int issued = 0;
+    bool ok = true;
+    for (int t = 0; t < un.n; ++t) {
+        const int slot = t % C::KST;
+        if (!wait_bar_backoff(bar_addr(bars, C::B_KVEMPTY + slot), ((t / C::KST) & 1) ^ 1, ctl, 31)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            const int k0 = (un.lo + t) * C::BN;
+            const uint32_t fb = bar_addr(bars, C::B_KVFULL + slot);
+            ptx::mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+            const uint32_t dk = ptx::smem_addr(sKV + slot * 2 * C::KV_BYTES);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) {
+                ptx::tma_load_4d(dk + c * C::KV_BOX, &p.tm_k, fb, c * 64, k0, un.kvh, un.b, pol_last);
+                ptx::tma_load_4d(dk + C::KV_BYTES + c * C::KV_BOX, &p.tm_v, fb, c * 64, k0, un.kvh, un.b,
+                                 pol_last);
+            }
+        }
+        __syncwarp();
+        ++issued;
+    }
+    wait_bar_drain(bar_addr(bars, C::B_QFULL), 0);
+    if (!ok) {
+        for (int t = issued - C::KST > 0 ? issued - C::KST : 0; t < issued; ++t)
+            wait_bar_drain(bar_addr(bars, C::B_KVFULL + t % C::KST), (t / C::KST) & 1);
+    }
+}
+
+template <int D, bool kFP16>
+__device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
+                               uint8_t *sKV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+    using C = BwdQCfg<D>;
+    constexpr uint32_t kIdescS = make_idesc(C::BM, C::BN, kFP16, false);
+    constexpr uint32_t kIdescG = make_idesc(C::BM, D, kFP16, true);  // dQ: N = d, K MN-major
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t qd = smem_desc(ptx::smem_addr(sQ), 16);
+    const uint64_t od = smem_desc(ptx::smem_addr(sDO), 16);
+    bool ok = un.n == 0 || wait_bar(bar_addr(bars, C::B_QFULL), 0, ctl, 32);
+    for (int t = 0; ok && t <= un.n; ++t) {
+        if (t < un.n) {
+            const int slot = t % C::KST;
+            if (!wait_bar(bar_addr(bars, C::B_KVFULL + slot), (t / C::KST) & 1, ctl, 33)) {
+                ok = false;
+                break;
+            }
+            if (t >= 1 && !wait_bar(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 34)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+                const uint32_t ka = ptx::smem_addr(sKV + slot * 2 * C::KV_BYTES);
+                const uint64_t kd = smem_desc(ka, 16);
+                const uint64_t vd = smem_desc(ka + C::KV_BYTES, 16);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
+                                kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
+                                kIdescS, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            }
+            __syncwarp();
+        }
+        if (t >= 1) {
+            const int tp = t - 1, slot = tp % C::KST;
+            if (!wait_bar(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 35)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+                // K as the MN-major B operand: K = keys (16 = 2048 bytes), N = d.
+                const uint64_t km = smem_desc(ptx::smem_addr(sKV + slot * 2 * C::KV_BYTES), C::KV_BOX);
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 16; ++kk)
+                    ptx::mma_ts(tmem + C::DQ_COL, tmem + C::DS_COL + kk * 8, km + (uint32_t)((kk * 2048) >> 4),
+                                kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+                ptx::mma_commit(bar_addr(bars, C::B_KVEMPTY + slot));
+                if (tp + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_DONE));
+            }
+            __syncwarp();
+        }
+    }
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    __syncwarp();
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+// dS of 64 key columns (col0 .. col0 + 63 of the tile) into 32 packed words.
+template <bool kFP16>
+__device__ __forceinline__ void q_ds_half(const uint32_t (&s)[64], const uint32_t (&dp)[64], float c,
+                                          float L, float Dl, bool masked, int lo, int hi, int col0,
+                                          uint32_t (&w)[32]) {
+#pragma unroll
+    for (int e = 0; e < 64; e += 2) {
+        float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[e]), c, -L));
+        float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -L));
+        if (masked) {
+            p0 = (col0 + e >= lo && col0 + e < hi) ? p0 : 0.f;
+            p1 = (col0 + e + 1 >= lo && col0 + e + 1 < hi) ? p1 : 0.f;
+        }
+        w[e / 2] = pack2b<kFP16>(p0 * (__uint_as_float(dp[e]) - Dl), p1 * (__uint_as_float(dp[e + 1]) - Dl));
+    }
+}
+
+template <int D, bool kFP16>
+__device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t bars, uint32_t tmem,
+                                   Ctl *ctl) {
+    using C = BwdQCfg<D>;
+    const int tid = (int)threadIdx.x;  // = query row of the tile = TMEM lane
+    const int warp = tid >> 5;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int i = un.i0 + tid;
+    const bool row_ok = i < p.Sq;
+    const size_t srow = ((size_t)un.b * p.H + un.h) * (size_t)p.Sq_pad + (size_t)i;
+    const float L = p.l2[srow];      // +inf on padding rows: P = 0
+    const float Dl = p.delta[srow];
+    const float c = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < un.n; ++t) {
+        const int k0 = (un.lo + t) * C::BN;
+        // Key column k0 + col is visible to row i iff lo <= col < hi.
+        int lo = 0, hi = min(C::BN, p.Sk - k0);
+        if (p.mask_kind != kMaskNone) hi = min(hi, i - k0 + 1);
+        if (p.mask_kind == kMaskWindow) lo = max(0, i - p.window + 1 - k0);
+        const bool masked = lo > 0 || hi < C::BN;
+        if (!wait_bar(bar_addr(bars, C::B_SFULL), t & 1, ctl, 36)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        {
+            uint32_t s[64], dp[64], w[32];
+            ptx::tmem_ld_x32<0>(lane_base + C::S_COL, s);
+            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
+            ptx::tmem_ld_x32<0>(lane_base + C::DP_COL, dp);
+            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 32, dp);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<64>(s);
+            ptx::reg_fence<64>(dp);
+            q_ds_half<kFP16>(s, dp, c, L, Dl, masked, lo, hi, 0, w);
+            // dQ of step t-1 has read the dS area
+            if (t >= 1 && !wait_bar(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            ptx::tmem_st_x32<0>(lane_base + C::DS_COL, w);
+        }
+        {
+            uint32_t s[64], dp[64], w[32];
+            ptx::tmem_ld_x32<0>(lane_base + C::S_COL + 64, s);
+            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 96, s);
+            ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + 64, dp);
+            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 96, dp);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<64>(s);
+            ptx::reg_fence<64>(dp);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
+            q_ds_half<kFP16>(s, dp, c, L, Dl, masked, lo, hi, 64, w);
+            ptx::tmem_st_x32<0>(lane_base + C::DS_COL + 32, w);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
+    }
+
+    uint8_t *dq_row = static_cast<uint8_t *>(p.dq) +
+                      (((size_t)un.b * p.H + un.h) * (size_t)p.Sq + (size_t)i) * D * 2;
+    if (un.n == 0) {
+        if (row_ok) store_zero_row(dq_row, D * 2);
+        return;
+    }
+    if (!ok || !wait_bar(bar_addr(bars, C::B_DONE), 0, ctl, 38)) return;
+    ptx::tc_fence_after();
+#pragma unroll
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld_x32<0>(lane_base + C::DQ_COL + cc * 32, r);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<32>(r);
+        if (row_ok) store_row32<kFP16>(dq_row + cc * 64, r, p.scale);
+    }
+}
+
+template <int D, bool kFP16>
+__global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ BwdParams p) {
+    using C = BwdQCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sDO = sQ + C::Q_BYTES;
+    uint8_t *sKV = sDO + C::Q_BYTES;
+    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
+    Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);
+    const uint32_t bars = ptx::smem_addr(bar_mem);
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar_addr(bars, C::B_QFULL), 1);
+        for (int s = 0; s < C::KST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_KVFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_KVEMPTY + s), 1);
+        }
+        ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_SFREE), C::NUM_COMPUTE);
+        ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_COMPUTE);
+        ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ctl->abort = 0;
+        ctl->limit_ns = p.wait_limit_ns;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == C::TMA_WARP && ptx::lane_id() == 0) {
+        ptx::prefetch_tensormap(&p.tm_q);
+        ptx::prefetch_tensormap(&p.tm_do);
+        ptx::prefetch_tensormap(&p.tm_k);
+        ptx::prefetch_tensormap(&p.tm_v);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const QUnit un = decode_q_unit(p);
+
+    if (warp < C::NUM_COMPUTE / 32) {
+        bwd_q_compute_role<D, kFP16>(p, un, bars, tmem, ctl);
+    } else if (warp == C::MMA_WARP) {
+        bwd_q_mma_role<D, kFP16>(p, un, sQ, sDO, sKV, bars, tmem, ctl);
+    } else {
+        bwd_q_tma_role<D>(p, un, sQ, sDO, sKV, bars, ctl);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

@@ -31,8 +31,8 @@ DTYPE_BF16 = 0
 DTYPE_FP16 = 1
 
 # Every entry point declared in include/fa.h.
-EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_workspace_query", "fa_status_string",
-           "fa_describe", "fa_get_device_error")
+EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_bwd", "fa_bwd_workspace_query",
+           "fa_workspace_query", "fa_status_string", "fa_describe", "fa_get_device_error")
 
 
 class FAError(RuntimeError):
@@ -70,6 +70,12 @@ def load(path: str | None = None):
         lib.fa_fwd_gqa.restype = _i
         lib.fa_fwd_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i,
                                    ctypes.c_float, _i, _i, _i, _vp]
+        lib.fa_bwd.restype = _i
+        lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                               _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i, _vp]
+        lib.fa_bwd_workspace_query.restype = _i
+        lib.fa_bwd_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                               ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_workspace_query.restype = _i
         lib.fa_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i,
                                            ctypes.POINTER(ctypes.c_size_t)]
@@ -116,6 +122,26 @@ def fwd_gqa_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, B:
                              int(B), int(H), int(H_kv), int(Sq), int(Sk), int(d),
                              ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
                              _vp(stream))
+
+
+def bwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, do_ptr: int,
+            dq_ptr: int, dk_ptr: int, dv_ptr: int, ws_ptr: int, ws_bytes: int, B: int, H: int,
+            H_kv: int, Sq: int, Sk: int, d: int, scale: float, mask_kind: int, window: int,
+            stream: int, dtype: int = DTYPE_BF16) -> int:
+    """Call fa_bwd with raw device pointers; returns the status."""
+    return load().fa_bwd(_vp(q_ptr), _vp(k_ptr), _vp(v_ptr), _vp(o_ptr), _vp(lse_ptr),
+                         _vp(do_ptr), _vp(dq_ptr), _vp(dk_ptr), _vp(dv_ptr), _vp(ws_ptr),
+                         ctypes.c_size_t(ws_bytes), int(B), int(H), int(H_kv), int(Sq), int(Sk),
+                         int(d), ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
+                         _vp(stream))
+
+
+def bwd_workspace_query(B, H, H_kv, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):
+    """(status, bytes) of fa_bwd_workspace_query."""
+    n = ctypes.c_size_t(12345)
+    st = load().fa_bwd_workspace_query(int(B), int(H), int(H_kv), int(Sq), int(Sk), int(d),
+                                       mask_code(mask), int(window), int(dtype), ctypes.byref(n))
+    return st, n.value
 
 
 def workspace_query(B, H, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):
@@ -190,6 +216,51 @@ def forward(q, k, v, scale: float | None = None, mask="none", window: int = 0,
                          int(window), sp, dt)
         _check(st, "fa_fwd_gqa")
     return out, lse
+
+
+def backward(q, k, v, o, lse, dout, scale: float | None = None, mask="none", window: int = 0,
+             dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Attention backward on CUDA tensors (fa_bwd): returns (dq, dk, dv).
+
+    q, o, dout [B, H, Sq, d]; k, v [B, H_kv, Sk, d] (bf16 or fp16, one dtype);
+    lse fp32 [B, H, Sq] from ``forward`` with the same scale, mask and window.
+    The workspace (a uint8 CUDA tensor) is allocated here unless given.
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("lse", lse)):
+        if not t.is_cuda:
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be contiguous")
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype):
+        raise FAError(FA_ERR_INVALID_ARG, "q, k, v, o, dout must share one dtype")
+    if lse.dtype != torch.float32:
+        raise FAError(FA_ERR_INVALID_ARG, "lse must be float32")
+    dt = _dtype_code(q)
+    B, H, Sq, d = q.shape
+    H_kv, Sk = k.shape[1], k.shape[2]
+    if (tuple(k.shape) != (B, H_kv, Sk, d) or tuple(v.shape) != (B, H_kv, Sk, d)
+            or tuple(o.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape)
+            or tuple(lse.shape) != (B, H, Sq)):
+        raise FAError(FA_ERR_INVALID_ARG, "shapes: q, o, dout [B,H,Sq,d]; k, v [B,H_kv,Sk,d]; lse [B,H,Sq]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st, ws_bytes = bwd_workspace_query(B, H, H_kv, Sq, Sk, d, mask, window, dt)
+    _check(st, "fa_bwd_workspace_query")
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = bwd_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                 dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(),
+                 workspace.numel(), B, H, H_kv, Sq, Sk, d, float(scale), mask_code(mask),
+                 int(window), sp, dt)
+    _check(st, "fa_bwd")
+    return dq, dk, dv
 
 
 def forward_host(q, k, v, scale: float | None = None, mask="none", window: int = 0,

@@ -161,6 +161,14 @@ def generate(w: Workload, seed: int | None = None) -> Inputs:
     return Inputs(w, qb, kb, vb)
 
 
+def grad_output(w: Workload, seed: int | None = None) -> np.ndarray:
+    """dO for the backward, [B, H, Sq, d]: standard normal float32 from
+    ``PCG64(seed + 500)`` (seed = the workload's), rounded to the 16-bit type;
+    returns the 16-bit patterns."""
+    rng = np.random.Generator(np.random.PCG64((w.seed if seed is None else seed) + 500))
+    return to_bits(rng.standard_normal(w.shape_q(), dtype=np.float32), w.dtype)
+
+
 def custom(B, H, Sq, Sk, d, dtype=BF16, mask="none", window=0, seed=0, spiky_keys=False,
            name="custom", Hkv=0) -> Inputs:
     """An ad-hoc shape drawn by the same recipe (Hkv > 0: K/V with Hkv heads)."""

@@ -41,6 +41,26 @@ def attention_flops(w) -> float:
     return 4.0 * w.d * w.B * w.H * visible_pairs_closed_form(w.Sq, w.Sk, w.mask, w.window)
 
 
+def attention_bwd_flops(w) -> float:
+    """Mask-adjusted backward FLOPs: 10*d per visible pair, the five tile
+    products of the backward (S again, dV, dP, dQ, dK), i.e. 2.5x the forward.
+    (The kernels form S and dP twice, 14*d per pair; the rate counts the
+    algorithm's 10*d.)"""
+    return 2.5 * attention_flops(w)
+
+
+def bwd_algorithmic_bytes(w) -> int:
+    """Bytes the backward must move at minimum: read Q, K, V, O, dO, lse and
+    write dQ, dK, dV (the per-row statistics workspace excluded)."""
+    e = 2
+    hkv = getattr(w, "kv_heads", w.H)
+    return (e * w.B * w.H * w.Sq * w.d * 3          # Q, O, dO
+            + e * w.B * hkv * w.Sk * w.d * 2        # K, V
+            + 4 * w.B * w.H * w.Sq                  # lse
+            + e * w.B * w.H * w.Sq * w.d            # dQ
+            + e * w.B * hkv * w.Sk * w.d * 2)       # dK, dV
+
+
 def algorithmic_bytes(w) -> int:
     """Bytes the fused forward must move at minimum: read Q,K,V once, write O, lse."""
     e = 2

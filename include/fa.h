@@ -110,6 +110,50 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
                      int mask_kind, int window, int dtype, fa_stream_t stream);
 
 /*
+ * fa_bwd -- attention backward: dQ, dK, dV from Q, K, V, the forward's O and
+ * lse, and dO = dLoss/dO ("FlashAttention: Why Tiling...", section "The
+ * backward pass: recompute instead of storing").  Each score tile is
+ * recomputed on chip from Q and K, its probabilities rebuilt from lse
+ * (P = exp(scale q.k - lse)); then dV = P^T dO, dP = dO V^T, the softmax
+ * Jacobian gives dS = P (dP - delta) with delta_i = dO_i . O_i, and
+ * dQ = scale dS K, dK = scale dS^T Q.  No S x S matrix reaches device memory.
+ * Deterministic: no atomics, the same inputs give the same bits.
+ *
+ *   q, o, dout  [B, H, Sq, d]; k, v [B, H_kv, Sk, d]; lse [B, H, Sq] fp32 as
+ *               written by fa_fwd / fa_fwd_gqa for the same q, k, v, scale,
+ *               mask and window (-inf marks a row that sees no key)
+ *   dq          [B, H, Sq, d] output; dk, dv [B, H_kv, Sk, d] outputs (with
+ *               shared K/V heads, summed over the query heads that read them)
+ *   workspace   device scratch of at least fa_bwd_workspace_query() bytes,
+ *               256-byte aligned; its contents on entry do not matter and on
+ *               return are the per-row statistics of this call
+ *   d           64 or 128 (256: FA_ERR_UNSUPPORTED -- the dK and dV
+ *               accumulators of a 128-key tile need 2 d of the 512 tensor-
+ *               memory columns)
+ *   dtype       FA_DTYPE_BF16 or FA_DTYPE_FP16 for all 16-bit tensors
+ *   the rest    as for fa_fwd_gqa
+ * All tensors are contiguous and 16-byte aligned (lse 4-byte).  Outputs may
+ * not overlap each other, the inputs or the workspace (FA_ERR_INVALID_ARG).
+ * Sq == 0 sets dk and dv to zero; q, o, lse, dout, dq and the workspace are
+ * then not examined.  Enqueues three kernels on `stream` (row statistics,
+ * dK/dV, dQ) and returns; allocates nothing.  Waits are bounded as in the
+ * forward and report through fa_get_device_error().
+ */
+fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                 const void *dout, void *dq, void *dk, void *dv, void *workspace,
+                 size_t workspace_bytes, int B, int H, int H_kv, int Sq, int Sk, int d,
+                 float scale, int mask_kind, int window, int dtype, fa_stream_t stream);
+
+/*
+ * fa_bwd_workspace_query -- workspace bytes fa_bwd needs (2 x 4 bytes per
+ * query row, rows padded per head to a multiple of 128), and the status
+ * fa_bwd would return for these sizes on the current device (pointer checks
+ * aside).  bytes must be non-NULL; it is 0 whenever the status is not FA_OK.
+ */
+fa_status fa_bwd_workspace_query(int B, int H, int H_kv, int Sq, int Sk, int d, int mask_kind,
+                                 int window, int dtype, size_t *bytes);
+
+/*
  * fa_workspace_query -- device scratch bytes fa_fwd needs for this problem
  * (always 0: the forward keeps every intermediate on chip, so its memory is
  * linear in the sequence length -- "FlashAttention: Why Tiling...", section

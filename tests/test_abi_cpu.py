@@ -168,3 +168,47 @@ def test_python_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(fa.FAError):
         fa.load(str(tmp_path / "libfa.so"))
+
+
+def _bwd(**kw):
+    g = 1 << 30
+    a = dict(q_ptr=FAKE, k_ptr=FAKE + g, v_ptr=FAKE + 2 * g, o_ptr=FAKE + 3 * g,
+             lse_ptr=FAKE + 4 * g, do_ptr=FAKE + 5 * g, dq_ptr=FAKE + 6 * g, dk_ptr=FAKE + 7 * g,
+             dv_ptr=FAKE + 8 * g, ws_ptr=FAKE + 9 * g, ws_bytes=1 << 20, B=1, H=4, H_kv=2,
+             Sq=128, Sk=128, d=128, scale=0.088, mask_kind=fa.MASK_CAUSAL, window=0, stream=0,
+             dtype=fa.DTYPE_BF16)
+    a.update(kw)
+    return fa.bwd_raw(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=256), fa.FA_ERR_UNSUPPORTED),         # dK + dV accumulators exceed tensor memory
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=3), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_kind=4), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(H_kv=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_kind=fa.MASK_SLIDING_WINDOW, window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=2 * 4 * 4 * 128 - 4), fa.FA_ERR_INVALID_ARG),   # one float short
+    (dict(ws_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(dq_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_ptr=FAKE + 9 * (1 << 30) + 16), fa.FA_ERR_MISALIGNED),  # workspace wants 256 B
+    (dict(do_ptr=FAKE + 5 * (1 << 30) + 8), fa.FA_ERR_MISALIGNED),
+    (dict(lse_ptr=FAKE + 4 * (1 << 30) + 2), fa.FA_ERR_MISALIGNED),
+    (dict(dq_ptr=FAKE + 64), fa.FA_ERR_INVALID_ARG),                 # dq overlaps q
+    (dict(dv_ptr=FAKE + 7 * (1 << 30) + 4096), fa.FA_ERR_INVALID_ARG),  # dv overlaps dk
+    (dict(ws_ptr=FAKE + 8 * (1 << 30)), fa.FA_ERR_INVALID_ARG),       # workspace on dv
+])
+def test_bwd_invalid_calls_are_rejected_before_launch(lib, kw, status):
+    assert _bwd(**kw) == status
+
+
+def test_bwd_workspace_query_sizes(lib):
+    # rejected sizes report their status and 0 bytes, before any device query
+    assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 256) == (fa.FA_ERR_UNSUPPORTED, 0)
+    assert fa.bwd_workspace_query(1, 3, 2, 128, 128, 128) == (fa.FA_ERR_INVALID_ARG, 0)
+    assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 128, "window", 0) == (fa.FA_ERR_INVALID_ARG, 0)

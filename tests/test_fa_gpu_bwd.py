@@ -1,0 +1,179 @@
+"""GPU parity of the attention backward (fa_bwd) against the fp64 oracle.
+
+The GPU forward produces O and lse, the GPU backward takes them with dO and
+returns dQ, dK, dV; the oracle differentiates the exact attention of the same
+16-bit inputs.  Tolerance (per gradient tensor G, see the design notes): the
+kernel rounds P and dS to the 16-bit input type before the tile products that
+use them and rounds each gradient once at the end, so every element carries a
+few roundings of relative size 2^-9 (bf16) of the terms it sums.  The tests
+ask max |G - G_ref| <= 2^-6 max |G_ref| + 2^-16 and mean |G - G_ref| <= 2^-7
+mean |G_ref| + 2^-16 (the absolute 2^-16 covers tensors whose exact value is
+0, such as dQ with a single key, where delta = dO . O carries the rounding of
+O): a mistake in the chain (a dropped term, a wrong index or operand) gives
+errors of the order of |G| itself.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from exact_io_aware_30_gb300 import fa, inputs
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+MAX_REL = 2.0 ** -6
+MEAN_REL = 2.0 ** -7
+ABS_FLOOR = 2.0 ** -16
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_io_aware_30_gb300 import build
+    build.build()
+    fa.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+
+
+def _dev(bits, dtype):
+    tdt = torch.bfloat16 if dtype == inputs.BF16 else torch.float16
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).cuda()
+
+
+def _np(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_gpu_bwd(inp, dout_bits):
+    w = inp.workload
+    q, k, v, do = (_dev(b, w.dtype) for b in (inp.q_bits, inp.k_bits, inp.v_bits, dout_bits))
+    o, lse = fa.forward(q, k, v, scale=w.scale, mask=w.mask, window=w.window)
+    dq, dk, dv = fa.backward(q, k, v, o, lse, do, scale=w.scale, mask=w.mask, window=w.window)
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    return _np(dq), _np(dk), _np(dv)
+
+
+def compare_grads(got, ref, names=("dq", "dk", "dv")):
+    stats = {}
+    for name, g, r in zip(names, got, ref):
+        assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+        err = np.abs(g - r)
+        scale_max = float(np.abs(r).max())
+        scale_mean = float(np.abs(r).mean())
+        st = dict(max=float(err.max()), mean=float(err.mean()), ref_max=scale_max,
+                  ref_mean=scale_mean)
+        stats[name] = st
+        assert err.max() <= MAX_REL * scale_max + ABS_FLOOR, (name, st)
+        assert err.mean() <= MEAN_REL * scale_mean + ABS_FLOOR, (name, st)
+    return stats
+
+
+def bwd_case(B, H, Sq, Sk, d, dtype, mask, window=0, seed=0, Hkv=0, spiky=False):
+    inp = inputs.custom(B, H, Sq, Sk, d, dtype, mask, window, seed=seed, Hkv=Hkv,
+                        spiky_keys=spiky)
+    dob = inputs.grad_output(inp.workload)
+    got = run_gpu_bwd(inp, dob)
+    qf, kf, vf = inp.f64()
+    ref = oracle.attention_bwd(qf, kf, vf, inputs.bits_to_f64(dob, dtype), inp.workload.scale,
+                               mask, window)
+    return compare_grads(got, ref), got, ref
+
+
+SHAPES = [(1, 1), (64, 64), (127, 127), (128, 128), (129, 129), (300, 300), (300, 173),
+          (173, 300), (700, 700)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP16])
+@pytest.mark.parametrize("mask,window", [("none", 0), ("causal", 0), ("window", 1),
+                                         ("window", 77), ("window", 300)])
+def test_bwd_parity_small(d, dtype, mask, window):
+    for i, (Sq, Sk) in enumerate(SHAPES):
+        stats, _, _ = bwd_case(1, 2, Sq, Sk, d, dtype, mask, window, seed=50 + i)
+        print(Sq, Sk, stats)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_many_units_heads_and_batches(d):
+    bwd_case(3, 5, 400, 400, d, inputs.BF16, "causal", seed=60 + d)
+    bwd_case(2, 4, 333, 517, d, inputs.BF16, "none", seed=61 + d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("H,Hkv", [(4, 2), (6, 1), (8, 8)])
+def test_bwd_grouped_query_heads(d, H, Hkv):
+    bwd_case(2, H, 300, 260, d, inputs.BF16, "causal", seed=70 + H + Hkv, Hkv=Hkv)
+    bwd_case(1, H, 200, 333, d, inputs.FP16, "window", 90, seed=71 + H + Hkv, Hkv=Hkv)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_spiky_keys(d):
+    bwd_case(1, 2, 600, 600, d, inputs.BF16, "none", seed=80 + d, spiky=True)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_rows_without_keys_get_zero_dq(d):
+    # window with Sq > Sk: rows i >= Sk + W - 1 see no key, and keys past the
+    # last row's window are seen by nobody
+    _, got, ref = bwd_case(1, 2, 400, 40, d, inputs.BF16, "window", 17, seed=90 + d)
+    dq = got[0]
+    assert np.all(dq[:, :, 40 + 16:] == 0.0)
+
+
+def test_bwd_keys_seen_by_no_row_get_zero():
+    # causal with Sk > Sq: keys j >= Sq are hidden from every row
+    _, got, _ = bwd_case(1, 2, 100, 300, 128, inputs.BF16, "causal", seed=95)
+    assert np.all(got[1][:, :, 100:] == 0.0) and np.all(got[2][:, :, 100:] == 0.0)
+
+
+def test_bwd_deterministic():
+    inp = inputs.custom(2, 3, 500, 500, 128, inputs.BF16, "causal", seed=96)
+    dob = inputs.grad_output(inp.workload)
+    a = run_gpu_bwd(inp, dob)
+    b = run_gpu_bwd(inp, dob)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_bwd_empty_query_zeroes_dk_dv():
+    k = torch.randn(1, 2, 50, 64, device="cuda").to(torch.bfloat16)
+    q = torch.zeros(1, 2, 0, 64, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 2, 0, dtype=torch.float32, device="cuda")
+    dk = torch.full_like(k, 7.0)
+    dv = torch.full_like(k, 7.0)
+    fa.backward(q, k, k, q, lse, q, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
+
+
+def test_bwd_head_dim_256_is_refused():
+    q = torch.zeros(1, 1, 8, 256, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(1, 1, 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.backward(q, q, q, q, lse, q)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+BWD_FULL = inputs.Workload("bwd_b1h32_s8192_d128_fp16_causal", 1, 32, 8192, 8192, 128,
+                           inputs.FP16, "causal", seed=1003)
+
+
+def test_bwd_full_size_two_heads():
+    # the benchmark's backward workload (8k tokens x 32 heads, causal, fp16),
+    # run whole on the GPU; the oracle differentiates heads 0 and 31, which
+    # are independent of the others
+    w = BWD_FULL
+    inp = inputs.generate(w)
+    dob = inputs.grad_output(w)
+    dq, dk, dv = run_gpu_bwd(inp, dob)
+    qf, kf, vf = inp.f64()
+    dof = inputs.bits_to_f64(dob, w.dtype)
+    for h in (0, w.H - 1):
+        sl = slice(h, h + 1)
+        ref = oracle.attention_bwd(qf[:, sl], kf[:, sl], vf[:, sl], dof[:, sl], w.scale, w.mask)
+        stats = compare_grads((dq[:, sl], dk[:, sl], dv[:, sl]), ref)
+        print(f"{w.name} head {h}: {stats}")
