@@ -26,7 +26,11 @@
 
 namespace fa {
 
-
+// Fixed device workspace of fa_bwd_noalloc (32 MiB: 4,194,304 padded query
+// rows of two fp32 statistics each).  Shared by every call on a device, so
+// calls that overlap in time on that device race on it.
+constexpr size_t kNoAllocWsBytes = (size_t)32 << 20;
+static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocWsBytes];
 
 namespace {
 
@@ -39,6 +43,7 @@ struct DeviceInfo {
     int l2_bytes = 0;
     bool attr_set[6] = {false, false, false, false, false, false};
     bool attr_bwd[8] = {false, false, false, false, false, false, false, false};
+    void *noalloc_ws = nullptr;  // device address of g_noalloc_ws in this device's context
 };
 
 std::mutex g_mutex;
@@ -533,6 +538,36 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  size_t workspace_bytes, int B, int H, int H_kv, int Sq, int Sk, int d, float scale,
                  int mask_kind, int window, int dtype, fa_stream_t stream) {
     return fa::bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, workspace, workspace_bytes, B, H, H_kv,
+                        Sq, Sk, d, scale, mask_kind, window, dtype,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv, int B,
+                         int H, int H_kv, int Sq, int Sk, int d, float scale, int mask_kind,
+                         int window, int dtype, fa_stream_t stream) {
+    fa_status st = fa::check_bwd_sizes(B, H, H_kv, Sq, Sk, d, mask_kind, window, dtype);
+    if (st != FA_OK) return st;
+    if (fa::bwd_workspace_bytes(B, H, Sq) > fa::kNoAllocWsBytes) return FA_ERR_INVALID_ARG;
+    int dev = 0;
+    fa::DeviceInfo *info = nullptr;
+    st = fa::device_info(&dev, &info);
+    if (st != FA_OK) return st;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(fa::g_mutex);
+        if (!info->noalloc_ws) {
+            // first call on this device (which is current here): look the array up once
+            void *addr = nullptr;
+            if (cudaGetSymbolAddress(&addr, fa::g_noalloc_ws) != cudaSuccess || !addr)
+                return FA_ERR_CUDA;
+            info->noalloc_ws = addr;
+        }
+        ws = info->noalloc_ws;
+    }
+    // Nothing in the workspace has to start at zero: the row-statistics kernel
+    // writes every entry the other two kernels read.
+    return fa::bwd_impl(q, k, v, o, lse, dout, dq, dk, dv, ws, fa::kNoAllocWsBytes, B, H, H_kv,
                         Sq, Sk, d, scale, mask_kind, window, dtype,
                         reinterpret_cast<cudaStream_t>(stream));
 }

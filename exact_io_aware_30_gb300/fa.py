@@ -31,8 +31,9 @@ DTYPE_BF16 = 0
 DTYPE_FP16 = 1
 
 # Every entry point declared in include/fa.h.
-EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_bwd", "fa_bwd_workspace_query",
-           "fa_workspace_query", "fa_status_string", "fa_describe", "fa_get_device_error")
+EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_bwd", "fa_bwd_noalloc",
+           "fa_bwd_workspace_query", "fa_workspace_query", "fa_status_string", "fa_describe",
+           "fa_get_device_error")
 
 
 class FAError(RuntimeError):
@@ -73,6 +74,9 @@ def load(path: str | None = None):
         lib.fa_bwd.restype = _i
         lib.fa_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i, _vp]
+        lib.fa_bwd_noalloc.restype = _i
+        lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                       _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i, _vp]
         lib.fa_bwd_workspace_query.restype = _i
         lib.fa_bwd_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                                ctypes.POINTER(ctypes.c_size_t)]
@@ -134,6 +138,18 @@ def bwd_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, do_ptr
                          ctypes.c_size_t(ws_bytes), int(B), int(H), int(H_kv), int(Sq), int(Sk),
                          int(d), ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
                          _vp(stream))
+
+
+def bwd_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int, do_ptr: int,
+                    dq_ptr: int, dk_ptr: int, dv_ptr: int, B: int, H: int, H_kv: int, Sq: int,
+                    Sk: int, d: int, scale: float, mask_kind: int, window: int, stream: int,
+                    dtype: int = DTYPE_BF16) -> int:
+    """Call fa_bwd_noalloc (the library's fixed workspace) with raw device pointers."""
+    return load().fa_bwd_noalloc(_vp(q_ptr), _vp(k_ptr), _vp(v_ptr), _vp(o_ptr), _vp(lse_ptr),
+                                 _vp(do_ptr), _vp(dq_ptr), _vp(dk_ptr), _vp(dv_ptr), int(B),
+                                 int(H), int(H_kv), int(Sq), int(Sk), int(d),
+                                 ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
+                                 _vp(stream))
 
 
 def bwd_workspace_query(B, H, H_kv, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):

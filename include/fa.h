@@ -145,6 +145,28 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
                  float scale, int mask_kind, int window, int dtype, fa_stream_t stream);
 
 /*
+ * fa_bwd_noalloc -- fa_bwd for callers that cannot provide device memory:
+ * the same computation and results, with the workspace taken from a fixed
+ * 32 MiB array in the library's device memory instead of the caller.  The
+ * pages have no counterpart to this entry point; it exists for the calling
+ * convention only.
+ *
+ *   arguments   as for fa_bwd, without workspace and workspace_bytes
+ *   limit       fa_bwd_workspace_query() bytes <= 32 MiB, i.e.
+ *               B * H * ceil(Sq / 128) * 128 <= 4,194,304 query rows;
+ *               larger problems return FA_ERR_INVALID_ARG (use fa_bwd)
+ * The first call on a device looks up the array's device address (with that
+ * device current) and should come before any stream capture.  Nothing is
+ * allocated or freed by any call.  Every call on a device uses the same array:
+ * calls whose work overlaps in time on one device (another stream, another
+ * host thread) race on it and give undefined results.
+ */
+fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void *o,
+                         const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                         int B, int H, int H_kv, int Sq, int Sk, int d, float scale,
+                         int mask_kind, int window, int dtype, fa_stream_t stream);
+
+/*
  * fa_bwd_workspace_query -- workspace bytes fa_bwd needs (2 x 4 bytes per
  * query row, rows padded per head to a multiple of 128), and the status
  * fa_bwd would return for these sizes on the current device (pointer checks
