@@ -160,10 +160,18 @@ struct BwdKVCfg {
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int STAT_BYTES = 2 * BM * 4;  // l2 of the step's rows, then delta
-    static constexpr int NUM_COMPUTE = 128;        // warps 0-3: one key row per thread
-    static constexpr int MMA_WARP = 4;
-    static constexpr int TMA_WARP = 5;
-    static constexpr int NUM_THREADS = 192;
+    // Warps 0-3 compute: warp w owns key rows 32 w .. + 31 (its TMEM lanes),
+    // one per thread, and all 64 query columns of every step; warp 4 issues
+    // the MMAs, warp 5 the copies.  (Eight compute warps splitting the
+    // columns measured slower: this kernel's per-step MMA issue, 24
+    // instructions of which 16 are N = 64, is the tighter limit, and the
+    // issuing warp then shares its sub-partition with two compute warps.)
+    static constexpr int NUM_COMPUTE = 128;
+    static constexpr int WG = NUM_COMPUTE / 128;   // warpgroups splitting the columns
+    static constexpr int COLS = BM / WG;           // query columns per compute warp
+    static constexpr int MMA_WARP = NUM_COMPUTE / 32;
+    static constexpr int TMA_WARP = MMA_WARP + 1;
+    static constexpr int NUM_THREADS = NUM_COMPUTE + 64;
     // Tensor memory: dV and dK accumulators, S^T and dP^T (fp32, 64 columns
     // each), P^T and dS^T (16-bit pairs, 32 columns each).
     static constexpr uint32_t TMEM_COLS = 512;
@@ -350,43 +358,48 @@ template <int D, bool kFP16>
 __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const uint8_t *sStat,
                                     uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdKVCfg<D>;
-    const int tid = (int)threadIdx.x;  // = key row of the tile = TMEM lane
-    const int warp = tid >> 5;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const int j = un.j0 + tid;
+    constexpr int NC = C::COLS;
+    const int warp = (int)threadIdx.x >> 5;
+    const int r = 32 * (warp & 3) + ((int)threadIdx.x & 31);  // key row of the tile = TMEM lane
+    const int h = warp >> 2;                                  // query columns h*NC .. + NC
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int j = un.j0 + r;
     const bool row_ok = j < p.Sk;
     const float c = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < un.steps; ++t) {
         const int slot = t % C::ST;
-        const int i0 = (un.it_lo + t % un.n_i) * C::BM;
+        const int i0 = (un.it_lo + t % un.n_i) * C::BM + h * NC;  // first query row of the columns
         // The statistics arrived with the step's Q tile; S^T and dP^T are ready.
         ok = ok && wait_bar(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
         ok = ok && wait_bar(bar_addr(bars, C::B_SFULL), t & 1, ctl, 27);
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t s[64], dp[64];
-        ptx::tmem_ld_x32<0>(lane_base + C::S_COL, s);
-        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
-        ptx::tmem_ld_x32<0>(lane_base + C::DP_COL, dp);
-        ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 32, dp);
+        uint32_t s[NC], dp[NC];
+        ptx::tmem_ld_x32<0>(lane_base + C::S_COL + h * NC, s);
+        ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
+        if constexpr (NC == 64) {
+            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
+            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 32, dp);
+        }
         ptx::tmem_wait_ld();
-        ptx::reg_fence<64>(s);
-        ptx::reg_fence<64>(dp);
+        ptx::reg_fence<NC>(s);
+        ptx::reg_fence<NC>(dp);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
 
-        // Query column i0 + col is visible to key j iff lo <= col < hi.
-        int lo = 0, hi = C::BM;
+        // Query row i0 + col is visible to key j iff lo <= col < hi.
+        int lo = 0, hi = NC;
         if (p.mask_kind != kMaskNone) lo = j - i0;
-        if (p.mask_kind == kMaskWindow) hi = (int)min((long long)C::BM, (long long)j + p.window - i0);
-        if (!row_ok) lo = C::BM;
-        const bool masked = lo > 0 || hi < C::BM;
-        const float4 *L4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES);
-        const float4 *D4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4);
-        uint32_t pw[32], dsw[32];
+        if (p.mask_kind == kMaskWindow) hi = (int)min((long long)NC, (long long)j + p.window - i0);
+        if (!row_ok) lo = NC;
+        const bool masked = lo > 0 || hi < NC;
+        const float4 *L4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES) + h * (NC / 4);
+        const float4 *D4 =
+            reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4) + h * (NC / 4);
+        uint32_t pw[NC / 2], dsw[NC / 2];
 #pragma unroll
-        for (int q = 0; q < C::BM / 4; ++q) {
+        for (int q = 0; q < NC / 4; ++q) {
             const float4 l = L4[q], dl = D4[q];
             const float lv[4] = {l.x, l.y, l.z, l.w}, dv[4] = {dl.x, dl.y, dl.z, dl.w};
             float pv[4], dsv[4];
@@ -409,39 +422,45 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
             break;
         }
         ptx::tc_fence_after();
-        ptx::tmem_st_x32<0>(lane_base + C::P_COL, pw);
-        ptx::tmem_st_x32<0>(lane_base + C::DS_COL, dsw);
+        if constexpr (NC == 64) {
+            ptx::tmem_st_x32<0>(lane_base + C::P_COL, pw);
+            ptx::tmem_st_x32<0>(lane_base + C::DS_COL, dsw);
+        } else {
+            ptx::tmem_st_x16<0>(lane_base + C::P_COL + h * (NC / 2), pw);
+            ptx::tmem_st_x16<0>(lane_base + C::DS_COL + h * (NC / 2), dsw);
+        }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
     }
 
-    // Epilogue: dV and scale * dK of this thread's key row.
+    // Epilogue: dV and scale * dK of this thread's key row, columns h*D/WG ..
     if (un.steps > 0) {
         if (!ok || !wait_bar(bar_addr(bars, C::B_DONE), 0, ctl, 29)) return;
         ptx::tc_fence_after();
     }
+    constexpr int HALF = D / C::WG;
     const size_t row = ((size_t)un.b * p.Hkv + un.kvh) * (size_t)p.Sk + (size_t)j;
-    uint8_t *dv_row = static_cast<uint8_t *>(p.dv) + row * D * 2;
-    uint8_t *dk_row = static_cast<uint8_t *>(p.dk) + row * D * 2;
+    uint8_t *dv_row = static_cast<uint8_t *>(p.dv) + row * D * 2 + h * HALF * 2;
+    uint8_t *dk_row = static_cast<uint8_t *>(p.dk) + row * D * 2 + h * HALF * 2;
     if (un.steps == 0) {
         if (row_ok) {
-            store_zero_row(dv_row, D * 2);
-            store_zero_row(dk_row, D * 2);
+            store_zero_row(dv_row, HALF * 2);
+            store_zero_row(dk_row, HALF * 2);
         }
         return;
     }
 #pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld_x32<0>(lane_base + C::DV_COL + cc * 32, r);
+    for (int cc = 0; cc < HALF / 32; ++cc) {
+        uint32_t rr[32];
+        ptx::tmem_ld_x32<0>(lane_base + C::DV_COL + h * HALF + cc * 32, rr);
         ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(r);
-        if (row_ok) store_row32<kFP16>(dv_row + cc * 64, r, 1.f);
-        ptx::tmem_ld_x32<0>(lane_base + C::DK_COL + cc * 32, r);
+        ptx::reg_fence<32>(rr);
+        if (row_ok) store_row32<kFP16>(dv_row + cc * 64, rr, 1.f);
+        ptx::tmem_ld_x32<0>(lane_base + C::DK_COL + h * HALF + cc * 32, rr);
         ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(r);
-        if (row_ok) store_row32<kFP16>(dk_row + cc * 64, r, p.scale);
+        ptx::reg_fence<32>(rr);
+        if (row_ok) store_row32<kFP16>(dk_row + cc * 64, rr, p.scale);
     }
 }
 
@@ -518,15 +537,20 @@ template <int D>
 struct BwdQCfg {
     static constexpr int BM = 128;                // query rows per CTA = TMEM lanes
     static constexpr int BN = 128;                // keys per step
-    static constexpr int KST = (D == 64) ? 3 : 2; // K/V stages
+    static constexpr int KST = (D == 64) ? 4 : 3; // K stages (free once dQ of the step ran)
+    static constexpr int VST = (D == 64) ? 3 : 2; // V stages (free once dP of the step ran)
     static constexpr int Q_BOX = BM * 128;
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;
-    static constexpr int NUM_COMPUTE = 128;       // warps 0-3: one query row per thread
-    static constexpr int MMA_WARP = 4;
-    static constexpr int TMA_WARP = 5;
-    static constexpr int NUM_THREADS = 192;
+    // Warps 0-7 compute: warp w owns query rows 32 (w & 3) .. + 31 (its TMEM
+    // lanes), one per thread, and key columns 64 (w >> 2) .. + 63 of every
+    // step; warp 8 issues the MMAs, warp 9 the copies.
+    static constexpr int NUM_COMPUTE = 256;
+    static constexpr int COLS = BN / 2;
+    static constexpr int MMA_WARP = 8;
+    static constexpr int TMA_WARP = 9;
+    static constexpr int NUM_THREADS = 320;
     // Tensor memory: S and dP (fp32, BN columns each), the dQ accumulator,
     // dS (16-bit pairs, BN/2 columns).
     static constexpr uint32_t TMEM_COLS = 512;
@@ -535,16 +559,18 @@ struct BwdQCfg {
     static constexpr uint32_t DQ_COL = 256;
     static constexpr uint32_t DS_COL = 384;
     static constexpr int B_QFULL = 0;
-    static constexpr int B_KVFULL = 1;                // [KST]
-    static constexpr int B_KVEMPTY = B_KVFULL + KST;  // [KST]
-    static constexpr int B_SFULL = B_KVEMPTY + KST;
+    static constexpr int B_KFULL = 1;                 // [KST]
+    static constexpr int B_KEMPTY = B_KFULL + KST;    // [KST]
+    static constexpr int B_VFULL = B_KEMPTY + KST;    // [VST]
+    static constexpr int B_VEMPTY = B_VFULL + VST;    // [VST]
+    static constexpr int B_SFULL = B_VEMPTY + VST;
     static constexpr int B_SFREE = B_SFULL + 1;
     static constexpr int B_PFULL = B_SFREE + 1;
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_DONE = B_PFREE + 1;
     static constexpr int B_DRAIN = B_DONE + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
-    static constexpr int SMEM_TILES = 2 * Q_BYTES + KST * 2 * KV_BYTES;
+    static constexpr int SMEM_TILES = 2 * Q_BYTES + (KST + VST) * KV_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(D <= 128, "one dQ accumulator of d columns next to S and dP");
     static_assert(DQ_COL + D <= DS_COL && DS_COL + BN / 2 <= TMEM_COLS, "tensor memory overflow");
@@ -582,7 +608,7 @@ __device__ __forceinline__ QUnit decode_q_unit(const BwdParams &p) {
 
 template <int D>
 __device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
-                               uint8_t *sKV, uint32_t bars, Ctl *ctl) {
+                               uint8_t *sK, uint8_t *sV, uint32_t bars, Ctl *ctl) {
     using C = BwdQCfg<D>;
     const bool leader = ptx::lane_id() == 0;
     const uint64_t pol_last = ptx::policy_evict_last();
@@ -599,39 +625,54 @@ __device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
                              pol_first);
         }
     }
-    int issued = 0;
+    // V of a step frees earlier (after dP) than K (after dQ), so the copies
+    // go out in the order K_t, V_t and a V copy rarely waits behind a K slot.
+    int k_issued = 0, v_issued = 0;
     bool ok = true;
-    for (int t = 0; t < un.n; ++t) {
-        const int slot = t % C::KST;
-        if (!wait_bar_backoff(bar_addr(bars, C::B_KVEMPTY + slot), ((t / C::KST) & 1) ^ 1, ctl, 31)) {
+    for (int t = 0; t < un.n && ok; ++t) {
+        const int k0 = (un.lo + t) * C::BN;
+        const int ks = t % C::KST, vs = t % C::VST;
+        if (!wait_bar_backoff(bar_addr(bars, C::B_KEMPTY + ks), ((t / C::KST) & 1) ^ 1, ctl, 31)) {
             ok = false;
             break;
         }
         if (leader) {
-            const int k0 = (un.lo + t) * C::BN;
-            const uint32_t fb = bar_addr(bars, C::B_KVFULL + slot);
-            ptx::mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
-            const uint32_t dk = ptx::smem_addr(sKV + slot * 2 * C::KV_BYTES);
+            const uint32_t fb = bar_addr(bars, C::B_KFULL + ks);
+            ptx::mbar_arrive_expect_tx(fb, C::KV_BYTES);
 #pragma unroll
-            for (int c = 0; c < D / 64; ++c) {
-                ptx::tma_load_4d(dk + c * C::KV_BOX, &p.tm_k, fb, c * 64, k0, un.kvh, un.b, pol_last);
-                ptx::tma_load_4d(dk + C::KV_BYTES + c * C::KV_BOX, &p.tm_v, fb, c * 64, k0, un.kvh, un.b,
-                                 pol_last);
-            }
+            for (int c = 0; c < D / 64; ++c)
+                ptx::tma_load_4d(ptx::smem_addr(sK + ks * C::KV_BYTES) + c * C::KV_BOX, &p.tm_k, fb, c * 64,
+                                 k0, un.kvh, un.b, pol_last);
         }
         __syncwarp();
-        ++issued;
+        ++k_issued;
+        if (!wait_bar_backoff(bar_addr(bars, C::B_VEMPTY + vs), ((t / C::VST) & 1) ^ 1, ctl, 39)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            const uint32_t fb = bar_addr(bars, C::B_VFULL + vs);
+            ptx::mbar_arrive_expect_tx(fb, C::KV_BYTES);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                ptx::tma_load_4d(ptx::smem_addr(sV + vs * C::KV_BYTES) + c * C::KV_BOX, &p.tm_v, fb, c * 64,
+                                 k0, un.kvh, un.b, pol_last);
+        }
+        __syncwarp();
+        ++v_issued;
     }
     wait_bar_drain(bar_addr(bars, C::B_QFULL), 0);
     if (!ok) {
-        for (int t = issued - C::KST > 0 ? issued - C::KST : 0; t < issued; ++t)
-            wait_bar_drain(bar_addr(bars, C::B_KVFULL + t % C::KST), (t / C::KST) & 1);
+        for (int t = k_issued - C::KST > 0 ? k_issued - C::KST : 0; t < k_issued; ++t)
+            wait_bar_drain(bar_addr(bars, C::B_KFULL + t % C::KST), (t / C::KST) & 1);
+        for (int t = v_issued - C::VST > 0 ? v_issued - C::VST : 0; t < v_issued; ++t)
+            wait_bar_drain(bar_addr(bars, C::B_VFULL + t % C::VST), (t / C::VST) & 1);
     }
 }
 
 template <int D, bool kFP16>
 __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
-                               uint8_t *sKV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+                               uint8_t *sK, uint8_t *sV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdQCfg<D>;
     constexpr uint32_t kIdescS = make_idesc(C::BM, C::BN, kFP16, false);
     constexpr uint32_t kIdescG = make_idesc(C::BM, D, kFP16, true);  // dQ: N = d, K MN-major
@@ -641,8 +682,9 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
     bool ok = un.n == 0 || wait_bar(bar_addr(bars, C::B_QFULL), 0, ctl, 32);
     for (int t = 0; ok && t <= un.n; ++t) {
         if (t < un.n) {
-            const int slot = t % C::KST;
-            if (!wait_bar(bar_addr(bars, C::B_KVFULL + slot), (t / C::KST) & 1, ctl, 33)) {
+            const int ks = t % C::KST, vs = t % C::VST;
+            if (!wait_bar(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 33) ||
+                !wait_bar(bar_addr(bars, C::B_VFULL + vs), (t / C::VST) & 1, ctl, 40)) {
                 ok = false;
                 break;
             }
@@ -652,9 +694,8 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
             }
             ptx::tc_fence_after();
             if (leader) {
-                const uint32_t ka = ptx::smem_addr(sKV + slot * 2 * C::KV_BYTES);
-                const uint64_t kd = smem_desc(ka, 16);
-                const uint64_t vd = smem_desc(ka + C::KV_BYTES, 16);
+                const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::KV_BYTES), 16);
+                const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::KV_BYTES), 16);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
@@ -664,6 +705,7 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
                     ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
                                 kIdescS, kk > 0 ? 1u : 0u);
                 ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
             }
             __syncwarp();
         }
@@ -676,13 +718,13 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
             ptx::tc_fence_after();
             if (leader) {
                 // K as the MN-major B operand: K = keys (16 = 2048 bytes), N = d.
-                const uint64_t km = smem_desc(ptx::smem_addr(sKV + slot * 2 * C::KV_BYTES), C::KV_BOX);
+                const uint64_t km = smem_desc(ptx::smem_addr(sK + slot * C::KV_BYTES), C::KV_BOX);
 #pragma unroll
                 for (int kk = 0; kk < C::BN / 16; ++kk)
                     ptx::mma_ts(tmem + C::DQ_COL, tmem + C::DS_COL + kk * 8, km + (uint32_t)((kk * 2048) >> 4),
                                 kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
                 ptx::mma_commit(bar_addr(bars, C::B_PFREE));
-                ptx::mma_commit(bar_addr(bars, C::B_KVEMPTY + slot));
+                ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + slot));
                 if (tp + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_DONE));
             }
             __syncwarp();
@@ -693,31 +735,16 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
     wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
 }
 
-// dS of 64 key columns (col0 .. col0 + 63 of the tile) into 32 packed words.
-template <bool kFP16>
-__device__ __forceinline__ void q_ds_half(const uint32_t (&s)[64], const uint32_t (&dp)[64], float c,
-                                          float L, float Dl, bool masked, int lo, int hi, int col0,
-                                          uint32_t (&w)[32]) {
-#pragma unroll
-    for (int e = 0; e < 64; e += 2) {
-        float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[e]), c, -L));
-        float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -L));
-        if (masked) {
-            p0 = (col0 + e >= lo && col0 + e < hi) ? p0 : 0.f;
-            p1 = (col0 + e + 1 >= lo && col0 + e + 1 < hi) ? p1 : 0.f;
-        }
-        w[e / 2] = pack2b<kFP16>(p0 * (__uint_as_float(dp[e]) - Dl), p1 * (__uint_as_float(dp[e + 1]) - Dl));
-    }
-}
-
 template <int D, bool kFP16>
 __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t bars, uint32_t tmem,
                                    Ctl *ctl) {
     using C = BwdQCfg<D>;
-    const int tid = (int)threadIdx.x;  // = query row of the tile = TMEM lane
-    const int warp = tid >> 5;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const int i = un.i0 + tid;
+    constexpr int NC = C::COLS;
+    const int warp = (int)threadIdx.x >> 5;
+    const int r = 32 * (warp & 3) + ((int)threadIdx.x & 31);  // query row of the tile = TMEM lane
+    const int h = warp >> 2;                                  // key columns h*NC .. + NC
+    const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int i = un.i0 + r;
     const bool row_ok = i < p.Sq;
     const size_t srow = ((size_t)un.b * p.H + un.h) * (size_t)p.Sq_pad + (size_t)i;
     const float L = p.l2[srow];      // +inf on padding rows: P = 0
@@ -725,69 +752,66 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
     const float c = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < un.n; ++t) {
-        const int k0 = (un.lo + t) * C::BN;
+        const int k0 = (un.lo + t) * C::BN + h * NC;  // first key of this warp's columns
         // Key column k0 + col is visible to row i iff lo <= col < hi.
-        int lo = 0, hi = min(C::BN, p.Sk - k0);
+        int lo = 0, hi = min(NC, p.Sk - k0);
         if (p.mask_kind != kMaskNone) hi = min(hi, i - k0 + 1);
         if (p.mask_kind == kMaskWindow) lo = max(0, i - p.window + 1 - k0);
-        const bool masked = lo > 0 || hi < C::BN;
+        const bool masked = lo > 0 || hi < NC;
         if (!wait_bar(bar_addr(bars, C::B_SFULL), t & 1, ctl, 36)) {
             ok = false;
             break;
         }
         ptx::tc_fence_after();
-        {
-            uint32_t s[64], dp[64], w[32];
-            ptx::tmem_ld_x32<0>(lane_base + C::S_COL, s);
-            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
-            ptx::tmem_ld_x32<0>(lane_base + C::DP_COL, dp);
-            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 32, dp);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<64>(s);
-            ptx::reg_fence<64>(dp);
-            q_ds_half<kFP16>(s, dp, c, L, Dl, masked, lo, hi, 0, w);
-            // dQ of step t-1 has read the dS area
-            if (t >= 1 && !wait_bar(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
-                ok = false;
-                break;
+        uint32_t s[NC], dp[NC], w[NC / 2];
+        ptx::tmem_ld_x32<0>(lane_base + C::S_COL + h * NC, s);
+        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + h * NC + 32, s);
+        ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
+        ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + h * NC + 32, dp);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<NC>(s);
+        ptx::reg_fence<NC>(dp);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
+#pragma unroll
+        for (int e = 0; e < NC; e += 2) {
+            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[e]), c, -L));
+            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -L));
+            if (masked) {
+                p0 = (e >= lo && e < hi) ? p0 : 0.f;
+                p1 = (e + 1 >= lo && e + 1 < hi) ? p1 : 0.f;
             }
-            ptx::tc_fence_after();
-            ptx::tmem_st_x32<0>(lane_base + C::DS_COL, w);
+            w[e / 2] = pack2b<kFP16>(p0 * (__uint_as_float(dp[e]) - Dl),
+                                     p1 * (__uint_as_float(dp[e + 1]) - Dl));
         }
-        {
-            uint32_t s[64], dp[64], w[32];
-            ptx::tmem_ld_x32<0>(lane_base + C::S_COL + 64, s);
-            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 96, s);
-            ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + 64, dp);
-            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 96, dp);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<64>(s);
-            ptx::reg_fence<64>(dp);
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
-            q_ds_half<kFP16>(s, dp, c, L, Dl, masked, lo, hi, 64, w);
-            ptx::tmem_st_x32<0>(lane_base + C::DS_COL + 32, w);
+        // dQ of step t-1 has read the dS area
+        if (t >= 1 && !wait_bar(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
+            ok = false;
+            break;
         }
+        ptx::tc_fence_after();
+        ptx::tmem_st_x32<0>(lane_base + C::DS_COL + h * (NC / 2), w);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
     }
 
+    constexpr int HALF = D / 2;
     uint8_t *dq_row = static_cast<uint8_t *>(p.dq) +
-                      (((size_t)un.b * p.H + un.h) * (size_t)p.Sq + (size_t)i) * D * 2;
+                      (((size_t)un.b * p.H + un.h) * (size_t)p.Sq + (size_t)i) * D * 2 + h * HALF * 2;
     if (un.n == 0) {
-        if (row_ok) store_zero_row(dq_row, D * 2);
+        if (row_ok) store_zero_row(dq_row, HALF * 2);
         return;
     }
     if (!ok || !wait_bar(bar_addr(bars, C::B_DONE), 0, ctl, 38)) return;
     ptx::tc_fence_after();
 #pragma unroll
-    for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld_x32<0>(lane_base + C::DQ_COL + cc * 32, r);
+    for (int cc = 0; cc < HALF / 32; ++cc) {
+        uint32_t rr[32];
+        ptx::tmem_ld_x32<0>(lane_base + C::DQ_COL + h * HALF + cc * 32, rr);
         ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(r);
-        if (row_ok) store_row32<kFP16>(dq_row + cc * 64, r, p.scale);
+        ptx::reg_fence<32>(rr);
+        if (row_ok) store_row32<kFP16>(dq_row + cc * 64, rr, p.scale);
     }
 }
 
@@ -800,7 +824,8 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem;
     uint8_t *sDO = sQ + C::Q_BYTES;
-    uint8_t *sKV = sDO + C::Q_BYTES;
+    uint8_t *sK = sDO + C::Q_BYTES;
+    uint8_t *sV = sK + C::KST * C::KV_BYTES;
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);
@@ -810,8 +835,12 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar_addr(bars, C::B_QFULL), 1);
         for (int s = 0; s < C::KST; ++s) {
-            ptx::mbar_init(bar_addr(bars, C::B_KVFULL + s), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_KVEMPTY + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_KFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_VFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_VEMPTY + s), 1);
         }
         ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_SFREE), C::NUM_COMPUTE);
@@ -843,9 +872,9 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
     if (warp < C::NUM_COMPUTE / 32) {
         bwd_q_compute_role<D, kFP16>(p, un, bars, tmem, ctl);
     } else if (warp == C::MMA_WARP) {
-        bwd_q_mma_role<D, kFP16>(p, un, sQ, sDO, sKV, bars, tmem, ctl);
+        bwd_q_mma_role<D, kFP16>(p, un, sQ, sDO, sK, sV, bars, tmem, ctl);
     } else {
-        bwd_q_tma_role<D>(p, un, sQ, sDO, sKV, bars, ctl);
+        bwd_q_tma_role<D>(p, un, sQ, sDO, sK, sV, bars, ctl);
     }
     __syncwarp();
     ptx::tc_fence_before();
