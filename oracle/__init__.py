@@ -119,6 +119,12 @@ class OracleLib:
             _dp, _dp, _dp, _dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_int,
             _dp, _dp, _dp]
+        _i32p = ctypes.POINTER(ctypes.c_int32)
+        lib.oracle_attn_paged.restype = ctypes.c_int
+        lib.oracle_attn_paged.argtypes = [
+            _dp, _dp, _dp, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+            _dp, _dp]
         lib.oracle_set_threads.restype = None
         lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_max_threads.restype = ctypes.c_int
@@ -197,6 +203,32 @@ class OracleLib:
             raise ValueError("oracle_attn_bwd rejected its arguments")
         return dq, dk, dv
 
+    def attention_paged(self, q, k_cache, v_cache, block_table, seq_lens, scale: float,
+                        mask="none"):
+        """Attention of the Sq new rows of each request over its paged K/V cache.
+
+        q: [B, H, Sq, d]; k_cache, v_cache: [num_blocks, Hkv, block_size, d];
+        block_table: int [B, max_blocks]; seq_lens: int [B] (cached tokens,
+        the last Sq being the new rows').  mask: "none" or "causal" (row i at
+        position seq_lens[b] - Sq + i).  Returns (o [B,H,Sq,d], lse [B,H,Sq]).
+        """
+        q, kc, vc = _f64(q), _f64(k_cache), _f64(v_cache)
+        bt = np.ascontiguousarray(block_table, dtype=np.int32)
+        sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+        B, H, Sq, d = q.shape
+        nb, Hkv, bs, d2 = kc.shape
+        if vc.shape != kc.shape or d2 != d or bt.ndim != 2 or bt.shape[0] != B or sl.shape != (B,):
+            raise ValueError("shapes: q [B,H,Sq,d]; caches [blocks,Hkv,bs,d]; table [B,n]; lens [B]")
+        o = np.empty((B, H, Sq, d), np.float64)
+        lse = np.empty((B, H, Sq), np.float64)
+        i32 = ctypes.POINTER(ctypes.c_int32)
+        rc = self.lib.oracle_attn_paged(_ptr(q), _ptr(kc), _ptr(vc), bt.ctypes.data_as(i32),
+                                        sl.ctypes.data_as(i32), B, H, Hkv, Sq, d, bs, bt.shape[1],
+                                        nb, float(scale), _mask(mask), _ptr(o), _ptr(lse))
+        if rc != 0:
+            raise ValueError("oracle_attn_paged rejected its arguments")
+        return o, lse
+
     def online_trace(self, q_row, K, V, scale: float, block_size: int):
         """Running (m, l, unnormalised O) after each key block for one query row.
 
@@ -257,6 +289,10 @@ def attention_blocked(*args, **kwargs):
 
 def attention_bwd(*args, **kwargs):
     return default().attention_bwd(*args, **kwargs)
+
+
+def attention_paged(*args, **kwargs):
+    return default().attention_paged(*args, **kwargs)
 
 
 def online_trace(*args, **kwargs):

@@ -560,3 +560,96 @@ int oracle_attn_bwd(const double *q, const double *k, const double *v, const dou
     free(rt);
     return failed ? -1 : 0;
 }
+
+/*
+ * Attention of new query rows over a paged key/value cache
+ * ("Flash attention and memory-efficient attention variants", sections
+ * "A different bottleneck: the KV cache during inference" and "PagedAttention:
+ * memory management borrowed from an operating system"): the cache is split
+ * into fixed-size physical blocks of block_size tokens, and each request's
+ * block table maps its logical block n (tokens n*block_size ..) to a physical
+ * block anywhere in the pool; the attention walks the table and gathers.
+ *
+ * Request b holds seq_lens[b] cached tokens, the last Sq of which belong to
+ * its Sq new query rows (Sq = 1 is one decoding step).  Query row i sits at
+ * position seq_lens[b] - Sq + i.  Visibility (the reading for decoding, where
+ * the newest token is the last position):
+ *   mask_kind 0  none:    every cached token j < seq_lens[b];
+ *   mask_kind 1  causal:  tokens j <= seq_lens[b] - Sq + i.
+ *
+ * q: [B, H, Sq, d]; k_cache, v_cache: [num_blocks, Hkv, block_size, d];
+ * block_table: [B, max_blocks] (entries past the request's last block are not
+ * read); seq_lens: [B], each in [Sq, max_blocks * block_size]; o: [B, H, Sq,
+ * d]; lse: [B, H, Sq].  Query head h reads K/V head h / (H / Hkv).
+ */
+int oracle_attn_paged(const double *q, const double *k_cache, const double *v_cache,
+                      const int32_t *block_table, const int32_t *seq_lens, int B, int H, int Hkv,
+                      int Sq, int d, int block_size, int max_blocks, int num_blocks,
+                      double scale, int mask_kind, double *o, double *lse)
+{
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Sq < 1 || d < 1 || block_size < 1 ||
+        max_blocks < 1 || num_blocks < 1 || (mask_kind != ORC_MASK_NONE && mask_kind != ORC_MASK_CAUSAL))
+        return -1;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        if (L < Sq || L > max_blocks * block_size)
+            return -1;
+        for (int n = 0; n < (L + block_size - 1) / block_size; ++n)
+            if (block_table[(int64_t)b * max_blocks + n] < 0 ||
+                block_table[(int64_t)b * max_blocks + n] >= num_blocks)
+                return -1;
+    }
+    const int group = H / Hkv;
+    const int64_t n_rows = (int64_t)B * H * Sq;
+    int failed = 0;
+#pragma omp parallel
+    {
+        int max_len = 0;
+        for (int b = 0; b < B; ++b)
+            if (seq_lens[b] > max_len)
+                max_len = seq_lens[b];
+        double *S = (double *)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+        if (S == NULL) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (S == NULL)
+                continue;
+            const int64_t b = r / ((int64_t)H * Sq), h = (r / Sq) % H, i = r % Sq;
+            const int64_t kvh = h / group;
+            const int L = seq_lens[b];
+            const int64_t last = (mask_kind == ORC_MASK_CAUSAL) ? L - Sq + i : L - 1;
+            const double *qi = q + r * (int64_t)d;
+            double m = -INFINITY;
+            for (int64_t j = 0; j <= last; ++j) {
+                const int64_t blk = block_table[b * max_blocks + j / block_size];
+                const double *kj = k_cache + ((blk * Hkv + kvh) * block_size + j % block_size) * (int64_t)d;
+                double dot = 0.0;
+                for (int c = 0; c < d; ++c)
+                    dot += qi[c] * kj[c];
+                S[j] = scale * dot;
+                if (S[j] > m)
+                    m = S[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j <= last; ++j) {
+                S[j] = exp(S[j] - m);
+                l += S[j];
+            }
+            double *oi = o + r * (int64_t)d;
+            for (int c = 0; c < d; ++c)
+                oi[c] = 0.0;
+            for (int64_t j = 0; j <= last; ++j) {
+                const int64_t blk = block_table[b * max_blocks + j / block_size];
+                const double *vj = v_cache + ((blk * Hkv + kvh) * block_size + j % block_size) * (int64_t)d;
+                for (int c = 0; c < d; ++c)
+                    oi[c] += (S[j] / l) * vj[c];
+            }
+            lse[r] = m + log(l);
+        }
+        free(S);
+    }
+    return failed ? -1 : 0;
+}

@@ -447,6 +447,84 @@ def test_bwd_closed_forms():
     check_bwd_closed_forms(oracle.default(), np.random.default_rng(23))
 
 
+# ---------------------------------------------------------------------------
+# Paged K/V cache (decoding)
+# ---------------------------------------------------------------------------
+
+def _paged_case(rng, B, H, Hkv, Sq, d, bs, lens, num_blocks):
+    max_blocks = max(-(-L // bs) for L in lens) + 1
+    perm = rng.permutation(num_blocks)
+    table = np.full((B, max_blocks), -7, np.int32)  # entries past a request's blocks: junk
+    used = 0
+    for b, L in enumerate(lens):
+        n = -(-L // bs)
+        table[b, :n] = perm[used:used + n]
+        used += n
+    kc = rng.standard_normal((num_blocks, Hkv, bs, d))
+    vc = rng.standard_normal((num_blocks, Hkv, bs, d))
+    q = rng.standard_normal((B, H, Sq, d))
+    return q, kc, vc, table, np.array(lens, np.int32)
+
+
+def _gather(cache, table, b, L, bs):
+    """[Hkv, L, d] of request b, gathered by numpy fancy indexing."""
+    j = np.arange(L)
+    return cache[table[b, j // bs], :, j % bs].transpose(1, 0, 2)
+
+
+def check_paged(orc, rng):
+    """Paged attention equals contiguous attention over the gathered cache."""
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    for (B, H, Hkv, Sq, d, bs, lens) in ((3, 4, 2, 1, 8, 4, (9, 1, 16)),
+                                         (2, 2, 2, 3, 5, 8, (3, 30)),
+                                         (2, 6, 1, 2, 4, 16, (17, 40))):
+        q, kc, vc, table, sl = _paged_case(rng, B, H, Hkv, Sq, d, bs, lens, 40)
+        for mask in ("none", "causal"):
+            o, lse = orc.attention_paged(q, kc, vc, table, sl, 0.4, mask)
+            for b, L in enumerate(lens):
+                K, V = _gather(kc, table, b, L, bs), _gather(vc, table, b, L, bs)
+                if mask == "none":
+                    o_ref, l_ref = orc.attention(q[b:b + 1], K[None], V[None], 0.4, "none")
+                    np.testing.assert_allclose(o[b], o_ref[0], rtol=1e-12, atol=1e-13)
+                    np.testing.assert_allclose(lse[b], l_ref[0], rtol=1e-12, atol=1e-13)
+                # query row i sits at position L - Sq + i: an explicit band for torch
+                band = np.arange(L)[None, :] <= (L - Sq + np.arange(Sq))[:, None]
+                am = torch.from_numpy(band) if mask == "causal" else None
+                rep = H // Hkv
+                ref = F.scaled_dot_product_attention(
+                    torch.from_numpy(q[b:b + 1]),
+                    torch.from_numpy(K[None]).repeat_interleave(rep, dim=1),
+                    torch.from_numpy(V[None]).repeat_interleave(rep, dim=1),
+                    attn_mask=am, scale=0.4).numpy()
+                np.testing.assert_allclose(o[b], ref[0], rtol=1e-11, atol=1e-12)
+
+
+def test_paged_matches_contiguous_attention():
+    check_paged(oracle.default(), np.random.default_rng(24))
+
+
+def test_paged_ignores_block_placement_and_unused_memory():
+    rng = np.random.default_rng(25)
+    q, kc, vc, table, sl = _paged_case(rng, 2, 2, 2, 2, 6, 4, (11, 7), 12)
+    o, lse = oracle.attention_paged(q, kc, vc, table, sl, 0.5, "causal")
+    # move every block elsewhere and rewrite the table
+    perm = rng.permutation(12)
+    kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+    kc2[perm], vc2[perm] = kc, vc
+    table2 = np.where(table >= 0, perm[np.clip(table, 0, None)], table).astype(np.int32)
+    # blocks nobody references hold NaN
+    used = set(int(x) for x in table2.ravel() if x >= 0)
+    for blk in range(12):
+        if blk not in used:
+            kc2[blk] = np.nan
+            vc2[blk] = np.nan
+    o2, lse2 = oracle.attention_paged(q, kc2, vc2, table2, sl, 0.5, "causal")
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+    with pytest.raises(ValueError):  # a length past the table's blocks
+        oracle.attention_paged(q, kc, vc, table, np.array([11, 99], np.int32), 0.5)
+
+
 def test_row_subset_matches_full():
     rng = np.random.default_rng(7)
     q, k, v = _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4), _rand(rng, 2, 3, 10, 4)
@@ -510,6 +588,10 @@ MUTATIONS = [
     ("bwd: P without the row sum (dK/dV pass)", "- rm[r]) / rl[r];", "- rm[r]);"),
     ("bwd: dP against k", "dP[j] = orc_dot(doi, vh + j * (int64_t)d, d);",
      "dP[j] = orc_dot(doi, kh + j * (int64_t)d, d);"),
+    ("paged: token offset in block", "+ j % block_size) * (int64_t)d;\n                double dot",
+     "+ j / block_size) * (int64_t)d;\n                double dot"),
+    ("paged: causal row position off by one", "? L - Sq + i : L - 1;", "? L - Sq + i - 1 : L - 1;"),
+    ("paged: wrong K/V head", "const int64_t kvh = h / group;", "const int64_t kvh = h % Hkv;"),
     ("bwd: key pass skips the causal mask", "if (rl[r] == 0.0 || !orc_visible(mask_kind, window, i, j))",
      "if (rl[r] == 0.0)"),
 ]
@@ -526,7 +608,7 @@ def test_planted_mistake_is_caught(tmp_path, name, old, new):
     checks = [check_worked_example, check_online_softmax_1d, check_library_reduction,
               check_torch_sdpa, check_closed_forms, check_invariants,
               check_blocked_equals_naive, check_brute_force, check_gqa,
-              check_bwd_finite_differences, check_bwd_torch, check_bwd_closed_forms]
+              check_bwd_finite_differences, check_bwd_torch, check_bwd_closed_forms, check_paged]
     caught = 0
     for chk in checks:
         try:
