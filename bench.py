@@ -500,6 +500,150 @@ def run_ours_bwd(args, w):
     return result
 
 
+def paged_kv_bytes(w, lens) -> int:
+    """K and V bytes a decoding step must read: every cached token once per K/V head."""
+    return int(np.sum(lens.astype(np.int64))) * w.Hkv * w.d * 2 * 2
+
+
+def paged_flops(w, lens) -> float:
+    """4*d per visible (row, token) pair, summed over heads and requests."""
+    tot = 0
+    for L in lens.astype(np.int64):
+        if w.mask == "causal":
+            tot += sum(int(L) - w.Sq + i + 1 for i in range(w.Sq))
+        else:
+            tot += int(L) * w.Sq
+    return 4.0 * w.d * w.H * tot
+
+
+def run_ours_decode(args, w):
+    """One step = one fa_decode_paged call (key-range kernel + combine) over a
+    resident paged cache; the metric is the K/V bytes the step must read per
+    second."""
+    import torch
+    from exact_io_aware_30_gb300 import build, fa
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    build.build()
+    fa.load()
+    inp = inputs.generate_paged(w)
+    tdt = torch.bfloat16 if w.dtype == inputs.BF16 else torch.float16
+    q_h = torch.from_numpy(inp.q_bits.view(np.int16)).view(tdt).pin_memory()
+    kc = torch.from_numpy(inp.k_bits.view(np.int16)).view(tdt).to(dev)
+    vc = torch.from_numpy(inp.v_bits.view(np.int16)).view(tdt).to(dev)
+    table_h = torch.from_numpy(inp.block_table).pin_memory()
+    lens_h = torch.from_numpy(inp.seq_lens).pin_memory()
+    q, table, lens = q_h.to(dev), table_h.to(dev), lens_h.to(dev)
+    stream = torch.cuda.current_stream(dev)
+    dtc = fa.DTYPE_FP16 if w.dtype == inputs.FP16 else fa.DTYPE_BF16
+    st, ws_bytes = fa.decode_workspace_query(w.B, w.H, w.Hkv, w.Sq, w.d, w.block_size,
+                                             inp.block_table.shape[1], kc.shape[0], w.max_seq_len,
+                                             w.mask, dtc)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.Sq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    kv_bytes = paged_kv_bytes(w, inp.seq_lens)
+    alg_bytes = kv_bytes + 2 * 2 * q.numel() + 4 * lse.numel()
+    flops = paged_flops(w, inp.seq_lens)
+
+    def step(qq=q, tt=table, ll=lens):
+        fa.decode_paged(qq, kc, vc, tt, ll, w.max_seq_len, scale=w.scale, mask=w.mask, out=o,
+                        lse=lse, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1.0)
+        step()
+    torch.cuda.synchronize()
+    if fa.device_error() != fa.FA_OK:
+        raise RuntimeError("device pipeline timeout during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(physical_gpu_index(0))
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(1.0)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    call_ms = [a_.elapsed_time(b_) for a_, b_ in zip(starts, ends)]
+    ms = float(np.mean(call_ms))
+    # end to end: the step's new rows, block table and lengths from pinned host
+    # memory in, O and lse out; the cache stays resident, as in serving
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(3, min(args.steps, 20))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        flush.fill_(1.0)
+        step(q_h.to(dev, non_blocking=True), table_h.to(dev, non_blocking=True),
+             lens_h.to(dev, non_blocking=True))
+        o_h.copy_(o, non_blocking=True)
+        l_h.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if fa.device_error() != fa.FA_OK:
+        raise RuntimeError("device pipeline timeout during the timed region")
+    _, hbm_peak, peak_src = load_peaks()
+    gbs = kv_bytes / (ms * 1e-3) / 1e9
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        qf, kf, vf = inp.f64()
+        nb = max(1, w.B // 8)
+        t0 = time.perf_counter()
+        oracle.attention_paged(qf[:nb], kf, vf, inp.block_table[:nb], inp.seq_lens[:nb], w.scale,
+                               w.mask)
+        dt = time.perf_counter() - t0
+        sub = paged_kv_bytes(w, inp.seq_lens[:nb])
+        cpu = {"value": sub / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+               "kind": "oracle",
+               "sample": f"{nb} of {w.B} requests, {sub / 1e6:.0f} MB of K/V, {dt:.1f} s, fp64 oracle"}
+    h2d = q_h.numel() * 2 + table_h.numel() * 4 + lens_h.numel() * 4
+    d2h = o_h.numel() * 2 + l_h.numel() * 4
+    result = {
+        "metric": "paged decode K/V read bandwidth (GB/s of cached K and V the step must read)",
+        "value": gbs,
+        "unit": "GB/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16" if w.dtype == inputs.FP16 else "bf16",
+        "data": "synthetic (seeded N(0,1) rounded to 16 bits; lengths uniform, blocks permuted)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.Hkv, "Sq": w.Sq,
+                   "head_dim": w.d, "block_size": w.block_size, "max_seq_len": w.max_seq_len,
+                   "mean_seq_len": float(np.mean(inp.seq_lens)), "mask": w.mask,
+                   "kv_bytes_per_step": kv_bytes, "tflops": flops / (ms * 1e-3) / 1e12,
+                   "l2": "flushed (256 MiB write) before every step", "parallelism": "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": f"{peak_src} HBM copy bandwidth",
+                     "traffic": None, "algorithmic_bytes": alg_bytes,
+                     "kernel": "fa_decode_paged call (key-range kernel + combine)",
+                     "kernel_ms_median": float(np.median(call_ms)),
+                     "kernel_ms_min": float(np.min(call_ms))},
+        "cpu_baseline": cpu,
+        "e2e": {"value": kv_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+    print(json.dumps(result), flush=True)
+    return result
+
+
 def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -554,13 +698,17 @@ def main(argv=None):
                     help="override the head count (smaller profiling case of the same kernel)")
     ap.add_argument("--seq", type=int, default=0,
                     help="override Sq = Sk (sequence-length sweeps of the same kernel)")
-    ap.add_argument("--direction", choices=["fwd", "bwd"], default="fwd",
-                    help="bwd: time the backward (fa_bwd) on the same workload")
+    ap.add_argument("--direction", choices=["fwd", "bwd", "decode"], default="fwd",
+                    help="bwd: time the backward (fa_bwd) on the same workload; decode: time "
+                         "fa_decode_paged on a paged-cache workload (--workload indexes those)")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="K/V heads shared by the query heads (grouped-query attention)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
+    if args.direction == "decode":
+        wd = args.workload if args.workload != str(DEFAULT_WORKLOAD) else "0"
+        return run_ours_decode(args, inputs.PAGED_WORKLOADS[int(wd)])
     wl = int(args.workload) if args.workload.isdigit() else args.workload
     w = inputs.workload(wl)
     if args.heads or args.seq or args.kv_heads:

@@ -142,6 +142,18 @@ __device__ __forceinline__ void store_zero_row(void *dst, int bytes) {
     for (int c = 0; c < bytes; c += 16) ptx::st_global_v4(d8 + c, 0u, 0u, 0u, 0u);
 }
 
+// Warp-uniform bounded waits: every lane gets the answer of the whole warp,
+// so a timeout seen by one lane never splits the warp in front of a
+// warp-collective tcgen05 load or store, or of a __syncwarp.  (Callers keep
+// their `ok` flags warp-uniform too.)
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, Ctl *ctl, int site) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, ctl, site));
+}
+
+__device__ __forceinline__ bool wait_warp_backoff(uint32_t bar, uint32_t parity, Ctl *ctl, int site) {
+    return __all_sync(0xffffffffu, wait_bar_backoff(bar, parity, ctl, site));
+}
+
 // 16-column steps of a 128-byte-swizzled K-major operand made of 64-column
 // boxes `box` bytes apart: 32 bytes inside a box, then the next box.
 __device__ __forceinline__ uint32_t kmajor_step(int kk, int box) {
@@ -252,7 +264,7 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     bool ok = true;
     for (int s = 0; s < un.steps; ++s) {
         const int slot = s % C::ST;
-        if (!wait_bar_backoff(bar_addr(bars, C::B_QEMPTY + slot), ((s / C::ST) & 1) ^ 1, ctl, 21)) {
+        if (!wait_warp_backoff(bar_addr(bars, C::B_QEMPTY + slot), ((s / C::ST) & 1) ^ 1, ctl, 21)) {
             ok = false;
             break;
         }
@@ -293,16 +305,16 @@ __device__ void bwd_kv_mma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     const bool leader = ptx::lane_id() == 0;
     const uint64_t dk_desc = smem_desc(ptx::smem_addr(sK), 16);
     const uint64_t dv_desc = smem_desc(ptx::smem_addr(sV), 16);
-    bool ok = un.steps == 0 || wait_bar(bar_addr(bars, C::B_KVFULL), 0, ctl, 22);
+    bool ok = un.steps == 0 || wait_warp(bar_addr(bars, C::B_KVFULL), 0, ctl, 22);
     for (int t = 0; ok && t <= un.steps; ++t) {
         if (t < un.steps) {
             const int slot = t % C::ST;
-            if (!wait_bar(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 23)) {
+            if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 23)) {
                 ok = false;
                 break;
             }
             // the compute warps have read S^T and dP^T of step t-1
-            if (t >= 1 && !wait_bar(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 24)) {
+            if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 24)) {
                 ok = false;
                 break;
             }
@@ -324,7 +336,7 @@ __device__ void bwd_kv_mma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
         }
         if (t >= 1) {
             const int tp = t - 1, slot = tp % C::ST;
-            if (!wait_bar(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 25)) {
+            if (!wait_warp(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 25)) {
                 ok = false;
                 break;
             }
@@ -371,8 +383,8 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
         const int slot = t % C::ST;
         const int i0 = (un.it_lo + t % un.n_i) * C::BM + h * NC;  // first query row of the columns
         // The statistics arrived with the step's Q tile; S^T and dP^T are ready.
-        ok = ok && wait_bar(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
-        ok = ok && wait_bar(bar_addr(bars, C::B_SFULL), t & 1, ctl, 27);
+        ok = ok && wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
+        ok = ok && wait_warp(bar_addr(bars, C::B_SFULL), t & 1, ctl, 27);
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t s[NC], dp[NC];
@@ -417,7 +429,7 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
             dsw[2 * q + 1] = pack2b<kFP16>(dsv[2], dsv[3]);
         }
         // dV / dK of step t-1 have read the P and dS areas
-        if (t >= 1 && !wait_bar(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 28)) {
+        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 28)) {
             ok = false;
             break;
         }
@@ -436,7 +448,7 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
 
     // Epilogue: dV and scale * dK of this thread's key row, columns h*D/WG ..
     if (un.steps > 0) {
-        if (!ok || !wait_bar(bar_addr(bars, C::B_DONE), 0, ctl, 29)) return;
+        if (!ok || !wait_warp(bar_addr(bars, C::B_DONE), 0, ctl, 29)) return;
         ptx::tc_fence_after();
     }
     constexpr int HALF = D / C::WG;
@@ -632,7 +644,7 @@ __device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
     for (int t = 0; t < un.n && ok; ++t) {
         const int k0 = (un.lo + t) * C::BN;
         const int ks = t % C::KST, vs = t % C::VST;
-        if (!wait_bar_backoff(bar_addr(bars, C::B_KEMPTY + ks), ((t / C::KST) & 1) ^ 1, ctl, 31)) {
+        if (!wait_warp_backoff(bar_addr(bars, C::B_KEMPTY + ks), ((t / C::KST) & 1) ^ 1, ctl, 31)) {
             ok = false;
             break;
         }
@@ -646,7 +658,7 @@ __device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
         }
         __syncwarp();
         ++k_issued;
-        if (!wait_bar_backoff(bar_addr(bars, C::B_VEMPTY + vs), ((t / C::VST) & 1) ^ 1, ctl, 39)) {
+        if (!wait_warp_backoff(bar_addr(bars, C::B_VEMPTY + vs), ((t / C::VST) & 1) ^ 1, ctl, 39)) {
             ok = false;
             break;
         }
@@ -679,16 +691,16 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
     const bool leader = ptx::lane_id() == 0;
     const uint64_t qd = smem_desc(ptx::smem_addr(sQ), 16);
     const uint64_t od = smem_desc(ptx::smem_addr(sDO), 16);
-    bool ok = un.n == 0 || wait_bar(bar_addr(bars, C::B_QFULL), 0, ctl, 32);
+    bool ok = un.n == 0 || wait_warp(bar_addr(bars, C::B_QFULL), 0, ctl, 32);
     for (int t = 0; ok && t <= un.n; ++t) {
         if (t < un.n) {
             const int ks = t % C::KST, vs = t % C::VST;
-            if (!wait_bar(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 33) ||
-                !wait_bar(bar_addr(bars, C::B_VFULL + vs), (t / C::VST) & 1, ctl, 40)) {
+            if (!wait_warp(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 33) ||
+                !wait_warp(bar_addr(bars, C::B_VFULL + vs), (t / C::VST) & 1, ctl, 40)) {
                 ok = false;
                 break;
             }
-            if (t >= 1 && !wait_bar(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 34)) {
+            if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 34)) {
                 ok = false;
                 break;
             }
@@ -711,7 +723,7 @@ __device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
         }
         if (t >= 1) {
             const int tp = t - 1, slot = tp % C::KST;
-            if (!wait_bar(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 35)) {
+            if (!wait_warp(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 35)) {
                 ok = false;
                 break;
             }
@@ -758,7 +770,7 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
         if (p.mask_kind != kMaskNone) hi = min(hi, i - k0 + 1);
         if (p.mask_kind == kMaskWindow) lo = max(0, i - p.window + 1 - k0);
         const bool masked = lo > 0 || hi < NC;
-        if (!wait_bar(bar_addr(bars, C::B_SFULL), t & 1, ctl, 36)) {
+        if (!wait_warp(bar_addr(bars, C::B_SFULL), t & 1, ctl, 36)) {
             ok = false;
             break;
         }
@@ -785,7 +797,7 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
                                      p1 * (__uint_as_float(dp[e + 1]) - Dl));
         }
         // dQ of step t-1 has read the dS area
-        if (t >= 1 && !wait_bar(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
+        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
             ok = false;
             break;
         }
@@ -803,7 +815,7 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
         if (row_ok) store_zero_row(dq_row, HALF * 2);
         return;
     }
-    if (!ok || !wait_bar(bar_addr(bars, C::B_DONE), 0, ctl, 38)) return;
+    if (!ok || !wait_warp(bar_addr(bars, C::B_DONE), 0, ctl, 38)) return;
     ptx::tc_fence_after();
 #pragma unroll
     for (int cc = 0; cc < HALF / 32; ++cc) {

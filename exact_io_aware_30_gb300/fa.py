@@ -32,8 +32,8 @@ DTYPE_FP16 = 1
 
 # Every entry point declared in include/fa.h.
 EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_bwd", "fa_bwd_noalloc",
-           "fa_bwd_workspace_query", "fa_workspace_query", "fa_status_string", "fa_describe",
-           "fa_get_device_error")
+           "fa_bwd_workspace_query", "fa_decode_paged", "fa_decode_workspace_query",
+           "fa_workspace_query", "fa_status_string", "fa_describe", "fa_get_device_error")
 
 
 class FAError(RuntimeError):
@@ -77,6 +77,13 @@ def load(path: str | None = None):
         lib.fa_bwd_noalloc.restype = _i
         lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i, _vp]
+        lib.fa_decode_paged.restype = _i
+        lib.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                                        _i, _i, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i,
+                                        _i, _vp]
+        lib.fa_decode_workspace_query.restype = _i
+        lib.fa_decode_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                                  ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_bwd_workspace_query.restype = _i
         lib.fa_bwd_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                                ctypes.POINTER(ctypes.c_size_t)]
@@ -150,6 +157,75 @@ def bwd_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int
                                  int(H), int(H_kv), int(Sq), int(Sk), int(d),
                                  ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
                                  _vp(stream))
+
+
+def decode_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, o_ptr, lse_ptr, ws_ptr, ws_bytes, B, H,
+               H_kv, Sq, d, block_size, max_blocks, num_blocks, max_seq_len, scale, mask_kind,
+               dtype, stream) -> int:
+    """Call fa_decode_paged with raw device pointers; returns the status."""
+    return load().fa_decode_paged(_vp(q_ptr), _vp(k_ptr), _vp(v_ptr), _vp(table_ptr),
+                                  _vp(lens_ptr), _vp(o_ptr), _vp(lse_ptr), _vp(ws_ptr),
+                                  ctypes.c_size_t(ws_bytes), int(B), int(H), int(H_kv), int(Sq),
+                                  int(d), int(block_size), int(max_blocks), int(num_blocks),
+                                  int(max_seq_len), ctypes.c_float(scale), int(mask_kind),
+                                  int(dtype), _vp(stream))
+
+
+def decode_workspace_query(B, H, H_kv, Sq, d, block_size, max_blocks, num_blocks, max_seq_len,
+                           mask="none", dtype=DTYPE_BF16):
+    """(status, bytes) of fa_decode_workspace_query."""
+    n = ctypes.c_size_t(12345)
+    st = load().fa_decode_workspace_query(int(B), int(H), int(H_kv), int(Sq), int(d),
+                                          int(block_size), int(max_blocks), int(num_blocks),
+                                          int(max_seq_len), mask_code(mask), int(dtype),
+                                          ctypes.byref(n))
+    return st, n.value
+
+
+def decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
+                 scale: float | None = None, mask="none", out=None, lse=None, workspace=None,
+                 stream=None):
+    """Attention of q's new rows over a paged K/V cache (fa_decode_paged).
+
+    q [B, H, Sq, d]; k_cache, v_cache [num_blocks, H_kv, block_size, d] (one
+    16-bit dtype); block_table int32 [B, max_blocks] and seq_lens int32 [B] on
+    the same CUDA device.  Returns (o, lse).
+    """
+    import torch
+    for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("block_table", block_table), ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous CUDA tensor")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype):
+        raise FAError(FA_ERR_INVALID_ARG, "q and the caches must share one dtype")
+    if block_table.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise FAError(FA_ERR_INVALID_ARG, "block_table and seq_lens must be int32")
+    dt = _dtype_code(q)
+    B, H, Sq, d = q.shape
+    nb, H_kv, bs, d2 = k_cache.shape
+    if (tuple(v_cache.shape) != tuple(k_cache.shape) or d2 != d or block_table.dim() != 2
+            or block_table.shape[0] != B or tuple(seq_lens.shape) != (B,)):
+        raise FAError(FA_ERR_INVALID_ARG, "shapes: q [B,H,Sq,d]; caches [blocks,H_kv,bs,d]; "
+                      "block_table [B,n]; seq_lens [B]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    mb = block_table.shape[1]
+    st, ws_bytes = decode_workspace_query(B, H, H_kv, Sq, d, bs, mb, nb, max_seq_len, mask, dt)
+    _check(st, "fa_decode_workspace_query")
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    out = torch.empty_like(q) if out is None else out
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = decode_raw(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
+                    seq_lens.data_ptr(), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
+                    workspace.numel(), B, H, H_kv, Sq, d, bs, mb, nb, max_seq_len, float(scale),
+                    mask_code(mask), dt, sp)
+    _check(st, "fa_decode_paged")
+    return out, lse
 
 
 def bwd_workspace_query(B, H, H_kv, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):

@@ -174,3 +174,90 @@ def custom(B, H, Sq, Sk, d, dtype=BF16, mask="none", window=0, seed=0, spiky_key
     """An ad-hoc shape drawn by the same recipe (Hkv > 0: K/V with Hkv heads)."""
     w = Workload(name, B, H, Sq, Sk, d, dtype, mask, window, spiky_keys, seed, Hkv)
     return generate(w)
+
+
+# ----------------------------------------------------------------------------
+# Paged K/V cache (decoding)
+# ----------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class PagedWorkload:
+    """Decoding over a paged cache: B requests, each with seq_len cached tokens
+    in blocks of block_size tokens (the last Sq of them the new rows')."""
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    Sq: int
+    d: int
+    block_size: int
+    max_seq_len: int
+    dtype: str
+    mask: str = "causal"
+    min_seq_len: int = 1
+    seed: int = 0
+    spare_blocks: int = 8   # blocks in the pool that no request uses
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0) / np.sqrt(np.float32(self.d)))
+
+
+# Decoding for a 13B model shaped like OPT-13B (40 heads x 128 = hidden 5120,
+# fp16), cache blocks of 16 tokens and a 2,048-token context window, as the
+# paged-cache section of "Flash attention and memory-efficient attention
+# variants" describes it; 128 concurrent requests with lengths spread
+# uniformly over the window.
+PAGED_WORKLOADS = [
+    PagedWorkload("decode_b128_h40_d128_bs16_ctx2048_fp16", 128, 40, 40, 1, 128, 16, 2048, FP16,
+                  seed=2001),
+    PagedWorkload("decode_b64_h32kv8_d128_bs64_ctx8192_bf16", 64, 32, 8, 1, 128, 64, 8192, BF16,
+                  seed=2002),
+]
+
+
+@dataclass
+class PagedInputs:
+    workload: PagedWorkload
+    q_bits: np.ndarray        # uint16 [B, H, Sq, d]
+    k_bits: np.ndarray        # uint16 [num_blocks, Hkv, block_size, d]
+    v_bits: np.ndarray        # uint16 [num_blocks, Hkv, block_size, d]
+    block_table: np.ndarray   # int32 [B, max_blocks]
+    seq_lens: np.ndarray      # int32 [B]
+
+    def f64(self):
+        dt = self.workload.dtype
+        return (bits_to_f64(self.q_bits, dt), bits_to_f64(self.k_bits, dt),
+                bits_to_f64(self.v_bits, dt))
+
+
+def generate_paged(w: PagedWorkload) -> PagedInputs:
+    """Seeded paged-cache inputs: lengths uniform in [max(Sq, min_seq_len),
+    max_seq_len] (the first request gets max_seq_len), each request's blocks
+    a random set of physical blocks (a permutation of the pool), table
+    entries past a request's blocks set to -1; then Q, K cache, V cache drawn
+    N(0, 1) float32 and rounded to the 16-bit type."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    lo = max(w.Sq, w.min_seq_len)
+    lens = rng.integers(lo, w.max_seq_len + 1, size=w.B).astype(np.int32)
+    lens[0] = w.max_seq_len
+    max_blocks = -(-w.max_seq_len // w.block_size)
+    need = [-(-int(L) // w.block_size) for L in lens]
+    num_blocks = sum(need) + w.spare_blocks
+    perm = rng.permutation(num_blocks).astype(np.int32)
+    table = np.full((w.B, max_blocks), -1, np.int32)
+    used = 0
+    for b, n in enumerate(need):
+        table[b, :n] = perm[used:used + n]
+        used += n
+    q = to_bits(rng.standard_normal((w.B, w.H, w.Sq, w.d), dtype=np.float32), w.dtype)
+    shape = (num_blocks, w.Hkv, w.block_size, w.d)
+    k = to_bits(rng.standard_normal(shape, dtype=np.float32), w.dtype)
+    v = to_bits(rng.standard_normal(shape, dtype=np.float32), w.dtype)
+    return PagedInputs(w, q, k, v, table, lens)
+
+
+def custom_paged(B, H, Hkv, Sq, d, block_size, max_seq_len, dtype=BF16, mask="causal",
+                 min_seq_len=1, seed=0) -> PagedInputs:
+    return generate_paged(PagedWorkload("custom_paged", B, H, Hkv, Sq, d, block_size,
+                                        max_seq_len, dtype, mask, min_seq_len, seed))

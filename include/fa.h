@@ -176,6 +176,56 @@ fa_status fa_bwd_workspace_query(int B, int H, int H_kv, int Sq, int Sk, int d, 
                                  int window, int dtype, size_t *bytes);
 
 /*
+ * fa_decode_paged -- attention of the newest Sq rows of each request over its
+ * paged K/V cache, as in decoding ("Flash attention and memory-efficient
+ * attention variants", sections "A different bottleneck: the KV cache during
+ * inference" and "PagedAttention: memory management borrowed from an
+ * operating system").  The cache is a pool of physical blocks of block_size
+ * tokens; request b's block table maps its logical block n (tokens
+ * n*block_size .. (n+1)*block_size - 1) to a physical block.  Exact softmax
+ * attention over the gathered tokens; each request's keys are cut into ranges
+ * that run in parallel, and the partial results are merged by their lse.
+ *
+ *   q            [B, H, Sq, d] 16-bit: the new rows (Sq = 1 for one step)
+ *   k_cache      [num_blocks, H_kv, block_size, d] 16-bit
+ *   v_cache      same layout
+ *   block_table  device int32 [B, max_blocks]; entries past a request's last
+ *                block are not read; an entry outside [0, num_blocks) reads
+ *                zeros
+ *   seq_lens     device int32 [B]: cached tokens of each request, the last Sq
+ *                of which are the new rows' own; must lie in
+ *                [Sq, max_seq_len] (values outside are clamped into it)
+ *   o, lse       [B, H, Sq, d] 16-bit and [B, H, Sq] fp32 outputs
+ *   workspace    at least fa_decode_workspace_query() bytes, 256-byte aligned
+ *   H_kv         K/V heads, dividing H; (H / H_kv) * Sq <= 128
+ *   d            64 or 128; block_size 16, 32, 64 or 128
+ *   max_seq_len  host bound on seq_lens (it sizes the key ranges)
+ *   mask_kind    FA_MASK_NONE (every cached token) or FA_MASK_CAUSAL: row i
+ *                sits at position seq_lens[b] - Sq + i and sees tokens up to
+ *                it (the reading for decoding: the new rows are the last)
+ *   dtype        FA_DTYPE_BF16 or FA_DTYPE_FP16
+ * Cache slots past a request's length may hold any values, inf and NaN
+ * included: they are hidden and never reach O.  Errors and the device flag
+ * are as for fa_fwd; the library allocates nothing.  Two launches.
+ */
+fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                          const int *block_table, const int *seq_lens, void *o, float *lse,
+                          void *workspace, size_t workspace_bytes, int B, int H, int H_kv,
+                          int Sq, int d, int block_size, int max_blocks, int num_blocks,
+                          int max_seq_len, float scale, int mask_kind, int dtype,
+                          fa_stream_t stream);
+
+/*
+ * fa_decode_workspace_query -- workspace bytes fa_decode_paged needs on the
+ * current device (partial rows of every key range: (d + 1) x 4 bytes per row
+ * and range) and the status it would return for these sizes.  bytes must be
+ * non-NULL; it is 0 whenever the status is not FA_OK.
+ */
+fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int block_size,
+                                    int max_blocks, int num_blocks, int max_seq_len,
+                                    int mask_kind, int dtype, size_t *bytes);
+
+/*
  * fa_workspace_query -- device scratch bytes fa_fwd needs for this problem
  * (always 0: the forward keeps every intermediate on chip, so its memory is
  * linear in the sequence length -- "FlashAttention: Why Tiling...", section
