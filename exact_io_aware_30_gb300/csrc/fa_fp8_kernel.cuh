@@ -1,0 +1,390 @@
+// fa_fp8_kernel.cuh -- the fused attention forward with 8-bit (e4m3) inputs,
+// for sm_103a (GB300): the low-precision path that "FlashAttention: IO-aware
+// attention kernels" (section "Concept") names as a later variant.  The
+// arithmetic is that of the tiled forward pass ("FlashAttention: Why Tiling
+// Attention Makes Transformers Fast Without Changing the Result", sections
+// "Online softmax: correct as you go" and "The tiled forward pass").
+//
+// Inputs are e4m3 codes with one dequantisation factor per tensor: the value
+// of a stored code x is x * q_descale (k_descale, v_descale).  The kernel
+// computes S = Q K^T on the 8-bit tensor path (kind::f8f6f4, fp32
+// accumulation) with the factors and 1/sqrt(d)-type scale folded into the
+// exponent's multiplier, keeps a running max, sum and unnormalised O per row,
+// and stores P as e4m3 (times 256, so that weights in [2^-17, 1] keep normal
+// or subnormal codes) for O += P V on the same 8-bit path.  O is written as
+// bf16, lse in fp32.
+//
+// V is taken transposed, [B, H_kv, d, Sk]: both tile products then read
+// K-major operands (keys contiguous for V^T), the operand layout every 8-bit
+// tcgen05 form accepts.
+//
+// One CTA per 128-row query tile (longest first); warps 0-3 softmax and
+// epilogue (one row per thread), warp 4 issues the MMAs, warp 5 the TMA copies
+// (Q once, K and V^T tiles through rings of four slots each).
+#pragma once
+
+#include <math.h>
+#include <stdint.h>
+
+#include "fa_bwd_kernel.cuh"
+
+namespace fa {
+
+struct Fp8Params {
+    CUtensorMap tm_q;   // e4m3 [B, H, Sq, d], box {d, 128 rows}
+    CUtensorMap tm_k;   // e4m3 [B, Hkv, Sk, d], box {d, 128 keys}
+    CUtensorMap tm_vt;  // e4m3 [B, Hkv, d, Sk], box {128 keys, d rows}
+    void *o;            // bf16 [B, H, Sq, d]
+    float *lse;         // fp32 [B, H, Sq]
+    int B, H, Hkv, kv_group, Sq, Sk;
+    int mask_kind, window;
+    float c;            // scale * q_descale * k_descale * log2(e), kept positive
+    float o_mul;        // v_descale / 256 (P is stored times 256)
+    int n_qtiles;
+    uint64_t wait_limit_ns;
+};
+
+struct Fp8Cfg {
+    static constexpr int D = 128;
+    static constexpr int BN = 128;
+    static constexpr int KST = 4;
+    static constexpr int VST = 4;
+    static constexpr int Q_BYTES = 128 * D;   // one 128-byte-wide box
+    static constexpr int TILE_BYTES = BN * D;  // K tile, or V^T tile (d rows x 128 keys)
+    static constexpr int NUM_SOFTMAX = 128;
+    static constexpr int MMA_WARP = 4;
+    static constexpr int TMA_WARP = 5;
+    static constexpr int NUM_THREADS = 192;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0;     // two S buffers
+    static constexpr uint32_t O_COL = 256;
+    static constexpr uint32_t P_COL = 384;   // 128 keys of e4m3: 32 columns
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_KFULL = 1;
+    static constexpr int B_KEMPTY = B_KFULL + KST;
+    static constexpr int B_VFULL = B_KEMPTY + KST;
+    static constexpr int B_VEMPTY = B_VFULL + VST;
+    static constexpr int B_SFULL = B_VEMPTY + VST;  // [2]
+    static constexpr int B_SFREE = B_SFULL + 2;     // [2]
+    static constexpr int B_PFULL = B_SFREE + 2;
+    static constexpr int B_PFREE = B_PFULL + 1;
+    static constexpr int B_OFINAL = B_PFREE + 1;
+    static constexpr int B_DRAIN = B_OFINAL + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
+    static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
+    static constexpr float P_MUL = 256.f;
+    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+};
+
+struct Fp8Unit {
+    int b, h, kvh, i0, lo, n;  // key tiles lo .. lo + n
+};
+
+__device__ __forceinline__ Fp8Unit decode_fp8_unit(const Fp8Params &p) {
+    Fp8Unit u;
+    const int BH = p.B * p.H;
+    const int g = p.n_qtiles - 1 - (int)blockIdx.x / BH;  // longest query tiles first
+    const int bh = (int)blockIdx.x % BH;
+    u.b = bh / p.H;
+    u.h = bh - u.b * p.H;
+    u.kvh = u.h / p.kv_group;
+    u.i0 = g * 128;
+    const int row_end = min(u.i0 + 128, p.Sq);
+    int key_end = p.Sk;
+    if (p.mask_kind != kMaskNone) key_end = min(p.Sk, row_end);
+    int key_beg = 0;
+    if (p.mask_kind == kMaskWindow) key_beg = max(0, u.i0 - p.window + 1);
+    if (key_beg < key_end) {
+        u.lo = key_beg / 128;
+        u.n = (key_end + 127) / 128 - u.lo;
+    } else {
+        u.lo = 0;
+        u.n = 0;
+    }
+    return u;
+}
+
+__device__ void fp8_tma_role(const Fp8Params &p, const Fp8Unit &un, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
+                             uint32_t bars, Ctl *ctl) {
+    using C = Fp8Cfg;
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t pol_kv = ptx::policy_evict_last();
+    if (un.n == 0) return;
+    if (leader) {
+        const uint32_t fb = bar_addr(bars, C::B_QFULL);
+        ptx::mbar_arrive_expect_tx(fb, C::Q_BYTES);
+        ptx::tma_load_4d(ptx::smem_addr(sQ), &p.tm_q, fb, 0, un.i0, un.h, un.b, ptx::policy_evict_first());
+    }
+    int k_issued = 0, v_issued = 0;
+    bool ok = true;
+    for (int t = 0; t < un.n && ok; ++t) {
+        const int k0 = (un.lo + t) * C::BN;
+        const int ks = t % C::KST, vs = t % C::VST;
+        if (!wait_warp_backoff(bar_addr(bars, C::B_KEMPTY + ks), ((t / C::KST) & 1) ^ 1, ctl, 61)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            const uint32_t fb = bar_addr(bars, C::B_KFULL + ks);
+            ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+            ptx::tma_load_4d(ptx::smem_addr(sK + ks * C::TILE_BYTES), &p.tm_k, fb, 0, k0, un.kvh, un.b, pol_kv);
+        }
+        __syncwarp();
+        ++k_issued;
+        if (!wait_warp_backoff(bar_addr(bars, C::B_VEMPTY + vs), ((t / C::VST) & 1) ^ 1, ctl, 62)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            const uint32_t fb = bar_addr(bars, C::B_VFULL + vs);
+            ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
+            ptx::tma_load_4d(ptx::smem_addr(sV + vs * C::TILE_BYTES), &p.tm_vt, fb, k0, 0, un.kvh, un.b, pol_kv);
+        }
+        __syncwarp();
+        ++v_issued;
+    }
+    wait_bar_drain(bar_addr(bars, C::B_QFULL), 0);
+    if (!ok) {
+        for (int t = k_issued - C::KST > 0 ? k_issued - C::KST : 0; t < k_issued; ++t)
+            wait_bar_drain(bar_addr(bars, C::B_KFULL + t % C::KST), (t / C::KST) & 1);
+        for (int t = v_issued - C::VST > 0 ? v_issued - C::VST : 0; t < v_issued; ++t)
+            wait_bar_drain(bar_addr(bars, C::B_VFULL + t % C::VST), (t / C::VST) & 1);
+    }
+}
+
+__device__ void fp8_mma_role(const Fp8Params &p, const Fp8Unit &un, uint8_t *sQ, uint8_t *sK, uint8_t *sV,
+                             uint32_t bars, uint32_t tmem, Ctl *ctl) {
+    using C = Fp8Cfg;
+    // e4m3 x e4m3 -> fp32 (type code 0 for both), both operands K-major
+    constexpr uint32_t kIdescS = make_idesc(128, C::BN, true, false);
+    constexpr uint32_t kIdescO = make_idesc(128, C::D, true, false);
+    const bool leader = ptx::lane_id() == 0;
+    const uint64_t qd = smem_desc(ptx::smem_addr(sQ), 16);
+    bool ok = un.n == 0 || wait_warp(bar_addr(bars, C::B_QFULL), 0, ctl, 63);
+    for (int t = 0; ok && t <= un.n; ++t) {
+        if (t < un.n) {
+            const int ks = t % C::KST;
+            const uint32_t b = (uint32_t)t & 1u;
+            if (!wait_warp(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 64)) {
+                ok = false;
+                break;
+            }
+            if (t >= 2 && !wait_warp(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1) & 1, ctl, 65)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+                const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::TILE_BYTES), 16);
+                // 32 elements (32 bytes) per instruction inside the 128-byte row
+#pragma unroll
+                for (int kk = 0; kk < C::D / 32; ++kk)
+                    ptx::mma_ss_f8(tmem + C::S_COL + b * C::BN, qd + (uint32_t)((kk * 32) >> 4),
+                                   kd + (uint32_t)((kk * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
+                ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + ks));
+            }
+            __syncwarp();
+        }
+        if (t >= 1) {
+            const int tp = t - 1, vs = tp % C::VST;
+            if (!wait_warp(bar_addr(bars, C::B_VFULL + vs), (tp / C::VST) & 1, ctl, 66) ||
+                !wait_warp(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 67)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+                // V^T tile: N = d rows of 128 keys (128 bytes), K-major
+                const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::TILE_BYTES), 16);
+#pragma unroll
+                for (int kk = 0; kk < C::BN / 32; ++kk)
+                    ptx::mma_ts_f8(tmem + C::O_COL, tmem + C::P_COL + kk * 8, vd + (uint32_t)((kk * 32) >> 4),
+                                   kIdescO, (tp > 0 || kk > 0) ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
+                if (tp + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
+            }
+            __syncwarp();
+        }
+    }
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
+    __syncwarp();
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+__device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t bars, uint32_t tmem,
+                                 Ctl *ctl) {
+    using C = Fp8Cfg;
+    const int r = (int)threadIdx.x;
+    const int warp = r >> 5;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const int i = un.i0 + r;  // query row
+    const float c = p.c;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < un.n; ++t) {
+        const uint32_t b = (uint32_t)t & 1u;
+        const int k0 = (un.lo + t) * C::BN;
+        if (!wait_warp(bar_addr(bars, C::B_SFULL + (int)b), (t >> 1) & 1, ctl, 68)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        uint32_t s[C::BN];
+        ptx::tmem_ld_x32<0>(lane_base + C::S_COL + b * C::BN, s);
+        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + b * C::BN + 32, s);
+        ptx::tmem_ld_x32<64>(lane_base + C::S_COL + b * C::BN + 64, s);
+        ptx::tmem_ld_x32<96>(lane_base + C::S_COL + b * C::BN + 96, s);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence<C::BN>(s);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_SFREE + (int)b));
+
+        // key k0 + e is visible to row i iff lo <= e < hi
+        int lo = 0, hi = min(C::BN, p.Sk - k0);
+        if (p.mask_kind != kMaskNone) hi = min(hi, i - k0 + 1);
+        if (p.mask_kind == kMaskWindow) lo = max(0, i - p.window + 1 - k0);
+        float mt = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < C::BN; ++e) {
+            const float x = __uint_as_float(s[e]) * c;
+            const float y = (e >= lo && e < hi) ? x : -INFINITY;
+            s[e] = __float_as_uint(y);
+            mt = fmaxf(mt, y);
+        }
+        const float m_new = fmaxf(m, mt);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = ptx::ex2_approx(m - m_use);
+        uint32_t pw[C::BN / 4];
+        float ps = 0.f;
+#pragma unroll
+        for (int e = 0; e < C::BN; e += 4) {
+            const float p0 = ptx::ex2_approx(__uint_as_float(s[e]) - m_use);
+            const float p1 = ptx::ex2_approx(__uint_as_float(s[e + 1]) - m_use);
+            const float p2 = ptx::ex2_approx(__uint_as_float(s[e + 2]) - m_use);
+            const float p3 = ptx::ex2_approx(__uint_as_float(s[e + 3]) - m_use);
+            ps += (p0 + p1) + (p2 + p3);
+            pw[e / 4] = ptx::pack_e4m3x4(p0 * C::P_MUL, p1 * C::P_MUL, p2 * C::P_MUL, p3 * C::P_MUL);
+        }
+        l = l * alpha + ps;
+        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 69)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        if (t >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int cc = 0; cc < C::D / 32; ++cc) {
+                uint32_t o[32];
+                ptx::tmem_ld_x32<0>(lane_base + C::O_COL + cc * 32, o);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<32>(o);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                ptx::tmem_st_x32<0>(lane_base + C::O_COL + cc * 32, o);
+            }
+        }
+        m = m_new;
+        ptx::tmem_st_x32<0>(lane_base + C::P_COL, pw);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
+    }
+
+    // Epilogue (whole warps): O / l as bf16 and the row's lse.
+    const bool row_ok = i < p.Sq;
+    const size_t row = ((size_t)un.b * p.H + un.h) * (size_t)p.Sq + (size_t)(row_ok ? i : 0);
+    uint8_t *orow = static_cast<uint8_t *>(p.o) + row * C::D * 2;
+    if (un.n > 0) {
+        if (!ok || !wait_warp(bar_addr(bars, C::B_OFINAL), 0, ctl, 70)) return;
+        ptx::tc_fence_after();
+    }
+    const bool seen = un.n > 0 && l > 0.f;
+    const float mul = seen ? p.o_mul / l : 0.f;
+#pragma unroll
+    for (int cc = 0; cc < C::D / 32; ++cc) {
+        uint32_t o[32];
+        if (un.n > 0) {
+            ptx::tmem_ld_x32<0>(lane_base + C::O_COL + cc * 32, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(o);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+        }
+        if (row_ok) store_row32<false>(orow + cc * 64, o, mul);
+    }
+    if (row_ok) p.lse[row] = seen ? (m + __log2f(l)) * kLn2 : -INFINITY;
+}
+
+__global__ void __launch_bounds__(Fp8Cfg::NUM_THREADS, 1) fa_fwd_fp8_kernel(const __grid_constant__ Fp8Params p) {
+    using C = Fp8Cfg;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem;
+    uint8_t *sK = sQ + C::Q_BYTES;
+    uint8_t *sV = sK + C::KST * C::TILE_BYTES;
+    uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
+    Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);
+    const uint32_t bars = ptx::smem_addr(bar_mem);
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(bar_addr(bars, C::B_QFULL), 1);
+        for (int s = 0; s < C::KST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_KFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_KEMPTY + s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
+            ptx::mbar_init(bar_addr(bars, C::B_VFULL + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_VEMPTY + s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_SFREE + b), C::NUM_SOFTMAX);
+        }
+        ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_SOFTMAX);
+        ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ctl->abort = 0;
+        ctl->limit_ns = p.wait_limit_ns;
+        ptx::fence_mbar_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == C::MMA_WARP) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_holder), C::TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    if (warp == C::TMA_WARP && ptx::lane_id() == 0) {
+        ptx::prefetch_tensormap(&p.tm_q);
+        ptx::prefetch_tensormap(&p.tm_k);
+        ptx::prefetch_tensormap(&p.tm_vt);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+    const Fp8Unit un = decode_fp8_unit(p);
+
+    if (warp < C::NUM_SOFTMAX / 32) {
+        fp8_softmax_role(p, un, bars, tmem, ctl);
+    } else if (warp == C::MMA_WARP) {
+        fp8_mma_role(p, un, sQ, sK, sV, bars, tmem, ctl);
+    } else {
+        fp8_tma_role(p, un, sQ, sK, sV, bars, ctl);
+    }
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == C::MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace fa

@@ -31,7 +31,7 @@ DTYPE_BF16 = 0
 DTYPE_FP16 = 1
 
 # Every entry point declared in include/fa.h.
-EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_bwd", "fa_bwd_noalloc",
+EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
            "fa_bwd_workspace_query", "fa_decode_paged", "fa_decode_workspace_query",
            "fa_workspace_query", "fa_status_string", "fa_describe", "fa_get_device_error")
 
@@ -77,6 +77,9 @@ def load(path: str | None = None):
         lib.fa_bwd_noalloc.restype = _i
         lib.fa_bwd_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                        _i, _i, _i, _i, _i, _i, ctypes.c_float, _i, _i, _i, _vp]
+        lib.fa_fwd_fp8.restype = _i
+        lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float,
+                                   ctypes.c_float, ctypes.c_float, ctypes.c_float, _i, _i, _vp]
         lib.fa_decode_paged.restype = _i
         lib.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                         _i, _i, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i,
@@ -157,6 +160,47 @@ def bwd_noalloc_raw(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, lse_ptr: int
                                  int(H), int(H_kv), int(Sq), int(Sk), int(d),
                                  ctypes.c_float(scale), int(mask_kind), int(window), int(dtype),
                                  _vp(stream))
+
+
+def fwd_fp8_raw(q_ptr, k_ptr, vt_ptr, o_ptr, lse_ptr, B, H, H_kv, Sq, Sk, d, scale, q_descale,
+                k_descale, v_descale, mask_kind, window, stream) -> int:
+    """Call fa_fwd_fp8 with raw device pointers; returns the status."""
+    return load().fa_fwd_fp8(_vp(q_ptr), _vp(k_ptr), _vp(vt_ptr), _vp(o_ptr), _vp(lse_ptr), int(B),
+                             int(H), int(H_kv), int(Sq), int(Sk), int(d), ctypes.c_float(scale),
+                             ctypes.c_float(q_descale), ctypes.c_float(k_descale),
+                             ctypes.c_float(v_descale), int(mask_kind), int(window), _vp(stream))
+
+
+def forward_fp8(q, k, vt, q_descale: float, k_descale: float, v_descale: float,
+                scale: float | None = None, mask="none", window: int = 0, out=None, lse=None,
+                stream=None):
+    """8-bit forward (fa_fwd_fp8) on CUDA uint8 tensors of e4m3 codes.
+
+    q [B, H, Sq, d]; k [B, H_kv, Sk, d]; vt = V transposed [B, H_kv, d, Sk].
+    Returns (o bf16 [B, H, Sq, d], lse fp32 [B, H, Sq]).
+    """
+    import torch
+    for name, t in (("q", q), ("k", k), ("vt", vt)):
+        if not t.is_cuda or not t.is_contiguous() or t.dim() != 4 or t.element_size() != 1:
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous 4-D CUDA tensor of bytes")
+    B, H, Sq, d = q.shape
+    H_kv, Sk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, H_kv, Sk, d) or tuple(vt.shape) != (B, H_kv, d, Sk):
+        raise FAError(FA_ERR_INVALID_ARG, "k must be [B,H_kv,Sk,d] and vt [B,H_kv,d,Sk]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, H, Sq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = fwd_fp8_raw(q.data_ptr(), k.data_ptr(), vt.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                     H_kv, Sq, Sk, d, float(scale), float(q_descale), float(k_descale),
+                     float(v_descale), mask_code(mask), int(window), sp)
+    _check(st, "fa_fwd_fp8")
+    return out, lse
 
 
 def decode_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, o_ptr, lse_ptr, ws_ptr, ws_bytes, B, H,

@@ -261,3 +261,97 @@ def custom_paged(B, H, Hkv, Sq, d, block_size, max_seq_len, dtype=BF16, mask="ca
                  min_seq_len=1, seed=0) -> PagedInputs:
     return generate_paged(PagedWorkload("custom_paged", B, H, Hkv, Sq, d, block_size,
                                         max_seq_len, dtype, mask, min_seq_len, seed))
+
+
+# ----------------------------------------------------------------------------
+# 8-bit (e4m3) inputs
+# ----------------------------------------------------------------------------
+
+def e4m3_table() -> np.ndarray:
+    """float64 value of every e4m3 code (1 sign, 4 exponent bits with bias 7,
+    3 mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448)."""
+    codes = np.arange(256)
+    sign = np.where(codes & 0x80, -1.0, 1.0)
+    e = (codes >> 3) & 0xF
+    m = codes & 0x7
+    val = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    val = sign * val
+    val[(e == 15) & (m == 7)] = np.nan
+    return val
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest e4m3 value (ties to the even code), saturating
+    at +-448; uint8 codes."""
+    tab = e4m3_table()
+    pos = tab[:0x7F]                  # codes 0x00 .. 0x7E: 0 .. 448, increasing
+    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), 448.0)
+    hi = np.clip(np.searchsorted(pos, a, side="left"), 1, len(pos) - 1)
+    lo = hi - 1
+    dlo, dhi = a - pos[lo], pos[hi] - a
+    pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))
+    pick = np.where(a == pos[hi], hi, pick)
+    code = pick.astype(np.uint8)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+
+
+def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    return e4m3_table()[np.asarray(bits, dtype=np.uint8)]
+
+
+@dataclass(frozen=True)
+class Fp8Workload:
+    name: str
+    B: int
+    H: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    d: int
+    mask: str
+    window: int = 0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0) / np.sqrt(np.float32(self.d)))
+
+
+@dataclass
+class Fp8Inputs:
+    workload: Fp8Workload
+    q_bits: np.ndarray    # uint8 e4m3 [B, H, Sq, d]
+    k_bits: np.ndarray    # uint8 e4m3 [B, Hkv, Sk, d]
+    vt_bits: np.ndarray   # uint8 e4m3 [B, Hkv, d, Sk] (V transposed)
+    q_descale: float
+    k_descale: float
+    v_descale: float
+
+    def f64(self):
+        """Dequantised q, k, v (v as [B, Hkv, Sk, d])."""
+        q = e4m3_bits_to_f64(self.q_bits) * self.q_descale
+        k = e4m3_bits_to_f64(self.k_bits) * self.k_descale
+        v = e4m3_bits_to_f64(self.vt_bits).transpose(0, 1, 3, 2) * self.v_descale
+        return q, k, np.ascontiguousarray(v)
+
+
+def generate_fp8(w: Fp8Workload) -> Fp8Inputs:
+    """Q, then K, then V drawn N(0, 1) float32 from PCG64(seed); each tensor
+    quantised to e4m3 with one factor, descale = max|x| / 448 (a power of two
+    above it, so that the factor is exact); V stored transposed."""
+    rng = np.random.Generator(np.random.PCG64(w.seed))
+    out = []
+    for shape in ((w.B, w.H, w.Sq, w.d), (w.B, w.Hkv, w.Sk, w.d), (w.B, w.Hkv, w.Sk, w.d)):
+        x = rng.standard_normal(shape, dtype=np.float32)
+        amax = float(np.abs(x).max()) if x.size else 1.0
+        descale = float(2.0 ** np.ceil(np.log2(max(amax, 1e-30) / 448.0)))
+        out.append((f32_to_e4m3_bits(x / descale), descale))
+    (qb, qs), (kb, ks), (vb, vs) = out
+    vt = np.ascontiguousarray(vb.transpose(0, 1, 3, 2))
+    return Fp8Inputs(w, qb, kb, vt, qs, ks, vs)
+
+
+# The 8k-token, 32-head causal shape in 8 bits.
+FP8_WORKLOADS = [
+    Fp8Workload("fp8_b1h32_s8192_d128_causal", 1, 32, 32, 8192, 8192, 128, "causal", seed=3001),
+]

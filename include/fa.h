@@ -176,6 +176,31 @@ fa_status fa_bwd_workspace_query(int B, int H, int H_kv, int Sq, int Sk, int d, 
                                  int window, int dtype, size_t *bytes);
 
 /*
+ * fa_fwd_fp8 -- the fused forward with 8-bit inputs ("FlashAttention:
+ * IO-aware attention kernels", section "Concept", names low-precision paths
+ * as a later variant).  Q, K and V are e4m3 codes with one dequantisation
+ * factor per tensor (value = code x descale); S = Q K^T and P V run on the
+ * 8-bit tensor path with fp32 accumulation, the running max, sum and
+ * rescaling are those of fa_fwd, P is rounded to e4m3 (scaled by 256) before
+ * P V, O is written as bf16 and lse (natural log of the scaled row sums) as
+ * fp32.  Exact up to the rounding of P: each output element differs from the
+ * exact attention of the dequantised inputs by at most about 2^-4 of
+ * sum_j P_ij |v_jc|, plus its bf16 rounding.
+ *
+ *   q    [B, H, Sq, d] e4m3; k [B, H_kv, Sk, d] e4m3
+ *   vt   V transposed, [B, H_kv, d, Sk] e4m3 (both tile products then read
+ *        K-major operands); Sk a multiple of 16 (16-byte rows)
+ *   o    [B, H, Sq, d] bf16; lse [B, H, Sq] fp32
+ *   d    128 (else FA_ERR_UNSUPPORTED)
+ *   scale, q_descale, k_descale, v_descale: finite; descales > 0
+ *   the rest as for fa_fwd_gqa (masks, window, H_kv grouping, errors)
+ */
+fa_status fa_fwd_fp8(const void *q, const void *k, const void *vt, void *o, float *lse, int B,
+                     int H, int H_kv, int Sq, int Sk, int d, float scale, float q_descale,
+                     float k_descale, float v_descale, int mask_kind, int window,
+                     fa_stream_t stream);
+
+/*
  * fa_decode_paged -- attention of the newest Sq rows of each request over its
  * paged K/V cache, as in decoding ("Flash attention and memory-efficient
  * attention variants", sections "A different bottleneck: the KV cache during

@@ -1,0 +1,118 @@
+"""GPU parity of the 8-bit forward (fa_fwd_fp8) against the fp64 oracle on
+the dequantised inputs.
+
+Tolerance, from the arithmetic: S is exact up to fp32 accumulation of
+products of e4m3 values, and the only rounding on the way to O is that of P
+to e4m3 (3 mantissa bits: relative error at most 2^-4 for normal codes; the
+factor 256 keeps weights down to 2^-14 normal) and of O to bf16.  So per
+element |O - O_ref| <= 2^-4 sum_j P_ij |v_jc| + 2^-8 |O_ref| (+1e-6), where
+sum_j P_ij |v_jc| is the oracle's attention over |V|.  The lse is computed
+from unrounded weights: |lse - lse_ref| <= 1e-3 as in the 16-bit forward.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from exact_io_aware_30_gb300 import fa, inputs
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from exact_io_aware_30_gb300 import build
+    build.build()
+    fa.load()
+    torch.cuda.set_device(0)
+    yield
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+
+
+def run_gpu(inp):
+    w = inp.workload
+    q, k, vt = (torch.from_numpy(np.ascontiguousarray(b)).cuda()
+                for b in (inp.q_bits, inp.k_bits, inp.vt_bits))
+    o, lse = fa.forward_fp8(q, k, vt, inp.q_descale, inp.k_descale, inp.v_descale, scale=w.scale,
+                            mask=w.mask, window=w.window)
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def check(inp, rows=None):
+    w = inp.workload
+    o, lse = run_gpu(inp)
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
+    pv_abs, _ = oracle.attention(qf, kf, np.abs(vf), w.scale, w.mask, w.window, rows=rows)
+    if rows is not None:
+        o, lse = o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows]
+    assert np.all(np.isfinite(o))
+    bound = 2.0 ** -4 * pv_abs + 2.0 ** -8 * np.abs(o_ref) + 1e-6
+    err = np.abs(o - o_ref)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(fin, np.isfinite(lse))
+    stats = dict(max=float(err.max()), mean=float(err.mean()),
+                 worst_ratio=float((err / bound).max()),
+                 lse=float(np.abs(lse[fin] - lse_ref[fin]).max()) if fin.any() else 0.0)
+    assert np.all(err <= bound), stats
+    assert stats["lse"] <= 1e-3, stats
+    return stats
+
+
+SHAPES = [(1, 16), (7, 32), (127, 128), (128, 128), (129, 144), (300, 304), (300, 176),
+          (173, 304), (700, 704)]
+
+
+@pytest.mark.parametrize("mask,window", [("none", 0), ("causal", 0), ("window", 1), ("window", 77)])
+def test_fp8_parity_small(mask, window):
+    for i, (Sq, Sk) in enumerate(SHAPES):
+        w = inputs.Fp8Workload("t", 1, 2, 2, Sq, Sk, 128, mask, window, seed=40 + i)
+        print(Sq, Sk, check(inputs.generate_fp8(w)))
+
+
+@pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (6, 1)])
+def test_fp8_heads_batches_and_groups(H, Hkv):
+    w = inputs.Fp8Workload("t", 2, H, Hkv, 400, 512, 128, "causal", seed=50 + H + Hkv)
+    print(check(inputs.generate_fp8(w)))
+
+
+def test_fp8_rows_without_keys():
+    w = inputs.Fp8Workload("t", 1, 2, 2, 300, 48, 128, "window", 17, seed=55)
+    inp = inputs.generate_fp8(w)
+    check(inp)
+    o, lse = run_gpu(inp)
+    empty = np.arange(300) >= 48 + 16
+    assert np.all(o[:, :, empty] == 0) and np.all(np.isneginf(lse[:, :, empty]))
+
+
+def test_fp8_refusals():
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.uint8, device="cuda")
+    vt = torch.zeros(1, 1, 64, 16, dtype=torch.uint8, device="cuda")
+    k = torch.zeros(1, 1, 16, 64, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward_fp8(q, k, vt, 1.0, 1.0, 1.0)
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # d = 64
+    q = torch.zeros(1, 1, 8, 128, dtype=torch.uint8, device="cuda")
+    k = torch.zeros(1, 1, 20, 128, dtype=torch.uint8, device="cuda")
+    vt = torch.zeros(1, 1, 128, 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward_fp8(q, k, vt, 1.0, 1.0, 1.0)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG  # Sk not a multiple of 16
+    k = torch.zeros(1, 1, 32, 128, dtype=torch.uint8, device="cuda")
+    vt = torch.zeros(1, 1, 128, 32, dtype=torch.uint8, device="cuda")
+    with pytest.raises(fa.FAError) as e:
+        fa.forward_fp8(q, k, vt, 1.0, 0.0, 1.0)
+    assert e.value.status == fa.FA_ERR_INVALID_ARG  # descale must be positive
+
+
+def test_fp8_full_size_sampled():
+    w = inputs.FP8_WORKLOADS[0]
+    inp = inputs.generate_fp8(w)
+    rng = np.random.default_rng(33)
+    rows = np.unique(np.concatenate([rng.integers(0, w.B * w.H * w.Sq, 256),
+                                     [0, 127, 128, w.Sq - 1, w.B * w.H * w.Sq - 1]]))
+    print(w.name, check(inp, rows=rows))

@@ -645,3 +645,32 @@ def test_generator_is_seeded_and_spiky():
     for h in range(2):
         assert (norms[0, h] > 8.0).sum() >= 1
     assert len(inputs.WORKLOADS) == 5
+
+
+def test_e4m3_rounding_matches_torch():
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    rng = np.random.default_rng(12)
+    x = np.concatenate([rng.standard_normal(200000).astype(np.float32) * 40,
+                        rng.standard_normal(20000).astype(np.float32) * 1e-2,
+                        np.array([448, 0.0, -0.0, 2 ** -9, 2 ** -10, 3 * 2 ** -10, 1.0625, 1.1875,
+                                  -17.0, 240.0, 232.0], np.float32)])
+    x = x[np.abs(x) <= 448]  # above 448 the code saturates here
+    bits = inputs.f32_to_e4m3_bits(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(bits, ref)
+    assert np.array_equal(inputs.e4m3_bits_to_f64(bits),
+                          torch.from_numpy(ref).view(torch.float8_e4m3fn).to(torch.float64).numpy())
+    assert inputs.f32_to_e4m3_bits(np.array([1000.0, -1e6], np.float32)).tolist() == [0x7E, 0xFE]
+
+
+def test_fp8_generator_dequantises_exactly():
+    w = inputs.Fp8Workload("t", 1, 2, 1, 40, 48, 128, "causal", seed=3)
+    a = inputs.generate_fp8(w)
+    q, k, v = a.f64()
+    assert q.shape == (1, 2, 40, 128) and k.shape == v.shape == (1, 1, 48, 128)
+    # descales are powers of two and every value is an e4m3 value times its factor
+    for f in (a.q_descale, a.k_descale, a.v_descale):
+        assert 2.0 ** np.round(np.log2(f)) == f
+    assert np.array_equal(inputs.e4m3_bits_to_f64(a.vt_bits).transpose(0, 1, 3, 2) * a.v_descale, v)
