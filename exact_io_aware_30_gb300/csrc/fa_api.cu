@@ -702,7 +702,7 @@ fa_status fp8_impl(const void *q, const void *k, const void *vt, void *o, float 
     p.mask_kind = mask_kind;
     p.window = (mask_kind == FA_MASK_SLIDING_WINDOW) ? window : 0;
     p.c = std::fmax((float)((double)scale * q_descale * k_descale * 1.4426950408889634), FLT_MIN);
-    p.o_mul = v_descale / Fp8Cfg::P_MUL;
+    p.o_mul = v_descale;  // the weights' factor 2^P_LOG2 cancels in O / l
     p.n_qtiles = (Sq + 127) / 128;
     p.wait_limit_ns = fa::kWaitLimitNs;
     const int smem = Fp8Cfg::SMEM_BYTES;

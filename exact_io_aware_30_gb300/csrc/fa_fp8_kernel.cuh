@@ -9,10 +9,12 @@
 // of a stored code x is x * q_descale (k_descale, v_descale).  The kernel
 // computes S = Q K^T on the 8-bit tensor path (kind::f8f6f4, fp32
 // accumulation) with the factors and 1/sqrt(d)-type scale folded into the
-// exponent's multiplier, keeps a running max, sum and unnormalised O per row,
-// and stores P as e4m3 (times 256, so that weights in [2^-17, 1] keep normal
-// or subnormal codes) for O += P V on the same 8-bit path.  O is written as
-// bf16, lse in fp32.
+// exponent's multiplier, keeps a running reference max, sum and unnormalised
+// O per row, and stores P as e4m3 for O += P V on the same 8-bit path.  The
+// reference moves (and O is rescaled) only when a tile's max exceeds it by
+// more than 2^4, as the forward defers rescaling; weights, at most 2^4, are
+// stored times 2^4 (at most 256, inside e4m3's range of 448).  O is written
+// as bf16, lse in fp32.
 //
 // V is taken transposed, [B, H_kv, d, Sk]: both tile products then read
 // K-major operands (keys contiguous for V^T), the operand layout every 8-bit
@@ -39,7 +41,7 @@ struct Fp8Params {
     int B, H, Hkv, kv_group, Sq, Sk;
     int mask_kind, window;
     float c;            // scale * q_descale * k_descale * log2(e), kept positive
-    float o_mul;        // v_descale / 256 (P is stored times 256)
+    float o_mul;        // v_descale (the weights' stored factor cancels in O / l)
     int n_qtiles;
     uint64_t wait_limit_ns;
 };
@@ -73,7 +75,8 @@ struct Fp8Cfg {
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
-    static constexpr float P_MUL = 256.f;
+    static constexpr float TAU = 4.f;     // log2 of the stale-reference slack
+    static constexpr float P_LOG2 = 4.f;  // weights are stored times 2^P_LOG2 (<= 2^8)
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
 
@@ -246,29 +249,46 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
         int lo = 0, hi = min(C::BN, p.Sk - k0);
         if (p.mask_kind != kMaskNone) hi = min(hi, i - k0 + 1);
         if (p.mask_kind == kMaskWindow) lo = max(0, i - p.window + 1 - k0);
-        float mt = -INFINITY;
+        const bool masked = lo > 0 || hi < C::BN;
+        if (masked) {
 #pragma unroll
-        for (int e = 0; e < C::BN; ++e) {
-            const float x = __uint_as_float(s[e]) * c;
-            const float y = (e >= lo && e < hi) ? x : -INFINITY;
-            s[e] = __float_as_uint(y);
-            mt = fmaxf(mt, y);
+            for (int e = 0; e < C::BN; ++e)
+                if (e < lo || e >= hi) s[e] = __float_as_uint(-INFINITY);
         }
-        const float m_new = fmaxf(m, mt);
+        float smax = __uint_as_float(s[0]);
+#pragma unroll
+        for (int e = 1; e + 1 < C::BN; e += 2)
+            smax = ptx::max3(smax, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
+        smax = fmaxf(smax, __uint_as_float(s[C::BN - 1]));
+        // Deferred rescaling: the reference max moves only when the tile's max
+        // exceeds it by more than 2^4, so weights stay below 2^4 (stored times
+        // 2^4: at most 256, inside e4m3's range) and O is rescaled rarely.
+        const float mt = smax * c;  // -inf when no key of the tile is visible
+        const bool grow = mt > m + C::TAU;
+        const float m_new = grow ? mt : m;
         const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = ptx::ex2_approx(m - m_use);
+        const float alpha = ptx::ex2_approx(m - m_use);  // 1 unless the reference moved
+        const float shift = m_use - C::P_LOG2;           // weights carry the factor 2^P_LOG2
+        const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(-shift, -shift);
+        uint64_t acc0 = ptx::f32x2(0.f, 0.f), acc1 = acc0;
         uint32_t pw[C::BN / 4];
-        float ps = 0.f;
 #pragma unroll
         for (int e = 0; e < C::BN; e += 4) {
-            const float p0 = ptx::ex2_approx(__uint_as_float(s[e]) - m_use);
-            const float p1 = ptx::ex2_approx(__uint_as_float(s[e + 1]) - m_use);
-            const float p2 = ptx::ex2_approx(__uint_as_float(s[e + 2]) - m_use);
-            const float p3 = ptx::ex2_approx(__uint_as_float(s[e + 3]) - m_use);
-            ps += (p0 + p1) + (p2 + p3);
-            pw[e / 4] = ptx::pack_e4m3x4(p0 * C::P_MUL, p1 * C::P_MUL, p2 * C::P_MUL, p3 * C::P_MUL);
+            float x0, x1, x2, x3;
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2, n2),
+                              x0, x1);
+            ptx::unpack_f32x2(
+                ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), c2, n2), x2, x3);
+            const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
+            const float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
+            acc0 = ptx::add_f32x2(acc0, ptx::f32x2(p0, p1));
+            acc1 = ptx::add_f32x2(acc1, ptx::f32x2(p2, p3));
+            pw[e / 4] = ptx::pack_e4m3x4(p0, p1, p2, p3);
         }
-        l = l * alpha + ps;
+        float a0, a1, a2, a3;
+        ptx::unpack_f32x2(acc0, a0, a1);
+        ptx::unpack_f32x2(acc1, a2, a3);
+        l = l * alpha + ((a0 + a1) + (a2 + a3));
         if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 69)) {
             ok = false;
             break;
@@ -316,7 +336,8 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
         }
         if (row_ok) store_row32<false>(orow + cc * 64, o, mul);
     }
-    if (row_ok) p.lse[row] = seen ? (m + __log2f(l)) * kLn2 : -INFINITY;
+    // l sums the weights times 2^P_LOG2 against the reference m
+    if (row_ok) p.lse[row] = seen ? (m - C::P_LOG2 + __log2f(l)) * kLn2 : -INFINITY;
 }
 
 __global__ void __launch_bounds__(Fp8Cfg::NUM_THREADS, 1) fa_fwd_fp8_kernel(const __grid_constant__ Fp8Params p) {
