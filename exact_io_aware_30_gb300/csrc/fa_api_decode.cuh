@@ -1,0 +1,174 @@
+// fa_api_decode.cuh -- host side of decoding over a paged cache
+// (fa_decode_paged, fa_decode_workspace_query).
+// Included once, by fa_api.cu, after its shared helpers (device probe, tensor
+// maps, argument checks); holds the argument checks, tensor maps and launches
+// of these entry points.
+#pragma once
+
+#include "fa_decode_kernel.cuh"
+
+namespace fa {
+
+namespace {
+
+// ---------------------------------------------------------------- paged decode
+
+struct DecPlan {
+    int n_splits = 1, tiles_per_split = 1;
+    size_t part_o_bytes = 0, bytes = 0;
+};
+
+fa_status check_dec_sizes(int B, int H, int Hkv, int Sq, int d, int block_size, int max_blocks,
+                          int num_blocks, int max_seq_len, int mask_kind, int dtype) {
+    if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL) return FA_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
+        return FA_ERR_UNSUPPORTED;
+    if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Sq < 1) return FA_ERR_INVALID_ARG;
+    if ((long long)(H / Hkv) * Sq > 128) return FA_ERR_UNSUPPORTED;  // packed rows of one K/V head
+    if (max_blocks < 1 || num_blocks < 1 || max_seq_len < Sq ||
+        (long long)max_seq_len > (long long)max_blocks * block_size)
+        return FA_ERR_INVALID_ARG;
+    if ((long long)B * H * Sq > 0x7fffffffLL / 2 || (long long)B * max_blocks > 0x7fffffffLL)
+        return FA_ERR_INVALID_ARG;
+    return FA_OK;
+}
+
+// Key ranges per (request, K/V head): enough splits that about two CTAs per
+// SM are in flight, never more than the longest request has 128-key tiles.
+DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int num_sms) {
+    DecPlan pl;
+    const long long tiles = (max_seq_len + 127) / 128;
+    const long long base = (long long)B * Hkv;
+    long long n = (2LL * num_sms + base - 1) / base;
+    n = std::max(1LL, std::min(n, tiles));
+    const long long per = (tiles + n - 1) / n;
+    pl.tiles_per_split = (int)per;
+    pl.n_splits = (int)((tiles + per - 1) / per);
+    const size_t rows = (size_t)B * H * Sq;
+    pl.part_o_bytes = ((size_t)pl.n_splits * rows * d * 4 + 255) / 256 * 256;
+    pl.bytes = pl.part_o_bytes + (size_t)pl.n_splits * rows * 4;
+    return pl;
+}
+
+template <int D, bool kFP16>
+fa_status launch_decode(const DecParams &p, void *o, float *lse, DeviceInfo &info, cudaStream_t stream) {
+    using C = DecCfg<D>;
+    auto kern = fa_decode_kernel<D, kFP16>;
+    const int slot = (D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
+    const int smem = std::max(C::SMEM_BYTES, kBwdMinSmem);  // one CTA (and its 512 TMEM columns) per SM
+    if (set_smem(kern, smem, info.attr_dec[slot]) != FA_OK) return FA_ERR_CUDA;
+    const long long grid = (long long)p.B * p.Hkv * p.n_splits;
+    kern<<<(unsigned)grid, C::NUM_THREADS, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    const int rows = p.B * p.H * p.Sq;
+    fa_decode_combine_kernel<D, kFP16><<<(rows + 7) / 8, 256, 0, stream>>>(p.part_o, p.part_lse, o, lse,
+                                                                          rows, p.n_splits);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, const int *block_table,
+                      const int *seq_lens, void *o, float *lse, void *workspace, size_t workspace_bytes,
+                      int B, int H, int Hkv, int Sq, int d, int block_size, int max_blocks,
+                      int num_blocks, int max_seq_len, float scale, int mask_kind, int dtype,
+                      cudaStream_t stream) {
+    fa_status st = check_dec_sizes(B, H, Hkv, Sq, d, block_size, max_blocks, num_blocks, max_seq_len,
+                                   mask_kind, dtype);
+    if (st != FA_OK) return st;
+    if (!std::isfinite(scale) || scale < 0.f) return FA_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse || !workspace)
+        return FA_ERR_INVALID_ARG;
+    const uintptr_t a16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_cache) |
+                          reinterpret_cast<uintptr_t>(v_cache) | reinterpret_cast<uintptr_t>(o);
+    const uintptr_t a4 = reinterpret_cast<uintptr_t>(lse) | reinterpret_cast<uintptr_t>(block_table) |
+                         reinterpret_cast<uintptr_t>(seq_lens);
+    if ((a16 & 15u) || (a4 & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+        return FA_ERR_MISALIGNED;
+    int dev = 0;
+    DeviceInfo *info = nullptr;
+    st = device_info(&dev, &info);
+    if (st != FA_OK) return st;
+    const DecPlan pl = plan_decode(B, H, Hkv, Sq, d, max_seq_len, info->num_sms);
+    if (workspace_bytes < pl.bytes) return FA_ERR_INVALID_ARG;
+    const size_t rows = (size_t)B * H * Sq;
+    const size_t qo = rows * d * 2, cache = (size_t)num_blocks * Hkv * block_size * d * 2;
+    const void *ins[5] = {q, k_cache, v_cache, block_table, seq_lens};
+    const size_t in_bytes[5] = {qo, cache, cache, (size_t)B * max_blocks * 4, (size_t)B * 4};
+    void *outs[3] = {o, lse, workspace};
+    const size_t out_bytes[3] = {qo, rows * 4, pl.bytes};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 5; ++b)
+            if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA_ERR_INVALID_ARG;
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA_ERR_INVALID_ARG;
+    }
+
+    const bool fp16 = dtype == FA_DTYPE_FP16;
+    DecParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!make_map(&p.tm_q, q, d, (int)rows, 1, 1, 128, fp16) ||
+        !make_map(&p.tm_k, k_cache, d, block_size, Hkv, num_blocks, block_size, fp16) ||
+        !make_map(&p.tm_v, v_cache, d, block_size, Hkv, num_blocks, block_size, fp16))
+        return FA_ERR_CUDA;
+    p.block_table = block_table;
+    p.seq_lens = seq_lens;
+    p.part_o = static_cast<float *>(workspace);
+    p.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.B = B;
+    p.H = H;
+    p.Hkv = Hkv;
+    p.kv_group = H / Hkv;
+    p.Sq = Sq;
+    p.R = p.kv_group * Sq;
+    p.bs = block_size;
+    p.max_blocks = max_blocks;
+    p.max_seq_len = max_seq_len;
+    p.mask_kind = mask_kind;
+    p.n_splits = pl.n_splits;
+    p.tiles_per_split = pl.tiles_per_split;
+    p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
+    p.wait_limit_ns = fa::kWaitLimitNs;
+    if (log_enabled())
+        std::fprintf(stderr, "[fa] fa_decode_paged d=%d B=%d H=%d Hkv=%d Sq=%d bs=%d max_len=%d splits=%d x %d tiles\n",
+                     d, B, H, Hkv, Sq, block_size, max_seq_len, pl.n_splits, pl.tiles_per_split);
+    if (d == 64)
+        return fp16 ? launch_decode<64, true>(p, o, lse, *info, stream)
+                    : launch_decode<64, false>(p, o, lse, *info, stream);
+    return fp16 ? launch_decode<128, true>(p, o, lse, *info, stream)
+                : launch_decode<128, false>(p, o, lse, *info, stream);
+}
+
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
+                          const int *block_table, const int *seq_lens, void *o, float *lse,
+                          void *workspace, size_t workspace_bytes, int B, int H, int H_kv, int Sq,
+                          int d, int block_size, int max_blocks, int num_blocks, int max_seq_len,
+                          float scale, int mask_kind, int dtype, fa_stream_t stream) {
+    return fa::decode_impl(q, k_cache, v_cache, block_table, seq_lens, o, lse, workspace,
+                           workspace_bytes, B, H, H_kv, Sq, d, block_size, max_blocks, num_blocks,
+                           max_seq_len, scale, mask_kind, dtype, reinterpret_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int block_size,
+                                    int max_blocks, int num_blocks, int max_seq_len, int mask_kind,
+                                    int dtype, size_t *bytes) {
+    if (!bytes) return FA_ERR_INVALID_ARG;
+    *bytes = 0;
+    fa_status st = fa::check_dec_sizes(B, H, H_kv, Sq, d, block_size, max_blocks, num_blocks,
+                                       max_seq_len, mask_kind, dtype);
+    if (st != FA_OK) return st;
+    int dev = 0;
+    fa::DeviceInfo *info = nullptr;
+    st = fa::device_info(&dev, &info);
+    if (st == FA_OK) *bytes = fa::plan_decode(B, H, H_kv, Sq, d, max_seq_len, info->num_sms).bytes;
+    return st;
+}
+
+}  // extern "C"

@@ -14,21 +14,23 @@
 // tensor memory.
 //
 // GB300 mapping (one CTA per SM, persistent over work units):
-//   * a work unit is one query tile of 128 rows of one (batch, head); units
-//     are taken longest-first in a snake order over the CTAs;
-//   * one TMA warp streams the Q tile and a ring of stages into shared
-//     memory (128-byte swizzle, 64 columns per box); stage k of a unit holds
-//     key tile k and value tile k-1, the two tiles one MMA iteration uses;
-//   * two MMA warps (one issuing lane each) run the tcgen05 MMAs with fp32
-//     accumulators in tensor memory: one issues S = Q K^T (both operands in
-//     shared memory) into two S buffers, each as soon as the softmax has
-//     read the buffer's previous tile, so S of tile j+2 is computed while
-//     the softmax works on tile j+1; the other issues O += P V (P read from
-//     its own tensor-memory area) as soon as the softmax has written P;
-//   * one softmax warpgroup owns the 128 rows, one row per thread (= one
-//     TMEM lane): it reads a row of S, masks boundary tiles, exponentiates,
-//     writes P (16-bit) back over S, rescales O in tensor memory when the max
-//     grew enough, and runs the epilogue (O / l, lse).
+//   * a work unit is one 128-row query tile of one (batch, head); the host
+//     deals the units to the CTAs (least loaded first) in groups of heads
+//     whose K and V fit in a third of the L2, so each K/V byte comes from
+//     DRAM about once;
+//   * warp 10 streams the Q tile and a ring of K tiles, warp 11 a ring of V
+//     tiles, by TMA (128-byte swizzle, 64-column boxes);
+//   * warp 8 issues S = Q K^T (tcgen05, both operands in shared memory) into
+//     two S buffers in tensor memory, each as soon as the softmax has read
+//     that buffer's previous tile; warp 9 issues O += P V with P read from
+//     its own double-buffered tensor-memory area;
+//   * warps 0-7 are the softmax: warp w owns 16 rows (TMEM lanes) and every
+//     key column of a tile in the 16-lane tcgen05.ld layout, where a row's
+//     columns sit in one quad of threads, so max and sum take two shuffles
+//     and the warps never synchronise during a unit; they mask boundary
+//     tiles, exponentiate, write P (16-bit), rescale O in tensor memory when
+//     the reference max moves, and run the epilogue (O / l through a bulk
+//     tensor store for d <= 128, and lse).
 //
 // Rescaling is deferred until the running max has grown by more than 2^8
 // (log2 units).  Until then the accumulator and the sums both stay referenced
