@@ -821,7 +821,11 @@ def main(argv=None):
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.direction == "fp8":
-        return run_ours_fp8(args, inputs.FP8_WORKLOADS[0])
+        wf = inputs.FP8_WORKLOADS[0]
+        if args.heads:
+            import dataclasses
+            wf = dataclasses.replace(wf, H=args.heads, Hkv=args.heads, name=f"{wf.name}_h{args.heads}")
+        return run_ours_fp8(args, wf)
     if args.direction == "decode":
         wd = args.workload if args.workload != str(DEFAULT_WORKLOAD) else "0"
         return run_ours_decode(args, inputs.PAGED_WORKLOADS[int(wd)])

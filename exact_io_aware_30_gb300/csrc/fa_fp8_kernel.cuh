@@ -20,9 +20,11 @@
 // K-major operands (keys contiguous for V^T), the operand layout every 8-bit
 // tcgen05 form accepts.
 //
-// One CTA per 128-row query tile (longest first); warps 0-3 softmax and
-// epilogue (one row per thread), warp 4 issues the MMAs, warp 5 the TMA copies
-// (Q once, K and V^T tiles through rings of four slots each).
+// One CTA per 128-row query tile (longest first), two CTAs per SM; warps 0-3
+// softmax and epilogue (one row per thread), warp 4 issues the MMAs, warp 5
+// the TMA copies (Q once, K and V^T tiles through rings of three and two
+// slots).  Within a CTA a tile's S, softmax and P V follow one another; the
+// other CTA on the SM fills the tensor core and the issue slots meanwhile.
 #pragma once
 
 #include <math.h>
@@ -49,27 +51,29 @@ struct Fp8Params {
 struct Fp8Cfg {
     static constexpr int D = 128;
     static constexpr int BN = 128;
-    static constexpr int KST = 4;
-    static constexpr int VST = 4;
+    static constexpr int KST = 3;
+    static constexpr int VST = 2;
     static constexpr int Q_BYTES = 128 * D;   // one 128-byte-wide box
     static constexpr int TILE_BYTES = BN * D;  // K tile, or V^T tile (d rows x 128 keys)
     static constexpr int NUM_SOFTMAX = 128;
     static constexpr int MMA_WARP = 4;
     static constexpr int TMA_WARP = 5;
     static constexpr int NUM_THREADS = 192;
-    static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t S_COL = 0;     // two S buffers
-    static constexpr uint32_t O_COL = 256;
-    static constexpr uint32_t P_COL = 384;   // 128 keys of e4m3: 32 columns
+    // Two CTAs share an SM (each its 256 tensor-memory columns): S, then O.
+    // P (128 keys of e4m3: 32 columns) is written over the first columns of
+    // S once the softmax has read S, so the next S waits for P V.
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t S_COL = 0;
+    static constexpr uint32_t O_COL = 128;
+    static constexpr uint32_t P_COL = 0;
     static constexpr int B_QFULL = 0;
     static constexpr int B_KFULL = 1;
     static constexpr int B_KEMPTY = B_KFULL + KST;
     static constexpr int B_VFULL = B_KEMPTY + KST;
     static constexpr int B_VEMPTY = B_VFULL + VST;
-    static constexpr int B_SFULL = B_VEMPTY + VST;  // [2]
-    static constexpr int B_SFREE = B_SFULL + 2;     // [2]
-    static constexpr int B_PFULL = B_SFREE + 2;
-    static constexpr int B_PFREE = B_PFULL + 1;
+    static constexpr int B_SFULL = B_VEMPTY + VST;
+    static constexpr int B_PFULL = B_SFULL + 1;
+    static constexpr int B_PFREE = B_PFULL + 1;     // P V done: S's columns are free again
     static constexpr int B_OFINAL = B_PFREE + 1;
     static constexpr int B_DRAIN = B_OFINAL + 1;
     static constexpr int NUM_BARS = B_DRAIN + 1;
@@ -77,7 +81,7 @@ struct Fp8Cfg {
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static constexpr float TAU = 4.f;     // log2 of the stale-reference slack
     static constexpr float P_LOG2 = 4.f;  // weights are stored times 2^P_LOG2 (<= 2^8)
-    static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
+    static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs per SM");
 };
 
 struct Fp8Unit {
@@ -165,52 +169,47 @@ __device__ void fp8_mma_role(const Fp8Params &p, const Fp8Unit &un, uint8_t *sQ,
     const bool leader = ptx::lane_id() == 0;
     const uint64_t qd = smem_desc(ptx::smem_addr(sQ), 16);
     bool ok = un.n == 0 || wait_warp(bar_addr(bars, C::B_QFULL), 0, ctl, 63);
-    for (int t = 0; ok && t <= un.n; ++t) {
-        if (t < un.n) {
-            const int ks = t % C::KST;
-            const uint32_t b = (uint32_t)t & 1u;
-            if (!wait_warp(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 64)) {
-                ok = false;
-                break;
-            }
-            if (t >= 2 && !wait_warp(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1) & 1, ctl, 65)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            if (leader) {
-                const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::TILE_BYTES), 16);
-                // 32 elements (32 bytes) per instruction inside the 128-byte row
-#pragma unroll
-                for (int kk = 0; kk < C::D / 32; ++kk)
-                    ptx::mma_ss_f8(tmem + C::S_COL + b * C::BN, qd + (uint32_t)((kk * 32) >> 4),
-                                   kd + (uint32_t)((kk * 32) >> 4), kIdescS, kk > 0 ? 1u : 0u);
-                ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
-                ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + ks));
-            }
-            __syncwarp();
+    for (int t = 0; ok && t < un.n; ++t) {
+        const int ks = t % C::KST, vs = t % C::VST;
+        if (!wait_warp(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 64)) {
+            ok = false;
+            break;
         }
-        if (t >= 1) {
-            const int tp = t - 1, vs = tp % C::VST;
-            if (!wait_warp(bar_addr(bars, C::B_VFULL + vs), (tp / C::VST) & 1, ctl, 66) ||
-                !wait_warp(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 67)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            if (leader) {
-                // V^T tile: N = d rows of 128 keys (128 bytes), K-major
-                const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::TILE_BYTES), 16);
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 32; ++kk)
-                    ptx::mma_ts_f8(tmem + C::O_COL, tmem + C::P_COL + kk * 8, vd + (uint32_t)((kk * 32) >> 4),
-                                   kIdescO, (tp > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(bar_addr(bars, C::B_PFREE));
-                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
-                if (tp + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
-            }
-            __syncwarp();
+        // P V of tile t-1 has read P out of S's columns
+        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 65)) {
+            ok = false;
+            break;
         }
+        ptx::tc_fence_after();
+        if (leader) {
+            const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::TILE_BYTES), 16);
+            // 32 elements (32 bytes) per instruction inside the 128-byte row
+#pragma unroll
+            for (int kk = 0; kk < C::D / 32; ++kk)
+                ptx::mma_ss_f8(tmem + C::S_COL, qd + (uint32_t)((kk * 32) >> 4), kd + (uint32_t)((kk * 32) >> 4),
+                               kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + ks));
+        }
+        __syncwarp();
+        if (!wait_warp(bar_addr(bars, C::B_VFULL + vs), (t / C::VST) & 1, ctl, 66) ||
+            !wait_warp(bar_addr(bars, C::B_PFULL), t & 1, ctl, 67)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        if (leader) {
+            // V^T tile: N = d rows of 128 keys (128 bytes), K-major
+            const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::TILE_BYTES), 16);
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 32; ++kk)
+                ptx::mma_ts_f8(tmem + C::O_COL, tmem + C::P_COL + kk * 8, vd + (uint32_t)((kk * 32) >> 4),
+                               kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+            ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
+            if (t + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
+        }
+        __syncwarp();
     }
     if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
     __syncwarp();
@@ -228,22 +227,19 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int t = 0; t < un.n; ++t) {
-        const uint32_t b = (uint32_t)t & 1u;
         const int k0 = (un.lo + t) * C::BN;
-        if (!wait_warp(bar_addr(bars, C::B_SFULL + (int)b), (t >> 1) & 1, ctl, 68)) {
+        if (!wait_warp(bar_addr(bars, C::B_SFULL), t & 1, ctl, 68)) {
             ok = false;
             break;
         }
         ptx::tc_fence_after();
         uint32_t s[C::BN];
-        ptx::tmem_ld_x32<0>(lane_base + C::S_COL + b * C::BN, s);
-        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + b * C::BN + 32, s);
-        ptx::tmem_ld_x32<64>(lane_base + C::S_COL + b * C::BN + 64, s);
-        ptx::tmem_ld_x32<96>(lane_base + C::S_COL + b * C::BN + 96, s);
+        ptx::tmem_ld_x32<0>(lane_base + C::S_COL, s);
+        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
+        ptx::tmem_ld_x32<64>(lane_base + C::S_COL + 64, s);
+        ptx::tmem_ld_x32<96>(lane_base + C::S_COL + 96, s);
         ptx::tmem_wait_ld();
         ptx::reg_fence<C::BN>(s);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(bars, C::B_SFREE + (int)b));
 
         // key k0 + e is visible to row i iff lo <= e < hi
         int lo = 0, hi = min(C::BN, p.Sk - k0);
@@ -289,11 +285,8 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
         ptx::unpack_f32x2(acc0, a0, a1);
         ptx::unpack_f32x2(acc1, a2, a3);
         l = l * alpha + ((a0 + a1) + (a2 + a3));
-        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 69)) {
-            ok = false;
-            break;
-        }
-        ptx::tc_fence_after();
+        // S of this tile was issued after P V of the previous one had run, so
+        // O is stable and P may go over S's columns
         if (t >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
             for (int cc = 0; cc < C::D / 32; ++cc) {
@@ -340,7 +333,7 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
     if (row_ok) p.lse[row] = seen ? (m - C::P_LOG2 + __log2f(l)) * kLn2 : -INFINITY;
 }
 
-__global__ void __launch_bounds__(Fp8Cfg::NUM_THREADS, 1) fa_fwd_fp8_kernel(const __grid_constant__ Fp8Params p) {
+__global__ void __launch_bounds__(Fp8Cfg::NUM_THREADS, 2) fa_fwd_fp8_kernel(const __grid_constant__ Fp8Params p) {
     using C = Fp8Cfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -364,10 +357,7 @@ __global__ void __launch_bounds__(Fp8Cfg::NUM_THREADS, 1) fa_fwd_fp8_kernel(cons
             ptx::mbar_init(bar_addr(bars, C::B_VFULL + s), 1);
             ptx::mbar_init(bar_addr(bars, C::B_VEMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_SFREE + b), C::NUM_SOFTMAX);
-        }
+        ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_SOFTMAX);
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
