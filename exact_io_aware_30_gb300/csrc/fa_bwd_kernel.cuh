@@ -181,9 +181,10 @@ struct BwdKVCfg {
     static constexpr int NUM_COMPUTE = 128;
     static constexpr int WG = NUM_COMPUTE / 128;   // warpgroups splitting the columns
     static constexpr int COLS = BM / WG;           // query columns per compute warp
-    static constexpr int MMA_WARP = NUM_COMPUTE / 32;
-    static constexpr int TMA_WARP = MMA_WARP + 1;
-    static constexpr int NUM_THREADS = NUM_COMPUTE + 64;
+    static constexpr int MMA_WARP = NUM_COMPUTE / 32;  // issues S^T and dP^T
+    static constexpr int MMA_G_WARP = MMA_WARP + 1;    // issues dV and dK
+    static constexpr int TMA_WARP = MMA_WARP + 2;
+    static constexpr int NUM_THREADS = NUM_COMPUTE + 96;
     // Tensor memory: dV and dK accumulators, S^T and dP^T (fp32, 64 columns
     // each), P^T and dS^T (16-bit pairs, 32 columns each).
     static constexpr uint32_t TMEM_COLS = 512;
@@ -201,8 +202,8 @@ struct BwdKVCfg {
     static constexpr int B_PFULL = B_SFREE + 1;
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_DONE = B_PFREE + 1;
-    static constexpr int B_DRAIN = B_DONE + 1;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_DRAIN = B_DONE + 1;  // [2]: each issuer's MMAs finished
+    static constexpr int NUM_BARS = B_DRAIN + 2;
     static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(D <= 128, "dK and dV accumulators need 2 x d tensor-memory columns");
@@ -296,74 +297,90 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     }
 }
 
+// The two MMA issuers of the dK/dV kernel.  A tcgen05.mma costs tens of
+// cycles of single-thread issue, and a step needs 24 of them, so the score
+// products (S^T, dP^T) and the gradient products (dV, dK) go out from two
+// warps.  A Q/dO stage is free once both have read it (QEMPTY takes one
+// commit from each).
 template <int D, bool kFP16>
-__device__ void bwd_kv_mma_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
-                                uint8_t *sQ, uint8_t *sDO, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+__device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
+                                  uint8_t *sQ, uint8_t *sDO, uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdKVCfg<D>;
     constexpr uint32_t kIdescS = make_idesc(C::BN, C::BM, kFP16, false);  // M = keys, N = query rows
-    constexpr uint32_t kIdescG = make_idesc(C::BN, D, kFP16, true);       // dV, dK: N = d, B MN-major
     const bool leader = ptx::lane_id() == 0;
     const uint64_t dk_desc = smem_desc(ptx::smem_addr(sK), 16);
     const uint64_t dv_desc = smem_desc(ptx::smem_addr(sV), 16);
     bool ok = un.steps == 0 || wait_warp(bar_addr(bars, C::B_KVFULL), 0, ctl, 22);
-    for (int t = 0; ok && t <= un.steps; ++t) {
-        if (t < un.steps) {
-            const int slot = t % C::ST;
-            if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 23)) {
-                ok = false;
-                break;
-            }
-            // the compute warps have read S^T and dP^T of step t-1
-            if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 24)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            if (leader) {
-                const uint64_t qd = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), 16);
-                const uint64_t od = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), 16);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(tmem + C::S_COL, dk_desc + kmajor_step(kk, C::KV_BOX),
-                                qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(tmem + C::DP_COL, dv_desc + kmajor_step(kk, C::KV_BOX),
-                                od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
-                ptx::mma_commit(bar_addr(bars, C::B_SFULL));
-            }
-            __syncwarp();
+    for (int t = 0; ok && t < un.steps; ++t) {
+        const int slot = t % C::ST;
+        if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 23)) {
+            ok = false;
+            break;
         }
-        if (t >= 1) {
-            const int tp = t - 1, slot = tp % C::ST;
-            if (!wait_warp(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 25)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            if (leader) {
-                // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
-                // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
-                const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), C::Q_BOX);
-                const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), C::Q_BOX);
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)
-                    ptx::mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
-                                kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < C::BM / 16; ++kk)
-                    ptx::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + (uint32_t)((kk * 2048) >> 4),
-                                kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(bar_addr(bars, C::B_PFREE));
-                ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
-                if (tp + 1 == un.steps) ptx::mma_commit(bar_addr(bars, C::B_DONE));
-            }
-            __syncwarp();
+        // the compute warps have read S^T and dP^T of step t-1
+        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 24)) {
+            ok = false;
+            break;
         }
+        ptx::tc_fence_after();
+        if (leader) {
+            const uint64_t qd = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), 16);
+            const uint64_t od = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), 16);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::mma_ss(tmem + C::S_COL, dk_desc + kmajor_step(kk, C::KV_BOX),
+                            qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::mma_ss(tmem + C::DP_COL, dv_desc + kmajor_step(kk, C::KV_BOX),
+                            od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
+        }
+        __syncwarp();
     }
     if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
     __syncwarp();
     wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+template <int D, bool kFP16>
+__device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t *sQ, uint8_t *sDO,
+                                  uint32_t bars, uint32_t tmem, Ctl *ctl) {
+    using C = BwdKVCfg<D>;
+    constexpr uint32_t kIdescG = make_idesc(C::BN, D, kFP16, true);  // dV, dK: N = d, B MN-major
+    const bool leader = ptx::lane_id() == 0;
+    bool ok = true;
+    for (int t = 0; ok && t < un.steps; ++t) {
+        const int slot = t % C::ST;
+        if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 30) ||
+            !wait_warp(bar_addr(bars, C::B_PFULL), t & 1, ctl, 25)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        if (leader) {
+            // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
+            // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
+            const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), C::Q_BOX);
+            const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), C::Q_BOX);
+#pragma unroll
+            for (int kk = 0; kk < C::BM / 16; ++kk)
+                ptx::mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
+                            kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < C::BM / 16; ++kk)
+                ptx::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + (uint32_t)((kk * 2048) >> 4),
+                            kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+            ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
+            if (t + 1 == un.steps) ptx::mma_commit(bar_addr(bars, C::B_DONE));
+        }
+        __syncwarp();
+    }
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN + 1));
+    __syncwarp();
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
 }
 
 template <int D, bool kFP16>
@@ -410,23 +427,32 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
         const float4 *D4 =
             reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4) + h * (NC / 4);
         uint32_t pw[NC / 2], dsw[NC / 2];
+        const uint64_t c2 = ptx::f32x2(c, c);
 #pragma unroll
         for (int q = 0; q < NC / 4; ++q) {
             const float4 l = L4[q], dl = D4[q];
-            const float lv[4] = {l.x, l.y, l.z, l.w}, dv[4] = {dl.x, dl.y, dl.z, dl.w};
-            float pv[4], dsv[4];
+            float x0, x1, x2, x3, g0, g1, g2, g3;
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q]), __uint_as_float(s[4 * q + 1])),
+                                             c2, ptx::f32x2(-l.x, -l.y)), x0, x1);
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q + 2]), __uint_as_float(s[4 * q + 3])),
+                                             c2, ptx::f32x2(-l.z, -l.w)), x2, x3);
+            float pv[4] = {ptx::ex2_approx(x0), ptx::ex2_approx(x1), ptx::ex2_approx(x2), ptx::ex2_approx(x3)};
+            if (masked) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int col = 4 * q + e;
-                float pe = ptx::ex2_approx(fmaf(__uint_as_float(s[col]), c, -lv[e]));
-                if (masked) pe = (col >= lo && col < hi) ? pe : 0.f;
-                pv[e] = pe;
-                dsv[e] = pe * (__uint_as_float(dp[col]) - dv[e]);
+                for (int e = 0; e < 4; ++e) pv[e] = (4 * q + e >= lo && 4 * q + e < hi) ? pv[e] : 0.f;
             }
+            ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q]), __uint_as_float(dp[4 * q + 1])),
+                                             ptx::f32x2(-dl.x, -dl.y)), g0, g1);
+            ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q + 2]), __uint_as_float(dp[4 * q + 3])),
+                                             ptx::f32x2(-dl.z, -dl.w)), g2, g3);
+            float d0, d1, d2, d3;
+            const uint64_t z2 = ptx::f32x2(0.f, 0.f);
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(pv[0], pv[1]), ptx::f32x2(g0, g1), z2), d0, d1);
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(pv[2], pv[3]), ptx::f32x2(g2, g3), z2), d2, d3);
             pw[2 * q] = pack2b<kFP16>(pv[0], pv[1]);
             pw[2 * q + 1] = pack2b<kFP16>(pv[2], pv[3]);
-            dsw[2 * q] = pack2b<kFP16>(dsv[0], dsv[1]);
-            dsw[2 * q + 1] = pack2b<kFP16>(dsv[2], dsv[3]);
+            dsw[2 * q] = pack2b<kFP16>(d0, d1);
+            dsw[2 * q + 1] = pack2b<kFP16>(d2, d3);
         }
         // dV / dK of step t-1 have read the P and dS areas
         if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 28)) {
@@ -498,7 +524,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_KVFULL), 1);
         for (int s = 0; s < C::ST; ++s) {
             ptx::mbar_init(bar_addr(bars, C::B_QFULL + s), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + s), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + s), 2);  // one commit from each issuer
         }
         ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_SFREE), C::NUM_COMPUTE);
@@ -506,6 +532,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();
@@ -530,7 +557,9 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
     if (warp < C::NUM_COMPUTE / 32) {
         bwd_kv_compute_role<D, kFP16>(p, un, sStat, bars, tmem, ctl);
     } else if (warp == C::MMA_WARP) {
-        bwd_kv_mma_role<D, kFP16>(p, un, sK, sV, sQ, sDO, bars, tmem, ctl);
+        bwd_kv_mma_s_role<D, kFP16>(p, un, sK, sV, sQ, sDO, bars, tmem, ctl);
+    } else if (warp == C::MMA_G_WARP) {
+        bwd_kv_mma_g_role<D, kFP16>(p, un, sQ, sDO, bars, tmem, ctl);
     } else {
         bwd_kv_tma_role<D>(p, un, sK, sV, sQ, sDO, sStat, bars, ctl);
     }
