@@ -603,11 +603,16 @@ def run_ours_decode(args, w):
     if not args.no_cpu_baseline:
         import oracle
         qf, kf, vf = inp.f64()
-        nb = max(1, w.B // 8)
-        t0 = time.perf_counter()
-        oracle.attention_paged(qf[:nb], kf, vf, inp.block_table[:nb], inp.seq_lens[:nb], w.scale,
-                               w.mask)
-        dt = time.perf_counter() - t0
+        # grow the sample of requests until it takes about 10 s
+        nb = 1
+        while True:
+            t0 = time.perf_counter()
+            oracle.attention_paged(qf[:nb], kf, vf, inp.block_table[:nb], inp.seq_lens[:nb], w.scale,
+                                   w.mask)
+            dt = time.perf_counter() - t0
+            if dt >= 10.0 or nb >= w.B:
+                break
+            nb = min(w.B, max(nb + 1, int(nb * min(8.0, 10.0 / max(dt, 1e-3)))))
         sub = paged_kv_bytes(w, inp.seq_lens[:nb])
         cpu = {"value": sub / dt / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
                "kind": "oracle",
