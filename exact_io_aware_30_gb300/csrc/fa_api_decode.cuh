@@ -21,7 +21,7 @@ struct DecPlan {
 fa_status check_dec_sizes(int B, int H, int Hkv, int Sq, int d, int block_size, int max_blocks,
                           int num_blocks, int max_seq_len, int mask_kind, int dtype) {
     if (dtype != FA_DTYPE_BF16 && dtype != FA_DTYPE_FP16) return FA_ERR_UNSUPPORTED;
-    if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL) return FA_ERR_UNSUPPORTED;
     if (block_size != 16 && block_size != 32 && block_size != 64 && block_size != 128)
         return FA_ERR_UNSUPPORTED;
@@ -39,7 +39,8 @@ fa_status check_dec_sizes(int B, int H, int Hkv, int Sq, int d, int block_size, 
 // SM are in flight, never more than the longest request has 128-key tiles.
 DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int num_sms) {
     DecPlan pl;
-    const long long tiles = (max_seq_len + 127) / 128;
+    const int bn = d == 256 ? DecCfg<256>::BN : DecCfg<128>::BN;  // keys per tile
+    const long long tiles = (max_seq_len + bn - 1) / bn;
     const long long base = (long long)B * Hkv;
     long long n = (2LL * num_sms + base - 1) / base;
     n = std::max(1LL, std::min(n, tiles));
@@ -52,13 +53,19 @@ DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int n
     return pl;
 }
 
+// Whether each decode kernel's shared-memory limit is set, per device
+// (guarded by g_mutex; d = 64, 128, 256 x bf16, fp16).
+bool g_dec_attr[kMaxDevices][6];
+
 template <int D, bool kFP16>
 fa_status launch_decode(const DecParams &p, void *o, float *lse, DeviceInfo &info, cudaStream_t stream) {
     using C = DecCfg<D>;
     auto kern = fa_decode_kernel<D, kFP16>;
-    const int slot = (D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
+    const int slot = (D == 256 ? 4 : D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
     const int smem = std::max(C::SMEM_BYTES, kBwdMinSmem);  // one CTA (and its 512 TMEM columns) per SM
-    if (set_smem(kern, smem, info.attr_dec[slot]) != FA_OK) return FA_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+    if (set_smem(kern, smem, g_dec_attr[dev][slot]) != FA_OK) return FA_ERR_CUDA;
     const long long grid = (long long)p.B * p.Hkv * p.n_splits;
     kern<<<(unsigned)grid, C::NUM_THREADS, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
@@ -106,11 +113,12 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     }
 
     const bool fp16 = dtype == FA_DTYPE_FP16;
+    const int bn_tile = d == 256 ? DecCfg<256>::BN : DecCfg<128>::BN;
     DecParams p;
     std::memset(&p, 0, sizeof(p));
     if (!make_map(&p.tm_q, q, d, (int)rows, 1, 1, 128, fp16) ||
-        !make_map(&p.tm_k, k_cache, d, block_size, Hkv, num_blocks, block_size, fp16) ||
-        !make_map(&p.tm_v, v_cache, d, block_size, Hkv, num_blocks, block_size, fp16))
+        !make_map(&p.tm_k, k_cache, d, block_size, Hkv, num_blocks, std::min(block_size, bn_tile), fp16) ||
+        !make_map(&p.tm_v, v_cache, d, block_size, Hkv, num_blocks, std::min(block_size, bn_tile), fp16))
         return FA_ERR_CUDA;
     p.block_table = block_table;
     p.seq_lens = seq_lens;
@@ -136,6 +144,9 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     if (d == 64)
         return fp16 ? launch_decode<64, true>(p, o, lse, *info, stream)
                     : launch_decode<64, false>(p, o, lse, *info, stream);
+    if (d == 256)
+        return fp16 ? launch_decode<256, true>(p, o, lse, *info, stream)
+                    : launch_decode<256, false>(p, o, lse, *info, stream);
     return fp16 ? launch_decode<128, true>(p, o, lse, *info, stream)
                 : launch_decode<128, false>(p, o, lse, *info, stream);
 }

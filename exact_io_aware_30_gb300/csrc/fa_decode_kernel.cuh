@@ -56,9 +56,11 @@ struct DecParams {
 
 template <int D>
 struct DecCfg {
-    static constexpr int BN = 128;  // keys per tile
-    static constexpr int KST = 3;
-    static constexpr int VST = 3;
+    // d = 256 takes 64-key tiles, so that two S buffers, its 256-column O and
+    // P fit in tensor memory and two-slot rings in shared memory.
+    static constexpr int BN = (D == 256) ? 64 : 128;  // keys per tile
+    static constexpr int KST = (D == 256) ? 2 : 3;
+    static constexpr int VST = (D == 256) ? 2 : 3;
     static constexpr int Q_BOX = 128 * 128;
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BYTES = 128 * D * 2;
@@ -69,7 +71,7 @@ struct DecCfg {
     static constexpr int NUM_THREADS = 192;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0;    // two S buffers, BN columns each
-    static constexpr uint32_t O_COL = 256;
+    static constexpr uint32_t O_COL = 2 * BN;
     static constexpr uint32_t P_COL = 384;  // BN / 2 columns of 16-bit pairs
     static constexpr int B_QFULL = 0;
     static constexpr int B_KFULL = 1;
@@ -85,7 +87,6 @@ struct DecCfg {
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
-    static_assert(D <= 128, "O accumulator of d columns next to two S buffers");
     static_assert(O_COL + D <= P_COL && P_COL + BN / 2 <= TMEM_COLS, "tensor memory overflow");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
@@ -95,6 +96,7 @@ struct DecUnit {
     int b, kvh, split, L, k_beg, k_end, n;
 };
 
+template <int D>
 __device__ __forceinline__ DecUnit decode_dec_unit(const DecParams &p) {
     DecUnit u;
     u.split = (int)blockIdx.x % p.n_splits;
@@ -104,30 +106,45 @@ __device__ __forceinline__ DecUnit decode_dec_unit(const DecParams &p) {
     // the caller guarantees Sq <= seq_lens[b] <= max_seq_len; clamp anyway so
     // that no index leaves the block table
     u.L = min(max(p.seq_lens[u.b], p.Sq), p.max_seq_len);
-    u.k_beg = u.split * p.tiles_per_split * DecCfg<128>::BN;
-    u.k_end = min(u.k_beg + p.tiles_per_split * DecCfg<128>::BN, u.L);
-    u.n = u.k_end > u.k_beg ? (u.k_end - u.k_beg + DecCfg<128>::BN - 1) / DecCfg<128>::BN : 0;
+    constexpr int BN = DecCfg<D>::BN;
+    u.k_beg = u.split * p.tiles_per_split * BN;
+    u.k_end = min(u.k_beg + p.tiles_per_split * BN, u.L);
+    u.n = u.k_end > u.k_beg ? (u.k_end - u.k_beg + BN - 1) / BN : 0;
     return u;
 }
 
-// Loads key tile t of the unit (128 keys = 128 / bs blocks) of one cache into
-// a ring slot.  Blocks past the request's last one repeat its last block: the
-// bytes still arrive (the barrier counts them) and the keys are masked.
+// Loads key tile t of the unit (BN keys) of one cache into a ring slot, as
+// boxes of min(block_size, BN) rows (a box never crosses a block).  Boxes past
+// the request's last block repeat its last block's first rows: the bytes still
+// arrive (the barrier counts them) and the keys are masked.
 template <int D>
 __device__ __forceinline__ void dec_load_tile(const DecParams &p, const DecUnit &un, const CUtensorMap *tm,
                                               uint32_t dst, uint32_t fb, int t, uint64_t pol) {
     using C = DecCfg<D>;
     ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
-    const int per_tile = C::BN / p.bs;
     const int n_last = (un.L + p.bs - 1) / p.bs - 1;
-    const int n0 = (un.k_beg + t * C::BN) / p.bs;
+    const int key0 = un.k_beg + t * C::BN;
     const int *row = p.block_table + (size_t)un.b * p.max_blocks;
-    for (int blk = 0; blk < per_tile; ++blk) {
-        const int n = min(n0 + blk, n_last);
+    // (with 128-key tiles every supported block size divides the tile)
+    if (C::BN >= 128 || p.bs <= C::BN) {  // whole blocks
+        const int per_tile = C::BN / p.bs;
+        const int n0 = key0 / p.bs;
+        for (int blk = 0; blk < per_tile; ++blk) {
+            const int phys = row[min(n0 + blk, n_last)];
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+                ptx::tma_load_4d(dst + c * C::KV_BOX + blk * p.bs * 128, tm, fb, c * 64, 0, un.kvh, phys, pol);
+        }
+    } else {  // one BN-row box inside a larger block
+        int n = key0 / p.bs, y = key0 % p.bs;
+        if (n > n_last) {
+            n = n_last;
+            y = 0;
+        }
         const int phys = row[n];
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-            ptx::tma_load_4d(dst + c * C::KV_BOX + blk * p.bs * 128, tm, fb, c * 64, 0, un.kvh, phys, pol);
+            ptx::tma_load_4d(dst + c * C::KV_BOX, tm, fb, c * 64, y, un.kvh, phys, pol);
     }
 }
 
@@ -264,8 +281,10 @@ __device__ void dec_softmax_role(const DecParams &p, const DecUnit &un, uint8_t 
         uint32_t s[C::BN];
         ptx::tmem_ld_x32<0>(lane_base + C::S_COL + b * C::BN, s);
         ptx::tmem_ld_x32<32>(lane_base + C::S_COL + b * C::BN + 32, s);
-        ptx::tmem_ld_x32<64>(lane_base + C::S_COL + b * C::BN + 64, s);
-        ptx::tmem_ld_x32<96>(lane_base + C::S_COL + b * C::BN + 96, s);
+        if constexpr (C::BN == 128) {
+            ptx::tmem_ld_x32<64>(lane_base + C::S_COL + b * C::BN + 64, s);
+            ptx::tmem_ld_x32<96>(lane_base + C::S_COL + b * C::BN + 96, s);
+        }
         ptx::tmem_wait_ld();
         ptx::reg_fence<C::BN>(s);
         ptx::tc_fence_before();
@@ -317,7 +336,7 @@ __device__ void dec_softmax_role(const DecParams &p, const DecUnit &un, uint8_t 
         }
         m = m_new;
         ptx::tmem_st_x32<0>(lane_base + C::P_COL, pw);
-        ptx::tmem_st_x32<32>(lane_base + C::P_COL + 32, pw);
+        if constexpr (C::BN == 128) ptx::tmem_st_x32<32>(lane_base + C::P_COL + 32, pw);
         if (t + 1 == un.n && un.k_beg + (t + 1) * C::BN > un.L) {
             // last tile reaches past the request's keys: zero those V rows, so
             // that junk in an unused cache slot (even inf or NaN) meets P = 0
@@ -327,7 +346,7 @@ __device__ void dec_softmax_role(const DecParams &p, const DecUnit &un, uint8_t 
                 ok = false;
                 break;
             }
-            if (k0 + r >= un.L) {
+            if (r < C::BN && k0 + r >= un.L) {  // the tile's rows are its BN keys
                 uint8_t *row = sV + vs * C::TILE_BYTES + r * 128;
 #pragma unroll
                 for (int cc = 0; cc < D / 64; ++cc)
@@ -431,7 +450,7 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const DecUnit un = decode_dec_unit(p);
+    const DecUnit un = decode_dec_unit<D>(p);
 
     if (warp < C::NUM_SOFTMAX / 32) {
         dec_softmax_role<D, kFP16>(p, un, sV, bars, tmem, ctl);
@@ -484,7 +503,9 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int e = 0; e < PER; e += 2) w16[e / 2] = pack2b<kFP16>(acc[e] * inv, acc[e + 1] * inv);
     uint8_t *dst = static_cast<uint8_t *>(o) + ((size_t)row * D + lane * PER) * 2;
-    if constexpr (PER == 4) {
+    if constexpr (PER == 8) {
+        *reinterpret_cast<uint4 *>(dst) = make_uint4(w16[0], w16[1], w16[2], w16[3]);
+    } else if constexpr (PER == 4) {
         *reinterpret_cast<uint2 *>(dst) = make_uint2(w16[0], w16[1]);
     } else {
         *reinterpret_cast<uint32_t *>(dst) = w16[0];

@@ -223,7 +223,7 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *vt, void *o, floa
  *   o, lse       [B, H, Sq, d] 16-bit and [B, H, Sq] fp32 outputs
  *   workspace    at least fa_decode_workspace_query() bytes, 256-byte aligned
  *   H_kv         K/V heads, dividing H; (H / H_kv) * Sq <= 128
- *   d            64 or 128; block_size 16, 32, 64 or 128
+ *   d            64, 128 or 256; block_size 16, 32, 64 or 128
  *   max_seq_len  host bound on seq_lens (it sizes the key ranges)
  *   mask_kind    FA_MASK_NONE (every cached token) or FA_MASK_CAUSAL: row i
  *                sits at position seq_lens[b] - Sq + i and sees tokens up to

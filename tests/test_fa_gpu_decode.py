@@ -72,7 +72,7 @@ def check(inp):
     return stats
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP16])
 @pytest.mark.parametrize("block_size", [16, 32, 64, 128])
 @pytest.mark.parametrize("mask", ["none", "causal"])
@@ -81,7 +81,7 @@ def test_decode_one_row(d, dtype, block_size, mask):
     print(check(inp))
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("H,Hkv,Sq", [(8, 8, 1), (8, 2, 4), (32, 1, 4), (16, 4, 3), (6, 3, 7)])
 def test_decode_groups_and_several_rows(d, H, Hkv, Sq):
     # up to 128 packed rows per K/V head (32 heads x 4 rows on one K/V head)
@@ -105,8 +105,9 @@ def test_decode_lengths_at_block_edges():
         check(inp)
 
 
-def test_decode_junk_in_unused_cache_slots_never_leaks():
-    inp = inputs.custom_paged(3, 4, 4, 2, 128, 16, 333, inputs.BF16, "causal", seed=7)
+@pytest.mark.parametrize("d", [128, 256])
+def test_decode_junk_in_unused_cache_slots_never_leaks(d):
+    inp = inputs.custom_paged(3, 4, 4, 2, d, 16, 333, inputs.BF16, "causal", seed=7)
     o1, l1 = run_gpu(inp)
     kb, vb = inp.k_bits.copy(), inp.v_bits.copy()
     nan = np.uint16(0x7FC0)
@@ -131,10 +132,10 @@ def test_decode_is_deterministic():
 
 
 def test_decode_unsupported_requests_raise():
-    q = torch.zeros(1, 2, 1, 256, dtype=torch.bfloat16, device="cuda")
-    kc = torch.zeros(4, 2, 16, 256, dtype=torch.bfloat16, device="cuda")
     t = torch.zeros(1, 4, dtype=torch.int32, device="cuda")
     ln = torch.ones(1, dtype=torch.int32, device="cuda")
+    q = torch.zeros(1, 2, 1, 96, dtype=torch.bfloat16, device="cuda")
+    kc = torch.zeros(4, 2, 16, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa.FAError) as e:
         fa.decode_paged(q, kc, kc, t, ln, 16)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
