@@ -18,6 +18,19 @@ static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocWsBytes];
 
 namespace {
 
+// Test hook shared by the backward, decode and 8-bit entry points (the
+// forward has its own): FA_DEBUG_STALL_MS=N (1..10000) makes each launch's
+// first compute-warp wait one that nothing completes, with N ms as the limit
+// of every wait, so that the bounded-wait path runs without any fault.
+// Returns the limit in ns, 0 when the hook is off.
+uint64_t debug_stall_ns() {
+    if (const char *e = std::getenv("FA_DEBUG_STALL_MS")) {
+        const long ms = std::strtol(e, nullptr, 10);
+        if (ms > 0 && ms <= 10000) return (uint64_t)ms * 1000000ull;
+    }
+    return 0;
+}
+
 // ---------------------------------------------------------------- backward
 
 size_t bwd_pad_rows(int Sq) {
@@ -142,6 +155,10 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     pkv.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
     pkv.scale = scale;
     pkv.wait_limit_ns = fa::kWaitLimitNs;
+    if (const uint64_t ns = debug_stall_ns()) {
+        pkv.stall_test = 1;
+        pkv.wait_limit_ns = ns;
+    }
     pq = pkv;
     pkv.n_tiles = (Sk + 127) / 128;
     pkv.n_units = B * Hkv * pkv.n_tiles;

@@ -138,6 +138,10 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.tiles_per_split = pl.tiles_per_split;
     p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
     p.wait_limit_ns = fa::kWaitLimitNs;
+    if (const uint64_t ns = debug_stall_ns()) {
+        p.stall_test = 1;
+        p.wait_limit_ns = ns;
+    }
     if (log_enabled())
         std::fprintf(stderr, "[fa] fa_decode_paged d=%d B=%d H=%d Hkv=%d Sq=%d bs=%d max_len=%d splits=%d x %d tiles\n",
                      d, B, H, Hkv, Sq, block_size, max_seq_len, pl.n_splits, pl.tiles_per_split);

@@ -75,6 +75,10 @@ fa_status fp8_impl(const void *q, const void *k, const void *vt, void *o, float 
     p.o_mul = v_descale;  // the weights' factor 2^P_LOG2 cancels in O / l
     p.n_qtiles = (Sq + 127) / 128;
     p.wait_limit_ns = fa::kWaitLimitNs;
+    if (const uint64_t ns = debug_stall_ns()) {
+        p.stall_test = 1;
+        p.wait_limit_ns = ns;
+    }
     const int smem = Fp8Cfg::SMEM_BYTES;
     if (set_smem(fa_fwd_fp8_kernel, smem, info->attr_fp8) != FA_OK) return FA_ERR_CUDA;
     fa_fwd_fp8_kernel<<<(unsigned)units, Fp8Cfg::NUM_THREADS, smem, stream>>>(p);

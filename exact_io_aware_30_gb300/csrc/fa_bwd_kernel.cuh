@@ -60,6 +60,7 @@ struct BwdParams {
     int n_units;       // CTAs of the launch
     int n_tiles;       // dK/dV: key tiles per K/V head; dQ: query tiles per head
     uint64_t wait_limit_ns;
+    int stall_test;    // test only: the compute warps' first wait is on a barrier nothing completes
 };
 
 constexpr int kBwdPadRows = 128;  // workspace rows per head are padded to this multiple
@@ -203,7 +204,8 @@ struct BwdKVCfg {
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_DONE = B_PFREE + 1;
     static constexpr int B_DRAIN = B_DONE + 1;  // [2]: each issuer's MMAs finished
-    static constexpr int NUM_BARS = B_DRAIN + 2;
+    static constexpr int B_NEVER = B_DRAIN + 2;  // no arrivals (the stall test's wait)
+    static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(D <= 128, "dK and dV accumulators need 2 x d tensor-memory columns");
@@ -401,7 +403,8 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
         const int i0 = (un.it_lo + t % un.n_i) * C::BM + h * NC;  // first query row of the columns
         // The statistics arrived with the step's Q tile; S^T and dP^T are ready.
         ok = ok && wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
-        ok = ok && wait_warp(bar_addr(bars, C::B_SFULL), t & 1, ctl, 27);
+        ok = ok && wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL), t & 1,
+                             ctl, 27);
         if (!ok) break;
         ptx::tc_fence_after();
         uint32_t s[NC], dp[NC];
@@ -533,6 +536,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();
@@ -610,7 +614,8 @@ struct BwdQCfg {
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_DONE = B_PFREE + 1;
     static constexpr int B_DRAIN = B_DONE + 1;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_NEVER = B_DRAIN + 1;  // no arrivals (the stall test's wait)
+    static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * Q_BYTES + (KST + VST) * KV_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(D <= 128, "one dQ accumulator of d columns next to S and dP");
@@ -799,7 +804,7 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
         if (p.mask_kind != kMaskNone) hi = min(hi, i - k0 + 1);
         if (p.mask_kind == kMaskWindow) lo = max(0, i - p.window + 1 - k0);
         const bool masked = lo > 0 || hi < NC;
-        if (!wait_warp(bar_addr(bars, C::B_SFULL), t & 1, ctl, 36)) {
+        if (!wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL), t & 1, ctl, 36)) {
             ok = false;
             break;
         }
@@ -889,6 +894,7 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();

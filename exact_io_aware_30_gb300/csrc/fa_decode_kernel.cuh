@@ -52,6 +52,7 @@ struct DecParams {
     int n_splits, tiles_per_split;
     float scale_log2;
     uint64_t wait_limit_ns;
+    int stall_test;          // test only: the softmax's first wait is on a barrier nothing completes
 };
 
 template <int D>
@@ -84,7 +85,8 @@ struct DecCfg {
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_OFINAL = B_PFREE + 1;
     static constexpr int B_DRAIN = B_OFINAL + 1;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_NEVER = B_DRAIN + 1;  // no arrivals (the stall test's wait)
+    static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(O_COL + D <= P_COL && P_COL + BN / 2 <= TMEM_COLS, "tensor memory overflow");
@@ -273,7 +275,8 @@ __device__ void dec_softmax_role(const DecParams &p, const DecUnit &un, uint8_t 
     for (int t = 0; t < un.n; ++t) {
         const uint32_t b = (uint32_t)t & 1u;
         const int k0 = un.k_beg + t * C::BN;
-        if (!wait_warp(bar_addr(bars, C::B_SFULL + (int)b), (t >> 1) & 1, ctl, 48)) {
+        if (!wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL + (int)b), (t >> 1) & 1,
+                       ctl, 48)) {
             ok = false;
             break;
         }
@@ -432,6 +435,7 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();

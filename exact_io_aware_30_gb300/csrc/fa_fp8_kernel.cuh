@@ -46,6 +46,7 @@ struct Fp8Params {
     float o_mul;        // v_descale (the weights' stored factor cancels in O / l)
     int n_qtiles;
     uint64_t wait_limit_ns;
+    int stall_test;     // test only: the softmax's first wait is on a barrier nothing completes
 };
 
 struct Fp8Cfg {
@@ -76,7 +77,8 @@ struct Fp8Cfg {
     static constexpr int B_PFREE = B_PFULL + 1;     // P V done: S's columns are free again
     static constexpr int B_OFINAL = B_PFREE + 1;
     static constexpr int B_DRAIN = B_OFINAL + 1;
-    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int B_NEVER = B_DRAIN + 1;  // no arrivals (the stall test's wait)
+    static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static constexpr float TAU = 4.f;     // log2 of the stale-reference slack
@@ -228,7 +230,7 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
     bool ok = true;
     for (int t = 0; t < un.n; ++t) {
         const int k0 = (un.lo + t) * C::BN;
-        if (!wait_warp(bar_addr(bars, C::B_SFULL), t & 1, ctl, 68)) {
+        if (!wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL), t & 1, ctl, 68)) {
             ok = false;
             break;
         }
@@ -362,6 +364,7 @@ __global__ void __launch_bounds__(Fp8Cfg::NUM_THREADS, 2) fa_fwd_fp8_kernel(cons
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();

@@ -280,8 +280,8 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len);
  * A kernel that times out stops its pipeline and finishes normally (its O
  * and lse are then undefined); the context stays usable.  For testing that
  * path, the environment variable FA_DEBUG_STALL_MS=N (1..10000) makes each
- * launch's first softmax wait one that nothing completes, with a limit of
- * N ms instead of about 2 s.
+ * launch's first softmax (or compute-warp) wait one that nothing completes,
+ * with a limit of N ms instead of about 2 s, in every entry point's kernels.
  */
 fa_status fa_get_device_error(void);
 

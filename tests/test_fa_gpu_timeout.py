@@ -1,7 +1,8 @@
 """Bounded pipeline waits on the GPU: a wait that runs out sets the device
 status word, the kernel winds down without a fault, and the context stays
 usable.  The wait is made to run out with FA_DEBUG_STALL_MS, which points the
-first softmax wait of the launch at a barrier nothing completes."""
+first softmax (or compute-warp) wait of each launch at a barrier nothing
+completes, for the forward, the backward, paged decoding and the 8-bit forward."""
 import time
 
 import numpy as np
@@ -53,3 +54,83 @@ def test_timed_out_wait_is_reported_and_context_recovers(monkeypatch, d):
     lse = lse.cpu().numpy().astype(np.float64)
     assert np.abs(o - o_ref).mean() <= 1e-3
     assert np.abs(lse - lse_ref).max() <= 1e-3
+
+
+def _check_recovers(run, check):
+    """run() under the stall hook must report the timeout within 10 s, and the
+    same call afterwards must be right (check)."""
+    import os
+    assert fa.device_error() == fa.FA_OK
+    os.environ["FA_DEBUG_STALL_MS"] = "50"
+    try:
+        t0 = time.time()
+        run()
+        torch.cuda.synchronize()
+        elapsed = time.time() - t0
+    finally:
+        del os.environ["FA_DEBUG_STALL_MS"]
+    assert fa.device_error() == fa.FA_ERR_DEVICE_TIMEOUT
+    assert fa.device_error() == fa.FA_OK
+    assert elapsed < 10.0
+    out = run()
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    check(out)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_timeout_is_reported_and_context_recovers(d):
+    inp = inputs.custom(1, 2, 300, 300, d, inputs.BF16, "causal", seed=32)
+    q, k, v = (_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    dob = inputs.grad_output(inp.workload)
+    do = _dev(dob)
+    o, lse = fa.forward(q, k, v, scale=inp.workload.scale, mask="causal")
+    torch.cuda.synchronize()
+
+    def run():
+        return fa.backward(q, k, v, o, lse, do, scale=inp.workload.scale, mask="causal")
+
+    def check(grads):
+        qf, kf, vf = inp.f64()
+        refs = oracle.attention_bwd(qf, kf, vf, inputs.bits_to_f64(dob, inputs.BF16),
+                                    inp.workload.scale, "causal")
+        for g, r in zip(grads, refs):
+            err = np.abs(g.float().cpu().numpy().astype(np.float64) - r)
+            assert err.max() <= 2.0 ** -6 * np.abs(r).max() + 2.0 ** -16
+
+    _check_recovers(run, check)
+
+
+def test_decode_timeout_is_reported_and_context_recovers():
+    inp = inputs.custom_paged(3, 4, 2, 1, 128, 16, 400, inputs.BF16, "causal", seed=33)
+    q, kc, vc = (_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    table = torch.from_numpy(inp.block_table).cuda()
+    lens = torch.from_numpy(inp.seq_lens).cuda()
+
+    def run():
+        return fa.decode_paged(q, kc, vc, table, lens, 400, mask="causal")
+
+    def check(out):
+        qf, kf, vf = inp.f64()
+        o_ref, _ = oracle.attention_paged(qf, kf, vf, inp.block_table, inp.seq_lens,
+                                          inp.workload.scale, "causal")
+        assert np.abs(out[0].float().cpu().numpy().astype(np.float64) - o_ref).mean() <= 1e-3
+
+    _check_recovers(run, check)
+
+
+def test_fp8_timeout_is_reported_and_context_recovers():
+    w = inputs.Fp8Workload("t", 1, 2, 2, 300, 304, 128, "causal", seed=34)
+    inp = inputs.generate_fp8(w)
+    q, k, vt = (torch.from_numpy(np.ascontiguousarray(b)).cuda()
+                for b in (inp.q_bits, inp.k_bits, inp.vt_bits))
+
+    def run():
+        return fa.forward_fp8(q, k, vt, inp.q_descale, inp.k_descale, inp.v_descale, mask="causal")
+
+    def check(out):
+        qf, kf, vf = inp.f64()
+        o_ref, _ = oracle.attention(qf, kf, vf, w.scale, "causal")
+        assert np.abs(out[0].float().cpu().numpy().astype(np.float64) - o_ref).mean() <= 1e-2
+
+    _check_recovers(run, check)
