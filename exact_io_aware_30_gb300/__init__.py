@@ -1,4 +1,5 @@
-"""GB300 (sm_103a) fused exact attention forward.
+"""GB300 (sm_103a) fused exact attention: the forward (16-bit, grouped K/V
+heads, 8-bit inputs), its backward, and decoding over a paged K/V cache.
 
 The compute lives in ``libfa.so`` (CUDA, built by ``build.build()``); the
 Python layer in ``fa.py`` only marshals arguments into its C ABI

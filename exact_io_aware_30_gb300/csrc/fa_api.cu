@@ -41,7 +41,7 @@ struct DeviceInfo {
     bool attr_set[6] = {false, false, false, false, false, false};
     bool attr_bwd[8] = {false, false, false, false, false, false, false, false};
     void *noalloc_ws = nullptr;  // device address of g_noalloc_ws in this device's context
-    bool attr_dec[4] = {false, false, false, false};
+    bool attr_dec[6] = {false, false, false, false, false, false};
     bool attr_fp8 = false;
 };
 

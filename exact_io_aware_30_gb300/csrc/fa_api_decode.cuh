@@ -53,19 +53,13 @@ DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int n
     return pl;
 }
 
-// Whether each decode kernel's shared-memory limit is set, per device
-// (guarded by g_mutex; d = 64, 128, 256 x bf16, fp16).
-bool g_dec_attr[kMaxDevices][6];
-
 template <int D, bool kFP16>
 fa_status launch_decode(const DecParams &p, void *o, float *lse, DeviceInfo &info, cudaStream_t stream) {
     using C = DecCfg<D>;
     auto kern = fa_decode_kernel<D, kFP16>;
     const int slot = (D == 256 ? 4 : D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
     const int smem = std::max(C::SMEM_BYTES, kBwdMinSmem);  // one CTA (and its 512 TMEM columns) per SM
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
-    if (set_smem(kern, smem, g_dec_attr[dev][slot]) != FA_OK) return FA_ERR_CUDA;
+    if (set_smem(kern, smem, info.attr_dec[slot]) != FA_OK) return FA_ERR_CUDA;
     const long long grid = (long long)p.B * p.Hkv * p.n_splits;
     kern<<<(unsigned)grid, C::NUM_THREADS, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;

@@ -1,8 +1,9 @@
 """ctypes binding of libfa.so (include/fa.h) -- argument marshalling only.
 
-Every step of the attention forward runs inside the library's CUDA kernel;
-this module checks tensor metadata, allocates outputs with torch and passes
-raw pointers and sizes through the C ABI.  If the library is missing or
+Every step of the attention forward, backward and paged decoding runs inside
+the library's CUDA kernels; this module checks tensor metadata, allocates
+outputs (and workspaces) with torch and passes raw pointers and sizes through
+the C ABI.  If the library is missing or
 refuses a request, it raises: there is no other code path.
 """
 from __future__ import annotations

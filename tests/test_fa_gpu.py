@@ -317,3 +317,9 @@ def test_gqa_full_size_sampled():
     o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
     stats = compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype)
     print(f"{w.name}: {stats}")
+
+
+def test_more_units_than_the_schedule_holds():
+    # 13,000 one-tile units: past the 12,288 a precomputed schedule can carry,
+    # so the kernel falls back to its snake order over the units
+    full_case(260, 50, 100, 100, 64, inputs.BF16, "causal", seed=14)
