@@ -179,50 +179,65 @@ class ClockSampler:
 # CPU baseline: the fp64 oracle on a bounded sample of the workload
 # ----------------------------------------------------------------------------
 
-def cpu_oracle_sample(w, inp=None, target_s: float = 12.0, threads: int | None = None):
-    """Time the oracle (as it stands) on a spread sample of query rows.
+def _oracle_rows(w, n):
+    """n query rows spread evenly over all heads, and their mask-adjusted FLOPs."""
+    total = w.B * w.H * w.Sq
+    idx = np.linspace(0, total - 1, num=min(n, total)).astype(np.int64)
+    i = idx % w.Sq
+    if w.mask == "none":
+        vis = np.full(i.shape, w.Sk)
+    elif w.mask == "causal":
+        vis = np.minimum(i + 1, w.Sk)
+    else:
+        vis = np.clip(np.minimum(i, w.Sk - 1) - np.maximum(0, i - w.window + 1) + 1, 0, None)
+    return idx, 4.0 * w.d * float(vis.sum())
 
-    Returns (TFLOP/s, cores, description).  The sample is grown from a small
-    calibration run so that the timed call takes about target_s seconds.
-    """
+
+def calibrate_oracle_rows(w, f64, target_s: float) -> int:
+    """Number of spread query rows the oracle handles in about target_s s
+    (f64: the workload's q, k, v as float64)."""
+    import oracle
+    qf, kf, vf = f64
+    total = w.B * w.H * w.Sq
+    n, dt = 16, 0.0
+    while True:
+        rows, _ = _oracle_rows(w, n)
+        t0 = time.perf_counter()
+        oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= min(0.25, target_s) or n >= total:
+            break
+        n *= 4
+    return int(min(total, max(16, n * target_s / max(dt, 1e-6))))
+
+
+def time_oracle_rows(w, f64, n: int):
+    """One timed oracle call on n spread rows: (TFLOP/s, seconds, description)."""
+    import oracle
+    qf, kf, vf = f64
+    rows, fl = _oracle_rows(w, n)
+    t0 = time.perf_counter()
+    oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
+    dt = time.perf_counter() - t0
+    desc = (f"{len(rows)} of {w.B * w.H * w.Sq} query rows (evenly spaced over all heads), "
+            f"{fl / 1e9:.1f} GFLOP mask-adjusted, {dt:.2f} s, fp64 oracle")
+    return fl / dt / 1e12, dt, desc
+
+
+def cpu_oracle_sample(w, inp=None, target_s: float = 12.0, threads: int | None = None):
+    """Time the oracle (as it stands) on a spread sample of query rows sized
+    to take about target_s seconds.  Returns (TFLOP/s, cores, description,
+    seconds)."""
     import oracle
     if threads:
         oracle.set_threads(threads)
     cores = oracle.max_threads()
     if inp is None:
         inp = inputs.generate(w)
-    qf, kf, vf = inp.f64()
-    BH, Sq = w.B * w.H, w.Sq
-    total = BH * Sq
-
-    def rows_and_flops(n):
-        idx = np.linspace(0, total - 1, num=min(n, total)).astype(np.int64)
-        i = idx % Sq
-        if w.mask == "none":
-            vis = np.full(i.shape, w.Sk)
-        elif w.mask == "causal":
-            vis = np.minimum(i + 1, w.Sk)
-        else:
-            vis = np.clip(np.minimum(i, w.Sk - 1) - np.maximum(0, i - w.window + 1) + 1, 0, None)
-        return idx, 4.0 * w.d * float(vis.sum())
-
-    n = 64
-    while True:
-        rows, fl = rows_and_flops(n)
-        t0 = time.perf_counter()
-        oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
-        dt = time.perf_counter() - t0
-        if dt >= 0.5 or n >= total:
-            break
-        n *= 4
-    n_final = int(min(total, max(64, n * target_s / max(dt, 1e-6))))
-    rows, fl = rows_and_flops(n_final)
-    t0 = time.perf_counter()
-    oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
-    dt = time.perf_counter() - t0
-    desc = (f"{len(rows)} of {total} query rows (evenly spaced over all heads), "
-            f"{fl / 1e9:.1f} GFLOP mask-adjusted, {dt:.1f} s, fp64 oracle")
-    return fl / dt / 1e12, cores, desc, dt
+    f64 = inp.f64()
+    n = calibrate_oracle_rows(w, f64, target_s)
+    tf, dt, desc = time_oracle_rows(w, f64, n)
+    return tf, cores, desc, dt
 
 
 # ----------------------------------------------------------------------------
@@ -767,15 +782,20 @@ def run_reference(args, w):
     rank, world, _ = dist_env()
     if rank != 0:
         return None
+    import oracle
     inp = inputs.generate(w)
-    # each step: a bounded sample of the workload, sized so that warm-up plus
-    # the timed steps stay within a few minutes
-    per_step = max(2.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    cores = oracle.max_threads()
+    # each step: one oracle call on a fixed spread sample of the workload's
+    # rows, sized once so that warm-up plus the timed steps take about two
+    # and a half minutes in all
+    per_step = min(20.0, 150.0 / max(1, args.steps + args.warmup))
+    f64 = inp.f64()
+    n = calibrate_oracle_rows(w, f64, per_step)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, inp, target_s=per_step * 0.25)
-    vals, times, desc, cores = [], [], "", 0
+        time_oracle_rows(w, f64, n)
+    vals, times, desc = [], [], ""
     for _ in range(args.steps):
-        tf, cores, desc, dt = cpu_oracle_sample(w, inp, target_s=per_step)
+        tf, dt, desc = time_oracle_rows(w, f64, n)
         vals.append(tf)
         times.append(dt)
     value = float(np.mean(vals))
