@@ -39,7 +39,7 @@ struct DeviceInfo {
     int num_sms = 0;
     int l2_bytes = 0;
     bool attr_set[6] = {false, false, false, false, false, false};
-    bool attr_bwd[8] = {false, false, false, false, false, false, false, false};
+    bool attr_bwd[12] = {};  // dK/dV then dQ kernels, d = 64, 128, 256 x bf16, fp16
     void *noalloc_ws = nullptr;  // device address of g_noalloc_ws in this device's context
     bool attr_dec[6] = {false, false, false, false, false, false};
     bool attr_fp8 = false;

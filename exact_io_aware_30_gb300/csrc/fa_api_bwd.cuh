@@ -49,8 +49,7 @@ fa_status check_bwd_sizes(int B, int H, int Hkv, int Sq, int Sk, int d, int mask
     fa_status st = check_sizes(B, H, Sq, Sk, d, mask_kind, window, dtype);
     if (st != FA_OK) return st;
     if (Hkv < 1 || H % Hkv != 0) return FA_ERR_INVALID_ARG;
-    if (d > 128) return FA_ERR_UNSUPPORTED;  // dK and dV accumulators: 2 x d tensor-memory columns
-    const long long kv_units = (long long)B * Hkv * (((long long)Sk + 127) / 128);
+    const long long kv_units = (long long)B * Hkv * (((long long)Sk + 127) / 128) * (d > 128 ? 2 : 1);
     if (kv_units > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     return FA_OK;
 }
@@ -58,7 +57,7 @@ fa_status check_bwd_sizes(int B, int H, int Hkv, int Sq, int Sk, int d, int mask
 template <int D, bool kFP16>
 fa_status launch_bwd(const BwdParams &pkv, const BwdParams &pq, const void *o, const void *dout,
                      const float *lse, DeviceInfo &info, cudaStream_t stream) {
-    const int slot = (D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
+    const int slot = (D == 256 ? 4 : D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
     const long long rows = (long long)pq.B * pq.H * pq.Sq_pad;
     constexpr int RPB = 256 / (D / 8);
     fa_bwd_prep_kernel<D, kFP16><<<(unsigned)((rows + RPB - 1) / RPB), 256, 0, stream>>>(
@@ -75,7 +74,7 @@ fa_status launch_bwd(const BwdParams &pkv, const BwdParams &pq, const void *o, c
 
     auto kq = fa_bwd_dq_kernel<D, kFP16>;
     const int q_smem = std::max(BwdQCfg<D>::SMEM_BYTES, kBwdMinSmem);
-    if (set_smem(kq, q_smem, info.attr_bwd[4 + slot]) != FA_OK) return FA_ERR_CUDA;
+    if (set_smem(kq, q_smem, info.attr_bwd[6 + slot]) != FA_OK) return FA_ERR_CUDA;
     kq<<<pq.n_units, BwdQCfg<D>::NUM_THREADS, q_smem, stream>>>(pq);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
@@ -161,11 +160,12 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     }
     pq = pkv;
     pkv.n_tiles = (Sk + 127) / 128;
-    pkv.n_units = B * Hkv * pkv.n_tiles;
+    pkv.n_units = B * Hkv * pkv.n_tiles * (d > 128 ? 2 : 1);  // d = 256: two CTAs per key tile
+    const int q_bn = d == 256 ? BwdQCfg<256>::BN : BwdQCfg<128>::BN;
     if (!make_map(&pq.tm_q, q, d, Sq, H, B, BwdQCfg<128>::BM, fp16) ||
         !make_map(&pq.tm_do, dout, d, Sq, H, B, BwdQCfg<128>::BM, fp16) ||
-        !make_map(&pq.tm_k, k, d, Sk, Hkv, B, BwdQCfg<128>::BN, fp16) ||
-        !make_map(&pq.tm_v, v, d, Sk, Hkv, B, BwdQCfg<128>::BN, fp16))
+        !make_map(&pq.tm_k, k, d, Sk, Hkv, B, q_bn, fp16) ||
+        !make_map(&pq.tm_v, v, d, Sk, Hkv, B, q_bn, fp16))
         return FA_ERR_CUDA;
     pq.n_tiles = (Sq + 127) / 128;
     pq.n_units = B * H * pq.n_tiles;
@@ -180,6 +180,9 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
         case 128:
             return fp16 ? launch_bwd<128, true>(pkv, pq, o, dout, lse, *info, stream)
                         : launch_bwd<128, false>(pkv, pq, o, dout, lse, *info, stream);
+        case 256:
+            return fp16 ? launch_bwd<256, true>(pkv, pq, o, dout, lse, *info, stream)
+                        : launch_bwd<256, false>(pkv, pq, o, dout, lse, *info, stream);
         default:
             return FA_ERR_UNSUPPORTED;
     }

@@ -167,7 +167,13 @@ template <int D>
 struct BwdKVCfg {
     static constexpr int BM = 64;    // query rows per step (N of S^T, K of dV / dK)
     static constexpr int BN = 128;   // keys per CTA (M of every MMA = TMEM lanes)
-    static constexpr int ST = 3;     // stages of the (Q, dO, statistics) ring
+    // d = 256: the dK and dV accumulators of a 128-key tile would need all 512
+    // tensor-memory columns, so two CTAs share the tile, each accumulating one
+    // 128-column half of dK and dV (both form S^T and dP^T over the whole d).
+    // Its K, V, Q and dO tiles leave room for one Q/dO stage only.
+    static constexpr int DA = (D > 128) ? 128 : D;  // accumulator columns per CTA
+    static constexpr int NH = D / DA;               // CTAs per key tile
+    static constexpr int ST = (D > 128) ? 1 : 3;    // stages of the (Q, dO, statistics) ring
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BOX = BM * 128;
     static constexpr int KV_BYTES = BN * D * 2;
@@ -208,23 +214,27 @@ struct BwdKVCfg {
     static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
-    static_assert(D <= 128, "dK and dV accumulators need 2 x d tensor-memory columns");
-    static_assert(DK_COL + D <= S_COL && DS_COL + BM / 2 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(DK_COL + DA <= S_COL && DS_COL + BM / 2 <= TMEM_COLS, "tensor memory overflow");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
 
 // The rows of the K/V tile of one CTA and the query tiles that see them.
 struct KVUnit {
+    int half;              // which DA-column half of dK and dV this CTA accumulates
     int b, kvh, j0, jend;  // keys [j0, jend)
     int it_lo, n_i;        // query tiles it_lo .. it_lo + n_i of every query head of the group
     int steps;             // kv_group * n_i
 };
 
+template <int D>
 __device__ __forceinline__ KVUnit decode_kv_unit(const BwdParams &p) {
     KVUnit u;
+    constexpr int NH = BwdKVCfg<D>::NH;
     const int n_bk = p.B * p.Hkv;
-    const int jt = (int)blockIdx.x / n_bk;  // key tile: all heads' first tiles first (longest)
-    const int bk = (int)blockIdx.x - jt * n_bk;
+    u.half = (int)blockIdx.x % NH;
+    const int id = (int)blockIdx.x / NH;
+    const int jt = id / n_bk;  // key tile: all heads' first tiles first (longest)
+    const int bk = id - jt * n_bk;
     u.b = bk / p.Hkv;
     u.kvh = bk - u.b * p.Hkv;
     u.j0 = jt * 128;
@@ -350,7 +360,7 @@ template <int D, bool kFP16>
 __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t *sQ, uint8_t *sDO,
                                   uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdKVCfg<D>;
-    constexpr uint32_t kIdescG = make_idesc(C::BN, D, kFP16, true);  // dV, dK: N = d, B MN-major
+    constexpr uint32_t kIdescG = make_idesc(C::BN, C::DA, kFP16, true);  // dV, dK: N = DA, B MN-major
     const bool leader = ptx::lane_id() == 0;
     bool ok = true;
     for (int t = 0; ok && t < un.steps; ++t) {
@@ -364,8 +374,10 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
         if (leader) {
             // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
             // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
-            const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), C::Q_BOX);
-            const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), C::Q_BOX);
+            // this CTA's DA columns start at 64-column box half * DA / 64
+            const uint32_t col0 = (uint32_t)(un.half * (C::DA / 64) * C::Q_BOX);
+            const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES) + col0, C::Q_BOX);
+            const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES) + col0, C::Q_BOX);
 #pragma unroll
             for (int kk = 0; kk < C::BM / 16; ++kk)
                 ptx::mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
@@ -480,10 +492,11 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
         if (!ok || !wait_warp(bar_addr(bars, C::B_DONE), 0, ctl, 29)) return;
         ptx::tc_fence_after();
     }
-    constexpr int HALF = D / C::WG;
+    constexpr int HALF = C::DA / C::WG;  // accumulator columns this warp stores
     const size_t row = ((size_t)un.b * p.Hkv + un.kvh) * (size_t)p.Sk + (size_t)j;
-    uint8_t *dv_row = static_cast<uint8_t *>(p.dv) + row * D * 2 + h * HALF * 2;
-    uint8_t *dk_row = static_cast<uint8_t *>(p.dk) + row * D * 2 + h * HALF * 2;
+    const size_t col = (size_t)un.half * C::DA + (size_t)h * HALF;
+    uint8_t *dv_row = static_cast<uint8_t *>(p.dv) + (row * D + col) * 2;
+    uint8_t *dk_row = static_cast<uint8_t *>(p.dk) + (row * D + col) * 2;
     if (un.steps == 0) {
         if (row_ok) {
             store_zero_row(dv_row, HALF * 2);
@@ -556,7 +569,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const KVUnit un = decode_kv_unit(p);
+    const KVUnit un = decode_kv_unit<D>(p);
 
     if (warp < C::NUM_COMPUTE / 32) {
         bwd_kv_compute_role<D, kFP16>(p, un, sStat, bars, tmem, ctl);
@@ -581,9 +594,11 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
 template <int D>
 struct BwdQCfg {
     static constexpr int BM = 128;                // query rows per CTA = TMEM lanes
-    static constexpr int BN = 128;                // keys per step
-    static constexpr int KST = (D == 64) ? 4 : 3; // K stages (free once dQ of the step ran)
-    static constexpr int VST = (D == 64) ? 3 : 2; // V stages (free once dP of the step ran)
+    // d = 256 takes 64-key steps: its 256-column dQ accumulator then fits in
+    // tensor memory next to S, dP and dS, and its tiles in shared memory.
+    static constexpr int BN = (D == 256) ? 64 : 128;               // keys per step
+    static constexpr int KST = (D == 64) ? 4 : (D == 128) ? 3 : 2;  // K stages (free after dQ)
+    static constexpr int VST = (D == 64) ? 3 : (D == 128) ? 2 : 1;  // V stages (free after dP)
     static constexpr int Q_BOX = BM * 128;
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BYTES = BM * D * 2;
@@ -600,8 +615,8 @@ struct BwdQCfg {
     // dS (16-bit pairs, BN/2 columns).
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t S_COL = 0;
-    static constexpr uint32_t DP_COL = 128;
-    static constexpr uint32_t DQ_COL = 256;
+    static constexpr uint32_t DP_COL = BN;
+    static constexpr uint32_t DQ_COL = 2 * BN;
     static constexpr uint32_t DS_COL = 384;
     static constexpr int B_QFULL = 0;
     static constexpr int B_KFULL = 1;                 // [KST]
@@ -618,7 +633,6 @@ struct BwdQCfg {
     static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * Q_BYTES + (KST + VST) * KV_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
-    static_assert(D <= 128, "one dQ accumulator of d columns next to S and dP");
     static_assert(DQ_COL + D <= DS_COL && DS_COL + BN / 2 <= TMEM_COLS, "tensor memory overflow");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
@@ -628,7 +642,9 @@ struct QUnit {
     int lo, n;  // key tiles lo .. lo + n
 };
 
+template <int D>
 __device__ __forceinline__ QUnit decode_q_unit(const BwdParams &p) {
+    constexpr int BN = BwdQCfg<D>::BN;
     QUnit u;
     const int BH = p.B * p.H;
     const int g = p.n_tiles - 1 - (int)blockIdx.x / BH;  // longest query tiles first
@@ -643,8 +659,8 @@ __device__ __forceinline__ QUnit decode_q_unit(const BwdParams &p) {
     int key_beg = 0;
     if (p.mask_kind == kMaskWindow) key_beg = max(0, u.i0 - p.window + 1);
     if (key_beg < key_end) {
-        u.lo = key_beg / 128;
-        u.n = (key_end + 127) / 128 - u.lo;
+        u.lo = key_beg / BN;
+        u.n = (key_end + BN - 1) / BN - u.lo;
     } else {
         u.lo = 0;
         u.n = 0;
@@ -811,9 +827,11 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
         ptx::tc_fence_after();
         uint32_t s[NC], dp[NC], w[NC / 2];
         ptx::tmem_ld_x32<0>(lane_base + C::S_COL + h * NC, s);
-        ptx::tmem_ld_x32<32>(lane_base + C::S_COL + h * NC + 32, s);
         ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
-        ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + h * NC + 32, dp);
+        if constexpr (NC == 64) {
+            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + h * NC + 32, s);
+            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + h * NC + 32, dp);
+        }
         ptx::tmem_wait_ld();
         ptx::reg_fence<NC>(s);
         ptx::reg_fence<NC>(dp);
@@ -836,7 +854,11 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
             break;
         }
         ptx::tc_fence_after();
-        ptx::tmem_st_x32<0>(lane_base + C::DS_COL + h * (NC / 2), w);
+        if constexpr (NC == 64) {
+            ptx::tmem_st_x32<0>(lane_base + C::DS_COL + h * (NC / 2), w);
+        } else {
+            ptx::tmem_st_x16<0>(lane_base + C::DS_COL + h * (NC / 2), w);
+        }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
@@ -914,7 +936,7 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-    const QUnit un = decode_q_unit(p);
+    const QUnit un = decode_q_unit<D>(p);
 
     if (warp < C::NUM_COMPUTE / 32) {
         bwd_q_compute_role<D, kFP16>(p, un, bars, tmem, ctl);

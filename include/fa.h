@@ -127,9 +127,8 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
  *   workspace   device scratch of at least fa_bwd_workspace_query() bytes,
  *               256-byte aligned; its contents on entry do not matter and on
  *               return are the per-row statistics of this call
- *   d           64 or 128 (256: FA_ERR_UNSUPPORTED -- the dK and dV
- *               accumulators of a 128-key tile need 2 d of the 512 tensor-
- *               memory columns)
+ *   d           64, 128 or 256 (for 256 two CTAs share each 128-key tile,
+ *               each accumulating half of the dK and dV columns)
  *   dtype       FA_DTYPE_BF16 or FA_DTYPE_FP16 for all 16-bit tensors
  *   the rest    as for fa_fwd_gqa
  * All tensors are contiguous and 16-byte aligned (lse 4-byte).  Outputs may

@@ -182,8 +182,8 @@ def _bwd(**kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(d=256), fa.FA_ERR_UNSUPPORTED),         # dK + dV accumulators exceed tensor memory
     (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
     (dict(dtype=3), fa.FA_ERR_UNSUPPORTED),
     (dict(mask_kind=4), fa.FA_ERR_UNSUPPORTED),
     (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),
@@ -209,6 +209,6 @@ def test_bwd_invalid_calls_are_rejected_before_launch(lib, kw, status):
 
 def test_bwd_workspace_query_sizes(lib):
     # rejected sizes report their status and 0 bytes, before any device query
-    assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 256) == (fa.FA_ERR_UNSUPPORTED, 0)
+    assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 96) == (fa.FA_ERR_UNSUPPORTED, 0)
     assert fa.bwd_workspace_query(1, 3, 2, 128, 128, 128) == (fa.FA_ERR_INVALID_ARG, 0)
     assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 128, "window", 0) == (fa.FA_ERR_INVALID_ARG, 0)

@@ -5,12 +5,19 @@ returns dQ, dK, dV; the oracle differentiates the exact attention of the same
 16-bit inputs.  Tolerance (per gradient tensor G, see the design notes): the
 kernel rounds P and dS to the 16-bit input type before the tile products that
 use them and rounds each gradient once at the end, so every element carries a
-few roundings of relative size 2^-9 (bf16) of the terms it sums.  The tests
-ask max |G - G_ref| <= 2^-6 max |G_ref| + 2^-16 and mean |G - G_ref| <= 2^-7
-mean |G_ref| + 2^-16 (the absolute 2^-16 covers tensors whose exact value is
-0, such as dQ with a single key, where delta = dO . O carries the rounding of
-O): a mistake in the chain (a dropped term, a wrong index or operand) gives
-errors of the order of |G| itself.
+few roundings of relative size 2^-9 (bf16) of the terms it sums.  One more
+term reaches dQ and dK: the Jacobian's row term delta_i = dO_i . O_i is
+taken from O as stored (16-bit), and its rounding enters every dS_ij of the
+row with the same sign, so it adds scale * d_delta_i * sum_j P_ij k_j to dQ_i
+(and the like to dK) instead of averaging out; with concentrated attention
+(spiky keys) this reaches about 2^-7 of the mean.  (Measured: against a
+reference that uses the kernel's delta, dQ's mean error is 0.2 % at d = 128
+and 256 with spiky keys; against the exact gradient 0.7-0.8 %.)  The tests
+ask max |G - G_ref| <= 2^-6 max |G_ref| + 2^-16, and mean |G - G_ref| <=
+2^-6 mean |G_ref| + 2^-16 for dQ and dK, 2^-7 for dV, which delta does not
+reach (the absolute 2^-16 covers tensors whose exact value is 0, such as dQ
+with a single key): a mistake in the chain (a dropped term, a wrong index or
+operand) gives errors of the order of |G| itself.
 """
 import numpy as np
 import pytest
@@ -23,7 +30,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 MAX_REL = 2.0 ** -6
-MEAN_REL = 2.0 ** -7
+MEAN_REL = {"dq": 2.0 ** -6, "dk": 2.0 ** -6, "dv": 2.0 ** -7}
 ABS_FLOOR = 2.0 ** -16
 
 
@@ -68,7 +75,7 @@ def compare_grads(got, ref, names=("dq", "dk", "dv")):
                   ref_mean=scale_mean)
         stats[name] = st
         assert err.max() <= MAX_REL * scale_max + ABS_FLOOR, (name, st)
-        assert err.mean() <= MEAN_REL * scale_mean + ABS_FLOOR, (name, st)
+        assert err.mean() <= MEAN_REL[name] * scale_mean + ABS_FLOOR, (name, st)
     return stats
 
 
@@ -87,7 +94,7 @@ SHAPES = [(1, 1), (64, 64), (127, 127), (128, 128), (129, 129), (300, 300), (300
           (173, 300), (700, 700)]
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP16])
 @pytest.mark.parametrize("mask,window", [("none", 0), ("causal", 0), ("window", 1),
                                          ("window", 77), ("window", 300)])
@@ -97,25 +104,25 @@ def test_bwd_parity_small(d, dtype, mask, window):
         print(Sq, Sk, stats)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_many_units_heads_and_batches(d):
     bwd_case(3, 5, 400, 400, d, inputs.BF16, "causal", seed=60 + d)
     bwd_case(2, 4, 333, 517, d, inputs.BF16, "none", seed=61 + d)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("H,Hkv", [(4, 2), (6, 1), (8, 8)])
 def test_bwd_grouped_query_heads(d, H, Hkv):
     bwd_case(2, H, 300, 260, d, inputs.BF16, "causal", seed=70 + H + Hkv, Hkv=Hkv)
     bwd_case(1, H, 200, 333, d, inputs.FP16, "window", 90, seed=71 + H + Hkv, Hkv=Hkv)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_spiky_keys(d):
     bwd_case(1, 2, 600, 600, d, inputs.BF16, "none", seed=80 + d, spiky=True)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bwd_rows_without_keys_get_zero_dq(d):
     # window with Sq > Sk: rows i >= Sk + W - 1 see no key, and keys past the
     # last row's window are seen by nobody
@@ -150,12 +157,17 @@ def test_bwd_empty_query_zeroes_dk_dv():
     assert torch.count_nonzero(dk) == 0 and torch.count_nonzero(dv) == 0
 
 
-def test_bwd_head_dim_256_is_refused():
-    q = torch.zeros(1, 1, 8, 256, dtype=torch.bfloat16, device="cuda")
+def test_bwd_unsupported_head_dim_is_refused():
+    q = torch.zeros(1, 1, 8, 96, dtype=torch.bfloat16, device="cuda")
     lse = torch.zeros(1, 1, 8, dtype=torch.float32, device="cuda")
     with pytest.raises(fa.FAError) as e:
         fa.backward(q, q, q, q, lse, q)
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
+
+
+def test_bwd_d256_keys_seen_by_no_row_get_zero():
+    _, got, _ = bwd_case(1, 2, 100, 300, 256, inputs.BF16, "causal", seed=97)
+    assert np.all(got[1][:, :, 100:] == 0.0) and np.all(got[2][:, :, 100:] == 0.0)
 
 
 BWD_FULL = inputs.Workload("bwd_b1h32_s8192_d128_fp16_causal", 1, 32, 8192, 8192, 128,
