@@ -831,7 +831,9 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=str(DEFAULT_WORKLOAD))
+    ap.add_argument("--workload", default=None,
+                    help="workload name or index (default: the forward's 8k causal d = 128 "
+                         "workload; index 0 of the decode and 8-bit lists)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--heads", type=int, default=0,
                     help="override the head count (smaller profiling case of the same kernel)")
@@ -839,22 +841,23 @@ def main(argv=None):
                     help="override Sq = Sk (sequence-length sweeps of the same kernel)")
     ap.add_argument("--direction", choices=["fwd", "bwd", "decode", "fp8"], default="fwd",
                     help="bwd: time the backward (fa_bwd) on the same workload; decode: time "
-                         "fa_decode_paged on a paged-cache workload (--workload indexes those)")
+                         "fa_decode_paged on a paged-cache workload (--workload indexes those); "
+                         "fp8: fa_fwd_fp8 (--workload indexes the 8-bit workloads)")
     ap.add_argument("--kv-heads", type=int, default=0,
                     help="K/V heads shared by the query heads (grouped-query attention)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")
     if args.direction == "fp8":
-        wf = inputs.FP8_WORKLOADS[0]
+        wf = inputs.FP8_WORKLOADS[int(args.workload or 0)]
         if args.heads:
             import dataclasses
             wf = dataclasses.replace(wf, H=args.heads, Hkv=args.heads, name=f"{wf.name}_h{args.heads}")
         return run_ours_fp8(args, wf)
     if args.direction == "decode":
-        wd = args.workload if args.workload != str(DEFAULT_WORKLOAD) else "0"
-        return run_ours_decode(args, inputs.PAGED_WORKLOADS[int(wd)])
-    wl = int(args.workload) if args.workload.isdigit() else args.workload
+        return run_ours_decode(args, inputs.PAGED_WORKLOADS[int(args.workload or 0)])
+    wl = str(DEFAULT_WORKLOAD) if args.workload is None else args.workload
+    wl = int(wl) if wl.isdigit() else wl
     w = inputs.workload(wl)
     if args.heads or args.seq or args.kv_heads:
         import dataclasses

@@ -42,7 +42,7 @@ struct DeviceInfo {
     bool attr_bwd[12] = {};  // dK/dV then dQ kernels, d = 64, 128, 256 x bf16, fp16
     void *noalloc_ws = nullptr;  // device address of g_noalloc_ws in this device's context
     bool attr_dec[6] = {false, false, false, false, false, false};
-    bool attr_fp8 = false;
+    bool attr_fp8[3] = {false, false, false};  // 8-bit forward, d = 64, 128, 256
 };
 
 std::mutex g_mutex;

@@ -11,8 +11,10 @@ namespace fa {
 namespace {
 
 // 4-D map over a contiguous 8-bit tensor with dims {x, y, z, w} (x
-// contiguous), box {bx, by, 1, 1}, 128-byte swizzle.
+// contiguous), box {bx, by, 1, 1}; rows of bx bytes with the swizzle of that
+// width (128 or 64 bytes).
 bool make_map8(CUtensorMap *m, const void *base, int x, int y, int z, int w, int bx, int by) {
+    if (bx != 128 && bx != 64) return false;
     auto enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[4] = {(cuuint64_t)x, (cuuint64_t)y, (cuuint64_t)z, (cuuint64_t)w};
@@ -20,17 +22,37 @@ bool make_map8(CUtensorMap *m, const void *base, int x, int y, int z, int w, int
     cuuint32_t box[4] = {(cuuint32_t)bx, (cuuint32_t)by, 1, 1};
     cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box,
-                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     bx == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 // ---------------------------------------------------------------- 8-bit forward
 
+template <int D>
+fa_status launch_fp8(Fp8Params &p, const void *q, const void *k, const void *vt, long long units,
+                     DeviceInfo *info, cudaStream_t stream) {
+    using C = typename Fp8Pick<D>::C;
+    // Q and K in row chunks of at most 128 bytes; V^T in boxes of BN keys x d rows
+    if (!make_map8(&p.tm_q, q, D, p.Sq, p.H, p.B, C::CHUNK, 128) ||
+        !make_map8(&p.tm_k, k, D, p.Sk, p.Hkv, p.B, C::CHUNK, C::BN) ||
+        !make_map8(&p.tm_vt, vt, p.Sk, D, p.Hkv, p.B, C::BN, D))
+        return FA_ERR_CUDA;
+    const int slot = D == 64 ? 0 : D == 128 ? 1 : 2;
+    // Request enough shared memory that no more CTAs share an SM than their
+    // tensor-memory allocations fit (two of 256 columns, or one of 512).
+    const int smem = C::SMEM_BYTES > 80 * 1024 ? C::SMEM_BYTES : 80 * 1024;
+    if (set_smem(fa_fwd_fp8_kernel<C>, smem, info->attr_fp8[slot]) != FA_OK) return FA_ERR_CUDA;
+    fa_fwd_fp8_kernel<C><<<(unsigned)units, C::NUM_THREADS, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
 fa_status fp8_impl(const void *q, const void *k, const void *vt, void *o, float *lse, int B, int H,
                    int Hkv, int Sq, int Sk, int d, float scale, float q_descale, float k_descale,
                    float v_descale, int mask_kind, int window, cudaStream_t stream) {
-    if (d != 128) return FA_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
     if (mask_kind != FA_MASK_NONE && mask_kind != FA_MASK_CAUSAL && mask_kind != FA_MASK_SLIDING_WINDOW)
         return FA_ERR_UNSUPPORTED;
     if (B < 1 || H < 1 || Hkv < 1 || H % Hkv != 0 || Sk < 1 || Sq < 0) return FA_ERR_INVALID_ARG;
@@ -58,9 +80,6 @@ fa_status fp8_impl(const void *q, const void *k, const void *vt, void *o, float 
     if (st != FA_OK) return st;
     Fp8Params p;
     std::memset(&p, 0, sizeof(p));
-    if (!make_map8(&p.tm_q, q, d, Sq, H, B, d, 128) || !make_map8(&p.tm_k, k, d, Sk, Hkv, B, d, 128) ||
-        !make_map8(&p.tm_vt, vt, Sk, d, Hkv, B, 128, d))
-        return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;
     p.B = B;
@@ -79,11 +98,9 @@ fa_status fp8_impl(const void *q, const void *k, const void *vt, void *o, float 
         p.stall_test = 1;
         p.wait_limit_ns = ns;
     }
-    const int smem = Fp8Cfg::SMEM_BYTES;
-    if (set_smem(fa_fwd_fp8_kernel, smem, info->attr_fp8) != FA_OK) return FA_ERR_CUDA;
-    fa_fwd_fp8_kernel<<<(unsigned)units, Fp8Cfg::NUM_THREADS, smem, stream>>>(p);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-    return FA_OK;
+    if (d == 64) return launch_fp8<64>(p, q, k, vt, units, info, stream);
+    if (d == 128) return launch_fp8<128>(p, q, k, vt, units, info, stream);
+    return launch_fp8<256>(p, q, k, vt, units, info, stream);
 }
 
 

@@ -351,7 +351,10 @@ def generate_fp8(w: Fp8Workload) -> Fp8Inputs:
     return Fp8Inputs(w, qb, kb, vt, qs, ks, vs)
 
 
-# The 8k-token, 32-head causal shape in 8 bits.
+# The 8k-token causal shape in 8 bits; heads x d fixed at 4096 across the
+# three head dimensions, so the three do the same number of flops.
 FP8_WORKLOADS = [
     Fp8Workload("fp8_b1h32_s8192_d128_causal", 1, 32, 32, 8192, 8192, 128, "causal", seed=3001),
+    Fp8Workload("fp8_b1h64_s8192_d64_causal", 1, 64, 64, 8192, 8192, 64, "causal", seed=3002),
+    Fp8Workload("fp8_b1h16_s8192_d256_causal", 1, 16, 16, 8192, 8192, 256, "causal", seed=3003),
 ]

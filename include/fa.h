@@ -180,8 +180,8 @@ fa_status fa_bwd_workspace_query(int B, int H, int H_kv, int Sq, int Sk, int d, 
  * as a later variant).  Q, K and V are e4m3 codes with one dequantisation
  * factor per tensor (value = code x descale); S = Q K^T and P V run on the
  * 8-bit tensor path with fp32 accumulation, the running max, sum and
- * rescaling are those of fa_fwd, P is rounded to e4m3 (scaled by 256) before
- * P V, O is written as bf16 and lse (natural log of the scaled row sums) as
+ * rescaling are those of fa_fwd, P is rounded to e4m3 (weights of at most
+ * 2^4, stored times 2^4) before P V, O is written as bf16 and lse (natural log of the scaled row sums) as
  * fp32.  Exact up to the rounding of P: each output element differs from the
  * exact attention of the dequantised inputs by at most about 2^-4 of
  * sum_j P_ij |v_jc|, plus its bf16 rounding.
@@ -190,7 +190,7 @@ fa_status fa_bwd_workspace_query(int B, int H, int H_kv, int Sq, int Sk, int d, 
  *   vt   V transposed, [B, H_kv, d, Sk] e4m3 (both tile products then read
  *        K-major operands); Sk a multiple of 16 (16-byte rows)
  *   o    [B, H, Sq, d] bf16; lse [B, H, Sq] fp32
- *   d    128 (else FA_ERR_UNSUPPORTED)
+ *   d    64, 128 or 256 (else FA_ERR_UNSUPPORTED)
  *   scale, q_descale, k_descale, v_descale: finite; descales > 0
  *   the rest as for fa_fwd_gqa (masks, window, H_kv grouping, errors)
  */

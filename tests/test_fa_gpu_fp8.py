@@ -88,21 +88,39 @@ SHAPES = [(1, 16), (7, 32), (127, 128), (128, 128), (129, 144), (300, 304), (300
           (173, 304), (700, 704)]
 
 
+DIMS = [64, 128, 256]
+
+
+@pytest.mark.parametrize("d", DIMS)
 @pytest.mark.parametrize("mask,window", [("none", 0), ("causal", 0), ("window", 1), ("window", 77)])
-def test_fp8_parity_small(mask, window):
+def test_fp8_parity_small(mask, window, d):
     for i, (Sq, Sk) in enumerate(SHAPES):
-        w = inputs.Fp8Workload("t", 1, 2, 2, Sq, Sk, 128, mask, window, seed=40 + i)
+        w = inputs.Fp8Workload("t", 1, 2, 2, Sq, Sk, d, mask, window, seed=40 + i + d)
         print(Sq, Sk, check(inputs.generate_fp8(w)))
 
 
+@pytest.mark.parametrize("d", DIMS)
 @pytest.mark.parametrize("H,Hkv", [(4, 4), (8, 2), (6, 1)])
-def test_fp8_heads_batches_and_groups(H, Hkv):
-    w = inputs.Fp8Workload("t", 2, H, Hkv, 400, 512, 128, "causal", seed=50 + H + Hkv)
+def test_fp8_heads_batches_and_groups(H, Hkv, d):
+    w = inputs.Fp8Workload("t", 2, H, Hkv, 400, 512, d, "causal", seed=50 + H + Hkv + d)
     print(check(inputs.generate_fp8(w)))
 
 
-def test_fp8_rows_without_keys():
-    w = inputs.Fp8Workload("t", 1, 2, 2, 300, 48, 128, "window", 17, seed=55)
+@pytest.mark.parametrize("d", [64, 256])
+def test_fp8_long_rows(d):
+    """Many key tiles per row (both S buffers cycle many times at d = 256),
+    with large logits so that the reference max moves and O is rescaled."""
+    w = inputs.Fp8Workload("t", 1, 2, 1, 1100, 2048, d, "none", seed=70 + d)
+    inp = inputs.generate_fp8(w)
+    print(check(inp))
+    hot = inputs.Fp8Inputs(w, inp.q_bits, inp.k_bits, inp.vt_bits, inp.q_descale * 4.0,
+                           inp.k_descale * 4.0, inp.v_descale)
+    print(check(hot))
+
+
+@pytest.mark.parametrize("d", DIMS)
+def test_fp8_rows_without_keys(d):
+    w = inputs.Fp8Workload("t", 1, 2, 2, 300, 48, d, "window", 17, seed=55)
     inp = inputs.generate_fp8(w)
     check(inp)
     o, lse = run_gpu(inp)
@@ -111,12 +129,12 @@ def test_fp8_rows_without_keys():
 
 
 def test_fp8_refusals():
-    q = torch.zeros(1, 1, 8, 64, dtype=torch.uint8, device="cuda")
-    vt = torch.zeros(1, 1, 64, 16, dtype=torch.uint8, device="cuda")
-    k = torch.zeros(1, 1, 16, 64, dtype=torch.uint8, device="cuda")
+    q = torch.zeros(1, 1, 8, 96, dtype=torch.uint8, device="cuda")
+    vt = torch.zeros(1, 1, 96, 16, dtype=torch.uint8, device="cuda")
+    k = torch.zeros(1, 1, 16, 96, dtype=torch.uint8, device="cuda")
     with pytest.raises(fa.FAError) as e:
         fa.forward_fp8(q, k, vt, 1.0, 1.0, 1.0)
-    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # d = 64
+    assert e.value.status == fa.FA_ERR_UNSUPPORTED  # d = 96
     q = torch.zeros(1, 1, 8, 128, dtype=torch.uint8, device="cuda")
     k = torch.zeros(1, 1, 20, 128, dtype=torch.uint8, device="cuda")
     vt = torch.zeros(1, 1, 128, 20, dtype=torch.uint8, device="cuda")
@@ -130,8 +148,9 @@ def test_fp8_refusals():
     assert e.value.status == fa.FA_ERR_INVALID_ARG  # descale must be positive
 
 
-def test_fp8_full_size_sampled():
-    w = inputs.FP8_WORKLOADS[0]
+@pytest.mark.parametrize("wi", range(len(inputs.FP8_WORKLOADS)))
+def test_fp8_full_size_sampled(wi):
+    w = inputs.FP8_WORKLOADS[wi]
     inp = inputs.generate_fp8(w)
     rng = np.random.default_rng(33)
     rows = np.unique(np.concatenate([rng.integers(0, w.B * w.H * w.Sq, 256),
