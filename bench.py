@@ -634,6 +634,11 @@ def run_ours_decode(args, w):
                "sample": f"{nb} of {w.B} requests, {sub / 1e6:.0f} MB of K/V, {dt:.1f} s, fp64 oracle"}
     h2d = q_h.numel() * 2 + table_h.numel() * 4 + lens_h.numel() * 4
     d2h = o_h.numel() * 2 + l_h.numel() * 4
+    # the library's choice: CUDA cores for at most 2 rows per K/V head, else tensor cores
+    forced = os.environ.get("FA_DECODE_KERNEL", "")
+    rows = (w.H // w.Hkv) * w.Sq
+    kname = {"mma": "fa_decode_kernel", "gemv": "fa_decode_gemv_kernel"}.get(
+        forced, "fa_decode_gemv_kernel" if rows <= 2 else "fa_decode_kernel")
     result = {
         "metric": "paged decode K/V read bandwidth (GB/s of cached K and V the step must read)",
         "value": gbs,
@@ -655,7 +660,7 @@ def run_ours_decode(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_src} HBM copy bandwidth",
                      "traffic": None, "algorithmic_bytes": alg_bytes,
-                     "kernel": "fa_decode_paged call (key-range kernel + combine)",
+                     "kernel": f"fa_decode_paged call ({kname} + combine)",
                      "kernel_ms_median": float(np.median(call_ms)),
                      "kernel_ms_min": float(np.min(call_ms))},
         "cpu_baseline": cpu,
@@ -855,7 +860,13 @@ def main(argv=None):
             wf = dataclasses.replace(wf, H=args.heads, Hkv=args.heads, name=f"{wf.name}_h{args.heads}")
         return run_ours_fp8(args, wf)
     if args.direction == "decode":
-        return run_ours_decode(args, inputs.PAGED_WORKLOADS[int(args.workload or 0)])
+        wp = inputs.PAGED_WORKLOADS[int(args.workload or 0)]
+        if args.kv_heads:
+            if args.kv_heads < 1 or wp.H % args.kv_heads:
+                ap.error("--kv-heads must divide the head count")
+            import dataclasses
+            wp = dataclasses.replace(wp, Hkv=args.kv_heads, name=f"{wp.name}_kv{args.kv_heads}")
+        return run_ours_decode(args, wp)
     wl = str(DEFAULT_WORKLOAD) if args.workload is None else args.workload
     wl = int(wl) if wl.isdigit() else wl
     w = inputs.workload(wl)

@@ -43,6 +43,7 @@ struct DeviceInfo {
     void *noalloc_ws = nullptr;  // device address of g_noalloc_ws in this device's context
     bool attr_dec[6] = {false, false, false, false, false, false};
     bool attr_fp8[3] = {false, false, false};  // 8-bit forward, d = 64, 128, 256
+    bool attr_gemv[12] = {};  // few-row decode: d = 64, 128, 256 x bf16, fp16 x 1, 2 rows
 };
 
 std::mutex g_mutex;

@@ -5,7 +5,7 @@
 // of these entry points.
 #pragma once
 
-#include "fa_decode_kernel.cuh"
+#include "fa_decode_gemv_kernel.cuh"
 
 namespace fa {
 
@@ -14,9 +14,31 @@ namespace {
 // ---------------------------------------------------------------- paged decode
 
 struct DecPlan {
-    int n_splits = 1, tiles_per_split = 1;
+    int n_splits = 1, tiles_per_split = 1, keys_per_split = 0;
     size_t part_o_bytes = 0, bytes = 0;
 };
+
+// The kernel that serves R rows per K/V head: the CUDA-core one
+// (fa_decode_gemv_kernel) up to 2 rows, where the products are matrix-vector
+// ones and it streams the cache faster, else the tensor-core one
+// (fa_decode_kernel).  FA_DECODE_KERNEL=mma or =gemv in the environment forces
+// one (tests, comparisons); gemv takes at most 2 rows.
+constexpr int kDecMma = 0;
+constexpr int kDecGemv = 1;
+constexpr int kGemvMaxRows = 2;
+
+fa_status decode_path(int R, int *path) {
+    const char *e = std::getenv("FA_DECODE_KERNEL");
+    if (e && std::strcmp(e, "mma") == 0) {
+        *path = kDecMma;
+    } else if (e && std::strcmp(e, "gemv") == 0) {
+        if (R > kGemvMaxRows) return FA_ERR_UNSUPPORTED;
+        *path = kDecGemv;
+    } else {
+        *path = R <= kGemvMaxRows ? kDecGemv : kDecMma;
+    }
+    return FA_OK;
+}
 
 fa_status check_dec_sizes(int B, int H, int Hkv, int Sq, int d, int block_size, int max_blocks,
                           int num_blocks, int max_seq_len, int mask_kind, int dtype) {
@@ -35,17 +57,21 @@ fa_status check_dec_sizes(int B, int H, int Hkv, int Sq, int d, int block_size, 
     return FA_OK;
 }
 
-// Key ranges per (request, K/V head): enough splits that about two CTAs per
-// SM are in flight, never more than the longest request has 128-key tiles.
-DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int num_sms) {
+// Key ranges per (request, K/V head).  Tensor-core kernel (one CTA per SM):
+// enough splits that about two CTAs per SM are in flight, never more than the
+// longest request has 128-key tiles.  CUDA-core kernel (two CTAs per SM):
+// about eight CTAs per SM over the grid, in whole stages of 8192 / d keys.
+DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int num_sms, int path) {
     DecPlan pl;
-    const int bn = d == 256 ? DecCfg<256>::BN : DecCfg<128>::BN;  // keys per tile
+    const int bn = path == kDecGemv ? 8192 / d : d == 256 ? DecCfg<256>::BN : DecCfg<128>::BN;
     const long long tiles = (max_seq_len + bn - 1) / bn;
     const long long base = (long long)B * Hkv;
-    long long n = (2LL * num_sms + base - 1) / base;
+    const long long want = (path == kDecGemv ? 8LL : 2LL) * num_sms;
+    long long n = (want + base - 1) / base;
     n = std::max(1LL, std::min(n, tiles));
     const long long per = (tiles + n - 1) / n;
     pl.tiles_per_split = (int)per;
+    pl.keys_per_split = (int)(per * bn);
     pl.n_splits = (int)((tiles + per - 1) / per);
     const size_t rows = (size_t)B * H * Sq;
     pl.part_o_bytes = ((size_t)pl.n_splits * rows * d * 4 + 255) / 256 * 256;
@@ -70,6 +96,28 @@ fa_status launch_decode(const DecParams &p, void *o, float *lse, DeviceInfo &inf
     return FA_OK;
 }
 
+template <int D, bool kFP16, int RT>
+fa_status launch_gemv_rt(const GemvParams &p, void *o, float *lse, DeviceInfo &info, cudaStream_t stream) {
+    using C = GemvCfg<D>;
+    auto kern = fa_decode_gemv_kernel<D, kFP16, RT>;
+    const int slot = ((D == 256 ? 2 : D == 128 ? 1 : 0) * 2 + (kFP16 ? 1 : 0)) * 2 + (RT - 1);
+    if (set_smem(kern, C::SMEM_BYTES, info.attr_gemv[slot]) != FA_OK) return FA_ERR_CUDA;
+    const long long grid = (long long)p.B * p.Hkv * p.n_splits;
+    kern<<<(unsigned)grid, C::NUM_THREADS, C::SMEM_BYTES, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    const int rows = p.B * p.H * p.Sq;
+    fa_decode_combine_kernel<D, kFP16><<<(rows + 7) / 8, 256, 0, stream>>>(p.part_o, p.part_lse, o, lse,
+                                                                          rows, p.n_splits);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+template <int D, bool kFP16>
+fa_status launch_gemv(const GemvParams &p, void *o, float *lse, DeviceInfo &info, cudaStream_t stream) {
+    if (p.R == 1) return launch_gemv_rt<D, kFP16, 1>(p, o, lse, info, stream);
+    return launch_gemv_rt<D, kFP16, 2>(p, o, lse, info, stream);
+}
+
 fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, const int *block_table,
                       const int *seq_lens, void *o, float *lse, void *workspace, size_t workspace_bytes,
                       int B, int H, int Hkv, int Sq, int d, int block_size, int max_blocks,
@@ -91,7 +139,10 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     DeviceInfo *info = nullptr;
     st = device_info(&dev, &info);
     if (st != FA_OK) return st;
-    const DecPlan pl = plan_decode(B, H, Hkv, Sq, d, max_seq_len, info->num_sms);
+    int path = kDecMma;
+    st = decode_path((H / Hkv) * Sq, &path);
+    if (st != FA_OK) return st;
+    const DecPlan pl = plan_decode(B, H, Hkv, Sq, d, max_seq_len, info->num_sms, path);
     if (workspace_bytes < pl.bytes) return FA_ERR_INVALID_ARG;
     const size_t rows = (size_t)B * H * Sq;
     const size_t qo = rows * d * 2, cache = (size_t)num_blocks * Hkv * block_size * d * 2;
@@ -107,6 +158,48 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     }
 
     const bool fp16 = dtype == FA_DTYPE_FP16;
+    if (log_enabled())
+        std::fprintf(stderr, "[fa] fa_decode_paged %s d=%d B=%d H=%d Hkv=%d Sq=%d bs=%d max_len=%d splits=%d x %d keys\n",
+                     path == kDecGemv ? "gemv" : "mma", d, B, H, Hkv, Sq, block_size, max_seq_len, pl.n_splits,
+                     pl.keys_per_split);
+    if (path == kDecGemv) {
+        GemvParams g;
+        std::memset(&g, 0, sizeof(g));
+        g.q = q;
+        g.k_cache = k_cache;
+        g.v_cache = v_cache;
+        g.block_table = block_table;
+        g.seq_lens = seq_lens;
+        g.part_o = static_cast<float *>(workspace);
+        g.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+        g.B = B;
+        g.H = H;
+        g.Hkv = Hkv;
+        g.kv_group = H / Hkv;
+        g.Sq = Sq;
+        g.R = g.kv_group * Sq;
+        g.bs = block_size;
+        g.max_blocks = max_blocks;
+        g.num_blocks = num_blocks;
+        g.max_seq_len = max_seq_len;
+        g.mask_kind = mask_kind;
+        g.n_splits = pl.n_splits;
+        g.keys_per_split = pl.keys_per_split;
+        g.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
+        g.wait_limit_ns = fa::kWaitLimitNs;
+        if (const uint64_t ns = debug_stall_ns()) {
+            g.stall_test = 1;
+            g.wait_limit_ns = ns;
+        }
+        if (d == 64)
+            return fp16 ? launch_gemv<64, true>(g, o, lse, *info, stream)
+                        : launch_gemv<64, false>(g, o, lse, *info, stream);
+        if (d == 256)
+            return fp16 ? launch_gemv<256, true>(g, o, lse, *info, stream)
+                        : launch_gemv<256, false>(g, o, lse, *info, stream);
+        return fp16 ? launch_gemv<128, true>(g, o, lse, *info, stream)
+                    : launch_gemv<128, false>(g, o, lse, *info, stream);
+    }
     const int bn_tile = d == 256 ? DecCfg<256>::BN : DecCfg<128>::BN;
     DecParams p;
     std::memset(&p, 0, sizeof(p));
@@ -136,9 +229,6 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
         p.stall_test = 1;
         p.wait_limit_ns = ns;
     }
-    if (log_enabled())
-        std::fprintf(stderr, "[fa] fa_decode_paged d=%d B=%d H=%d Hkv=%d Sq=%d bs=%d max_len=%d splits=%d x %d tiles\n",
-                     d, B, H, Hkv, Sq, block_size, max_seq_len, pl.n_splits, pl.tiles_per_split);
     if (d == 64)
         return fp16 ? launch_decode<64, true>(p, o, lse, *info, stream)
                     : launch_decode<64, false>(p, o, lse, *info, stream);
@@ -176,7 +266,10 @@ fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int b
     int dev = 0;
     fa::DeviceInfo *info = nullptr;
     st = fa::device_info(&dev, &info);
-    if (st == FA_OK) *bytes = fa::plan_decode(B, H, H_kv, Sq, d, max_seq_len, info->num_sms).bytes;
+    if (st != FA_OK) return st;
+    int path = fa::kDecMma;
+    st = fa::decode_path((H / H_kv) * Sq, &path);
+    if (st == FA_OK) *bytes = fa::plan_decode(B, H, H_kv, Sq, d, max_seq_len, info->num_sms, path).bytes;
     return st;
 }
 

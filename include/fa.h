@@ -230,7 +230,14 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *vt, void *o, floa
  *   dtype        FA_DTYPE_BF16 or FA_DTYPE_FP16
  * Cache slots past a request's length may hold any values, inf and NaN
  * included: they are hidden and never reach O.  Errors and the device flag
- * are as for fa_fwd; the library allocates nothing.  Two launches.
+ * are as for fa_fwd; the library allocates nothing.  Two launches: the
+ * key-range kernel, then the merge.  With at most 2 rows per K/V head
+ * ((H / H_kv) * Sq <= 2) the key-range kernel runs on the CUDA cores (the
+ * products are matrix-vector ones), else on the tensor cores; the environment
+ * variable FA_DECODE_KERNEL=mma or =gemv forces one (gemv: at most 2 rows,
+ * else FA_ERR_UNSUPPORTED) and must not change between
+ * fa_decode_workspace_query and the call, since the two kernels split the
+ * keys differently.
  */
 fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
                           const int *block_table, const int *seq_lens, void *o, float *lse,

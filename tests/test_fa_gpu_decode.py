@@ -27,6 +27,18 @@ def _lib():
     assert fa.device_error() == fa.FA_OK
 
 
+@pytest.fixture(autouse=True, params=["auto", "mma"])
+def kernel(request, monkeypatch):
+    """Every test runs twice: with the library's own choice of kernel (the
+    CUDA-core one for at most 2 rows per K/V head, else the tensor-core one)
+    and with the tensor-core kernel forced."""
+    if request.param == "auto":
+        monkeypatch.delenv("FA_DECODE_KERNEL", raising=False)
+    else:
+        monkeypatch.setenv("FA_DECODE_KERNEL", request.param)
+    return request.param
+
+
 def _dev16(bits, dtype):
     tdt = torch.bfloat16 if dtype == inputs.BF16 else torch.float16
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(tdt).cuda()
@@ -123,6 +135,38 @@ def test_decode_junk_in_unused_cache_slots_never_leaks(d):
         vb[blk, :, fill:] = inf
     o2, l2 = run_gpu(inp, kb, vb)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("bad", [-1, "past"])
+def test_decode_out_of_range_table_entry_reads_zeros(bad):
+    """A table entry outside [0, num_blocks) inside a request's blocks reads
+    as a block of zeros: the result equals the oracle's on a pool with an
+    all-zero block at that entry."""
+    inp = inputs.custom_paged(3, 4, 2, 1, 128, 16, 300, inputs.BF16, "causal", min_seq_len=200,
+                              seed=12)
+    nb = inp.k_bits.shape[0]
+    table = inp.block_table.copy()
+    table[1, 2] = -1 if bad == -1 else nb + 5
+    w = inp.workload
+    q = _dev16(inp.q_bits, w.dtype)
+    kc, vc = _dev16(inp.k_bits, w.dtype), _dev16(inp.v_bits, w.dtype)
+    o, lse = fa.decode_paged(q, kc, vc, torch.from_numpy(table).cuda(),
+                             torch.from_numpy(inp.seq_lens).cuda(), w.max_seq_len, scale=w.scale,
+                             mask=w.mask)
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+    # the same attention on a valid table: the entry points at an added zero block
+    qf, kf, vf = inp.f64()
+    zeros = np.zeros_like(kf[:1])
+    kz, vz = np.concatenate([kf, zeros]), np.concatenate([vf, zeros])
+    table_ref = inp.block_table.copy()
+    table_ref[1, 2] = nb
+    o_ref, lse_ref = oracle.attention_paged(qf, kz, vz, table_ref, inp.seq_lens, w.scale, w.mask)
+    err = np.abs(o - o_ref)
+    assert np.maximum(err - 0.5 * _ulp(o_ref, w.dtype), 0.0).max() <= MAX_TOL
+    assert err.mean() <= MEAN_TOL and np.abs(lse - lse_ref).max() <= LSE_TOL
 
 
 def test_decode_is_deterministic():

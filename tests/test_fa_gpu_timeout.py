@@ -101,7 +101,9 @@ def test_backward_timeout_is_reported_and_context_recovers(d):
     _check_recovers(run, check)
 
 
-def test_decode_timeout_is_reported_and_context_recovers():
+@pytest.mark.parametrize("kernel", ["gemv", "mma"])
+def test_decode_timeout_is_reported_and_context_recovers(kernel, monkeypatch):
+    monkeypatch.setenv("FA_DECODE_KERNEL", kernel)  # 2 rows per K/V head: either kernel serves
     inp = inputs.custom_paged(3, 4, 2, 1, 128, 16, 400, inputs.BF16, "causal", seed=33)
     q, kc, vc = (_dev(b) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
     table = torch.from_numpy(inp.block_table).cuda()
