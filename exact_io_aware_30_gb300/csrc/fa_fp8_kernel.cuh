@@ -323,11 +323,18 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
             for (int e = 0; e < C::BN; ++e)
                 if (e < lo || e >= hi) s[e] = __float_as_uint(-INFINITY);
         }
-        float smax = __uint_as_float(s[0]);
+        // tile max as four independent chains (the latency of one serial
+        // chain of BN/2 three-way maxima would sit on every tile's path)
+        static_assert(C::BN % 8 == 0, "tile max in groups of eight");
+        float mx[4];
 #pragma unroll
-        for (int e = 1; e + 1 < C::BN; e += 2)
-            smax = ptx::max3(smax, __uint_as_float(s[e]), __uint_as_float(s[e + 1]));
-        smax = fmaxf(smax, __uint_as_float(s[C::BN - 1]));
+        for (int j = 0; j < 4; ++j) mx[j] = fmaxf(__uint_as_float(s[j]), __uint_as_float(s[4 + j]));
+#pragma unroll
+        for (int e = 8; e + 8 <= C::BN; e += 8)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mx[j] = ptx::max3(mx[j], __uint_as_float(s[e + j]), __uint_as_float(s[e + 4 + j]));
+        const float smax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         // Deferred rescaling: the reference max moves only when the tile's max
         // exceeds it by more than 2^4, so weights stay below 2^4 (stored times
         // 2^4: at most 256, inside e4m3's range) and O is rescaled rarely.
@@ -338,7 +345,9 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
         const float alpha = ptx::ex2_approx(m - m_use);  // 1 unless the reference moved
         const float shift = m_use - C::P_LOG2;           // weights carry the factor 2^P_LOG2
         const uint64_t c2 = ptx::f32x2(c, c), n2 = ptx::f32x2(-shift, -shift);
-        uint64_t acc0 = ptx::f32x2(0.f, 0.f), acc1 = acc0;
+        uint64_t acc[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[j] = ptx::f32x2(0.f, 0.f);
         uint32_t pw[C::BN / 4];
 #pragma unroll
         for (int e = 0; e < C::BN; e += 4) {
@@ -349,14 +358,15 @@ __device__ void fp8_softmax_role(const Fp8Params &p, const Fp8Unit &un, uint32_t
                 ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e + 2]), __uint_as_float(s[e + 3])), c2, n2), x2, x3);
             const float p0 = ptx::ex2_approx(x0), p1 = ptx::ex2_approx(x1);
             const float p2 = ptx::ex2_approx(x2), p3 = ptx::ex2_approx(x3);
-            acc0 = ptx::add_f32x2(acc0, ptx::f32x2(p0, p1));
-            acc1 = ptx::add_f32x2(acc1, ptx::f32x2(p2, p3));
+            const int j = (e / 4) & 1;  // four independent accumulator pairs
+            acc[2 * j] = ptx::add_f32x2(acc[2 * j], ptx::f32x2(p0, p1));
+            acc[2 * j + 1] = ptx::add_f32x2(acc[2 * j + 1], ptx::f32x2(p2, p3));
             pw[e / 4] = ptx::pack_e4m3x4(p0, p1, p2, p3);
         }
-        float a0, a1, a2, a3;
-        ptx::unpack_f32x2(acc0, a0, a1);
-        ptx::unpack_f32x2(acc1, a2, a3);
-        l = l * alpha + ((a0 + a1) + (a2 + a3));
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) ptx::unpack_f32x2(acc[j], a[2 * j], a[2 * j + 1]);
+        l = l * alpha + (((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7])));
         if (t >= 1 && __any_sync(0xffffffffu, alpha != 1.f)) {
             // O must hold P V of every earlier tile.  With one S buffer, S of
             // this tile was issued after P V of the previous one had run; with
