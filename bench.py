@@ -86,24 +86,31 @@ def load_peaks():
 FWD_SOURCES = ("fa_api.cu", "fa_fwd_kernel.cuh", "sm103_ptx.cuh")
 
 
-def kernel_source_digest() -> str:
+# The sources the decode kernels (and their launch) are built from: each
+# includes the headers below it.
+DEC_SOURCES = ("fa_api.cu", "fa_api_decode.cuh", "fa_decode_gemv_kernel.cuh", "fa_decode_kernel.cuh",
+               "fa_bwd_kernel.cuh", "fa_fwd_kernel.cuh", "sm103_ptx.cuh")
+
+
+def kernel_source_digest(sources=FWD_SOURCES) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_io_aware_30_gb300", "csrc")
-    for name in FWD_SOURCES:
+    for name in sources:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "fa_fwd_kernel_traffic.md")
+def recorded_traffic(workload_name: str, summary="fa_fwd_kernel_traffic.md", sources=FWD_SOURCES):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    summary (its `traffic <workload> source=<digest> bytes_per_launch=<n>`
+    lines), if it was taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", summary)
     if not os.path.exists(path):
         return None
-    digest = kernel_source_digest()
+    digest = kernel_source_digest(sources)
     pat = re.compile(r"^traffic\s+(\S+)\s+source=(\w+)\s+bytes_per_launch=(\d+)", re.M)
     for m in pat.finditer(open(path).read()):
         if m.group(1) == workload_name and m.group(2) == digest:
@@ -659,7 +666,11 @@ def run_ours_decode(args, w):
                    "l2": "flushed (256 MiB write) before every step", "parallelism": "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": f"{peak_src} HBM copy bandwidth",
-                     "traffic": None, "algorithmic_bytes": alg_bytes,
+                     "traffic": recorded_traffic(
+                         w.name, "fa_decode_gemv_kernel_launches_decode_b128_h40_d128_bs16_ctx2048_fp16.md",
+                         DEC_SOURCES) if kname == "fa_decode_gemv_kernel" else None,
+                     "traffic_kernel": kname,
+                     "algorithmic_bytes": alg_bytes,
                      "kernel": f"fa_decode_paged call ({kname} + combine)",
                      "kernel_ms_median": float(np.median(call_ms)),
                      "kernel_ms_min": float(np.min(call_ms))},

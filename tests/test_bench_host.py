@@ -69,3 +69,19 @@ def test_cpu_baseline_sampler_small():
 def test_recorded_traffic_requires_matching_source(tmp_path, monkeypatch):
     # a stale digest never yields a traffic figure
     assert bench.recorded_traffic("no_such_workload") is None
+
+
+def test_recorded_decode_traffic_is_keyed_to_the_decode_sources():
+    # the committed decode summary carries a traffic line for the one-row
+    # workload; it is read only under the digest of the decode sources
+    name = "decode_b128_h40_d128_bs16_ctx2048_fp16"
+    summary = "fa_decode_gemv_kernel_launches_decode_b128_h40_d128_bs16_ctx2048_fp16.md"
+    got = bench.recorded_traffic(name, summary, bench.DEC_SOURCES)
+    text = open(os.path.join(bench.ROOT, "profiles", summary)).read()
+    recorded = bench.kernel_source_digest(bench.DEC_SOURCES) in text
+    assert (got is not None) == recorded
+    if got is not None:
+        assert got > 0
+    # the forward's digest never matches it
+    assert bench.recorded_traffic(name, summary) is None
+
