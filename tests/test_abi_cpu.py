@@ -212,3 +212,81 @@ def test_bwd_workspace_query_sizes(lib):
     assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 96) == (fa.FA_ERR_UNSUPPORTED, 0)
     assert fa.bwd_workspace_query(1, 3, 2, 128, 128, 128) == (fa.FA_ERR_INVALID_ARG, 0)
     assert fa.bwd_workspace_query(1, 4, 2, 128, 128, 128, "window", 0) == (fa.FA_ERR_INVALID_ARG, 0)
+
+
+def _dec(**kw):
+    g = 1 << 30
+    a = dict(q_ptr=FAKE, k_ptr=FAKE + g, v_ptr=FAKE + 2 * g, table_ptr=FAKE + 3 * g,
+             lens_ptr=FAKE + 4 * g, o_ptr=FAKE + 5 * g, lse_ptr=FAKE + 6 * g, ws_ptr=FAKE + 7 * g,
+             ws_bytes=1 << 24, B=2, H=8, H_kv=2, Sq=1, d=128, block_size=16, max_blocks=64,
+             num_blocks=128, max_seq_len=1024, scale=0.088, mask_kind=fa.MASK_CAUSAL,
+             dtype=fa.DTYPE_BF16, stream=0)
+    a.update(kw)
+    return fa.decode_raw(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_kind=fa.MASK_SLIDING_WINDOW), fa.FA_ERR_UNSUPPORTED),  # decode: none or causal
+    (dict(block_size=24), fa.FA_ERR_UNSUPPORTED),
+    (dict(block_size=256, max_blocks=4), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=64, H_kv=1, Sq=4), fa.FA_ERR_UNSUPPORTED),                # 256 packed rows > 128
+    (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(Sq=0), fa.FA_ERR_INVALID_ARG),
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(num_blocks=0), fa.FA_ERR_INVALID_ARG),
+    (dict(max_seq_len=64 * 16 + 1), fa.FA_ERR_INVALID_ARG),            # beyond the table
+    (dict(Sq=2, max_seq_len=1), fa.FA_ERR_INVALID_ARG),                # fewer tokens than rows
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(table_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=FAKE + 8), fa.FA_ERR_MISALIGNED),
+    (dict(lens_ptr=FAKE + 4 * (1 << 30) + 2), fa.FA_ERR_MISALIGNED),
+    (dict(ws_ptr=FAKE + 7 * (1 << 30) + 16), fa.FA_ERR_MISALIGNED),     # workspace wants 256 B
+])
+def test_decode_invalid_calls_are_rejected_before_launch(lib, kw, status):
+    assert _dec(**kw) == status
+
+
+def test_decode_workspace_query_sizes(lib):
+    # rejected sizes report their status and 0 bytes, before any device query
+    q = fa.decode_workspace_query
+    assert q(2, 8, 2, 1, 96, 16, 64, 128, 1024) == (fa.FA_ERR_UNSUPPORTED, 0)
+    assert q(2, 8, 2, 1, 128, 24, 64, 128, 1024) == (fa.FA_ERR_UNSUPPORTED, 0)
+    assert q(2, 64, 1, 4, 128, 16, 64, 128, 1024) == (fa.FA_ERR_UNSUPPORTED, 0)
+    assert q(2, 3, 2, 1, 128, 16, 64, 128, 1024) == (fa.FA_ERR_INVALID_ARG, 0)
+    assert q(2, 8, 2, 1, 128, 16, 64, 128, 2048) == (fa.FA_ERR_INVALID_ARG, 0)
+
+
+def _fp8(**kw):
+    g = 1 << 30
+    a = dict(q_ptr=FAKE, k_ptr=FAKE + g, vt_ptr=FAKE + 2 * g, o_ptr=FAKE + 3 * g,
+             lse_ptr=FAKE + 4 * g, B=1, H=4, H_kv=2, Sq=256, Sk=256, d=128, scale=0.088,
+             q_descale=1.0, k_descale=1.0, v_descale=1.0, mask_kind=fa.MASK_CAUSAL, window=0,
+             stream=0)
+    a.update(kw)
+    return fa.fwd_fp8_raw(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(d=512), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_kind=3), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=3, H_kv=2), fa.FA_ERR_INVALID_ARG),
+    (dict(Sk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sk=200), fa.FA_ERR_INVALID_ARG),                              # V^T rows: 16-byte multiples
+    (dict(mask_kind=fa.MASK_SLIDING_WINDOW, window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), fa.FA_ERR_INVALID_ARG),
+    (dict(k_descale=0.0), fa.FA_ERR_INVALID_ARG),
+    (dict(v_descale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(q_descale=-1.0), fa.FA_ERR_INVALID_ARG),
+    (dict(vt_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=FAKE + 8), fa.FA_ERR_MISALIGNED),
+    (dict(lse_ptr=FAKE + 4 * (1 << 30) + 2), fa.FA_ERR_MISALIGNED),
+    (dict(o_ptr=FAKE + 64), fa.FA_ERR_INVALID_ARG),                     # o overlaps q
+    (dict(Sq=0, q_ptr=0, o_ptr=0), fa.FA_OK),                          # no rows: nothing to do
+])
+def test_fp8_invalid_calls_are_rejected_before_launch(lib, kw, status):
+    assert _fp8(**kw) == status
