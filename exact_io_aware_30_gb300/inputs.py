@@ -74,13 +74,34 @@ WORKLOADS = [
 ]
 
 
+# Further forward workloads, by name: the 8k x 32-head causal case in bf16
+# (the same draws as the fp16 one, rounded to bf16), and a d = 64 case with
+# the same flops (twice the heads at half the head dimension).
+EXTRA_WORKLOADS = [
+    Workload("b1h32_s8192_d128_bf16_causal", 1, 32, 8192, 8192, 128, BF16, "causal", seed=1003),
+    Workload("b1h64_s8192_d64_bf16_causal", 1, 64, 8192, 8192, 64, BF16, "causal", seed=1006),
+]
+
+
 def workload(index_or_name) -> Workload:
     if isinstance(index_or_name, int):
         return WORKLOADS[index_or_name]
-    for w in WORKLOADS:
+    for w in WORKLOADS + EXTRA_WORKLOADS:
         if w.name == index_or_name:
             return w
     raise KeyError(index_or_name)
+
+
+def with_dtype(w: Workload, dtype: str) -> Workload:
+    """The same workload (same seed, so the same draws) rounded to another
+    16-bit type; the name's type tag follows."""
+    if dtype == w.dtype:
+        return w
+    name = w.name.replace(f"_{w.dtype}_", f"_{dtype}_")
+    if name == w.name:
+        name = f"{w.name}_{dtype}"
+    return Workload(name, w.B, w.H, w.Sq, w.Sk, w.d, dtype, w.mask, w.window, w.spiky_keys,
+                    w.seed, w.Hkv)
 
 
 # ----------------------------------------------------------------------------

@@ -1,13 +1,13 @@
 """GPU parity: the sm_103a kernel (through the C ABI) against the fp64 oracle.
 
 Tolerances for bf16/fp16 inputs: max |O - O_ref| <= 1e-2, mean |O - O_ref|
-<= 1e-3, max |lse - lse_ref| <= 1e-3.  O is returned in the 16-bit input
-type, so even a correctly rounded result is off by up to half a unit in the
-last place (ulp) of that type: 0.0078 for bf16 |O| in [2, 4), 0.0156 in
-[4, 8).  The max criterion is therefore asserted on
-max(|O - O_ref| - ulp(O_ref)/2, 0); the raw max is asserted too for fp16
-(whose half-ulp is 8x smaller) and printed for every case.  Mean and lse
-criteria are asserted raw.
+<= 1e-3, max |lse - lse_ref| <= 1e-3, asserted raw.  One reading: O is
+returned in the 16-bit input type, so even a correctly rounded result is off
+by up to half a unit in the last place (ulp) of that type, 0.0156 for bf16
+|O| in [4, 8).  Where half an ulp of max |O_ref| is itself above 1e-2 (bf16
+outputs reaching |O| >= 4: the spiky-key workload), the max criterion is
+asserted on max(|O - O_ref| - ulp(O_ref)/2, 0) instead of the raw max; the
+raw max is printed for every case.  Mean and lse criteria are always raw.
 """
 import json
 import math
@@ -70,11 +70,14 @@ def compare(o, lse, o_ref, lse_ref, dtype, raw_max=None):
     fin = np.isfinite(lse_ref)
     assert np.array_equal(fin, np.isfinite(lse)), "lse -inf pattern differs"
     lerr = np.abs(lse[fin] - lse_ref[fin]) if fin.any() else np.zeros(1)
-    stats = dict(max=float(err.max()), mean=float(err.mean()), max_adj=float(adj.max()),
-                 lse=float(lerr.max()))
-    assert adj.max() <= MAX_TOL, stats
     if raw_max is None:
-        raw_max = dtype == inputs.FP16
+        # the raw max is a fair bar wherever rounding max|O_ref| to the type
+        # alone cannot exceed it
+        raw_max = 0.5 * float(_ulp(np.abs(o_ref).max(), dtype)) < MAX_TOL
+    stats = dict(max=float(err.max()), mean=float(err.mean()), max_adj=float(adj.max()),
+                 lse=float(lerr.max()), raw_max_asserted=bool(raw_max),
+                 ref_absmax=float(np.abs(o_ref).max()))
+    assert adj.max() <= MAX_TOL, stats
     if raw_max:
         assert err.max() <= MAX_TOL, stats
     assert err.mean() <= MEAN_TOL, stats
@@ -210,42 +213,31 @@ def test_host_buffers_end_to_end():
 
 
 # ---------------------------------------------------------------------------
-# The five named workloads at full size, in the launch configuration the
-# benchmark times: the first is checked element by element, the others on
-# sampled rows the oracle computes one by one (plus whole-output properties).
+# The named workloads at full size, in the launch configuration the benchmark
+# times, checked element by element over the whole output (the oracle runs
+# every row; about 8 s for the 8k x 32-head case on 16 host cores)
 # ---------------------------------------------------------------------------
 
-def test_workload_0_full():
-    w = inputs.workload(0)
+def whole_output(w, tag=""):
     inp = inputs.generate(w)
     o, lse = run_gpu(inp)
     qf, kf, vf = inp.f64()
+    del inp
     o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window)
-    compare(o, lse, o_ref, lse_ref, w.dtype)
+    del qf, kf, vf
+    stats = compare(o, lse, o_ref, lse_ref, w.dtype)
+    print("PARITY " + json.dumps(dict(workload=w.name, rows=int(lse.size), **stats)))
+    return stats
 
 
-def _sample_rows(w, n, rng):
-    BH = w.B * w.H
-    rows = set()
-    for bh in (0, BH - 1):
-        for i in (0, 1, 127, 128, 255, 256, w.Sq - 129, w.Sq - 128, w.Sq - 1):
-            if 0 <= i < w.Sq:
-                rows.add(bh * w.Sq + i)
-    rows.update(int(x) for x in rng.integers(0, BH * w.Sq, size=n))
-    return np.array(sorted(rows), dtype=np.int64)
+def test_workload_0_full():
+    whole_output(inputs.workload(0))
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4])
-def test_workload_full_size_sampled(idx):
-    w = inputs.workload(idx)
-    inp = inputs.generate(w)
-    o, lse = run_gpu(inp)
-    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    rows = _sample_rows(w, 384, np.random.default_rng(idx))
-    qf, kf, vf = inp.f64()
-    o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
-    stats = compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype)
-    print(f"{w.name}: {stats}")
+@pytest.mark.parametrize("name", [inputs.workload(i).name for i in (1, 2, 3, 4)]
+                         + [w.name for w in inputs.EXTRA_WORKLOADS])
+def test_workload_full_size_whole_output(name):
+    whole_output(inputs.workload(name))
 
 
 # ---------------------------------------------------------------------------
@@ -306,17 +298,9 @@ GQA_FULL = inputs.Workload("b1h32kv8_s8192_d128_fp16_causal_gqa", 1, 32, 8192, 8
                            inputs.FP16, "causal", seed=1013, Hkv=8)
 
 
-def test_gqa_full_size_sampled():
+def test_gqa_full_size_whole_output():
     # 8k tokens x 32 query heads sharing 8 K/V heads, in the benchmark's launch
-    w = GQA_FULL
-    inp = inputs.generate(w)
-    o, lse = run_gpu(inp)
-    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
-    rows = _sample_rows(w, 384, np.random.default_rng(31))
-    qf, kf, vf = inp.f64()
-    o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, w.mask, w.window, rows=rows)
-    stats = compare(o.reshape(-1, w.d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, w.dtype)
-    print(f"{w.name}: {stats}")
+    whole_output(GQA_FULL)
 
 
 def test_more_units_than_the_schedule_holds():
