@@ -1,9 +1,9 @@
 // fa_api.cu -- host side of the C ABI declared in include/fa.h: argument
 // validation, TMA tensor-map encoding, kernel selection and launch.  This file
 // holds the shared helpers and the forward (fa_fwd, fa_fwd_fp16, fa_fwd_gqa);
-// the backward, paged decoding and the 8-bit forward are in fa_api_bwd.cuh,
-// fa_api_decode.cuh and fa_api_fp8.cuh, included at the end (one translation
-// unit).
+// the backward, paged decoding, the 8-bit forward and the forward from host
+// memory are in fa_api_bwd.cuh, fa_api_decode.cuh, fa_api_fp8.cuh and
+// fa_api_host.cuh, included at the end (one translation unit).
 //
 // Validation happens before anything is enqueued and never falls back to a
 // different kernel: an unsupported head dim, dtype or mask is an error
@@ -20,6 +20,7 @@
 #include <cstring>
 #include <mutex>
 #include <algorithm>
+#include <atomic>
 #include <queue>
 #include <utility>
 #include <vector>
@@ -51,9 +52,26 @@ DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 bool g_encode_probed = false;
 
+// Test hook (fa_set_debug_stall_ms): while set to N ms, each launch's first
+// softmax (or compute-warp) wait is one that nothing completes, with N ms as
+// the limit of every wait, so that the bounded-wait path runs without any
+// fault.  0 = off.
+std::atomic<int> g_debug_stall_ms{0};
+
+// The wait limit of the test hook in ns, 0 when the hook is off.
+uint64_t debug_stall_ns() {
+    const int ms = g_debug_stall_ms.load(std::memory_order_relaxed);
+    return ms > 0 ? (uint64_t)ms * 1000000ull : 0;
+}
+
+// FA_LOG=1 in the environment logs each launch's configuration to stderr
+// (read once, at the first call).
 bool log_enabled() {
-    const char *e = std::getenv("FA_LOG");
-    return e && e[0] && e[0] != '0';
+    static const bool on = [] {
+        const char *e = std::getenv("FA_LOG");
+        return e && e[0] && e[0] != '0';
+    }();
+    return on;
 }
 
 // Probe the current device once: compute capability 10.3 and SM count.
@@ -320,15 +338,9 @@ fa_status fwd_impl(const void *q, const void *k, const void *v, void *o, float *
     p.scale_log2 = std::fmax((float)((double)scale * 1.4426950408889634), FLT_MIN);
     p.o_vec8 = (reinterpret_cast<uintptr_t>(o) & 31u) == 0;
     p.wait_limit_ns = fa::kWaitLimitNs;
-    // Test hook: FA_DEBUG_STALL_MS=N makes the launch's first softmax wait
-    // one that nothing completes, with N ms as the wait limit, so that the
-    // bounded-wait path can be exercised without any fault.
-    if (const char *e = std::getenv("FA_DEBUG_STALL_MS")) {
-        const long ms = std::strtol(e, nullptr, 10);
-        if (ms > 0 && ms <= 10000) {
-            p.stall_test = 1;
-            p.wait_limit_ns = (uint64_t)ms * 1000000ull;
-        }
+    if (const uint64_t ns = debug_stall_ns()) {  // test hook, off unless set
+        p.stall_test = 1;
+        p.wait_limit_ns = ns;
     }
     p.n_qtiles = (Sq + 127) / 128;
     p.n_units = B * H * p.n_qtiles;
@@ -384,11 +396,6 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
 }
 
 
-
-
-
-
-
 fa_status fa_workspace_query(int B, int H, int Sq, int Sk, int d, int mask_kind, int window,
                              int dtype, size_t *bytes) {
     if (!bytes) return FA_ERR_INVALID_ARG;
@@ -431,6 +438,12 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     return FA_OK;
 }
 
+fa_status fa_set_debug_stall_ms(int ms) {
+    if (ms < 0 || ms > 10000) return FA_ERR_INVALID_ARG;
+    fa::g_debug_stall_ms.store(ms, std::memory_order_relaxed);
+    return FA_OK;
+}
+
 fa_status fa_get_device_error(void) {
     int v = 0;
     if (cudaMemcpyFromSymbol(&v, fa::g_fa_status, sizeof(int)) != cudaSuccess) return FA_ERR_CUDA;
@@ -443,7 +456,8 @@ fa_status fa_get_device_error(void) {
 }  // extern "C"
 
 // The other entry points, each with its kernels: the backward, decoding over a
-// paged cache, and the 8-bit forward.
+// paged cache, the 8-bit forward, and the forward from host memory.
 #include "fa_api_bwd.cuh"
 #include "fa_api_decode.cuh"
 #include "fa_api_fp8.cuh"
+#include "fa_api_host.cuh"

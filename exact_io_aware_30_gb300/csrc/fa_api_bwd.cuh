@@ -18,19 +18,6 @@ static __device__ __align__(256) unsigned char g_noalloc_ws[kNoAllocWsBytes];
 
 namespace {
 
-// Test hook shared by the backward, decode and 8-bit entry points (the
-// forward has its own): FA_DEBUG_STALL_MS=N (1..10000) makes each launch's
-// first compute-warp wait one that nothing completes, with N ms as the limit
-// of every wait, so that the bounded-wait path runs without any fault.
-// Returns the limit in ns, 0 when the hook is off.
-uint64_t debug_stall_ns() {
-    if (const char *e = std::getenv("FA_DEBUG_STALL_MS")) {
-        const long ms = std::strtol(e, nullptr, 10);
-        if (ms > 0 && ms <= 10000) return (uint64_t)ms * 1000000ull;
-    }
-    return 0;
-}
-
 // ---------------------------------------------------------------- backward
 
 size_t bwd_pad_rows(int Sq) {

@@ -18,24 +18,25 @@ struct DecPlan {
     size_t part_o_bytes = 0, bytes = 0;
 };
 
-// The kernel that serves R rows per K/V head: the CUDA-core one
-// (fa_decode_gemv_kernel) up to 2 rows, where the products are matrix-vector
-// ones and it streams the cache faster, else the tensor-core one
-// (fa_decode_kernel).  FA_DECODE_KERNEL=mma or =gemv in the environment forces
-// one (tests, comparisons); gemv takes at most 2 rows.
+// The kernel that serves R rows per K/V head.  FA_DECODE_AUTO: the CUDA-core
+// one (fa_decode_gemv_kernel) up to 2 rows, where the products are
+// matrix-vector ones and it streams the cache faster, else the tensor-core
+// one (fa_decode_kernel).  FA_DECODE_TENSOR_CORES / FA_DECODE_CUDA_CORES
+// force one; the CUDA-core kernel takes at most 2 rows.
 constexpr int kDecMma = 0;
 constexpr int kDecGemv = 1;
 constexpr int kGemvMaxRows = 2;
 
-fa_status decode_path(int R, int *path) {
-    const char *e = std::getenv("FA_DECODE_KERNEL");
-    if (e && std::strcmp(e, "mma") == 0) {
+fa_status decode_path(int R, int choice, int *path) {
+    if (choice == FA_DECODE_TENSOR_CORES) {
         *path = kDecMma;
-    } else if (e && std::strcmp(e, "gemv") == 0) {
+    } else if (choice == FA_DECODE_CUDA_CORES) {
         if (R > kGemvMaxRows) return FA_ERR_UNSUPPORTED;
         *path = kDecGemv;
-    } else {
+    } else if (choice == FA_DECODE_AUTO) {
         *path = R <= kGemvMaxRows ? kDecGemv : kDecMma;
+    } else {
+        return FA_ERR_UNSUPPORTED;
     }
     return FA_OK;
 }
@@ -122,7 +123,7 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
                       const int *seq_lens, void *o, float *lse, void *workspace, size_t workspace_bytes,
                       int B, int H, int Hkv, int Sq, int d, int block_size, int max_blocks,
                       int num_blocks, int max_seq_len, float scale, int mask_kind, int dtype,
-                      cudaStream_t stream) {
+                      int kernel, cudaStream_t stream) {
     fa_status st = check_dec_sizes(B, H, Hkv, Sq, d, block_size, max_blocks, num_blocks, max_seq_len,
                                    mask_kind, dtype);
     if (st != FA_OK) return st;
@@ -135,12 +136,12 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
                          reinterpret_cast<uintptr_t>(seq_lens);
     if ((a16 & 15u) || (a4 & 3u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return FA_ERR_MISALIGNED;
+    int path = kDecMma;
+    st = decode_path((H / Hkv) * Sq, kernel, &path);
+    if (st != FA_OK) return st;
     int dev = 0;
     DeviceInfo *info = nullptr;
     st = device_info(&dev, &info);
-    if (st != FA_OK) return st;
-    int path = kDecMma;
-    st = decode_path((H / Hkv) * Sq, &path);
     if (st != FA_OK) return st;
     const DecPlan pl = plan_decode(B, H, Hkv, Sq, d, max_seq_len, info->num_sms, path);
     if (workspace_bytes < pl.bytes) return FA_ERR_INVALID_ARG;
@@ -249,28 +250,30 @@ fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cach
                           const int *block_table, const int *seq_lens, void *o, float *lse,
                           void *workspace, size_t workspace_bytes, int B, int H, int H_kv, int Sq,
                           int d, int block_size, int max_blocks, int num_blocks, int max_seq_len,
-                          float scale, int mask_kind, int dtype, fa_stream_t stream) {
+                          float scale, int mask_kind, int dtype, int kernel, fa_stream_t stream) {
     return fa::decode_impl(q, k_cache, v_cache, block_table, seq_lens, o, lse, workspace,
                            workspace_bytes, B, H, H_kv, Sq, d, block_size, max_blocks, num_blocks,
-                           max_seq_len, scale, mask_kind, dtype, reinterpret_cast<cudaStream_t>(stream));
+                           max_seq_len, scale, mask_kind, dtype, kernel,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int block_size,
                                     int max_blocks, int num_blocks, int max_seq_len, int mask_kind,
-                                    int dtype, size_t *bytes) {
+                                    int dtype, int kernel, size_t *bytes) {
     if (!bytes) return FA_ERR_INVALID_ARG;
     *bytes = 0;
     fa_status st = fa::check_dec_sizes(B, H, H_kv, Sq, d, block_size, max_blocks, num_blocks,
                                        max_seq_len, mask_kind, dtype);
     if (st != FA_OK) return st;
+    int path = fa::kDecMma;
+    st = fa::decode_path((H / H_kv) * Sq, kernel, &path);
+    if (st != FA_OK) return st;
     int dev = 0;
     fa::DeviceInfo *info = nullptr;
     st = fa::device_info(&dev, &info);
     if (st != FA_OK) return st;
-    int path = fa::kDecMma;
-    st = fa::decode_path((H / H_kv) * Sq, &path);
-    if (st == FA_OK) *bytes = fa::plan_decode(B, H, H_kv, Sq, d, max_seq_len, info->num_sms, path).bytes;
-    return st;
+    *bytes = fa::plan_decode(B, H, H_kv, Sq, d, max_seq_len, info->num_sms, path).bytes;
+    return FA_OK;
 }
 
 }  // extern "C"

@@ -30,11 +30,17 @@ MASKS = {"none": MASK_NONE, "causal": MASK_CAUSAL, "window": MASK_SLIDING_WINDOW
 
 DTYPE_BF16 = 0
 DTYPE_FP16 = 1
+DECODE_AUTO = 0            # fa_decode_paged kernel choice
+DECODE_TENSOR_CORES = 1
+DECODE_CUDA_CORES = 2
+_DECODE_KERNELS = {"auto": DECODE_AUTO, "tensor_cores": DECODE_TENSOR_CORES,
+                   "cuda_cores": DECODE_CUDA_CORES}
 
 # Every entry point declared in include/fa.h.
 EXPORTS = ("fa_fwd", "fa_fwd_fp16", "fa_fwd_gqa", "fa_fwd_fp8", "fa_bwd", "fa_bwd_noalloc",
            "fa_bwd_workspace_query", "fa_decode_paged", "fa_decode_workspace_query",
-           "fa_workspace_query", "fa_status_string", "fa_describe", "fa_get_device_error")
+           "fa_workspace_query", "fa_status_string", "fa_describe", "fa_get_device_error",
+           "fa_fwd_host", "fa_fwd_host_workspace_query", "fa_set_debug_stall_ms")
 
 
 class FAError(RuntimeError):
@@ -84,13 +90,21 @@ def load(path: str | None = None):
         lib.fa_decode_paged.restype = _i
         lib.fa_decode_paged.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                         _i, _i, _i, _i, _i, _i, _i, _i, _i, ctypes.c_float, _i,
-                                        _i, _vp]
+                                        _i, _i, _vp]
         lib.fa_decode_workspace_query.restype = _i
-        lib.fa_decode_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
+        lib.fa_decode_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i,
                                                   ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_set_debug_stall_ms.restype = _i
+        lib.fa_set_debug_stall_ms.argtypes = [_i]
         lib.fa_bwd_workspace_query.restype = _i
         lib.fa_bwd_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
                                                ctypes.POINTER(ctypes.c_size_t)]
+        lib.fa_fwd_host.restype = _i
+        lib.fa_fwd_host.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i,
+                                    _i, _i, _i, ctypes.c_float, _i, _i, _i, _vp]
+        lib.fa_fwd_host_workspace_query.restype = _i
+        lib.fa_fwd_host_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i, _i,
+                                                    ctypes.POINTER(ctypes.c_size_t)]
         lib.fa_workspace_query.restype = _i
         lib.fa_workspace_query.argtypes = [_i, _i, _i, _i, _i, _i, _i, _i,
                                            ctypes.POINTER(ctypes.c_size_t)]
@@ -206,35 +220,45 @@ def forward_fp8(q, k, vt, q_descale: float, k_descale: float, v_descale: float,
 
 def decode_raw(q_ptr, k_ptr, v_ptr, table_ptr, lens_ptr, o_ptr, lse_ptr, ws_ptr, ws_bytes, B, H,
                H_kv, Sq, d, block_size, max_blocks, num_blocks, max_seq_len, scale, mask_kind,
-               dtype, stream) -> int:
+               dtype, stream, kernel=DECODE_AUTO) -> int:
     """Call fa_decode_paged with raw device pointers; returns the status."""
     return load().fa_decode_paged(_vp(q_ptr), _vp(k_ptr), _vp(v_ptr), _vp(table_ptr),
                                   _vp(lens_ptr), _vp(o_ptr), _vp(lse_ptr), _vp(ws_ptr),
                                   ctypes.c_size_t(ws_bytes), int(B), int(H), int(H_kv), int(Sq),
                                   int(d), int(block_size), int(max_blocks), int(num_blocks),
                                   int(max_seq_len), ctypes.c_float(scale), int(mask_kind),
-                                  int(dtype), _vp(stream))
+                                  int(dtype), int(kernel), _vp(stream))
+
+
+def decode_kernel_code(kernel) -> int:
+    """"auto", "tensor_cores", "cuda_cores" (or the FA_DECODE_* code)."""
+    if isinstance(kernel, str):
+        if kernel not in _DECODE_KERNELS:
+            raise FAError(FA_ERR_UNSUPPORTED, f"decode kernel {kernel!r}: one of {list(_DECODE_KERNELS)}")
+        return _DECODE_KERNELS[kernel]
+    return int(kernel)
 
 
 def decode_workspace_query(B, H, H_kv, Sq, d, block_size, max_blocks, num_blocks, max_seq_len,
-                           mask="none", dtype=DTYPE_BF16):
+                           mask="none", dtype=DTYPE_BF16, kernel=DECODE_AUTO):
     """(status, bytes) of fa_decode_workspace_query."""
     n = ctypes.c_size_t(12345)
     st = load().fa_decode_workspace_query(int(B), int(H), int(H_kv), int(Sq), int(d),
                                           int(block_size), int(max_blocks), int(num_blocks),
                                           int(max_seq_len), mask_code(mask), int(dtype),
-                                          ctypes.byref(n))
+                                          decode_kernel_code(kernel), ctypes.byref(n))
     return st, n.value
 
 
 def decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
                  scale: float | None = None, mask="none", out=None, lse=None, workspace=None,
-                 stream=None):
+                 stream=None, kernel="auto"):
     """Attention of q's new rows over a paged K/V cache (fa_decode_paged).
 
     q [B, H, Sq, d]; k_cache, v_cache [num_blocks, H_kv, block_size, d] (one
     16-bit dtype); block_table int32 [B, max_blocks] and seq_lens int32 [B] on
-    the same CUDA device.  Returns (o, lse).
+    the same CUDA device.  kernel: "auto" (the library's choice by rows per
+    K/V head), "tensor_cores" or "cuda_cores".  Returns (o, lse).
     """
     import torch
     for name, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
@@ -255,7 +279,8 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     mb = block_table.shape[1]
-    st, ws_bytes = decode_workspace_query(B, H, H_kv, Sq, d, bs, mb, nb, max_seq_len, mask, dt)
+    kc = decode_kernel_code(kernel)
+    st, ws_bytes = decode_workspace_query(B, H, H_kv, Sq, d, bs, mb, nb, max_seq_len, mask, dt, kc)
     _check(st, "fa_decode_workspace_query")
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
@@ -268,7 +293,7 @@ def decode_paged(q, k_cache, v_cache, block_table, seq_lens, max_seq_len: int,
     st = decode_raw(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_table.data_ptr(),
                     seq_lens.data_ptr(), out.data_ptr(), lse.data_ptr(), workspace.data_ptr(),
                     workspace.numel(), B, H, H_kv, Sq, d, bs, mb, nb, max_seq_len, float(scale),
-                    mask_code(mask), dt, sp)
+                    mask_code(mask), dt, sp, kc)
     _check(st, "fa_decode_paged")
     return out, lse
 
@@ -298,6 +323,12 @@ def describe(d: int, mask="none", dtype=DTYPE_BF16) -> str:
 
 def device_error() -> int:
     return load().fa_get_device_error()
+
+
+def set_debug_stall_ms(ms: int) -> None:
+    """Test hook (fa_set_debug_stall_ms): with ms > 0 every later launch's
+    first pipeline wait runs out after ms; 0 turns it off."""
+    _check(load().fa_set_debug_stall_ms(int(ms)), "fa_set_debug_stall_ms")
 
 
 def _dtype_code(t) -> int:
@@ -400,25 +431,67 @@ def backward(q, k, v, o, lse, dout, scale: float | None = None, mask="none", win
     return dq, dk, dv
 
 
-def forward_host(q, k, v, scale: float | None = None, mask="none", window: int = 0,
-                 device=None, stream=None):
-    """End-to-end call from host (CPU) tensors: copy in, run, copy out.
+def fwd_host_raw(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, ws_ptr, ws_bytes, B, H, H_kv, Sq, Sk, d,
+                 scale, mask_code_, window, dtype, stream_ptr) -> int:
+    """fa_fwd_host with raw pointers (host buffers, device workspace)."""
+    return load().fa_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, ws_ptr, ws_bytes, B, H, H_kv,
+                              Sq, Sk, d, scale, mask_code_, window, dtype, stream_ptr)
 
-    q, k, v are CPU tensors (pinned for asynchronous copies).  Returns CPU
-    (o, lse) after the stream has finished.
+
+def host_workspace_query(B, H, H_kv, Sq, Sk, d, mask="none", window=0, dtype=DTYPE_BF16):
+    n = ctypes.c_size_t(0)
+    st = load().fa_fwd_host_workspace_query(B, H, H_kv, Sq, Sk, d, mask_code(mask), int(window),
+                                            dtype, ctypes.byref(n))
+    return st, n.value
+
+
+def forward_host(q, k, v, scale: float | None = None, mask="none", window: int = 0,
+                 out=None, lse=None, workspace=None, device=None, stream=None, sync: bool = True):
+    """End to end from host (CPU) tensors through fa_fwd_host: the library
+    copies Q, K, V in, runs the forward and copies O and lse out, chunk by
+    chunk with the copies overlapping the kernels.
+
+    q [B, H, Sq, d], k and v [B, H_kv, Sk, d] CPU tensors (bf16 or fp16;
+    pinned memory for asynchronous copies).  ``out`` / ``lse``: CPU tensors to
+    write (allocated pinned here if not given); ``workspace``: a uint8 CUDA
+    tensor of at least ``host_workspace_query`` bytes (allocated here if not
+    given).  With sync=False the call returns once enqueued on ``stream``.
+    Returns (out, lse).
     """
     import torch
     dev = torch.device(device or "cuda")
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.is_cuda:
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a host tensor (use forward)")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise FAError(FA_ERR_INVALID_ARG, f"{name} must be a contiguous [B,H,S,d] tensor")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise FAError(FA_ERR_INVALID_ARG, "q, k, v must share one dtype")
+    dt = _dtype_code(q)
+    B, H, Sq, d = q.shape
+    H_kv, Sk = k.shape[1], k.shape[2]
+    if tuple(k.shape) != (B, H_kv, Sk, d) or tuple(v.shape) != (B, H_kv, Sk, d):
+        raise FAError(FA_ERR_INVALID_ARG, "k and v must be [B,H_kv,Sk,d] matching q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, pin_memory=True)
+    if out.is_cuda or lse.is_cuda or tuple(out.shape) != tuple(q.shape) or \
+            tuple(lse.shape) != (B, H, Sq) or out.dtype != q.dtype or lse.dtype != torch.float32:
+        raise FAError(FA_ERR_INVALID_ARG, "out / lse must be host tensors like q / [B,H,Sq] fp32")
+    st, ws_bytes = host_workspace_query(B, H, H_kv, Sq, Sk, d, mask, window, dt)
+    _check(st, "fa_fwd_host_workspace_query")
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    with torch.cuda.stream(stream):
-        qd = q.to(dev, non_blocking=True)
-        kd = k.to(dev, non_blocking=True)
-        vd = v.to(dev, non_blocking=True)
-        o, lse = forward(qd, kd, vd, scale, mask, window, stream=stream)
-        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-        o_h.copy_(o, non_blocking=True)
-        l_h.copy_(lse, non_blocking=True)
-    stream.synchronize()
-    return o_h, l_h
+    sp = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = fwd_host_raw(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                      workspace.data_ptr(), workspace.numel(), B, H, H_kv, Sq, Sk, d, float(scale),
+                      mask_code(mask), int(window), dt, sp)
+    _check(st, "fa_fwd_host")
+    if sync:
+        stream.synchronize()
+    return out, lse

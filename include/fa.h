@@ -54,6 +54,8 @@ typedef enum fa_status {
 
 enum { FA_MASK_NONE = 0, FA_MASK_CAUSAL = 1, FA_MASK_SLIDING_WINDOW = 2 };
 enum { FA_DTYPE_BF16 = 0, FA_DTYPE_FP16 = 1 };
+/* Kernel choice of fa_decode_paged / fa_decode_workspace_query. */
+enum { FA_DECODE_AUTO = 0, FA_DECODE_TENSOR_CORES = 1, FA_DECODE_CUDA_CORES = 2 };
 
 /*
  * fa_fwd -- fused attention forward, bf16 inputs and output.
@@ -228,33 +230,82 @@ fa_status fa_fwd_fp8(const void *q, const void *k, const void *vt, void *o, floa
  *                sits at position seq_lens[b] - Sq + i and sees tokens up to
  *                it (the reading for decoding: the new rows are the last)
  *   dtype        FA_DTYPE_BF16 or FA_DTYPE_FP16
+ *   kernel       FA_DECODE_AUTO: with at most 2 rows per K/V head
+ *                ((H / H_kv) * Sq <= 2) the key-range kernel runs on the CUDA
+ *                cores (the products are matrix-vector ones), else on the
+ *                tensor cores.  FA_DECODE_TENSOR_CORES / FA_DECODE_CUDA_CORES
+ *                force one (CUDA cores: at most 2 rows, else
+ *                FA_ERR_UNSUPPORTED); other values FA_ERR_UNSUPPORTED.  The
+ *                two kernels split the keys differently, so pass the same
+ *                choice to fa_decode_workspace_query.
  * Cache slots past a request's length may hold any values, inf and NaN
  * included: they are hidden and never reach O.  Errors and the device flag
  * are as for fa_fwd; the library allocates nothing.  Two launches: the
- * key-range kernel, then the merge.  With at most 2 rows per K/V head
- * ((H / H_kv) * Sq <= 2) the key-range kernel runs on the CUDA cores (the
- * products are matrix-vector ones), else on the tensor cores; the environment
- * variable FA_DECODE_KERNEL=mma or =gemv forces one (gemv: at most 2 rows,
- * else FA_ERR_UNSUPPORTED) and must not change between
- * fa_decode_workspace_query and the call, since the two kernels split the
- * keys differently.
+ * key-range kernel, then the merge.
  */
 fa_status fa_decode_paged(const void *q, const void *k_cache, const void *v_cache,
                           const int *block_table, const int *seq_lens, void *o, float *lse,
                           void *workspace, size_t workspace_bytes, int B, int H, int H_kv,
                           int Sq, int d, int block_size, int max_blocks, int num_blocks,
-                          int max_seq_len, float scale, int mask_kind, int dtype,
+                          int max_seq_len, float scale, int mask_kind, int dtype, int kernel,
                           fa_stream_t stream);
 
 /*
  * fa_decode_workspace_query -- workspace bytes fa_decode_paged needs on the
- * current device (partial rows of every key range: (d + 1) x 4 bytes per row
- * and range) and the status it would return for these sizes.  bytes must be
- * non-NULL; it is 0 whenever the status is not FA_OK.
+ * current device with this kernel choice (partial rows of every key range:
+ * (d + 1) x 4 bytes per row and range) and the status it would return for
+ * these sizes.  bytes must be non-NULL; it is 0 whenever the status is not
+ * FA_OK.
  */
 fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int block_size,
                                     int max_blocks, int num_blocks, int max_seq_len,
-                                    int mask_kind, int dtype, size_t *bytes);
+                                    int mask_kind, int dtype, int kernel, size_t *bytes);
+
+/*
+ * fa_fwd_host -- the forward end to end from host memory: Q, K, V are
+ * copied into a device workspace, the fused forward of fa_fwd_gqa runs there,
+ * and O and lse are copied back to host memory.  The arithmetic and the
+ * results are those of fa_fwd_gqa (the method's "what goes in, what comes
+ * out" -- "FlashAttention: IO-aware attention kernels" -- with the host
+ * copies around it).  The problem is cut into up to 8 chunks of whole K/V
+ * heads (with the query heads that read them); chunk c+1's inputs are copied
+ * in on a library stream while chunk c runs on `stream` and chunk c-1's
+ * outputs are copied out on a second library stream, so the copies overlap
+ * the kernels and each other.
+ *
+ *   q_host, o_host  host pointers, [B, H, Sq, d] 16-bit (dtype)
+ *   k_host, v_host  host pointers, [B, H_kv, Sk, d] 16-bit
+ *   lse_host        host pointer, [B, H, Sq] fp32
+ *                   Pinned (page-locked) host memory gives asynchronous
+ *                   copies; pageable memory works but the copies then
+ *                   serialise.  Device pointers are refused
+ *                   (FA_ERR_INVALID_ARG): use fa_fwd / fa_fwd_gqa.
+ *   workspace       device memory of at least fa_fwd_host_workspace_query()
+ *                   bytes (Q, K, V, O and lse), 256-byte aligned; owned by
+ *                   the caller; its contents on entry do not matter
+ *   the rest        as for fa_fwd_gqa
+ * The call returns once everything is enqueued; `stream` reaches its next
+ * work only after O and lse have landed in host memory, so synchronising
+ * `stream` is enough before reading them.  The host buffers and the
+ * workspace must stay valid until then.  The library's two copy streams and
+ * their events are created by the first call on a device (no device memory
+ * is allocated); the enqueue of concurrent calls is serialised by a lock.
+ * Sq == 0: FA_OK, nothing is enqueued.  A CUDA error part way through the
+ * enqueue returns FA_ERR_CUDA with the earlier chunks already enqueued.
+ */
+fa_status fa_fwd_host(const void *q_host, const void *k_host, const void *v_host,
+                      void *o_host, float *lse_host, void *workspace, size_t workspace_bytes,
+                      int B, int H, int H_kv, int Sq, int Sk, int d, float scale,
+                      int mask_kind, int window, int dtype, fa_stream_t stream);
+
+/*
+ * fa_fwd_host_workspace_query -- device workspace bytes fa_fwd_host needs
+ * (the 16-bit Q, K, V and O and the fp32 lse, each rounded up to 256 bytes)
+ * and the status it would return for these sizes on the current device
+ * (pointer checks aside).  bytes must be non-NULL; 0 unless FA_OK.
+ */
+fa_status fa_fwd_host_workspace_query(int B, int H, int H_kv, int Sq, int Sk, int d,
+                                      int mask_kind, int window, int dtype, size_t *bytes);
 
 /*
  * fa_workspace_query -- device scratch bytes fa_fwd needs for this problem
@@ -284,12 +335,19 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len);
  * caller synchronises the stream first.  FA_OK if no kernel raised it,
  * FA_ERR_DEVICE_TIMEOUT if one did, FA_ERR_CUDA if it cannot be read.
  * A kernel that times out stops its pipeline and finishes normally (its O
- * and lse are then undefined); the context stays usable.  For testing that
- * path, the environment variable FA_DEBUG_STALL_MS=N (1..10000) makes each
- * launch's first softmax (or compute-warp) wait one that nothing completes,
- * with a limit of N ms instead of about 2 s, in every entry point's kernels.
+ * and lse are then undefined); the context stays usable.
  */
 fa_status fa_get_device_error(void);
+
+/*
+ * fa_set_debug_stall_ms -- test hook for the timeout path.  With ms in
+ * 1..10000, every later launch of every entry point makes its first softmax
+ * (or compute-warp) wait one that nothing completes, with a limit of ms
+ * instead of about 2 s: the wait runs out, the kernel winds down and raises
+ * the device flag, without any fault.  0 turns the hook off (the default).
+ * Process-wide; FA_ERR_INVALID_ARG outside 0..10000.
+ */
+fa_status fa_set_debug_stall_ms(int ms);
 
 #ifdef __cplusplus
 }

@@ -250,6 +250,15 @@ def test_decode_invalid_calls_are_rejected_before_launch(lib, kw, status):
     assert _dec(**kw) == status
 
 
+@pytest.mark.parametrize("kw,status", [
+    (dict(kernel=7), fa.FA_ERR_UNSUPPORTED),                         # no such kernel choice
+    (dict(kernel=-1), fa.FA_ERR_UNSUPPORTED),
+    (dict(kernel=fa.DECODE_CUDA_CORES), fa.FA_ERR_UNSUPPORTED),      # 4 rows per K/V head > 2
+])
+def test_decode_kernel_choice_is_checked(lib, kw, status):
+    assert _dec(**kw) == status
+
+
 def test_decode_workspace_query_sizes(lib):
     # rejected sizes report their status and 0 bytes, before any device query
     q = fa.decode_workspace_query
@@ -290,3 +299,46 @@ def _fp8(**kw):
 ])
 def test_fp8_invalid_calls_are_rejected_before_launch(lib, kw, status):
     assert _fp8(**kw) == status
+
+
+def _host(**kw):
+    g = 1 << 30
+    a = dict(q_ptr=FAKE, k_ptr=FAKE + g, v_ptr=FAKE + 2 * g, o_ptr=FAKE + 3 * g,
+             lse_ptr=FAKE + 4 * g, ws_ptr=FAKE + 5 * g, ws_bytes=1 << 30, B=1, H=4, H_kv=2,
+             Sq=300, Sk=300, d=128, scale=0.088, mask_code_=fa.MASK_CAUSAL, window=0,
+             dtype=fa.DTYPE_BF16, stream_ptr=0)
+    a.update(kw)
+    return fa.fwd_host_raw(**a)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=96), fa.FA_ERR_UNSUPPORTED),
+    (dict(dtype=2), fa.FA_ERR_UNSUPPORTED),
+    (dict(mask_code_=5), fa.FA_ERR_UNSUPPORTED),
+    (dict(H=3), fa.FA_ERR_INVALID_ARG),                       # H_kv does not divide H
+    (dict(B=0), fa.FA_ERR_INVALID_ARG),
+    (dict(Sk=0), fa.FA_ERR_INVALID_ARG),
+    (dict(mask_code_=fa.MASK_SLIDING_WINDOW, window=0), fa.FA_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), fa.FA_ERR_INVALID_ARG),
+    (dict(q_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(lse_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_ptr=0), fa.FA_ERR_INVALID_ARG),
+    (dict(ws_bytes=1000), fa.FA_ERR_INVALID_ARG),              # workspace too small
+    (dict(ws_ptr=FAKE + 5 * (1 << 30) + 128), fa.FA_ERR_MISALIGNED),
+    (dict(Sq=0, q_ptr=0, ws_ptr=0), fa.FA_OK),                 # nothing to do
+])
+def test_host_invalid_calls_are_rejected_before_any_copy(lib, kw, status):
+    assert _host(**kw) == status
+
+
+def test_host_workspace_query_sizes(lib):
+    # Q, K, V, O and lse, each rounded up to 256 bytes; rejected sizes give 0
+    assert fa.host_workspace_query(1, 4, 2, 300, 300, 96) == (fa.FA_ERR_UNSUPPORTED, 0)
+    assert fa.host_workspace_query(1, 3, 2, 300, 300, 128) == (fa.FA_ERR_INVALID_ARG, 0)
+
+
+def test_debug_stall_hook_range(lib):
+    # the test hook is set explicitly (no environment variable); off by default
+    assert lib.fa_set_debug_stall_ms(-1) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_debug_stall_ms(10001) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_set_debug_stall_ms(0) == fa.FA_OK

@@ -27,16 +27,18 @@ def _lib():
     assert fa.device_error() == fa.FA_OK
 
 
-@pytest.fixture(autouse=True, params=["auto", "mma"])
-def kernel(request, monkeypatch):
+_KERNEL = {"which": "auto"}
+
+
+@pytest.fixture(autouse=True, params=["auto", "tensor_cores"])
+def kernel(request):
     """Every test runs twice: with the library's own choice of kernel (the
     CUDA-core one for at most 2 rows per K/V head, else the tensor-core one)
-    and with the tensor-core kernel forced."""
-    if request.param == "auto":
-        monkeypatch.delenv("FA_DECODE_KERNEL", raising=False)
-    else:
-        monkeypatch.setenv("FA_DECODE_KERNEL", request.param)
-    return request.param
+    and with the tensor-core kernel forced (fa_decode_paged's kernel
+    argument)."""
+    _KERNEL["which"] = request.param
+    yield request.param
+    _KERNEL["which"] = "auto"
 
 
 def _dev16(bits, dtype):
@@ -59,7 +61,8 @@ def run_gpu(inp, k_bits=None, v_bits=None):
     vc = _dev16(inp.v_bits if v_bits is None else v_bits, w.dtype)
     table = torch.from_numpy(inp.block_table).cuda()
     lens = torch.from_numpy(inp.seq_lens).cuda()
-    o, lse = fa.decode_paged(q, kc, vc, table, lens, w.max_seq_len, scale=w.scale, mask=w.mask)
+    o, lse = fa.decode_paged(q, kc, vc, table, lens, w.max_seq_len, scale=w.scale, mask=w.mask,
+                             kernel=_KERNEL["which"])
     torch.cuda.synchronize()
     assert fa.device_error() == fa.FA_OK
     return o.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
@@ -152,7 +155,7 @@ def test_decode_out_of_range_table_entry_reads_zeros(bad):
     kc, vc = _dev16(inp.k_bits, w.dtype), _dev16(inp.v_bits, w.dtype)
     o, lse = fa.decode_paged(q, kc, vc, torch.from_numpy(table).cuda(),
                              torch.from_numpy(inp.seq_lens).cuda(), w.max_seq_len, scale=w.scale,
-                             mask=w.mask)
+                             mask=w.mask, kernel=_KERNEL["which"])
     torch.cuda.synchronize()
     assert fa.device_error() == fa.FA_OK
     o = o.float().cpu().numpy().astype(np.float64)
@@ -181,12 +184,12 @@ def test_decode_unsupported_requests_raise():
     q = torch.zeros(1, 2, 1, 96, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(4, 2, 16, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(fa.FAError) as e:
-        fa.decode_paged(q, kc, kc, t, ln, 16)
+        fa.decode_paged(q, kc, kc, t, ln, 16, kernel=_KERNEL["which"])
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
     q = torch.zeros(1, 2, 1, 128, dtype=torch.bfloat16, device="cuda")
     kc = torch.zeros(4, 2, 24, 128, dtype=torch.bfloat16, device="cuda")  # block of 24 tokens
     with pytest.raises(fa.FAError) as e:
-        fa.decode_paged(q, kc, kc, t, ln, 16)
+        fa.decode_paged(q, kc, kc, t, ln, 16, kernel=_KERNEL["which"])
     assert e.value.status == fa.FA_ERR_UNSUPPORTED
 
 
