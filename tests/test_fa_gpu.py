@@ -92,7 +92,11 @@ def full_case(B, H, Sq, Sk, d, dtype, mask, window=0, seed=0, spiky=False, scale
     o, lse = run_gpu(inp, scale=sc)
     qf, kf, vf = inp.f64()
     o_ref, lse_ref = oracle.attention(qf, kf, vf, sc, mask, window)
-    return compare(o, lse, o_ref, lse_ref, dtype), (o, lse, o_ref, lse_ref)
+    # spiky keys: the large-running-max workload, judged like it on the
+    # half-ulp-adjusted max (its dominant weights make |O| approach 4, where
+    # the bf16 rounding of P and O alone comes within a hair of 1e-2)
+    raw = False if (spiky and dtype == inputs.BF16) else None
+    return compare(o, lse, o_ref, lse_ref, dtype, raw_max=raw), (o, lse, o_ref, lse_ref)
 
 
 # ---------------------------------------------------------------------------
