@@ -274,14 +274,6 @@ fa_status launch(const Params &p, int num_sms, DeviceInfo &info, cudaStream_t st
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!info.attr_set[slot]) {
-            // The warpgroups' register split (setmaxnreg) hands out exactly
-            // the registers the CTA is launched with; a kernel built with
-            // fewer per thread would leave the increase waiting, so refuse it.
-            cudaFuncAttributes fa_attr;
-            if (cudaFuncGetAttributes(&fa_attr, kern) != cudaSuccess) return FA_ERR_CUDA;
-            if ((long long)fa_attr.numRegs * C::NUM_THREADS <
-                256LL * (C::REG_SOFTMAX + C::REG_OTHER))
-                return FA_ERR_UNSUPPORTED;
             if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::SMEM_BYTES) != cudaSuccess)
                 return FA_ERR_CUDA;
@@ -437,9 +429,9 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
                   "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=2 softmax_wgs=2 "
-                  "epilogue_wg=1 q_buffers=%d k_slots=%d v_slots=%d threads=%d smem=%d mask=%s persistent",
-                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), d <= 128 ? 2 : 1,
-                  fa::k_slots_for(d), fa::v_slots_for(d), fa::Cfg<128>::NUM_THREADS,
+                  "k_slots=%d v_slots=%d threads=%d smem=%d mask=%s persistent",
+                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::k_slots_for(d), fa::v_slots_for(d),
+                  fa::Cfg<128>::NUM_THREADS,
                   d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES
                                                                : fa::Cfg<256>::SMEM_BYTES,
                   masks[mask_kind]);

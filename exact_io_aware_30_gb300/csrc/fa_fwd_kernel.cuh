@@ -29,15 +29,8 @@
 //     columns sit in one quad of threads, so max and sum take two shuffles
 //     and the warps never synchronise during a unit; they mask boundary
 //     tiles, exponentiate, write P (16-bit), rescale O in tensor memory when
-//     the reference max moves, and at the end of a unit hand each row's sums
-//     and reference max to the epilogue warps;
-//   * warps 12-15 are the epilogue: O / l, one row per thread, through the
-//     unit's own Q buffer (free once its last S is done) and a bulk tensor
-//     store for d <= 128, straight rows for d = 256, and lse -- while the
-//     softmax warps already work on the next unit, whose Q (second buffer)
-//     is resident before the unit starts.
-// The softmax warpgroups run with more registers than the others
-// (setmaxnreg).
+//     the reference max moves, and run the epilogue (O / l through a bulk
+//     tensor store for d <= 128, and lse).
 //
 // Rescaling is deferred until the running max has grown by more than 2^8
 // (log2 units).  Until then the accumulator and the sums both stay referenced
@@ -112,30 +105,16 @@ struct Cfg {
     static constexpr int HALF = BN / 2;                  // key columns per softmax warpgroup
     static constexpr int KST = (D == 64) ? 8 : 3;
     static constexpr int VST = (D == 64) ? 4 : 2;
-    // Q buffers: d <= 128 keeps two, so that the next unit's Q is resident
-    // before the current unit ends; the finished unit's Q buffer then serves
-    // as the staging tile of its O.  d = 256 has room for one (its O rows go
-    // straight to device memory).
-    static constexpr int QBUF = (D <= 128) ? 2 : 1;
     // Warps 0-7: two softmax warpgroups (warpgroup h owns key columns
     // [h*HALF, (h+1)*HALF) of every tile, all 128 rows); warp 8: S MMAs;
-    // warp 9: P V MMAs; warp 10: TMA of Q and K; warp 11: TMA of V;
-    // warps 12-15: the epilogue (O / l, the O store and lse of each unit,
-    // one row per thread), which overlaps the next unit's first tiles.
+    // warp 9: P V MMAs; warp 10: TMA of Q and K; warp 11: TMA of V.
     static constexpr int NUM_SOFTMAX = 256;
-    static constexpr int NUM_EPI = 128;
-    static constexpr int NUM_WARPS = 16;
+    static constexpr int NUM_WARPS = 12;
     static constexpr int NUM_THREADS = 32 * NUM_WARPS;
     static constexpr int S_WARP = 8;
     static constexpr int PV_WARP = 9;
     static constexpr int TMA_WARP = 10;
     static constexpr int TMA_V_WARP = 11;
-    static constexpr int EPI_WARP0 = 12;
-    // Register split (setmaxnreg, per warpgroup): the softmax warpgroups get
-    // REG_SOFTMAX per thread, the issuer/producer and epilogue warpgroups
-    // REG_OTHER; 256 * (REG_SOFTMAX + REG_OTHER) = the 64K registers of the SM.
-    static constexpr uint32_t REG_SOFTMAX = 184;
-    static constexpr uint32_t REG_OTHER = 72;
     static constexpr int CHUNKS = D / 64;              // 64-column (128-byte) boxes per row
     static constexpr int Q_CHUNK = kBM * 128;          // bytes of one Q box
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
@@ -150,9 +129,9 @@ struct Cfg {
     static constexpr uint32_t P_COL0 = 384;
     static constexpr uint32_t P_STRIDE = 64;
     // Barrier indices.
-    static constexpr int B_QFULL = 0;                   // [QBUF]: Q buffer loaded
-    static constexpr int B_QEMPTY = B_QFULL + QBUF;     // [QBUF]: Q buffer free again
-    static constexpr int B_KFULL = B_QEMPTY + QBUF;     // [KST]: K slot loaded
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_QEMPTY = 1;
+    static constexpr int B_KFULL = 2;                   // [KST]: K slot loaded
     static constexpr int B_KEMPTY = B_KFULL + KST;      // [KST]: K slot read by its S MMAs
     static constexpr int B_VFULL = B_KEMPTY + KST;      // [VST]: V slot loaded
     static constexpr int B_VEMPTY = B_VFULL + VST;      // [VST]: V slot read by its P V MMAs
@@ -164,18 +143,19 @@ struct Cfg {
     static constexpr int B_OFREE = B_OFINAL + 1;        // epilogue has read O
     static constexpr int B_DRAIN = B_OFREE + 1;         // [2]: each issuer's MMAs finished
     static constexpr int B_NEVER = B_DRAIN + 2;         // no arrivals (the stall test's wait)
-    static constexpr int B_STATS = B_NEVER + 1;         // one phase per unit: row statistics written
-    static constexpr int B_XFREE = B_STATS + 1;         // one phase per unit: statistics read
-    static constexpr int NUM_BARS = B_XFREE + 1;
-    static constexpr int SMEM_TILES = QBUF * Q_BYTES + (KST + VST) * TILE_BYTES;
-    static constexpr int XCH_BYTES = 3 * kBM * 4;  // per row: the two sums and the reference max
+    static constexpr int NUM_BARS = B_NEVER + 1;
+    // d <= 128: the epilogue stages the normalised O tile (the Q tile's shape)
+    // in shared memory for one bulk tensor store; d = 256 has no room for it
+    // and stores rows directly.
+    static constexpr int O_STAGE_BYTES = (D <= 128) ? Q_BYTES : 0;
+    static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES + O_STAGE_BYTES;
+    static constexpr int XCH_BYTES = 3 * kBM * 4;  // per row: two sums and the reference max
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 24 + XCH_BYTES;
     static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
                   "tensor memory overflow");
     static_assert(BN / 2 <= (int)P_STRIDE, "P areas overlap");
     static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
-    static_assert(256 * (REG_SOFTMAX + REG_OTHER) <= 65536, "register split over the SM's file");
 };
 
 // ---------------------------------------------------------------- helpers
@@ -248,45 +228,6 @@ __device__ __noinline__ void wait_bar_drain(uint32_t bar, uint32_t parity) {
     }
 }
 
-// The forward kernel's waits: the same bounded waits, inlined.  Every call
-// in the forward kernel is inlined because its warpgroups run with different
-// register budgets (setmaxnreg), which a call to a separately compiled
-// function would not allow.
-__device__ __forceinline__ bool fwd_wait(uint32_t bar, uint32_t parity, Ctl *ctl, int site) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (;;) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (ctl->abort) return false;
-        if (ptx::globaltimer_ns() - t0 > ctl->limit_ns) {
-            ctl->abort = 1;
-            atomicCAS(&g_fa_status, 0, 0x100 + site);
-            return false;
-        }
-    }
-}
-
-__device__ __forceinline__ bool fwd_wait_backoff(uint32_t bar, uint32_t parity, Ctl *ctl, int site) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    for (;;) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-        if (ctl->abort) return false;
-        if (ptx::globaltimer_ns() - t0 > ctl->limit_ns) {
-            ctl->abort = 1;
-            atomicCAS(&g_fa_status, 0, 0x100 + site);
-            return false;
-        }
-        __nanosleep(256);
-    }
-}
-
-__device__ __forceinline__ void fwd_wait_drain(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) return;
-    }
-}
-
 // Unit k of this CTA (n_units once the CTA has no more): from the host's
 // schedule, or else in a snake order (even rounds left to right, odd rounds
 // right to left, so that with units sorted longest-first each CTA's sum of
@@ -351,7 +292,7 @@ __device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *rin
                                              Ctl *ctl) {
     using C = Cfg<D>;
     const uint32_t slot = it % (uint32_t)nslots;
-    if (!fwd_wait_backoff(bar_addr(bars, empty0 + (int)slot), ((it / (uint32_t)nslots) & 1) ^ 1,
+    if (!wait_bar_backoff(bar_addr(bars, empty0 + (int)slot), ((it / (uint32_t)nslots) & 1) ^ 1,
                           ctl, 2))
         return false;
     if (leader) {
@@ -371,7 +312,7 @@ __device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *rin
 __device__ __forceinline__ void drain_ring(uint32_t bars, int full0, int nslots, uint32_t it) {
     for (int sl = 0; sl < nslots; ++sl) {
         const uint32_t fills = it > (uint32_t)sl ? (it - (uint32_t)sl + nslots - 1) / (uint32_t)nslots : 0u;
-        if (fills) fwd_wait_drain(bar_addr(bars, full0 + sl), (fills - 1) & 1);
+        if (fills) wait_bar_drain(bar_addr(bars, full0 + sl), (fills - 1) & 1);
     }
 }
 
@@ -392,17 +333,14 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
-        // Q buffer qb of this unit, and the fill of it this is (a buffer is
-        // free again once the unit before last that used it has ended).
-        const uint32_t qb = q_cnt % (uint32_t)C::QBUF, qfill = q_cnt / (uint32_t)C::QBUF;
-        if (!fwd_wait_backoff(bar_addr(bars, C::B_QEMPTY + (int)qb), (qfill & 1) ^ 1, ctl, 1)) {
+        if (!wait_bar_backoff(bar_addr(bars, C::B_QEMPTY), (q_cnt & 1) ^ 1, ctl, 1)) {
             ok = false;
             break;
         }
         if (leader) {
-            const uint32_t fb = bar_addr(bars, C::B_QFULL + (int)qb);
+            const uint32_t fb = bar_addr(bars, C::B_QFULL);
             ptx::mbar_arrive_expect_tx(fb, C::Q_BYTES);
-            const uint32_t dst = ptx::smem_addr(sQ + qb * C::Q_BYTES);
+            const uint32_t dst = ptx::smem_addr(sQ);
 #pragma unroll
             for (int c = 0; c < C::CHUNKS; ++c)
                 ptx::tma_load_4d(dst + c * C::Q_CHUNK, &p.tm_q, fb, c * 64, un.i0, un.h, un.b, pol_q);
@@ -414,7 +352,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
     }
     if (!ok) {  // let every copy already issued land before the CTA can exit
         drain_ring(bars, C::B_KFULL, C::KST, k_it);
-        drain_ring(bars, C::B_QFULL, C::QBUF, q_cnt);
+        if (q_cnt) wait_bar_drain(bar_addr(bars, C::B_QFULL), (q_cnt - 1) & 1);
     }
 }
 
@@ -449,7 +387,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
     constexpr int BN = C::BN;
     constexpr uint32_t kIdescS = make_idesc(kBM, BN, kFP16, false);
     const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
-    const uint32_t q_addr = ptx::smem_addr(sQ);
+    const uint64_t dq = smem_desc(ptx::smem_addr(sQ), 16);
     const uint32_t k_addr = ptx::smem_addr(sK);
     uint32_t k_it = 0;   // K tiles consumed
     uint32_t t_cnt = 0;  // key tiles issued (S buffer = t & 1)
@@ -462,22 +400,17 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
-        const uint32_t qb = q_cnt % (uint32_t)C::QBUF;
-        if (!fwd_wait(bar_addr(bars, C::B_QFULL + (int)qb), (q_cnt / (uint32_t)C::QBUF) & 1, ctl, 6)) {
-            ok = false;
-            break;
-        }
-        const uint64_t dq = smem_desc(q_addr + qb * C::Q_BYTES, 16);
+        if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, ctl, 6)) { ok = false; break; }
         for (int i = 0; i < n; ++i, ++k_it) {
             const uint32_t t = t_cnt + (uint32_t)i;
             const uint32_t slot = k_it % C::KST;
             const uint32_t b = t & 1u;
-            if (!fwd_wait(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, ctl, 3)) {
+            if (!wait_bar(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, ctl, 3)) {
                 ok = false;
                 break;
             }
             if (t >= 2 &&  // the softmax has read tile t-2 out of this buffer
-                !fwd_wait(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1u) & 1u, ctl, 12)) {
+                !wait_bar(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1u) & 1u, ctl, 12)) {
                 ok = false;
                 break;
             }
@@ -493,9 +426,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
                     ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
-                // With one Q buffer it is free once the unit's last S has read
-                // it; with two, the epilogue frees it after staging O there.
-                if (C::QBUF == 1 && i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));
+                if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
                 ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + (int)slot));
             }
             __syncwarp();
@@ -506,7 +437,7 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
     }
     if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
     __syncwarp();
-    fwd_wait_drain(bar_addr(bars, C::B_DRAIN), 0);
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
 }
 
 // P V issuer: O (+)= P V for every key tile, as soon as the softmax has
@@ -536,7 +467,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
         for (int i = 0; i < n; ++i, ++v_it) {
             const uint32_t t = t_cnt + (uint32_t)i;
             const uint32_t slot = v_it % C::VST;
-            if (!fwd_wait(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, ctl, 3)) {
+            if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, ctl, 3)) {
                 ok = false;
                 break;
             }
@@ -544,13 +475,13 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
             // two tiles, and the softmax cannot write P of tile t+2 before this
             // P V has run, so the parity wait is unambiguous.
             const uint32_t pb = t & 1u;
-            if (!fwd_wait(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, ctl, 4)) {
+            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, ctl, 4)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             if (i == 0 && o_used) {
-                if (!fwd_wait(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, ctl, 5)) {
+                if (!wait_bar(bar_addr(bars, C::B_OFREE), ofree_cnt & 1, ctl, 5)) {
                     ok = false;
                     break;
                 }
@@ -577,7 +508,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
     }
     if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN + 1));
     __syncwarp();
-    fwd_wait_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
 }
 
 // ---------------------------------------------------------------- softmax role
@@ -587,12 +518,14 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
 // tcgen05 shapes, thread t holds rows t/4 and t/4 + 8 of that block; a row's
 // columns are spread over the 4 threads of a quad, so its max and sum are
 // combined with two shuffles and the softmax warps never wait for one another
-// during a unit.  At the end of a unit they hand each row's sums and
-// reference max to the epilogue warps through shared memory and go straight
-// on to the next unit.  The epilogue warps (12-15) use the one-row-per-thread
-// 32x32b shape: warp 12 + w reads TMEM lanes 32 w .. 32 w + 31.
-// Barrier of the 128 epilogue threads around the staged O tile.
-constexpr uint32_t kEpilogueBar = 1;
+// during a unit.  The epilogue uses the one-row-per-thread 32x32b shape (warp
+// w: rows 32 (w & 3) + lane, O columns half w >> 2), so the two warps that own
+// a 32-row block meet once per unit on named barrier 1 + (w & 3) to hand each
+// other the row sums.
+constexpr uint32_t kPairBar0 = 1;
+constexpr uint32_t kPairThreads = 64;
+// Barrier of all 256 softmax threads around the staged O tile.
+constexpr uint32_t kEpilogueBar = 5;
 
 template <bool kFP16>
 __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
@@ -706,8 +639,114 @@ __device__ __forceinline__ float quad_sum(float v) {
     return v;
 }
 
+// A unit's epilogue: wait for its last P V; full-row sums over the quad,
+// handed through shared memory to the one-row-per-thread layout; divide by l
+// once; store this warp's half of the O row (and lse).
 template <int D, bool kFP16>
-__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch, Ctl *ctl) {
+__device__ __noinline__ void softmax_epilogue(const Params &p, uint32_t bars, Ctl *ctl, float *xch,
+                                              uint8_t *sO, uint32_t o_tmem, uint32_t u_cnt, int i0,
+                                              int hd, int bt, size_t row_flat, bool row_ok,
+                                              uint8_t *ohalf, float m_a, float m_b, float l_a,
+                                              float l_b, float le_a, float le_b) {
+    using C = Cfg<D>;
+    const int warp = (int)(threadIdx.x >> 5), t = (int)(threadIdx.x & 31);
+    const int qw = warp & 3, hh = warp >> 2;
+    const int tq = t & 3;
+    const int ra = 32 * qw + 16 * hh + (t >> 2), rb = ra + 8;
+    const int re = 32 * qw + t;
+    const uint32_t pair_bar = kPairBar0 + (uint32_t)qw;
+    float *xl = xch, *xle = xch + kBM, *xm = xch + 2 * kBM;
+    wait_bar(bar_addr(bars, C::B_OFINAL), u_cnt & 1u, ctl, 9);  // u_cnt: units finished before
+    ptx::tc_fence_after();
+    {
+        const float sa = quad_sum(l_a), sb = quad_sum(l_b);
+        const float ea = kFP16 ? sa : quad_sum(le_a), eb = kFP16 ? sb : quad_sum(le_b);
+        ptx::named_bar_sync(pair_bar, kPairThreads);  // the previous unit's values fully read
+        if (tq == 0) {
+            xl[ra] = sa;
+            xl[rb] = sb;
+            xle[ra] = ea;
+            xle[rb] = eb;
+            xm[ra] = m_a;
+            xm[rb] = m_b;
+        }
+        ptx::named_bar_sync(pair_bar, kPairThreads);
+    }
+    const float l_all = xl[re], le_all = xle[re], m_ref = xm[re];
+    const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
+    if constexpr (C::O_STAGE_BYTES > 0) {
+        // Normalise this thread's D/2 columns of O into registers, release
+        // O to the next unit's P V, then stage the tile in shared memory in
+        // the tensor map's layout (64-column boxes of 128-byte rows, 16-byte
+        // chunks swizzled by row & 7) and write it with one bulk store.
+        // Rows past Sq fall outside the tensor and are not written.
+        uint32_t w[D / 4];
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(ov);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[cc * 16 + e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
+                                              __uint_as_float(ov[2 * e + 1]) * inv_l);
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+        const uint32_t so = ptx::smem_addr(sO);
+        if (threadIdx.x == 0) ptx::bulk_wait_read_all();  // the previous tile has left sO
+        ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
+#pragma unroll
+        for (int cidx = 0; cidx < D / 16; ++cidx) {
+            const int col = hh * (D / 2) + cidx * 8;  // first of the chunk's 8 columns
+            const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + re * 128 +
+                                                  ((((col & 63) >> 3) ^ (re & 7)) << 4));
+            ptx::st_shared_v4(addr, w[4 * cidx], w[4 * cidx + 1], w[4 * cidx + 2], w[4 * cidx + 3]);
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::named_bar_sync(kEpilogueBar, C::NUM_SOFTMAX);
+        if (threadIdx.x == 0) {
+#pragma unroll
+            for (int bx = 0; bx < D / 64; ++bx)
+                ptx::tma_store_4d(&p.tm_o, so + bx * (kBM * 128), bx * 64, i0, hd, bt);
+            ptx::bulk_commit_group();
+        }
+    } else {
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32<0>(o_tmem + cc * 32, ov);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(ov);
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                w[e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
+                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
+            if (row_ok) {
+                uint8_t *dst = ohalf + cc * 64;
+                if (p.o_vec8) {
+                    ptx::st_global_v8(dst, *reinterpret_cast<const uint32_t(*)[8]>(&w[0]));
+                    ptx::st_global_v8(dst + 32, *reinterpret_cast<const uint32_t(*)[8]>(&w[8]));
+                } else {
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4)
+                        ptx::st_global_v4(dst + v4 * 16, w[4 * v4], w[4 * v4 + 1], w[4 * v4 + 2],
+                                          w[4 * v4 + 3]);
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
+    }
+    if (row_ok && hh == 0)
+        p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
+}
+
+template <int D, bool kFP16>
+__device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, float *xch, uint8_t *sO,
+                             Ctl *ctl) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
     constexpr int NR = BN / 2;  // registers of one S tile per thread: 2 rows x BN/4 columns
@@ -719,16 +758,30 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
     const int rb = ra + 8;
     const uint32_t blk = tmem + ((uint32_t)rblk << 16);
     const uint32_t o_blk = blk + C::O_COL0;   // all O columns of the 16 rows (rescales)
-    float *xl = xch, *xle = xch + kBM, *xm = xch + 2 * kBM;
+    const int re = 32 * qw + t;               // row of the one-row-per-thread epilogue
+    const uint32_t o_tmem = tmem + ((uint32_t)(32 * qw) << 16) + C::O_COL0 + (uint32_t)(hh * (D / 2));
     const float c = p.scale_log2;
     uint32_t t_cnt = 0;  // key tiles processed (S buffer = t & 1; one P V each)
-    uint32_t u_cnt = 0;  // units completed (one statistics hand-over each)
+    uint32_t u_cnt = 0;  // units completed (one O-final phase each)
 
     for (int k = 0;; ++k) {
         const int u = unit_at(k, p);
         if (u >= p.n_units) break;
         const Unit un = decode_unit<D>(u, p);
-        if (!un.valid) continue;  // no key visible to any row: the epilogue writes the guard
+        const int row_e = un.i0 + re;
+        const bool row_ok = row_e < p.Sq;
+        const size_t head = (size_t)(un.b * p.H + un.h) * (size_t)p.Sq;
+        const size_t row_flat = head + (size_t)row_e;
+        uint8_t *ohalf = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2 + (size_t)(hh * D);
+        if (!un.valid) {
+            // No key visible to any row of this tile: guarded output.
+            if (row_ok) {
+#pragma unroll
+                for (int cc = 0; cc < D / 16; ++cc) ptx::st_global_v4(ohalf + cc * 16, 0, 0, 0, 0);
+                if (hh == 0) p.lse[row_flat] = -INFINITY;
+            }
+            continue;
+        }
         // Visible keys of rows a and b: absolute key indices [lo, hi].
         const int row_a = un.i0 + ra, row_b = un.i0 + rb;
         const int hi_a = (p.mask_kind == kMaskNone) ? p.Sk - 1 : min(row_a, p.Sk - 1);
@@ -749,7 +802,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // (Under the stall test the CTA's first wait is on a barrier no one
             // arrives at: it runs out, and the kernel winds down with the
             // device status word set.)
-            fwd_wait(bar_addr(bars, (p.stall_test && tt == 0) ? C::B_NEVER : C::B_SFULL + b),
+            wait_bar(bar_addr(bars, (p.stall_test && tt == 0) ? C::B_NEVER : C::B_SFULL + b),
                      (tt >> 1) & 1u, ctl, 7);
             ptx::tc_fence_after();
             uint32_t sr[NR];
@@ -814,17 +867,15 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // O barrier b completes once for each tile whose P sits in area b:
             // completion k of barrier t & 1 is P V of tile t with k = t >> 1.
             // Rescaling O needs every earlier P V finished: wait for P V of tile
-            // t-1 (a commit covers all earlier MMAs of its issuer; a rescale
-            // never happens on a unit's first tile, so tile t-1 is of this
-            // unit, and its P V followed the epilogue's read of the previous
-            // unit's O).  Rewriting P area t & 1 needs P V of tile t-2.  Each
-            // barrier's next completion needs a P this thread has not written
-            // yet, and the one before was waited for two tiles ago, so the
-            // parity waits are unambiguous.
+            // t-1 (a commit covers all earlier MMAs of its issuer).  Rewriting P
+            // area t & 1 needs P V of tile t-2.  The P V of the previous unit
+            // are covered by its final barrier.  Each barrier's next completion
+            // needs a P this thread has not written yet, and the one before was
+            // waited for two tiles ago, so the parity waits are unambiguous.
             const uint32_t pb = tt & 1u;
             if (rescale) {  // warp-uniform
                 if (i > 0)
-                    fwd_wait(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u,
+                    wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u,
                              ctl, 8);
                 ptx::tc_fence_after();
 #pragma unroll
@@ -843,11 +894,8 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             l_b = alpha_b * l_b + lr_bt;
             le_a = alpha_a * le_a + le_at;
             le_b = alpha_b * le_b + le_bt;
-            // P area tt & 1 was last read by P V of tile tt - 2, possibly in
-            // the previous unit (the softmax no longer waits for a unit's
-            // last P V: the epilogue warps do).
-            if (tt >= 2)
-                fwd_wait(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, ctl, 10);
+            if (i >= 2)
+                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, ctl, 10);
             ptx::tc_fence_after();
             if constexpr (NR == 64)
                 ptx::tmem_st_16x128b_x16<0>(blk + C::P_COL0 + pb * C::P_STRIDE, pk);
@@ -858,125 +906,14 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + (int)pb));
         }
 
-        // Hand the unit's row statistics to the epilogue: full-row sums over
-        // the quad, written once the epilogue has read the previous unit's.
-        // Completion k of the free barrier is the epilogue's read of unit k,
-        // and unit k + 1's statistics cannot be read before they are
-        // written, so the parity waits are unambiguous.
-        {
-            const float sa = quad_sum(l_a), sb = quad_sum(l_b);
-            const float ea = kFP16 ? sa : quad_sum(le_a), eb = kFP16 ? sb : quad_sum(le_b);
-            if (u_cnt > 0) fwd_wait(bar_addr(bars, C::B_XFREE), (u_cnt - 1u) & 1u, ctl, 13);
-            if (tq == 0) {
-                xl[ra] = sa;
-                xl[rb] = sb;
-                xle[ra] = ea;
-                xle[rb] = eb;
-                xm[ra] = m_a;
-                xm[rb] = m_b;
-            }
-            ptx::mbar_arrive(bar_addr(bars, C::B_STATS));  // release: the writes above come first
-        }
+        // Epilogue, out of line: it runs once per unit, and keeping it out of
+        // the tile loop keeps the loop's code compact.
+        softmax_epilogue<D, kFP16>(p, bars, ctl, xch, sO, o_tmem, u_cnt, un.i0, un.h, un.b, row_flat,
+                                   row_ok, ohalf, m_a, m_b, l_a, l_b, le_a, le_b);
         ++u_cnt;
     }
-}
-
-// Epilogue warp 12 + w owns row 32 w + lane of every query tile (TMEM lane
-// = row in the 32x32b shape).  Per unit: wait for the softmax's row
-// statistics and for the last P V, read the row of O chunk by chunk, divide
-// by l once, release O to the next unit's P V, and store the row -- for
-// d <= 128 into the unit's (now unused) Q buffer in the tensor map's layout
-// (64-column boxes of 128-byte rows, 16-byte chunks swizzled by row & 7), then
-// one bulk tensor store; for d = 256 straight to device memory -- and lse.
-// Units no key is visible to get O = 0 and lse = -inf (the guarded row).
-template <int D, bool kFP16>
-__device__ void epilogue_role(const Params &p, uint8_t *sQ, uint32_t bars, uint32_t tmem,
-                              const float *xch, Ctl *ctl) {
-    using C = Cfg<D>;
-    const int warp = (int)(threadIdx.x >> 5), t = (int)(threadIdx.x & 31);
-    const int ew = warp & 3;
-    const int re = 32 * ew + t;
-    const bool elected = (warp == C::EPI_WARP0) && t == 0;
-    const uint32_t o_tmem = tmem + ((uint32_t)(32 * ew) << 16) + C::O_COL0;
-    const float *xl = xch, *xle = xch + kBM, *xm = xch + 2 * kBM;
-    uint32_t v_cnt = 0;  // units with keys handled (one statistics, O-final and Q phase each)
-
-    for (int k = 0;; ++k) {
-        const int u = unit_at(k, p);
-        if (u >= p.n_units) break;
-        const Unit un = decode_unit<D>(u, p);
-        const int row_e = un.i0 + re;
-        const bool row_ok = row_e < p.Sq;
-        const size_t row_flat = (size_t)(un.b * p.H + un.h) * (size_t)p.Sq + (size_t)row_e;
-        uint8_t *orow = reinterpret_cast<uint8_t *>(p.o) + row_flat * D * 2;
-        if (!un.valid) {
-            if (row_ok) {
-#pragma unroll
-                for (int cc = 0; cc < D / 8; ++cc) ptx::st_global_v4(orow + cc * 16, 0, 0, 0, 0);
-                p.lse[row_flat] = -INFINITY;
-            }
-            continue;
-        }
-        fwd_wait(bar_addr(bars, C::B_STATS), v_cnt & 1u, ctl, 14);
-        const float l_all = xl[re], le_all = xle[re], m_ref = xm[re];
-        ptx::mbar_arrive(bar_addr(bars, C::B_XFREE));
-        fwd_wait(bar_addr(bars, C::B_OFINAL), v_cnt & 1u, ctl, 9);
-        ptx::tc_fence_after();
-        const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
-        const uint32_t qb = v_cnt % (uint32_t)C::QBUF;
-        const uint32_t so = ptx::smem_addr(sQ + qb * C::Q_BYTES);
-#pragma unroll
-        for (int cc = 0; cc < D / 16; ++cc) {  // 16 columns of the row at a time
-            uint32_t ov[16];
-            ptx::tmem_ld_x16<0>(o_tmem + cc * 16, ov);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<16>(ov);
-            if (cc == D / 16 - 1) {  // every column of O read: the next unit's P V may start
-                ptx::tc_fence_before();
-                ptx::mbar_arrive(bar_addr(bars, C::B_OFREE));
-            }
-            uint32_t w[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                w[e] = pack2<kFP16>(__uint_as_float(ov[2 * e]) * inv_l,
-                                    __uint_as_float(ov[2 * e + 1]) * inv_l);
-            if constexpr (C::QBUF == 2) {
-#pragma unroll
-                for (int c8 = 0; c8 < 2; ++c8) {
-                    const int col = cc * 16 + c8 * 8;  // first of the 16-byte chunk's 8 columns
-                    const uint32_t addr = so + (uint32_t)((col >> 6) * (kBM * 128) + re * 128 +
-                                                          ((((col & 63) >> 3) ^ (re & 7)) << 4));
-                    ptx::st_shared_v4(addr, w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
-                }
-            } else if (row_ok) {
-                uint8_t *dst = orow + cc * 32;
-                if (p.o_vec8) {
-                    ptx::st_global_v8(dst, w);
-                } else {
-                    ptx::st_global_v4(dst, w[0], w[1], w[2], w[3]);
-                    ptx::st_global_v4(dst + 16, w[4], w[5], w[6], w[7]);
-                }
-            }
-        }
-        if constexpr (C::QBUF == 2) {
-            // Rows past Sq fall outside the tensor and are not written.  Once
-            // the store has read the tile, the Q buffer may take a new Q.
-            ptx::fence_proxy_async_smem();
-            ptx::named_bar_sync(kEpilogueBar, C::NUM_EPI);
-            if (elected) {
-#pragma unroll
-                for (int bx = 0; bx < D / 64; ++bx)
-                    ptx::tma_store_4d(&p.tm_o, so + bx * (kBM * 128), bx * 64, un.i0, un.h, un.b);
-                ptx::bulk_commit_group();
-                ptx::bulk_wait_read_all();
-                ptx::mbar_arrive(bar_addr(bars, C::B_QEMPTY + (int)qb));
-            }
-        }
-        if (row_ok) p.lse[row_flat] = (le_all > 0.f) ? (m_ref + log2f(le_all)) * kLn2 : -INFINITY;
-        ++v_cnt;
-    }
-    if constexpr (C::QBUF == 2) {
-        if (elected) ptx::bulk_wait_all();  // the staged tiles must outlive the stores
+    if constexpr (C::O_STAGE_BYTES > 0) {
+        if (threadIdx.x == 0) ptx::bulk_wait_all();  // sO must outlive the stores
     }
 }
 
@@ -989,9 +926,10 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *sQ = smem;                          // QBUF Q tiles (each also stages its unit's O)
-    uint8_t *sK = smem + C::QBUF * C::Q_BYTES;
+    uint8_t *sQ = smem;
+    uint8_t *sK = smem + C::Q_BYTES;
     uint8_t *sV = sK + C::KST * C::TILE_BYTES;
+    uint8_t *sO = sV + C::VST * C::TILE_BYTES;  // O staging (d <= 128)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);    // 8-byte aligned
@@ -1002,10 +940,8 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     const uint32_t lane = ptx::lane_id();
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < C::QBUF; ++b) {
-            ptx::mbar_init(bar_addr(bars, C::B_QFULL + b), 1);
-            ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + b), 1);
-        }
+        ptx::mbar_init(bar_addr(bars, C::B_QFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_QEMPTY), 1);
         for (int s = 0; s < C::KST; ++s) {
             ptx::mbar_init(bar_addr(bars, C::B_KFULL + s), 1);
             ptx::mbar_init(bar_addr(bars, C::B_KEMPTY + s), 1);
@@ -1023,12 +959,10 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
             ptx::mbar_init(bar_addr(bars, C::B_OFULL + b), 1);
         }
         ptx::mbar_init(bar_addr(bars, C::B_OFINAL), 1);
-        ptx::mbar_init(bar_addr(bars, C::B_OFREE), C::NUM_EPI);
+        ptx::mbar_init(bar_addr(bars, C::B_OFREE), C::NUM_SOFTMAX);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
         ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
-        ptx::mbar_init(bar_addr(bars, C::B_STATS), C::NUM_SOFTMAX);
-        ptx::mbar_init(bar_addr(bars, C::B_XFREE), C::NUM_EPI);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
         ptx::fence_mbar_init();
@@ -1042,30 +976,23 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         ptx::prefetch_tensormap(&p.tm_q);
         ptx::prefetch_tensormap(&p.tm_k);
         ptx::prefetch_tensormap(&p.tm_v);
-        if (C::QBUF == 2) ptx::prefetch_tensormap(&p.tm_o);
+        if (C::O_STAGE_BYTES > 0) ptx::prefetch_tensormap(&p.tm_o);
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    // Register split: every warp of a warpgroup runs the same setmaxnreg.
     if (warp < C::NUM_SOFTMAX / 32) {
-        ptx::setmaxnreg_inc<C::REG_SOFTMAX>();
-        softmax_role<D, kFP16>(p, bars, tmem, xch, ctl);
+        softmax_role<D, kFP16>(p, bars, tmem, xch, sO, ctl);
+    } else if (warp == C::S_WARP) {
+        mma_s_role<D, kFP16>(p, sQ, sK, bars, tmem, ctl);
+    } else if (warp == C::PV_WARP) {
+        mma_pv_role<D, kFP16>(p, sV, bars, tmem, ctl);
+    } else if (warp == C::TMA_WARP) {
+        tma_qk_role<D>(p, sQ, sK, bars, ctl);
     } else {
-        ptx::setmaxnreg_dec<C::REG_OTHER>();
-        if (warp == C::S_WARP) {
-            mma_s_role<D, kFP16>(p, sQ, sK, bars, tmem, ctl);
-        } else if (warp == C::PV_WARP) {
-            mma_pv_role<D, kFP16>(p, sV, bars, tmem, ctl);
-        } else if (warp == C::TMA_WARP) {
-            tma_qk_role<D>(p, sQ, sK, bars, ctl);
-        } else if (warp == C::TMA_V_WARP) {
-            tma_v_role<D>(p, sV, bars, ctl);
-        } else {
-            epilogue_role<D, kFP16>(p, sQ, bars, tmem, xch, ctl);
-        }
+        tma_v_role<D>(p, sV, bars, ctl);
     }
     __syncwarp();
     ptx::tc_fence_before();
