@@ -42,6 +42,7 @@ struct DeviceInfo {
     bool attr_set[6] = {false, false, false, false, false, false};
     bool attr_bwd[12] = {};  // dK/dV then dQ kernels, d = 64, 128, 256 x bf16, fp16
     void *noalloc_ws = nullptr;  // device address of g_noalloc_ws in this device's context
+    unsigned long long noalloc_ctx = 0;  // id of the context that address belongs to
     bool attr_dec[6] = {false, false, false, false, false, false};
     bool attr_fp8[3] = {false, false, false};  // 8-bit forward, d = 64, 128, 256
     bool attr_gemv[12] = {};  // few-row decode: d = 64, 128, 256 x bf16, fp16 x 1, 2 rows
@@ -96,6 +97,40 @@ fa_status device_info(int *dev_out, DeviceInfo **info) {
     *dev_out = dev;
     *info = &d;
     return d.supported ? FA_OK : FA_ERR_UNSUPPORTED;
+}
+
+// Unique id of the calling thread's current CUDA context (0 if it cannot be
+// told).  A device's context is destroyed and made anew by cudaDeviceReset;
+// addresses of device symbols looked up in the old one are then stale.
+unsigned long long current_ctx_id() {
+    typedef CUresult (*GetCurrent)(CUcontext *);
+    typedef CUresult (*GetId)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static bool probed = false;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!probed) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult qres;
+            if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                                 &qres) == cudaSuccess &&
+                qres == cudaDriverEntryPointSuccess)
+                get_current = reinterpret_cast<GetCurrent>(fn);
+            fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &qres) ==
+                    cudaSuccess &&
+                qres == cudaDriverEntryPointSuccess)
+                get_id = reinterpret_cast<GetId>(fn);
+            probed = true;
+        }
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx &&
+        get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -202,14 +202,19 @@ fa_status fa_bwd_noalloc(const void *q, const void *k, const void *v, const void
     st = fa::device_info(&dev, &info);
     if (st != FA_OK) return st;
     void *ws = nullptr;
+    const unsigned long long ctx = fa::current_ctx_id();
     {
         std::lock_guard<std::mutex> lock(fa::g_mutex);
-        if (!info->noalloc_ws) {
-            // first call on this device (which is current here): look the array up once
+        // The first call on this device (current here) looks the array up;
+        // so does the first call in a new context of the device (after a
+        // cudaDeviceReset the old address is stale).  A failed lookup is not
+        // cached: the next call tries again.
+        if (!info->noalloc_ws || (ctx != 0 && ctx != info->noalloc_ctx)) {
             void *addr = nullptr;
             if (cudaGetSymbolAddress(&addr, fa::g_noalloc_ws) != cudaSuccess || !addr)
                 return FA_ERR_CUDA;
             info->noalloc_ws = addr;
+            info->noalloc_ctx = ctx;
         }
         ws = info->noalloc_ws;
     }

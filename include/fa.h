@@ -157,8 +157,12 @@ fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, con
  *               B * H * ceil(Sq / 128) * 128 <= 4,194,304 query rows;
  *               larger problems return FA_ERR_INVALID_ARG (use fa_bwd)
  * The first call on a device looks up the array's device address (with that
- * device current) and should come before any stream capture.  Nothing is
- * allocated or freed by any call.  Every call on a device uses the same array:
+ * device current) and should come before any stream capture: under capture
+ * that lookup may fail, and the call then returns FA_ERR_CUDA having enqueued
+ * nothing; a failed lookup is not remembered, so one plain call made before
+ * the capture fixes it.  The address is looked up again in a new context of
+ * the device (after cudaDeviceReset).  Nothing is allocated or freed by any
+ * call.  Every call on a device uses the same array:
  * calls whose work overlaps in time on one device (another stream, another
  * host thread) race on it and give undefined results.
  */

@@ -75,3 +75,24 @@ def test_sizes_over_the_limit_are_refused():
                             z.data_ptr(), 1, 33, 33, 131072, 131072, 128, 0.088, fa.MASK_CAUSAL,
                             0, 0, fa.DTYPE_BF16)
     assert st == fa.FA_ERR_INVALID_ARG
+
+
+def test_a_problem_filling_the_whole_array_is_accepted_and_exact():
+    # 32768 batches of one one-row head pad to 32768 x 128 = 4,194,304 rows:
+    # exactly the 32 MiB array, so this call writes its last bytes
+    a = _problem(32768, 1, 1, 1, 64, inputs.BF16, "none", 0, seed=903)
+    got = _noalloc(a)
+    torch.cuda.synchronize()
+    ref = _with_workspace(a)
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
+    # one more batch is over the limit
+    z = torch.zeros(16, dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros(4, dtype=torch.float32, device="cuda")
+    st = fa.bwd_noalloc_raw(z.data_ptr(), z.data_ptr(), z.data_ptr(), z.data_ptr(),
+                            lse.data_ptr(), z.data_ptr(), z.data_ptr(), z.data_ptr(),
+                            z.data_ptr(), 32769, 1, 1, 1, 1, 64, 0.125, fa.MASK_NONE, 0, 0,
+                            fa.DTYPE_BF16)
+    assert st == fa.FA_ERR_INVALID_ARG
