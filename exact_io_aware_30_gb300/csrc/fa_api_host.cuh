@@ -16,8 +16,12 @@
 namespace fa {
 namespace {
 
-constexpr int kHostMaxChunks = 8;
-constexpr size_t kHostMinChunkBytes = 8u << 20;  // inputs per chunk worth a separate copy
+// Chunks: the first chunk's copy-in and the last chunk's kernel and copy-out
+// are not overlapped, so more chunks shorten that fill and drain; the
+// kernels (a quarter of the copies' time on the long workloads) absorb the
+// smaller chunks' lower efficiency.
+constexpr int kHostMaxChunks = 16;
+constexpr size_t kHostMinChunkBytes = 4u << 20;  // inputs per chunk worth a separate copy
 
 struct HostStreams {
     bool ready = false;

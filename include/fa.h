@@ -271,7 +271,7 @@ fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int b
  * and O and lse are copied back to host memory.  The arithmetic and the
  * results are those of fa_fwd_gqa (the method's "what goes in, what comes
  * out" -- "FlashAttention: IO-aware attention kernels" -- with the host
- * copies around it).  The problem is cut into up to 8 chunks of whole K/V
+ * copies around it).  The problem is cut into up to 16 chunks of whole K/V
  * heads (with the query heads that read them); chunk c+1's inputs are copied
  * in on a library stream while chunk c runs on `stream` and chunk c-1's
  * outputs are copied out on a second library stream, so the copies overlap
