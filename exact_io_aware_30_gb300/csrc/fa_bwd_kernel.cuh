@@ -170,10 +170,13 @@ struct BwdKVCfg {
     // d = 256: the dK and dV accumulators of a 128-key tile would need all 512
     // tensor-memory columns, so two CTAs share the tile, each accumulating one
     // 128-column half of dK and dV (both form S^T and dP^T over the whole d).
-    // Its K, V, Q and dO tiles leave room for one Q/dO stage only.
+    // Its K, V, Q and dO tiles leave room for one Q/dO stage only.  A stage
+    // is free only after dV and dK of its step, a step after the compute
+    // warps have seen it, so the ring runs about two stages ahead of the
+    // score products; d = 128 fits four stages, d = 64 six.
     static constexpr int DA = (D > 128) ? 128 : D;  // accumulator columns per CTA
     static constexpr int NH = D / DA;               // CTAs per key tile
-    static constexpr int ST = (D > 128) ? 1 : 3;    // stages of the (Q, dO, statistics) ring
+    static constexpr int ST = (D > 128) ? 1 : (D == 128) ? 4 : 6;  // stages of the (Q, dO, statistics) ring
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BOX = BM * 128;
     static constexpr int KV_BYTES = BN * D * 2;
@@ -605,12 +608,16 @@ struct BwdQCfg {
     static constexpr int KV_BYTES = BN * D * 2;
     // Warps 0-7 compute: warp w owns query rows 32 (w & 3) .. + 31 (its TMEM
     // lanes), one per thread, and key columns 64 (w >> 2) .. + 63 of every
-    // step; warp 8 issues the MMAs, warp 9 the copies.
+    // step; warp 8 issues S and dP, warp 9 dQ, warp 10 the copies.  A
+    // tcgen05.mma blocks its issuing thread while the tensor pipe's queue is
+    // full, so with one issuer dQ of step t waited behind the score products
+    // of step t+1 and the next score products behind dQ.
     static constexpr int NUM_COMPUTE = 256;
     static constexpr int COLS = BN / 2;
     static constexpr int MMA_WARP = 8;
-    static constexpr int TMA_WARP = 9;
-    static constexpr int NUM_THREADS = 320;
+    static constexpr int MMA_G_WARP = 9;
+    static constexpr int TMA_WARP = 10;
+    static constexpr int NUM_THREADS = 352;
     // Tensor memory: S and dP (fp32, BN columns each), the dQ accumulator,
     // dS (16-bit pairs, BN/2 columns).
     static constexpr uint32_t TMEM_COLS = 512;
@@ -628,8 +635,8 @@ struct BwdQCfg {
     static constexpr int B_PFULL = B_SFREE + 1;
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_DONE = B_PFREE + 1;
-    static constexpr int B_DRAIN = B_DONE + 1;
-    static constexpr int B_NEVER = B_DRAIN + 1;  // no arrivals (the stall test's wait)
+    static constexpr int B_DRAIN = B_DONE + 1;    // [2]: each issuer's MMAs finished
+    static constexpr int B_NEVER = B_DRAIN + 2;  // no arrivals (the stall test's wait)
     static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * Q_BYTES + (KST + VST) * KV_BYTES;
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
@@ -732,69 +739,83 @@ __device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
     }
 }
 
+// The two MMA issuers of the dQ kernel: S and dP of step t go out as soon as
+// the compute warps have read step t-1's, dQ += dS K of step t as soon as its
+// dS is written.  A K slot is free after dQ, a V slot after dP.
 template <int D, bool kFP16>
-__device__ void bwd_q_mma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
-                               uint8_t *sK, uint8_t *sV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+__device__ void bwd_q_mma_s_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
+                                 uint8_t *sK, uint8_t *sV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdQCfg<D>;
     constexpr uint32_t kIdescS = make_idesc(C::BM, C::BN, kFP16, false);
-    constexpr uint32_t kIdescG = make_idesc(C::BM, D, kFP16, true);  // dQ: N = d, K MN-major
     const bool leader = ptx::lane_id() == 0;
     const uint64_t qd = smem_desc(ptx::smem_addr(sQ), 16);
     const uint64_t od = smem_desc(ptx::smem_addr(sDO), 16);
     bool ok = un.n == 0 || wait_warp(bar_addr(bars, C::B_QFULL), 0, ctl, 32);
-    for (int t = 0; ok && t <= un.n; ++t) {
-        if (t < un.n) {
-            const int ks = t % C::KST, vs = t % C::VST;
-            if (!wait_warp(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 33) ||
-                !wait_warp(bar_addr(bars, C::B_VFULL + vs), (t / C::VST) & 1, ctl, 40)) {
-                ok = false;
-                break;
-            }
-            if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 34)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            if (leader) {
-                const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::KV_BYTES), 16);
-                const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::KV_BYTES), 16);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
-                                kIdescS, kk > 0 ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
-                                kIdescS, kk > 0 ? 1u : 0u);
-                ptx::mma_commit(bar_addr(bars, C::B_SFULL));
-                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
-            }
-            __syncwarp();
+    for (int t = 0; ok && t < un.n; ++t) {
+        const int ks = t % C::KST, vs = t % C::VST;
+        if (!wait_warp(bar_addr(bars, C::B_KFULL + ks), (t / C::KST) & 1, ctl, 33) ||
+            !wait_warp(bar_addr(bars, C::B_VFULL + vs), (t / C::VST) & 1, ctl, 40)) {
+            ok = false;
+            break;
         }
-        if (t >= 1) {
-            const int tp = t - 1, slot = tp % C::KST;
-            if (!wait_warp(bar_addr(bars, C::B_PFULL), tp & 1, ctl, 35)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            if (leader) {
-                // K as the MN-major B operand: K = keys (16 = 2048 bytes), N = d.
-                const uint64_t km = smem_desc(ptx::smem_addr(sK + slot * C::KV_BYTES), C::KV_BOX);
-#pragma unroll
-                for (int kk = 0; kk < C::BN / 16; ++kk)
-                    ptx::mma_ts(tmem + C::DQ_COL, tmem + C::DS_COL + kk * 8, km + (uint32_t)((kk * 2048) >> 4),
-                                kIdescG, (tp > 0 || kk > 0) ? 1u : 0u);
-                ptx::mma_commit(bar_addr(bars, C::B_PFREE));
-                ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + slot));
-                if (tp + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_DONE));
-            }
-            __syncwarp();
+        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 34)) {
+            ok = false;
+            break;
         }
+        ptx::tc_fence_after();
+        if (leader) {
+            const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::KV_BYTES), 16);
+            const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::KV_BYTES), 16);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
+                            kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
+                            kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
+        }
+        __syncwarp();
     }
     if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
     __syncwarp();
     wait_bar_drain(bar_addr(bars, C::B_DRAIN), 0);
+}
+
+template <int D, bool kFP16>
+__device__ void bwd_q_mma_g_role(const BwdParams &p, const QUnit &un, uint8_t *sK, uint32_t bars,
+                                 uint32_t tmem, Ctl *ctl) {
+    using C = BwdQCfg<D>;
+    constexpr uint32_t kIdescG = make_idesc(C::BM, D, kFP16, true);  // dQ: N = d, K MN-major
+    const bool leader = ptx::lane_id() == 0;
+    bool ok = true;
+    for (int t = 0; ok && t < un.n; ++t) {
+        const int slot = t % C::KST;
+        // K of step t has landed (this warp reads it too); dS of step t is written
+        if (!wait_warp(bar_addr(bars, C::B_KFULL + slot), (t / C::KST) & 1, ctl, 52) ||
+            !wait_warp(bar_addr(bars, C::B_PFULL), t & 1, ctl, 35)) {
+            ok = false;
+            break;
+        }
+        ptx::tc_fence_after();
+        if (leader) {
+            // K as the MN-major B operand: K = keys (16 = 2048 bytes), N = d.
+            const uint64_t km = smem_desc(ptx::smem_addr(sK + slot * C::KV_BYTES), C::KV_BOX);
+#pragma unroll
+            for (int kk = 0; kk < C::BN / 16; ++kk)
+                ptx::mma_ts(tmem + C::DQ_COL, tmem + C::DS_COL + kk * 8, km + (uint32_t)((kk * 2048) >> 4),
+                            kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+            ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + slot));
+            if (t + 1 == un.n) ptx::mma_commit(bar_addr(bars, C::B_DONE));
+        }
+        __syncwarp();
+    }
+    if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN + 1));
+    __syncwarp();
+    wait_bar_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
 }
 
 template <int D, bool kFP16>
@@ -812,6 +833,8 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
     const float L = p.l2[srow];      // +inf on padding rows: P = 0
     const float Dl = p.delta[srow];
     const float c = p.scale_log2;
+    const uint64_t c2 = ptx::f32x2(c, c), nl2 = ptx::f32x2(-L, -L), nd2 = ptx::f32x2(-Dl, -Dl);
+    const uint64_t mz2 = ptx::f32x2(-0.f, -0.f);
     bool ok = true;
     for (int t = 0; t < un.n; ++t) {
         const int k0 = (un.lo + t) * C::BN + h * NC;  // first key of this warp's columns
@@ -837,16 +860,24 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
         ptx::reg_fence<NC>(dp);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
+        // Packed fp32 pairs: s c - L and dP - delta as one instruction per
+        // pair each, and P (dP - delta) as an fma with -0 (the exact product,
+        // sign of zero included).
 #pragma unroll
         for (int e = 0; e < NC; e += 2) {
-            float p0 = ptx::ex2_approx(fmaf(__uint_as_float(s[e]), c, -L));
-            float p1 = ptx::ex2_approx(fmaf(__uint_as_float(s[e + 1]), c, -L));
+            float x0, x1, g0, g1, d0, d1;
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2,
+                                             nl2), x0, x1);
+            float p0 = ptx::ex2_approx(x0);
+            float p1 = ptx::ex2_approx(x1);
             if (masked) {
                 p0 = (e >= lo && e < hi) ? p0 : 0.f;
                 p1 = (e + 1 >= lo && e + 1 < hi) ? p1 : 0.f;
             }
-            w[e / 2] = pack2b<kFP16>(p0 * (__uint_as_float(dp[e]) - Dl),
-                                     p1 * (__uint_as_float(dp[e + 1]) - Dl));
+            ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2),
+                              g0, g1);
+            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(p0, p1), ptx::f32x2(g0, g1), mz2), d0, d1);
+            w[e / 2] = pack2b<kFP16>(d0, d1);
         }
         // dQ of step t-1 has read the dS area
         if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
@@ -916,6 +947,7 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
         ptx::mbar_init(bar_addr(bars, C::B_NEVER), 1);
         ctl->abort = 0;
         ctl->limit_ns = p.wait_limit_ns;
@@ -941,7 +973,9 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
     if (warp < C::NUM_COMPUTE / 32) {
         bwd_q_compute_role<D, kFP16>(p, un, bars, tmem, ctl);
     } else if (warp == C::MMA_WARP) {
-        bwd_q_mma_role<D, kFP16>(p, un, sQ, sDO, sK, sV, bars, tmem, ctl);
+        bwd_q_mma_s_role<D, kFP16>(p, un, sQ, sDO, sK, sV, bars, tmem, ctl);
+    } else if (warp == C::MMA_G_WARP) {
+        bwd_q_mma_g_role<D, kFP16>(p, un, sK, bars, tmem, ctl);
     } else {
         bwd_q_tma_role<D>(p, un, sQ, sDO, sK, sV, bars, ctl);
     }
