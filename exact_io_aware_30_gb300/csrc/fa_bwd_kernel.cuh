@@ -182,42 +182,50 @@ struct BwdKVCfg {
     static constexpr int KV_BYTES = BN * D * 2;
     static constexpr int Q_BYTES = BM * D * 2;
     static constexpr int STAT_BYTES = 2 * BM * 4;  // l2 of the step's rows, then delta
-    // Warps 0-3 compute: warp w owns key rows 32 w .. + 31 (its TMEM lanes),
-    // one per thread, and all 64 query columns of every step; warp 4 issues
-    // the MMAs, warp 5 the copies.  (Eight compute warps splitting the
-    // columns measured slower: this kernel's per-step MMA issue, 24
-    // instructions of which 16 are N = 64, is the tighter limit, and the
-    // issuing warp then shares its sub-partition with two compute warps.)
-    static constexpr int NUM_COMPUTE = 128;
-    static constexpr int WG = NUM_COMPUTE / 128;   // warpgroups splitting the columns
-    static constexpr int COLS = BM / WG;           // query columns per compute warp
+    // Compute warps: one warpgroup at d >= 128, two at d = 64, where they
+    // take alternate steps (warpgroup g works on the steps t with
+    // t & 1 == g).  Warp w owns key rows 32 (w & 3) .. + 31 (its TMEM
+    // lanes), one per thread, and all 64 query columns of its steps (two
+    // warpgroups: in two halves of 32, for registers).  At d = 64 the tensor
+    // core's work per step halves and one warp per sub-partition leaves the
+    // latency-bound exponent and packing chain exposed; at d = 128 a second
+    // warpgroup measured slower (the MMA issuers then share their
+    // sub-partitions with two compute warps).  The next warps issue S^T and
+    // dP^T, dV and dK, and the copies.
+    static constexpr int NUM_COMPUTE = (D == 64) ? 256 : 128;
+    static constexpr int WG = NUM_COMPUTE / 128;   // warpgroups alternating steps
+    static constexpr int COLS = BM;                // query columns per compute thread and step
     static constexpr int MMA_WARP = NUM_COMPUTE / 32;  // issues S^T and dP^T
     static constexpr int MMA_G_WARP = MMA_WARP + 1;    // issues dV and dK
     static constexpr int TMA_WARP = MMA_WARP + 2;
     static constexpr int NUM_THREADS = NUM_COMPUTE + 96;
-    // Tensor memory: dV and dK accumulators, S^T and dP^T (fp32, 64 columns
-    // each), P^T and dS^T (16-bit pairs, 32 columns each).
+    // Tensor memory: dV and dK accumulators, then two score buffers; step t
+    // uses buffer t & 1: S^T and dP^T (fp32, 64 columns each) at S_COL and
+    // DP_COL + BUF * (t & 1).  P^T and dS^T of the step (16-bit pairs, 32
+    // columns each) are written over the first halves of its own S^T and
+    // dP^T, which the compute warps have read by then, so the score products
+    // of step t+1 run on the tensor core while the compute warps work on
+    // step t, and a buffer is free again once dV and dK of its step are done.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t DV_COL = 0;
     static constexpr uint32_t DK_COL = 128;
     static constexpr uint32_t S_COL = 256;
     static constexpr uint32_t DP_COL = 320;
-    static constexpr uint32_t P_COL = 384;
-    static constexpr uint32_t DS_COL = 416;
+    static constexpr uint32_t BUF = 128;
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;              // [ST]
     static constexpr int B_QEMPTY = B_QFULL + ST;  // [ST]
-    static constexpr int B_SFULL = B_QEMPTY + ST;
-    static constexpr int B_SFREE = B_SFULL + 1;
-    static constexpr int B_PFULL = B_SFREE + 1;
-    static constexpr int B_PFREE = B_PFULL + 1;
-    static constexpr int B_DONE = B_PFREE + 1;
+    static constexpr int B_SFULL = B_QEMPTY + ST;  // [2]: scores of buffer b formed
+    static constexpr int B_PFULL = B_SFULL + 2;    // [2]: P^T, dS^T of buffer b written
+    static constexpr int B_PFREE = B_PFULL + 2;    // [2]: dV, dK of buffer b done
+    static constexpr int B_DONE = B_PFREE + 2;
     static constexpr int B_DRAIN = B_DONE + 1;  // [2]: each issuer's MMAs finished
     static constexpr int B_NEVER = B_DRAIN + 2;  // no arrivals (the stall test's wait)
     static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
-    static_assert(DK_COL + DA <= S_COL && DS_COL + BM / 2 <= TMEM_COLS, "tensor memory overflow");
+    static_assert(DK_COL + DA <= S_COL && DP_COL + BUF + BM <= TMEM_COLS && S_COL + BM <= DP_COL,
+                  "tensor memory overflow");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
 
@@ -332,8 +340,9 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
             ok = false;
             break;
         }
-        // the compute warps have read S^T and dP^T of step t-1
-        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_SFREE), (t - 1) & 1, ctl, 24)) {
+        // buffer t & 1 is free once dV and dK of step t-2 are done
+        const int b = t & 1;
+        if (t >= 2 && !wait_warp(bar_addr(bars, C::B_PFREE + b), ((t - 2) >> 1) & 1, ctl, 24)) {
             ok = false;
             break;
         }
@@ -341,15 +350,16 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
         if (leader) {
             const uint64_t qd = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), 16);
             const uint64_t od = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), 16);
+            const uint32_t boff = (uint32_t)b * C::BUF;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ss(tmem + C::S_COL, dk_desc + kmajor_step(kk, C::KV_BOX),
+                ptx::mma_ss(tmem + C::S_COL + boff, dk_desc + kmajor_step(kk, C::KV_BOX),
                             qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ss(tmem + C::DP_COL, dv_desc + kmajor_step(kk, C::KV_BOX),
+                ptx::mma_ss(tmem + C::DP_COL + boff, dv_desc + kmajor_step(kk, C::KV_BOX),
                             od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
-            ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
             ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
         }
         __syncwarp();
@@ -368,8 +378,9 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
     bool ok = true;
     for (int t = 0; ok && t < un.steps; ++t) {
         const int slot = t % C::ST;
+        const int b = t & 1;
         if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 30) ||
-            !wait_warp(bar_addr(bars, C::B_PFULL), t & 1, ctl, 25)) {
+            !wait_warp(bar_addr(bars, C::B_PFULL + b), (t >> 1) & 1, ctl, 25)) {
             ok = false;
             break;
         }
@@ -381,15 +392,16 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
             const uint32_t col0 = (uint32_t)(un.half * (C::DA / 64) * C::Q_BOX);
             const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES) + col0, C::Q_BOX);
             const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES) + col0, C::Q_BOX);
+            const uint32_t boff = (uint32_t)b * C::BUF;
 #pragma unroll
             for (int kk = 0; kk < C::BM / 16; ++kk)
-                ptx::mma_ts(tmem + C::DV_COL, tmem + C::P_COL + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
+                ptx::mma_ts(tmem + C::DV_COL, tmem + C::S_COL + boff + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
                             kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
             for (int kk = 0; kk < C::BM / 16; ++kk)
-                ptx::mma_ts(tmem + C::DK_COL, tmem + C::DS_COL + kk * 8, qm + (uint32_t)((kk * 2048) >> 4),
+                ptx::mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + boff + kk * 8, qm + (uint32_t)((kk * 2048) >> 4),
                             kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
-            ptx::mma_commit(bar_addr(bars, C::B_PFREE));
+            ptx::mma_commit(bar_addr(bars, C::B_PFREE + b));
             ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
             if (t + 1 == un.steps) ptx::mma_commit(bar_addr(bars, C::B_DONE));
         }
@@ -400,94 +412,106 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
     wait_bar_drain(bar_addr(bars, C::B_DRAIN + 1), 0);
 }
 
+// P^T = exp2(S^T c - lse2) (masked) and dS^T = P^T (dP^T - delta) of the
+// query columns col0 .. col0 + NC of one step, for this thread's key row j:
+// s and dp hold the row's S^T and dP^T there, L4 and D4 the step's row
+// statistics; pw and dsw get the 16-bit pairs.
+template <int NC, bool kFP16>
+__device__ __forceinline__ void bwd_kv_p_ds(const uint32_t (&s)[NC], const uint32_t (&dp)[NC],
+                                            const float4 *L4, const float4 *D4, int col0, int lo, int hi,
+                                            bool masked, float c, uint32_t (&pw)[NC / 2],
+                                            uint32_t (&dsw)[NC / 2]) {
+    const uint64_t c2 = ptx::f32x2(c, c);
+    const uint64_t z2 = ptx::f32x2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < NC / 4; ++q) {
+        const int cq = col0 + 4 * q;  // query column of element 0
+        const float4 l = L4[cq / 4], dl = D4[cq / 4];
+        float x0, x1, x2, x3, g0, g1, g2, g3;
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q]), __uint_as_float(s[4 * q + 1])),
+                                         c2, ptx::f32x2(-l.x, -l.y)), x0, x1);
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q + 2]), __uint_as_float(s[4 * q + 3])),
+                                         c2, ptx::f32x2(-l.z, -l.w)), x2, x3);
+        float pv[4] = {ptx::ex2_approx(x0), ptx::ex2_approx(x1), ptx::ex2_approx(x2), ptx::ex2_approx(x3)};
+        if (masked) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[e] = (cq + e >= lo && cq + e < hi) ? pv[e] : 0.f;
+        }
+        ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q]), __uint_as_float(dp[4 * q + 1])),
+                                         ptx::f32x2(-dl.x, -dl.y)), g0, g1);
+        ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q + 2]), __uint_as_float(dp[4 * q + 3])),
+                                         ptx::f32x2(-dl.z, -dl.w)), g2, g3);
+        float d0, d1, d2, d3;
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(pv[0], pv[1]), ptx::f32x2(g0, g1), z2), d0, d1);
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(pv[2], pv[3]), ptx::f32x2(g2, g3), z2), d2, d3);
+        pw[2 * q] = pack2b<kFP16>(pv[0], pv[1]);
+        pw[2 * q + 1] = pack2b<kFP16>(pv[2], pv[3]);
+        dsw[2 * q] = pack2b<kFP16>(d0, d1);
+        dsw[2 * q + 1] = pack2b<kFP16>(d2, d3);
+    }
+}
+
 template <int D, bool kFP16>
 __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const uint8_t *sStat,
                                     uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdKVCfg<D>;
     constexpr int NC = C::COLS;
+    constexpr int HC = NC / C::WG;  // columns per pass: P^T and dS^T of a pass overwrite only
+                                    // columns of S^T and dP^T that this thread has read
     const int warp = (int)threadIdx.x >> 5;
     const int r = 32 * (warp & 3) + ((int)threadIdx.x & 31);  // key row of the tile = TMEM lane
-    const int h = warp >> 2;                                  // query columns h*NC .. + NC
+    const int h = C::WG == 1 ? 0 : warp >> 2;                 // warpgroup: steps t = h mod WG
     const uint32_t lane_base = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const int j = un.j0 + r;
     const bool row_ok = j < p.Sk;
     const float c = p.scale_log2;
     bool ok = true;
-    for (int t = 0; t < un.steps; ++t) {
+    for (int t = h; t < un.steps; t += C::WG) {
         const int slot = t % C::ST;
-        const int i0 = (un.it_lo + t % un.n_i) * C::BM + h * NC;  // first query row of the columns
+        const int b = t & 1;  // score buffer
+        const uint32_t s_col = C::S_COL + (uint32_t)b * C::BUF, dp_col = C::DP_COL + (uint32_t)b * C::BUF;
+        const int i0 = (un.it_lo + t % un.n_i) * C::BM;  // first query row of the step
         // The statistics arrived with the step's Q tile; S^T and dP^T are ready.
         ok = ok && wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
-        ok = ok && wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL), t & 1,
-                             ctl, 27);
+        ok = ok && wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL + b),
+                             (t >> 1) & 1, ctl, 27);
         if (!ok) break;
         ptx::tc_fence_after();
-        uint32_t s[NC], dp[NC];
-        ptx::tmem_ld_x32<0>(lane_base + C::S_COL + h * NC, s);
-        ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
-        if constexpr (NC == 64) {
-            ptx::tmem_ld_x32<32>(lane_base + C::S_COL + 32, s);
-            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + 32, dp);
-        }
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<NC>(s);
-        ptx::reg_fence<NC>(dp);
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
-
         // Query row i0 + col is visible to key j iff lo <= col < hi.
         int lo = 0, hi = NC;
         if (p.mask_kind != kMaskNone) lo = j - i0;
         if (p.mask_kind == kMaskWindow) hi = (int)min((long long)NC, (long long)j + p.window - i0);
         if (!row_ok) lo = NC;
         const bool masked = lo > 0 || hi < NC;
-        const float4 *L4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES) + h * (NC / 4);
-        const float4 *D4 =
-            reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4) + h * (NC / 4);
-        uint32_t pw[NC / 2], dsw[NC / 2];
-        const uint64_t c2 = ptx::f32x2(c, c);
+        const float4 *L4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES);
+        const float4 *D4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4);
 #pragma unroll
-        for (int q = 0; q < NC / 4; ++q) {
-            const float4 l = L4[q], dl = D4[q];
-            float x0, x1, x2, x3, g0, g1, g2, g3;
-            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q]), __uint_as_float(s[4 * q + 1])),
-                                             c2, ptx::f32x2(-l.x, -l.y)), x0, x1);
-            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q + 2]), __uint_as_float(s[4 * q + 3])),
-                                             c2, ptx::f32x2(-l.z, -l.w)), x2, x3);
-            float pv[4] = {ptx::ex2_approx(x0), ptx::ex2_approx(x1), ptx::ex2_approx(x2), ptx::ex2_approx(x3)};
-            if (masked) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) pv[e] = (4 * q + e >= lo && 4 * q + e < hi) ? pv[e] : 0.f;
+        for (int pass = 0; pass < C::WG; ++pass) {
+            uint32_t s[HC], dp[HC], pw[HC / 2], dsw[HC / 2];
+            ptx::tmem_ld_x32<0>(lane_base + s_col + pass * HC, s);
+            ptx::tmem_ld_x32<0>(lane_base + dp_col + pass * HC, dp);
+            if constexpr (HC == 64) {
+                ptx::tmem_ld_x32<32>(lane_base + s_col + 32, s);
+                ptx::tmem_ld_x32<32>(lane_base + dp_col + 32, dp);
             }
-            ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q]), __uint_as_float(dp[4 * q + 1])),
-                                             ptx::f32x2(-dl.x, -dl.y)), g0, g1);
-            ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q + 2]), __uint_as_float(dp[4 * q + 3])),
-                                             ptx::f32x2(-dl.z, -dl.w)), g2, g3);
-            float d0, d1, d2, d3;
-            const uint64_t z2 = ptx::f32x2(0.f, 0.f);
-            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(pv[0], pv[1]), ptx::f32x2(g0, g1), z2), d0, d1);
-            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(pv[2], pv[3]), ptx::f32x2(g2, g3), z2), d2, d3);
-            pw[2 * q] = pack2b<kFP16>(pv[0], pv[1]);
-            pw[2 * q + 1] = pack2b<kFP16>(pv[2], pv[3]);
-            dsw[2 * q] = pack2b<kFP16>(d0, d1);
-            dsw[2 * q + 1] = pack2b<kFP16>(d2, d3);
-        }
-        // dV / dK of step t-1 have read the P and dS areas
-        if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 28)) {
-            ok = false;
-            break;
-        }
-        ptx::tc_fence_after();
-        if constexpr (NC == 64) {
-            ptx::tmem_st_x32<0>(lane_base + C::P_COL, pw);
-            ptx::tmem_st_x32<0>(lane_base + C::DS_COL, dsw);
-        } else {
-            ptx::tmem_st_x16<0>(lane_base + C::P_COL + h * (NC / 2), pw);
-            ptx::tmem_st_x16<0>(lane_base + C::DS_COL + h * (NC / 2), dsw);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<HC>(s);
+            ptx::reg_fence<HC>(dp);
+            bwd_kv_p_ds<HC, kFP16>(s, dp, L4, D4, pass * HC, lo, hi, masked, c, pw, dsw);
+            // P^T and dS^T of the pass over the step's S^T and dP^T columns
+            // pass * HC / 2 .. + HC / 2 (one pass: 0..31 after reading 0..63;
+            // two: 0..15 after 0..31, then 16..31 after 32..63)
+            if constexpr (HC == 64) {
+                ptx::tmem_st_x32<0>(lane_base + s_col, pw);
+                ptx::tmem_st_x32<0>(lane_base + dp_col, dsw);
+            } else {
+                ptx::tmem_st_x16<0>(lane_base + s_col + pass * (HC / 2), pw);
+                ptx::tmem_st_x16<0>(lane_base + dp_col + pass * (HC / 2), dsw);
+            }
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_addr(bars, C::B_PFULL));
+        ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + b));
     }
 
     // Epilogue: dV and scale * dK of this thread's key row, columns h*D/WG ..
@@ -545,10 +569,11 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
             ptx::mbar_init(bar_addr(bars, C::B_QFULL + s), 1);
             ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + s), 2);  // one commit from each issuer
         }
-        ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
-        ptx::mbar_init(bar_addr(bars, C::B_SFREE), C::NUM_COMPUTE);
-        ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_COMPUTE);
-        ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), C::NUM_COMPUTE / C::WG);
+            ptx::mbar_init(bar_addr(bars, C::B_PFREE + b), 1);
+        }
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
@@ -766,16 +791,17 @@ __device__ void bwd_q_mma_s_role(const BwdParams &p, const QUnit &un, uint8_t *s
         if (leader) {
             const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::KV_BYTES), 16);
             const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::KV_BYTES), 16);
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
-                            kIdescS, kk > 0 ? 1u : 0u);
+            // dP first: its V slot is free as soon as dP completes
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
                             kIdescS, kk > 0 ? 1u : 0u);
-            ptx::mma_commit(bar_addr(bars, C::B_SFULL));
             ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
+                            kIdescS, kk > 0 ? 1u : 0u);
+            ptx::mma_commit(bar_addr(bars, C::B_SFULL));
         }
         __syncwarp();
     }
