@@ -655,9 +655,17 @@ struct BwdQCfg {
     static constexpr int B_KEMPTY = B_KFULL + KST;    // [KST]
     static constexpr int B_VFULL = B_KEMPTY + KST;    // [VST]
     static constexpr int B_VEMPTY = B_VFULL + VST;    // [VST]
-    static constexpr int B_SFULL = B_VEMPTY + VST;
-    static constexpr int B_SFREE = B_SFULL + 1;
-    static constexpr int B_PFULL = B_SFREE + 1;
+    // d = 128: S and dP have their own ready and free barriers, so the
+    // compute warps exponentiate S while dP is still being formed and the
+    // next S starts as soon as this one is read.  At d = 64 and 256 the extra
+    // round trip cost more than it hid: there dP goes first (its V slot frees
+    // earlier) and S's barriers cover both.
+    static constexpr bool SPLIT = (D == 128);
+    static constexpr int B_SFULL = B_VEMPTY + VST;  // S formed (and dP, unless SPLIT)
+    static constexpr int B_SFREE = B_SFULL + 1;     // S (and dP) read by the compute warps
+    static constexpr int B_DPFULL = B_SFREE + 1;    // SPLIT: dP formed
+    static constexpr int B_DPFREE = B_DPFULL + 1;   // SPLIT: dP read by the compute warps
+    static constexpr int B_PFULL = B_DPFREE + 1;
     static constexpr int B_PFREE = B_PFULL + 1;
     static constexpr int B_DONE = B_PFREE + 1;
     static constexpr int B_DRAIN = B_DONE + 1;    // [2]: each issuer's MMAs finished
@@ -764,9 +772,11 @@ __device__ void bwd_q_tma_role(const BwdParams &p, const QUnit &un, uint8_t *sQ,
     }
 }
 
-// The two MMA issuers of the dQ kernel: S and dP of step t go out as soon as
-// the compute warps have read step t-1's, dQ += dS K of step t as soon as its
-// dS is written.  A K slot is free after dQ, a V slot after dP.
+// The two MMA issuers of the dQ kernel: S of step t goes out as soon as the
+// compute warps have read S of step t-1, then dP as soon as they have read
+// dP of step t-1 (without SPLIT: dP, then S, once both of step t-1 are
+// read); dQ += dS K of step t as soon as its dS is written.  A K slot is free
+// after dQ, a V slot after dP.
 template <int D, bool kFP16>
 __device__ void bwd_q_mma_s_role(const BwdParams &p, const QUnit &un, uint8_t *sQ, uint8_t *sDO,
                                  uint8_t *sK, uint8_t *sV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
@@ -788,10 +798,33 @@ __device__ void bwd_q_mma_s_role(const BwdParams &p, const QUnit &un, uint8_t *s
             break;
         }
         ptx::tc_fence_after();
-        if (leader) {
+        if constexpr (C::SPLIT) {
             const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::KV_BYTES), 16);
             const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::KV_BYTES), 16);
-            // dP first: its V slot is free as soon as dP completes
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::S_COL, qd + kmajor_step(kk, C::Q_BOX), kd + kmajor_step(kk, C::KV_BOX),
+                                kIdescS, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_SFULL));
+            }
+            __syncwarp();
+            if (t >= 1 && !wait_warp(bar_addr(bars, C::B_DPFREE), (t - 1) & 1, ctl, 55)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
+                                kIdescS, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::B_DPFULL));
+                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + vs));
+            }
+        } else if (leader) {
+            const uint64_t kd = smem_desc(ptx::smem_addr(sK + ks * C::KV_BYTES), 16);
+            const uint64_t vd = smem_desc(ptx::smem_addr(sV + vs * C::KV_BYTES), 16);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 ptx::mma_ss(tmem + C::DP_COL, od + kmajor_step(kk, C::Q_BOX), vd + kmajor_step(kk, C::KV_BOX),
@@ -876,34 +909,72 @@ __device__ void bwd_q_compute_role(const BwdParams &p, const QUnit &un, uint32_t
         ptx::tc_fence_after();
         uint32_t s[NC], dp[NC], w[NC / 2];
         ptx::tmem_ld_x32<0>(lane_base + C::S_COL + h * NC, s);
-        ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
+        if constexpr (!C::SPLIT) ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
         if constexpr (NC == 64) {
             ptx::tmem_ld_x32<32>(lane_base + C::S_COL + h * NC + 32, s);
-            ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + h * NC + 32, dp);
+            if constexpr (!C::SPLIT) ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + h * NC + 32, dp);
         }
         ptx::tmem_wait_ld();
         ptx::reg_fence<NC>(s);
-        ptx::reg_fence<NC>(dp);
+        if constexpr (!C::SPLIT) ptx::reg_fence<NC>(dp);
         ptx::tc_fence_before();
         ptx::mbar_arrive(bar_addr(bars, C::B_SFREE));
         // Packed fp32 pairs: s c - L and dP - delta as one instruction per
         // pair each, and P (dP - delta) as an fma with -0 (the exact product,
         // sign of zero included).
+        if constexpr (C::SPLIT) {
+            // P = exp2(s c - L) (masked) while dP is still being formed
 #pragma unroll
-        for (int e = 0; e < NC; e += 2) {
-            float x0, x1, g0, g1, d0, d1;
-            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])), c2,
-                                             nl2), x0, x1);
-            float p0 = ptx::ex2_approx(x0);
-            float p1 = ptx::ex2_approx(x1);
-            if (masked) {
-                p0 = (e >= lo && e < hi) ? p0 : 0.f;
-                p1 = (e + 1 >= lo && e + 1 < hi) ? p1 : 0.f;
+            for (int e = 0; e < NC; e += 2) {
+                float x0, x1;
+                ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                                 c2, nl2), x0, x1);
+                float p0 = ptx::ex2_approx(x0);
+                float p1 = ptx::ex2_approx(x1);
+                if (masked) {
+                    p0 = (e >= lo && e < hi) ? p0 : 0.f;
+                    p1 = (e + 1 >= lo && e + 1 < hi) ? p1 : 0.f;
+                }
+                s[e] = __float_as_uint(p0);
+                s[e + 1] = __float_as_uint(p1);
             }
-            ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), nd2),
-                              g0, g1);
-            ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(p0, p1), ptx::f32x2(g0, g1), mz2), d0, d1);
-            w[e / 2] = pack2b<kFP16>(d0, d1);
+            if (!wait_warp(bar_addr(bars, C::B_DPFULL), t & 1, ctl, 56)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            ptx::tmem_ld_x32<0>(lane_base + C::DP_COL + h * NC, dp);
+            if constexpr (NC == 64) ptx::tmem_ld_x32<32>(lane_base + C::DP_COL + h * NC + 32, dp);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<NC>(dp);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_addr(bars, C::B_DPFREE));
+#pragma unroll
+            for (int e = 0; e < NC; e += 2) {
+                float g0, g1, d0, d1;
+                ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                                 nd2), g0, g1);
+                ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                                 ptx::f32x2(g0, g1), mz2), d0, d1);
+                w[e / 2] = pack2b<kFP16>(d0, d1);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < NC; e += 2) {
+                float x0, x1, g0, g1, d0, d1;
+                ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[e]), __uint_as_float(s[e + 1])),
+                                                 c2, nl2), x0, x1);
+                float p0 = ptx::ex2_approx(x0);
+                float p1 = ptx::ex2_approx(x1);
+                if (masked) {
+                    p0 = (e >= lo && e < hi) ? p0 : 0.f;
+                    p1 = (e + 1 >= lo && e + 1 < hi) ? p1 : 0.f;
+                }
+                ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                                 nd2), g0, g1);
+                ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(p0, p1), ptx::f32x2(g0, g1), mz2), d0, d1);
+                w[e / 2] = pack2b<kFP16>(d0, d1);
+            }
         }
         // dQ of step t-1 has read the dS area
         if (t >= 1 && !wait_warp(bar_addr(bars, C::B_PFREE), (t - 1) & 1, ctl, 37)) {
@@ -969,6 +1040,8 @@ __global__ void __launch_bounds__(BwdQCfg<D>::NUM_THREADS, 1)
         }
         ptx::mbar_init(bar_addr(bars, C::B_SFULL), 1);
         ptx::mbar_init(bar_addr(bars, C::B_SFREE), C::NUM_COMPUTE);
+        ptx::mbar_init(bar_addr(bars, C::B_DPFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DPFREE), C::NUM_COMPUTE);
         ptx::mbar_init(bar_addr(bars, C::B_PFULL), C::NUM_COMPUTE);
         ptx::mbar_init(bar_addr(bars, C::B_PFREE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
