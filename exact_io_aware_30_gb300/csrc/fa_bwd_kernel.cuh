@@ -215,8 +215,12 @@ struct BwdKVCfg {
     static constexpr int B_KVFULL = 0;
     static constexpr int B_QFULL = 1;              // [ST]
     static constexpr int B_QEMPTY = B_QFULL + ST;  // [ST]
-    static constexpr int B_SFULL = B_QEMPTY + ST;  // [2]: scores of buffer b formed
-    static constexpr int B_PFULL = B_SFULL + 2;    // [2]: P^T, dS^T of buffer b written
+    // One compute warpgroup: S^T of a buffer is announced on its own, so the
+    // exponentials start while dP^T is still being formed.
+    static constexpr bool SPLIT = (WG == 1);
+    static constexpr int B_SFULL = B_QEMPTY + ST;  // [2]: S^T (and dP^T, unless SPLIT) of buffer b formed
+    static constexpr int B_DPFULL = B_SFULL + 2;   // [2]: SPLIT: dP^T of buffer b formed
+    static constexpr int B_PFULL = B_DPFULL + 2;   // [2]: P^T, dS^T of buffer b written
     static constexpr int B_PFREE = B_PFULL + 2;    // [2]: dV, dK of buffer b done
     static constexpr int B_DONE = B_PFREE + 2;
     static constexpr int B_DRAIN = B_DONE + 1;  // [2]: each issuer's MMAs finished
@@ -355,11 +359,12 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
             for (int kk = 0; kk < D / 16; ++kk)
                 ptx::mma_ss(tmem + C::S_COL + boff, dk_desc + kmajor_step(kk, C::KV_BOX),
                             qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
+            if constexpr (C::SPLIT) ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 ptx::mma_ss(tmem + C::DP_COL + boff, dv_desc + kmajor_step(kk, C::KV_BOX),
                             od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
-            ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
+            ptx::mma_commit(bar_addr(bars, C::SPLIT ? C::B_DPFULL + b : C::B_SFULL + b));
             ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
         }
         __syncwarp();
@@ -451,6 +456,53 @@ __device__ __forceinline__ void bwd_kv_p_ds(const uint32_t (&s)[NC], const uint3
     }
 }
 
+// The two halves of bwd_kv_p_ds for a split step: P^T (fp32 into s, and
+// packed into pw) from S^T alone, then dS^T from the fp32 P^T and dP^T.
+template <int NC, bool kFP16>
+__device__ __forceinline__ void bwd_kv_p(uint32_t (&s)[NC], const float4 *L4, int lo, int hi, bool masked,
+                                         float c, uint32_t (&pw)[NC / 2]) {
+    const uint64_t c2 = ptx::f32x2(c, c);
+#pragma unroll
+    for (int q = 0; q < NC / 4; ++q) {
+        const float4 l = L4[q];
+        float x0, x1, x2, x3;
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q]), __uint_as_float(s[4 * q + 1])),
+                                         c2, ptx::f32x2(-l.x, -l.y)), x0, x1);
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(s[4 * q + 2]), __uint_as_float(s[4 * q + 3])),
+                                         c2, ptx::f32x2(-l.z, -l.w)), x2, x3);
+        float pv[4] = {ptx::ex2_approx(x0), ptx::ex2_approx(x1), ptx::ex2_approx(x2), ptx::ex2_approx(x3)};
+        if (masked) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) pv[e] = (4 * q + e >= lo && 4 * q + e < hi) ? pv[e] : 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[4 * q + e] = __float_as_uint(pv[e]);
+        pw[2 * q] = pack2b<kFP16>(pv[0], pv[1]);
+        pw[2 * q + 1] = pack2b<kFP16>(pv[2], pv[3]);
+    }
+}
+
+template <int NC, bool kFP16>
+__device__ __forceinline__ void bwd_kv_ds(const uint32_t (&pf)[NC], const uint32_t (&dp)[NC], const float4 *D4,
+                                          uint32_t (&dsw)[NC / 2]) {
+    const uint64_t z2 = ptx::f32x2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < NC / 4; ++q) {
+        const float4 dl = D4[q];
+        float g0, g1, g2, g3, d0, d1, d2, d3;
+        ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q]), __uint_as_float(dp[4 * q + 1])),
+                                         ptx::f32x2(-dl.x, -dl.y)), g0, g1);
+        ptx::unpack_f32x2(ptx::add_f32x2(ptx::f32x2(__uint_as_float(dp[4 * q + 2]), __uint_as_float(dp[4 * q + 3])),
+                                         ptx::f32x2(-dl.z, -dl.w)), g2, g3);
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(pf[4 * q]), __uint_as_float(pf[4 * q + 1])),
+                                         ptx::f32x2(g0, g1), z2), d0, d1);
+        ptx::unpack_f32x2(ptx::fma_f32x2(ptx::f32x2(__uint_as_float(pf[4 * q + 2]), __uint_as_float(pf[4 * q + 3])),
+                                         ptx::f32x2(g2, g3), z2), d2, d3);
+        dsw[2 * q] = pack2b<kFP16>(d0, d1);
+        dsw[2 * q + 1] = pack2b<kFP16>(d2, d3);
+    }
+}
+
 template <int D, bool kFP16>
 __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const uint8_t *sStat,
                                     uint32_t bars, uint32_t tmem, Ctl *ctl) {
@@ -485,6 +537,28 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
         const bool masked = lo > 0 || hi < NC;
         const float4 *L4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES);
         const float4 *D4 = reinterpret_cast<const float4 *>(sStat + slot * C::STAT_BYTES + C::BM * 4);
+        if constexpr (C::SPLIT) {
+            uint32_t s[NC], dp[NC], pw[NC / 2], dsw[NC / 2];
+            ptx::tmem_ld_x32<0>(lane_base + s_col, s);
+            ptx::tmem_ld_x32<32>(lane_base + s_col + 32, s);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<NC>(s);
+            bwd_kv_p<NC, kFP16>(s, L4, lo, hi, masked, c, pw);
+            if (!wait_warp(bar_addr(bars, C::B_DPFULL + b), (t >> 1) & 1, ctl, 57)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            ptx::tmem_ld_x32<0>(lane_base + dp_col, dp);
+            ptx::tmem_ld_x32<32>(lane_base + dp_col + 32, dp);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<NC>(dp);
+            bwd_kv_ds<NC, kFP16>(s, dp, D4, dsw);
+            // P^T and dS^T over the first halves of this step's S^T and dP^T
+            // (read into registers above)
+            ptx::tmem_st_x32<0>(lane_base + s_col, pw);
+            ptx::tmem_st_x32<0>(lane_base + dp_col, dsw);
+        } else {
 #pragma unroll
         for (int pass = 0; pass < C::WG; ++pass) {
             uint32_t s[HC], dp[HC], pw[HC / 2], dsw[HC / 2];
@@ -508,6 +582,7 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
                 ptx::tmem_st_x16<0>(lane_base + s_col + pass * (HC / 2), pw);
                 ptx::tmem_st_x16<0>(lane_base + dp_col + pass * (HC / 2), dsw);
             }
+        }
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -571,6 +646,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bar_addr(bars, C::B_SFULL + b), 1);
+            ptx::mbar_init(bar_addr(bars, C::B_DPFULL + b), 1);
             ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), C::NUM_COMPUTE / C::WG);
             ptx::mbar_init(bar_addr(bars, C::B_PFREE + b), 1);
         }
