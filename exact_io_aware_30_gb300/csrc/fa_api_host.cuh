@@ -4,11 +4,14 @@
 // The forward end to end from host memory: Q, K, V are copied into a device
 // workspace the caller provides, the fused forward runs there, and O and lse
 // are copied back.  The problem is cut into chunks of whole K/V heads (with
-// the query heads that read them), and three streams overlap the chunks:
-// a copy-in stream moves chunk c+1's Q, K, V while the caller's stream runs
-// chunk c's forward and a copy-out stream returns chunk c-1's O and lse.
-// The time of a call then approaches the largest of the three totals rather
-// than their sum.  Chunk c is an ordinary forward with B = 1: the flattened
+// the query heads that read them), and the chunks overlap: a copy-in stream
+// moves chunk c+1's Q, K, V while chunk c's forward runs and a copy-out
+// stream returns chunk c-1's O and lse.  The forwards go round-robin to
+// kHostComputeStreams streams: a chunk of one or two heads has fewer query
+// tiles than the GPU has SMs, and the next chunk's forward fills the SMs
+// its predecessor leaves idle.  The time of a call then approaches the
+// largest of the three totals rather than their sum.  Chunk c is an
+// ordinary forward with B = 1: the flattened
 // (batch, K/V head) pairs of a chunk are consecutive in every tensor, and
 // query head (b, h) reads K/V pair (b * H + h) / (H / H_kv) of the flattened
 // numbering, so the chunk's local heads keep their grouping.
@@ -17,15 +20,18 @@ namespace fa {
 namespace {
 
 // Chunks: the first chunk's copy-in and the last chunk's kernel and copy-out
-// are not overlapped, so more chunks shorten that fill and drain; the
-// kernels (a quarter of the copies' time on the long workloads) absorb the
-// smaller chunks' lower efficiency.
-constexpr int kHostMaxChunks = 16;
-constexpr size_t kHostMinChunkBytes = 4u << 20;  // inputs per chunk worth a separate copy
+// are not overlapped, so more chunks shorten that fill and drain, but every
+// chunk adds five copies whose fixed costs add up: on GB300 8 chunks of at
+// least 8 MB measured best (16 and 32 were 6 and 22 % slower on the causal
+// 8k workload, 4 about 3 %).
+constexpr int kHostMaxChunks = 8;
+constexpr size_t kHostMinChunkBytes = 8u << 20;  // inputs per chunk worth a separate copy
+constexpr int kHostComputeStreams = 4;
 
 struct HostStreams {
     bool ready = false;
     cudaStream_t in = nullptr, out = nullptr;
+    cudaStream_t cmp[kHostComputeStreams] = {};
     cudaEvent_t start = nullptr, done = nullptr;
     cudaEvent_t copied[kHostMaxChunks] = {};
     cudaEvent_t computed[kHostMaxChunks] = {};
@@ -44,6 +50,8 @@ fa_status host_streams(int dev, HostStreams **hs) {
                   cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
                   cudaEventCreateWithFlags(&h.start, ef) == cudaSuccess &&
                   cudaEventCreateWithFlags(&h.done, ef) == cudaSuccess;
+        for (int c = 0; ok && c < kHostComputeStreams; ++c)
+            ok = cudaStreamCreateWithFlags(&h.cmp[c], cudaStreamNonBlocking) == cudaSuccess;
         for (int c = 0; ok && c < kHostMaxChunks; ++c)
             ok = cudaEventCreateWithFlags(&h.copied[c], ef) == cudaSuccess &&
                  cudaEventCreateWithFlags(&h.computed[c], ef) == cudaSuccess;
@@ -142,14 +150,17 @@ fa_status fwd_host_impl(const void *q_h, const void *k_h, const void *v_h, void 
                             cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
             cudaMemcpyAsync(wsb + L.v + kvoff, static_cast<const char *>(v_h) + kvoff, kvn,
                             cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
-            cudaEventRecord(hs->copied[c], hs->in) != cudaSuccess ||
-            cudaStreamWaitEvent(stream, hs->copied[c], 0) != cudaSuccess)
+            cudaEventRecord(hs->copied[c], hs->in) != cudaSuccess)
             return FA_ERR_CUDA;
+        // (the copy-in stream waited for the caller's earlier work, so the
+        // compute streams inherit that through copied[c])
+        cudaStream_t cs = hs->cmp[c % kHostComputeStreams];
+        if (cudaStreamWaitEvent(cs, hs->copied[c], 0) != cudaSuccess) return FA_ERR_CUDA;
         st = fwd_impl(wsb + L.q + qoff, wsb + L.k + kvoff, wsb + L.v + kvoff, wsb + L.o + qoff,
                       reinterpret_cast<float *>(wsb + L.lse + loff), 1, (int)(np * G), (int)np,
-                      Sq, Sk, d, scale, mask_kind, window, dtype, stream);
+                      Sq, Sk, d, scale, mask_kind, window, dtype, cs);
         if (st != FA_OK) return st;
-        if (cudaEventRecord(hs->computed[c], stream) != cudaSuccess ||
+        if (cudaEventRecord(hs->computed[c], cs) != cudaSuccess ||
             cudaStreamWaitEvent(hs->out, hs->computed[c], 0) != cudaSuccess ||
             cudaMemcpyAsync(static_cast<char *>(o_h) + qoff, wsb + L.o + qoff, qn,
                             cudaMemcpyDeviceToHost, hs->out) != cudaSuccess ||
@@ -158,7 +169,7 @@ fa_status fwd_host_impl(const void *q_h, const void *k_h, const void *v_h, void 
             return FA_ERR_CUDA;
     }
     // The caller's stream reaches its next work only once O and lse are on
-    // the host.
+    // the host (every forward finished before its chunk's copy-out).
     if (cudaEventRecord(hs->done, hs->out) != cudaSuccess ||
         cudaStreamWaitEvent(stream, hs->done, 0) != cudaSuccess)
         return FA_ERR_CUDA;

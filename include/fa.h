@@ -271,11 +271,12 @@ fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int b
  * and O and lse are copied back to host memory.  The arithmetic and the
  * results are those of fa_fwd_gqa (the method's "what goes in, what comes
  * out" -- "FlashAttention: IO-aware attention kernels" -- with the host
- * copies around it).  The problem is cut into up to 16 chunks of whole K/V
+ * copies around it).  The problem is cut into up to 8 chunks of whole K/V
  * heads (with the query heads that read them); chunk c+1's inputs are copied
- * in on a library stream while chunk c runs on `stream` and chunk c-1's
- * outputs are copied out on a second library stream, so the copies overlap
- * the kernels and each other.
+ * in on a library stream while chunk c's forward runs on one of four library
+ * compute streams (round robin, so a chunk too small to fill the GPU leaves
+ * its idle SMs to the next one) and chunk c-1's outputs are copied out on a
+ * further library stream, so the copies overlap the kernels and each other.
  *
  *   q_host, o_host  host pointers, [B, H, Sq, d] 16-bit (dtype)
  *   k_host, v_host  host pointers, [B, H_kv, Sk, d] 16-bit
@@ -291,9 +292,10 @@ fa_status fa_decode_workspace_query(int B, int H, int H_kv, int Sq, int d, int b
  * The call returns once everything is enqueued; `stream` reaches its next
  * work only after O and lse have landed in host memory, so synchronising
  * `stream` is enough before reading them.  The host buffers and the
- * workspace must stay valid until then.  The library's two copy streams and
- * their events are created by the first call on a device (no device memory
- * is allocated); the enqueue of concurrent calls is serialised by a lock.
+ * workspace must stay valid until then.  The library's copy and compute
+ * streams and their events are created by the first call on a device (no
+ * device memory is allocated); the enqueue of concurrent calls is
+ * serialised by a lock.
  * Sq == 0: FA_OK, nothing is enqueued.  A CUDA error part way through the
  * enqueue returns FA_ERR_CUDA with the earlier chunks already enqueued.
  */
