@@ -21,15 +21,18 @@
 //      128;
 //   2. fa_bwd_dkdv_kernel: one CTA per (batch, K/V head, 128-key tile).  K and
 //      V stay in shared memory; 64-row tiles of Q and dO of every query head
-//      that reads this K/V head stream through a ring.  Per step the MMA warp
-//      computes S^T = K Q^T and dP^T = V dO^T into tensor memory (lane = key),
-//      the four compute warps turn them into P^T and dS^T (16-bit, tensor
-//      memory), and the MMA warp accumulates dV += P^T dO and dK += dS^T Q in
-//      tensor memory (P^T and dS^T as the A operand from tensor memory);
+//      that reads this K/V head stream through a ring.  Per step one MMA warp
+//      computes S^T = K Q^T and dP^T = V dO^T into one of two score buffers
+//      in tensor memory (lane = key), the compute warps turn them into P^T
+//      and dS^T (16-bit, written over the step's own S^T and dP^T), and a
+//      second MMA warp accumulates dV += P^T dO and dK += dS^T Q in tensor
+//      memory (P^T and dS^T as the A operand from tensor memory), while the
+//      next step's scores form in the other buffer;
 //   3. fa_bwd_dq_kernel: one CTA per (batch, head, 128-row query tile).  Q and
-//      dO stay in shared memory, K/V tiles stream through a ring; per step
-//      S = Q K^T and dP = dO V^T (lane = query row), dS in tensor memory, and
-//      dQ += dS K with K read as the MN-major B operand.
+//      dO stay in shared memory, K/V tiles stream through two rings; per step
+//      one MMA warp computes S = Q K^T and dP = dO V^T (lane = query row), the
+//      compute warps write dS to tensor memory, and a second MMA warp
+//      accumulates dQ += dS K with K read as the MN-major B operand.
 // Two kernels instead of one with atomic dQ updates keep the result
 // deterministic and need no fp32 dQ buffer; the price is that S and dP are
 // formed twice (7 tile products per (query, key) tile instead of 5).
@@ -324,11 +327,13 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     }
 }
 
-// The two MMA issuers of the dK/dV kernel.  A tcgen05.mma costs tens of
-// cycles of single-thread issue, and a step needs 24 of them, so the score
-// products (S^T, dP^T) and the gradient products (dV, dK) go out from two
-// warps.  A Q/dO stage is free once both have read it (QEMPTY takes one
-// commit from each).
+// The two MMA issuers of the dK/dV kernel.  A tcgen05.mma blocks its issuing
+// thread while the tensor pipe's queue is full (an N = 64 score product with
+// both operands in shared memory takes about 48 cycles, bound by the
+// shared-memory reads), so the score products (S^T, dP^T) and the gradient
+// products (dV, dK) go out from two warps and neither waits behind the
+// other's queue.  A Q/dO stage is free once both have read it (QEMPTY takes
+// one commit from each).
 template <int D, bool kFP16>
 __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
                                   uint8_t *sQ, uint8_t *sDO, uint32_t bars, uint32_t tmem, Ctl *ctl) {
