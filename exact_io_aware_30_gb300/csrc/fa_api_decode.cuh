@@ -16,7 +16,12 @@ namespace {
 struct DecPlan {
     int n_splits = 1, tiles_per_split = 1, keys_per_split = 0;
     size_t part_o_bytes = 0, bytes = 0;
+    size_t order_off = 0;  // tensor-core kernel: the longest-first CTA order (0: none)
 };
+
+// Units up to which the tensor-core kernel's CTAs are put in longest-first
+// order by fa_decode_order_kernel (one CTA, about 2 us at this size).
+constexpr long long kDecOrderMax = 1 << 18;
 
 // The kernel that serves R rows per K/V head.  FA_DECODE_AUTO: the CUDA-core
 // one (fa_decode_gemv_kernel) up to 2 rows, where the products are
@@ -77,6 +82,11 @@ DecPlan plan_decode(int B, int H, int Hkv, int Sq, int d, int max_seq_len, int n
     const size_t rows = (size_t)B * H * Sq;
     pl.part_o_bytes = ((size_t)pl.n_splits * rows * d * 4 + 255) / 256 * 256;
     pl.bytes = pl.part_o_bytes + (size_t)pl.n_splits * rows * 4;
+    const long long units = base * pl.n_splits;
+    if (path == kDecMma && units <= kDecOrderMax) {
+        pl.order_off = (pl.bytes + 255) / 256 * 256;
+        pl.bytes = pl.order_off + (size_t)units * 4;
+    }
     return pl;
 }
 
@@ -88,6 +98,12 @@ fa_status launch_decode(const DecParams &p, void *o, float *lse, DeviceInfo &inf
     const int smem = std::max(C::SMEM_BYTES, kBwdMinSmem);  // one CTA (and its 512 TMEM columns) per SM
     if (set_smem(kern, smem, info.attr_dec[slot]) != FA_OK) return FA_ERR_CUDA;
     const long long grid = (long long)p.B * p.Hkv * p.n_splits;
+    if (p.order) {
+        fa_decode_order_kernel<C::BN><<<1, 1024, 0, stream>>>(p.seq_lens, p.B, p.Hkv, p.Sq, p.max_seq_len,
+                                                              p.n_splits, p.tiles_per_split,
+                                                              const_cast<int *>(p.order));
+        if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    }
     kern<<<(unsigned)grid, C::NUM_THREADS, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
     const int rows = p.B * p.H * p.Sq;
@@ -212,6 +228,8 @@ fa_status decode_impl(const void *q, const void *k_cache, const void *v_cache, c
     p.seq_lens = seq_lens;
     p.part_o = static_cast<float *>(workspace);
     p.part_lse = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + pl.part_o_bytes);
+    p.order = pl.order_off ? reinterpret_cast<const int *>(static_cast<uint8_t *>(workspace) + pl.order_off)
+                           : nullptr;
     p.B = B;
     p.H = H;
     p.Hkv = Hkv;

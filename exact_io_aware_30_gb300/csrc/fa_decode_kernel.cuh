@@ -46,6 +46,7 @@ struct DecParams {
     const int *seq_lens;     // [B]
     float *part_o;           // [n_splits, B*H*Sq, d] fp32, normalised per split
     float *part_lse;         // [n_splits, B*H*Sq] fp32, natural log; -inf: split saw no key
+    const int *order;        // CTA x runs unit order[x] (longest first), or unit x when null
     int B, H, Hkv, kv_group, Sq, R;  // R = kv_group * Sq rows per CTA
     int bs, max_blocks, max_seq_len;
     int mask_kind;
@@ -101,8 +102,9 @@ struct DecUnit {
 template <int D>
 __device__ __forceinline__ DecUnit decode_dec_unit(const DecParams &p) {
     DecUnit u;
-    u.split = (int)blockIdx.x % p.n_splits;
-    const int bk = (int)blockIdx.x / p.n_splits;
+    const int unit = p.order ? p.order[blockIdx.x] : (int)blockIdx.x;
+    u.split = unit % p.n_splits;
+    const int bk = unit / p.n_splits;
     u.b = bk / p.Hkv;
     u.kvh = bk - u.b * p.Hkv;
     // the caller guarantees Sq <= seq_lens[b] <= max_seq_len; clamp anyway so
@@ -470,6 +472,46 @@ __global__ void __launch_bounds__(DecCfg<D>::NUM_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, C::TMEM_COLS);
     }
+}
+
+// Longest-first order of the decode CTAs.  The host does not know the
+// requests' lengths, so this one-CTA kernel counts the key tiles of every
+// (request, K/V head, key range) unit -- the same ranges decode_dec_unit
+// takes -- and lists the units by decreasing tile count (a counting sort on
+// min(tiles, 255); the order within a count does not matter, since every
+// unit writes its own partial slot).  CTA x of the decode kernel then runs
+// unit order[x]: with one CTA per SM and lengths that differ by up to the
+// whole context, the last wave otherwise leaves SMs idle behind a few long
+// requests.
+template <int BN>
+__global__ void __launch_bounds__(1024)
+    fa_decode_order_kernel(const int *__restrict__ seq_lens, int B, int Hkv, int Sq, int max_seq_len,
+                           int n_splits, int tiles_per_split, int *__restrict__ order) {
+    __shared__ int start[256];
+    const int n = B * Hkv * n_splits;
+    for (int i = (int)threadIdx.x; i < 256; i += (int)blockDim.x) start[i] = 0;
+    __syncthreads();
+    auto key = [&](int u) -> int {
+        const int split = u % n_splits;
+        const int b = u / n_splits / Hkv;
+        const int L = min(max(seq_lens[b], Sq), max_seq_len);
+        const int k_beg = split * tiles_per_split * BN;
+        const int k_end = min(k_beg + tiles_per_split * BN, L);
+        const int tiles = k_end > k_beg ? (k_end - k_beg + BN - 1) / BN : 0;
+        return 255 - min(tiles, 255);  // ascending key = descending tile count
+    };
+    for (int u = (int)threadIdx.x; u < n; u += (int)blockDim.x) atomicAdd(&start[key(u)], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int run = 0;
+        for (int i = 0; i < 256; ++i) {
+            const int c = start[i];
+            start[i] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int u = (int)threadIdx.x; u < n; u += (int)blockDim.x) order[atomicAdd(&start[key(u)], 1)] = u;
 }
 
 // Merges the n_splits partial rows: one warp per row, lanes over d.
