@@ -92,3 +92,18 @@ def test_host_forward_empty_query_is_a_noop():
     k = torch.zeros(1, 2, 5, 128, dtype=torch.bfloat16)
     o, lse = fa.forward_host(q, k, k)
     assert o.numel() == 0 and lse.numel() == 0
+
+
+def test_host_forward_with_as_many_chunks_as_heads():
+    # 8 K/V heads of 8.4 MB each make 8 chunks; with the half-weight first and
+    # last chunks the first one is empty and skipped.  Bitwise the device
+    # forward (itself checked against the oracle elsewhere).
+    B, H, S, d = 1, 8, 11000, 128
+    inp = inputs.custom(B, H, S, S, d, inputs.BF16, "causal", 0, seed=1299)
+    w = inp.workload
+    qh, kh, vh = (_host(b, inputs.BF16) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    o_h, l_h = fa.forward_host(qh, kh, vh, scale=w.scale, mask="causal")
+    assert fa.device_error() == fa.FA_OK
+    o_d, l_d = fa.forward(qh.cuda(), kh.cuda(), vh.cuda(), scale=w.scale, mask="causal")
+    torch.cuda.synchronize()
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
