@@ -103,7 +103,7 @@ struct Cfg {
     // VST slots (one tile each), filling the shared memory left after Q.
     static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
     static constexpr int HALF = BN / 2;                  // key columns per softmax warpgroup
-    static constexpr int KST = (D == 64) ? 8 : 3;
+    static constexpr int KST = (D == 64) ? 4 : (D == 128) ? 2 : 3;
     static constexpr int VST = (D == 64) ? 4 : 2;
     // Warps 0-7: two softmax warpgroups (warpgroup h owns key columns
     // [h*HALF, (h+1)*HALF) of every tile, all 128 rows); warp 8: S MMAs;
@@ -120,14 +120,25 @@ struct Cfg {
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
+    // d <= 128: each V slot carries one more 64-column box after the tile's
+    // boxes, whose first column is all ones (written once at the kernel's
+    // start).  For bf16 the P V product then runs with N = D + 16 and also
+    // accumulates, in O's column D, the sum of the rounded weights it used --
+    // the divisor of O -- so the softmax spends no additions on it.
+    static constexpr bool SUMCOL = (D <= 128);
+    static constexpr int V_SLOT_BYTES = TILE_BYTES + (SUMCOL ? KV_CHUNK : 0);
     // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, and two P
     // areas (BN/2 columns each, two 16-bit values per column) at P_COL0 and
     // P_COL0 + P_STRIDE; P of key tile t goes to area t & 1, so the softmax
     // of tile t+1 never waits for P V of tile t.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t O_COL0 = (D == 256) ? 128 : 256;
-    static constexpr uint32_t P_COL0 = 384;
-    static constexpr uint32_t P_STRIDE = 64;
+    static constexpr uint32_t O_COLS = D + (SUMCOL ? 16 : 0);  // O, and for bf16 its sum column D
+    // d = 128: one P area (its second area's columns hold O's sum column);
+    // P of tile t+1 is written once P V of tile t has read the area
+    // (measured +2 % on fp16 even without the sum column).
+    static constexpr uint32_t P_COL0 = (D == 128) ? 448 : 384;
+    static constexpr uint32_t P_STRIDE = (D == 128) ? 0 : 64;
     // Barrier indices.
     static constexpr int B_QFULL = 0;
     static constexpr int B_QEMPTY = 1;
@@ -148,12 +159,12 @@ struct Cfg {
     // in shared memory for one bulk tensor store; d = 256 has no room for it
     // and stores rows directly.
     static constexpr int O_STAGE_BYTES = (D <= 128) ? Q_BYTES : 0;
-    static constexpr int SMEM_TILES = Q_BYTES + (KST + VST) * TILE_BYTES + O_STAGE_BYTES;
+    static constexpr int SMEM_TILES = Q_BYTES + KST * TILE_BYTES + VST * V_SLOT_BYTES + O_STAGE_BYTES;
     static constexpr int XCH_BYTES = 3 * kBM * 4;  // per row: two sums and the reference max
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 24 + XCH_BYTES;
-    static_assert(O_COL0 + D <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
+    static_assert(O_COL0 + O_COLS <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
                   "tensor memory overflow");
-    static_assert(BN / 2 <= (int)P_STRIDE, "P areas overlap");
+    static_assert(P_STRIDE == 0 || BN / 2 <= (int)P_STRIDE, "P areas overlap");
     static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
@@ -286,7 +297,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
 // Loads tile `key0 / BN` of a K or V tensor into the next slot of its ring
 // (the whole warp waits for the slot, one lane issues).
 template <int D>
-__device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *ring, uint32_t bars,
+__device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *ring, int slot_bytes, uint32_t bars,
                                              int full0, int empty0, int nslots, uint32_t &it,
                                              int key0, const Unit &un, bool leader, uint64_t pol,
                                              Ctl *ctl) {
@@ -298,7 +309,7 @@ __device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *rin
     if (leader) {
         const uint32_t fb = bar_addr(bars, full0 + (int)slot);
         ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
-        const uint32_t dst = ptx::smem_addr(ring + slot * C::TILE_BYTES);
+        const uint32_t dst = ptx::smem_addr(ring + slot * slot_bytes);
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c)
             ptx::tma_load_4d(dst + c * C::KV_CHUNK, tm, fb, c * 64, key0, un.kvh, un.b, pol);
@@ -347,7 +358,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
         }
         ++q_cnt;
         for (int j = un.lo; j < un.hi && ok; ++j)
-            ok = load_kv_tile<D>(&p.tm_k, sK, bars, C::B_KFULL, C::B_KEMPTY, C::KST, k_it, j * C::BN, un,
+            ok = load_kv_tile<D>(&p.tm_k, sK, C::TILE_BYTES, bars, C::B_KFULL, C::B_KEMPTY, C::KST, k_it, j * C::BN, un,
                                  leader, pol_kv, ctl);
     }
     if (!ok) {  // let every copy already issued land before the CTA can exit
@@ -370,7 +381,7 @@ __device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, Ctl *ctl
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
         for (int j = un.lo; j < un.hi && ok; ++j)
-            ok = load_kv_tile<D>(&p.tm_v, sV, bars, C::B_VFULL, C::B_VEMPTY, C::VST, v_it, j * C::BN, un,
+            ok = load_kv_tile<D>(&p.tm_v, sV, C::V_SLOT_BYTES, bars, C::B_VFULL, C::B_VEMPTY, C::VST, v_it, j * C::BN, un,
                                  leader, pol_kv, ctl);
     }
     if (!ok) drain_ring(bars, C::B_VFULL, C::VST, v_it);
@@ -447,7 +458,8 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
                             Ctl *ctl) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
-    constexpr uint32_t kIdescO = make_idesc(kBM, D, kFP16, true);
+    // bf16 with the sum column: N = D + 16 (the ones box follows the tile's boxes)
+    constexpr uint32_t kIdescO = make_idesc(kBM, (C::SUMCOL && !kFP16) ? (int)C::O_COLS : D, kFP16, true);
     const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint32_t v_addr = ptx::smem_addr(sV);
     const uint32_t o_tmem = tmem + C::O_COL0;
@@ -488,7 +500,7 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
                 ++ofree_cnt;
                 ptx::tc_fence_after();
             }
-            const uint64_t dv = smem_desc(v_addr + slot * C::TILE_BYTES, C::KV_CHUNK);
+            const uint64_t dv = smem_desc(v_addr + slot * C::V_SLOT_BYTES, C::KV_CHUNK);
             if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
@@ -589,7 +601,7 @@ __device__ __forceinline__ void quad_row_max(const uint32_t (&sr)[NR], float &ma
 // (bf16 keeps only 8 significant bits, enough for a dominant weight's
 // rounding to show in O); fp16's 11 bits make that negligible, so fp16
 // divides by the exact sum.
-template <int NR, bool kFP16>
+template <int NR, bool kFP16, bool kRoundedSum = !kFP16>
 __device__ __forceinline__ void quad_exp(const uint32_t (&sr)[NR], float c, float na, float nb,
                                          uint32_t (&pk)[NR / 2], float &le_a, float &le_b,
                                          float &lr_a, float &lr_b) {
@@ -612,7 +624,7 @@ __device__ __forceinline__ void quad_exp(const uint32_t (&sr)[NR], float c, floa
             sb = ptx::add_f32x2(sb, ptx::f32x2(e0, e1));
         else
             sa = ptx::add_f32x2(sa, ptx::f32x2(e0, e1));
-        if constexpr (!kFP16) {
+        if constexpr (kRoundedSum) {
             const bool odd = (e >> 2) & 1;
             float &acc = row_b ? (odd ? rb1 : rb0) : (odd ? ra1 : ra0);
             acc = ptx::add_bf16x2_to_f32(pw, acc);
@@ -623,7 +635,7 @@ __device__ __forceinline__ void quad_exp(const uint32_t (&sr)[NR], float c, floa
     ptx::unpack_f32x2(sb, b0, b1);
     le_a += a0 + a1;
     le_b += b0 + b1;
-    if constexpr (kFP16) {
+    if constexpr (!kRoundedSum) {
         lr_a += a0 + a1;
         lr_b += b0 + b1;
     } else {
@@ -672,7 +684,14 @@ __device__ __noinline__ void softmax_epilogue(const Params &p, uint32_t bars, Ct
         }
         ptx::named_bar_sync(pair_bar, kPairThreads);
     }
-    const float l_all = xl[re], le_all = xle[re], m_ref = xm[re];
+    float l_all = xl[re];
+    const float le_all = xle[re], m_ref = xm[re];
+    if constexpr (C::SUMCOL && !kFP16) {
+        // the divisor the P V products accumulated in O's column D (o_tmem
+        // addresses this warp's half of the row, at column hh * D/2)
+        l_all = __uint_as_float(ptx::tmem_ld_x1(o_tmem - (uint32_t)(hh * (D / 2)) + D));
+        ptx::tmem_wait_ld();
+    }
     const float inv_l = (l_all > 0.f) ? 1.f / l_all : 0.f;
     if constexpr (C::O_STAGE_BYTES > 0) {
         // Normalise this thread's D/2 columns of O into registers, release
@@ -839,7 +858,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
 #pragma unroll 1
             for (int pass = 0;; ++pass) {
                 le_at = le_bt = lr_at = lr_bt = 0.f;
-                quad_exp<NR, kFP16>(sr, c, (m_a == -INFINITY) ? 0.f : -m_a,
+                quad_exp<NR, kFP16, !kFP16 && !C::SUMCOL>(sr, c, (m_a == -INFINITY) ? 0.f : -m_a,
                                     (m_b == -INFINITY) ? 0.f : -m_b, pk, le_at, le_bt, lr_at, lr_bt);
                 if (first || pass > 0) break;
                 // No reference yet (every earlier key of the row hidden) counts
@@ -864,14 +883,15 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
                 }
                 rescale = true;
             }
-            // O barrier b completes once for each tile whose P sits in area b:
+            // O barrier b completes once for each tile t with t & 1 == b:
             // completion k of barrier t & 1 is P V of tile t with k = t >> 1.
             // Rescaling O needs every earlier P V finished: wait for P V of tile
             // t-1 (a commit covers all earlier MMAs of its issuer).  Rewriting P
-            // area t & 1 needs P V of tile t-2.  The P V of the previous unit
-            // are covered by its final barrier.  Each barrier's next completion
-            // needs a P this thread has not written yet, and the one before was
-            // waited for two tiles ago, so the parity waits are unambiguous.
+            // needs P V of tile t-2 (two areas) or t-1 (one area).  The P V of
+            // the previous unit are covered by its final barrier.  Each
+            // barrier's next completion needs a P this thread has not written
+            // yet, and the one before was waited for two tiles ago, so the
+            // parity waits are unambiguous.
             const uint32_t pb = tt & 1u;
             if (rescale) {  // warp-uniform
                 if (i > 0)
@@ -889,12 +909,24 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
                         ov[e] = __float_as_uint(__uint_as_float(ov[e]) * ((e & 2) ? alpha_b : alpha_a));
                     ptx::tmem_st_16x256b_x8<0>(o_blk + cc * 64, ov);
                 }
+                if constexpr (C::SUMCOL && !kFP16) {  // the divisor column rescales with O
+                    uint32_t sv[8];
+                    ptx::tmem_ld_16x256b_x2<0>(o_blk + D, sv);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence<8>(sv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        sv[e] = __float_as_uint(__uint_as_float(sv[e]) * ((e & 2) ? alpha_b : alpha_a));
+                    ptx::tmem_st_16x256b_x2<0>(o_blk + D, sv);
+                }
             }
             l_a = alpha_a * l_a + lr_at;
             l_b = alpha_b * l_b + lr_bt;
             le_a = alpha_a * le_a + le_at;
             le_b = alpha_b * le_b + le_bt;
-            if (i >= 2)
+            if (C::P_STRIDE == 0 && i >= 1)  // one P area: P V of tile t-1 has read it
+                wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u, ctl, 10);
+            if (C::P_STRIDE != 0 && i >= 2)  // P area t & 1 was last read by P V of tile t-2
                 wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, ctl, 10);
             ptx::tc_fence_after();
             if constexpr (NR == 64)
@@ -929,7 +961,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
     uint8_t *sQ = smem;
     uint8_t *sK = smem + C::Q_BYTES;
     uint8_t *sV = sK + C::KST * C::TILE_BYTES;
-    uint8_t *sO = sV + C::VST * C::TILE_BYTES;  // O staging (d <= 128)
+    uint8_t *sO = sV + C::VST * C::V_SLOT_BYTES;  // O staging (d <= 128)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);    // 8-byte aligned
@@ -977,6 +1009,20 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         ptx::prefetch_tensormap(&p.tm_k);
         ptx::prefetch_tensormap(&p.tm_v);
         if (C::O_STAGE_BYTES > 0) ptx::prefetch_tensormap(&p.tm_o);
+    }
+    if constexpr (C::SUMCOL && !kFP16) {
+        // The ones box of every V slot, in the tile's 128-byte-swizzled layout
+        // (key row r, 16-byte chunk c stored at chunk c ^ (r & 7)): column 0
+        // (element 0 of logical chunk 0) is 1.0, the rest 0.
+        constexpr int kChunks = C::KV_CHUNK / 16;  // 16-byte chunks of one box
+        for (int idx = (int)threadIdx.x; idx < C::VST * kChunks; idx += C::NUM_THREADS) {
+            const int slot = idx / kChunks, rem = idx - slot * kChunks;
+            const int r = rem >> 3, phys = rem & 7;
+            const uint32_t one = (phys == (r & 7)) ? 0x3F80u : 0u;  // bf16 1.0 in the low half
+            ptx::st_shared_v4(ptx::smem_addr(sV + slot * C::V_SLOT_BYTES + C::CHUNKS * C::KV_CHUNK) + rem * 16, one,
+                              0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();  // the tensor core reads the boxes through the async proxy
     }
     ptx::tc_fence_before();
     __syncthreads();

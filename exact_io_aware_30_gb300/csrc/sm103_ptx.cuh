@@ -269,6 +269,31 @@ __device__ __forceinline__ void tmem_ld_16x256b_x8(uint32_t taddr, uint32_t (&r)
                  : "r"(taddr));
 }
 
+// 16x256b, 2 repetitions (16 columns): r[OFF .. OFF+8).
+template <int OFF, int M>
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[M]) {
+    static_assert(OFF + 8 <= M, "register array too small");
+    asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[OFF + 0]), "=r"(r[OFF + 1]), "=r"(r[OFF + 2]), "=r"(r[OFF + 3]), "=r"(r[OFF + 4]), "=r"(r[OFF + 5]), "=r"(r[OFF + 6]), "=r"(r[OFF + 7])
+                 : "r"(taddr));
+}
+
+// 16x256b store, 2 repetitions (16 columns): r[OFF .. OFF+8).
+template <int OFF, int M>
+__device__ __forceinline__ void tmem_st_16x256b_x2(uint32_t taddr, const uint32_t (&r)[M]) {
+    static_assert(OFF + 8 <= M, "register array too small");
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x2.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :: "r"(taddr), "r"(r[OFF + 0]), "r"(r[OFF + 1]), "r"(r[OFF + 2]), "r"(r[OFF + 3]), "r"(r[OFF + 4]), "r"(r[OFF + 5]), "r"(r[OFF + 6]), "r"(r[OFF + 7])
+                 : "memory");
+}
+
+// One 32-bit column of this thread's TMEM lane (32x32b shape, one repetition).
+__device__ __forceinline__ uint32_t tmem_ld_x1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return r;
+}
+
 // 16x256b store, 8 repetitions (64 columns): r[OFF .. OFF+32).
 template <int OFF, int M>
 __device__ __forceinline__ void tmem_st_16x256b_x8(uint32_t taddr, const uint32_t (&r)[M]) {
