@@ -308,6 +308,6 @@ def test_gqa_full_size_whole_output():
 
 
 def test_more_units_than_the_schedule_holds():
-    # 13,000 one-tile units: past the 12,288 a precomputed schedule can carry,
+    # 13,000 one-tile units: past the 4,096 a precomputed schedule can carry,
     # so the kernel falls back to its snake order over the units
     full_case(260, 50, 100, 100, 64, inputs.BF16, "causal", seed=14)
