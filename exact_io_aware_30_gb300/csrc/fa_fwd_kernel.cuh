@@ -647,6 +647,15 @@ __device__ __forceinline__ void quad_exp(const uint32_t (&sr)[NR], float c, floa
     }
 }
 
+// P of one tile (this thread's packed pairs) into its area of tensor memory.
+template <int NR>
+__device__ __forceinline__ void store_p(uint32_t col, const uint32_t (&pk)[NR / 2]) {
+    if constexpr (NR == 64)
+        ptx::tmem_st_16x128b_x16<0>(col, pk);
+    else
+        ptx::tmem_st_16x128b_x8<0>(col, pk);
+}
+
 // Sum over the quad (all 4 threads end with the total).
 __device__ __forceinline__ float quad_sum(float v) {
     v += __shfl_xor_sync(0xffffffffu, v, 1);
@@ -846,7 +855,15 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // 2^8, so when no thread of the warp exceeds the bound every weight
             // is valid as computed.  Otherwise the warp takes the row maxima,
             // and each row whose max grew by more than the bound moves its
-            // reference, rescales and is exponentiated again.
+            // reference, rescales and is exponentiated (and stored) again.
+            // d = 64 (two P areas, tensor work per tile half that of d = 128):
+            // the area is nearly always free, and P goes to tensor memory
+            // before that test, whose vote then overlaps the store (the P V
+            // product sees P only after the arrival at the end of the tile;
+            // measured +4 %).  d = 128 (one P area) runs the test while P V of
+            // tile t-1 may still hold the area; d = 256 measured slower with
+            // the store first.
+            constexpr bool kStoreFirst = (D == 64);
             const bool first = (i == 0);
             if (first) {
                 float ma, mb;
@@ -858,11 +875,22 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             float le_at, le_bt, lr_at, lr_bt;  // this tile's sums (this thread's columns)
             float alpha_a = 1.f, alpha_b = 1.f;
             bool rescale = false;
+            const uint32_t pb = tt & 1u;
+            const uint32_t p_col = blk + C::P_COL0 + pb * C::P_STRIDE;
 #pragma unroll 1
             for (int pass = 0;; ++pass) {
+                if (kStoreFirst && pass > 0) ptx::tmem_wait_st();  // the first P has left the registers
                 le_at = le_bt = lr_at = lr_bt = 0.f;
                 quad_exp<NR, kFP16, !kFP16 && !C::SUMCOL>(sr, c, (m_a == -INFINITY) ? 0.f : -m_a,
                                     (m_b == -INFINITY) ? 0.f : -m_b, pk, le_at, le_bt, lr_at, lr_bt);
+                if constexpr (kStoreFirst) {
+                    if (pass == 0) {
+                        if (i >= 2)  // P area t & 1 was last read by P V of tile t-2
+                            wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, ctl, 10);
+                        ptx::tc_fence_after();
+                    }
+                    store_p<NR>(p_col, pk);
+                }
                 if (first || pass > 0) break;
                 // No reference yet (every earlier key of the row hidden) counts
                 // as exceeding the bound as soon as a key is visible.
@@ -895,7 +923,6 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             // barrier's next completion needs a P this thread has not written
             // yet, and the one before was waited for two tiles ago, so the
             // parity waits are unambiguous.
-            const uint32_t pb = tt & 1u;
             if (rescale) {  // warp-uniform
                 if (i > 0)
                     wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u,
@@ -927,15 +954,13 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
             l_b = alpha_b * l_b + lr_bt;
             le_a = alpha_a * le_a + le_at;
             le_b = alpha_b * le_b + le_bt;
-            if (C::P_STRIDE == 0 && i >= 1)  // one P area: P V of tile t-1 has read it
-                wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u, ctl, 10);
-            if (C::P_STRIDE != 0 && i >= 2)  // P area t & 1 was last read by P V of tile t-2
-                wait_bar(bar_addr(bars, C::B_OFULL + (int)pb), ((tt >> 1) - 1u) & 1u, ctl, 10);
-            ptx::tc_fence_after();
-            if constexpr (NR == 64)
-                ptx::tmem_st_16x128b_x16<0>(blk + C::P_COL0 + pb * C::P_STRIDE, pk);
-            else
-                ptx::tmem_st_16x128b_x8<0>(blk + C::P_COL0 + pb * C::P_STRIDE, pk);
+            if constexpr (!kStoreFirst) {
+                if (i >= 1)  // one P area: P V of tile t-1 has read it
+                    wait_bar(bar_addr(bars, C::B_OFULL + (int)((tt - 1u) & 1u)), ((tt - 1u) >> 1) & 1u, ctl,
+                             10);
+                ptx::tc_fence_after();
+                store_p<NR>(p_col, pk);
+            }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_PFULL + (int)pb));
