@@ -463,9 +463,11 @@ fa_status fa_describe(int d, int mask_kind, int dtype, char *buf, size_t len) {
     }
     static const char *masks[] = {"none", "causal", "sliding_window"};
     std::snprintf(buf, len,
-                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=2 softmax_wgs=2 "
+                  "fa_fwd_kernel<d=%d,%s> sm_103a tcgen05+TMA: BM=128 BN=%d s_buffers=%d softmax_wgs=2 "
                   "k_slots=%d v_slots=%d threads=%d smem=%d mask=%s persistent",
-                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d), fa::k_slots_for(d), fa::v_slots_for(d),
+                  d, dtype == FA_DTYPE_FP16 ? "fp16" : "bf16", fa::bn_for(d),
+                  d == 256 ? fa::Cfg<256>::NSB : d == 128 ? fa::Cfg<128>::NSB : fa::Cfg<64>::NSB,
+                  fa::k_slots_for(d), fa::v_slots_for(d),
                   fa::Cfg<128>::NUM_THREADS,
                   d == 64 ? fa::Cfg<64>::SMEM_BYTES : d == 128 ? fa::Cfg<128>::SMEM_BYTES
                                                                : fa::Cfg<256>::SMEM_BYTES,

@@ -101,13 +101,18 @@ static_assert(sizeof(Params) <= 32764, "kernel parameter space");
 
 template <int D>
 struct Cfg {
-    // d = 256 uses 64-key tiles so that two S buffers and its 256-column O fit
-    // in tensor memory.  K and V tiles stream through two rings of KST and
-    // VST slots (one tile each), filling the shared memory left after Q.
-    static constexpr int BN = (D == 256) ? 64 : 128;     // keys per K/V tile
+    // 128-key tiles.  K and V tiles stream through two rings of KST and VST
+    // slots, filling the shared memory left after Q; a slot holds one piece
+    // of a tile: the whole tile at d <= 128, a 128-column half at d = 256,
+    // where 64 KB tiles would leave room for one K and one V tile only.
+    // The S product of a tile runs piece by piece (N = 128 throughout, so
+    // the tensor core, not the shared-memory reads, sets its pace), and so
+    // does its P V product (one 128-column half of O per piece).
+    static constexpr int BN = 128;                       // keys per K/V tile
     static constexpr int HALF = BN / 2;                  // key columns per softmax warpgroup
-    static constexpr int KST = (D == 64) ? 4 : (D == 128) ? 2 : 3;
-    static constexpr int VST = (D == 64) ? 4 : 2;
+    static constexpr int NPC = (D == 256) ? 2 : 1;       // pieces per K or V tile
+    static constexpr int KST = (D == 64) ? 4 : (D == 128) ? 2 : 3;  // K ring slots (pieces)
+    static constexpr int VST = (D == 64) ? 4 : 2;                   // V ring slots (pieces)
     // Warps 0-7: two softmax warpgroups (warpgroup h owns key columns
     // [h*HALF, (h+1)*HALF) of every tile, all 128 rows); warp 8: S MMAs;
     // warp 9: P V MMAs; warp 10: TMA of Q and K; warp 11: TMA of V.
@@ -123,18 +128,26 @@ struct Cfg {
     static constexpr int KV_CHUNK = BN * 128;          // bytes of one K or V box
     static constexpr int Q_BYTES = kBM * D * 2;
     static constexpr int TILE_BYTES = BN * D * 2;      // one K or one V tile
+    static constexpr int PIECE_COLS = D / NPC;         // columns of one piece
+    static constexpr int PIECE_CHUNKS = PIECE_COLS / 64;
+    static constexpr int PIECE_BYTES = TILE_BYTES / NPC;
     // d <= 128: each V slot carries one more 64-column box after the tile's
     // boxes, whose first column is all ones (written once at the kernel's
     // start).  For bf16 the P V product then runs with N = D + 16 and also
     // accumulates, in O's column D, the sum of the rounded weights it used --
     // the divisor of O -- so the softmax spends no additions on it.
     static constexpr bool SUMCOL = (D <= 128);
-    static constexpr int V_SLOT_BYTES = TILE_BYTES + (SUMCOL ? KV_CHUNK : 0);
-    // Tensor memory: S buffers at columns 0 and BN, O from O_COL0, and two P
-    // areas (BN/2 columns each, two 16-bit values per column) at P_COL0 and
-    // P_COL0 + P_STRIDE; P of key tile t goes to area t & 1, so the softmax
-    // of tile t+1 never waits for P V of tile t.
+    static constexpr int V_SLOT_BYTES = PIECE_BYTES + (SUMCOL ? KV_CHUNK : 0);
+    // Tensor memory: NSB S buffers from column 0 (tile t in buffer t % NSB),
+    // O from O_COL0, and two P areas (BN/2 columns each, two 16-bit values
+    // per column) at P_COL0 and P_COL0 + P_STRIDE; P of key tile t goes to
+    // area t & 1, so the softmax of tile t+1 never waits for P V of tile t.
+    // d = 256: O takes 256 columns, leaving one S buffer; the tensor core's
+    // 2,048 cycles per tile then exceed the softmax's, and S of tile t+1
+    // (issued once the softmax has copied S of tile t out) is ready before
+    // the softmax needs it.
     static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int NSB = (D == 256) ? 1 : 2;
     static constexpr uint32_t O_COL0 = (D == 256) ? 128 : 256;
     static constexpr uint32_t O_COLS = D + (SUMCOL ? 16 : 0);  // O, and for bf16 its sum column D
     // d = 128: one P area (its second area's columns hold O's sum column);
@@ -162,13 +175,14 @@ struct Cfg {
     // in shared memory for one bulk tensor store; d = 256 has no room for it
     // and stores rows directly.
     static constexpr int O_STAGE_BYTES = (D <= 128) ? Q_BYTES : 0;
-    static constexpr int SMEM_TILES = Q_BYTES + KST * TILE_BYTES + VST * V_SLOT_BYTES + O_STAGE_BYTES;
+    static constexpr int SMEM_TILES = Q_BYTES + KST * PIECE_BYTES + VST * V_SLOT_BYTES + O_STAGE_BYTES;
     static constexpr int XCH_BYTES = 3 * kBM * 4;  // per row: two sums and the reference max
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 24 + XCH_BYTES;
     static_assert(O_COL0 + O_COLS <= P_COL0 && P_COL0 + P_STRIDE + BN / 2 <= TMEM_COLS,
                   "tensor memory overflow");
     static_assert(P_STRIDE == 0 || BN / 2 <= (int)P_STRIDE, "P areas overlap");
-    static_assert(2 * BN <= (int)O_COL0, "S buffers overlap O");
+    static_assert(NSB * BN <= (int)O_COL0, "S buffers overlap O");
+    static_assert(PIECE_COLS % 64 == 0 && D % NPC == 0, "pieces of whole 64-column boxes");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
 
@@ -297,27 +311,32 @@ __device__ __forceinline__ Unit decode_unit(int u, const Params &p) {
 
 // ---------------------------------------------------------------- TMA roles
 
-// Loads tile `key0 / BN` of a K or V tensor into the next slot of its ring
-// (the whole warp waits for the slot, one lane issues).
+// Loads tile `key0 / BN` of a K or V tensor, piece by piece, into the next
+// slots of its ring (the whole warp waits for each slot, one lane issues).
+// `it` counts pieces.
 template <int D>
 __device__ __forceinline__ bool load_kv_tile(const CUtensorMap *tm, uint8_t *ring, int slot_bytes, uint32_t bars,
                                              int full0, int empty0, int nslots, uint32_t &it,
                                              int key0, const Unit &un, bool leader, uint64_t pol,
                                              Ctl *ctl) {
     using C = Cfg<D>;
-    const uint32_t slot = it % (uint32_t)nslots;
-    if (!wait_bar_backoff(bar_addr(bars, empty0 + (int)slot), ((it / (uint32_t)nslots) & 1) ^ 1,
-                          ctl, 2))
-        return false;
-    if (leader) {
-        const uint32_t fb = bar_addr(bars, full0 + (int)slot);
-        ptx::mbar_arrive_expect_tx(fb, C::TILE_BYTES);
-        const uint32_t dst = ptx::smem_addr(ring + slot * slot_bytes);
 #pragma unroll
-        for (int c = 0; c < C::CHUNKS; ++c)
-            ptx::tma_load_4d(dst + c * C::KV_CHUNK, tm, fb, c * 64, key0, un.kvh, un.b, pol);
+    for (int pc = 0; pc < C::NPC; ++pc) {
+        const uint32_t slot = it % (uint32_t)nslots;
+        if (!wait_bar_backoff(bar_addr(bars, empty0 + (int)slot), ((it / (uint32_t)nslots) & 1) ^ 1,
+                              ctl, 2))
+            return false;
+        if (leader) {
+            const uint32_t fb = bar_addr(bars, full0 + (int)slot);
+            ptx::mbar_arrive_expect_tx(fb, C::PIECE_BYTES);
+            const uint32_t dst = ptx::smem_addr(ring + slot * slot_bytes);
+#pragma unroll
+            for (int c = 0; c < C::PIECE_CHUNKS; ++c)
+                ptx::tma_load_4d(dst + c * C::KV_CHUNK, tm, fb, pc * C::PIECE_COLS + c * 64, key0, un.kvh,
+                                 un.b, pol);
+        }
+        ++it;
     }
-    ++it;
     return true;
 }
 
@@ -361,7 +380,7 @@ __device__ void tma_qk_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t 
         }
         ++q_cnt;
         for (int j = un.lo; j < un.hi && ok; ++j)
-            ok = load_kv_tile<D>(&p.tm_k, sK, C::TILE_BYTES, bars, C::B_KFULL, C::B_KEMPTY, C::KST, k_it, j * C::BN, un,
+            ok = load_kv_tile<D>(&p.tm_k, sK, C::PIECE_BYTES, bars, C::B_KFULL, C::B_KEMPTY, C::KST, k_it, j * C::BN, un,
                                  leader, pol_kv, ctl);
     }
     if (!ok) {  // let every copy already issued land before the CTA can exit
@@ -392,8 +411,8 @@ __device__ void tma_v_role(const Params &p, uint8_t *sV, uint32_t bars, Ctl *ctl
 
 // ---------------------------------------------------------------- MMA roles
 
-// S issuer: S_b = Q K^T for every key tile, into buffer b = t & 1 as soon as
-// the softmax has read that buffer's previous tile.
+// S issuer: S_b = Q K^T for every key tile, into buffer b = t % NSB as soon
+// as the softmax has read that buffer's previous tile, piece by piece of K.
 template <int D, bool kFP16>
 __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t bars,
                            uint32_t tmem, Ctl *ctl) {
@@ -403,8 +422,8 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
     const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint64_t dq = smem_desc(ptx::smem_addr(sQ), 16);
     const uint32_t k_addr = ptx::smem_addr(sK);
-    uint32_t k_it = 0;   // K tiles consumed
-    uint32_t t_cnt = 0;  // key tiles issued (S buffer = t & 1)
+    uint32_t k_it = 0;   // K pieces consumed
+    uint32_t t_cnt = 0;  // key tiles issued (S buffer = t % NSB)
     uint32_t q_cnt = 0;  // Q tiles consumed
     bool ok = true;
 
@@ -415,35 +434,42 @@ __device__ void mma_s_role(const Params &p, uint8_t *sQ, uint8_t *sK, uint32_t b
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
         if (!wait_bar(bar_addr(bars, C::B_QFULL), q_cnt & 1, ctl, 6)) { ok = false; break; }
-        for (int i = 0; i < n; ++i, ++k_it) {
+        for (int i = 0; i < n && ok; ++i) {
             const uint32_t t = t_cnt + (uint32_t)i;
-            const uint32_t slot = k_it % C::KST;
-            const uint32_t b = t & 1u;
-            if (!wait_bar(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, ctl, 3)) {
-                ok = false;
-                break;
-            }
-            if (t >= 2 &&  // the softmax has read tile t-2 out of this buffer
-                !wait_bar(bar_addr(bars, C::B_SFREE + (int)b), ((t >> 1) - 1u) & 1u, ctl, 12)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const uint64_t dk = smem_desc(k_addr + slot * C::TILE_BYTES, 16);
+            const uint32_t b = t % (uint32_t)C::NSB;
             const uint32_t d_tmem = tmem + b * BN;
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    // 16-column steps: 32 bytes inside a 128-byte box, then the next box.
-                    const uint32_t off_a = (uint32_t)(((kk >> 2) * C::Q_CHUNK + (kk & 3) * 32) >> 4);
-                    const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
-                    ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, kk > 0 ? 1u : 0u);
+#pragma unroll 1
+            for (int pc = 0; pc < C::NPC; ++pc, ++k_it) {
+                const uint32_t slot = k_it % C::KST;
+                if (!wait_bar(bar_addr(bars, C::B_KFULL + (int)slot), (k_it / C::KST) & 1, ctl, 3)) {
+                    ok = false;
+                    break;
                 }
-                ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
-                if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
-                ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + (int)slot));
+                if (pc == 0 && t >= (uint32_t)C::NSB &&  // the softmax has read tile t-NSB out of this buffer
+                    !wait_bar(bar_addr(bars, C::B_SFREE + (int)b), ((t / C::NSB) - 1u) & 1u, ctl, 12)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint64_t dk = smem_desc(k_addr + slot * C::PIECE_BYTES, 16);
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < C::PIECE_COLS / 16; ++kk) {
+                        // 16-column steps: 32 bytes inside a 128-byte box, then the
+                        // next box (Q: column step gk of the whole row, K: kk of the piece).
+                        const int gk = pc * (C::PIECE_COLS / 16) + kk;
+                        const uint32_t off_a = (uint32_t)(((gk >> 2) * C::Q_CHUNK + (gk & 3) * 32) >> 4);
+                        const uint32_t off_b = (uint32_t)(((kk >> 2) * C::KV_CHUNK + (kk & 3) * 32) >> 4);
+                        ptx::mma_ss(d_tmem, dq + off_a, dk + off_b, kIdescS, (pc > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (pc + 1 == C::NPC) {
+                        ptx::mma_commit(bar_addr(bars, C::B_SFULL + (int)b));
+                        if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY));  // last read of Q
+                    }
+                    ptx::mma_commit(bar_addr(bars, C::B_KEMPTY + (int)slot));
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (!ok) break;
         t_cnt += (uint32_t)n;
@@ -461,13 +487,15 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
                             Ctl *ctl) {
     using C = Cfg<D>;
     constexpr int BN = C::BN;
-    // bf16 with the sum column: N = D + 16 (the ones box follows the tile's boxes)
-    constexpr uint32_t kIdescO = make_idesc(kBM, (C::SUMCOL && !kFP16) ? (int)C::O_COLS : D, kFP16, true);
+    // One product per piece: N = the piece's columns of O; bf16 with the sum
+    // column: N = D + 16 (the ones box follows the tile's boxes).
+    constexpr uint32_t kIdescO =
+        make_idesc(kBM, (C::SUMCOL && !kFP16) ? (int)C::O_COLS : C::PIECE_COLS, kFP16, true);
     const bool leader = ptx::lane_id() == 0;  // the whole warp waits, one lane issues
     const uint32_t v_addr = ptx::smem_addr(sV);
     const uint32_t o_tmem = tmem + C::O_COL0;
     const uint32_t p_tmem = tmem + C::P_COL0;
-    uint32_t v_it = 0;       // V tiles consumed
+    uint32_t v_it = 0;       // V pieces consumed
     uint32_t t_cnt = 0;      // key tiles processed (one P V each)
     uint32_t ofree_cnt = 0;  // epilogues waited for
     bool o_used = false;
@@ -479,18 +507,14 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
         const Unit un = decode_unit<D>(u, p);
         if (!un.valid) continue;
         const int n = un.hi - un.lo;
-        for (int i = 0; i < n; ++i, ++v_it) {
+        for (int i = 0; i < n && ok; ++i) {
             const uint32_t t = t_cnt + (uint32_t)i;
-            const uint32_t slot = v_it % C::VST;
-            if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, ctl, 3)) {
-                ok = false;
-                break;
-            }
             // P of tile t is in area t & 1; that area's barrier completes once per
             // two tiles, and the softmax cannot write P of tile t+2 before this
             // P V has run, so the parity wait is unambiguous.
             const uint32_t pb = t & 1u;
-            if (!wait_bar(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, ctl, 4)) {
+            if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)(v_it % C::VST)), (v_it / C::VST) & 1, ctl, 3) ||
+                !wait_bar(bar_addr(bars, C::B_PFULL + (int)pb), (t >> 1) & 1u, ctl, 4)) {
                 ok = false;
                 break;
             }
@@ -503,19 +527,32 @@ __device__ void mma_pv_role(const Params &p, uint8_t *sV, uint32_t bars, uint32_
                 ++ofree_cnt;
                 ptx::tc_fence_after();
             }
-            const uint64_t dv = smem_desc(v_addr + slot * C::V_SLOT_BYTES, C::KV_CHUNK);
-            if (leader) {
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
-                    ptx::mma_ts(o_tmem, p_tmem + pb * C::P_STRIDE + kk * 8,
-                                dv + (uint32_t)((kk * 2048) >> 4), kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll 1
+            for (int pc = 0; pc < C::NPC; ++pc, ++v_it) {
+                const uint32_t slot = v_it % C::VST;
+                if (pc > 0) {  // the first piece was waited for above
+                    if (!wait_bar(bar_addr(bars, C::B_VFULL + (int)slot), (v_it / C::VST) & 1, ctl, 3)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
                 }
-                ptx::mma_commit(bar_addr(bars, C::B_OFULL + (int)pb));
-                if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
-                ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + (int)slot));
+                const uint64_t dv = smem_desc(v_addr + slot * C::V_SLOT_BYTES, C::KV_CHUNK);
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // 16 keys = two 8-row groups (2048 bytes) of V; P: 8 columns.
+                        ptx::mma_ts(o_tmem + (uint32_t)(pc * C::PIECE_COLS), p_tmem + pb * C::P_STRIDE + kk * 8,
+                                    dv + (uint32_t)((kk * 2048) >> 4), kIdescO, (i > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    if (pc + 1 == C::NPC) {
+                        ptx::mma_commit(bar_addr(bars, C::B_OFULL + (int)pb));
+                        if (i + 1 == n) ptx::mma_commit(bar_addr(bars, C::B_OFINAL));
+                    }
+                    ptx::mma_commit(bar_addr(bars, C::B_VEMPTY + (int)slot));
+                }
+                __syncwarp();
             }
-            __syncwarp();
         }
         if (!ok) break;
         t_cnt += (uint32_t)n;
@@ -792,7 +829,7 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
     const int re = 32 * qw + t;               // row of the one-row-per-thread epilogue
     const uint32_t o_tmem = tmem + ((uint32_t)(32 * qw) << 16) + C::O_COL0 + (uint32_t)(hh * (D / 2));
     const float c = p.scale_log2;
-    uint32_t t_cnt = 0;  // key tiles processed (S buffer = t & 1; one P V each)
+    uint32_t t_cnt = 0;  // key tiles processed (S buffer = t % NSB; one P V each)
     uint32_t u_cnt = 0;  // units completed (one O-final phase each)
 
     for (int k = 0;; ++k) {
@@ -829,19 +866,19 @@ __device__ void softmax_role(const Params &p, uint32_t bars, uint32_t tmem, floa
         for (int j = un.lo; j < un.hi; ++j) {
             const int i = j - un.lo;  // step within the unit
             const uint32_t tt = t_cnt++;
-            const int b = (int)(tt & 1u);
+            const int b = (int)(tt % (uint32_t)C::NSB);
             // (Under the stall test the CTA's first wait is on a barrier no one
             // arrives at: it runs out, and the kernel winds down with the
             // device status word set.)
             wait_bar(bar_addr(bars, (p.stall_test && tt == 0) ? C::B_NEVER : C::B_SFULL + b),
-                     (tt >> 1) & 1u, ctl, 7);
+                     (tt / C::NSB) & 1u, ctl, 7);
             ptx::tc_fence_after();
             uint32_t sr[NR];
             ptx::tmem_ld_16x256b_x8<0>(blk + (uint32_t)(b * BN), sr);
             if constexpr (NR == 64) ptx::tmem_ld_16x256b_x8<32>(blk + (uint32_t)(b * BN) + 64, sr);
             ptx::tmem_wait_ld();
             ptx::reg_fence<NR>(sr);
-            // The S buffer may now be overwritten with tile t+2.
+            // The S buffer may now be overwritten with tile t+NSB.
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar_addr(bars, C::B_SFREE + b));
 
@@ -988,7 +1025,7 @@ __global__ void __launch_bounds__(Cfg<D>::NUM_THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem;
     uint8_t *sK = smem + C::Q_BYTES;
-    uint8_t *sV = sK + C::KST * C::TILE_BYTES;
+    uint8_t *sV = sK + C::KST * C::PIECE_BYTES;
     uint8_t *sO = sV + C::VST * C::V_SLOT_BYTES;  // O staging (d <= 128)
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
