@@ -147,7 +147,7 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
     }
     pq = pkv;
     pkv.n_tiles = (Sk + 127) / 128;
-    pkv.n_units = B * Hkv * pkv.n_tiles * (d > 128 ? 2 : 1);  // d = 256: two CTAs per key tile
+    pkv.n_units = B * Hkv * pkv.n_tiles * (d > 128 ? 2 : 1);  // d = 256: two CTAs (dV, dK) per key tile
     const int q_bn = d == 256 ? BwdQCfg<256>::BN : BwdQCfg<128>::BN;
     if (!make_map(&pq.tm_q, q, d, Sq, H, B, BwdQCfg<128>::BM, fp16) ||
         !make_map(&pq.tm_do, dout, d, Sq, H, B, BwdQCfg<128>::BM, fp16) ||

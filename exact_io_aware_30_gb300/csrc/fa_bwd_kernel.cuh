@@ -171,14 +171,17 @@ struct BwdKVCfg {
     static constexpr int BM = 64;    // query rows per step (N of S^T, K of dV / dK)
     static constexpr int BN = 128;   // keys per CTA (M of every MMA = TMEM lanes)
     // d = 256: the dK and dV accumulators of a 128-key tile would need all 512
-    // tensor-memory columns, so two CTAs share the tile, each accumulating one
-    // 128-column half of dK and dV (both form S^T and dP^T over the whole d).
-    // Its K, V, Q and dO tiles leave room for one Q/dO stage only.  A stage
-    // is free only after dV and dK of its step, a step after the compute
-    // warps have seen it, so the ring runs about two stages ahead of the
-    // score products; d = 128 fits four stages, d = 64 six.
-    static constexpr int DA = (D > 128) ? 128 : D;  // accumulator columns per CTA
-    static constexpr int NH = D / DA;               // CTAs per key tile
+    // tensor-memory columns, so two CTAs share the tile by role: role 0
+    // accumulates dV (it forms S^T and P^T only), role 1 dK (S^T, dP^T and
+    // dS^T), each over the whole d.  dP^T is thus formed once per tile, and
+    // the role-0 CTAs, which carry about 60 % of the role-1 work, let the
+    // block scheduler balance the rest.  K, V, Q and dO leave room for one
+    // Q/dO stage only.  A stage is free only after dV and dK of its step, a
+    // step after the compute warps have seen it, so the ring runs about two
+    // stages ahead of the score products; d = 128 fits four stages, d = 64 six.
+    static constexpr int DA = D;                    // accumulator columns per CTA
+    static constexpr bool ROLES = (D > 128);        // one of dV, dK per CTA
+    static constexpr int NH = ROLES ? 2 : 1;        // CTAs per key tile
     static constexpr int ST = (D > 128) ? 1 : (D == 128) ? 4 : 6;  // stages of the (Q, dO, statistics) ring
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BOX = BM * 128;
@@ -211,7 +214,7 @@ struct BwdKVCfg {
     // step t, and a buffer is free again once dV and dK of its step are done.
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t DV_COL = 0;
-    static constexpr uint32_t DK_COL = 128;
+    static constexpr uint32_t DK_COL = ROLES ? 0 : 128;  // roles: the one accumulator at 0
     static constexpr uint32_t S_COL = 256;
     static constexpr uint32_t DP_COL = 320;
     static constexpr uint32_t BUF = 128;
@@ -231,14 +234,15 @@ struct BwdKVCfg {
     static constexpr int NUM_BARS = B_NEVER + 1;
     static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
-    static_assert(DK_COL + DA <= S_COL && DP_COL + BUF + BM <= TMEM_COLS && S_COL + BM <= DP_COL,
+    static_assert(DK_COL + DA <= S_COL && DV_COL + DA <= S_COL && (ROLES || DV_COL + DA <= DK_COL) &&
+                      DP_COL + BUF + BM <= TMEM_COLS && S_COL + BM <= DP_COL,
                   "tensor memory overflow");
     static_assert(SMEM_BYTES <= 232448, "shared memory overflow");
 };
 
 // The rows of the K/V tile of one CTA and the query tiles that see them.
 struct KVUnit {
-    int half;              // which DA-column half of dK and dV this CTA accumulates
+    int role;              // d = 256: 0 = this CTA accumulates dV, 1 = dK (else 0: both)
     int b, kvh, j0, jend;  // keys [j0, jend)
     int it_lo, n_i;        // query tiles it_lo .. it_lo + n_i of every query head of the group
     int steps;             // kv_group * n_i
@@ -249,7 +253,7 @@ __device__ __forceinline__ KVUnit decode_kv_unit(const BwdParams &p) {
     KVUnit u;
     constexpr int NH = BwdKVCfg<D>::NH;
     const int n_bk = p.B * p.Hkv;
-    u.half = (int)blockIdx.x % NH;
+    u.role = (int)blockIdx.x % NH;
     const int id = (int)blockIdx.x / NH;
     const int jt = id / n_bk;  // key tile: all heads' first tiles first (longest)
     const int bk = id - jt * n_bk;
@@ -280,15 +284,17 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     const bool leader = ptx::lane_id() == 0;
     const uint64_t pol_last = ptx::policy_evict_last();
     if (un.steps == 0) return;  // no query row sees these keys: nothing to load
+    const bool need_v = !(C::ROLES && un.role == 0);  // the dV role forms no dP^T
     if (leader) {
         const uint32_t fb = bar_addr(bars, C::B_KVFULL);
-        ptx::mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+        ptx::mbar_arrive_expect_tx(fb, (need_v ? 2 : 1) * C::KV_BYTES);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c) {
             ptx::tma_load_4d(ptx::smem_addr(sK) + c * C::KV_BOX, &p.tm_k, fb, c * 64, un.j0, un.kvh, un.b,
                              pol_last);
-            ptx::tma_load_4d(ptx::smem_addr(sV) + c * C::KV_BOX, &p.tm_v, fb, c * 64, un.j0, un.kvh, un.b,
-                             pol_last);
+            if (need_v)
+                ptx::tma_load_4d(ptx::smem_addr(sV) + c * C::KV_BOX, &p.tm_v, fb, c * 64, un.j0, un.kvh, un.b,
+                                 pol_last);
         }
     }
     int issued = 0;
@@ -365,11 +371,13 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
                 ptx::mma_ss(tmem + C::S_COL + boff, dk_desc + kmajor_step(kk, C::KV_BOX),
                             qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
             if constexpr (C::SPLIT) ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
+            if (!(C::ROLES && un.role == 0)) {
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                ptx::mma_ss(tmem + C::DP_COL + boff, dv_desc + kmajor_step(kk, C::KV_BOX),
-                            od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
-            ptx::mma_commit(bar_addr(bars, C::SPLIT ? C::B_DPFULL + b : C::B_SFULL + b));
+                for (int kk = 0; kk < D / 16; ++kk)
+                    ptx::mma_ss(tmem + C::DP_COL + boff, dv_desc + kmajor_step(kk, C::KV_BOX),
+                                od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
+                ptx::mma_commit(bar_addr(bars, C::SPLIT ? C::B_DPFULL + b : C::B_SFULL + b));
+            }
             ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
         }
         __syncwarp();
@@ -398,19 +406,21 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
         if (leader) {
             // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
             // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
-            // this CTA's DA columns start at 64-column box half * DA / 64
-            const uint32_t col0 = (uint32_t)(un.half * (C::DA / 64) * C::Q_BOX);
-            const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES) + col0, C::Q_BOX);
-            const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES) + col0, C::Q_BOX);
+            const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), C::Q_BOX);
+            const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), C::Q_BOX);
             const uint32_t boff = (uint32_t)b * C::BUF;
+            if (!(C::ROLES && un.role == 1)) {
 #pragma unroll
-            for (int kk = 0; kk < C::BM / 16; ++kk)
-                ptx::mma_ts(tmem + C::DV_COL, tmem + C::S_COL + boff + kk * 8, om + (uint32_t)((kk * 2048) >> 4),
-                            kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::DV_COL, tmem + C::S_COL + boff + kk * 8,
+                                om + (uint32_t)((kk * 2048) >> 4), kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (!(C::ROLES && un.role == 0)) {
 #pragma unroll
-            for (int kk = 0; kk < C::BM / 16; ++kk)
-                ptx::mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + boff + kk * 8, qm + (uint32_t)((kk * 2048) >> 4),
-                            kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < C::BM / 16; ++kk)
+                    ptx::mma_ts(tmem + C::DK_COL, tmem + C::DP_COL + boff + kk * 8,
+                                qm + (uint32_t)((kk * 2048) >> 4), kIdescG, (t > 0 || kk > 0) ? 1u : 0u);
+            }
             ptx::mma_commit(bar_addr(bars, C::B_PFREE + b));
             ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
             if (t + 1 == un.steps) ptx::mma_commit(bar_addr(bars, C::B_DONE));
@@ -549,20 +559,25 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
             ptx::tmem_wait_ld();
             ptx::reg_fence<NC>(s);
             bwd_kv_p<NC, kFP16>(s, L4, lo, hi, masked, c, pw);
-            if (!wait_warp(bar_addr(bars, C::B_DPFULL + b), (t >> 1) & 1, ctl, 57)) {
-                ok = false;
-                break;
+            if (C::ROLES && un.role == 0) {
+                // dV role: P^T over the first half of this step's S^T
+                ptx::tmem_st_x32<0>(lane_base + s_col, pw);
+            } else {
+                if (!wait_warp(bar_addr(bars, C::B_DPFULL + b), (t >> 1) & 1, ctl, 57)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                ptx::tmem_ld_x32<0>(lane_base + dp_col, dp);
+                ptx::tmem_ld_x32<32>(lane_base + dp_col + 32, dp);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence<NC>(dp);
+                bwd_kv_ds<NC, kFP16>(s, dp, D4, dsw);
+                // P^T (unless the dK role) and dS^T over the first halves of
+                // this step's S^T and dP^T (read into registers above)
+                if (!C::ROLES) ptx::tmem_st_x32<0>(lane_base + s_col, pw);
+                ptx::tmem_st_x32<0>(lane_base + dp_col, dsw);
             }
-            ptx::tc_fence_after();
-            ptx::tmem_ld_x32<0>(lane_base + dp_col, dp);
-            ptx::tmem_ld_x32<32>(lane_base + dp_col + 32, dp);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence<NC>(dp);
-            bwd_kv_ds<NC, kFP16>(s, dp, D4, dsw);
-            // P^T and dS^T over the first halves of this step's S^T and dP^T
-            // (read into registers above)
-            ptx::tmem_st_x32<0>(lane_base + s_col, pw);
-            ptx::tmem_st_x32<0>(lane_base + dp_col, dsw);
         } else {
 #pragma unroll
         for (int pass = 0; pass < C::WG; ++pass) {
@@ -600,28 +615,33 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
         ptx::tc_fence_after();
     }
     constexpr int HALF = C::DA / C::WG;  // accumulator columns this warp stores
+    const bool st_dv = !(C::ROLES && un.role == 1), st_dk = !(C::ROLES && un.role == 0);
     const size_t row = ((size_t)un.b * p.Hkv + un.kvh) * (size_t)p.Sk + (size_t)j;
-    const size_t col = (size_t)un.half * C::DA + (size_t)h * HALF;
+    const size_t col = (size_t)h * HALF;
     uint8_t *dv_row = static_cast<uint8_t *>(p.dv) + (row * D + col) * 2;
     uint8_t *dk_row = static_cast<uint8_t *>(p.dk) + (row * D + col) * 2;
     if (un.steps == 0) {
         if (row_ok) {
-            store_zero_row(dv_row, HALF * 2);
-            store_zero_row(dk_row, HALF * 2);
+            if (st_dv) store_zero_row(dv_row, HALF * 2);
+            if (st_dk) store_zero_row(dk_row, HALF * 2);
         }
         return;
     }
 #pragma unroll
     for (int cc = 0; cc < HALF / 32; ++cc) {
         uint32_t rr[32];
-        ptx::tmem_ld_x32<0>(lane_base + C::DV_COL + h * HALF + cc * 32, rr);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(rr);
-        if (row_ok) store_row32<kFP16>(dv_row + cc * 64, rr, 1.f);
-        ptx::tmem_ld_x32<0>(lane_base + C::DK_COL + h * HALF + cc * 32, rr);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence<32>(rr);
-        if (row_ok) store_row32<kFP16>(dk_row + cc * 64, rr, p.scale);
+        if (st_dv) {
+            ptx::tmem_ld_x32<0>(lane_base + C::DV_COL + h * HALF + cc * 32, rr);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(rr);
+            if (row_ok) store_row32<kFP16>(dv_row + cc * 64, rr, 1.f);
+        }
+        if (st_dk) {
+            ptx::tmem_ld_x32<0>(lane_base + C::DK_COL + h * HALF + cc * 32, rr);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence<32>(rr);
+            if (row_ok) store_row32<kFP16>(dk_row + cc * 64, rr, p.scale);
+        }
     }
 }
 
