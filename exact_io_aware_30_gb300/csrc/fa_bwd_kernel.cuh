@@ -183,6 +183,9 @@ struct BwdKVCfg {
     static constexpr bool ROLES = (D > 128);        // one of dV, dK per CTA
     static constexpr int NH = ROLES ? 2 : 1;        // CTAs per key tile
     static constexpr int ST = (D > 128) ? 1 : (D == 128) ? 4 : 6;  // stages of the (Q, dO, statistics) ring
+    // The dV role loads no V tile and takes a second stage in its place.
+    static constexpr int ST_DV = ROLES ? 2 : ST;
+    static constexpr int STM = ST_DV > ST ? ST_DV : ST;  // barriers and statistics slots
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BOX = BM * 128;
     static constexpr int KV_BYTES = BN * D * 2;
@@ -219,12 +222,12 @@ struct BwdKVCfg {
     static constexpr uint32_t DP_COL = 320;
     static constexpr uint32_t BUF = 128;
     static constexpr int B_KVFULL = 0;
-    static constexpr int B_QFULL = 1;              // [ST]
-    static constexpr int B_QEMPTY = B_QFULL + ST;  // [ST]
+    static constexpr int B_QFULL = 1;               // [STM]
+    static constexpr int B_QEMPTY = B_QFULL + STM;  // [STM]
     // One compute warpgroup: S^T of a buffer is announced on its own, so the
     // exponentials start while dP^T is still being formed.
     static constexpr bool SPLIT = (WG == 1);
-    static constexpr int B_SFULL = B_QEMPTY + ST;  // [2]: S^T (and dP^T, unless SPLIT) of buffer b formed
+    static constexpr int B_SFULL = B_QEMPTY + STM;  // [2]: S^T (and dP^T, unless SPLIT) of buffer b formed
     static constexpr int B_DPFULL = B_SFULL + 2;   // [2]: SPLIT: dP^T of buffer b formed
     static constexpr int B_PFULL = B_DPFULL + 2;   // [2]: P^T, dS^T of buffer b written
     static constexpr int B_PFREE = B_PFULL + 2;    // [2]: dV, dK of buffer b done
@@ -232,7 +235,8 @@ struct BwdKVCfg {
     static constexpr int B_DRAIN = B_DONE + 1;  // [2]: each issuer's MMAs finished
     static constexpr int B_NEVER = B_DRAIN + 2;  // no arrivals (the stall test's wait)
     static constexpr int NUM_BARS = B_NEVER + 1;
-    static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * (2 * Q_BYTES + STAT_BYTES);
+    static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * 2 * Q_BYTES + STM * STAT_BYTES;
+    static_assert(ST_DV == ST || (ST_DV == ST + 1 && 2 * Q_BYTES <= KV_BYTES), "the dV role's extra stage fits in V's place");
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(DK_COL + DA <= S_COL && DV_COL + DA <= S_COL && (ROLES || DV_COL + DA <= DK_COL) &&
                       DP_COL + BUF + BM <= TMEM_COLS && S_COL + BM <= DP_COL,
@@ -276,6 +280,24 @@ __device__ __forceinline__ KVUnit decode_kv_unit(const BwdParams &p) {
     return u;
 }
 
+// Q/dO stages of this CTA, and the Q and dO buffers of stage `slot`: stages
+// below ST have their own area; the dV role's extra stage uses V's.
+template <int D>
+__device__ __forceinline__ int kv_stages(const KVUnit &un) {
+    using C = BwdKVCfg<D>;
+    return (C::ROLES && un.role == 0) ? C::ST_DV : C::ST;
+}
+template <int D>
+__device__ __forceinline__ uint8_t *q_stage(uint8_t *sQ, uint8_t *sV, int slot) {
+    using C = BwdKVCfg<D>;
+    return slot < C::ST ? sQ + slot * C::Q_BYTES : sV;
+}
+template <int D>
+__device__ __forceinline__ uint8_t *do_stage(uint8_t *sDO, uint8_t *sV, int slot) {
+    using C = BwdKVCfg<D>;
+    return slot < C::ST ? sDO + slot * C::Q_BYTES : sV + C::Q_BYTES;
+}
+
 template <int D>
 __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
                                 uint8_t *sQ, uint8_t *sDO, uint8_t *sStat, uint32_t bars,
@@ -299,9 +321,10 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     }
     int issued = 0;
     bool ok = true;
+    const int nst = kv_stages<D>(un);
     for (int s = 0; s < un.steps; ++s) {
-        const int slot = s % C::ST;
-        if (!wait_warp_backoff(bar_addr(bars, C::B_QEMPTY + slot), ((s / C::ST) & 1) ^ 1, ctl, 21)) {
+        const int slot = s % nst;
+        if (!wait_warp_backoff(bar_addr(bars, C::B_QEMPTY + slot), ((s / nst) & 1) ^ 1, ctl, 21)) {
             ok = false;
             break;
         }
@@ -312,9 +335,9 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
             ptx::mbar_arrive_expect_tx(fb, 2 * C::Q_BYTES + C::STAT_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
-                ptx::tma_load_4d(ptx::smem_addr(sQ + slot * C::Q_BYTES) + c * C::Q_BOX, &p.tm_q, fb, c * 64,
+                ptx::tma_load_4d(ptx::smem_addr(q_stage<D>(sQ, sV, slot)) + c * C::Q_BOX, &p.tm_q, fb, c * 64,
                                  i0, hq, un.b, pol_last);
-                ptx::tma_load_4d(ptx::smem_addr(sDO + slot * C::Q_BYTES) + c * C::Q_BOX, &p.tm_do, fb,
+                ptx::tma_load_4d(ptx::smem_addr(do_stage<D>(sDO, sV, slot)) + c * C::Q_BOX, &p.tm_do, fb,
                                  c * 64, i0, hq, un.b, pol_last);
             }
             const size_t row0 = ((size_t)un.b * p.H + hq) * (size_t)p.Sq_pad + (size_t)i0;
@@ -328,8 +351,8 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
     // Let every copy already issued land before the CTA can exit.
     wait_bar_drain(bar_addr(bars, C::B_KVFULL), 0);
     if (!ok) {
-        for (int s = issued - C::ST > 0 ? issued - C::ST : 0; s < issued; ++s)
-            wait_bar_drain(bar_addr(bars, C::B_QFULL + s % C::ST), (s / C::ST) & 1);
+        for (int s = issued - nst > 0 ? issued - nst : 0; s < issued; ++s)
+            wait_bar_drain(bar_addr(bars, C::B_QFULL + s % nst), (s / nst) & 1);
     }
 }
 
@@ -349,9 +372,10 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
     const uint64_t dk_desc = smem_desc(ptx::smem_addr(sK), 16);
     const uint64_t dv_desc = smem_desc(ptx::smem_addr(sV), 16);
     bool ok = un.steps == 0 || wait_warp(bar_addr(bars, C::B_KVFULL), 0, ctl, 22);
+    const int nst = kv_stages<D>(un);
     for (int t = 0; ok && t < un.steps; ++t) {
-        const int slot = t % C::ST;
-        if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 23)) {
+        const int slot = t % nst;
+        if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / nst) & 1, ctl, 23)) {
             ok = false;
             break;
         }
@@ -363,8 +387,8 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
         }
         ptx::tc_fence_after();
         if (leader) {
-            const uint64_t qd = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), 16);
-            const uint64_t od = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), 16);
+            const uint64_t qd = smem_desc(ptx::smem_addr(q_stage<D>(sQ, sV, slot)), 16);
+            const uint64_t od = smem_desc(ptx::smem_addr(do_stage<D>(sDO, sV, slot)), 16);
             const uint32_t boff = (uint32_t)b * C::BUF;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
@@ -389,15 +413,16 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
 
 template <int D, bool kFP16>
 __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t *sQ, uint8_t *sDO,
-                                  uint32_t bars, uint32_t tmem, Ctl *ctl) {
+                                  uint8_t *sV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdKVCfg<D>;
     constexpr uint32_t kIdescG = make_idesc(C::BN, C::DA, kFP16, true);  // dV, dK: N = DA, B MN-major
     const bool leader = ptx::lane_id() == 0;
     bool ok = true;
+    const int nst = kv_stages<D>(un);
     for (int t = 0; ok && t < un.steps; ++t) {
-        const int slot = t % C::ST;
+        const int slot = t % nst;
         const int b = t & 1;
-        if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 30) ||
+        if (!wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / nst) & 1, ctl, 30) ||
             !wait_warp(bar_addr(bars, C::B_PFULL + b), (t >> 1) & 1, ctl, 25)) {
             ok = false;
             break;
@@ -406,8 +431,8 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
         if (leader) {
             // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
             // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
-            const uint64_t om = smem_desc(ptx::smem_addr(sDO + slot * C::Q_BYTES), C::Q_BOX);
-            const uint64_t qm = smem_desc(ptx::smem_addr(sQ + slot * C::Q_BYTES), C::Q_BOX);
+            const uint64_t om = smem_desc(ptx::smem_addr(do_stage<D>(sDO, sV, slot)), C::Q_BOX);
+            const uint64_t qm = smem_desc(ptx::smem_addr(q_stage<D>(sQ, sV, slot)), C::Q_BOX);
             const uint32_t boff = (uint32_t)b * C::BUF;
             if (!(C::ROLES && un.role == 1)) {
 #pragma unroll
@@ -533,13 +558,14 @@ __device__ void bwd_kv_compute_role(const BwdParams &p, const KVUnit &un, const 
     const bool row_ok = j < p.Sk;
     const float c = p.scale_log2;
     bool ok = true;
+    const int nst = kv_stages<D>(un);
     for (int t = h; t < un.steps; t += C::WG) {
-        const int slot = t % C::ST;
+        const int slot = t % nst;
         const int b = t & 1;  // score buffer
         const uint32_t s_col = C::S_COL + (uint32_t)b * C::BUF, dp_col = C::DP_COL + (uint32_t)b * C::BUF;
         const int i0 = (un.it_lo + t % un.n_i) * C::BM;  // first query row of the step
         // The statistics arrived with the step's Q tile; S^T and dP^T are ready.
-        ok = ok && wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / C::ST) & 1, ctl, 26);
+        ok = ok && wait_warp(bar_addr(bars, C::B_QFULL + slot), (t / nst) & 1, ctl, 26);
         ok = ok && wait_warp(bar_addr(bars, (p.stall_test && t == 0) ? C::B_NEVER : C::B_SFULL + b),
                              (t >> 1) & 1, ctl, 27);
         if (!ok) break;
@@ -656,7 +682,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
     uint8_t *sV = sK + C::KV_BYTES;
     uint8_t *sQ = sV + C::KV_BYTES;
     uint8_t *sDO = sQ + C::ST * C::Q_BYTES;
-    uint8_t *sStat = sDO + C::ST * C::Q_BYTES;
+    uint8_t *sStat = sDO + C::ST * C::Q_BYTES;  // STM slots
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);  // 8-byte aligned
@@ -665,7 +691,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         ptx::mbar_init(bar_addr(bars, C::B_KVFULL), 1);
-        for (int s = 0; s < C::ST; ++s) {
+        for (int s = 0; s < C::STM; ++s) {
             ptx::mbar_init(bar_addr(bars, C::B_QFULL + s), 1);
             ptx::mbar_init(bar_addr(bars, C::B_QEMPTY + s), 2);  // one commit from each issuer
         }
@@ -705,7 +731,7 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
     } else if (warp == C::MMA_WARP) {
         bwd_kv_mma_s_role<D, kFP16>(p, un, sK, sV, sQ, sDO, bars, tmem, ctl);
     } else if (warp == C::MMA_G_WARP) {
-        bwd_kv_mma_g_role<D, kFP16>(p, un, sQ, sDO, bars, tmem, ctl);
+        bwd_kv_mma_g_role<D, kFP16>(p, un, sQ, sDO, sV, bars, tmem, ctl);
     } else {
         bwd_kv_tma_role<D>(p, un, sK, sV, sQ, sDO, sStat, bars, ctl);
     }
