@@ -176,15 +176,18 @@ struct BwdKVCfg {
     // dS^T), each over the whole d.  dP^T is thus formed once per tile, and
     // the role-0 CTAs, which carry about 60 % of the role-1 work, let the
     // block scheduler balance the rest.  K, V, Q and dO leave room for one
-    // Q/dO stage only.  A stage is free only after dV and dK of its step, a
-    // step after the compute warps have seen it, so the ring runs about two
-    // stages ahead of the score products; d = 128 fits four stages, d = 64 six.
+    // Q/dO stage plus 32 KB: the dK role, whose dO is done once dP^T is
+    // formed, keeps dO on a ring of its own (one buffer) and Q with the
+    // statistics on a ring of two (the second in those 32 KB); the dV role
+    // loads no V and takes a second Q/dO stage in its place.  A stage is free
+    // only after dV and dK of its step, a step after the compute warps have
+    // seen it, so the ring runs about two stages ahead of the score products;
+    // d = 128 fits four stages, d = 64 six.
     static constexpr int DA = D;                    // accumulator columns per CTA
     static constexpr bool ROLES = (D > 128);        // one of dV, dK per CTA
     static constexpr int NH = ROLES ? 2 : 1;        // CTAs per key tile
     static constexpr int ST = (D > 128) ? 1 : (D == 128) ? 4 : 6;  // stages of the (Q, dO, statistics) ring
-    // The dV role loads no V tile and takes a second stage in its place.
-    static constexpr int ST_DV = ROLES ? 2 : ST;
+    static constexpr int ST_DV = ROLES ? 2 : ST;  // stages of the dV role; the dK role's Q ring
     static constexpr int STM = ST_DV > ST ? ST_DV : ST;  // barriers and statistics slots
     static constexpr int KV_BOX = BN * 128;
     static constexpr int Q_BOX = BM * 128;
@@ -231,12 +234,16 @@ struct BwdKVCfg {
     static constexpr int B_DPFULL = B_SFULL + 2;   // [2]: SPLIT: dP^T of buffer b formed
     static constexpr int B_PFULL = B_DPFULL + 2;   // [2]: P^T, dS^T of buffer b written
     static constexpr int B_PFREE = B_PFULL + 2;    // [2]: dV, dK of buffer b done
-    static constexpr int B_DONE = B_PFREE + 2;
+    static constexpr int B_DOFULL = B_PFREE + 2;   // ROLES, dK role: the dO buffer loaded
+    static constexpr int B_DOEMPTY = B_DOFULL + 1; // ROLES, dK role: dP^T done with it
+    static constexpr int B_DONE = B_DOEMPTY + 1;
     static constexpr int B_DRAIN = B_DONE + 1;  // [2]: each issuer's MMAs finished
     static constexpr int B_NEVER = B_DRAIN + 2;  // no arrivals (the stall test's wait)
     static constexpr int NUM_BARS = B_NEVER + 1;
-    static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * 2 * Q_BYTES + STM * STAT_BYTES;
+    static constexpr int X_BYTES = ROLES ? Q_BYTES : 0;  // the dK role's second Q buffer
+    static constexpr int SMEM_TILES = 2 * KV_BYTES + ST * 2 * Q_BYTES + X_BYTES + STM * STAT_BYTES;
     static_assert(ST_DV == ST || (ST_DV == ST + 1 && 2 * Q_BYTES <= KV_BYTES), "the dV role's extra stage fits in V's place");
+    static_assert(!ROLES || ST == 1, "the dK role's dO ring holds one buffer, at stage 0's dO area");
     static constexpr int SMEM_BYTES = 1024 + SMEM_TILES + NUM_BARS * 8 + 32;
     static_assert(DK_COL + DA <= S_COL && DV_COL + DA <= S_COL && (ROLES || DV_COL + DA <= DK_COL) &&
                       DP_COL + BUF + BM <= TMEM_COLS && S_COL + BM <= DP_COL,
@@ -280,27 +287,34 @@ __device__ __forceinline__ KVUnit decode_kv_unit(const BwdParams &p) {
     return u;
 }
 
-// Q/dO stages of this CTA, and the Q and dO buffers of stage `slot`: stages
-// below ST have their own area; the dV role's extra stage uses V's.
+// Q (and statistics) stages of this CTA, whether its dO has a ring of its
+// own (the dK role: one buffer), and the Q and dO buffers of stage `slot`:
+// stages below ST have their own area; the dV role's extra stage uses V's,
+// the dK role's extra Q buffer the area after the dO stages (sX).
 template <int D>
 __device__ __forceinline__ int kv_stages(const KVUnit &un) {
     using C = BwdKVCfg<D>;
-    return (C::ROLES && un.role == 0) ? C::ST_DV : C::ST;
+    return C::ROLES ? C::ST_DV : C::ST;
 }
 template <int D>
-__device__ __forceinline__ uint8_t *q_stage(uint8_t *sQ, uint8_t *sV, int slot) {
-    using C = BwdKVCfg<D>;
-    return slot < C::ST ? sQ + slot * C::Q_BYTES : sV;
+__device__ __forceinline__ bool own_do_ring(const KVUnit &un) {
+    return BwdKVCfg<D>::ROLES && un.role == 1;
 }
 template <int D>
-__device__ __forceinline__ uint8_t *do_stage(uint8_t *sDO, uint8_t *sV, int slot) {
+__device__ __forceinline__ uint8_t *q_stage(uint8_t *sQ, uint8_t *sV, uint8_t *sX, const KVUnit &un, int slot) {
     using C = BwdKVCfg<D>;
-    return slot < C::ST ? sDO + slot * C::Q_BYTES : sV + C::Q_BYTES;
+    return slot < C::ST ? sQ + slot * C::Q_BYTES : (own_do_ring<D>(un) ? sX : sV);
+}
+template <int D>
+__device__ __forceinline__ uint8_t *do_stage(uint8_t *sDO, uint8_t *sV, const KVUnit &un, int slot) {
+    using C = BwdKVCfg<D>;
+    return (slot < C::ST || own_do_ring<D>(un)) ? sDO + (own_do_ring<D>(un) ? 0 : slot * C::Q_BYTES)
+                                                 : sV + C::Q_BYTES;
 }
 
 template <int D>
 __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
-                                uint8_t *sQ, uint8_t *sDO, uint8_t *sStat, uint32_t bars,
+                                uint8_t *sQ, uint8_t *sDO, uint8_t *sX, uint8_t *sStat, uint32_t bars,
                                 Ctl *ctl) {
     using C = BwdKVCfg<D>;
     const bool leader = ptx::lane_id() == 0;
@@ -319,26 +333,28 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
                                  pol_last);
         }
     }
-    int issued = 0;
+    int issued = 0, do_issued = 0;
     bool ok = true;
     const int nst = kv_stages<D>(un);
+    const bool sep = own_do_ring<D>(un);  // dO on a ring of its own (one buffer)
     for (int s = 0; s < un.steps; ++s) {
         const int slot = s % nst;
         if (!wait_warp_backoff(bar_addr(bars, C::B_QEMPTY + slot), ((s / nst) & 1) ^ 1, ctl, 21)) {
             ok = false;
             break;
         }
+        const int hq = un.kvh * p.kv_group + s / un.n_i;
+        const int i0 = (un.it_lo + s % un.n_i) * C::BM;
         if (leader) {
-            const int hq = un.kvh * p.kv_group + s / un.n_i;
-            const int i0 = (un.it_lo + s % un.n_i) * C::BM;
             const uint32_t fb = bar_addr(bars, C::B_QFULL + slot);
-            ptx::mbar_arrive_expect_tx(fb, 2 * C::Q_BYTES + C::STAT_BYTES);
+            ptx::mbar_arrive_expect_tx(fb, (sep ? 1 : 2) * C::Q_BYTES + C::STAT_BYTES);
 #pragma unroll
             for (int c = 0; c < D / 64; ++c) {
-                ptx::tma_load_4d(ptx::smem_addr(q_stage<D>(sQ, sV, slot)) + c * C::Q_BOX, &p.tm_q, fb, c * 64,
-                                 i0, hq, un.b, pol_last);
-                ptx::tma_load_4d(ptx::smem_addr(do_stage<D>(sDO, sV, slot)) + c * C::Q_BOX, &p.tm_do, fb,
+                ptx::tma_load_4d(ptx::smem_addr(q_stage<D>(sQ, sV, sX, un, slot)) + c * C::Q_BOX, &p.tm_q, fb,
                                  c * 64, i0, hq, un.b, pol_last);
+                if (!sep)
+                    ptx::tma_load_4d(ptx::smem_addr(do_stage<D>(sDO, sV, un, slot)) + c * C::Q_BOX, &p.tm_do,
+                                     fb, c * 64, i0, hq, un.b, pol_last);
             }
             const size_t row0 = ((size_t)un.b * p.H + hq) * (size_t)p.Sq_pad + (size_t)i0;
             const uint32_t st = ptx::smem_addr(sStat + slot * C::STAT_BYTES);
@@ -347,12 +363,29 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
         }
         __syncwarp();
         ++issued;
+        if (sep) {
+            if (!wait_warp_backoff(bar_addr(bars, C::B_DOEMPTY), (s & 1) ^ 1, ctl, 74)) {
+                ok = false;
+                break;
+            }
+            if (leader) {
+                const uint32_t fd = bar_addr(bars, C::B_DOFULL);
+                ptx::mbar_arrive_expect_tx(fd, C::Q_BYTES);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c)
+                    ptx::tma_load_4d(ptx::smem_addr(sDO) + c * C::Q_BOX, &p.tm_do, fd, c * 64, i0, hq, un.b,
+                                     pol_last);
+            }
+            __syncwarp();
+            ++do_issued;
+        }
     }
     // Let every copy already issued land before the CTA can exit.
     wait_bar_drain(bar_addr(bars, C::B_KVFULL), 0);
     if (!ok) {
         for (int s = issued - nst > 0 ? issued - nst : 0; s < issued; ++s)
             wait_bar_drain(bar_addr(bars, C::B_QFULL + s % nst), (s / nst) & 1);
+        if (do_issued) wait_bar_drain(bar_addr(bars, C::B_DOFULL), (do_issued - 1) & 1);
     }
 }
 
@@ -365,7 +398,8 @@ __device__ void bwd_kv_tma_role(const BwdParams &p, const KVUnit &un, uint8_t *s
 // one commit from each).
 template <int D, bool kFP16>
 __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t *sK, uint8_t *sV,
-                                  uint8_t *sQ, uint8_t *sDO, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+                                  uint8_t *sQ, uint8_t *sDO, uint8_t *sX, uint32_t bars, uint32_t tmem,
+                                  Ctl *ctl) {
     using C = BwdKVCfg<D>;
     constexpr uint32_t kIdescS = make_idesc(C::BN, C::BM, kFP16, false);  // M = keys, N = query rows
     const bool leader = ptx::lane_id() == 0;
@@ -386,24 +420,37 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
             break;
         }
         ptx::tc_fence_after();
+        const bool sep = own_do_ring<D>(un);
+        const uint64_t qd = smem_desc(ptx::smem_addr(q_stage<D>(sQ, sV, sX, un, slot)), 16);
+        const uint64_t od = smem_desc(ptx::smem_addr(do_stage<D>(sDO, sV, un, slot)), 16);
+        const uint32_t boff = (uint32_t)b * C::BUF;
         if (leader) {
-            const uint64_t qd = smem_desc(ptx::smem_addr(q_stage<D>(sQ, sV, slot)), 16);
-            const uint64_t od = smem_desc(ptx::smem_addr(do_stage<D>(sDO, sV, slot)), 16);
-            const uint32_t boff = (uint32_t)b * C::BUF;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
                 ptx::mma_ss(tmem + C::S_COL + boff, dk_desc + kmajor_step(kk, C::KV_BOX),
                             qd + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
             if constexpr (C::SPLIT) ptx::mma_commit(bar_addr(bars, C::B_SFULL + b));
-            if (!(C::ROLES && un.role == 0)) {
+            if (sep) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));  // Q's last read here
+        }
+        if (!(C::ROLES && un.role == 0)) {
+            if (sep) {  // dO on its own ring (one buffer)
+                __syncwarp();
+                if (!wait_warp(bar_addr(bars, C::B_DOFULL), t & 1, ctl, 73)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+            }
+            if (leader) {
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     ptx::mma_ss(tmem + C::DP_COL + boff, dv_desc + kmajor_step(kk, C::KV_BOX),
                                 od + kmajor_step(kk, C::Q_BOX), kIdescS, kk > 0 ? 1u : 0u);
                 ptx::mma_commit(bar_addr(bars, C::SPLIT ? C::B_DPFULL + b : C::B_SFULL + b));
+                if (sep) ptx::mma_commit(bar_addr(bars, C::B_DOEMPTY));
             }
-            ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
         }
+        if (leader && !sep) ptx::mma_commit(bar_addr(bars, C::B_QEMPTY + slot));
         __syncwarp();
     }
     if (leader) ptx::mma_commit(bar_addr(bars, C::B_DRAIN));
@@ -413,7 +460,7 @@ __device__ void bwd_kv_mma_s_role(const BwdParams &p, const KVUnit &un, uint8_t 
 
 template <int D, bool kFP16>
 __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t *sQ, uint8_t *sDO,
-                                  uint8_t *sV, uint32_t bars, uint32_t tmem, Ctl *ctl) {
+                                  uint8_t *sV, uint8_t *sX, uint32_t bars, uint32_t tmem, Ctl *ctl) {
     using C = BwdKVCfg<D>;
     constexpr uint32_t kIdescG = make_idesc(C::BN, C::DA, kFP16, true);  // dV, dK: N = DA, B MN-major
     const bool leader = ptx::lane_id() == 0;
@@ -431,8 +478,8 @@ __device__ void bwd_kv_mma_g_role(const BwdParams &p, const KVUnit &un, uint8_t 
         if (leader) {
             // dO and Q as MN-major B operands: K = query rows (16 = two 8-row
             // groups, 2048 bytes), N = d in 64-column boxes Q_BOX apart.
-            const uint64_t om = smem_desc(ptx::smem_addr(do_stage<D>(sDO, sV, slot)), C::Q_BOX);
-            const uint64_t qm = smem_desc(ptx::smem_addr(q_stage<D>(sQ, sV, slot)), C::Q_BOX);
+            const uint64_t om = smem_desc(ptx::smem_addr(do_stage<D>(sDO, sV, un, slot)), C::Q_BOX);
+            const uint64_t qm = smem_desc(ptx::smem_addr(q_stage<D>(sQ, sV, sX, un, slot)), C::Q_BOX);
             const uint32_t boff = (uint32_t)b * C::BUF;
             if (!(C::ROLES && un.role == 1)) {
 #pragma unroll
@@ -682,7 +729,8 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
     uint8_t *sV = sK + C::KV_BYTES;
     uint8_t *sQ = sV + C::KV_BYTES;
     uint8_t *sDO = sQ + C::ST * C::Q_BYTES;
-    uint8_t *sStat = sDO + C::ST * C::Q_BYTES;  // STM slots
+    uint8_t *sX = sDO + C::ST * C::Q_BYTES;     // X_BYTES
+    uint8_t *sStat = sX + C::X_BYTES;           // STM slots
     uint64_t *bar_mem = reinterpret_cast<uint64_t *>(smem + C::SMEM_TILES);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bar_mem + C::NUM_BARS);
     Ctl *ctl = reinterpret_cast<Ctl *>(tmem_holder + 2);  // 8-byte aligned
@@ -701,6 +749,8 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
             ptx::mbar_init(bar_addr(bars, C::B_PFULL + b), C::NUM_COMPUTE / C::WG);
             ptx::mbar_init(bar_addr(bars, C::B_PFREE + b), 1);
         }
+        ptx::mbar_init(bar_addr(bars, C::B_DOFULL), 1);
+        ptx::mbar_init(bar_addr(bars, C::B_DOEMPTY), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DONE), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN), 1);
         ptx::mbar_init(bar_addr(bars, C::B_DRAIN + 1), 1);
@@ -729,11 +779,11 @@ __global__ void __launch_bounds__(BwdKVCfg<D>::NUM_THREADS, 1)
     if (warp < C::NUM_COMPUTE / 32) {
         bwd_kv_compute_role<D, kFP16>(p, un, sStat, bars, tmem, ctl);
     } else if (warp == C::MMA_WARP) {
-        bwd_kv_mma_s_role<D, kFP16>(p, un, sK, sV, sQ, sDO, bars, tmem, ctl);
+        bwd_kv_mma_s_role<D, kFP16>(p, un, sK, sV, sQ, sDO, sX, bars, tmem, ctl);
     } else if (warp == C::MMA_G_WARP) {
-        bwd_kv_mma_g_role<D, kFP16>(p, un, sQ, sDO, sV, bars, tmem, ctl);
+        bwd_kv_mma_g_role<D, kFP16>(p, un, sQ, sDO, sV, sX, bars, tmem, ctl);
     } else {
-        bwd_kv_tma_role<D>(p, un, sK, sV, sQ, sDO, sStat, bars, ctl);
+        bwd_kv_tma_role<D>(p, un, sK, sV, sQ, sDO, sX, sStat, bars, ctl);
     }
     __syncwarp();
     ptx::tc_fence_before();
