@@ -19,11 +19,12 @@
 //     whose K and V fit in a third of the L2, so each K/V byte comes from
 //     DRAM about once;
 //   * warp 10 streams the Q tile and a ring of K tiles, warp 11 a ring of V
-//     tiles, by TMA (128-byte swizzle, 64-column boxes);
+//     tiles, by TMA (128-byte swizzle, 64-column boxes; at d = 256 the rings
+//     hold 128-column halves of the tiles);
 //   * warp 8 issues S = Q K^T (tcgen05, both operands in shared memory) into
-//     two S buffers in tensor memory, each as soon as the softmax has read
-//     that buffer's previous tile; warp 9 issues O += P V with P read from
-//     its own double-buffered tensor-memory area;
+//     the S buffers in tensor memory (two; one at d = 256), each as soon as
+//     the softmax has read that buffer's previous tile; warp 9 issues
+//     O += P V with P read from tensor memory (two P areas; one at d = 128);
 //   * warps 0-7 are the softmax: warp w owns 16 rows (TMEM lanes) and every
 //     key column of a tile in the 16-lane tcgen05.ld layout, where a row's
 //     columns sit in one quad of threads, so max and sum take two shuffles
@@ -34,8 +35,8 @@
 //
 // Rescaling is deferred until the running max has grown by more than 2^8
 // (log2 units).  Until then the accumulator and the sums both stay referenced
-// to the same stale max, so the final O_acc / l is unchanged (the pages'
-// remark that FlashAttention-2 "defers most rescaling"); the stale reference
+// to the same stale max, so the final O_acc / l is unchanged (the pages note
+// that FlashAttention-2 postpones most of the rescaling); the stale reference
 // only lets unnormalised weights reach 2^8, far from fp32/bf16/fp16 limits.
 // The tile max itself is only computed when needed: a weight above 2^8
 // pushes the tile's sum above 2^8, so a tile whose sum stays within the bound
