@@ -20,6 +20,35 @@ namespace {
 
 // ---------------------------------------------------------------- backward
 
+// The dQ kernel needs only the row statistics, not dK or dV, so it runs on a
+// second stream beside the dK/dV kernel: launched after it, its CTAs take
+// the SMs that the dK/dV kernel's last wave leaves idle.  The caller's
+// stream waits for it before its next work (a fork and join of events,
+// which stream capture records as graph edges).  Created by a device's
+// first backward call; a lock serialises the enqueue, so the shared events
+// are never interleaved.
+struct BwdStreams {
+    bool ready = false;
+    cudaStream_t side = nullptr;
+    cudaEvent_t stats = nullptr, dq_done = nullptr;
+};
+BwdStreams g_bwd[kMaxDevices];  // guarded by g_bwd_mutex
+std::mutex g_bwd_mutex;
+
+fa_status bwd_streams(int dev, BwdStreams **bs) {
+    BwdStreams &b = g_bwd[dev];
+    if (!b.ready) {
+        const unsigned ef = cudaEventDisableTiming;
+        if (!b.side && cudaStreamCreateWithFlags(&b.side, cudaStreamNonBlocking) != cudaSuccess)
+            return FA_ERR_CUDA;
+        if (!b.stats && cudaEventCreateWithFlags(&b.stats, ef) != cudaSuccess) return FA_ERR_CUDA;
+        if (!b.dq_done && cudaEventCreateWithFlags(&b.dq_done, ef) != cudaSuccess) return FA_ERR_CUDA;
+        b.ready = true;
+    }
+    *bs = &b;
+    return FA_OK;
+}
+
 size_t bwd_pad_rows(int Sq) {
     return ((size_t)Sq + kBwdPadRows - 1) / kBwdPadRows * kBwdPadRows;
 }
@@ -43,7 +72,7 @@ fa_status check_bwd_sizes(int B, int H, int Hkv, int Sq, int Sk, int d, int mask
 
 template <int D, bool kFP16>
 fa_status launch_bwd(const BwdParams &pkv, const BwdParams &pq, const void *o, const void *dout,
-                     const float *lse, DeviceInfo &info, cudaStream_t stream) {
+                     const float *lse, DeviceInfo &info, int dev, cudaStream_t stream) {
     const int slot = (D == 256 ? 4 : D == 128 ? 2 : 0) + (kFP16 ? 1 : 0);
     const long long rows = (long long)pq.B * pq.H * pq.Sq_pad;
     constexpr int RPB = 256 / (D / 8);
@@ -56,14 +85,25 @@ fa_status launch_bwd(const BwdParams &pkv, const BwdParams &pq, const void *o, c
     auto kv = fa_bwd_dkdv_kernel<D, kFP16>;
     const int kv_smem = std::max(BwdKVCfg<D>::SMEM_BYTES, kBwdMinSmem);
     if (set_smem(kv, kv_smem, info.attr_bwd[slot]) != FA_OK) return FA_ERR_CUDA;
-    kv<<<pkv.n_units, BwdKVCfg<D>::NUM_THREADS, kv_smem, stream>>>(pkv);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
-
     auto kq = fa_bwd_dq_kernel<D, kFP16>;
     const int q_smem = std::max(BwdQCfg<D>::SMEM_BYTES, kBwdMinSmem);
     if (set_smem(kq, q_smem, info.attr_bwd[6 + slot]) != FA_OK) return FA_ERR_CUDA;
-    kq<<<pq.n_units, BwdQCfg<D>::NUM_THREADS, q_smem, stream>>>(pq);
+
+    std::lock_guard<std::mutex> lock(g_bwd_mutex);
+    BwdStreams *bs = nullptr;
+    if (bwd_streams(dev, &bs) != FA_OK) return FA_ERR_CUDA;
+    // the statistics are ready: fork
+    if (cudaEventRecord(bs->stats, stream) != cudaSuccess ||
+        cudaStreamWaitEvent(bs->side, bs->stats, 0) != cudaSuccess)
+        return FA_ERR_CUDA;
+    kv<<<pkv.n_units, BwdKVCfg<D>::NUM_THREADS, kv_smem, stream>>>(pkv);
     if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    kq<<<pq.n_units, BwdQCfg<D>::NUM_THREADS, q_smem, bs->side>>>(pq);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_CUDA;
+    // join: the caller's stream continues once dQ is done as well
+    if (cudaEventRecord(bs->dq_done, bs->side) != cudaSuccess ||
+        cudaStreamWaitEvent(stream, bs->dq_done, 0) != cudaSuccess)
+        return FA_ERR_CUDA;
     return FA_OK;
 }
 
@@ -162,14 +202,14 @@ fa_status bwd_impl(const void *q, const void *k, const void *v, const void *o, c
                      fp16 ? "fp16" : "bf16", B, H, Hkv, Sq, Sk, pkv.n_units, pq.n_units);
     switch (d) {
         case 64:
-            return fp16 ? launch_bwd<64, true>(pkv, pq, o, dout, lse, *info, stream)
-                        : launch_bwd<64, false>(pkv, pq, o, dout, lse, *info, stream);
+            return fp16 ? launch_bwd<64, true>(pkv, pq, o, dout, lse, *info, dev, stream)
+                        : launch_bwd<64, false>(pkv, pq, o, dout, lse, *info, dev, stream);
         case 128:
-            return fp16 ? launch_bwd<128, true>(pkv, pq, o, dout, lse, *info, stream)
-                        : launch_bwd<128, false>(pkv, pq, o, dout, lse, *info, stream);
+            return fp16 ? launch_bwd<128, true>(pkv, pq, o, dout, lse, *info, dev, stream)
+                        : launch_bwd<128, false>(pkv, pq, o, dout, lse, *info, dev, stream);
         case 256:
-            return fp16 ? launch_bwd<256, true>(pkv, pq, o, dout, lse, *info, stream)
-                        : launch_bwd<256, false>(pkv, pq, o, dout, lse, *info, stream);
+            return fp16 ? launch_bwd<256, true>(pkv, pq, o, dout, lse, *info, dev, stream)
+                        : launch_bwd<256, false>(pkv, pq, o, dout, lse, *info, dev, stream);
         default:
             return FA_ERR_UNSUPPORTED;
     }

@@ -311,3 +311,30 @@ def test_more_units_than_the_schedule_holds():
     # 13,000 one-tile units: past the 4,096 a precomputed schedule can carry,
     # so the kernel falls back to its snake order over the units
     full_case(260, 50, 100, 100, 64, inputs.BF16, "causal", seed=14)
+
+
+def test_forward_under_cuda_graph_capture():
+    # one launch on the caller's stream: captured into a CUDA graph and
+    # replayed, it gives the bits of a direct call
+    inp = inputs.custom(2, 8, 1000, 1000, 128, inputs.BF16, "causal", 0, seed=15)
+    w = inp.workload
+    q, k, v = (_to_dev(b, w.dtype) for b in (inp.q_bits, inp.k_bits, inp.v_bits))
+    o_ref, lse_ref = fa.forward(q, k, v, scale=w.scale, mask=w.mask)
+    o = torch.empty_like(q)
+    lse = torch.empty_like(lse_ref)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fa.forward(q, k, v, scale=w.scale, mask=w.mask, out=o, lse=lse)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.forward(q, k, v, scale=w.scale, mask=w.mask, out=o, lse=lse)
+    o.fill_(7.0)
+    lse.fill_(7.0)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)

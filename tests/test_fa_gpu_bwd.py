@@ -174,3 +174,40 @@ def test_bwd_full_size_two_heads():
                               qf[:, sl], kf[:, sl], vf[:, sl], dof[:, sl], w.scale, w.mask, 0,
                               w.dtype)
         print(f"{w.name} head {h}: {stats}")
+
+
+def test_bwd_under_cuda_graph_capture():
+    # The backward runs dQ on a library stream forked from and joined back to
+    # the caller's with events: captured into a CUDA graph and replayed, it
+    # gives the bits of a direct call (and the replay depends on nothing
+    # enqueued outside the graph).
+    inp = inputs.custom(1, 4, 700, 700, 128, inputs.BF16, "causal", 0, seed=98)
+    w = inp.workload
+    q, k, v, do = (_dev(b, w.dtype)
+                   for b in (inp.q_bits, inp.k_bits, inp.v_bits, inputs.grad_output(w)))
+    o, lse = fa.forward(q, k, v, scale=w.scale, mask=w.mask)
+    ref = fa.backward(q, k, v, o, lse, do, scale=w.scale, mask=w.mask)
+    torch.cuda.synchronize()
+    dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+    st, ws_bytes = fa.bwd_workspace_query(1, 4, 4, 700, 700, 128, "causal", 0, fa.DTYPE_BF16)
+    assert st == fa.FA_OK
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # a call outside the capture on the capture's stream first
+        fa.backward(q, k, v, o, lse, do, scale=w.scale, mask=w.mask, dq=dq, dk=dk, dv=dv,
+                    workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.backward(q, k, v, o, lse, do, scale=w.scale, mask=w.mask, dq=dq, dk=dk, dv=dv,
+                    workspace=ws)
+    for x in (dq, dk, dv):
+        x.fill_(7.0)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    for a, b in zip((dq, dk, dv), ref):
+        assert torch.equal(a, b)
