@@ -136,9 +136,14 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
  * All tensors are contiguous and 16-byte aligned (lse 4-byte).  Outputs may
  * not overlap each other, the inputs or the workspace (FA_ERR_INVALID_ARG).
  * Sq == 0 sets dk and dv to zero; q, o, lse, dout, dq and the workspace are
- * then not examined.  Enqueues three kernels on `stream` (row statistics,
- * dK/dV, dQ) and returns; allocates nothing.  Waits are bounded as in the
- * forward and report through fa_get_device_error().
+ * then not examined.  Enqueues three kernels and returns; allocates
+ * nothing.  The row statistics and dK/dV run on `stream`; dQ runs on a
+ * library stream of the current device (created by the first call, never
+ * destroyed), forked from `stream` after the statistics and joined back
+ * before any later work on `stream`, both by events: synchronising `stream`
+ * covers all three, and a stream capture on `stream` records the fork and
+ * join as graph edges.  Waits are bounded as in the forward and report
+ * through fa_get_device_error().
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                  const void *dout, void *dq, void *dk, void *dv, void *workspace,
