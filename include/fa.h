@@ -142,8 +142,10 @@ fa_status fa_fwd_gqa(const void *q, const void *k, const void *v, void *o, float
  * destroyed), forked from `stream` after the statistics and joined back
  * before any later work on `stream`, both by events: synchronising `stream`
  * covers all three, and a stream capture on `stream` records the fork and
- * join as graph edges.  Waits are bounded as in the forward and report
- * through fa_get_device_error().
+ * join as graph edges.  Calls may come from several host threads on several
+ * streams (a lock serialises their enqueue); their dQ kernels then share the
+ * library stream and run one after another.  Waits are bounded as in the
+ * forward and report through fa_get_device_error().
  */
 fa_status fa_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
                  const void *dout, void *dq, void *dk, void *dv, void *workspace,

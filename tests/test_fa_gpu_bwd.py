@@ -211,3 +211,45 @@ def test_bwd_under_cuda_graph_capture():
     assert fa.device_error() == fa.FA_OK
     for a, b in zip((dq, dk, dv), ref):
         assert torch.equal(a, b)
+
+
+def test_bwd_calls_from_two_threads_on_two_streams():
+    # Two host threads call the backward at once, each on its own stream:
+    # the library serialises the enqueue of its shared dQ stream and events,
+    # and each call's results are the bits of the same call made alone.
+    import threading
+    cases = []
+    for i, (S, mask) in enumerate(((600, "causal"), (900, "none"))):
+        inp = inputs.custom(1, 4, S, S, 128, inputs.BF16, mask, 0, seed=120 + i)
+        w = inp.workload
+        q, k, v, do = (_dev(b, w.dtype)
+                       for b in (inp.q_bits, inp.k_bits, inp.v_bits, inputs.grad_output(w)))
+        o, lse = fa.forward(q, k, v, scale=w.scale, mask=mask)
+        ref = fa.backward(q, k, v, o, lse, do, scale=w.scale, mask=mask)
+        cases.append((q, k, v, o, lse, do, w.scale, mask, ref))
+    torch.cuda.synchronize()
+    results = [None, None]
+    errors = []
+
+    def run(idx):
+        try:
+            q, k, v, o, lse, do, scale, mask, _ = cases[idx]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(3):
+                    results[idx] = fa.backward(q, k, v, o, lse, do, scale=scale, mask=mask, stream=s)
+            s.synchronize()
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    assert fa.device_error() == fa.FA_OK
+    for idx in range(2):
+        for a, b in zip(results[idx], cases[idx][8]):
+            assert torch.equal(a, b)
