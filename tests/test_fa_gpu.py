@@ -338,3 +338,20 @@ def test_forward_under_cuda_graph_capture():
     torch.cuda.synchronize()
     assert fa.device_error() == fa.FA_OK
     assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
+@pytest.mark.parametrize("d,S,H,mask,window", [(128, 32768, 4, "causal", 0), (256, 16384, 2, "none", 0),
+                                               (64, 32768, 4, "window", 5000)],
+                         ids=["d128-32k-causal", "d256-16k-none", "d64-32k-window"])
+def test_long_sequences_sampled_rows(d, S, H, mask, window):
+    # sequences longer than any benchmark workload (up to 256 key tiles per
+    # unit), checked on 96 evenly spaced rows that include the first and the
+    # last (the oracle computes those rows alone)
+    inp = inputs.custom(1, H, S, S, d, inputs.BF16, mask, window, seed=400 + d)
+    w = inp.workload
+    o, lse = run_gpu(inp)
+    rows = np.linspace(0, H * S - 1, 96).round().astype(np.int64)
+    qf, kf, vf = inp.f64()
+    o_ref, lse_ref = oracle.attention(qf, kf, vf, w.scale, mask, window, rows=rows)
+    stats = compare(o.reshape(-1, d)[rows], lse.reshape(-1)[rows], o_ref, lse_ref, inputs.BF16)
+    print(w.name, stats)
