@@ -176,12 +176,14 @@ def test_bwd_full_size_two_heads():
         print(f"{w.name} head {h}: {stats}")
 
 
-def test_bwd_under_cuda_graph_capture():
+@pytest.mark.parametrize("d", [128, 256])
+def test_bwd_under_cuda_graph_capture(d):
     # The backward runs dQ on a library stream forked from and joined back to
-    # the caller's with events: captured into a CUDA graph and replayed, it
-    # gives the bits of a direct call (and the replay depends on nothing
-    # enqueued outside the graph).
-    inp = inputs.custom(1, 4, 700, 700, 128, inputs.BF16, "causal", 0, seed=98)
+    # the caller's with events (and at d = 256 its dK/dV kernel as clusters
+    # of two): captured into a CUDA graph and replayed, it gives the bits of
+    # a direct call (and the replay depends on nothing enqueued outside the
+    # graph).
+    inp = inputs.custom(1, 4, 700, 700, d, inputs.BF16, "causal", 0, seed=98)
     w = inp.workload
     q, k, v, do = (_dev(b, w.dtype)
                    for b in (inp.q_bits, inp.k_bits, inp.v_bits, inputs.grad_output(w)))
@@ -189,7 +191,7 @@ def test_bwd_under_cuda_graph_capture():
     ref = fa.backward(q, k, v, o, lse, do, scale=w.scale, mask=w.mask)
     torch.cuda.synchronize()
     dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
-    st, ws_bytes = fa.bwd_workspace_query(1, 4, 4, 700, 700, 128, "causal", 0, fa.DTYPE_BF16)
+    st, ws_bytes = fa.bwd_workspace_query(1, 4, 4, 700, 700, d, "causal", 0, fa.DTYPE_BF16)
     assert st == fa.FA_OK
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     side = torch.cuda.Stream()
